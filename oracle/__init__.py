@@ -1,0 +1,121 @@
+"""Oracle for the causal dot product -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg (and its ``--impl reference`` arm) may import this package.  The CUDA
+product path never imports it, and this package imports nothing from the
+product package.
+
+The arithmetic lives in ``causal_product_oracle.c`` (plain C, fp64, the
+serial recurrence of triton-lang/triton issue #217, "Dot Product Computes
+Wrong Values": state += k v^T, then out = state^T q).  This module compiles
+it with gcc and exposes it through ctypes:
+
+    fwd(q, k, v)        -> out            (float64 [..., N, M])
+    bwd(q, k, v, g)     -> (dq, dk, dv)   (float64)
+
+Inputs are numpy arrays of shape [B, H, N, D] / [B, H, N, M] (any leading
+shape works; the last two axes are N and the feature axis).  They are
+converted to float32, which is exact for bfloat16 and float32 inputs; a
+float64 input is rejected because narrowing it would silently change the
+values under test.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "causal_product_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libcpo.so")
+
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build/libcpo.so`` (gcc, OpenMP).
+
+    No fast-math and no architecture-specific flags: the fp64 arithmetic is
+    evaluated exactly in source order on x86_64 and aarch64 alike.
+    """
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fopenmp",
+           "-shared", "-fPIC", "-std=c11", "-o", tmp, _SRC]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i64, p, c_int = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+            lib.cpo_fwd.argtypes = [p, p, p, p, i64, i64, i64, i64, c_int]
+            lib.cpo_fwd.restype = c_int
+            lib.cpo_bwd.argtypes = [p, p, p, p, p, p, p, i64, i64, i64, i64, c_int]
+            lib.cpo_bwd.restype = c_int
+            lib.cpo_threads.argtypes = [c_int]
+            lib.cpo_threads.restype = c_int
+            _lib = lib
+    return _lib
+
+
+def _as_f32(x) -> np.ndarray:
+    x = np.asarray(x)
+    if x.dtype == np.float64:
+        raise TypeError("oracle inputs must hold float32/bfloat16 values; "
+                        "pass float32 arrays (bf16 -> f32 is exact)")
+    return np.ascontiguousarray(x, dtype=np.float32)
+
+
+def _dims(q, k, v):
+    if q.ndim < 2 or q.shape != k.shape or q.shape[:-1] != v.shape[:-1]:
+        raise ValueError(f"shape mismatch: q{q.shape} k{k.shape} v{v.shape}")
+    lead = q.shape[:-2]
+    BH = int(np.prod(lead)) if lead else 1
+    return lead, BH, q.shape[-2], q.shape[-1], v.shape[-1]
+
+
+def threads(nthreads: int = 0) -> int:
+    """Threads the oracle uses for ``nthreads`` (0 = OpenMP default)."""
+    return int(_load().cpo_threads(int(nthreads)))
+
+
+def fwd(q, k, v, nthreads: int = 0) -> np.ndarray:
+    """out_i = sum_{j<=i} (q_i . k_j) v_j per leading slice, in fp64."""
+    q, k, v = _as_f32(q), _as_f32(k), _as_f32(v)
+    lead, BH, N, D, M = _dims(q, k, v)
+    out = np.zeros(lead + (N, M), dtype=np.float64)
+    rc = _load().cpo_fwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, out.ctypes.data,
+                         BH, N, D, M, int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle fwd failed ({rc})")
+    return out
+
+
+def bwd(q, k, v, g, nthreads: int = 0):
+    """(dq, dk, dv) of L = <g, out> for the causal product, in fp64."""
+    q, k, v, g = _as_f32(q), _as_f32(k), _as_f32(v), _as_f32(g)
+    lead, BH, N, D, M = _dims(q, k, v)
+    if g.shape != v.shape:
+        raise ValueError(f"grad shape {g.shape} != out shape {v.shape}")
+    dq = np.zeros(lead + (N, D), dtype=np.float64)
+    dk = np.zeros(lead + (N, D), dtype=np.float64)
+    dv = np.zeros(lead + (N, M), dtype=np.float64)
+    rc = _load().cpo_bwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, g.ctypes.data,
+                         dq.ctypes.data, dk.ctypes.data, dv.ctypes.data,
+                         BH, N, D, M, int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle bwd failed ({rc})")
+    return dq, dk, dv

@@ -1,0 +1,182 @@
+/*
+ * Oracle for the causal dot product -- TEST INFRASTRUCTURE ONLY.
+ *
+ * Only the test suite, the smoke check and the benchmark's CPU-baseline leg
+ * may load or run this code.  The product path (the CUDA library and its
+ * Python binding) never calls it and shares no code with it.
+ *
+ * What it computes (fp64 throughout, plain C, one (b,h) slice at a time):
+ *
+ *   Forward.  For one (b,h) with q,k in R^{N x D} and v in R^{N x M}:
+ *       S_i   = sum_{j<=i} k_j v_j^T                 (a D x M matrix)
+ *       out_i = S_i^T q_i  =  sum_{j<=i} (q_i . k_j) v_j
+ *   This is the recurrent form of causal linear attention that
+ *   triton-lang/triton issue #217 ("Dot Product Computes Wrong Values")
+ *   sets out to batch-parallelise: the opening comment names Algorithm 1 of
+ *   "Transformers are RNNs" and describes it as a prefix sum over the
+ *   sequence; the loop body shown later in the same issue adds the outer
+ *   product of the current key and value rows to a running state and then
+ *   reads the output out of that state with the query (the comment there
+ *   notes that the readout must use the query, not the key).  The state is
+ *   updated before the readout, so row i sees itself (inclusive, j <= i).
+ *   No normaliser and no 1/sqrt(D) scale are applied: neither appears in
+ *   that loop.
+ *
+ *   Backward.  The pages print no backward; it follows from the definition.
+ *   With g_i = dL/dout_i and L = sum_i <g_i, out_i>:
+ *       dq_i = S_i g_i                         (forward sweep over i)
+ *       R_j  = sum_{i>=j} q_i g_i^T            (reverse sweep over j)
+ *       dk_j = R_j v_j,    dv_j = R_j^T k_j
+ *
+ * Inputs are float32 arrays holding the exact values the GPU receives
+ * (bfloat16 values are exactly representable in float32 and in double);
+ * each slice is widened to double before any arithmetic.  Outputs are
+ * double.  Layout: contiguous row-major [BH][N][D] / [BH][N][M].
+ *
+ * Parallelism: OpenMP over the independent (b,h) slices only; the sweep
+ * inside a slice is the plain serial loop, in sequence order.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Widen one [N][C] float slice to double. */
+static void widen(const float *src, double *dst, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) dst[i] = (double)src[i];
+}
+
+/* Forward recurrence on one (b,h) slice; all arrays double, row-major. */
+static void fwd_slice(const double *q, const double *k, const double *v,
+                      double *out, double *S, int64_t N, int64_t D, int64_t M) {
+    memset(S, 0, sizeof(double) * (size_t)(D * M));
+    for (int64_t i = 0; i < N; ++i) {
+        const double *ki = k + i * D, *vi = v + i * M, *qi = q + i * D;
+        /* state update: S += k_i v_i^T */
+        for (int64_t d = 0; d < D; ++d) {
+            double kd = ki[d];
+            double *Sd = S + d * M;
+            for (int64_t m = 0; m < M; ++m) Sd[m] += kd * vi[m];
+        }
+        /* readout: out_i = S^T q_i */
+        double *oi = out + i * M;
+        for (int64_t m = 0; m < M; ++m) oi[m] = 0.0;
+        for (int64_t d = 0; d < D; ++d) {
+            double qd = qi[d];
+            const double *Sd = S + d * M;
+            for (int64_t m = 0; m < M; ++m) oi[m] += qd * Sd[m];
+        }
+    }
+}
+
+/* Backward on one (b,h) slice. */
+static void bwd_slice(const double *q, const double *k, const double *v,
+                      const double *g, double *dq, double *dk, double *dv,
+                      double *S, int64_t N, int64_t D, int64_t M) {
+    /* forward sweep: S_i = sum_{j<=i} k_j v_j^T ; dq_i = S_i g_i */
+    memset(S, 0, sizeof(double) * (size_t)(D * M));
+    for (int64_t i = 0; i < N; ++i) {
+        const double *ki = k + i * D, *vi = v + i * M, *gi = g + i * M;
+        for (int64_t d = 0; d < D; ++d) {
+            double kd = ki[d];
+            double *Sd = S + d * M;
+            for (int64_t m = 0; m < M; ++m) Sd[m] += kd * vi[m];
+        }
+        double *dqi = dq + i * D;
+        for (int64_t d = 0; d < D; ++d) {
+            const double *Sd = S + d * M;
+            double acc = 0.0;
+            for (int64_t m = 0; m < M; ++m) acc += Sd[m] * gi[m];
+            dqi[d] = acc;
+        }
+    }
+    /* reverse sweep: R_j = sum_{i>=j} q_i g_i^T ; dk_j = R_j v_j ; dv_j = R_j^T k_j */
+    double *R = S;
+    memset(R, 0, sizeof(double) * (size_t)(D * M));
+    for (int64_t j = N - 1; j >= 0; --j) {
+        const double *qj = q + j * D, *gj = g + j * M;
+        const double *kj = k + j * D, *vj = v + j * M;
+        for (int64_t d = 0; d < D; ++d) {
+            double qd = qj[d];
+            double *Rd = R + d * M;
+            for (int64_t m = 0; m < M; ++m) Rd[m] += qd * gj[m];
+        }
+        double *dkj = dk + j * D;
+        for (int64_t d = 0; d < D; ++d) {
+            const double *Rd = R + d * M;
+            double acc = 0.0;
+            for (int64_t m = 0; m < M; ++m) acc += Rd[m] * vj[m];
+            dkj[d] = acc;
+        }
+        double *dvj = dv + j * M;
+        for (int64_t m = 0; m < M; ++m) dvj[m] = 0.0;
+        for (int64_t d = 0; d < D; ++d) {
+            double kd = kj[d];
+            const double *Rd = R + d * M;
+            for (int64_t m = 0; m < M; ++m) dvj[m] += kd * Rd[m];
+        }
+    }
+}
+
+static int set_threads(int nthreads) {
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+    return omp_get_max_threads();
+#else
+    (void)nthreads;
+    return 1;
+#endif
+}
+
+/* Number of threads the oracle will use when called with `nthreads`
+ * (<= 0 means the OpenMP default). */
+int cpo_threads(int nthreads) { return set_threads(nthreads); }
+
+/* Forward over BH slices.  Returns 0 on success, -1 on a bad argument,
+ * -2 when a scratch allocation fails. */
+int cpo_fwd(const float *q, const float *k, const float *v, double *out,
+            int64_t BH, int64_t N, int64_t D, int64_t M, int nthreads) {
+    if (BH < 0 || N < 0 || D <= 0 || M <= 0) return -1;
+    if (BH == 0 || N == 0) return 0;
+    set_threads(nthreads);
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+    for (int64_t bh = 0; bh < BH; ++bh) {
+        double *buf = (double *)malloc(sizeof(double) * (size_t)(N * (2 * D + M) + D * M));
+        if (!buf) { err |= 1; continue; }
+        double *qd = buf, *kd = qd + N * D, *vd = kd + N * D, *S = vd + N * M;
+        widen(q + bh * N * D, qd, N * D);
+        widen(k + bh * N * D, kd, N * D);
+        widen(v + bh * N * M, vd, N * M);
+        fwd_slice(qd, kd, vd, out + bh * N * M, S, N, D, M);
+        free(buf);
+    }
+    return err ? -2 : 0;
+}
+
+/* Backward over BH slices: g is dL/dout; writes dq, dk, dv. */
+int cpo_bwd(const float *q, const float *k, const float *v, const float *g,
+            double *dq, double *dk, double *dv,
+            int64_t BH, int64_t N, int64_t D, int64_t M, int nthreads) {
+    if (BH < 0 || N < 0 || D <= 0 || M <= 0) return -1;
+    if (BH == 0 || N == 0) return 0;
+    set_threads(nthreads);
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+    for (int64_t bh = 0; bh < BH; ++bh) {
+        double *buf = (double *)malloc(sizeof(double) * (size_t)(N * (2 * D + 2 * M) + D * M));
+        if (!buf) { err |= 1; continue; }
+        double *qd = buf, *kd = qd + N * D, *vd = kd + N * D, *gd = vd + N * M;
+        double *S = gd + N * M;
+        widen(q + bh * N * D, qd, N * D);
+        widen(k + bh * N * D, kd, N * D);
+        widen(v + bh * N * M, vd, N * M);
+        widen(g + bh * N * M, gd, N * M);
+        bwd_slice(qd, kd, vd, gd, dq + bh * N * D, dk + bh * N * D, dv + bh * N * M,
+                  S, N, D, M);
+        free(buf);
+    }
+    return err ? -2 : 0;
+}

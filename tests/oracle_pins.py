@@ -1,0 +1,255 @@
+"""Pins for the causal-product oracle.
+
+Each pin checks an implementation ``impl`` (an object with ``fwd(q,k,v)``
+and ``bwd(q,k,v,g)`` returning float64 numpy arrays, like ``oracle``)
+against something other than the recurrence itself: hand-worked values,
+a brute-force quadratic form, closed forms, textbook special cases,
+linearity, causality and finite differences.  ``tests/test_oracle.py``
+runs them on the oracle; ``tests/test_oracle_mutants.py`` checks that each
+planted mistake in a copy of the oracle trips at least one of them.
+
+Every pin raises AssertionError on failure.
+"""
+from __future__ import annotations
+
+import json
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                      "hand_examples.json")
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _pos(rng, shape):
+    """elu(x)+1 features drawn in float32 (positive, like the workloads)."""
+    x = rng.standard_normal(shape).astype(np.float32)
+    return np.where(x > 0, x + 1, np.exp(x)).astype(np.float32)
+
+
+def _dyadic(rng, shape, lo=-4, hi=4, denom=16):
+    """Values k/denom in [lo, hi]: exact in float32, and sums of their
+    products are exact in float64 for the small shapes used here."""
+    return (rng.integers(lo * denom, hi * denom + 1, size=shape) / denom).astype(np.float32)
+
+
+def _rel(a, b):
+    scale = max(np.max(np.abs(b)), 1e-300)
+    return float(np.max(np.abs(a - b)) / scale)
+
+
+# --------------------------------------------------------------------------
+# forward pins
+# --------------------------------------------------------------------------
+
+def pin_golden(impl):
+    """Hand-worked examples in tests/golden/hand_examples.json."""
+    with open(GOLDEN) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        q = np.array(c["q"], np.float32)[None]
+        k = np.array(c["k"], np.float32)[None]
+        v = np.array(c["v"], np.float32)[None]
+        out = impl.fwd(q, k, v)[0]
+        assert np.array_equal(out, np.array(c["out"], np.float64)), (c["name"], out)
+        if "g" in c:
+            g = np.array(c["g"], np.float32)[None]
+            dq, dk, dv = impl.bwd(q, k, v, g)
+            for name, got in (("dq", dq), ("dk", dk), ("dv", dv)):
+                assert np.array_equal(got[0], np.array(c[name], np.float64)), (c["name"], name, got[0])
+
+
+def brute_force_fwd(q, k, v):
+    """(Q K^T masked to j <= i) V, in float64 -- quadratic, no recurrence."""
+    q, k, v = (np.asarray(t, np.float64) for t in (q, k, v))
+    N = q.shape[-2]
+    A = q @ np.swapaxes(k, -1, -2)
+    A = A * np.tril(np.ones((N, N)))
+    return A @ v
+
+
+def brute_force_bwd(q, k, v, g):
+    """Matrix-calculus form of the gradient of <g, (QK^T * tril) V>."""
+    q, k, v, g = (np.asarray(t, np.float64) for t in (q, k, v, g))
+    N = q.shape[-2]
+    L = np.tril(np.ones((N, N)))
+    T = lambda x: np.swapaxes(x, -1, -2)
+    GV = (g @ T(v)) * L          # [i, j] = g_i . v_j for j <= i
+    QK = (q @ T(k)) * L          # [i, j] = q_i . k_j for j <= i
+    return GV @ k, T(GV) @ q, T(QK) @ g
+
+
+def pin_brute_force(impl, shapes=((1, 1, 1, 1, 1), (2, 2, 17, 16, 16), (1, 3, 64, 8, 5),
+                                  (2, 1, 33, 3, 12))):
+    for s, (B, H, N, D, M) in enumerate(shapes):
+        rng = _rng(100 + s)
+        q, k = _pos(rng, (B, H, N, D)), _pos(rng, (B, H, N, D))
+        v = rng.standard_normal((B, H, N, M)).astype(np.float32)
+        got = impl.fwd(q, k, v)
+        ref = brute_force_fwd(q, k, v)
+        assert got.shape == ref.shape
+        assert _rel(got, ref) <= 1e-12, ("brute force", (B, H, N, D, M), _rel(got, ref))
+
+
+def pin_first_row_closed_form(impl):
+    """out_0 = (q_0 . k_0) v_0."""
+    rng = _rng(7)
+    q, k = _pos(rng, (2, 3, 9, 6)), _pos(rng, (2, 3, 9, 6))
+    v = rng.standard_normal((2, 3, 9, 4)).astype(np.float32)
+    out = impl.fwd(q, k, v)
+    qk = np.sum(q[..., 0, :].astype(np.float64) * k[..., 0, :], axis=-1)
+    ref = qk[..., None] * v[..., 0, :].astype(np.float64)
+    assert np.allclose(out[..., 0, :], ref, rtol=1e-14, atol=0), "first row"
+
+
+def pin_last_row_is_noncausal(impl):
+    """out_{N-1} = q_{N-1}^T (K^T V): the last row sees every key, so it is
+    non-causal linear attention, a plain matrix product."""
+    rng = _rng(8)
+    q, k = _pos(rng, (1, 2, 40, 7)), _pos(rng, (1, 2, 40, 7))
+    v = rng.standard_normal((1, 2, 40, 5)).astype(np.float32)
+    out = impl.fwd(q, k, v)
+    KV = np.einsum("bhnd,bhnm->bhdm", k.astype(np.float64), v.astype(np.float64))
+    ref = np.einsum("bhd,bhdm->bhm", q[..., -1, :].astype(np.float64), KV)
+    assert _rel(out[..., -1, :], ref) <= 1e-12, "last row"
+
+
+def pin_scalar_cumsum(impl):
+    """D = M = 1: out = q * cumsum(k * v), a textbook prefix sum."""
+    rng = _rng(9)
+    q = rng.standard_normal((3, 2, 50, 1)).astype(np.float32)
+    k = rng.standard_normal((3, 2, 50, 1)).astype(np.float32)
+    v = rng.standard_normal((3, 2, 50, 1)).astype(np.float32)
+    out = impl.fwd(q, k, v)
+    ref = q.astype(np.float64) * np.cumsum(k.astype(np.float64) * v, axis=-2)
+    assert _rel(out, ref) <= 1e-13, "D=M=1 cumsum"
+
+
+def pin_ones_cumsum(impl):
+    """q = k = 1: out_i = D * sum_{j<=i} v_j."""
+    rng = _rng(10)
+    D = 6
+    q = np.ones((1, 2, 30, D), np.float32)
+    v = rng.standard_normal((1, 2, 30, 4)).astype(np.float32)
+    out = impl.fwd(q, q.copy(), v)
+    ref = D * np.cumsum(v.astype(np.float64), axis=-2)
+    assert _rel(out, ref) <= 1e-13, "q=k=1 cumsum"
+
+
+def pin_zero_value(impl):
+    """v = 0 gives exactly 0 in every column (column 0 included)."""
+    rng = _rng(11)
+    q, k = _pos(rng, (1, 2, 20, 4)), _pos(rng, (1, 2, 20, 4))
+    v = np.zeros((1, 2, 20, 4), np.float32)
+    assert np.all(impl.fwd(q * 100, k, v) == 0.0), "v=0"
+    assert np.all(impl.fwd(q, k * 0, _pos(rng, (1, 2, 20, 4))) == 0.0), "k=0"
+
+
+def pin_linearity(impl):
+    """Linear in v and in q (dyadic inputs and scalars keep it exact)."""
+    rng = _rng(12)
+    q, k = _dyadic(rng, (1, 2, 24, 5)), _dyadic(rng, (1, 2, 24, 5))
+    v1, v2 = _dyadic(rng, (1, 2, 24, 3)), _dyadic(rng, (1, 2, 24, 3))
+    a, b = 0.5, -2.0
+    lhs = impl.fwd(q, k, (a * v1 + b * v2).astype(np.float32))
+    rhs = a * impl.fwd(q, k, v1) + b * impl.fwd(q, k, v2)
+    assert np.allclose(lhs, rhs, rtol=1e-13, atol=1e-13), "linear in v"
+    q2 = _dyadic(rng, (1, 2, 24, 5))
+    lhs = impl.fwd((a * q + b * q2).astype(np.float32), k, v1)
+    rhs = a * impl.fwd(q, k, v1) + b * impl.fwd(q2, k, v1)
+    assert np.allclose(lhs, rhs, rtol=1e-13, atol=1e-13), "linear in q"
+
+
+def pin_causality(impl):
+    """Changing k_j, v_j for j > i leaves out_i bitwise unchanged, and
+    changing q_j leaves every other row unchanged."""
+    rng = _rng(13)
+    N, cut = 32, 19
+    q, k = _pos(rng, (1, 1, N, 4)), _pos(rng, (1, 1, N, 4))
+    v = rng.standard_normal((1, 1, N, 3)).astype(np.float32)
+    base = impl.fwd(q, k, v)
+    k2, v2 = k.copy(), v.copy()
+    k2[..., cut + 1:, :] = _pos(rng, k2[..., cut + 1:, :].shape)
+    v2[..., cut + 1:, :] = rng.standard_normal(v2[..., cut + 1:, :].shape)
+    pert = impl.fwd(q, k2, v2)
+    assert np.array_equal(base[..., :cut + 1, :], pert[..., :cut + 1, :]), "future leaked"
+    assert not np.array_equal(base[..., cut + 1:, :], pert[..., cut + 1:, :]), "future ignored"
+    q3 = q.copy()
+    q3[..., cut, :] += 1.0
+    pert = impl.fwd(q3, k, v)
+    mask = np.ones(N, bool)
+    mask[cut] = False
+    assert np.array_equal(base[..., mask, :], pert[..., mask, :]), "q_i leaked to other rows"
+
+
+# --------------------------------------------------------------------------
+# backward pins
+# --------------------------------------------------------------------------
+
+def pin_finite_differences(impl, shape=(1, 2, 7, 3, 2)):
+    """dL/dx for L = <g, out> by central differences in every coordinate.
+
+    out is linear in each of q, k and v separately, so the central
+    difference with any step is exact up to rounding; dyadic inputs and a
+    unit step make it exact in float64.
+    """
+    B, H, N, D, M = shape
+    rng = _rng(14)
+    q, k = _dyadic(rng, (B, H, N, D)), _dyadic(rng, (B, H, N, D))
+    v, g = _dyadic(rng, (B, H, N, M)), _dyadic(rng, (B, H, N, M))
+    dq, dk, dv = impl.bwd(q, k, v, g)
+    g64 = g.astype(np.float64)
+
+    def loss(qq, kk, vv):
+        return float(np.sum(impl.fwd(qq, kk, vv) * g64))
+
+    for name, x, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        fd = np.zeros(x.shape, np.float64)
+        for idx in np.ndindex(*x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += 1.0
+            xm[idx] -= 1.0
+            args_p = {"q": q, "k": k, "v": v}
+            args_m = dict(args_p)
+            args_p[name], args_m[name] = xp, xm
+            fd[idx] = (loss(args_p["q"], args_p["k"], args_p["v"])
+                       - loss(args_m["q"], args_m["k"], args_m["v"])) / 2.0
+        assert np.allclose(grad, fd, rtol=1e-12, atol=1e-12), ("finite differences", name)
+
+
+def pin_bwd_brute_force(impl, shapes=((2, 2, 19, 8, 6), (1, 1, 64, 16, 16), (1, 2, 5, 1, 3))):
+    for s, (B, H, N, D, M) in enumerate(shapes):
+        rng = _rng(200 + s)
+        q, k = _pos(rng, (B, H, N, D)), _pos(rng, (B, H, N, D))
+        v = rng.standard_normal((B, H, N, M)).astype(np.float32)
+        g = rng.standard_normal((B, H, N, M)).astype(np.float32)
+        got = impl.bwd(q, k, v, g)
+        ref = brute_force_bwd(q, k, v, g)
+        for name, a, b in zip(("dq", "dk", "dv"), got, ref):
+            assert _rel(a, b) <= 1e-12, ("bwd brute force", name, (B, H, N, D, M), _rel(a, b))
+
+
+def pin_bwd_identities(impl):
+    """The gradients are causal products themselves:
+    dQ = fwd(g, v, k); dV = flip(fwd(flip k, flip q, flip g));
+    dK = flip(fwd(flip v, flip g, flip q)), flip = reverse the sequence."""
+    rng = _rng(15)
+    B, H, N, D, M = 1, 2, 23, 6, 4
+    q, k = _pos(rng, (B, H, N, D)), _pos(rng, (B, H, N, D))
+    v = rng.standard_normal((B, H, N, M)).astype(np.float32)
+    g = rng.standard_normal((B, H, N, M)).astype(np.float32)
+    dq, dk, dv = impl.bwd(q, k, v, g)
+    f = lambda x: np.ascontiguousarray(x[..., ::-1, :])
+    assert _rel(dq, impl.fwd(g, v, k)) <= 1e-13, "dq identity"
+    assert _rel(dv, f(impl.fwd(f(k), f(q), f(g)))) <= 1e-13, "dv identity"
+    assert _rel(dk, f(impl.fwd(f(v), f(g), f(q)))) <= 1e-13, "dk identity"
+
+
+FWD_PINS = [pin_golden, pin_brute_force, pin_first_row_closed_form, pin_last_row_is_noncausal,
+            pin_scalar_cumsum, pin_ones_cumsum, pin_zero_value, pin_linearity, pin_causality]
+BWD_PINS = [pin_finite_differences, pin_bwd_brute_force, pin_bwd_identities]
+ALL_PINS = FWD_PINS + BWD_PINS

@@ -1,0 +1,99 @@
+"""Planted mistakes in a copy of the oracle must trip at least one pin.
+
+Each mutant is the oracle's C source with one plausible mistake (a dropped
+term, a wrong operand, a wrong index, an exclusive instead of inclusive
+prefix, a transposed state) compiled into a temporary library and run
+through the same pins as the real oracle.  Nothing here touches the real
+oracle's build.
+"""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "causal_product_oracle.c")
+
+MUTANTS = {
+    # readout with the key instead of the query (the listing's own TODO)
+    "readout_uses_key": [("double qd = qi[d];", "double qd = ki[d];")],
+    # half-weight state update (a scaled term)
+    "scaled_update": [("for (int64_t m = 0; m < M; ++m) Sd[m] += kd * vi[m];\n        }\n        /* readout",
+                       "for (int64_t m = 0; m < M; ++m) Sd[m] += 0.5 * kd * vi[m];\n        }\n        /* readout")],
+    # query of the previous row
+    "query_off_by_one": [("*qi = q + i * D;", "*qi = q + (i > 0 ? i - 1 : 0) * D;")],
+    # exclusive prefix: row i is taken out of the state for its own readout
+    "exclusive_prefix": [
+        ("/* readout: out_i = S^T q_i */",
+         "for (int64_t d = 0; d < D; ++d) for (int64_t m = 0; m < M; ++m) S[d * M + m] -= ki[d] * vi[m];"),
+        ("for (int64_t m = 0; m < M; ++m) oi[m] += qd * Sd[m];\n        }\n    }\n}",
+         "for (int64_t m = 0; m < M; ++m) oi[m] += qd * Sd[m];\n        }\n"
+         "        for (int64_t d = 0; d < D; ++d) for (int64_t m = 0; m < M; ++m) S[d * M + m] += ki[d] * vi[m];\n    }\n}")],
+    # dq with the value instead of the output gradient
+    "dq_uses_v": [("acc += Sd[m] * gi[m];", "acc += Sd[m] * vi[m];")],
+    # reverse sweep skips row 0
+    "reverse_drops_row0": [("for (int64_t j = N - 1; j >= 0; --j) {", "for (int64_t j = N - 1; j >= 1; --j) {")],
+    # dv with the query instead of the key
+    "dv_uses_q": [("double kd = kj[d];", "double kd = qj[d];")],
+    # reverse state accumulates k g^T instead of q g^T
+    "reverse_state_uses_k": [("double qd = qj[d];", "double qd = kj[d];")],
+    # dk reads the state transposed (indices kept in bounds for any D, M)
+    "dk_transposed": [("for (int64_t m = 0; m < M; ++m) acc += Rd[m] * vj[m];",
+                       "for (int64_t m = 0; m < M; ++m) acc += R[(m % D) * M + (d % M)] * vj[m];")],
+}
+
+
+class _Impl:
+    def __init__(self, path):
+        lib = ctypes.CDLL(path)
+        i64, p, c_int = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+        lib.cpo_fwd.argtypes = [p, p, p, p, i64, i64, i64, i64, c_int]
+        lib.cpo_bwd.argtypes = [p, p, p, p, p, p, p, i64, i64, i64, i64, c_int]
+        self.lib = lib
+
+    def fwd(self, q, k, v):
+        q, k, v = (np.ascontiguousarray(x, np.float32) for x in (q, k, v))
+        lead = q.shape[:-2]
+        BH = int(np.prod(lead)) if lead else 1
+        N, D, M = q.shape[-2], q.shape[-1], v.shape[-1]
+        out = np.zeros(lead + (N, M))
+        rc = self.lib.cpo_fwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, out.ctypes.data,
+                              BH, N, D, M, 1)
+        assert rc == 0
+        return out
+
+    def bwd(self, q, k, v, g):
+        q, k, v, g = (np.ascontiguousarray(x, np.float32) for x in (q, k, v, g))
+        lead = q.shape[:-2]
+        BH = int(np.prod(lead)) if lead else 1
+        N, D, M = q.shape[-2], q.shape[-1], v.shape[-1]
+        dq, dk, dv = np.zeros(lead + (N, D)), np.zeros(lead + (N, D)), np.zeros(lead + (N, M))
+        rc = self.lib.cpo_bwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, g.ctypes.data,
+                              dq.ctypes.data, dk.ctypes.data, dv.ctypes.data, BH, N, D, M, 1)
+        assert rc == 0
+        return dq, dk, dv
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    src = open(SRC).read()
+    for old, new in MUTANTS[name]:
+        assert src.count(old) == 1, f"mutation site for {name} not unique/present"
+        src = src.replace(old, new)
+    mpath = tmp_path / f"{name}.c"
+    mpath.write_text(src)
+    lib = tmp_path / f"lib{name}.so"
+    subprocess.run(["gcc", "-O1", "-fopenmp", "-shared", "-fPIC", "-std=c11", "-o", str(lib),
+                    str(mpath)], check=True)
+    impl = _Impl(str(lib))
+    caught = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin(impl)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"mutant {name} passed every pin"
