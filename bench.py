@@ -1,0 +1,399 @@
+#!/usr/bin/env python3
+"""Benchmark of the causal dot product (forward + backward) on GB300.
+
+One step = causal_product_fwd + causal_product_bwd over one batch of the
+bf16 workload B=8, H=16, N=4096, D=M=64 (inputs resident in HBM when the
+timed region starts; every input is larger than the 129 MB L2, so no flush
+is needed between iterations).  Prints ONE JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs the same per-GPU workload (weak scaling, no
+collective on the data path); the timed region is bracketed by a barrier
+and the maximum over ranks is reported.
+
+--impl reference times the fp64 CPU oracle (the plain recurrence) on the
+host cores, on a bounded sample of the same workload, in the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "bf16_b8h16_n4096_d64"
+METRIC = "causal-product fwd+bwd Mtokens/s·head"
+UNIT = "Mtok·head/s"
+
+# DRAM traffic of one launch of the tensor-core kernel measured by ncu
+# (dram__bytes_read.sum + dram__bytes_write.sum) together with the SHA-256 of
+# the kernel source it was measured on; a changed source reports null.
+PROFILED_TRAFFIC = {"source_sha256": None, "bytes_per_launch": None}
+
+
+def _env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def dist_setup():
+    world = _env_int("WORLD_SIZE", 1)
+    rank = _env_int("RANK", 0)
+    local = _env_int("LOCAL_RANK", 0)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" \
+        else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for r in csv.reader(io.StringIO(self.out or "")):
+            if len(r) < 9:
+                continue
+            try:
+                rows.append([x.strip() for x in r])
+            except Exception:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def kernel_sha():
+    h = hashlib.sha256()
+    for f in ("cp_tc.cu", "sm103_ptx.cuh"):
+        with open(os.path.join(ROOT, "prefix_sum_outer_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def algorithmic_bytes(w):
+    """Bytes the method must move per step: forward reads q, k, v and writes
+    out; backward reads q, k, v, g and writes dq, dk, dv."""
+    s = 2 if w.dtype == "bf16" else 4
+    per_th = s * (2 * w.D + 2 * w.M) + s * (4 * w.D + 3 * w.M)
+    return per_th * w.token_heads
+
+
+def cpu_baseline(w, budget_s=10.0):
+    """The oracle as it stands, all host cores, on a bounded sample of the
+    workload: the first `n` (b,h) slices, forward + backward."""
+    import oracle
+    from prefix_sum_outer_gb300.workloads import make_inputs
+    f = lambda t: t.float().numpy()
+    # calibrate on one slice, then size the sample for ~budget_s
+    q, k, v, g = make_inputs(1, 1, w.N, w.D, w.M, w.torch_dtype, seed=w.seed, feature=w.feature,
+                             x_std=w.x_std)
+    t0 = time.perf_counter()
+    oracle.fwd(f(q), f(k), f(v))
+    oracle.bwd(f(q), f(k), f(v), f(g))
+    one = time.perf_counter() - t0
+    cores = oracle.threads(0)
+    n = int(max(1, min(w.B * w.H, round(budget_s * cores / max(one, 1e-6)))))
+    q, k, v, g = make_inputs(1, n, w.N, w.D, w.M, w.torch_dtype, seed=w.seed, feature=w.feature,
+                             x_std=w.x_std)
+    qn, kn, vn, gn = f(q), f(k), f(v), f(g)
+    t0 = time.perf_counter()
+    oracle.fwd(qn, kn, vn)
+    oracle.bwd(qn, kn, vn, gn)
+    dt = time.perf_counter() - t0
+    return {"value": n * w.N / dt / 1e6, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {w.B * w.H} (b,h) slices x N={w.N}, fwd+bwd, fp64 C oracle, "
+                      f"{dt:.1f} s"}
+
+
+def run_reference(args, world, rank):
+    from prefix_sum_outer_gb300.workloads import WORKLOADS
+    if rank != 0:
+        return 0
+    import oracle
+    w = WORKLOADS[args.workload]
+    from prefix_sum_outer_gb300.workloads import make_inputs
+    f = lambda t: t.float().numpy()
+    cores = oracle.threads(0)
+    # size one step at ~3 s of oracle work
+    q, k, v, g = make_inputs(1, 1, w.N, w.D, w.M, w.torch_dtype, seed=w.seed, feature=w.feature,
+                             x_std=w.x_std)
+    t0 = time.perf_counter()
+    oracle.fwd(f(q), f(k), f(v))
+    oracle.bwd(f(q), f(k), f(v), f(g))
+    one = time.perf_counter() - t0
+    n = int(max(1, min(w.B * w.H, round(3.0 * cores / max(one, 1e-6)))))
+    q, k, v, g = make_inputs(1, n, w.N, w.D, w.M, w.torch_dtype, seed=w.seed, feature=w.feature,
+                             x_std=w.x_std)
+    qn, kn, vn, gn = f(q), f(k), f(v), f(g)
+    for _ in range(args.warmup):
+        oracle.fwd(qn, kn, vn)
+        oracle.bwd(qn, kn, vn, gn)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.fwd(qn, kn, vn)
+        oracle.bwd(qn, kn, vn, gn)
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    value = n * w.N / dt / 1e6
+    sample = f"{n} of {w.B * w.H} (b,h) slices x N={w.N} per step, fwd+bwd, fp64 C oracle"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N,
+                                        "D": w.D, "M": w.M, "input_dtype": w.dtype},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import prefix_sum_outer_gb300 as cp
+    from prefix_sum_outer_gb300.workloads import WORKLOADS, make_inputs
+
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device (the product has no CPU path)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = WORKLOADS[args.workload]
+    q, k, v, g = make_inputs(w.B, w.H, w.N, w.D, w.M, w.torch_dtype, seed=w.seed + 1000 * rank,
+                             feature=w.feature, x_std=w.x_std, backward=True)
+    qd, kd, vd, gd = (t.to(dev) for t in (q, k, v, g))
+    out = torch.empty_like(vd)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws_f = torch.empty(cp.causal_product_workspace_size(w.B, w.H, w.N, w.D, w.M, w.torch_dtype,
+                                                        False), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(cp.causal_product_workspace_size(w.B, w.H, w.N, w.D, w.M, w.torch_dtype,
+                                                        True), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        cp.causal_product_fwd(qd, kd, vd, out=out, workspace=ws_f, stream=stream)
+        cp.causal_product_bwd(qd, kd, vd, gd, dq, dk, dv, workspace=ws_b, stream=stream)
+
+    # kernels of ours launched per step (tensor-core path): forward 1 product,
+    # backward 3 products; a product split into segments adds one aggregate launch
+    from ctypes import c_int  # noqa: F401
+    launches_per_step = _launches_per_step(w)
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    if cp.causal_product_status(ws_f) != cp.CP_OK or cp.causal_product_status(ws_b) != cp.CP_OK:
+        raise RuntimeError("kernel status word reports an error after warm-up")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        time.sleep(0.3)  # let the sampler start
+        for e0, e1, e2 in ev:
+            e0.record(stream)
+            cp.causal_product_fwd(qd, kd, vd, out=out, workspace=ws_f, stream=stream)
+            e1.record(stream)
+            cp.causal_product_bwd(qd, kd, vd, gd, dq, dk, dv, workspace=ws_b, stream=stream)
+            e2.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    total_ms = ev[0][0].elapsed_time(ev[-1][2])
+    fwd_ms = sum(a.elapsed_time(b) for a, b, _ in ev)
+    bwd_ms = sum(b.elapsed_time(c) for _, b, c in ev)
+    total_ms = max_over_ranks(total_ms, world)
+    ms_per_step = total_ms / args.steps
+    value = w.token_heads * world * args.steps / (total_ms / 1e3) / 1e6
+
+    # ---- end to end: pinned host buffers in, results back to the host
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, hg = (t.pin_memory() for t in (q, k, v, g))
+        ho, hdq, hdk, hdv = (torch.empty(t.shape, dtype=t.dtype).pin_memory()
+                             for t in (out, dq, dk, dv))
+
+        def e2e_step():
+            qd.copy_(hq, non_blocking=True)
+            kd.copy_(hk, non_blocking=True)
+            vd.copy_(hv, non_blocking=True)
+            gd.copy_(hg, non_blocking=True)
+            step()
+            ho.copy_(out, non_blocking=True)
+            hdq.copy_(dq, non_blocking=True)
+            hdk.copy_(dk, non_blocking=True)
+            hdv.copy_(dv, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_e2e = max(3, min(args.steps, 10))
+        s0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(s0.elapsed_time(s1), world)
+        h2d = sum(t.numel() * t.element_size() for t in (q, k, v, g))
+        d2h = sum(t.numel() * t.element_size() for t in (out, dq, dk, dv))
+        e2e = {"value": w.token_heads * world * n_e2e / (e2e_ms / 1e3) / 1e6, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e}
+
+    # ---- roofline of the dominant kernel (the tensor-core causal-product kernel)
+    hbm_gbs, bf16_tf, peak_src = load_peaks()
+    s = 2 if w.dtype == "bf16" else 4
+    # every launch is one causal product over (BH, N) with D' + D' + M' + M'
+    # columns moved per row (q', k', v' read, out' written); for D = M all
+    # four products of a step move the same bytes
+    bytes_per_launch = s * (2 * w.D + 2 * w.M) * w.token_heads
+    n_products = 4
+    avg_launch_ms = (fwd_ms + bwd_ms) / (args.steps * n_products)
+    achieved = bytes_per_launch / (avg_launch_ms / 1e3) / 1e9
+    traffic = None
+    if PROFILED_TRAFFIC["source_sha256"] == kernel_sha():
+        traffic = PROFILED_TRAFFIC["bytes_per_launch"]
+    step_roofline_ms = algorithmic_bytes(w) / (hbm_gbs * 1e9) * 1e3
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "M": w.M,
+                   "features": w.feature, "l2": "inputs larger than L2 (no flush)",
+                   "fwd_ms": fwd_ms / args.steps, "bwd_ms": bwd_ms / args.steps,
+                   "step_hbm_roofline_frac": step_roofline_ms / ms_per_step,
+                   "parallelism": f"replicas x{world} (b,h)-sharded, no collective"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                     "frac": achieved / hbm_gbs, "traffic": traffic,
+                     "kernel": "tc_causal_kernel (one causal product per launch)",
+                     "peak_source": f"{peak_src} hbm_gbs",
+                     "bytes_per_launch": bytes_per_launch, "avg_launch_ms": avg_launch_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def _launches_per_step(w):
+    import prefix_sum_outer_gb300 as cp
+    lib = cp.load_library()
+    # a workspace larger than the status word means a segmented (two-launch) product
+    ws_fwd = lib.causal_product_workspace_size(w.B, w.H, w.N, w.D, w.M, 1, 0)
+    per_product = 2 if ws_fwd > 256 else 1
+    return 4 * per_product
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    world, rank, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            return run_reference(args, world, rank)
+        return run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

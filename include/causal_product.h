@@ -1,0 +1,118 @@
+/*
+ * causal_product.h -- C ABI of libcausal_product.so
+ *
+ * The causal dot product of causal linear attention, batched over
+ * batch x heads.  For every (b, h), with q, k in R^{N x D} and v in R^{N x M}:
+ *
+ *     out_i = sum_{j <= i} (q_i . k_j) v_j  =  S_i^T q_i,
+ *     S_i   = sum_{j <= i} k_j v_j^T        (a D x M running state).
+ *
+ * This is the prefix sum over the sequence that triton-lang/triton issue
+ * #217 ("Dot Product Computes Wrong Values") sets out to batch-parallelise
+ * (its opening comment names Algorithm 1 of "Transformers are RNNs"); the
+ * loop listing in that issue adds the outer product of the key and value
+ * rows to the state before reading the output out with the query, so row i
+ * includes j = i.  No normaliser and no 1/sqrt(D) scale are applied.
+ *
+ * The backward pass (not printed on the pages; derived from the
+ * definition with L = sum_i <g_i, out_i>) is
+ *
+ *     dq_i = sum_{j <= i} (g_i . v_j) k_j,
+ *     dk_j = sum_{i >= j} (g_i . v_j) q_i,
+ *     dv_j = sum_{i >= j} (q_i . k_j) g_i.
+ *
+ * Layout and ownership (every entry point):
+ *   - q, k, grad_q, grad_k: contiguous row-major [B][H][N][D];
+ *     v, out, grad_out, grad_v: contiguous row-major [B][H][N][M].
+ *     All are DEVICE pointers owned by the caller, 16-byte aligned.
+ *   - Outputs are written, never accumulated into, in the input dtype.
+ *     Outputs must not alias inputs.
+ *   - Accumulation and the running state are fp32 for both dtypes;
+ *     bf16 outputs are rounded to nearest-even once, at the end.
+ *   - All work is enqueued on `stream` (cudaStream_t; NULL = legacy default
+ *     stream).  No entry point synchronises the host except
+ *     causal_product_status().
+ *   - `workspace` is device scratch of at least
+ *     causal_product_workspace_size(...) bytes, owned by the caller, used
+ *     only until the enqueued work completes; it holds the per-segment fp32
+ *     state aggregates of the two-pass scan and a status word, which every
+ *     call resets (asynchronously, on `stream`) before its kernels run.  Passing
+ *     workspace = NULL makes the call allocate and free scratch itself
+ *     with cudaMallocAsync / cudaFreeAsync on `stream`; its status word is
+ *     then not observable.
+ *   - Concurrent calls on different streams need separate workspaces.
+ *
+ * Supported shapes: B, H >= 1; N >= 0 (N = 0 returns CP_OK and enqueues
+ * nothing); 1 <= D, M <= 256.  bf16 additionally needs D and M to be
+ * multiples of 8 (16-byte rows for the tensor-memory-access engine).
+ *
+ * Errors are reported before anything is enqueued (argument checks) or as
+ * CP_ERR_CUDA for a failed launch.  A kernel that finds one of its internal
+ * waits has not completed within about two seconds records
+ * CP_ERR_TIMEOUT in the workspace status word and returns early (its
+ * outputs are then undefined); causal_product_status() reads that word.
+ */
+#ifndef CAUSAL_PRODUCT_H_
+#define CAUSAL_PRODUCT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CP_DTYPE_F32 = 0,  /* fp32 in/out; fp32 FMA arithmetic (no TF32 rounding) */
+  CP_DTYPE_BF16 = 1  /* bf16 in/out; bf16 tensor-core products, fp32 accumulate */
+} cp_dtype_t;
+
+typedef enum {
+  CP_OK = 0,
+  CP_ERR_INVALID_ARG = 1,        /* null pointer, negative size, aliasing outputs */
+  CP_ERR_UNSUPPORTED_SHAPE = 2,  /* D or M outside [1, 256], or not a multiple of 8 (bf16) */
+  CP_ERR_UNSUPPORTED_DTYPE = 3,
+  CP_ERR_MISALIGNED = 4,         /* a pointer is not 16-byte aligned */
+  CP_ERR_WORKSPACE_TOO_SMALL = 5,
+  CP_ERR_CUDA = 6,               /* a CUDA runtime/driver call failed */
+  CP_ERR_TIMEOUT = 7,            /* a kernel's bounded wait expired (status word) */
+  CP_ERR_NO_DEVICE = 8           /* no usable sm_103 device */
+} cp_status_t;
+
+/* Bytes of device workspace causal_product_fwd (backward = 0) or
+ * causal_product_bwd (backward = 1) needs for this problem; always >= 256
+ * (the status word), a multiple of 256.  Pure host computation.  Returns 0
+ * for arguments the entry points would reject. */
+size_t causal_product_workspace_size(int64_t B, int64_t H, int64_t N, int64_t D, int64_t M,
+                                     cp_dtype_t dtype, int backward);
+
+/* Forward: out[b,h,i,:] = sum_{j<=i} (q[b,h,i,:] . k[b,h,j,:]) v[b,h,j,:].
+ * `stream` is a cudaStream_t passed as void*. */
+cp_status_t causal_product_fwd(const void* q, const void* k, const void* v, void* out,
+                               int64_t B, int64_t H, int64_t N, int64_t D, int64_t M,
+                               cp_dtype_t dtype, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/* Backward: given grad_out = dL/dout, writes grad_q, grad_k, grad_v (the
+ * formulas in the header comment).  Three causal products: dq is the
+ * forward product of (grad_out, v, k); dv and dk are reverse-order products
+ * of (k, q, grad_out) and (v, grad_out, q). */
+cp_status_t causal_product_bwd(const void* q, const void* k, const void* v, const void* grad_out,
+                               void* grad_q, void* grad_k, void* grad_v,
+                               int64_t B, int64_t H, int64_t N, int64_t D, int64_t M,
+                               cp_dtype_t dtype, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/* Synchronises `stream`, then returns and clears the status word in
+ * `workspace` (CP_OK or CP_ERR_TIMEOUT), or CP_ERR_CUDA if the stream
+ * reports an error. */
+cp_status_t causal_product_status(void* workspace, void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* causal_product_error_string(cp_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CAUSAL_PRODUCT_H_ */

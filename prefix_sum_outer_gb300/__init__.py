@@ -1,0 +1,198 @@
+"""GB300-native causal dot product (causal linear attention's prefix sum).
+
+Python face of ``libcausal_product.so`` (C ABI in ``include/causal_product.h``).
+This module only marshals arguments: every step of the computation runs in
+the library's CUDA kernels.  PyTorch supplies device memory and streams.
+
+    out = causal_product(q, k, v)              # autograd-aware
+    causal_product_fwd(q, k, v, out)           # raw entry points, same names
+    causal_product_bwd(q, k, v, g, dq, dk, dv) #   as the C ABI
+
+q, k: [B, H, N, D]; v: [B, H, N, M]; all contiguous, on one CUDA device,
+dtype float32 or bfloat16.  out_i = sum_{j<=i} (q_i . k_j) v_j.
+
+There is no fallback: if the library cannot be built or loaded, every call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "CP_OK", "CausalProductError", "causal_product", "causal_product_fwd", "causal_product_bwd",
+    "causal_product_workspace_size", "causal_product_status", "causal_product_error_string",
+    "library_path", "load_library",
+]
+
+CP_DTYPE_F32, CP_DTYPE_BF16 = 0, 1
+CP_OK = 0
+_DTYPES = {torch.float32: CP_DTYPE_F32, torch.bfloat16: CP_DTYPE_BF16}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class CausalProductError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = int(code)
+        super().__init__(f"{where}: {causal_product_error_string(code)}")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(rebuild: bool = True) -> ctypes.CDLL:
+    """Load the C ABI library (building it first if its sources changed)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build() if rebuild else _build.LIB
+            if not os.path.exists(path):
+                raise RuntimeError(f"libcausal_product.so not found at {path}")
+            lib = ctypes.CDLL(path)
+            p, i64, c_int, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+            lib.causal_product_workspace_size.argtypes = [i64, i64, i64, i64, i64, c_int, c_int]
+            lib.causal_product_workspace_size.restype = sz
+            lib.causal_product_fwd.argtypes = [p, p, p, p, i64, i64, i64, i64, i64, c_int, p, sz, p]
+            lib.causal_product_fwd.restype = c_int
+            lib.causal_product_bwd.argtypes = [p, p, p, p, p, p, p, i64, i64, i64, i64, i64, c_int,
+                                               p, sz, p]
+            lib.causal_product_bwd.restype = c_int
+            lib.causal_product_status.argtypes = [p, p]
+            lib.causal_product_status.restype = c_int
+            lib.causal_product_error_string.argtypes = [c_int]
+            lib.causal_product_error_string.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def causal_product_error_string(code: int) -> str:
+    return load_library().causal_product_error_string(int(code)).decode()
+
+
+def _dims(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor):
+    if q.dim() != 4 or k.shape != q.shape or v.dim() != 4 or v.shape[:3] != q.shape[:3]:
+        raise ValueError(f"expected q,k [B,H,N,D] and v [B,H,N,M]; got {tuple(q.shape)}, "
+                         f"{tuple(k.shape)}, {tuple(v.shape)}")
+    B, H, N, D = q.shape
+    return B, H, N, D, v.shape[3]
+
+
+def _dtype_code(*ts: torch.Tensor) -> int:
+    dt = ts[0].dtype
+    if dt not in _DTYPES or any(t.dtype != dt for t in ts):
+        raise TypeError(f"all tensors must share one dtype in {list(_DTYPES)}; "
+                        f"got {[t.dtype for t in ts]}")
+    return _DTYPES[dt]
+
+
+def _check_device(*ts: torch.Tensor):
+    dev = ts[0].device
+    if dev.type != "cuda":
+        raise RuntimeError("causal_product runs on CUDA tensors only (no CPU path)")
+    for t in ts:
+        if t.device != dev:
+            raise RuntimeError("all tensors must be on the same CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream], device) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return int(s.cuda_stream)
+
+
+def causal_product_workspace_size(B: int, H: int, N: int, D: int, M: int,
+                                  dtype: torch.dtype = torch.bfloat16,
+                                  backward: bool = False) -> int:
+    return int(load_library().causal_product_workspace_size(B, H, N, D, M, _DTYPES[dtype],
+                                                            int(bool(backward))))
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def causal_product_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                       out: Optional[torch.Tensor] = None,
+                       workspace: Optional[torch.Tensor] = None,
+                       stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """out[b,h,i] = sum_{j<=i} (q[b,h,i] . k[b,h,j]) v[b,h,j], enqueued on ``stream``."""
+    B, H, N, D, M = _dims(q, k, v)
+    code = _dtype_code(q, k, v)
+    if out is None:
+        out = torch.empty((B, H, N, M), dtype=q.dtype, device=q.device)
+    _check_device(q, k, v, out)
+    lib = load_library()
+    need = lib.causal_product_workspace_size(B, H, N, D, M, code, 0)
+    if workspace is None:
+        workspace = _workspace(need, q.device)
+    rc = lib.causal_product_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                B, H, N, D, M, code, workspace.data_ptr(), workspace.numel(),
+                                _stream_ptr(stream, q.device))
+    if rc != CP_OK:
+        raise CausalProductError(rc, "causal_product_fwd")
+    return out
+
+
+def causal_product_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, grad_out: torch.Tensor,
+                       grad_q: Optional[torch.Tensor] = None,
+                       grad_k: Optional[torch.Tensor] = None,
+                       grad_v: Optional[torch.Tensor] = None,
+                       workspace: Optional[torch.Tensor] = None,
+                       stream: Optional[torch.cuda.Stream] = None):
+    """(dq, dk, dv) of L = <grad_out, causal_product(q, k, v)>."""
+    B, H, N, D, M = _dims(q, k, v)
+    code = _dtype_code(q, k, v, grad_out)
+    if grad_out.shape != v.shape:
+        raise ValueError("grad_out must have v's shape")
+    grad_q = torch.empty_like(q) if grad_q is None else grad_q
+    grad_k = torch.empty_like(k) if grad_k is None else grad_k
+    grad_v = torch.empty_like(v) if grad_v is None else grad_v
+    _check_device(q, k, v, grad_out, grad_q, grad_k, grad_v)
+    lib = load_library()
+    need = lib.causal_product_workspace_size(B, H, N, D, M, code, 1)
+    if workspace is None:
+        workspace = _workspace(need, q.device)
+    rc = lib.causal_product_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), grad_out.data_ptr(),
+                                grad_q.data_ptr(), grad_k.data_ptr(), grad_v.data_ptr(),
+                                B, H, N, D, M, code, workspace.data_ptr(), workspace.numel(),
+                                _stream_ptr(stream, q.device))
+    if rc != CP_OK:
+        raise CausalProductError(rc, "causal_product_bwd")
+    return grad_q, grad_k, grad_v
+
+
+def causal_product_status(workspace: torch.Tensor,
+                          stream: Optional[torch.cuda.Stream] = None) -> int:
+    """Synchronise ``stream`` and return (and clear) the workspace status word."""
+    return int(load_library().causal_product_status(workspace.data_ptr(),
+                                                    _stream_ptr(stream, workspace.device)))
+
+
+class CausalProduct(torch.autograd.Function):
+    """Autograd wrapper: forward and backward both call the C ABI."""
+
+    @staticmethod
+    def forward(ctx, q, k, v):
+        q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+        ctx.save_for_backward(q, k, v)
+        return causal_product_fwd(q, k, v)
+
+    @staticmethod
+    def backward(ctx, g):
+        q, k, v = ctx.saved_tensors
+        return causal_product_bwd(q, k, v, g.contiguous().to(q.dtype))
+
+
+def causal_product(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor) -> torch.Tensor:
+    """Causal dot product with autograd support (no normaliser, no scale)."""
+    return CausalProduct.apply(q, k, v)

@@ -1,0 +1,204 @@
+// C ABI of libcausal_product.so: argument checks, planning, workspace
+// carving and the launches of the per-dtype kernels.  See
+// include/causal_product.h for the contract.
+#include <algorithm>
+#include <cstdint>
+
+#include "cp_internal.h"
+
+namespace cp {
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+cp_status_t check_dims(int64_t B, int64_t H, int64_t N, int64_t D, int64_t M, cp_dtype_t dtype) {
+  if (B <= 0 || H <= 0 || N < 0) return CP_ERR_INVALID_ARG;
+  if (dtype != CP_DTYPE_F32 && dtype != CP_DTYPE_BF16) return CP_ERR_UNSUPPORTED_DTYPE;
+  if (D < 1 || D > 256 || M < 1 || M > 256) return CP_ERR_UNSUPPORTED_SHAPE;
+  if (dtype == CP_DTYPE_BF16 && ((D % 8) != 0 || (M % 8) != 0)) return CP_ERR_UNSUPPORTED_SHAPE;
+  // index arithmetic inside the kernels uses 32-bit tile and problem counts
+  if (B * H > (int64_t)1 << 24 || N > (int64_t)1 << 31) return CP_ERR_UNSUPPORTED_SHAPE;
+  return CP_OK;
+}
+
+// Aggregate bytes one product of shape (BH, N, D', M') needs.
+size_t product_agg_bytes(int64_t BH, int64_t N, int64_t D, int64_t M, cp_dtype_t dtype) {
+  if (N == 0) return 0;
+  if (dtype == CP_DTYPE_F32) return simt_plan(BH, N, D, M).agg_bytes;
+  return tc_plan(BH, N, D, M).agg_bytes;
+}
+
+size_t workspace_bytes(int64_t BH, int64_t N, int64_t D, int64_t M, cp_dtype_t dtype,
+                       bool backward) {
+  size_t agg = product_agg_bytes(BH, N, D, M, dtype);
+  if (backward) {
+    // dq: (g, v, k) -> D' = M, M' = D ; dv: (k, q, g) -> D' = D, M' = M ;
+    // dk: (v, g, q) -> D' = M, M' = D.  They run one after another on the
+    // stream, so they share one aggregate area.
+    agg = std::max(agg, product_agg_bytes(BH, N, M, D, dtype));
+  }
+  return kStatusBytes + round_up(agg);
+}
+
+cp_status_t run_product(const Product& p, cp_dtype_t dtype, float* agg, int* status,
+                        cudaStream_t stream) {
+  if (dtype == CP_DTYPE_F32) {
+    const SimtPlan plan = simt_plan(p.BH, p.N, p.D, p.M);
+    return simt_launch(p, plan, agg, status, stream) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+  }
+  const TcPlan plan = tc_plan(p.BH, p.N, p.D, p.M);
+  return tc_launch(p, plan, agg, status, stream);
+}
+
+// Scratch for one call: the caller's workspace, or a stream-ordered
+// allocation released on the same stream when the call's work is enqueued.
+struct Scratch {
+  void* base = nullptr;
+  bool owned = false;
+  cudaStream_t stream = nullptr;
+  ~Scratch() {
+    if (owned && base != nullptr) cudaFreeAsync(base, stream);
+  }
+};
+
+cp_status_t acquire(Scratch& s, void* workspace, size_t workspace_bytes, size_t need,
+                    cudaStream_t stream) {
+  s.stream = stream;
+  if (workspace != nullptr) {
+    if (workspace_bytes < need) return CP_ERR_WORKSPACE_TOO_SMALL;
+    if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return CP_ERR_MISALIGNED;
+    s.base = workspace;
+    return CP_OK;
+  }
+  if (cudaMallocAsync(&s.base, need, stream) != cudaSuccess) {
+    s.base = nullptr;
+    return CP_ERR_CUDA;
+  }
+  s.owned = true;
+  return CP_OK;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+}  // namespace
+}  // namespace cp
+
+extern "C" {
+
+size_t causal_product_workspace_size(int64_t B, int64_t H, int64_t N, int64_t D, int64_t M,
+                                     cp_dtype_t dtype, int backward) {
+  if (cp::check_dims(B, H, N, D, M, dtype) != CP_OK) return 0;
+  return cp::workspace_bytes(B * H, N, D, M, dtype, backward != 0);
+}
+
+cp_status_t causal_product_fwd(const void* q, const void* k, const void* v, void* out, int64_t B,
+                               int64_t H, int64_t N, int64_t D, int64_t M, cp_dtype_t dtype,
+                               void* workspace, size_t workspace_bytes, void* stream_) {
+  cp_status_t st = cp::check_dims(B, H, N, D, M, dtype);
+  if (st != CP_OK) return st;
+  if (!q || !k || !v || !out) return CP_ERR_INVALID_ARG;
+  if (!cp::aligned16(q) || !cp::aligned16(k) || !cp::aligned16(v) || !cp::aligned16(out))
+    return CP_ERR_MISALIGNED;
+  const size_t es = dtype == CP_DTYPE_F32 ? 4 : 2;
+  const int64_t BH = B * H;
+  const size_t nqk = (size_t)BH * N * D * es, nv = (size_t)BH * N * M * es;
+  if (cp::overlaps(out, nv, q, nqk) || cp::overlaps(out, nv, k, nqk) ||
+      cp::overlaps(out, nv, v, nv))
+    return CP_ERR_INVALID_ARG;
+  const size_t need = cp::workspace_bytes(BH, N, D, M, dtype, false);
+  if (workspace != nullptr && workspace_bytes < need) return CP_ERR_WORKSPACE_TOO_SMALL;
+  if (N == 0) return CP_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  cp::Scratch s;
+  st = cp::acquire(s, workspace, workspace_bytes, need, stream);
+  if (st != CP_OK) return st;
+  int* status = static_cast<int*>(s.base);
+  float* agg = reinterpret_cast<float*>(static_cast<char*>(s.base) + cp::kStatusBytes);
+  if (cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess) return CP_ERR_CUDA;
+  cp::Product p{q, k, v, out, BH, N, D, M, false};
+  return cp::run_product(p, dtype, agg, status, stream);
+}
+
+cp_status_t causal_product_bwd(const void* q, const void* k, const void* v, const void* grad_out,
+                               void* grad_q, void* grad_k, void* grad_v, int64_t B, int64_t H,
+                               int64_t N, int64_t D, int64_t M, cp_dtype_t dtype, void* workspace,
+                               size_t workspace_bytes, void* stream_) {
+  cp_status_t st = cp::check_dims(B, H, N, D, M, dtype);
+  if (st != CP_OK) return st;
+  if (!q || !k || !v || !grad_out || !grad_q || !grad_k || !grad_v) return CP_ERR_INVALID_ARG;
+  const void* ptrs[7] = {q, k, v, grad_out, grad_q, grad_k, grad_v};
+  for (const void* p : ptrs)
+    if (!cp::aligned16(p)) return CP_ERR_MISALIGNED;
+  const size_t es = dtype == CP_DTYPE_F32 ? 4 : 2;
+  const int64_t BH = B * H;
+  const size_t nqk = (size_t)BH * N * D * es, nv = (size_t)BH * N * M * es;
+  const void* ins[4] = {q, k, v, grad_out};
+  const size_t in_sz[4] = {nqk, nqk, nv, nv};
+  void* outs[3] = {grad_q, grad_k, grad_v};
+  const size_t out_sz[3] = {nqk, nqk, nv};
+  for (int o = 0; o < 3; ++o) {
+    for (int i = 0; i < 4; ++i)
+      if (cp::overlaps(outs[o], out_sz[o], ins[i], in_sz[i])) return CP_ERR_INVALID_ARG;
+    for (int o2 = o + 1; o2 < 3; ++o2)
+      if (cp::overlaps(outs[o], out_sz[o], outs[o2], out_sz[o2])) return CP_ERR_INVALID_ARG;
+  }
+  const size_t need = cp::workspace_bytes(BH, N, D, M, dtype, true);
+  if (workspace != nullptr && workspace_bytes < need) return CP_ERR_WORKSPACE_TOO_SMALL;
+  if (N == 0) return CP_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  cp::Scratch s;
+  st = cp::acquire(s, workspace, workspace_bytes, need, stream);
+  if (st != CP_OK) return st;
+  int* status = static_cast<int*>(s.base);
+  float* agg = reinterpret_cast<float*>(static_cast<char*>(s.base) + cp::kStatusBytes);
+  if (cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess) return CP_ERR_CUDA;
+  // dq_i = sum_{j<=i} (g_i . v_j) k_j
+  cp::Product pq{grad_out, v, k, grad_q, BH, N, M, D, false};
+  // dv_j = sum_{i>=j} (k_j . q_i) g_i
+  cp::Product pv{k, q, grad_out, grad_v, BH, N, D, M, true};
+  // dk_j = sum_{i>=j} (v_j . g_i) q_i
+  cp::Product pk{v, grad_out, q, grad_k, BH, N, M, D, true};
+  st = cp::run_product(pq, dtype, agg, status, stream);
+  if (st == CP_OK) st = cp::run_product(pv, dtype, agg, status, stream);
+  if (st == CP_OK) st = cp::run_product(pk, dtype, agg, status, stream);
+  return st;
+}
+
+cp_status_t causal_product_status(void* workspace, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return CP_ERR_CUDA;
+  if (workspace == nullptr) return CP_OK;
+  int h = 0;
+  if (cudaMemcpy(&h, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return CP_ERR_CUDA;
+  if (h != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(workspace, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return CP_ERR_CUDA;
+  }
+  return h == 0 ? CP_OK : static_cast<cp_status_t>(h);
+}
+
+const char* causal_product_error_string(cp_status_t s) {
+  switch (s) {
+    case CP_OK: return "CP_OK";
+    case CP_ERR_INVALID_ARG: return "CP_ERR_INVALID_ARG: null pointer, bad size or aliasing outputs";
+    case CP_ERR_UNSUPPORTED_SHAPE: return "CP_ERR_UNSUPPORTED_SHAPE: D or M outside the supported range";
+    case CP_ERR_UNSUPPORTED_DTYPE: return "CP_ERR_UNSUPPORTED_DTYPE";
+    case CP_ERR_MISALIGNED: return "CP_ERR_MISALIGNED: pointers must be 16-byte aligned (workspace 256)";
+    case CP_ERR_WORKSPACE_TOO_SMALL: return "CP_ERR_WORKSPACE_TOO_SMALL";
+    case CP_ERR_CUDA: return "CP_ERR_CUDA: a CUDA call failed";
+    case CP_ERR_TIMEOUT: return "CP_ERR_TIMEOUT: a kernel wait expired";
+    case CP_ERR_NO_DEVICE: return "CP_ERR_NO_DEVICE";
+  }
+  return "unknown causal_product status";
+}
+
+}  // extern "C"

@@ -1,0 +1,67 @@
+// Internal interface between the C ABI (cp_api.cu) and the kernels.
+//
+// Every entry point is reduced to one or more "causal products":
+//     out_i = sum_{j in W(i)} (q_i . k_j) v_j,
+// with W(i) = {j <= i} (forward order) or {j >= i} (reverse order), over a
+// batch of BH independent problems.  The forward pass is one forward-order
+// product; the backward pass is three products with permuted operands
+// (dq: (g, v, k) forward; dv: (k, q, g) reverse; dk: (v, g, q) reverse).
+//
+// Each product is computed as a two-pass scan over the sequence:
+//   pass 1 (only when a problem is split into G > 1 segments): per-segment
+//          state aggregates A_s = sum_{j in segment s} k_j v_j^T (fp32);
+//   pass 2: every segment starts from the sum of the aggregates that precede
+//          it (in scan order, summed in a fixed order) and streams its tiles,
+//          carrying the fp32 state on chip.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/causal_product.h"
+
+namespace cp {
+
+// Planning is a pure function of the problem so that the workspace size is
+// known on the host without a device; it assumes the 152 SMs of a GB300.
+constexpr int kPlanSMs = 152;
+constexpr size_t kStatusBytes = 256;
+
+struct Product {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  int64_t BH, N, D, M;
+  bool reverse;
+};
+
+// ---- fp32 (SIMT FMA) path
+struct SimtPlan {
+  int C;        // rows per tile
+  int Mb;       // value columns per CTA
+  int n_mb;     // value-column blocks
+  int G;        // segments per problem
+  int64_t seg_rows;
+  size_t agg_bytes;
+};
+SimtPlan simt_plan(int64_t BH, int64_t N, int64_t D, int64_t M);
+cudaError_t simt_launch(const Product& p, const SimtPlan& plan, float* agg, int* status,
+                        cudaStream_t stream);
+
+// ---- bf16 (tcgen05 tensor-core) path
+struct TcPlan {
+  int DP;       // D padded to a multiple of 64
+  int MB;       // value columns per CTA (64 or 128)
+  int n_mb;     // value-column blocks
+  int n_tiles;  // 128-row tiles per problem
+  int seg_tiles;
+  int G;
+  size_t agg_bytes;
+  bool ok;
+};
+TcPlan tc_plan(int64_t BH, int64_t N, int64_t D, int64_t M);
+cp_status_t tc_launch(const Product& p, const TcPlan& plan, float* agg, int* status,
+                      cudaStream_t stream);
+
+}  // namespace cp

@@ -1,0 +1,201 @@
+// fp32 causal product on the CUDA cores (FFMA), chunked over the sequence.
+//
+// TF32 tensor-core rounding (10-bit mantissa) would not hold fp32 accuracy,
+// so the fp32 path uses plain fp32 FMA.  One CTA owns one (problem,
+// value-column block, segment).  It walks its segment in tiles of C rows:
+//     P      = Q_t K_t^T, masked to the causal triangle of the tile
+//     O_t    = Q_t S + P V_t            (S = state before the tile)
+//     S     += K_t^T V_t
+// which is the recurrence "state += k v^T; out = state^T q" of
+// triton-lang/triton issue #217 regrouped by tiles: within a tile the
+// prefix is the masked product, across tiles it is the carried state.
+#include <algorithm>
+
+#include "cp_internal.h"
+
+namespace cp {
+namespace {
+
+constexpr int kC = 32;          // rows per tile
+constexpr int kThreads = 256;
+constexpr int kMaxMb = 64;
+
+struct SimtArgs {
+  const float* q;
+  const float* k;
+  const float* v;
+  float* out;
+  int64_t N;
+  int D, M, Mb, n_mb, G, BH;
+  int64_t seg_rows;
+  int reverse;
+  const float* agg_in;  // [P][G][D][Mb] aggregates (pass 2 reads), may be null
+  float* agg_out;       // pass 1 writes
+  int agg_only;
+};
+
+__global__ void __launch_bounds__(kThreads) simt_kernel(SimtArgs a) {
+  extern __shared__ float smem[];
+  const int D = a.D, Mb = a.Mb;
+  const int ldq = D + 1;
+  float* Qs = smem;                  // [C][D+1]
+  float* Ks = Qs + kC * ldq;         // [C][D+1]
+  float* Vs = Ks + kC * ldq;         // [C][Mb]
+  float* Ps = Vs + kC * Mb;          // [C][C+1]
+  float* Ss = Ps + kC * (kC + 1);    // [D][Mb]
+
+  // block -> (segment, problem, value block); pass 1 skips the one segment
+  // whose aggregate nobody reads.
+  int idx = blockIdx.x;
+  const int mb = idx % a.n_mb;
+  idx /= a.n_mb;
+  const int bh = idx % a.BH;
+  int s = idx / a.BH;
+  if (a.agg_only && a.reverse) s += 1;
+  const int pidx = bh * a.n_mb + mb;
+  const int m0 = mb * Mb;
+  const int mw = min(Mb, a.M - m0);  // columns of this block that exist
+
+  const int64_t seg_lo = (int64_t)s * a.seg_rows;
+  const int64_t seg_hi = min(a.N, seg_lo + a.seg_rows);
+  const int64_t n_rows = seg_hi - seg_lo;
+  const int n_t = (int)((n_rows + kC - 1) / kC);
+
+  const float* qb = a.q + (int64_t)bh * a.N * D;
+  const float* kb = a.k + (int64_t)bh * a.N * D;
+  const float* vb = a.v + (int64_t)bh * a.N * a.M;
+  float* ob = a.out + (int64_t)bh * a.N * a.M;
+
+  // initial state: aggregates of the segments before this one in scan order
+  for (int e = threadIdx.x; e < D * Mb; e += kThreads) {
+    float acc = 0.f;
+    if (!a.agg_only && a.agg_in != nullptr) {
+      const int lo = a.reverse ? s + 1 : 0;
+      const int hi = a.reverse ? a.G : s;
+      for (int s2 = lo; s2 < hi; ++s2)
+        acc += a.agg_in[((int64_t)pidx * a.G + s2) * D * Mb + e];
+    }
+    Ss[e] = acc;
+  }
+
+  for (int it = 0; it < n_t; ++it) {
+    const int t = a.reverse ? (n_t - 1 - it) : it;
+    const int64_t r0 = seg_lo + (int64_t)t * kC;
+    __syncthreads();
+    for (int e = threadIdx.x; e < kC * D; e += kThreads) {
+      const int r = e / D, d = e % D;
+      const int64_t row = r0 + r;
+      const bool in = row < seg_hi;
+      Ks[r * ldq + d] = in ? kb[row * D + d] : 0.f;
+      if (!a.agg_only) Qs[r * ldq + d] = in ? qb[row * D + d] : 0.f;
+    }
+    for (int e = threadIdx.x; e < kC * Mb; e += kThreads) {
+      const int r = e / Mb, m = e % Mb;
+      const int64_t row = r0 + r;
+      Vs[e] = (row < seg_hi && m < mw) ? vb[row * a.M + m0 + m] : 0.f;
+    }
+    __syncthreads();
+    if (!a.agg_only) {
+      // P = Q K^T restricted to the causal triangle of the tile
+      for (int e = threadIdx.x; e < kC * kC; e += kThreads) {
+        const int i = e / kC, j = e % kC;
+        float acc = 0.f;
+        const bool keep = a.reverse ? (j >= i) : (j <= i);
+        if (keep) {
+          const float* qi = Qs + i * ldq;
+          const float* kj = Ks + j * ldq;
+          for (int d = 0; d < D; ++d) acc = fmaf(qi[d], kj[d], acc);
+        }
+        Ps[i * (kC + 1) + j] = acc;
+      }
+      __syncthreads();
+      // O = Q S + P V
+      for (int e = threadIdx.x; e < kC * Mb; e += kThreads) {
+        const int i = e / Mb, m = e % Mb;
+        const int64_t row = r0 + i;
+        if (row >= seg_hi || m >= mw) continue;
+        float acc = 0.f;
+        const float* qi = Qs + i * ldq;
+        for (int d = 0; d < D; ++d) acc = fmaf(qi[d], Ss[d * Mb + m], acc);
+        const float* pi = Ps + i * (kC + 1);
+        for (int j = 0; j < kC; ++j) acc = fmaf(pi[j], Vs[j * Mb + m], acc);
+        ob[row * a.M + m0 + m] = acc;
+      }
+      __syncthreads();
+    }
+    // S += K^T V
+    for (int e = threadIdx.x; e < D * Mb; e += kThreads) {
+      const int d = e / Mb, m = e % Mb;
+      float acc = Ss[e];
+      for (int j = 0; j < kC; ++j) acc = fmaf(Ks[j * ldq + d], Vs[j * Mb + m], acc);
+      Ss[e] = acc;
+    }
+  }
+  if (a.agg_only) {
+    __syncthreads();
+    float* dst = a.agg_out + ((int64_t)pidx * a.G + s) * D * Mb;
+    for (int e = threadIdx.x; e < D * Mb; e += kThreads) dst[e] = Ss[e];
+  }
+}
+
+size_t simt_smem_bytes(int D, int Mb) {
+  return sizeof(float) *
+         (size_t)(2 * kC * (D + 1) + kC * Mb + kC * (kC + 1) + D * Mb);
+}
+
+}  // namespace
+
+SimtPlan simt_plan(int64_t BH, int64_t N, int64_t D, int64_t M) {
+  SimtPlan p{};
+  p.C = kC;
+  p.Mb = (int)std::min<int64_t>(M, kMaxMb);
+  p.n_mb = (int)((M + p.Mb - 1) / p.Mb);
+  const int64_t problems = BH * p.n_mb;
+  const int64_t n_tiles = (N + kC - 1) / kC;
+  // aim for about two CTAs per SM; every segment holds at least 4 tiles
+  int64_t G = std::max<int64_t>(1, (2 * kPlanSMs) / std::max<int64_t>(problems, 1));
+  G = std::min<int64_t>(G, std::max<int64_t>(1, n_tiles / 4));
+  const int64_t tiles_per_seg = (n_tiles + G - 1) / std::max<int64_t>(G, 1);
+  p.seg_rows = std::max<int64_t>(1, tiles_per_seg) * kC;
+  p.G = (int)std::max<int64_t>(1, (N + p.seg_rows - 1) / p.seg_rows);
+  p.agg_bytes = p.G > 1 ? sizeof(float) * (size_t)problems * p.G * D * p.Mb : 0;
+  return p;
+}
+
+cudaError_t simt_launch(const Product& p, const SimtPlan& plan, float* agg, int* status,
+                        cudaStream_t stream) {
+  (void)status;
+  const size_t smem = simt_smem_bytes((int)p.D, plan.Mb);
+  cudaError_t e = cudaFuncSetAttribute(simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  SimtArgs a{};
+  a.q = static_cast<const float*>(p.q);
+  a.k = static_cast<const float*>(p.k);
+  a.v = static_cast<const float*>(p.v);
+  a.out = static_cast<float*>(p.out);
+  a.N = p.N;
+  a.D = (int)p.D;
+  a.M = (int)p.M;
+  a.Mb = plan.Mb;
+  a.n_mb = plan.n_mb;
+  a.G = plan.G;
+  a.BH = (int)p.BH;
+  a.seg_rows = plan.seg_rows;
+  a.reverse = p.reverse ? 1 : 0;
+  const int64_t problems = p.BH * plan.n_mb;
+  if (plan.G > 1) {
+    a.agg_only = 1;
+    a.agg_out = agg;
+    simt_kernel<<<(unsigned)(problems * (plan.G - 1)), kThreads, smem, stream>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    a.agg_only = 0;
+    a.agg_in = agg;
+    a.agg_out = nullptr;
+  }
+  simt_kernel<<<(unsigned)(problems * plan.G), kThreads, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace cp

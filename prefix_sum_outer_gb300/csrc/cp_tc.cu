@@ -1,0 +1,599 @@
+// bf16 causal product on the 5th-generation tensor cores (sm_103a).
+//
+// The recurrence "state += k v^T; out = state^T q" (triton-lang/triton issue
+// #217, the loop listing; the issue's opening comment calls it the prefix
+// sum of Algorithm 1 of "Transformers are RNNs") is regrouped into tiles of
+// 128 rows.  With S the fp32 D x M state before tile t:
+//     P   = Q_t K_t^T            masked to j <= i inside the tile (128x128)
+//     O_t = P V_t + Q_t S        (intra-tile part + inter-tile readout)
+//     S  += K_t^T V_t
+// All four are dense contractions and run as tcgen05.mma with bf16 operands
+// in shared memory and fp32 accumulators in tensor memory (TMEM).  The state
+// never leaves TMEM while a CTA walks its segment; a bf16 copy of it is
+// written to shared memory once per tile to serve as the MMA operand of
+// Q_t S.  P is masked and rounded to bf16 on its way from TMEM to shared
+// memory.
+//
+// CTA = 6 warps:
+//   warp 0       TMA producer: Q/K/V tiles into an NS-deep ring
+//   warp 1       TMEM allocator and single-thread MMA issuer
+//   warps 2..5   epilogue (one thread per TMEM lane = tile row): state and
+//                P conversion, output conversion and TMA store
+//
+// Long sequences with few problems are split into G segments per problem;
+// a first launch of the same kernel in aggregate-only mode writes each
+// segment's sum of k v^T, and every segment of the second launch starts
+// from the fixed-order sum of its predecessors' aggregates (a two-pass scan
+// across segments, deterministic).
+#include <algorithm>
+#include <cstdio>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "cp_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace cp {
+namespace tc {
+
+using namespace cp::ptx;
+
+constexpr int kTile = 128;             // rows per tile = MMA M
+constexpr int kBoxCols = 64;           // bf16 columns per TMA box (128 bytes)
+constexpr int kBoxBytes = kTile * 128; // one [128 x 64] bf16 box
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+constexpr int kSmemLimit = 232448;     // 227 KB opt-in dynamic shared memory
+
+struct Args {
+  int64_t N;
+  int n_tiles;
+  int seg_tiles;
+  int G;
+  int BH;
+  int n_mb;
+  int reverse;
+  const float* agg_in;   // [P][G][DP][MB]; null when G == 1
+  float* agg_out;        // aggregate-only launch writes here
+  int* status;
+};
+
+template <int DP, int MB>
+struct Layout {
+  static constexpr int kQBoxes = DP / kBoxCols;
+  static constexpr int kVBoxes = MB / kBoxCols;
+  static constexpr int kSBlocks = (DP + 127) / 128;
+  static constexpr int kQBytes = kQBoxes * kBoxBytes;
+  static constexpr int kVBytes = kVBoxes * kBoxBytes;
+  static constexpr int kStageBytes = 2 * kQBytes + kVBytes;
+  static constexpr int kPBytes = 2 * kBoxBytes;             // 128 x 128 bf16
+  static constexpr int kSBytes = kVBoxes * DP * 128;         // DP x MB bf16
+  static constexpr int kOBytes = kVBoxes * kBoxBytes;        // 128 x MB bf16
+  static constexpr int kFixed = kPBytes + kSBytes + kOBytes;
+  static constexpr int kBarBytes = 1024;
+  static constexpr int kAlignSlack = 1024;
+  static constexpr int kStagesFit = (kSmemLimit - kFixed - kBarBytes - kAlignSlack) / kStageBytes;
+  static constexpr int NS = kStagesFit > 4 ? 4 : kStagesFit;
+  static constexpr int kSmemBytes = NS * kStageBytes + kFixed + kBarBytes + kAlignSlack;
+  // TMEM columns: P (128) | O (MB) | S (kSBlocks x MB)
+  static constexpr int kColP = 0;
+  static constexpr int kColO = 128;
+  static constexpr int kColS = 128 + MB;
+  static constexpr int kColsUsed = 128 + MB + kSBlocks * MB;
+  static constexpr int kColsAlloc = kColsUsed <= 256 ? 256 : 512;
+  static_assert(NS >= 1, "tile does not fit in shared memory");
+  static_assert(kColsUsed <= 512, "accumulators do not fit in TMEM");
+  static_assert(DP % 64 == 0 && MB % 64 == 0, "64-column boxes");
+};
+
+// Byte offset of element (row, col) inside a [rows x 64k] bf16 tile stored
+// as 64-column boxes of `box_stride` bytes with the 128-byte swizzle (the
+// layout TMA writes and tcgen05 descriptors read): 16-byte chunk index
+// XOR row % 8.
+__device__ __forceinline__ uint32_t sw128_offset(int row, int col, int box_stride) {
+  const int box = col >> 6;
+  const int chunk = (col & 63) >> 3;
+  return box * box_stride + row * 128 + ((chunk ^ (row & 7)) << 4) + ((col & 7) << 1);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Convert 32 fp32 values (columns col0..col0+31 of `row`) to bf16 and store
+// them into a swizzled tile; col0 must be a multiple of 32.
+__device__ __forceinline__ void store_chunk32(uint8_t* tile, int row, int col0, int box_stride,
+                                              const uint32_t (&r)[32]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint4 w;
+    w.x = pack_bf16x2(__uint_as_float(r[8 * c + 0]), __uint_as_float(r[8 * c + 1]));
+    w.y = pack_bf16x2(__uint_as_float(r[8 * c + 2]), __uint_as_float(r[8 * c + 3]));
+    w.z = pack_bf16x2(__uint_as_float(r[8 * c + 4]), __uint_as_float(r[8 * c + 5]));
+    w.w = pack_bf16x2(__uint_as_float(r[8 * c + 6]), __uint_as_float(r[8 * c + 7]));
+    *reinterpret_cast<uint4*>(tile + sw128_offset(row, col0 + 8 * c, box_stride)) = w;
+  }
+}
+
+__device__ __forceinline__ void store_zero32(uint8_t* tile, int row, int col0, int box_stride) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    *reinterpret_cast<uint4*>(tile + sw128_offset(row, col0 + 8 * c, box_stride)) =
+        make_uint4(0, 0, 0, 0);
+}
+
+__device__ __forceinline__ void record_timeout(int* status, volatile int* abort_flag) {
+  *abort_flag = 1;
+  if (status != nullptr) atomicCAS(status, 0, (int)CP_ERR_TIMEOUT);
+}
+
+template <int DP, int MB, bool AGG_ONLY>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_o, const Args a) {
+  using L = Layout<DP, MB>;
+  constexpr int NS = L::NS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* ring = smem;
+  uint8_t* p_tile = ring + NS * L::kStageBytes;
+  uint8_t* s_tile = p_tile + L::kPBytes;
+  uint8_t* o_tile = s_tile + L::kSBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(o_tile + L::kOBytes);
+  uint64_t* full = bars;              // [NS] TMA -> MMA
+  uint64_t* empty = bars + NS;        // [NS] MMA -> TMA
+  uint64_t* p_done = bars + 2 * NS;   // MMA -> epilogue: P in TMEM
+  uint64_t* s_done = p_done + 1;      // MMA -> epilogue: state updated
+  uint64_t* o_done = p_done + 2;      // MMA -> epilogue: O in TMEM (and smem operands free)
+  uint64_t* p_ready = p_done + 3;     // epilogue -> MMA: bf16 P in smem, P TMEM read
+  uint64_t* s_ready = p_done + 4;     // epilogue -> MMA: bf16 S in smem, S TMEM read
+  uint64_t* o_free = p_done + 5;      // epilogue -> MMA: O TMEM read
+  uint64_t* fin = p_done + 6;         // MMA drain before TMEM release
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(p_done + 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(p_done + 9);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- block -> (segment, problem, value-column block)
+  int idx = blockIdx.x;
+  const int mb = idx % a.n_mb;
+  idx /= a.n_mb;
+  const int bh = idx % a.BH;
+  int seg = idx / a.BH;
+  if (AGG_ONLY && a.reverse) seg += 1;  // the first segment in scan order is never needed
+  const int t_first = seg * a.seg_tiles;
+  const int t_end = min(a.n_tiles, t_first + a.seg_tiles);
+  const int n_it = t_end - t_first;
+  const int pidx = bh * a.n_mb + mb;
+  const bool has_prefix =
+      !AGG_ONLY && a.agg_in != nullptr && (a.reverse ? (seg < a.G - 1) : (seg > 0));
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(p_done, 1);
+    mbar_init(s_done, 1);
+    mbar_init(o_done, 1);
+    mbar_init(p_ready, 4);
+    mbar_init(s_ready, 4);
+    mbar_init(o_free, 4);
+    mbar_init(fin, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    if (!AGG_ONLY) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_o);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, L::kColsAlloc);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      constexpr uint32_t kBytes =
+          AGG_ONLY ? (L::kQBytes + L::kVBytes) : (2 * L::kQBytes + L::kVBytes);
+      int it = 0;
+      for (; it < n_it; ++it) {
+        const int stage = it % NS;
+        if (it >= NS && !mbar_wait(&empty[stage], ((it / NS) - 1) & 1, abort_flag)) {
+          record_timeout(a.status, abort_flag);
+          break;
+        }
+        const int tile = a.reverse ? (t_end - 1 - it) : (t_first + it);
+        const int row0 = tile * kTile;
+        uint8_t* q_s = ring + stage * L::kStageBytes;
+        uint8_t* k_s = q_s + L::kQBytes;
+        uint8_t* v_s = k_s + L::kQBytes;
+        mbar_arrive_expect_tx(&full[stage], kBytes);
+#pragma unroll
+        for (int b = 0; b < L::kQBoxes; ++b) {
+          if (!AGG_ONLY)
+            tma_load_3d(q_s + b * kBoxBytes, &tm_q, &full[stage], b * kBoxCols, row0, bh, pol);
+          tma_load_3d(k_s + b * kBoxBytes, &tm_k, &full[stage], b * kBoxCols, row0, bh, pol);
+        }
+#pragma unroll
+        for (int b = 0; b < L::kVBoxes; ++b)
+          tma_load_3d(v_s + b * kBoxBytes, &tm_v, &full[stage], mb * MB + b * kBoxCols, row0, bh,
+                      pol);
+      }
+      if (*abort_flag) {
+        // let the copies already issued land before the CTA's memory goes away
+        const int lo = max(0, it - NS);
+        for (int j = lo; j < it; ++j) mbar_wait_timeout(&full[j % NS], (j / NS) & 1, CP_WAIT_TIMEOUT_NS);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_p = idesc_bf16_f32(128, 128, 0, 0);   // Q . K^T
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, MB, 1, 1);    // K^T . V
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, MB, 0, 1);    // P . V, Q . S
+      const uint32_t t_p = tmem + L::kColP;
+      const uint32_t t_o = tmem + L::kColO;
+      const uint32_t t_s = tmem + L::kColS;
+      const uint32_t p_addr = smem_u32(p_tile);
+      const uint32_t s_addr = smem_u32(s_tile);
+      bool ok = true;
+      for (int it = 0; it < n_it && ok; ++it) {
+        const int stage = it % NS;
+        const uint32_t q_addr = smem_u32(ring + stage * L::kStageBytes);
+        const uint32_t k_addr = q_addr + L::kQBytes;
+        const uint32_t v_addr = k_addr + L::kQBytes;
+        if (!mbar_wait(&full[stage], (it / NS) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        if (!AGG_ONLY) {
+          // P = Q K^T over D (both operands K-major)
+#pragma unroll
+          for (int kk = 0; kk < DP / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+            mma_bf16_ss(t_p, smem_desc_sw128(q_addr + off, 16, 1024),
+                        smem_desc_sw128(k_addr + off, 16, 1024), idesc_p, kk > 0);
+          }
+          mma_commit(p_done);
+          // the epilogue has copied the state to smem and released S in TMEM
+          if (!mbar_wait(s_ready, it & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+        }
+        // S += K^T V (A = K^T and B = V, both MN-major), one 128-row block of
+        // the state per 128 columns of K
+        const bool fresh = (it == 0) && !has_prefix;
+#pragma unroll
+        for (int sb = 0; sb < L::kSBlocks; ++sb) {
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            mma_bf16_ss(t_s + sb * MB,
+                        smem_desc_sw128(k_addr + 2 * sb * kBoxBytes + kk * 2048, kBoxBytes, 1024),
+                        smem_desc_sw128(v_addr + kk * 2048, kBoxBytes, 1024), idesc_s,
+                        (fresh && kk == 0) ? 0u : 1u);
+          }
+        }
+        if (!AGG_ONLY) {
+          mma_commit(s_done);
+          if (!mbar_wait(p_ready, it & 1, abort_flag)) { ok = false; break; }
+          if (it > 0 && !mbar_wait(o_free, (it - 1) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          // O = P V  (A = P K-major, B = V MN-major)
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+            mma_bf16_ss(t_o, smem_desc_sw128(p_addr + off, 16, 1024),
+                        smem_desc_sw128(v_addr + kk * 2048, kBoxBytes, 1024), idesc_o, kk > 0);
+          }
+          // O += Q S  (A = Q K-major, B = S MN-major)
+#pragma unroll
+          for (int kk = 0; kk < DP / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+            mma_bf16_ss(t_o, smem_desc_sw128(q_addr + off, 16, 1024),
+                        smem_desc_sw128(s_addr + kk * 2048, DP * 128, 1024), idesc_o, 1u);
+          }
+          mma_commit(o_done);
+        }
+        mma_commit(&empty[stage]);
+      }
+      if (AGG_ONLY && ok) mma_commit(s_done);
+      if (!ok) record_timeout(a.status, abort_flag);
+      // every MMA issued so far completes before TMEM is released
+      mma_commit(fin);
+      mbar_wait_timeout(fin, 0, CP_WAIT_TIMEOUT_NS);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int wq = warp & 3;                 // TMEM lane quarter of this warp
+    const int row = wq * 32 + lane;          // tile row = TMEM lane
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const int epi_tid = threadIdx.x - 64;    // 0..127
+    bool ok = true;
+
+    if (AGG_ONLY) {
+      if (!mbar_wait(s_done, 0, abort_flag)) {
+        record_timeout(a.status, abort_flag);
+      } else if (n_it > 0) {
+        tc_fence_after();
+        float* dst = a.agg_out + ((size_t)pidx * a.G + seg) * (size_t)DP * MB;
+#pragma unroll
+        for (int sb = 0; sb < L::kSBlocks; ++sb) {
+          if (sb * 128 + wq * 32 >= DP) continue;  // warp-uniform
+          const int d = sb * 128 + row;
+#pragma unroll
+          for (int c = 0; c < MB / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(lane_base + L::kColS + sb * MB + c * 32, r);
+            tmem_ld_wait();
+            float4* o4 = reinterpret_cast<float4*>(dst + (size_t)d * MB + c * 32);
+#pragma unroll
+            for (int x = 0; x < 8; ++x)
+              o4[x] = make_float4(__uint_as_float(r[4 * x]), __uint_as_float(r[4 * x + 1]),
+                                  __uint_as_float(r[4 * x + 2]), __uint_as_float(r[4 * x + 3]));
+          }
+        }
+      }
+    } else {
+      // initial state: fixed-order sum of the preceding segments' aggregates
+      if (has_prefix) {
+        const int lo = a.reverse ? seg + 1 : 0;
+        const int hi = a.reverse ? a.G : seg;
+#pragma unroll
+        for (int sb = 0; sb < L::kSBlocks; ++sb) {
+          if (sb * 128 + wq * 32 >= DP) continue;
+          const int d = sb * 128 + row;
+#pragma unroll
+          for (int c = 0; c < MB / 32; ++c) {
+            float acc[32];
+#pragma unroll
+            for (int x = 0; x < 32; ++x) acc[x] = 0.f;
+            for (int s2 = lo; s2 < hi; ++s2) {
+              const float4* src = reinterpret_cast<const float4*>(
+                  a.agg_in + (((size_t)pidx * a.G + s2) * DP + d) * MB + c * 32);
+#pragma unroll
+              for (int x = 0; x < 8; ++x) {
+                const float4 f = __ldg(src + x);
+                acc[4 * x] += f.x;
+                acc[4 * x + 1] += f.y;
+                acc[4 * x + 2] += f.z;
+                acc[4 * x + 3] += f.w;
+              }
+            }
+            uint32_t r[32];
+#pragma unroll
+            for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(acc[x]);
+            tmem_st32(lane_base + L::kColS + sb * MB + c * 32, r);
+          }
+        }
+        tmem_st_wait();
+      }
+
+      for (int it = 0; it < n_it && ok; ++it) {
+        const int tile = a.reverse ? (t_end - 1 - it) : (t_first + it);
+        // (a) bf16 copy of the state before this tile -> s_tile
+        if (it == 0 && !has_prefix) {
+#pragma unroll
+          for (int sb = 0; sb < L::kSBlocks; ++sb) {
+            if (sb * 128 + wq * 32 >= DP) continue;
+#pragma unroll
+            for (int c = 0; c < MB / 32; ++c) store_zero32(s_tile, sb * 128 + row, c * 32, DP * 128);
+          }
+        } else {
+          if (it > 0) {
+            if (!mbar_wait(s_done, (it - 1) & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+          }
+#pragma unroll
+          for (int sb = 0; sb < L::kSBlocks; ++sb) {
+            if (sb * 128 + wq * 32 >= DP) continue;
+#pragma unroll
+            for (int c = 0; c < MB / 32; ++c) {
+              uint32_t r[32];
+              tmem_ld32(lane_base + L::kColS + sb * MB + c * 32, r);
+              tmem_ld_wait();
+              store_chunk32(s_tile, sb * 128 + row, c * 32, DP * 128, r);
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_ready);
+
+        // (b) P: mask to the causal triangle of the tile, bf16 -> p_tile
+        if (!mbar_wait(p_done, it & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const bool all_masked = a.reverse ? (c < wq) : (c > wq);
+          if (all_masked) {
+            store_zero32(p_tile, row, c * 32, kBoxBytes);
+            continue;
+          }
+          uint32_t r[32];
+          tmem_ld32(lane_base + L::kColP + c * 32, r);
+          tmem_ld_wait();
+          if (c == wq) {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) {
+              const bool keep = a.reverse ? (x >= lane) : (x <= lane);
+              if (!keep) r[x] = 0u;
+            }
+          }
+          store_chunk32(p_tile, row, c * 32, kBoxBytes, r);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_ready);
+
+        // (c) O -> bf16 -> o_tile -> TMA store
+        if (!mbar_wait(o_done, it & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        if (epi_tid == 0) tma_store_wait_read_all();  // previous tile's store has read o_tile
+        named_barrier_sync(1, kEpiThreads);
+#pragma unroll
+        for (int c = 0; c < MB / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(lane_base + L::kColO + c * 32, r);
+          tmem_ld_wait();
+          store_chunk32(o_tile, row, c * 32, kBoxBytes, r);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(o_free);
+        fence_proxy_async_smem();
+        named_barrier_sync(1, kEpiThreads);
+        if (epi_tid == 0) {
+#pragma unroll
+          for (int b = 0; b < L::kVBoxes; ++b)
+            tma_store_3d(&tm_o, o_tile + b * kBoxBytes, mb * MB + b * kBoxCols, tile * kTile, bh);
+          tma_store_commit();
+        }
+      }
+      if (!ok) record_timeout(a.status, abort_flag);
+      if (epi_tid == 0) tma_store_wait_all();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::kColsAlloc);
+  }
+}
+
+// ------------------------------------------------------------------ host
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// [BH][N][cols] bf16, boxes of 64 columns x 128 rows x 1 problem, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* ptr, int64_t BH, int64_t N, int64_t cols) {
+  auto enc = get_encode();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)(N * cols * 2)};
+  cuuint32_t box[3] = {(cuuint32_t)kBoxCols, (cuuint32_t)kTile, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int DP, int MB, bool AGG>
+cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                       const CUtensorMap& o, const Args& a, unsigned grid, cudaStream_t st) {
+  using L = Layout<DP, MB>;
+  auto kern = tc_causal_kernel<DP, MB, AGG>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, L::kSmemBytes, st>>>(q, k, v, o, a);
+  return cudaGetLastError();
+}
+
+template <int DP, int MB>
+cudaError_t launch_pair(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                        const CUtensorMap& o, Args a, const TcPlan& plan, int64_t problems,
+                        float* agg, cudaStream_t st) {
+  cudaError_t e = cudaSuccess;
+  if (plan.G > 1) {
+    Args b = a;
+    b.agg_in = nullptr;
+    b.agg_out = agg;
+    e = launch_one<DP, MB, true>(q, k, v, o, b, (unsigned)(problems * (plan.G - 1)), st);
+    if (e != cudaSuccess) return e;
+    a.agg_in = agg;
+  }
+  return launch_one<DP, MB, false>(q, k, v, o, a, (unsigned)(problems * plan.G), st);
+}
+
+}  // namespace tc
+
+TcPlan tc_plan(int64_t BH, int64_t N, int64_t D, int64_t M) {
+  TcPlan p{};
+  p.DP = (int)((D + 63) / 64 * 64);
+  const int Mpad = (int)((M + 63) / 64 * 64);
+  // widest value block whose tile set fits shared memory and TMEM
+  if (p.DP <= 128 && Mpad >= 128)
+    p.MB = 128;
+  else
+    p.MB = 64;
+  p.n_mb = (Mpad + p.MB - 1) / p.MB;
+  p.n_tiles = (int)((N + tc::kTile - 1) / tc::kTile);
+  const int64_t problems = BH * p.n_mb;
+  int64_t G = 1;
+  if (problems * 4 < (int64_t)kPlanSMs * 3)  // fewer than 3/4 of the SMs busy: split
+    G = std::max<int64_t>(1, kPlanSMs / problems);
+  G = std::min<int64_t>(G, std::max(1, p.n_tiles));
+  p.seg_tiles = (int)((p.n_tiles + G - 1) / G);
+  p.G = p.seg_tiles > 0 ? (p.n_tiles + p.seg_tiles - 1) / p.seg_tiles : 1;
+  if (p.G < 1) p.G = 1;
+  p.agg_bytes = p.G > 1 ? sizeof(float) * (size_t)problems * p.G * p.DP * p.MB : 0;
+  p.ok = p.DP <= 256 && Mpad <= 256;
+  return p;
+}
+
+cp_status_t tc_launch(const Product& p, const TcPlan& plan, float* agg, int* status,
+                      cudaStream_t stream) {
+  if (!plan.ok) return CP_ERR_UNSUPPORTED_SHAPE;
+  CUtensorMap mq, mk, mv, mo;
+  if (!tc::make_map(&mq, p.q, p.BH, p.N, p.D) || !tc::make_map(&mk, p.k, p.BH, p.N, p.D) ||
+      !tc::make_map(&mv, p.v, p.BH, p.N, p.M) || !tc::make_map(&mo, p.out, p.BH, p.N, p.M))
+    return CP_ERR_UNSUPPORTED_SHAPE;
+  tc::Args a{};
+  a.N = p.N;
+  a.n_tiles = plan.n_tiles;
+  a.seg_tiles = plan.seg_tiles;
+  a.G = plan.G;
+  a.BH = (int)p.BH;
+  a.n_mb = plan.n_mb;
+  a.reverse = p.reverse ? 1 : 0;
+  a.status = status;
+  const int64_t problems = p.BH * plan.n_mb;
+  cudaError_t e;
+#define CP_TC_CASE(DP_, MB_)                                                                  \
+  if (plan.DP == DP_ && plan.MB == MB_)                                                       \
+    e = tc::launch_pair<DP_, MB_>(mq, mk, mv, mo, a, plan, problems, agg, stream);            \
+  else
+  CP_TC_CASE(64, 64)
+  CP_TC_CASE(64, 128)
+  CP_TC_CASE(128, 64)
+  CP_TC_CASE(128, 128)
+  CP_TC_CASE(192, 64)
+  CP_TC_CASE(256, 64)
+  return CP_ERR_UNSUPPORTED_SHAPE;
+#undef CP_TC_CASE
+  return e == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+}
+
+}  // namespace cp

@@ -1,0 +1,135 @@
+"""Host-side checks of the C ABI library (no GPU needed).
+
+The library must load, export every function include/causal_product.h
+declares, and reject bad arguments before it touches the device.  Only
+calls that return before any CUDA work are made here.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import prefix_sum_outer_gb300 as cp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+F32, BF16 = 0, 1
+(OK, INVALID_ARG, UNSUPPORTED_SHAPE, UNSUPPORTED_DTYPE, MISALIGNED, WS_TOO_SMALL, CUDA_ERR,
+ TIMEOUT, NO_DEVICE) = range(9)
+
+
+def declared_functions():
+    names = set()
+    for fname in os.listdir(HEADER_DIR):
+        if not fname.endswith(".h"):
+            continue
+        text = open(os.path.join(HEADER_DIR, fname)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*[A-Za-z_][\w\s\*]*?\b(causal_product\w*)\s*\(", text, re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return cp.load_library()
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for required in ("causal_product_fwd", "causal_product_bwd", "causal_product_workspace_size",
+                     "causal_product_status", "causal_product_error_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+def test_library_is_in_tree(lib):
+    path = cp.library_path()
+    assert os.path.exists(path)
+    assert os.path.commonpath([os.path.abspath(path), ROOT]) == ROOT
+
+
+def test_error_strings(lib):
+    for code in range(9):
+        s = cp.causal_product_error_string(code)
+        assert s and isinstance(s, str)
+    assert cp.causal_product_error_string(0) == "CP_OK"
+    assert "unknown" in cp.causal_product_error_string(99)
+
+
+def test_workspace_size(lib):
+    ws = lib.causal_product_workspace_size
+    # large batch x heads: one segment per problem, status word only
+    assert ws(8, 16, 4096, 64, 64, BF16, 0) == 256
+    assert ws(8, 16, 4096, 64, 64, BF16, 1) == 256
+    # few long problems: split into segments, aggregates needed
+    n = ws(2, 8, 32768, 128, 128, BF16, 1)
+    assert n > 256 and n % 256 == 0
+    assert ws(4, 8, 8229, 256, 64, BF16, 1) > 256
+    assert ws(1, 2, 64, 16, 16, F32, 0) >= 256
+    # rejected shapes give 0
+    assert ws(1, 1, 16, 0, 16, F32, 0) == 0
+    assert ws(1, 1, 16, 16, 300, F32, 0) == 0
+    assert ws(1, 1, 16, 12, 16, BF16, 0) == 0
+    assert ws(0, 1, 16, 16, 16, F32, 0) == 0
+    assert ws(1, 1, -1, 16, 16, F32, 0) == 0
+    assert ws(1, 1, 16, 16, 16, 5, 0) == 0
+
+
+A = 1 << 20  # a 16-byte-aligned fake device address; never dereferenced here
+
+
+def fwd(lib, q=A, k=2 * A, v=3 * A, out=4 * A, B=1, H=1, N=16, D=16, M=16, dtype=F32,
+        ws=None, ws_bytes=0):
+    return lib.causal_product_fwd(q, k, v, out, B, H, N, D, M, dtype, ws, ws_bytes, None)
+
+
+def test_fwd_argument_checks(lib):
+    assert fwd(lib, q=None) == INVALID_ARG
+    assert fwd(lib, out=None) == INVALID_ARG
+    assert fwd(lib, B=0) == INVALID_ARG
+    assert fwd(lib, N=-3) == INVALID_ARG
+    assert fwd(lib, D=0) == UNSUPPORTED_SHAPE
+    assert fwd(lib, M=257) == UNSUPPORTED_SHAPE
+    assert fwd(lib, D=12, dtype=BF16) == UNSUPPORTED_SHAPE
+    assert fwd(lib, dtype=9) == UNSUPPORTED_DTYPE
+    assert fwd(lib, q=A + 4) == MISALIGNED
+    assert fwd(lib, out=4 * A + 8) == MISALIGNED
+    # out overlapping an input
+    assert fwd(lib, out=A + 256) == INVALID_ARG
+    # caller workspace too small
+    assert fwd(lib, ws=8 * A, ws_bytes=16) == WS_TOO_SMALL
+    # N = 0: nothing to do, nothing touched
+    assert fwd(lib, N=0) == OK
+
+
+def test_bwd_argument_checks(lib):
+    def bwd(**kw):
+        args = dict(q=A, k=2 * A, v=3 * A, g=4 * A, dq=5 * A, dk=6 * A, dv=7 * A, B=1, H=1, N=16,
+                    D=16, M=16, dtype=F32, ws=None, ws_bytes=0)
+        args.update(kw)
+        return lib.causal_product_bwd(args["q"], args["k"], args["v"], args["g"], args["dq"],
+                                      args["dk"], args["dv"], args["B"], args["H"], args["N"],
+                                      args["D"], args["M"], args["dtype"], args["ws"],
+                                      args["ws_bytes"], None)
+    assert bwd(g=None) == INVALID_ARG
+    assert bwd(dk=None) == INVALID_ARG
+    assert bwd(dv=7 * A + 2) == MISALIGNED
+    assert bwd(dq=A) == INVALID_ARG            # grad aliases q
+    assert bwd(dk=5 * A) == INVALID_ARG        # two grads alias
+    assert bwd(D=20, dtype=BF16) == UNSUPPORTED_SHAPE
+    assert bwd(ws=8 * A, ws_bytes=1) == WS_TOO_SMALL
+    assert bwd(N=0) == OK
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+    q = torch.ones(1, 1, 4, 16)
+    with pytest.raises(RuntimeError):
+        cp.causal_product_fwd(q, q, q)
