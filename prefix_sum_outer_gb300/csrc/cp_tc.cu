@@ -68,8 +68,13 @@ struct Layout {
   static constexpr int kVBytes = kVBoxes * kBoxBytes;
   static constexpr int kStageBytes = 2 * kQBytes + kVBytes;
   static constexpr int kPBytes = 2 * kBoxBytes;             // 128 x 128 bf16
-  static constexpr int kSBytes = kVBoxes * DP * 128;         // DP x MB bf16
+  static constexpr int kSOneBytes = kVBoxes * DP * 128;      // DP x MB bf16
   static constexpr int kOBytes = kVBoxes * kBoxBytes;        // 128 x MB bf16
+  // The state operand of Q S is split into hi + lo bf16 parts (two MMAs)
+  // whenever both parts fit next to a one-stage ring.
+  static constexpr bool kSplit =
+      (kSmemLimit - kPBytes - 2 * kSOneBytes - kOBytes - 2048) >= kStageBytes;
+  static constexpr int kSBytes = (kSplit ? 2 : 1) * kSOneBytes;
   static constexpr int kFixed = kPBytes + kSBytes + kOBytes;
   static constexpr int kBarBytes = 1024;
   static constexpr int kAlignSlack = 1024;
@@ -115,6 +120,29 @@ __device__ __forceinline__ void store_chunk32(uint8_t* tile, int row, int col0, 
     w.z = pack_bf16x2(__uint_as_float(r[8 * c + 4]), __uint_as_float(r[8 * c + 5]));
     w.w = pack_bf16x2(__uint_as_float(r[8 * c + 6]), __uint_as_float(r[8 * c + 7]));
     *reinterpret_cast<uint4*>(tile + sw128_offset(row, col0 + 8 * c, box_stride)) = w;
+  }
+}
+
+// Split 32 fp32 values into hi = bf16(x) and lo = bf16(x - hi) and store
+// both (hi into `hi_tile`, lo into `lo_tile`, same swizzled layout).
+__device__ __forceinline__ void store_chunk32_split(uint8_t* hi_tile, uint8_t* lo_tile, int row,
+                                                    int col0, int box_stride,
+                                                    const uint32_t (&r)[32]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const float a = __uint_as_float(r[8 * c + 2 * x]);
+      const float b = __uint_as_float(r[8 * c + 2 * x + 1]);
+      h[x] = pack_bf16x2(a, b);
+      const float ah = __uint_as_float(h[x] << 16);
+      const float bh = __uint_as_float(h[x] & 0xffff0000u);
+      l[x] = pack_bf16x2(a - ah, b - bh);
+    }
+    const uint32_t off = sw128_offset(row, col0 + 8 * c, box_stride);
+    *reinterpret_cast<uint4*>(hi_tile + off) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(lo_tile + off) = make_uint4(l[0], l[1], l[2], l[3]);
   }
 }
 
@@ -301,12 +329,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_bf16_ss(t_o, smem_desc_sw128(p_addr + off, 16, 1024),
                         smem_desc_sw128(v_addr + kk * 2048, kBoxBytes, 1024), idesc_o, kk > 0);
           }
-          // O += Q S  (A = Q K-major, B = S MN-major)
+          // O += Q S  (A = Q K-major, B = S MN-major); with the split state
+          // O += Q S_hi + Q S_lo
 #pragma unroll
-          for (int kk = 0; kk < DP / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-            mma_bf16_ss(t_o, smem_desc_sw128(q_addr + off, 16, 1024),
-                        smem_desc_sw128(s_addr + kk * 2048, DP * 128, 1024), idesc_o, 1u);
+          for (int part = 0; part < (L::kSplit ? 2 : 1); ++part) {
+#pragma unroll
+            for (int kk = 0; kk < DP / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+              mma_bf16_ss(t_o, smem_desc_sw128(q_addr + off, 16, 1024),
+                          smem_desc_sw128(s_addr + part * L::kSOneBytes + kk * 2048, DP * 128,
+                                          1024),
+                          idesc_o, 1u);
+            }
           }
           mma_commit(o_done);
         }
@@ -392,7 +426,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int sb = 0; sb < L::kSBlocks; ++sb) {
             if (sb * 128 + wq * 32 >= DP) continue;
 #pragma unroll
-            for (int c = 0; c < MB / 32; ++c) store_zero32(s_tile, sb * 128 + row, c * 32, DP * 128);
+            for (int c = 0; c < MB / 32; ++c) {
+              store_zero32(s_tile, sb * 128 + row, c * 32, DP * 128);
+              if (L::kSplit)
+                store_zero32(s_tile + L::kSOneBytes, sb * 128 + row, c * 32, DP * 128);
+            }
           }
         } else {
           if (it > 0) {
@@ -407,7 +445,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               uint32_t r[32];
               tmem_ld32(lane_base + L::kColS + sb * MB + c * 32, r);
               tmem_ld_wait();
-              store_chunk32(s_tile, sb * 128 + row, c * 32, DP * 128, r);
+              if (L::kSplit)
+                store_chunk32_split(s_tile, s_tile + L::kSOneBytes, sb * 128 + row, c * 32,
+                                    DP * 128, r);
+              else
+                store_chunk32(s_tile, sb * 128 + row, c * 32, DP * 128, r);
             }
           }
         }

@@ -4,6 +4,9 @@ Every call goes through the C ABI (via the ctypes binding).  Inputs are the
 seeded synthetic workloads; the oracle reads exactly the values the GPU
 receives.
 """
+import json
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -31,10 +34,19 @@ def run_bwd(q, k, v, g):
     return r
 
 
+def _log(kind, shape, errs):
+    """Append measured errors to $CP_PARITY_LOG (JSON lines) when set."""
+    path = os.environ.get("CP_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"kind": kind, "shape": list(shape), "errs": errs}) + "\n")
+
+
 def check_fwd(q, k, v, dtype):
     out = run_fwd(q, k, v)
     ref = oracle.fwd(to_np(q), to_np(k), to_np(v))
     err = row_rel_err(to_np(out), ref)
+    _log("fwd_" + dtype, tuple(q.shape) + (v.shape[-1],), {"out": err})
     assert np.isfinite(err) and err <= TOL[dtype], f"fwd row-rel err {err:.3e} > {TOL[dtype]}"
     return err
 
@@ -45,6 +57,8 @@ def check_bwd(q, k, v, g, dtype):
     errs = {}
     for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
         errs[name] = row_rel_err(to_np(got), ref)
+    _log("bwd_" + dtype, tuple(q.shape) + (v.shape[-1],), errs)
+    for name in ("dq", "dk", "dv"):
         assert np.isfinite(errs[name]) and errs[name] <= TOL[dtype], \
             f"{name} row-rel err {errs[name]:.3e} > {TOL[dtype]}"
     return errs
