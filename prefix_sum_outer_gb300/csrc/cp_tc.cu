@@ -67,25 +67,28 @@ struct Layout {
   static constexpr int kQBytes = kQBoxes * kBoxBytes;
   static constexpr int kVBytes = kVBoxes * kBoxBytes;
   static constexpr int kStageBytes = 2 * kQBytes + kVBytes;
-  static constexpr int kPBytes = 2 * kBoxBytes;             // 128 x 128 bf16
   static constexpr int kSOneBytes = kVBoxes * DP * 128;      // DP x MB bf16
   static constexpr int kOBytes = kVBoxes * kBoxBytes;        // 128 x MB bf16
-  // The state operand of Q S is split into hi + lo bf16 parts (two MMAs)
-  // whenever both parts fit next to a one-stage ring.
-  static constexpr bool kSplit =
-      (kSmemLimit - kPBytes - 2 * kSOneBytes - kOBytes - 2048) >= kStageBytes;
-  static constexpr int kSBytes = (kSplit ? 2 : 1) * kSOneBytes;
-  static constexpr int kFixed = kPBytes + kSBytes + kOBytes;
   static constexpr int kBarBytes = 1024;
   static constexpr int kAlignSlack = 1024;
-  static constexpr int kStagesFit = (kSmemLimit - kFixed - kBarBytes - kAlignSlack) / kStageBytes;
+  static constexpr int kAvail = kSmemLimit - kBarBytes - kAlignSlack;
+  // TMEM: P (128 columns, fp32; later packed bf16 hi|lo) and O (MB columns)
+  // are double-buffered when they fit next to the state (kSBlocks x MB).
+  static constexpr int kColsDouble = 2 * 128 + 2 * MB + kSBlocks * MB;
+  // The state operand of Q S is split into hi + lo bf16 parts; its copy in
+  // shared memory is double-buffered together with P and O.
+  static constexpr int kStagesDouble = (kAvail - 4 * kSOneBytes - kOBytes) / kStageBytes;
+  static constexpr int NB = (kColsDouble <= 512 && kStagesDouble >= 2) ? 2 : 1;
+  static constexpr bool kSplit = (kAvail - NB * 2 * kSOneBytes - kOBytes) >= kStageBytes;
+  static constexpr int kSBufBytes = (kSplit ? 2 : 1) * kSOneBytes;
+  static constexpr int kFixed = NB * kSBufBytes + kOBytes;
+  static constexpr int kStagesFit = (kAvail - kFixed) / kStageBytes;
   static constexpr int NS = kStagesFit > 4 ? 4 : kStagesFit;
   static constexpr int kSmemBytes = NS * kStageBytes + kFixed + kBarBytes + kAlignSlack;
-  // TMEM columns: P (128) | O (MB) | S (kSBlocks x MB)
-  static constexpr int kColP = 0;
-  static constexpr int kColO = 128;
-  static constexpr int kColS = 128 + MB;
-  static constexpr int kColsUsed = 128 + MB + kSBlocks * MB;
+  static constexpr int kColP = 0;                 // + b * 128
+  static constexpr int kColO = NB * 128;          // + b * MB
+  static constexpr int kColS = NB * (128 + MB);   // + sb * MB
+  static constexpr int kColsUsed = kColS + kSBlocks * MB;
   static constexpr int kColsAlloc = kColsUsed <= 256 ? 256 : 512;
   static_assert(NS >= 1, "tile does not fit in shared memory");
   static_assert(kColsUsed <= 512, "accumulators do not fit in TMEM");
@@ -166,25 +169,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tm_o, const Args a) {
   using L = Layout<DP, MB>;
   constexpr int NS = L::NS;
+  constexpr int NB = L::NB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* ring = smem;
-  uint8_t* p_tile = ring + NS * L::kStageBytes;
-  uint8_t* s_tile = p_tile + L::kPBytes;
-  uint8_t* o_tile = s_tile + L::kSBytes;
+  uint8_t* s_tile = ring + NS * L::kStageBytes;     // [NB] x (hi | lo) bf16 state copies
+  uint8_t* o_tile = s_tile + NB * L::kSBufBytes;    // output staging for the TMA store
   uint64_t* bars = reinterpret_cast<uint64_t*>(o_tile + L::kOBytes);
   uint64_t* full = bars;              // [NS] TMA -> MMA
   uint64_t* empty = bars + NS;        // [NS] MMA -> TMA
-  uint64_t* p_done = bars + 2 * NS;   // MMA -> epilogue: P in TMEM
-  uint64_t* s_done = p_done + 1;      // MMA -> epilogue: state updated
-  uint64_t* o_done = p_done + 2;      // MMA -> epilogue: O in TMEM (and smem operands free)
-  uint64_t* p_ready = p_done + 3;     // epilogue -> MMA: bf16 P in smem, P TMEM read
-  uint64_t* s_ready = p_done + 4;     // epilogue -> MMA: bf16 S in smem, S TMEM read
-  uint64_t* o_free = p_done + 5;      // epilogue -> MMA: O TMEM read
-  uint64_t* fin = p_done + 6;         // MMA drain before TMEM release
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(p_done + 8);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(p_done + 9);
+  uint64_t* p_done = bars + 2 * NS;   // [NB] MMA -> epilogue: P(t) in TMEM
+  uint64_t* o_done = p_done + NB;     // [NB] MMA -> epilogue: O(t) in TMEM, operands released
+  uint64_t* o_free = o_done + NB;     // [NB] epilogue -> MMA: O(t) read out of TMEM
+  uint64_t* s_done = o_free + NB;     // MMA -> epilogue: state updated with tile t
+  uint64_t* s_ready = s_done + 1;     // epilogue -> MMA: bf16 state copy written, S read
+  uint64_t* p_ready = s_done + 2;     // epilogue -> MMA: masked bf16 P (hi|lo) in TMEM
+  uint64_t* fin = s_done + 3;         // MMA drain before TMEM release
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(s_done + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(s_done + 5);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -208,12 +211,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
-    mbar_init(p_done, 1);
+    for (int i = 0; i < NB; ++i) {
+      mbar_init(&p_done[i], 1);
+      mbar_init(&o_done[i], 1);
+      mbar_init(&o_free[i], 4);
+    }
     mbar_init(s_done, 1);
-    mbar_init(o_done, 1);
-    mbar_init(p_ready, 4);
     mbar_init(s_ready, 4);
-    mbar_init(o_free, 4);
+    mbar_init(p_ready, 4);
     mbar_init(fin, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -269,7 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (*abort_flag) {
         // let the copies already issued land before the CTA's memory goes away
         const int lo = max(0, it - NS);
-        for (int j = lo; j < it; ++j) mbar_wait_timeout(&full[j % NS], (j / NS) & 1, CP_WAIT_TIMEOUT_NS);
+        for (int j = lo; j < it; ++j)
+          mbar_wait_timeout(&full[j % NS], (j / NS) & 1, CP_WAIT_TIMEOUT_NS);
       }
     }
   } else if (warp == 1) {
@@ -278,28 +284,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_p = idesc_bf16_f32(128, 128, 0, 0);   // Q . K^T
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, MB, 1, 1);    // K^T . V
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, MB, 0, 1);    // P . V, Q . S
-      const uint32_t t_p = tmem + L::kColP;
-      const uint32_t t_o = tmem + L::kColO;
       const uint32_t t_s = tmem + L::kColS;
-      const uint32_t p_addr = smem_u32(p_tile);
       const uint32_t s_addr = smem_u32(s_tile);
       bool ok = true;
       for (int it = 0; it < n_it && ok; ++it) {
         const int stage = it % NS;
+        const int b = it % NB;
+        const uint32_t t_p = tmem + L::kColP + b * 128;
+        const uint32_t t_o = tmem + L::kColO + b * MB;
         const uint32_t q_addr = smem_u32(ring + stage * L::kStageBytes);
         const uint32_t k_addr = q_addr + L::kQBytes;
         const uint32_t v_addr = k_addr + L::kQBytes;
         if (!mbar_wait(&full[stage], (it / NS) & 1, abort_flag)) { ok = false; break; }
+        if (!AGG_ONLY && it >= NB &&
+            !mbar_wait(&o_done[b], ((it - NB) / NB) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
         if (!AGG_ONLY) {
-          // P = Q K^T over D (both operands K-major)
+          // P = Q K^T over D (both operands K-major), into P buffer b
 #pragma unroll
           for (int kk = 0; kk < DP / 16; ++kk) {
             const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
             mma_bf16_ss(t_p, smem_desc_sw128(q_addr + off, 16, 1024),
                         smem_desc_sw128(k_addr + off, 16, 1024), idesc_p, kk > 0);
           }
-          mma_commit(p_done);
+          mma_commit(&p_done[b]);
           // the epilogue has copied the state to smem and released S in TMEM
           if (!mbar_wait(s_ready, it & 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
@@ -320,29 +328,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!AGG_ONLY) {
           mma_commit(s_done);
           if (!mbar_wait(p_ready, it & 1, abort_flag)) { ok = false; break; }
-          if (it > 0 && !mbar_wait(o_free, (it - 1) & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          // O = P V  (A = P K-major, B = V MN-major)
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-            mma_bf16_ss(t_o, smem_desc_sw128(p_addr + off, 16, 1024),
-                        smem_desc_sw128(v_addr + kk * 2048, kBoxBytes, 1024), idesc_o, kk > 0);
+          if (it >= NB && !mbar_wait(&o_free[b], ((it - NB) / NB) & 1, abort_flag)) {
+            ok = false;
+            break;
           }
-          // O += Q S  (A = Q K-major, B = S MN-major); with the split state
-          // O += Q S_hi + Q S_lo
+          tc_fence_after();
+          // O = P_hi V + P_lo V (A = packed bf16 P in TMEM, B = V MN-major)
+#pragma unroll
+          for (int part = 0; part < 2; ++part) {
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk) {
+              const uint32_t acol = (kk >> 2) * 64 + part * 32 + (kk & 3) * 8;
+              mma_bf16_ts(t_o, t_p + acol, smem_desc_sw128(v_addr + kk * 2048, kBoxBytes, 1024),
+                          idesc_o, (part == 0 && kk == 0) ? 0u : 1u);
+            }
+          }
+          // O += Q S_hi (+ Q S_lo)  (A = Q K-major, B = bf16 state copy, MN-major)
+          const uint32_t sbuf = s_addr + b * L::kSBufBytes;
 #pragma unroll
           for (int part = 0; part < (L::kSplit ? 2 : 1); ++part) {
 #pragma unroll
             for (int kk = 0; kk < DP / 16; ++kk) {
               const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
               mma_bf16_ss(t_o, smem_desc_sw128(q_addr + off, 16, 1024),
-                          smem_desc_sw128(s_addr + part * L::kSOneBytes + kk * 2048, DP * 128,
+                          smem_desc_sw128(sbuf + part * L::kSOneBytes + kk * 2048, DP * 128,
                                           1024),
                           idesc_o, 1u);
             }
           }
-          mma_commit(o_done);
+          mma_commit(&o_done[b]);
         }
         mma_commit(&empty[stage]);
       }
@@ -418,95 +432,123 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
       }
 
-      for (int it = 0; it < n_it && ok; ++it) {
-        const int tile = a.reverse ? (t_end - 1 - it) : (t_first + it);
-        // (a) bf16 copy of the state before this tile -> s_tile
-        if (it == 0 && !has_prefix) {
+      // Iteration it converts the state and P of tile it, then reads out O of
+      // tile it - (NB - 1): with double buffers the output of one tile is
+      // drained while the MMAs of the next run.
+      for (int it = 0; it < n_it + NB - 1 && ok; ++it) {
+        if (it < n_it) {
+          const int b = it % NB;
+          uint8_t* sbuf = s_tile + b * L::kSBufBytes;
+          // (a) bf16 copy (hi, lo) of the state before tile it
+          if (it == 0 && !has_prefix) {
 #pragma unroll
-          for (int sb = 0; sb < L::kSBlocks; ++sb) {
-            if (sb * 128 + wq * 32 >= DP) continue;
+            for (int sb = 0; sb < L::kSBlocks; ++sb) {
+              if (sb * 128 + wq * 32 >= DP) continue;
 #pragma unroll
-            for (int c = 0; c < MB / 32; ++c) {
-              store_zero32(s_tile, sb * 128 + row, c * 32, DP * 128);
-              if (L::kSplit)
-                store_zero32(s_tile + L::kSOneBytes, sb * 128 + row, c * 32, DP * 128);
+              for (int c = 0; c < MB / 32; ++c) {
+                store_zero32(sbuf, sb * 128 + row, c * 32, DP * 128);
+                if (L::kSplit)
+                  store_zero32(sbuf + L::kSOneBytes, sb * 128 + row, c * 32, DP * 128);
+              }
+            }
+          } else {
+            if (it > 0) {
+              if (!mbar_wait(s_done, (it - 1) & 1, abort_flag)) { ok = false; break; }
+              tc_fence_after();
+            }
+#pragma unroll
+            for (int sb = 0; sb < L::kSBlocks; ++sb) {
+              if (sb * 128 + wq * 32 >= DP) continue;
+#pragma unroll
+              for (int c = 0; c < MB / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(lane_base + L::kColS + sb * MB + c * 32, r);
+                tmem_ld_wait();
+                if (L::kSplit)
+                  store_chunk32_split(sbuf, sbuf + L::kSOneBytes, sb * 128 + row, c * 32,
+                                      DP * 128, r);
+                else
+                  store_chunk32(sbuf, sb * 128 + row, c * 32, DP * 128, r);
+              }
             }
           }
-        } else {
-          if (it > 0) {
-            if (!mbar_wait(s_done, (it - 1) & 1, abort_flag)) { ok = false; break; }
-            tc_fence_after();
-          }
-#pragma unroll
-          for (int sb = 0; sb < L::kSBlocks; ++sb) {
-            if (sb * 128 + wq * 32 >= DP) continue;
-#pragma unroll
-            for (int c = 0; c < MB / 32; ++c) {
-              uint32_t r[32];
-              tmem_ld32(lane_base + L::kColS + sb * MB + c * 32, r);
-              tmem_ld_wait();
-              if (L::kSplit)
-                store_chunk32_split(s_tile, s_tile + L::kSOneBytes, sb * 128 + row, c * 32,
-                                    DP * 128, r);
-              else
-                store_chunk32(s_tile, sb * 128 + row, c * 32, DP * 128, r);
-            }
-          }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(s_ready);
+          fence_proxy_async_smem();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(s_ready);
 
-        // (b) P: mask to the causal triangle of the tile, bf16 -> p_tile
-        if (!mbar_wait(p_done, it & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
+          // (b) P of tile it: mask to the causal triangle of the tile, split
+          // into bf16 hi + lo and pack back into the same TMEM columns:
+          // half h (columns j in [64h, 64h+64)) -> hi at 64h + [0,32), lo at
+          // 64h + [32,64), two j per 32-bit column.
+          if (!mbar_wait(&p_done[b], (it / NB) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t pc = lane_base + L::kColP + b * 128;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const bool all_masked = a.reverse ? (c < wq) : (c > wq);
-          if (all_masked) {
-            store_zero32(p_tile, row, c * 32, kBoxBytes);
-            continue;
-          }
-          uint32_t r[32];
-          tmem_ld32(lane_base + L::kColP + c * 32, r);
-          tmem_ld_wait();
-          if (c == wq) {
+          for (int h = 0; h < 2; ++h) {
+            uint32_t r0[32], r1[32];
+            const int c0 = 2 * h, c1 = 2 * h + 1;
+            const bool z0 = a.reverse ? (c0 < wq) : (c0 > wq);  // chunk entirely masked
+            const bool z1 = a.reverse ? (c1 < wq) : (c1 > wq);
+            if (!z0) tmem_ld32(pc + 32 * c0, r0);
+            if (!z1) tmem_ld32(pc + 32 * c1, r1);
+            tmem_ld_wait();
 #pragma unroll
             for (int x = 0; x < 32; ++x) {
-              const bool keep = a.reverse ? (x >= lane) : (x <= lane);
-              if (!keep) r[x] = 0u;
+              const bool keep0 = !z0 && (c0 != wq || (a.reverse ? (x >= lane) : (x <= lane)));
+              const bool keep1 = !z1 && (c1 != wq || (a.reverse ? (x >= lane) : (x <= lane)));
+              if (!keep0) r0[x] = 0u;
+              if (!keep1) r1[x] = 0u;
             }
+            uint32_t hi[32], lo[32];
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+              const float a0 = __uint_as_float(r0[2 * x]), a1 = __uint_as_float(r0[2 * x + 1]);
+              hi[x] = pack_bf16x2(a0, a1);
+              lo[x] = pack_bf16x2(a0 - __uint_as_float(hi[x] << 16),
+                                  a1 - __uint_as_float(hi[x] & 0xffff0000u));
+              const float b0 = __uint_as_float(r1[2 * x]), b1 = __uint_as_float(r1[2 * x + 1]);
+              hi[16 + x] = pack_bf16x2(b0, b1);
+              lo[16 + x] = pack_bf16x2(b0 - __uint_as_float(hi[16 + x] << 16),
+                                       b1 - __uint_as_float(hi[16 + x] & 0xffff0000u));
+            }
+            tmem_st32(pc + 64 * h, hi);
+            tmem_st32(pc + 64 * h + 32, lo);
           }
-          store_chunk32(p_tile, row, c * 32, kBoxBytes, r);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(p_ready);
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(p_ready);
 
-        // (c) O -> bf16 -> o_tile -> TMA store
-        if (!mbar_wait(o_done, it & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        if (epi_tid == 0) tma_store_wait_read_all();  // previous tile's store has read o_tile
-        named_barrier_sync(1, kEpiThreads);
+        // (c) O of tile ct -> bf16 -> o_tile -> TMA store
+        const int ct = it - (NB - 1);
+        if (ct >= 0) {
+          const int b = ct % NB;
+          const int tile = a.reverse ? (t_end - 1 - ct) : (t_first + ct);
+          if (!mbar_wait(&o_done[b], (ct / NB) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          if (epi_tid == 0) tma_store_wait_read_all();  // previous store has read o_tile
+          named_barrier_sync(1, kEpiThreads);
 #pragma unroll
-        for (int c = 0; c < MB / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(lane_base + L::kColO + c * 32, r);
-          tmem_ld_wait();
-          store_chunk32(o_tile, row, c * 32, kBoxBytes, r);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(o_free);
-        fence_proxy_async_smem();
-        named_barrier_sync(1, kEpiThreads);
-        if (epi_tid == 0) {
+          for (int c = 0; c < MB / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(lane_base + L::kColO + b * MB + c * 32, r);
+            tmem_ld_wait();
+            store_chunk32(o_tile, row, c * 32, kBoxBytes, r);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&o_free[b]);
+          fence_proxy_async_smem();
+          named_barrier_sync(1, kEpiThreads);
+          if (epi_tid == 0) {
 #pragma unroll
-          for (int b = 0; b < L::kVBoxes; ++b)
-            tma_store_3d(&tm_o, o_tile + b * kBoxBytes, mb * MB + b * kBoxCols, tile * kTile, bh);
-          tma_store_commit();
+            for (int bx = 0; bx < L::kVBoxes; ++bx)
+              tma_store_3d(&tm_o, o_tile + bx * kBoxBytes, mb * MB + bx * kBoxCols, tile * kTile,
+                           bh);
+            tma_store_commit();
+          }
         }
       }
       if (!ok) record_timeout(a.status, abort_flag);
