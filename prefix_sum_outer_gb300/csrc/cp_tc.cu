@@ -42,8 +42,10 @@ using namespace cp::ptx;
 constexpr int kTile = 128;             // rows per tile = MMA M
 constexpr int kBoxCols = 64;           // bf16 columns per TMA box (128 bytes)
 constexpr int kBoxBytes = kTile * 128; // one [128 x 64] bf16 box
-constexpr int kThreads = 192;
-constexpr int kEpiThreads = 128;
+constexpr int kEpiWarps = 8;           // two warps per TMEM lane quarter
+constexpr int kGroups = kEpiWarps / 4;  // column groups sharing a lane quarter
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kSmemLimit = 232448;     // 227 KB opt-in dynamic shared memory
 
 struct Args {
@@ -214,11 +216,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < NB; ++i) {
       mbar_init(&p_done[i], 1);
       mbar_init(&o_done[i], 1);
-      mbar_init(&o_free[i], 4);
+      mbar_init(&o_free[i], kEpiWarps);
     }
     mbar_init(s_done, 1);
-    mbar_init(s_ready, 4);
-    mbar_init(p_ready, 4);
+    mbar_init(s_ready, kEpiWarps);
+    mbar_init(p_ready, kEpiWarps);
     mbar_init(fin, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -286,28 +288,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, MB, 0, 1);    // P . V, Q . S
       const uint32_t t_s = tmem + L::kColS;
       const uint32_t s_addr = smem_u32(s_tile);
+      auto stage_addr = [&](int it) { return smem_u32(ring + (it % NS) * L::kStageBytes); };
+      // P(it) = Q K^T over D (both operands K-major) into P buffer it % NB
+      auto issue_p = [&](int it) -> bool {
+        const int b = it % NB;
+        if (!mbar_wait(&full[it % NS], (it / NS) & 1, abort_flag)) return false;
+        // the O MMA that last read this P buffer (tile it - NB) has completed
+        if (it >= NB && !mbar_wait(&o_done[b], ((it - NB) / NB) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t q_addr = stage_addr(it), k_addr = q_addr + L::kQBytes;
+#pragma unroll
+        for (int kk = 0; kk < DP / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+          mma_bf16_ss(tmem + L::kColP + b * 128, smem_desc_sw128(q_addr + off, 16, 1024),
+                      smem_desc_sw128(k_addr + off, 16, 1024), idesc_p, kk > 0);
+        }
+        mma_commit(&p_done[b]);
+        return true;
+      };
       bool ok = true;
+      // With two P buffers, P of the next tile is issued before O of this
+      // one so that its conversion overlaps the O MMAs.
+      if (!AGG_ONLY && NB == 2 && n_it > 0) ok = issue_p(0);
       for (int it = 0; it < n_it && ok; ++it) {
         const int stage = it % NS;
         const int b = it % NB;
-        const uint32_t t_p = tmem + L::kColP + b * 128;
         const uint32_t t_o = tmem + L::kColO + b * MB;
-        const uint32_t q_addr = smem_u32(ring + stage * L::kStageBytes);
+        const uint32_t q_addr = stage_addr(it);
         const uint32_t k_addr = q_addr + L::kQBytes;
         const uint32_t v_addr = k_addr + L::kQBytes;
-        if (!mbar_wait(&full[stage], (it / NS) & 1, abort_flag)) { ok = false; break; }
-        if (!AGG_ONLY && it >= NB &&
-            !mbar_wait(&o_done[b], ((it - NB) / NB) & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
+        if (AGG_ONLY) {
+          if (!mbar_wait(&full[stage], (it / NS) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+        } else if (NB == 2) {
+          if (it + 1 < n_it && !issue_p(it + 1)) { ok = false; break; }
+        } else {
+          if (!issue_p(it)) { ok = false; break; }
+        }
         if (!AGG_ONLY) {
-          // P = Q K^T over D (both operands K-major), into P buffer b
-#pragma unroll
-          for (int kk = 0; kk < DP / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-            mma_bf16_ss(t_p, smem_desc_sw128(q_addr + off, 16, 1024),
-                        smem_desc_sw128(k_addr + off, 16, 1024), idesc_p, kk > 0);
-          }
-          mma_commit(&p_done[b]);
           // the epilogue has copied the state to smem and released S in TMEM
           if (!mbar_wait(s_ready, it & 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
@@ -333,12 +351,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          // O = P_hi V + P_lo V (A = packed bf16 P in TMEM, B = V MN-major)
+          // O = P_hi V + P_lo V (A = packed bf16 P in TMEM, B = V MN-major).
+          // Chunk c of P (columns 32c..32c+31) holds hi in its first 16 TMEM
+          // columns and lo in the next 16, two j per column.
+          const uint32_t t_p = tmem + L::kColP + b * 128;
 #pragma unroll
           for (int part = 0; part < 2; ++part) {
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk) {
-              const uint32_t acol = (kk >> 2) * 64 + part * 32 + (kk & 3) * 8;
+              const uint32_t acol = (kk >> 1) * 32 + part * 16 + (kk & 1) * 8;
               mma_bf16_ts(t_o, t_p + acol, smem_desc_sw128(v_addr + kk * 2048, kBoxBytes, 1024),
                           idesc_o, (part == 0 && kk == 0) ? 0u : 1u);
             }
@@ -369,9 +390,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int wq = warp & 3;                 // TMEM lane quarter of this warp
+    const int grp = (warp - 2) / 4;          // column group within the quarter
     const int row = wq * 32 + lane;          // tile row = TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-    const int epi_tid = threadIdx.x - 64;    // 0..127
+    const int epi_tid = threadIdx.x - 64;    // 0..kEpiThreads-1
     bool ok = true;
 
     if (AGG_ONLY) {
@@ -385,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (sb * 128 + wq * 32 >= DP) continue;  // warp-uniform
           const int d = sb * 128 + row;
 #pragma unroll
-          for (int c = 0; c < MB / 32; ++c) {
+          for (int c = grp; c < MB / 32; c += kGroups) {
             uint32_t r[32];
             tmem_ld32(lane_base + L::kColS + sb * MB + c * 32, r);
             tmem_ld_wait();
@@ -407,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (sb * 128 + wq * 32 >= DP) continue;
           const int d = sb * 128 + row;
 #pragma unroll
-          for (int c = 0; c < MB / 32; ++c) {
+          for (int c = grp; c < MB / 32; c += kGroups) {
             float acc[32];
 #pragma unroll
             for (int x = 0; x < 32; ++x) acc[x] = 0.f;
@@ -445,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int sb = 0; sb < L::kSBlocks; ++sb) {
               if (sb * 128 + wq * 32 >= DP) continue;
 #pragma unroll
-              for (int c = 0; c < MB / 32; ++c) {
+              for (int c = grp; c < MB / 32; c += kGroups) {
                 store_zero32(sbuf, sb * 128 + row, c * 32, DP * 128);
                 if (L::kSplit)
                   store_zero32(sbuf + L::kSOneBytes, sb * 128 + row, c * 32, DP * 128);
@@ -460,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int sb = 0; sb < L::kSBlocks; ++sb) {
               if (sb * 128 + wq * 32 >= DP) continue;
 #pragma unroll
-              for (int c = 0; c < MB / 32; ++c) {
+              for (int c = grp; c < MB / 32; c += kGroups) {
                 uint32_t r[32];
                 tmem_ld32(lane_base + L::kColS + sb * MB + c * 32, r);
                 tmem_ld_wait();
@@ -478,42 +500,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(s_ready);
 
           // (b) P of tile it: mask to the causal triangle of the tile, split
-          // into bf16 hi + lo and pack back into the same TMEM columns:
-          // half h (columns j in [64h, 64h+64)) -> hi at 64h + [0,32), lo at
-          // 64h + [32,64), two j per 32-bit column.
+          // into bf16 hi + lo and pack back into the chunk's own TMEM columns:
+          // chunk c (j in [32c, 32c+32)) -> hi at 32c + [0,16), lo at
+          // 32c + [16,32), two j per 32-bit column.
           if (!mbar_wait(&p_done[b], (it / NB) & 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint32_t pc = lane_base + L::kColP + b * 128;
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t r0[32], r1[32];
-            const int c0 = 2 * h, c1 = 2 * h + 1;
-            const bool z0 = a.reverse ? (c0 < wq) : (c0 > wq);  // chunk entirely masked
-            const bool z1 = a.reverse ? (c1 < wq) : (c1 > wq);
-            if (!z0) tmem_ld32(pc + 32 * c0, r0);
-            if (!z1) tmem_ld32(pc + 32 * c1, r1);
-            tmem_ld_wait();
+          for (int c = grp; c < 4; c += kGroups) {
+            uint32_t r[32], hl[32];
+            const bool zero = a.reverse ? (c < wq) : (c > wq);  // chunk entirely masked
+            if (zero) {
 #pragma unroll
-            for (int x = 0; x < 32; ++x) {
-              const bool keep0 = !z0 && (c0 != wq || (a.reverse ? (x >= lane) : (x <= lane)));
-              const bool keep1 = !z1 && (c1 != wq || (a.reverse ? (x >= lane) : (x <= lane)));
-              if (!keep0) r0[x] = 0u;
-              if (!keep1) r1[x] = 0u;
-            }
-            uint32_t hi[32], lo[32];
+              for (int x = 0; x < 32; ++x) hl[x] = 0u;
+            } else {
+              tmem_ld32(pc + 32 * c, r);
+              tmem_ld_wait();
+              if (c == wq) {
 #pragma unroll
-            for (int x = 0; x < 16; ++x) {
-              const float a0 = __uint_as_float(r0[2 * x]), a1 = __uint_as_float(r0[2 * x + 1]);
-              hi[x] = pack_bf16x2(a0, a1);
-              lo[x] = pack_bf16x2(a0 - __uint_as_float(hi[x] << 16),
-                                  a1 - __uint_as_float(hi[x] & 0xffff0000u));
-              const float b0 = __uint_as_float(r1[2 * x]), b1 = __uint_as_float(r1[2 * x + 1]);
-              hi[16 + x] = pack_bf16x2(b0, b1);
-              lo[16 + x] = pack_bf16x2(b0 - __uint_as_float(hi[16 + x] << 16),
-                                       b1 - __uint_as_float(hi[16 + x] & 0xffff0000u));
+                for (int x = 0; x < 32; ++x) {
+                  const bool keep = a.reverse ? (x >= lane) : (x <= lane);
+                  if (!keep) r[x] = 0u;
+                }
+              }
+#pragma unroll
+              for (int x = 0; x < 16; ++x) {
+                const float a0 = __uint_as_float(r[2 * x]), a1 = __uint_as_float(r[2 * x + 1]);
+                const uint32_t h = pack_bf16x2(a0, a1);
+                hl[x] = h;
+                hl[16 + x] = pack_bf16x2(a0 - __uint_as_float(h << 16),
+                                         a1 - __uint_as_float(h & 0xffff0000u));
+              }
             }
-            tmem_st32(pc + 64 * h, hi);
-            tmem_st32(pc + 64 * h + 32, lo);
+            tmem_st32(pc + 32 * c, hl);
           }
           tmem_st_wait();
           tc_fence_before();
@@ -531,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (epi_tid == 0) tma_store_wait_read_all();  // previous store has read o_tile
           named_barrier_sync(1, kEpiThreads);
 #pragma unroll
-          for (int c = 0; c < MB / 32; ++c) {
+          for (int c = grp; c < MB / 32; c += kGroups) {
             uint32_t r[32];
             tmem_ld32(lane_base + L::kColO + b * MB + c * 32, r);
             tmem_ld_wait();
