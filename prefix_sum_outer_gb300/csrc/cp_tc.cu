@@ -42,10 +42,14 @@ using namespace cp::ptx;
 constexpr int kTile = 128;             // rows per tile = MMA M
 constexpr int kBoxCols = 64;           // bf16 columns per TMA box (128 bytes)
 constexpr int kBoxBytes = kTile * 128; // one [128 x 64] bf16 box
-constexpr int kEpiWarps = 8;           // two warps per TMEM lane quarter
-constexpr int kGroups = kEpiWarps / 4;  // column groups sharing a lane quarter
-constexpr int kThreads = 64 + 32 * kEpiWarps;
-constexpr int kEpiThreads = 32 * kEpiWarps;
+// Warp roles: 0 TMA producer, 1 MMA issuer, then three converter groups
+// that each own one lane quarter of TMEM per warp.
+constexpr int kSWarp0 = 2, kSWarps = 4;    // state: fp32 S -> bf16 hi/lo operand copy
+constexpr int kPWarp0 = 6, kPWarps = 8;    // P: mask, split hi/lo, pack in TMEM (2 per quarter)
+constexpr int kOWarp0 = 14, kOWarps = 4;   // O: fp32 -> bf16 -> TMA store
+constexpr int kPGroups = kPWarps / 4;
+constexpr int kThreads = 32 * (kOWarp0 + kOWarps);
+constexpr int kOThreads = 32 * kOWarps;
 constexpr int kSmemLimit = 232448;     // 227 KB opt-in dynamic shared memory
 
 struct Args {
@@ -83,7 +87,10 @@ struct Layout {
   static constexpr int NB = (kColsDouble <= 512 && kStagesDouble >= 2) ? 2 : 1;
   static constexpr bool kSplit = (kAvail - NB * 2 * kSOneBytes - kOBytes) >= kStageBytes;
   static constexpr int kSBufBytes = (kSplit ? 2 : 1) * kSOneBytes;
-  static constexpr int kFixed = NB * kSBufBytes + kOBytes;
+  // output staging: two buffers (one store in flight) when they fit
+  static constexpr int kOBufs =
+      (kAvail - NB * kSBufBytes - 2 * kOBytes) / kStageBytes >= (NB == 2 ? 2 : 1) ? 2 : 1;
+  static constexpr int kFixed = NB * kSBufBytes + kOBufs * kOBytes;
   static constexpr int kStagesFit = (kAvail - kFixed) / kStageBytes;
   static constexpr int NS = kStagesFit > 4 ? 4 : kStagesFit;
   static constexpr int kSmemBytes = NS * kStageBytes + kFixed + kBarBytes + kAlignSlack;
@@ -177,19 +184,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* ring = smem;
   uint8_t* s_tile = ring + NS * L::kStageBytes;     // [NB] x (hi | lo) bf16 state copies
-  uint8_t* o_tile = s_tile + NB * L::kSBufBytes;    // output staging for the TMA store
-  uint64_t* bars = reinterpret_cast<uint64_t*>(o_tile + L::kOBytes);
+  uint8_t* o_tile = s_tile + NB * L::kSBufBytes;    // [kOBufs] output staging
+  uint64_t* bars = reinterpret_cast<uint64_t*>(o_tile + L::kOBufs * L::kOBytes);
   uint64_t* full = bars;              // [NS] TMA -> MMA
   uint64_t* empty = bars + NS;        // [NS] MMA -> TMA
-  uint64_t* p_done = bars + 2 * NS;   // [NB] MMA -> epilogue: P(t) in TMEM
-  uint64_t* o_done = p_done + NB;     // [NB] MMA -> epilogue: O(t) in TMEM, operands released
-  uint64_t* o_free = o_done + NB;     // [NB] epilogue -> MMA: O(t) read out of TMEM
-  uint64_t* s_done = o_free + NB;     // MMA -> epilogue: state updated with tile t
-  uint64_t* s_ready = s_done + 1;     // epilogue -> MMA: bf16 state copy written, S read
-  uint64_t* p_ready = s_done + 2;     // epilogue -> MMA: masked bf16 P (hi|lo) in TMEM
-  uint64_t* fin = s_done + 3;         // MMA drain before TMEM release
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(s_done + 4);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(s_done + 5);
+  uint64_t* p_done = bars + 2 * NS;   // [NB] MMA -> P group: P(t) in TMEM
+  uint64_t* p_ready = p_done + NB;    // [NB] P group -> MMA: masked bf16 P (hi|lo) packed
+  uint64_t* o_done = p_ready + NB;    // [NB] MMA -> O/S groups: O(t) done, operands released
+  uint64_t* o_free = o_done + NB;     // [NB] O group -> MMA: O(t) read out of TMEM
+  uint64_t* s_done = o_free + NB;     // MMA -> S group: state updated with tile t
+  uint64_t* s_ready = s_done + 1;     // S group -> MMA: bf16 state copy written, S read
+  uint64_t* fin = s_done + 2;         // MMA drain before TMEM release
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(s_done + 3);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(s_done + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -207,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int pidx = bh * a.n_mb + mb;
   const bool has_prefix =
       !AGG_ONLY && a.agg_in != nullptr && (a.reverse ? (seg < a.G - 1) : (seg > 0));
+  auto tile_of = [&](int it) { return a.reverse ? (t_end - 1 - it) : (t_first + it); };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -215,12 +223,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < NB; ++i) {
       mbar_init(&p_done[i], 1);
+      mbar_init(&p_ready[i], kPWarps);
       mbar_init(&o_done[i], 1);
-      mbar_init(&o_free[i], kEpiWarps);
+      mbar_init(&o_free[i], kOWarps);
     }
     mbar_init(s_done, 1);
-    mbar_init(s_ready, kEpiWarps);
-    mbar_init(p_ready, kEpiWarps);
+    mbar_init(s_ready, kSWarps);
     mbar_init(fin, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -242,6 +250,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  const int wq = warp & 3;                 // TMEM lane quarter of this warp
+  const int row = wq * 32 + lane;          // tile row = TMEM lane
+  const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -256,8 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           record_timeout(a.status, abort_flag);
           break;
         }
-        const int tile = a.reverse ? (t_end - 1 - it) : (t_first + it);
-        const int row0 = tile * kTile;
+        const int row0 = tile_of(it) * kTile;
         uint8_t* q_s = ring + stage * L::kStageBytes;
         uint8_t* k_s = q_s + L::kQBytes;
         uint8_t* v_s = k_s + L::kQBytes;
@@ -289,49 +299,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t t_s = tmem + L::kColS;
       const uint32_t s_addr = smem_u32(s_tile);
       auto stage_addr = [&](int it) { return smem_u32(ring + (it % NS) * L::kStageBytes); };
-      // P(it) = Q K^T over D (both operands K-major) into P buffer it % NB
-      auto issue_p = [&](int it) -> bool {
-        const int b = it % NB;
-        if (!mbar_wait(&full[it % NS], (it / NS) & 1, abort_flag)) return false;
-        // the O MMA that last read this P buffer (tile it - NB) has completed
-        if (it >= NB && !mbar_wait(&o_done[b], ((it - NB) / NB) & 1, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t q_addr = stage_addr(it), k_addr = q_addr + L::kQBytes;
-#pragma unroll
-        for (int kk = 0; kk < DP / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-          mma_bf16_ss(tmem + L::kColP + b * 128, smem_desc_sw128(q_addr + off, 16, 1024),
-                      smem_desc_sw128(k_addr + off, 16, 1024), idesc_p, kk > 0);
-        }
-        mma_commit(&p_done[b]);
-        return true;
-      };
-      bool ok = true;
-      // With two P buffers, P of the next tile is issued before O of this
-      // one so that its conversion overlaps the O MMAs.
-      if (!AGG_ONLY && NB == 2 && n_it > 0) ok = issue_p(0);
-      for (int it = 0; it < n_it && ok; ++it) {
-        const int stage = it % NS;
-        const int b = it % NB;
-        const uint32_t t_o = tmem + L::kColO + b * MB;
-        const uint32_t q_addr = stage_addr(it);
-        const uint32_t k_addr = q_addr + L::kQBytes;
-        const uint32_t v_addr = k_addr + L::kQBytes;
-        if (AGG_ONLY) {
-          if (!mbar_wait(&full[stage], (it / NS) & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-        } else if (NB == 2) {
-          if (it + 1 < n_it && !issue_p(it + 1)) { ok = false; break; }
-        } else {
-          if (!issue_p(it)) { ok = false; break; }
-        }
-        if (!AGG_ONLY) {
-          // the epilogue has copied the state to smem and released S in TMEM
-          if (!mbar_wait(s_ready, it & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-        }
+      auto issue_s = [&](int it) {
         // S += K^T V (A = K^T and B = V, both MN-major), one 128-row block of
         // the state per 128 columns of K
+        const uint32_t k_addr = stage_addr(it) + L::kQBytes;
+        const uint32_t v_addr = k_addr + L::kQBytes;
         const bool fresh = (it == 0) && !has_prefix;
 #pragma unroll
         for (int sb = 0; sb < L::kSBlocks; ++sb) {
@@ -343,59 +315,107 @@ __global__ void __launch_bounds__(kThreads, 1)
                         (fresh && kk == 0) ? 0u : 1u);
           }
         }
-        if (!AGG_ONLY) {
-          mma_commit(s_done);
-          if (!mbar_wait(p_ready, it & 1, abort_flag)) { ok = false; break; }
-          if (it >= NB && !mbar_wait(&o_free[b], ((it - NB) / NB) & 1, abort_flag)) {
-            ok = false;
-            break;
-          }
+      };
+      bool ok = true;
+      if (AGG_ONLY) {
+        for (int it = 0; it < n_it; ++it) {
+          if (!mbar_wait(&full[it % NS], (it / NS) & 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          // O = P_hi V + P_lo V (A = packed bf16 P in TMEM, B = V MN-major).
-          // Chunk c of P (columns 32c..32c+31) holds hi in its first 16 TMEM
-          // columns and lo in the next 16, two j per column.
-          const uint32_t t_p = tmem + L::kColP + b * 128;
-#pragma unroll
-          for (int part = 0; part < 2; ++part) {
-#pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk) {
-              const uint32_t acol = (kk >> 1) * 32 + part * 16 + (kk & 1) * 8;
-              mma_bf16_ts(t_o, t_p + acol, smem_desc_sw128(v_addr + kk * 2048, kBoxBytes, 1024),
-                          idesc_o, (part == 0 && kk == 0) ? 0u : 1u);
-            }
-          }
-          // O += Q S_hi (+ Q S_lo)  (A = Q K-major, B = bf16 state copy, MN-major)
-          const uint32_t sbuf = s_addr + b * L::kSBufBytes;
-#pragma unroll
-          for (int part = 0; part < (L::kSplit ? 2 : 1); ++part) {
+          issue_s(it);
+          mma_commit(&empty[it % NS]);
+        }
+        if (ok) mma_commit(s_done);
+      } else {
+        // Non-blocking scheduler over the three MMA groups of each tile:
+        //   P(t) = Q K^T          needs the stage loaded and P buffer t%NB free
+        //   S(t): S += K^T V      needs the state copied out for tile t
+        //   O(t) = P V + Q S      needs P(t) packed and O buffer t%NB free
+        // P runs at most NB-1 tiles ahead of O.
+        int nP = 0, nS = 0, nO = 0;
+        uint64_t t0 = globaltimer();
+        uint32_t idle = 0;
+        while (nO < n_it) {
+          bool progressed = false;
+          if (nP < n_it && nP <= nO + NB - 1 && mbar_try_wait(&full[nP % NS], (nP / NS) & 1) &&
+              (nP < NB || mbar_try_wait(&o_done[nP % NB], ((nP - NB) / NB) & 1))) {
+            tc_fence_after();
+            const uint32_t q_addr = stage_addr(nP), k_addr = q_addr + L::kQBytes;
+            const uint32_t t_p = tmem + L::kColP + (nP % NB) * 128;
 #pragma unroll
             for (int kk = 0; kk < DP / 16; ++kk) {
               const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-              mma_bf16_ss(t_o, smem_desc_sw128(q_addr + off, 16, 1024),
-                          smem_desc_sw128(sbuf + part * L::kSOneBytes + kk * 2048, DP * 128,
-                                          1024),
-                          idesc_o, 1u);
+              mma_bf16_ss(t_p, smem_desc_sw128(q_addr + off, 16, 1024),
+                          smem_desc_sw128(k_addr + off, 16, 1024), idesc_p, kk > 0);
+            }
+            mma_commit(&p_done[nP % NB]);
+            ++nP;
+            progressed = true;
+          }
+          if (nS < nP && mbar_try_wait(s_ready, nS & 1)) {
+            tc_fence_after();
+            issue_s(nS);
+            mma_commit(s_done);
+            ++nS;
+            progressed = true;
+          }
+          if (nO < nS && mbar_try_wait(&p_ready[nO % NB], (nO / NB) & 1) &&
+              (nO < NB || mbar_try_wait(&o_free[nO % NB], ((nO - NB) / NB) & 1))) {
+            tc_fence_after();
+            const int b = nO % NB;
+            const uint32_t q_addr = stage_addr(nO);
+            const uint32_t v_addr = q_addr + 2 * L::kQBytes;
+            const uint32_t t_o = tmem + L::kColO + b * MB;
+            const uint32_t t_p = tmem + L::kColP + b * 128;
+            // O = P_hi V + P_lo V (A = packed bf16 P in TMEM, B = V MN-major).
+            // Chunk c of P (columns 32c..32c+31) holds hi in its first 16
+            // TMEM columns and lo in the next 16, two j per column.
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+#pragma unroll
+              for (int kk = 0; kk < kTile / 16; ++kk) {
+                const uint32_t acol = (kk >> 1) * 32 + part * 16 + (kk & 1) * 8;
+                mma_bf16_ts(t_o, t_p + acol,
+                            smem_desc_sw128(v_addr + kk * 2048, kBoxBytes, 1024), idesc_o,
+                            (part == 0 && kk == 0) ? 0u : 1u);
+              }
+            }
+            // O += Q S_hi (+ Q S_lo)  (A = Q K-major, B = bf16 state copy, MN-major)
+            const uint32_t sbuf = s_addr + b * L::kSBufBytes;
+#pragma unroll
+            for (int part = 0; part < (L::kSplit ? 2 : 1); ++part) {
+#pragma unroll
+              for (int kk = 0; kk < DP / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+                mma_bf16_ss(t_o, smem_desc_sw128(q_addr + off, 16, 1024),
+                            smem_desc_sw128(sbuf + part * L::kSOneBytes + kk * 2048, DP * 128,
+                                            1024),
+                            idesc_o, 1u);
+              }
+            }
+            mma_commit(&o_done[b]);
+            mma_commit(&empty[nO % NS]);
+            ++nO;
+            progressed = true;
+          }
+          if (progressed) {
+            idle = 0;
+          } else if ((++idle & 63u) == 0) {
+            if (idle == 64) t0 = globaltimer();
+            if (*abort_flag || globaltimer() - t0 > CP_WAIT_TIMEOUT_NS) {
+              ok = false;
+              break;
             }
           }
-          mma_commit(&o_done[b]);
         }
-        mma_commit(&empty[stage]);
       }
-      if (AGG_ONLY && ok) mma_commit(s_done);
       if (!ok) record_timeout(a.status, abort_flag);
       // every MMA issued so far completes before TMEM is released
       mma_commit(fin);
       mbar_wait_timeout(fin, 0, CP_WAIT_TIMEOUT_NS);
     }
-  } else {
-    // ------------------------------------------------------------ epilogue
-    const int wq = warp & 3;                 // TMEM lane quarter of this warp
-    const int grp = (warp - 2) / 4;          // column group within the quarter
-    const int row = wq * 32 + lane;          // tile row = TMEM lane
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-    const int epi_tid = threadIdx.x - 64;    // 0..kEpiThreads-1
+  } else if (warp < kPWarp0) {
+    // ------------------------------------------------------------ state group
     bool ok = true;
-
     if (AGG_ONLY) {
       if (!mbar_wait(s_done, 0, abort_flag)) {
         record_timeout(a.status, abort_flag);
@@ -407,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (sb * 128 + wq * 32 >= DP) continue;  // warp-uniform
           const int d = sb * 128 + row;
 #pragma unroll
-          for (int c = grp; c < MB / 32; c += kGroups) {
+          for (int c = 0; c < MB / 32; ++c) {
             uint32_t r[32];
             tmem_ld32(lane_base + L::kColS + sb * MB + c * 32, r);
             tmem_ld_wait();
@@ -429,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (sb * 128 + wq * 32 >= DP) continue;
           const int d = sb * 128 + row;
 #pragma unroll
-          for (int c = grp; c < MB / 32; c += kGroups) {
+          for (int c = 0; c < MB / 32; ++c) {
             float acc[32];
 #pragma unroll
             for (int x = 0; x < 32; ++x) acc[x] = 0.f;
@@ -453,126 +473,138 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st_wait();
       }
-
-      // Iteration it converts the state and P of tile it, then reads out O of
-      // tile it - (NB - 1): with double buffers the output of one tile is
-      // drained while the MMAs of the next run.
-      for (int it = 0; it < n_it + NB - 1 && ok; ++it) {
-        if (it < n_it) {
-          const int b = it % NB;
-          uint8_t* sbuf = s_tile + b * L::kSBufBytes;
-          // (a) bf16 copy (hi, lo) of the state before tile it
-          if (it == 0 && !has_prefix) {
+      for (int it = 0; it < n_it && ok; ++it) {
+        const int b = it % NB;
+        uint8_t* sbuf = s_tile + b * L::kSBufBytes;
+        // the O MMA that last read this copy (tile it - NB) has completed
+        if (it >= NB && !mbar_wait(&o_done[b], ((it - NB) / NB) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (it == 0 && !has_prefix) {
 #pragma unroll
-            for (int sb = 0; sb < L::kSBlocks; ++sb) {
-              if (sb * 128 + wq * 32 >= DP) continue;
+          for (int sb = 0; sb < L::kSBlocks; ++sb) {
+            if (sb * 128 + wq * 32 >= DP) continue;
 #pragma unroll
-              for (int c = grp; c < MB / 32; c += kGroups) {
-                store_zero32(sbuf, sb * 128 + row, c * 32, DP * 128);
-                if (L::kSplit)
-                  store_zero32(sbuf + L::kSOneBytes, sb * 128 + row, c * 32, DP * 128);
-              }
-            }
-          } else {
-            if (it > 0) {
-              if (!mbar_wait(s_done, (it - 1) & 1, abort_flag)) { ok = false; break; }
-              tc_fence_after();
-            }
-#pragma unroll
-            for (int sb = 0; sb < L::kSBlocks; ++sb) {
-              if (sb * 128 + wq * 32 >= DP) continue;
-#pragma unroll
-              for (int c = grp; c < MB / 32; c += kGroups) {
-                uint32_t r[32];
-                tmem_ld32(lane_base + L::kColS + sb * MB + c * 32, r);
-                tmem_ld_wait();
-                if (L::kSplit)
-                  store_chunk32_split(sbuf, sbuf + L::kSOneBytes, sb * 128 + row, c * 32,
-                                      DP * 128, r);
-                else
-                  store_chunk32(sbuf, sb * 128 + row, c * 32, DP * 128, r);
-              }
+            for (int c = 0; c < MB / 32; ++c) {
+              store_zero32(sbuf, sb * 128 + row, c * 32, DP * 128);
+              if (L::kSplit) store_zero32(sbuf + L::kSOneBytes, sb * 128 + row, c * 32, DP * 128);
             }
           }
-          fence_proxy_async_smem();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(s_ready);
-
-          // (b) P of tile it: mask to the causal triangle of the tile, split
-          // into bf16 hi + lo and pack back into the chunk's own TMEM columns:
-          // chunk c (j in [32c, 32c+32)) -> hi at 32c + [0,16), lo at
-          // 32c + [16,32), two j per 32-bit column.
-          if (!mbar_wait(&p_done[b], (it / NB) & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t pc = lane_base + L::kColP + b * 128;
+        } else {
+          if (it > 0) {
+            if (!mbar_wait(s_done, (it - 1) & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+          }
 #pragma unroll
-          for (int c = grp; c < 4; c += kGroups) {
-            uint32_t r[32], hl[32];
-            const bool zero = a.reverse ? (c < wq) : (c > wq);  // chunk entirely masked
-            if (zero) {
+          for (int sb = 0; sb < L::kSBlocks; ++sb) {
+            if (sb * 128 + wq * 32 >= DP) continue;
 #pragma unroll
-              for (int x = 0; x < 32; ++x) hl[x] = 0u;
-            } else {
-              tmem_ld32(pc + 32 * c, r);
+            for (int c = 0; c < MB / 32; ++c) {
+              uint32_t r[32];
+              tmem_ld32(lane_base + L::kColS + sb * MB + c * 32, r);
               tmem_ld_wait();
-              if (c == wq) {
-#pragma unroll
-                for (int x = 0; x < 32; ++x) {
-                  const bool keep = a.reverse ? (x >= lane) : (x <= lane);
-                  if (!keep) r[x] = 0u;
-                }
-              }
-#pragma unroll
-              for (int x = 0; x < 16; ++x) {
-                const float a0 = __uint_as_float(r[2 * x]), a1 = __uint_as_float(r[2 * x + 1]);
-                const uint32_t h = pack_bf16x2(a0, a1);
-                hl[x] = h;
-                hl[16 + x] = pack_bf16x2(a0 - __uint_as_float(h << 16),
-                                         a1 - __uint_as_float(h & 0xffff0000u));
-              }
+              if (L::kSplit)
+                store_chunk32_split(sbuf, sbuf + L::kSOneBytes, sb * 128 + row, c * 32, DP * 128,
+                                    r);
+              else
+                store_chunk32(sbuf, sb * 128 + row, c * 32, DP * 128, r);
             }
-            tmem_st32(pc + 32 * c, hl);
-          }
-          tmem_st_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(p_ready);
-        }
-
-        // (c) O of tile ct -> bf16 -> o_tile -> TMA store
-        const int ct = it - (NB - 1);
-        if (ct >= 0) {
-          const int b = ct % NB;
-          const int tile = a.reverse ? (t_end - 1 - ct) : (t_first + ct);
-          if (!mbar_wait(&o_done[b], (ct / NB) & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          if (epi_tid == 0) tma_store_wait_read_all();  // previous store has read o_tile
-          named_barrier_sync(1, kEpiThreads);
-#pragma unroll
-          for (int c = grp; c < MB / 32; c += kGroups) {
-            uint32_t r[32];
-            tmem_ld32(lane_base + L::kColO + b * MB + c * 32, r);
-            tmem_ld_wait();
-            store_chunk32(o_tile, row, c * 32, kBoxBytes, r);
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&o_free[b]);
-          fence_proxy_async_smem();
-          named_barrier_sync(1, kEpiThreads);
-          if (epi_tid == 0) {
-#pragma unroll
-            for (int bx = 0; bx < L::kVBoxes; ++bx)
-              tma_store_3d(&tm_o, o_tile + bx * kBoxBytes, mb * MB + bx * kBoxCols, tile * kTile,
-                           bh);
-            tma_store_commit();
           }
         }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_ready);
       }
       if (!ok) record_timeout(a.status, abort_flag);
-      if (epi_tid == 0) tma_store_wait_all();
     }
+  } else if (warp < kOWarp0) {
+    // ------------------------------------------------------------ P group
+    // P of tile it: mask to the causal triangle of the tile, split into bf16
+    // hi + lo and pack back into the chunk's own TMEM columns: chunk c
+    // (j in [32c, 32c+32)) -> hi at 32c + [0,16), lo at 32c + [16,32), two j
+    // per 32-bit column.
+    const int grp = (warp - kPWarp0) / 4;
+    bool ok = true;
+    for (int it = 0; !AGG_ONLY && it < n_it && ok; ++it) {
+      const int b = it % NB;
+      if (!mbar_wait(&p_done[b], (it / NB) & 1, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t pc = lane_base + L::kColP + b * 128;
+#pragma unroll
+      for (int c = grp; c < 4; c += kPGroups) {
+        uint32_t r[32], hl[32];
+        const bool zero = a.reverse ? (c < wq) : (c > wq);  // chunk entirely masked
+        if (zero) {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) hl[x] = 0u;
+        } else {
+          tmem_ld32(pc + 32 * c, r);
+          tmem_ld_wait();
+          if (c == wq) {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) {
+              const bool keep = a.reverse ? (x >= lane) : (x <= lane);
+              if (!keep) r[x] = 0u;
+            }
+          }
+#pragma unroll
+          for (int x = 0; x < 16; ++x) {
+            const float a0 = __uint_as_float(r[2 * x]), a1 = __uint_as_float(r[2 * x + 1]);
+            const uint32_t h = pack_bf16x2(a0, a1);
+            hl[x] = h;
+            hl[16 + x] = pack_bf16x2(a0 - __uint_as_float(h << 16),
+                                     a1 - __uint_as_float(h & 0xffff0000u));
+          }
+        }
+        tmem_st32(pc + 32 * c, hl);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_ready[b]);
+    }
+    if (!ok) record_timeout(a.status, abort_flag);
+  } else {
+    // ------------------------------------------------------------ O group
+    const int o_tid = threadIdx.x - 32 * kOWarp0;   // 0..kOThreads-1
+    bool ok = true;
+    for (int it = 0; !AGG_ONLY && it < n_it && ok; ++it) {
+      const int b = it % NB;
+      uint8_t* ob = o_tile + (it % L::kOBufs) * L::kOBytes;
+      if (!mbar_wait(&o_done[b], (it / NB) & 1, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      // the store that last read this staging buffer has finished reading it
+      if (o_tid == 0) {
+        if (L::kOBufs == 2)
+          asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        else
+          tma_store_wait_read_all();
+      }
+      named_barrier_sync(1, kOThreads);
+#pragma unroll
+      for (int c = 0; c < MB / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(lane_base + L::kColO + b * MB + c * 32, r);
+        tmem_ld_wait();
+        store_chunk32(ob, row, c * 32, kBoxBytes, r);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&o_free[b]);
+      fence_proxy_async_smem();
+      named_barrier_sync(1, kOThreads);
+      if (o_tid == 0) {
+        const int tile = tile_of(it);
+#pragma unroll
+        for (int bx = 0; bx < L::kVBoxes; ++bx)
+          tma_store_3d(&tm_o, ob + bx * kBoxBytes, mb * MB + bx * kBoxCols, tile * kTile, bh);
+        tma_store_commit();
+      }
+    }
+    if (!ok) record_timeout(a.status, abort_flag);
+    if (o_tid == 0) tma_store_wait_all();
   }
 
   tc_fence_before();
