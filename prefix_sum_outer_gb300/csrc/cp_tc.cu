@@ -336,8 +336,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t idle = 0;
         while (nO < n_it) {
           bool progressed = false;
-          if (nP < n_it && nP <= nO + NB - 1 && mbar_try_wait(&full[nP % NS], (nP / NS) & 1) &&
-              (nP < NB || mbar_try_wait(&o_done[nP % NB], ((nP - NB) / NB) & 1))) {
+          if (nP < n_it && nP <= nO + NB - 1 && mbar_test_wait(&full[nP % NS], (nP / NS) & 1) &&
+              (nP < NB || mbar_test_wait(&o_done[nP % NB], ((nP - NB) / NB) & 1))) {
             tc_fence_after();
             const uint32_t q_addr = stage_addr(nP), k_addr = q_addr + L::kQBytes;
             const uint32_t t_p = tmem + L::kColP + (nP % NB) * 128;
@@ -351,15 +351,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++nP;
             progressed = true;
           }
-          if (nS < nP && mbar_try_wait(s_ready, nS & 1)) {
+          if (nS < nP && mbar_test_wait(s_ready, nS & 1)) {
             tc_fence_after();
             issue_s(nS);
             mma_commit(s_done);
             ++nS;
             progressed = true;
           }
-          if (nO < nS && mbar_try_wait(&p_ready[nO % NB], (nO / NB) & 1) &&
-              (nO < NB || mbar_try_wait(&o_free[nO % NB], ((nO - NB) / NB) & 1))) {
+          if (nO < nS && mbar_test_wait(&p_ready[nO % NB], (nO / NB) & 1) &&
+              (nO < NB || mbar_test_wait(&o_free[nO % NB], ((nO - NB) / NB) & 1))) {
             tc_fence_after();
             const int b = nO % NB;
             const uint32_t q_addr = stage_addr(nO);
