@@ -299,20 +299,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t t_s = tmem + L::kColS;
       const uint32_t s_addr = smem_u32(s_tile);
       auto stage_addr = [&](int it) { return smem_u32(ring + (it % NS) * L::kStageBytes); };
+      // Descriptor high words (SBO = 1024 for every operand, 128-byte swizzle)
+      constexpr uint32_t kHi = desc_hi(1024);
+      // Descriptor low words advance by (byte offset >> 4) per K step.
       auto issue_s = [&](int it) {
         // S += K^T V (A = K^T and B = V, both MN-major), one 128-row block of
         // the state per 128 columns of K
         const uint32_t k_addr = stage_addr(it) + L::kQBytes;
         const uint32_t v_addr = k_addr + L::kQBytes;
+        const uint32_t kt_lo = desc_lo(k_addr, kBoxBytes);
+        const uint32_t v_lo = desc_lo(v_addr, kBoxBytes);
         const bool fresh = (it == 0) && !has_prefix;
 #pragma unroll
         for (int sb = 0; sb < L::kSBlocks; ++sb) {
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
-            mma_bf16_ss(t_s + sb * MB,
-                        smem_desc_sw128(k_addr + 2 * sb * kBoxBytes + kk * 2048, kBoxBytes, 1024),
-                        smem_desc_sw128(v_addr + kk * 2048, kBoxBytes, 1024), idesc_s,
-                        (fresh && kk == 0) ? 0u : 1u);
+            mma_ss_lo<kHi, kHi>(t_s + sb * MB, kt_lo + ((2 * sb * kBoxBytes + kk * 2048) >> 4),
+                                v_lo + ((kk * 2048) >> 4), idesc_s, (fresh && kk == 0) ? 0u : 1u);
           }
         }
       };
@@ -340,12 +343,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               (nP < NB || mbar_test_wait(&o_done[nP % NB], ((nP - NB) / NB) & 1))) {
             tc_fence_after();
             const uint32_t q_addr = stage_addr(nP), k_addr = q_addr + L::kQBytes;
+            const uint32_t q_lo = desc_lo(q_addr, 16), k_lo = desc_lo(k_addr, 16);
             const uint32_t t_p = tmem + L::kColP + (nP % NB) * 128;
 #pragma unroll
             for (int kk = 0; kk < DP / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-              mma_bf16_ss(t_p, smem_desc_sw128(q_addr + off, 16, 1024),
-                          smem_desc_sw128(k_addr + off, 16, 1024), idesc_p, kk > 0);
+              const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+              mma_ss_lo<kHi, kHi>(t_p, q_lo + off, k_lo + off, idesc_p, kk > 0);
             }
             mma_commit(&p_done[nP % NB]);
             ++nP;
@@ -369,27 +372,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             // O = P_hi V + P_lo V (A = packed bf16 P in TMEM, B = V MN-major).
             // Chunk c of P (columns 32c..32c+31) holds hi in its first 16
             // TMEM columns and lo in the next 16, two j per column.
+            const uint32_t v_lo = desc_lo(v_addr, kBoxBytes);
 #pragma unroll
             for (int part = 0; part < 2; ++part) {
 #pragma unroll
               for (int kk = 0; kk < kTile / 16; ++kk) {
                 const uint32_t acol = (kk >> 1) * 32 + part * 16 + (kk & 1) * 8;
-                mma_bf16_ts(t_o, t_p + acol,
-                            smem_desc_sw128(v_addr + kk * 2048, kBoxBytes, 1024), idesc_o,
-                            (part == 0 && kk == 0) ? 0u : 1u);
+                mma_ts_lo<kHi>(t_o, t_p + acol, v_lo + ((kk * 2048) >> 4), idesc_o,
+                               (part == 0 && kk == 0) ? 0u : 1u);
               }
             }
             // O += Q S_hi (+ Q S_lo)  (A = Q K-major, B = bf16 state copy, MN-major)
-            const uint32_t sbuf = s_addr + b * L::kSBufBytes;
+            const uint32_t q_lo = desc_lo(q_addr, 16);
+            const uint32_t s_lo = desc_lo(s_addr + b * L::kSBufBytes, DP * 128);
 #pragma unroll
             for (int part = 0; part < (L::kSplit ? 2 : 1); ++part) {
 #pragma unroll
               for (int kk = 0; kk < DP / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-                mma_bf16_ss(t_o, smem_desc_sw128(q_addr + off, 16, 1024),
-                            smem_desc_sw128(sbuf + part * L::kSOneBytes + kk * 2048, DP * 128,
-                                            1024),
-                            idesc_o, 1u);
+                const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+                mma_ss_lo<kHi, kHi>(t_o, q_lo + off,
+                                    s_lo + ((part * L::kSOneBytes + kk * 2048) >> 4), idesc_o, 1u);
               }
             }
             mma_commit(&o_done[b]);
