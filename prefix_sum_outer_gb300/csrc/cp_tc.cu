@@ -44,10 +44,11 @@ constexpr int kBoxCols = 64;           // bf16 columns per TMA box (128 bytes)
 constexpr int kBoxBytes = kTile * 128; // one [128 x 64] bf16 box
 // Warp roles: 0 TMA producer, 1 MMA issuer, then three converter groups
 // that each own one lane quarter of TMEM per warp.
+// Fourteen warps keep every sub-partition at four warps or fewer, which
+// leaves 128 registers per thread.
 constexpr int kSWarp0 = 2, kSWarps = 4;    // state: fp32 S -> bf16 hi/lo operand copy
-constexpr int kPWarp0 = 6, kPWarps = 8;    // P: mask, split hi/lo, pack in TMEM (2 per quarter)
-constexpr int kOWarp0 = 14, kOWarps = 4;   // O: fp32 -> bf16 -> TMA store
-constexpr int kPGroups = kPWarps / 4;
+constexpr int kPWarp0 = 6, kPWarps = 4;    // P: mask, split hi/lo, pack in TMEM
+constexpr int kOWarp0 = 10, kOWarps = 4;   // O: fp32 -> bf16 -> TMA store
 constexpr int kThreads = 32 * (kOWarp0 + kOWarps);
 constexpr int kOThreads = 32 * kOWarps;
 constexpr int kSmemLimit = 232448;     // 227 KB opt-in dynamic shared memory
@@ -71,35 +72,47 @@ struct Layout {
   static constexpr int kVBoxes = MB / kBoxCols;
   static constexpr int kSBlocks = (DP + 127) / 128;
   static constexpr int kQBytes = kQBoxes * kBoxBytes;
+  static constexpr int kQKBytes = 2 * kQBytes;               // one Q tile + one K tile
   static constexpr int kVBytes = kVBoxes * kBoxBytes;
-  static constexpr int kStageBytes = 2 * kQBytes + kVBytes;
   static constexpr int kSOneBytes = kVBoxes * DP * 128;      // DP x MB bf16
   static constexpr int kOBytes = kVBoxes * kBoxBytes;        // 128 x MB bf16
   static constexpr int kBarBytes = 1024;
   static constexpr int kAlignSlack = 1024;
   static constexpr int kAvail = kSmemLimit - kBarBytes - kAlignSlack;
+  // Q/K and V tiles live in two rings: Q and K are released once P, the
+  // state update and Q S have been issued, V only after P V, so the V ring
+  // gets one stage more when it fits.  Returns NQK * 8 + NV.
+  static constexpr int rings(int budget) {
+    for (int n = 4; n >= 1; --n) {
+      if (n * kQKBytes + (n + 1) * kVBytes <= budget) return n * 8 + n + 1;
+      if (n * kQKBytes + n * kVBytes <= budget) return n * 8 + n;
+    }
+    return 0;
+  }
   // TMEM: P (128 columns, fp32; later packed bf16 hi|lo) and O (MB columns)
-  // are double-buffered when they fit next to the state (kSBlocks x MB).
+  // are double-buffered when they fit next to the state (kSBlocks x MB) and
+  // the rings keep two Q/K stages.
   static constexpr int kColsDouble = 2 * 128 + 2 * MB + kSBlocks * MB;
-  // The state operand of Q S is split into hi + lo bf16 parts; its copy in
-  // shared memory is double-buffered together with P and O.
-  static constexpr int kStagesDouble = (kAvail - 4 * kSOneBytes - kOBytes) / kStageBytes;
-  static constexpr int NB = (kColsDouble <= 512 && kStagesDouble >= 2) ? 2 : 1;
-  static constexpr bool kSplit = (kAvail - NB * 2 * kSOneBytes - kOBytes) >= kStageBytes;
+  static constexpr int NB =
+      (kColsDouble <= 512 && rings(kAvail - 4 * kSOneBytes - 2 * kOBytes) / 8 >= 2) ? 2 : 1;
+  // The state operand of Q S is split into hi + lo bf16 parts when it fits.
+  static constexpr bool kSplit = rings(kAvail - NB * 2 * kSOneBytes - kOBytes) / 8 >= 1;
   static constexpr int kSBufBytes = (kSplit ? 2 : 1) * kSOneBytes;
   // output staging: two buffers (one store in flight) when they fit
   static constexpr int kOBufs =
-      (kAvail - NB * kSBufBytes - 2 * kOBytes) / kStageBytes >= (NB == 2 ? 2 : 1) ? 2 : 1;
+      rings(kAvail - NB * kSBufBytes - 2 * kOBytes) / 8 >= (NB == 2 ? 2 : 1) ? 2 : 1;
   static constexpr int kFixed = NB * kSBufBytes + kOBufs * kOBytes;
-  static constexpr int kStagesFit = (kAvail - kFixed) / kStageBytes;
-  static constexpr int NS = kStagesFit > 4 ? 4 : kStagesFit;
-  static constexpr int kSmemBytes = NS * kStageBytes + kFixed + kBarBytes + kAlignSlack;
+  static constexpr int NQK = rings(kAvail - kFixed) / 8;
+  static constexpr int NV = rings(kAvail - kFixed) % 8;
+  static constexpr int kSmemBytes =
+      NQK * kQKBytes + NV * kVBytes + kFixed + kBarBytes + kAlignSlack;
   static constexpr int kColP = 0;                 // + b * 128
   static constexpr int kColO = NB * 128;          // + b * MB
   static constexpr int kColS = NB * (128 + MB);   // + sb * MB
   static constexpr int kColsUsed = kColS + kSBlocks * MB;
   static constexpr int kColsAlloc = kColsUsed <= 256 ? 256 : 512;
-  static_assert(NS >= 1, "tile does not fit in shared memory");
+  static_assert(NQK >= 1 && NV >= 1, "tile does not fit in shared memory");
+  static_assert(kSmemBytes <= kSmemLimit, "shared memory overflow");
   static_assert(kColsUsed <= 512, "accumulators do not fit in TMEM");
   static_assert(DP % 64 == 0 && MB % 64 == 0, "64-column boxes");
 };
@@ -165,6 +178,38 @@ __device__ __forceinline__ void store_zero32(uint8_t* tile, int row, int col0, i
         make_uint4(0, 0, 0, 0);
 }
 
+// In place: mask a 32-column chunk of P to the causal triangle (only the
+// diagonal chunk needs it; an entirely masked chunk becomes zero), split
+// each value into bf16 hi + lo and pack: columns 0..15 <- hi pairs,
+// columns 16..31 <- lo pairs.
+__device__ __forceinline__ void split_pack_p(uint32_t (&r)[32], bool zero, bool diag, int lane,
+                                             int reverse) {
+  if (zero) {
+#pragma unroll
+    for (int x = 0; x < 32; ++x) r[x] = 0u;
+    return;
+  }
+  if (diag) {
+#pragma unroll
+    for (int x = 0; x < 32; ++x) {
+      const bool keep = reverse ? (x >= lane) : (x <= lane);
+      if (!keep) r[x] = 0u;
+    }
+  }
+  // hi of pair x goes to r[x] (already consumed), lo waits in a 16-entry
+  // temporary until the pairs it would overwrite are consumed
+  uint32_t lo[16];
+#pragma unroll
+  for (int x = 0; x < 16; ++x) {
+    const float a0 = __uint_as_float(r[2 * x]), a1 = __uint_as_float(r[2 * x + 1]);
+    const uint32_t h = pack_bf16x2(a0, a1);
+    lo[x] = pack_bf16x2(a0 - __uint_as_float(h << 16), a1 - __uint_as_float(h & 0xffff0000u));
+    r[x] = h;
+  }
+#pragma unroll
+  for (int x = 0; x < 16; ++x) r[16 + x] = lo[x];
+}
+
 __device__ __forceinline__ void record_timeout(int* status, volatile int* abort_flag) {
   *abort_flag = 1;
   if (status != nullptr) atomicCAS(status, 0, (int)CP_ERR_TIMEOUT);
@@ -177,24 +222,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_o, const Args a) {
   using L = Layout<DP, MB>;
-  constexpr int NS = L::NS;
+  constexpr int NQK = L::NQK;
+  constexpr int NV = L::NV;
   constexpr int NB = L::NB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* ring = smem;
-  uint8_t* s_tile = ring + NS * L::kStageBytes;     // [NB] x (hi | lo) bf16 state copies
-  uint8_t* o_tile = s_tile + NB * L::kSBufBytes;    // [kOBufs] output staging
+  uint8_t* qk_ring = smem;                           // [NQK] x (Q tile | K tile)
+  uint8_t* v_ring = qk_ring + NQK * L::kQKBytes;     // [NV] x V tile
+  uint8_t* s_tile = v_ring + NV * L::kVBytes;        // [NB] x (hi | lo) bf16 state copies
+  uint8_t* o_tile = s_tile + NB * L::kSBufBytes;     // [kOBufs] output staging
   uint64_t* bars = reinterpret_cast<uint64_t*>(o_tile + L::kOBufs * L::kOBytes);
-  uint64_t* full = bars;              // [NS] TMA -> MMA
-  uint64_t* empty = bars + NS;        // [NS] MMA -> TMA
-  uint64_t* p_done = bars + 2 * NS;   // [NB] MMA -> P group: P(t) in TMEM
-  uint64_t* p_ready = p_done + NB;    // [NB] P group -> MMA: masked bf16 P (hi|lo) packed
-  uint64_t* o_done = p_ready + NB;    // [NB] MMA -> O/S groups: O(t) done, operands released
-  uint64_t* o_free = o_done + NB;     // [NB] O group -> MMA: O(t) read out of TMEM
-  uint64_t* s_done = o_free + NB;     // MMA -> S group: state updated with tile t
-  uint64_t* s_ready = s_done + 1;     // S group -> MMA: bf16 state copy written, S read
-  uint64_t* fin = s_done + 2;         // MMA drain before TMEM release
+  uint64_t* full_qk = bars;                 // [NQK] TMA -> MMA
+  uint64_t* empty_qk = full_qk + NQK;       // [NQK] MMA -> TMA
+  uint64_t* full_v = empty_qk + NQK;        // [NV]
+  uint64_t* empty_v = full_v + NV;          // [NV]
+  uint64_t* p_done = empty_v + NV;          // [NB] MMA -> P group: P(t) in TMEM
+  uint64_t* p_ready = p_done + NB;          // [NB] P group -> MMA: masked bf16 P (hi|lo) packed
+  uint64_t* o_done = p_ready + NB;          // [NB] MMA -> O/S groups: O(t) done, operands released
+  uint64_t* o_free = o_done + NB;           // [NB] O group -> MMA: O(t) read out of TMEM
+  uint64_t* s_done = o_free + NB;           // MMA -> S group: state updated with tile t
+  uint64_t* s_ready = s_done + 1;           // S group -> MMA: bf16 state copy written, S read
+  uint64_t* fin = s_done + 2;               // MMA drain before TMEM release
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(s_done + 3);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(s_done + 4);
 
@@ -217,9 +266,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tile_of = [&](int it) { return a.reverse ? (t_end - 1 - it) : (t_first + it); };
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NS; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+    for (int i = 0; i < NQK; ++i) {
+      mbar_init(&full_qk[i], 1);
+      mbar_init(&empty_qk[i], 1);
+    }
+    for (int i = 0; i < NV; ++i) {
+      mbar_init(&full_v[i], 1);
+      mbar_init(&empty_v[i], 1);
     }
     for (int i = 0; i < NB; ++i) {
       mbar_init(&p_done[i], 1);
@@ -256,38 +309,60 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // Polls both rings and refills whichever has a free stage (V never runs
+    // ahead of Q/K).
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      constexpr uint32_t kBytes =
-          AGG_ONLY ? (L::kQBytes + L::kVBytes) : (2 * L::kQBytes + L::kVBytes);
-      int it = 0;
-      for (; it < n_it; ++it) {
-        const int stage = it % NS;
-        if (it >= NS && !mbar_wait(&empty[stage], ((it / NS) - 1) & 1, abort_flag)) {
-          record_timeout(a.status, abort_flag);
-          break;
-        }
-        const int row0 = tile_of(it) * kTile;
-        uint8_t* q_s = ring + stage * L::kStageBytes;
-        uint8_t* k_s = q_s + L::kQBytes;
-        uint8_t* v_s = k_s + L::kQBytes;
-        mbar_arrive_expect_tx(&full[stage], kBytes);
+      constexpr uint32_t kQKTx = AGG_ONLY ? L::kQBytes : L::kQKBytes;
+      int nq = 0, nv = 0;
+      uint64_t t0 = globaltimer();
+      uint32_t idle = 0;
+      while (nq < n_it || nv < n_it) {
+        bool progressed = false;
+        if (nq < n_it &&
+            (nq < NQK || mbar_test_wait(&empty_qk[nq % NQK], ((nq / NQK) - 1) & 1))) {
+          const int st = nq % NQK;
+          const int row0 = tile_of(nq) * kTile;
+          uint8_t* q_s = qk_ring + st * L::kQKBytes;
+          uint8_t* k_s = q_s + L::kQBytes;
+          mbar_arrive_expect_tx(&full_qk[st], kQKTx);
 #pragma unroll
-        for (int b = 0; b < L::kQBoxes; ++b) {
-          if (!AGG_ONLY)
-            tma_load_3d(q_s + b * kBoxBytes, &tm_q, &full[stage], b * kBoxCols, row0, bh, pol);
-          tma_load_3d(k_s + b * kBoxBytes, &tm_k, &full[stage], b * kBoxCols, row0, bh, pol);
+          for (int b = 0; b < L::kQBoxes; ++b) {
+            if (!AGG_ONLY)
+              tma_load_3d(q_s + b * kBoxBytes, &tm_q, &full_qk[st], b * kBoxCols, row0, bh, pol);
+            tma_load_3d(k_s + b * kBoxBytes, &tm_k, &full_qk[st], b * kBoxCols, row0, bh, pol);
+          }
+          ++nq;
+          progressed = true;
         }
+        if (nv < nq && (nv < NV || mbar_test_wait(&empty_v[nv % NV], ((nv / NV) - 1) & 1))) {
+          const int st = nv % NV;
+          const int row0 = tile_of(nv) * kTile;
+          uint8_t* v_s = v_ring + st * L::kVBytes;
+          mbar_arrive_expect_tx(&full_v[st], L::kVBytes);
 #pragma unroll
-        for (int b = 0; b < L::kVBoxes; ++b)
-          tma_load_3d(v_s + b * kBoxBytes, &tm_v, &full[stage], mb * MB + b * kBoxCols, row0, bh,
-                      pol);
+          for (int b = 0; b < L::kVBoxes; ++b)
+            tma_load_3d(v_s + b * kBoxBytes, &tm_v, &full_v[st], mb * MB + b * kBoxCols, row0,
+                        bh, pol);
+          ++nv;
+          progressed = true;
+        }
+        if (progressed) {
+          idle = 0;
+        } else if ((++idle & 63u) == 0) {
+          if (idle == 64) t0 = globaltimer();
+          if (*abort_flag || globaltimer() - t0 > CP_WAIT_TIMEOUT_NS) {
+            record_timeout(a.status, abort_flag);
+            break;
+          }
+        }
       }
       if (*abort_flag) {
         // let the copies already issued land before the CTA's memory goes away
-        const int lo = max(0, it - NS);
-        for (int j = lo; j < it; ++j)
-          mbar_wait_timeout(&full[j % NS], (j / NS) & 1, CP_WAIT_TIMEOUT_NS);
+        for (int j = max(0, nq - NQK); j < nq; ++j)
+          mbar_wait_timeout(&full_qk[j % NQK], (j / NQK) & 1, CP_WAIT_TIMEOUT_NS);
+        for (int j = max(0, nv - NV); j < nv; ++j)
+          mbar_wait_timeout(&full_v[j % NV], (j / NV) & 1, CP_WAIT_TIMEOUT_NS);
       }
     }
   } else if (warp == 1) {
@@ -296,19 +371,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_p = idesc_bf16_f32(128, 128, 0, 0);   // Q . K^T
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, MB, 1, 1);    // K^T . V
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, MB, 0, 1);    // P . V, Q . S
+      constexpr uint32_t kHi = desc_hi(1024);  // SBO = 1024, 128-byte swizzle
       const uint32_t t_s = tmem + L::kColS;
       const uint32_t s_addr = smem_u32(s_tile);
-      auto stage_addr = [&](int it) { return smem_u32(ring + (it % NS) * L::kStageBytes); };
-      // Descriptor high words (SBO = 1024 for every operand, 128-byte swizzle)
-      constexpr uint32_t kHi = desc_hi(1024);
+      auto qk_addr = [&](int it) { return smem_u32(qk_ring + (it % NQK) * L::kQKBytes); };
+      auto v_addr = [&](int it) { return smem_u32(v_ring + (it % NV) * L::kVBytes); };
       // Descriptor low words advance by (byte offset >> 4) per K step.
       auto issue_s = [&](int it) {
         // S += K^T V (A = K^T and B = V, both MN-major), one 128-row block of
         // the state per 128 columns of K
-        const uint32_t k_addr = stage_addr(it) + L::kQBytes;
-        const uint32_t v_addr = k_addr + L::kQBytes;
-        const uint32_t kt_lo = desc_lo(k_addr, kBoxBytes);
-        const uint32_t v_lo = desc_lo(v_addr, kBoxBytes);
+        const uint32_t kt_lo = desc_lo(qk_addr(it) + L::kQBytes, kBoxBytes);
+        const uint32_t v_lo = desc_lo(v_addr(it), kBoxBytes);
         const bool fresh = (it == 0) && !has_prefix;
 #pragma unroll
         for (int sb = 0; sb < L::kSBlocks; ++sb) {
@@ -322,28 +395,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       if (AGG_ONLY) {
         for (int it = 0; it < n_it; ++it) {
-          if (!mbar_wait(&full[it % NS], (it / NS) & 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&full_qk[it % NQK], (it / NQK) & 1, abort_flag) ||
+              !mbar_wait(&full_v[it % NV], (it / NV) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           issue_s(it);
-          mma_commit(&empty[it % NS]);
+          mma_commit(&empty_qk[it % NQK]);
+          mma_commit(&empty_v[it % NV]);
         }
         if (ok) mma_commit(s_done);
       } else {
-        // Non-blocking scheduler over the three MMA groups of each tile:
-        //   P(t) = Q K^T          needs the stage loaded and P buffer t%NB free
-        //   S(t): S += K^T V      needs the state copied out for tile t
-        //   O(t) = P V + Q S      needs P(t) packed and O buffer t%NB free
-        // P runs at most NB-1 tiles ahead of O.
-        int nP = 0, nS = 0, nO = 0;
+        // Non-blocking scheduler over the four MMA groups of each tile:
+        //   S(t):  S += K^T V     needs V(t) landed and the state copied out
+        //   P(t) = Q K^T          needs Q/K(t) landed and P buffer t%NB free
+        //   QS(t): O = Q S        needs S(t) issued and O buffer t%NB free
+        //   PV(t): O += P V       needs P(t) packed by the P group
+        // Q/K(t) are released after QS(t), V(t) after PV(t).  P runs at most
+        // NB-1 tiles ahead of PV; the state chain S is served first.
+        int nP = 0, nS = 0, nQ = 0, nV = 0;
         uint64_t t0 = globaltimer();
         uint32_t idle = 0;
-        while (nO < n_it) {
+        while (nV < n_it) {
           bool progressed = false;
-          if (nP < n_it && nP <= nO + NB - 1 && mbar_test_wait(&full[nP % NS], (nP / NS) & 1) &&
+          if (nS < nP && mbar_test_wait(&full_v[nS % NV], (nS / NV) & 1) &&
+              mbar_test_wait(s_ready, nS & 1)) {
+            tc_fence_after();
+            issue_s(nS);
+            mma_commit(s_done);
+            ++nS;
+            progressed = true;
+          }
+          if (nP < n_it && nP <= nV + NB - 1 &&
+              mbar_test_wait(&full_qk[nP % NQK], (nP / NQK) & 1) &&
               (nP < NB || mbar_test_wait(&o_done[nP % NB], ((nP - NB) / NB) & 1))) {
             tc_fence_after();
-            const uint32_t q_addr = stage_addr(nP), k_addr = q_addr + L::kQBytes;
-            const uint32_t q_lo = desc_lo(q_addr, 16), k_lo = desc_lo(k_addr, 16);
+            const uint32_t q_lo = desc_lo(qk_addr(nP), 16);
+            const uint32_t k_lo = desc_lo(qk_addr(nP) + L::kQBytes, 16);
             const uint32_t t_p = tmem + L::kColP + (nP % NB) * 128;
 #pragma unroll
             for (int kk = 0; kk < DP / 16; ++kk) {
@@ -354,49 +443,48 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++nP;
             progressed = true;
           }
-          if (nS < nP && mbar_test_wait(s_ready, nS & 1)) {
+          if (nQ < nS && (nQ < NB || mbar_test_wait(&o_free[nQ % NB], ((nQ - NB) / NB) & 1))) {
             tc_fence_after();
-            issue_s(nS);
-            mma_commit(s_done);
-            ++nS;
-            progressed = true;
-          }
-          if (nO < nS && mbar_test_wait(&p_ready[nO % NB], (nO / NB) & 1) &&
-              (nO < NB || mbar_test_wait(&o_free[nO % NB], ((nO - NB) / NB) & 1))) {
-            tc_fence_after();
-            const int b = nO % NB;
-            const uint32_t q_addr = stage_addr(nO);
-            const uint32_t v_addr = q_addr + 2 * L::kQBytes;
-            const uint32_t t_o = tmem + L::kColO + b * MB;
-            const uint32_t t_p = tmem + L::kColP + b * 128;
-            // O = P_hi V + P_lo V (A = packed bf16 P in TMEM, B = V MN-major).
-            // Chunk c of P (columns 32c..32c+31) holds hi in its first 16
-            // TMEM columns and lo in the next 16, two j per column.
-            const uint32_t v_lo = desc_lo(v_addr, kBoxBytes);
-#pragma unroll
-            for (int part = 0; part < 2; ++part) {
-#pragma unroll
-              for (int kk = 0; kk < kTile / 16; ++kk) {
-                const uint32_t acol = (kk >> 1) * 32 + part * 16 + (kk & 1) * 8;
-                mma_ts_lo<kHi>(t_o, t_p + acol, v_lo + ((kk * 2048) >> 4), idesc_o,
-                               (part == 0 && kk == 0) ? 0u : 1u);
-              }
-            }
-            // O += Q S_hi (+ Q S_lo)  (A = Q K-major, B = bf16 state copy, MN-major)
-            const uint32_t q_lo = desc_lo(q_addr, 16);
+            const int b = nQ % NB;
+            // O = Q S_hi (+ Q S_lo)  (A = Q K-major, B = bf16 state copy, MN-major)
+            const uint32_t q_lo = desc_lo(qk_addr(nQ), 16);
             const uint32_t s_lo = desc_lo(s_addr + b * L::kSBufBytes, DP * 128);
+            const uint32_t t_o = tmem + L::kColO + b * MB;
 #pragma unroll
             for (int part = 0; part < (L::kSplit ? 2 : 1); ++part) {
 #pragma unroll
               for (int kk = 0; kk < DP / 16; ++kk) {
                 const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
                 mma_ss_lo<kHi, kHi>(t_o, q_lo + off,
-                                    s_lo + ((part * L::kSOneBytes + kk * 2048) >> 4), idesc_o, 1u);
+                                    s_lo + ((part * L::kSOneBytes + kk * 2048) >> 4), idesc_o,
+                                    (part == 0 && kk == 0) ? 0u : 1u);
+              }
+            }
+            // P(nQ), S(nQ) and QS(nQ) issued: Q and K of tile nQ can go
+            mma_commit(&empty_qk[nQ % NQK]);
+            ++nQ;
+            progressed = true;
+          }
+          if (nV < nQ && mbar_test_wait(&p_ready[nV % NB], (nV / NB) & 1)) {
+            tc_fence_after();
+            const int b = nV % NB;
+            const uint32_t t_o = tmem + L::kColO + b * MB;
+            const uint32_t t_p = tmem + L::kColP + b * 128;
+            const uint32_t v_lo = desc_lo(v_addr(nV), kBoxBytes);
+            // O += P_hi V + P_lo V (A = packed bf16 P in TMEM, B = V MN-major).
+            // Chunk c of P (columns 32c..32c+31) holds hi in its first 16
+            // TMEM columns and lo in the next 16, two j per column.
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+#pragma unroll
+              for (int kk = 0; kk < kTile / 16; ++kk) {
+                const uint32_t acol = (kk >> 1) * 32 + part * 16 + (kk & 1) * 8;
+                mma_ts_lo<kHi>(t_o, t_p + acol, v_lo + ((kk * 2048) >> 4), idesc_o, 1u);
               }
             }
             mma_commit(&o_done[b]);
-            mma_commit(&empty[nO % NS]);
-            ++nO;
+            mma_commit(&empty_v[nV % NV]);
+            ++nV;
             progressed = true;
           }
           if (progressed) {
@@ -527,40 +615,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     // hi + lo and pack back into the chunk's own TMEM columns: chunk c
     // (j in [32c, 32c+32)) -> hi at 32c + [0,16), lo at 32c + [16,32), two j
     // per 32-bit column.
-    const int grp = (warp - kPWarp0) / 4;
     bool ok = true;
     for (int it = 0; !AGG_ONLY && it < n_it && ok; ++it) {
       const int b = it % NB;
       if (!mbar_wait(&p_done[b], (it / NB) & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
       const uint32_t pc = lane_base + L::kColP + b * 128;
-#pragma unroll
-      for (int c = grp; c < 4; c += kPGroups) {
-        uint32_t r[32], hl[32];
-        const bool zero = a.reverse ? (c < wq) : (c > wq);  // chunk entirely masked
-        if (zero) {
-#pragma unroll
-          for (int x = 0; x < 32; ++x) hl[x] = 0u;
-        } else {
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        const bool z = a.reverse ? (c < wq) : (c > wq);  // chunk entirely masked
+        uint32_t r[32];
+        if (!z) {
           tmem_ld32(pc + 32 * c, r);
           tmem_ld_wait();
-          if (c == wq) {
-#pragma unroll
-            for (int x = 0; x < 32; ++x) {
-              const bool keep = a.reverse ? (x >= lane) : (x <= lane);
-              if (!keep) r[x] = 0u;
-            }
-          }
-#pragma unroll
-          for (int x = 0; x < 16; ++x) {
-            const float a0 = __uint_as_float(r[2 * x]), a1 = __uint_as_float(r[2 * x + 1]);
-            const uint32_t h = pack_bf16x2(a0, a1);
-            hl[x] = h;
-            hl[16 + x] = pack_bf16x2(a0 - __uint_as_float(h << 16),
-                                     a1 - __uint_as_float(h & 0xffff0000u));
-          }
         }
-        tmem_st32(pc + 32 * c, hl);
+        split_pack_p(r, z, c == wq, lane, a.reverse);
+        tmem_st32(pc + 32 * c, r);
       }
       tmem_st_wait();
       tc_fence_before();
