@@ -76,7 +76,8 @@ typedef enum {
   CP_ERR_WORKSPACE_TOO_SMALL = 5,
   CP_ERR_CUDA = 6,               /* a CUDA runtime/driver call failed */
   CP_ERR_TIMEOUT = 7,            /* a kernel's bounded wait expired (status word) */
-  CP_ERR_NO_DEVICE = 8           /* no usable sm_103 device */
+  CP_ERR_NO_DEVICE = 8,          /* no usable sm_103 device */
+  CP_ERR_NOALLOC_LIMIT = 9       /* problem too large for causal_product_fwd_noalloc's scratch */
 } cp_status_t;
 
 /* Bytes of device workspace causal_product_fwd (backward = 0) or
@@ -102,6 +103,32 @@ cp_status_t causal_product_bwd(const void* q, const void* k, const void* v, cons
                                int64_t B, int64_t H, int64_t N, int64_t D, int64_t M,
                                cp_dtype_t dtype, void* workspace, size_t workspace_bytes,
                                void* stream);
+
+/* Size of the static device scratch array behind causal_product_fwd_noalloc. */
+#define CP_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/* Forward pass that allocates nothing: no cudaMalloc, no stream-ordered or
+ * library allocation.  It is meant for callers that must not allocate device
+ * memory themselves or through this library -- for example code running
+ * inside a host framework that owns every device allocation (plugins of
+ * inference runtimes with their own memory pools), or code that must not
+ * call cudaMalloc because it may synchronise the device.  (The paper has no
+ * counterpart of this entry point; it is a deployment convenience.)
+ *
+ * Same arguments, layout, ownership and result as causal_product_fwd, minus
+ * the workspace: its scratch (status word and scan aggregates) lives in one
+ * file-scope __device__ array of CP_NOALLOC_SCRATCH_BYTES bytes that every
+ * GPU loading the library holds until the process exits.  The first call on
+ * a device, with that device current, looks up the array's device address
+ * (cudaGetSymbolAddress) and caches it; make that first call before any
+ * stream capture.  Problems whose scratch would exceed the array return
+ * CP_ERR_NOALLOC_LIMIT before enqueuing anything.  The array is shared by
+ * every call and keeps the last call's contents: the call clears the status
+ * word on `stream` before its kernels run, and calls that overlap on the GPU
+ * (different streams, no ordering between them) race on it. */
+cp_status_t causal_product_fwd_noalloc(const void* q, const void* k, const void* v, void* out,
+                                       int64_t B, int64_t H, int64_t N, int64_t D, int64_t M,
+                                       cp_dtype_t dtype, void* stream);
 
 /* Synchronises `stream`, then returns and clears the status word in
  * `workspace` (CP_OK or CP_ERR_TIMEOUT), or CP_ERR_CUDA if the stream

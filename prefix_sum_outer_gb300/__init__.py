@@ -27,6 +27,7 @@ from . import build as _build
 
 __all__ = [
     "CP_OK", "CausalProductError", "causal_product", "causal_product_fwd", "causal_product_bwd",
+    "causal_product_fwd_noalloc",
     "causal_product_workspace_size", "causal_product_status", "causal_product_error_string",
     "library_path", "load_library",
 ]
@@ -66,6 +67,9 @@ def load_library(rebuild: bool = True) -> ctypes.CDLL:
             lib.causal_product_bwd.argtypes = [p, p, p, p, p, p, p, i64, i64, i64, i64, i64, c_int,
                                                p, sz, p]
             lib.causal_product_bwd.restype = c_int
+            lib.causal_product_fwd_noalloc.argtypes = [p, p, p, p, i64, i64, i64, i64, i64, c_int,
+                                                       p]
+            lib.causal_product_fwd_noalloc.restype = c_int
             lib.causal_product_status.argtypes = [p, p]
             lib.causal_product_status.restype = c_int
             lib.causal_product_error_string.argtypes = [c_int]
@@ -140,6 +144,28 @@ def causal_product_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                                 _stream_ptr(stream, q.device))
     if rc != CP_OK:
         raise CausalProductError(rc, "causal_product_fwd")
+    return out
+
+
+def causal_product_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                               out: torch.Tensor,
+                               stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Forward pass through the library's allocation-free entry point.
+
+    For callers that must not allocate device memory (their host framework
+    owns all device allocations, or they cannot afford an implicit device
+    synchronisation): the library uses a fixed static scratch array instead
+    of a workspace, so ``out`` must be provided.  Calls that overlap on the
+    GPU share that array and race; order them on one stream.
+    """
+    B, H, N, D, M = _dims(q, k, v)
+    code = _dtype_code(q, k, v, out)
+    _check_device(q, k, v, out)
+    rc = load_library().causal_product_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                                   out.data_ptr(), B, H, N, D, M, code,
+                                                   _stream_ptr(stream, q.device))
+    if rc != CP_OK:
+        raise CausalProductError(rc, "causal_product_fwd_noalloc")
     return out
 
 

@@ -3,6 +3,7 @@
 // include/causal_product.h for the contract.
 #include <algorithm>
 #include <cstdint>
+#include <mutex>
 
 #include "cp_internal.h"
 
@@ -197,8 +198,60 @@ const char* causal_product_error_string(cp_status_t s) {
     case CP_ERR_CUDA: return "CP_ERR_CUDA: a CUDA call failed";
     case CP_ERR_TIMEOUT: return "CP_ERR_TIMEOUT: a kernel wait expired";
     case CP_ERR_NO_DEVICE: return "CP_ERR_NO_DEVICE";
+    case CP_ERR_NOALLOC_LIMIT:
+      return "CP_ERR_NOALLOC_LIMIT: the problem needs more scratch than the static array of "
+             "causal_product_fwd_noalloc holds";
   }
   return "unknown causal_product status";
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Forward pass without any allocation.  Its scratch is a file-scope device
+// array; host code only ever passes the array's device address (looked up
+// once per device), never the host-side symbol itself.
+namespace cp {
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[CP_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.
+cp_status_t noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CP_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return CP_ERR_NO_DEVICE;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return CP_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return CP_OK;
+}
+
+}  // namespace
+}  // namespace cp
+
+extern "C" cp_status_t causal_product_fwd_noalloc(const void* q, const void* k, const void* v,
+                                                  void* out, int64_t B, int64_t H, int64_t N,
+                                                  int64_t D, int64_t M, cp_dtype_t dtype,
+                                                  void* stream) {
+  cp_status_t st = cp::check_dims(B, H, N, D, M, dtype);
+  if (st != CP_OK) return st;
+  if (cp::workspace_bytes(B * H, N, D, M, dtype, false) > CP_NOALLOC_SCRATCH_BYTES)
+    return CP_ERR_NOALLOC_LIMIT;
+  if (N == 0) return causal_product_fwd(q, k, v, out, B, H, N, D, M, dtype, nullptr, 0, stream);
+  void* scratch = nullptr;
+  st = cp::noalloc_scratch(&scratch);
+  if (st != CP_OK) return st;
+  // With a caller-style workspace the forward entry point allocates nothing.
+  return causal_product_fwd(q, k, v, out, B, H, N, D, M, dtype, scratch,
+                            CP_NOALLOC_SCRATCH_BYTES, stream);
+}
