@@ -42,14 +42,16 @@ using namespace cp::ptx;
 constexpr int kTile = 128;             // rows per tile = MMA M
 constexpr int kBoxCols = 64;           // bf16 columns per TMA box (128 bytes)
 constexpr int kBoxBytes = kTile * 128; // one [128 x 64] bf16 box
-// Warp roles: 0 TMA producer, 1 MMA issuer, then three converter groups
-// that each own one lane quarter of TMEM per warp.
-// Fourteen warps keep every sub-partition at four warps or fewer, which
+// Warp roles: 0 TMA producer, 1 and 14 MMA issuers (the issuing thread's
+// instruction rate, not the tensor pipe, bounds a single issuer), then three
+// converter groups that each own one lane quarter of TMEM per warp.
+// Fifteen warps keep every sub-partition at four warps or fewer, which
 // leaves 128 registers per thread.
 constexpr int kSWarp0 = 2, kSWarps = 4;    // state: fp32 S -> bf16 hi/lo operand copy
 constexpr int kPWarp0 = 6, kPWarps = 4;    // P: mask, split hi/lo, pack in TMEM
 constexpr int kOWarp0 = 10, kOWarps = 4;   // O: fp32 -> bf16 -> TMA store
-constexpr int kThreads = 32 * (kOWarp0 + kOWarps);
+constexpr int kBWarp = 14;                 // second MMA issuer (P and P V)
+constexpr int kThreads = 32 * (kBWarp + 1);
 constexpr int kOThreads = 32 * kOWarps;
 constexpr int kSmemLimit = 232448;     // 227 KB opt-in dynamic shared memory
 
@@ -89,32 +91,44 @@ struct Layout {
     }
     return 0;
   }
-  // TMEM: P (128 columns, fp32; later packed bf16 hi|lo) and O (MB columns)
-  // are double-buffered when they fit next to the state (kSBlocks x MB) and
-  // the rings keep two Q/K stages.
-  static constexpr int kColsDouble = 2 * 128 + 2 * MB + kSBlocks * MB;
-  static constexpr int NB =
-      (kColsDouble <= 512 && rings(kAvail - 4 * kSOneBytes - 2 * kOBytes) / 8 >= 2) ? 2 : 1;
-  // The state operand of Q S is split into hi + lo bf16 parts when it fits.
-  static constexpr bool kSplit = rings(kAvail - NB * 2 * kSOneBytes - kOBytes) / 8 >= 1;
+  // TMEM holds NP buffers of P (128 columns, fp32; later packed bf16 hi|lo),
+  // the Q S accumulator O1, the P V accumulator O2 (MB columns) and the
+  // state (kSBlocks x MB).  O1 is 2 MB wide when it fits: Q [S_hi | S_lo]
+  // in one N = 2 MB chain, the two halves summed on read-out.  A P buffer is
+  // reused only after the P V that read it has completed.
+  static constexpr int cols(int np, bool wide) {
+    return np * 128 + (wide ? 2 : 1) * MB + MB + kSBlocks * MB;
+  }
+  static constexpr int NP = cols(2, false) <= 512 ? 2 : 1;
+  static constexpr bool kWide = cols(NP, true) <= 512 && 2 * MB <= 256;
+  static constexpr int kO1Cols = (kWide ? 2 : 1) * MB;
+  static constexpr int NO = 1;
+  // bf16 copies of the state in shared memory (one per tile in flight, at
+  // most two); the state operand of Q S is split into hi + lo parts when it
+  // fits next to a one-stage ring.
+  static constexpr int NSB =
+      (NP >= 2 && rings(kAvail - 4 * kSOneBytes - 2 * kOBytes) / 8 >= 2) ? 2 : 1;
+  static constexpr bool kSplit = rings(kAvail - NSB * 2 * kSOneBytes - kOBytes) / 8 >= 1;
   static constexpr int kSBufBytes = (kSplit ? 2 : 1) * kSOneBytes;
   // output staging: two buffers (one store in flight) when they fit
   static constexpr int kOBufs =
-      rings(kAvail - NB * kSBufBytes - 2 * kOBytes) / 8 >= (NB == 2 ? 2 : 1) ? 2 : 1;
-  static constexpr int kFixed = NB * kSBufBytes + kOBufs * kOBytes;
+      rings(kAvail - NSB * kSBufBytes - 2 * kOBytes) / 8 >= (NSB == 2 ? 2 : 1) ? 2 : 1;
+  static constexpr int kFixed = NSB * kSBufBytes + kOBufs * kOBytes;
   static constexpr int NQK = rings(kAvail - kFixed) / 8;
   static constexpr int NV = rings(kAvail - kFixed) % 8;
   static constexpr int kSmemBytes =
       NQK * kQKBytes + NV * kVBytes + kFixed + kBarBytes + kAlignSlack;
-  static constexpr int kColP = 0;                 // + b * 128
-  static constexpr int kColO = NB * 128;          // + b * MB
-  static constexpr int kColS = NB * (128 + MB);   // + sb * MB
+  static constexpr int kColP = 0;                        // + b * 128
+  static constexpr int kColO1 = NP * 128;                // Q S (kO1Cols)
+  static constexpr int kColO2 = kColO1 + kO1Cols;        // P V (MB)
+  static constexpr int kColS = kColO2 + MB;              // + sb * MB
   static constexpr int kColsUsed = kColS + kSBlocks * MB;
   static constexpr int kColsAlloc = kColsUsed <= 256 ? 256 : 512;
   static_assert(NQK >= 1 && NV >= 1, "tile does not fit in shared memory");
   static_assert(kSmemBytes <= kSmemLimit, "shared memory overflow");
   static_assert(kColsUsed <= 512, "accumulators do not fit in TMEM");
   static_assert(DP % 64 == 0 && MB % 64 == 0, "64-column boxes");
+  static_assert(!kWide || kSplit, "the wide Q S chain reads S_hi and S_lo side by side");
 };
 
 // Byte offset of element (row, col) inside a [rows x 64k] bf16 tile stored
@@ -224,28 +238,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   using L = Layout<DP, MB>;
   constexpr int NQK = L::NQK;
   constexpr int NV = L::NV;
-  constexpr int NB = L::NB;
+  constexpr int NP = L::NP;
+  constexpr int NSB = L::NSB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* qk_ring = smem;                           // [NQK] x (Q tile | K tile)
   uint8_t* v_ring = qk_ring + NQK * L::kQKBytes;     // [NV] x V tile
-  uint8_t* s_tile = v_ring + NV * L::kVBytes;        // [NB] x (hi | lo) bf16 state copies
-  uint8_t* o_tile = s_tile + NB * L::kSBufBytes;     // [kOBufs] output staging
+  uint8_t* s_tile = v_ring + NV * L::kVBytes;        // [NSB] x (hi | lo) bf16 state copies
+  uint8_t* o_tile = s_tile + NSB * L::kSBufBytes;    // [kOBufs] output staging
   uint64_t* bars = reinterpret_cast<uint64_t*>(o_tile + L::kOBufs * L::kOBytes);
   uint64_t* full_qk = bars;                 // [NQK] TMA -> MMA
   uint64_t* empty_qk = full_qk + NQK;       // [NQK] MMA -> TMA
   uint64_t* full_v = empty_qk + NQK;        // [NV]
   uint64_t* empty_v = full_v + NV;          // [NV]
-  uint64_t* p_done = empty_v + NV;          // [NB] MMA -> P group: P(t) in TMEM
-  uint64_t* p_ready = p_done + NB;          // [NB] P group -> MMA: masked bf16 P (hi|lo) packed
-  uint64_t* o_done = p_ready + NB;          // [NB] MMA -> O/S groups: O(t) done, operands released
-  uint64_t* o_free = o_done + NB;           // [NB] O group -> MMA: O(t) read out of TMEM
-  uint64_t* s_done = o_free + NB;           // MMA -> S group: state updated with tile t
-  uint64_t* s_ready = s_done + 1;           // S group -> MMA: bf16 state copy written, S read
-  uint64_t* fin = s_done + 2;               // MMA drain before TMEM release
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(s_done + 3);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(s_done + 4);
+  uint64_t* p_done = empty_v + NV;          // [NP] issuer B -> P group: P(t) in TMEM
+  uint64_t* p_ready = p_done + NP;          // [NP] P group -> B: masked bf16 P (hi|lo) packed
+  uint64_t* pv_done = p_ready + NP;         // [NP] B -> O group, B: O2(t) final, P buffer free
+  uint64_t* qs_done = pv_done + NP;         // [NSB] A -> S group: Q S(t) done, state copy free
+  uint64_t* o1_done = qs_done + NSB;        // A -> O group: O1(t) final
+  uint64_t* o_free = o1_done + 1;           // O group -> A, B: O1 and O2 of tile t read out
+  uint64_t* s_done = o_free + 1;            // A -> S group: state updated with tile t
+  uint64_t* s_ready = s_done + 1;           // S group -> A: bf16 state copy written, S read
+  uint64_t* fin = s_done + 2;               // [2] issuer drains before TMEM release
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(s_done + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(s_done + 5);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -266,23 +283,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tile_of = [&](int it) { return a.reverse ? (t_end - 1 - it) : (t_first + it); };
 
   if (threadIdx.x == 0) {
+    // a stage is released by both issuers (A: S / Q S, B: P / P V); in the
+    // aggregate-only mode issuer A alone consumes the rings
+    const uint32_t kRel = AGG_ONLY ? 1 : 2;
     for (int i = 0; i < NQK; ++i) {
       mbar_init(&full_qk[i], 1);
-      mbar_init(&empty_qk[i], 1);
+      mbar_init(&empty_qk[i], kRel);
     }
     for (int i = 0; i < NV; ++i) {
       mbar_init(&full_v[i], 1);
-      mbar_init(&empty_v[i], 1);
+      mbar_init(&empty_v[i], kRel);
     }
-    for (int i = 0; i < NB; ++i) {
+    for (int i = 0; i < NP; ++i) {
       mbar_init(&p_done[i], 1);
       mbar_init(&p_ready[i], kPWarps);
-      mbar_init(&o_done[i], 1);
-      mbar_init(&o_free[i], kOWarps);
+      mbar_init(&pv_done[i], 1);
     }
+    for (int i = 0; i < NSB; ++i) mbar_init(&qs_done[i], 1);
+    mbar_init(o1_done, 1);
+    mbar_init(o_free, kOWarps);
     mbar_init(s_done, 1);
     mbar_init(s_ready, kSWarps);
-    mbar_init(fin, 1);
+    mbar_init(&fin[0], 1);
+    mbar_init(&fin[1], 1);
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -365,14 +388,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait_timeout(&full_v[j % NV], (j / NV) & 1, CP_WAIT_TIMEOUT_NS);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+  } else if (warp == 1 || warp == kBWarp) {
+    // ------------------------------------------------------------ MMA issuers
+    // Issuer A (warp 1): the state chain S(t) and the inter-tile read-out
+    // Q S(t) into O1.  Issuer B (warp kBWarp): P(t) = Q K^T and the
+    // intra-tile P V(t) into O2.  The two never touch the same accumulator,
+    // so they need no ordering between them; a ring stage is released by a
+    // commit from each.
+    if (lane == 0 && (warp == 1 || !AGG_ONLY)) {
       constexpr uint32_t idesc_p = idesc_bf16_f32(128, 128, 0, 0);   // Q . K^T
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, MB, 1, 1);    // K^T . V
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, MB, 0, 1);    // P . V, Q . S
+      constexpr uint32_t idesc_ow = idesc_bf16_f32(128, 2 * MB, 0, 1);  // Q . [S_hi | S_lo]
       constexpr uint32_t kHi = desc_hi(1024);  // SBO = 1024, 128-byte swizzle
       const uint32_t t_s = tmem + L::kColS;
+      const uint32_t t_o1 = tmem + L::kColO1;
+      const uint32_t t_o2 = tmem + L::kColO2;
       const uint32_t s_addr = smem_u32(s_tile);
       auto qk_addr = [&](int it) { return smem_u32(qk_ring + (it % NQK) * L::kQKBytes); };
       auto v_addr = [&](int it) { return smem_u32(v_ring + (it % NV) * L::kVBytes); };
@@ -393,6 +424,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       bool ok = true;
+      uint64_t t0 = globaltimer();
+      uint32_t idle = 0;
+      auto idle_tick = [&](bool progressed) -> bool {  // false: give up
+        if (progressed) {
+          idle = 0;
+        } else if ((++idle & 63u) == 0) {
+          if (idle == 64) t0 = globaltimer();
+          if (*abort_flag || globaltimer() - t0 > CP_WAIT_TIMEOUT_NS) return false;
+        }
+        return true;
+      };
       if (AGG_ONLY) {
         for (int it = 0; it < n_it; ++it) {
           if (!mbar_wait(&full_qk[it % NQK], (it / NQK) & 1, abort_flag) ||
@@ -406,72 +448,88 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(&empty_v[it % NV]);
         }
         if (ok) mma_commit(s_done);
-      } else {
-        // Non-blocking scheduler over the four MMA groups of each tile:
-        //   S(t):  S += K^T V     needs V(t) landed and the state copied out
-        //   P(t) = Q K^T          needs Q/K(t) landed and P buffer t%NB free
-        //   QS(t): O = Q S        needs S(t) issued and O buffer t%NB free
-        //   PV(t): O += P V       needs P(t) packed by the P group
-        // Q/K(t) are released after QS(t), V(t) after PV(t).  P runs at most
-        // NB-1 tiles ahead of PV; the state chain S is served first.
-        int nP = 0, nS = 0, nQ = 0, nV = 0;
-        uint64_t t0 = globaltimer();
-        uint32_t idle = 0;
-        while (nV < n_it) {
+      } else if (warp == 1) {
+        // issuer A: S(t) needs Q/K(t), V(t) landed and the state copied out
+        // (s_ready); Q S(t) needs S(t) issued and O1 read out for t - 1.
+        int nS = 0, nQ = 0;
+        while (nQ < n_it) {
           bool progressed = false;
-          if (nS < nP && mbar_test_wait(&full_v[nS % NV], (nS / NV) & 1) &&
+          if (nS < n_it && mbar_test_wait(&full_qk[nS % NQK], (nS / NQK) & 1) &&
+              mbar_test_wait(&full_v[nS % NV], (nS / NV) & 1) &&
               mbar_test_wait(s_ready, nS & 1)) {
             tc_fence_after();
             issue_s(nS);
             mma_commit(s_done);
+            mma_commit(&empty_v[nS % NV]);
             ++nS;
             progressed = true;
           }
-          if (nP < n_it && nP <= nV + NB - 1 &&
+          if (nQ < nS && (nQ == 0 || mbar_test_wait(o_free, (nQ - 1) & 1))) {
+            tc_fence_after();
+            const uint32_t q_lo = desc_lo(qk_addr(nQ), 16);
+            const uint32_t s_lo = desc_lo(s_addr + (nQ % NSB) * L::kSBufBytes, DP * 128);
+            if (L::kWide) {
+              // O1 = Q [S_hi | S_lo]: hi and lo copies sit side by side as
+              // one MN-major operand of 2 MB columns
+#pragma unroll
+              for (int kk = 0; kk < DP / 16; ++kk) {
+                const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+                mma_ss_lo<kHi, kHi>(t_o1, q_lo + off, s_lo + ((kk * 2048) >> 4), idesc_ow,
+                                    kk > 0 ? 1u : 0u);
+              }
+            } else {
+              // O1 = Q S_hi (+ Q S_lo)
+#pragma unroll
+              for (int part = 0; part < (L::kSplit ? 2 : 1); ++part) {
+#pragma unroll
+                for (int kk = 0; kk < DP / 16; ++kk) {
+                  const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+                  mma_ss_lo<kHi, kHi>(t_o1, q_lo + off,
+                                      s_lo + ((part * L::kSOneBytes + kk * 2048) >> 4), idesc_o,
+                                      (part == 0 && kk == 0) ? 0u : 1u);
+                }
+              }
+            }
+            mma_commit(&qs_done[nQ % NSB]);
+            mma_commit(o1_done);
+            mma_commit(&empty_qk[nQ % NQK]);
+            ++nQ;
+            progressed = true;
+          }
+          if (!idle_tick(progressed)) { ok = false; break; }
+        }
+      } else {
+        // issuer B: P(t) needs Q/K(t) landed and P buffer t%NP free (P V of
+        // tile t - NP completed); P V(t) needs P(t) packed, V(t) landed and O2
+        // read out for t - 1.  P runs at most NP - 1 tiles ahead of P V.
+        int nP = 0, nV = 0;
+        while (nV < n_it) {
+          bool progressed = false;
+          if (nP < n_it && nP <= nV + NP - 1 &&
               mbar_test_wait(&full_qk[nP % NQK], (nP / NQK) & 1) &&
-              (nP < NB || mbar_test_wait(&o_done[nP % NB], ((nP - NB) / NB) & 1))) {
+              (nP < NP || mbar_test_wait(&pv_done[nP % NP], ((nP - NP) / NP) & 1))) {
             tc_fence_after();
             const uint32_t q_lo = desc_lo(qk_addr(nP), 16);
             const uint32_t k_lo = desc_lo(qk_addr(nP) + L::kQBytes, 16);
-            const uint32_t t_p = tmem + L::kColP + (nP % NB) * 128;
+            const uint32_t t_p = tmem + L::kColP + (nP % NP) * 128;
 #pragma unroll
             for (int kk = 0; kk < DP / 16; ++kk) {
               const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
               mma_ss_lo<kHi, kHi>(t_p, q_lo + off, k_lo + off, idesc_p, kk > 0);
             }
-            mma_commit(&p_done[nP % NB]);
+            mma_commit(&p_done[nP % NP]);
+            mma_commit(&empty_qk[nP % NQK]);
             ++nP;
             progressed = true;
           }
-          if (nQ < nS && (nQ < NB || mbar_test_wait(&o_free[nQ % NB], ((nQ - NB) / NB) & 1))) {
+          if (nV < nP && mbar_test_wait(&p_ready[nV % NP], (nV / NP) & 1) &&
+              mbar_test_wait(&full_v[nV % NV], (nV / NV) & 1) &&
+              (nV == 0 || mbar_test_wait(o_free, (nV - 1) & 1))) {
             tc_fence_after();
-            const int b = nQ % NB;
-            // O = Q S_hi (+ Q S_lo)  (A = Q K-major, B = bf16 state copy, MN-major)
-            const uint32_t q_lo = desc_lo(qk_addr(nQ), 16);
-            const uint32_t s_lo = desc_lo(s_addr + b * L::kSBufBytes, DP * 128);
-            const uint32_t t_o = tmem + L::kColO + b * MB;
-#pragma unroll
-            for (int part = 0; part < (L::kSplit ? 2 : 1); ++part) {
-#pragma unroll
-              for (int kk = 0; kk < DP / 16; ++kk) {
-                const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-                mma_ss_lo<kHi, kHi>(t_o, q_lo + off,
-                                    s_lo + ((part * L::kSOneBytes + kk * 2048) >> 4), idesc_o,
-                                    (part == 0 && kk == 0) ? 0u : 1u);
-              }
-            }
-            // P(nQ), S(nQ) and QS(nQ) issued: Q and K of tile nQ can go
-            mma_commit(&empty_qk[nQ % NQK]);
-            ++nQ;
-            progressed = true;
-          }
-          if (nV < nQ && mbar_test_wait(&p_ready[nV % NB], (nV / NB) & 1)) {
-            tc_fence_after();
-            const int b = nV % NB;
-            const uint32_t t_o = tmem + L::kColO + b * MB;
+            const int b = nV % NP;
             const uint32_t t_p = tmem + L::kColP + b * 128;
             const uint32_t v_lo = desc_lo(v_addr(nV), kBoxBytes);
-            // O += P_hi V + P_lo V (A = packed bf16 P in TMEM, B = V MN-major).
+            // O2 = P_hi V + P_lo V (A = packed bf16 P in TMEM, B = V MN-major).
             // Chunk c of P (columns 32c..32c+31) holds hi in its first 16
             // TMEM columns and lo in the next 16, two j per column.
 #pragma unroll
@@ -479,29 +537,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int kk = 0; kk < kTile / 16; ++kk) {
                 const uint32_t acol = (kk >> 1) * 32 + part * 16 + (kk & 1) * 8;
-                mma_ts_lo<kHi>(t_o, t_p + acol, v_lo + ((kk * 2048) >> 4), idesc_o, 1u);
+                mma_ts_lo<kHi>(t_o2, t_p + acol, v_lo + ((kk * 2048) >> 4), idesc_o,
+                               (part == 0 && kk == 0) ? 0u : 1u);
               }
             }
-            mma_commit(&o_done[b]);
+            mma_commit(&pv_done[b]);
             mma_commit(&empty_v[nV % NV]);
             ++nV;
             progressed = true;
           }
-          if (progressed) {
-            idle = 0;
-          } else if ((++idle & 63u) == 0) {
-            if (idle == 64) t0 = globaltimer();
-            if (*abort_flag || globaltimer() - t0 > CP_WAIT_TIMEOUT_NS) {
-              ok = false;
-              break;
-            }
-          }
+          if (!idle_tick(progressed)) { ok = false; break; }
         }
       }
       if (!ok) record_timeout(a.status, abort_flag);
-      // every MMA issued so far completes before TMEM is released
-      mma_commit(fin);
-      mbar_wait_timeout(fin, 0, CP_WAIT_TIMEOUT_NS);
+      // every MMA this thread issued completes before TMEM is released
+      uint64_t* my_fin = &fin[warp == 1 ? 0 : 1];
+      mma_commit(my_fin);
+      mbar_wait_timeout(my_fin, 0, CP_WAIT_TIMEOUT_NS);
     }
   } else if (warp < kPWarp0) {
     // ------------------------------------------------------------ state group
@@ -564,10 +616,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
       }
       for (int it = 0; it < n_it && ok; ++it) {
-        const int b = it % NB;
+        const int b = it % NSB;
         uint8_t* sbuf = s_tile + b * L::kSBufBytes;
-        // the O MMA that last read this copy (tile it - NB) has completed
-        if (it >= NB && !mbar_wait(&o_done[b], ((it - NB) / NB) & 1, abort_flag)) {
+        // the Q S that last read this copy (tile it - NSB) has completed
+        if (it >= NSB && !mbar_wait(&qs_done[b], ((it - NSB) / NSB) & 1, abort_flag)) {
           ok = false;
           break;
         }
@@ -617,8 +669,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // per 32-bit column.
     bool ok = true;
     for (int it = 0; !AGG_ONLY && it < n_it && ok; ++it) {
-      const int b = it % NB;
-      if (!mbar_wait(&p_done[b], (it / NB) & 1, abort_flag)) { ok = false; break; }
+      const int b = it % NP;
+      if (!mbar_wait(&p_done[b], (it / NP) & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
       const uint32_t pc = lane_base + L::kColP + b * 128;
 #pragma unroll 1
@@ -643,9 +695,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int o_tid = threadIdx.x - 32 * kOWarp0;   // 0..kOThreads-1
     bool ok = true;
     for (int it = 0; !AGG_ONLY && it < n_it && ok; ++it) {
-      const int b = it % NB;
       uint8_t* ob = o_tile + (it % L::kOBufs) * L::kOBytes;
-      if (!mbar_wait(&o_done[b], (it / NB) & 1, abort_flag)) { ok = false; break; }
+      if (!mbar_wait(o1_done, it & 1, abort_flag) ||
+          !mbar_wait(&pv_done[it % NP], (it / NP) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       // the store that last read this staging buffer has finished reading it
       if (o_tid == 0) {
@@ -655,16 +710,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_store_wait_read_all();
       }
       named_barrier_sync(1, kOThreads);
-#pragma unroll
+      // O = O1 (+ its lo half when wide) + O2
+#pragma unroll 1
       for (int c = 0; c < MB / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(lane_base + L::kColO + b * MB + c * 32, r);
+        uint32_t r[32], u[32];
+        tmem_ld32(lane_base + L::kColO1 + c * 32, r);
+        tmem_ld32(lane_base + L::kColO2 + c * 32, u);
         tmem_ld_wait();
+#pragma unroll
+        for (int x = 0; x < 32; ++x)
+          r[x] = __float_as_uint(__uint_as_float(r[x]) + __uint_as_float(u[x]));
+        if (L::kWide) {
+          tmem_ld32(lane_base + L::kColO1 + MB + c * 32, u);
+          tmem_ld_wait();
+#pragma unroll
+          for (int x = 0; x < 32; ++x)
+            r[x] = __float_as_uint(__uint_as_float(r[x]) + __uint_as_float(u[x]));
+        }
         store_chunk32(ob, row, c * 32, kBoxBytes, r);
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&o_free[b]);
+      if (lane == 0) mbar_arrive(o_free);
       fence_proxy_async_smem();
       named_barrier_sync(1, kOThreads);
       if (o_tid == 0) {
