@@ -42,16 +42,17 @@ using namespace cp::ptx;
 constexpr int kTile = 128;             // rows per tile = MMA M
 constexpr int kBoxCols = 64;           // bf16 columns per TMA box (128 bytes)
 constexpr int kBoxBytes = kTile * 128; // one [128 x 64] bf16 box
-// Warp roles: 0 TMA producer, 1 and 14 MMA issuers (the issuing thread's
-// instruction rate, not the tensor pipe, bounds a single issuer), then three
-// converter groups that each own one lane quarter of TMEM per warp.
-// Fifteen warps keep every sub-partition at four warps or fewer, which
-// leaves 128 registers per thread.
+// Warp roles: 0 TMA producer; 1, 14 and 15 MMA issuers (the issuing
+// thread's instruction rate, not the tensor pipe, bounds a single issuer);
+// three converter groups that each own one lane quarter of TMEM per warp.
+// Sixteen warps keep every sub-partition at four warps, which leaves 128
+// registers per thread.
 constexpr int kSWarp0 = 2, kSWarps = 4;    // state: fp32 S -> bf16 hi/lo operand copy
 constexpr int kPWarp0 = 6, kPWarps = 4;    // P: mask, split hi/lo, pack in TMEM
 constexpr int kOWarp0 = 10, kOWarps = 4;   // O: fp32 -> bf16 -> TMA store
-constexpr int kBWarp = 14;                 // second MMA issuer (P and P V)
-constexpr int kThreads = 32 * (kBWarp + 1);
+constexpr int kBWarp = 14;                 // MMA issuer of P
+constexpr int kCWarp = 15;                 // MMA issuer of P V
+constexpr int kThreads = 32 * (kCWarp + 1);
 constexpr int kOThreads = 32 * kOWarps;
 constexpr int kSmemLimit = 232448;     // 227 KB opt-in dynamic shared memory
 
@@ -253,16 +254,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* full_v = empty_qk + NQK;        // [NV]
   uint64_t* empty_v = full_v + NV;          // [NV]
   uint64_t* p_done = empty_v + NV;          // [NP] issuer B -> P group: P(t) in TMEM
-  uint64_t* p_ready = p_done + NP;          // [NP] P group -> B: masked bf16 P (hi|lo) packed
-  uint64_t* pv_done = p_ready + NP;         // [NP] B -> O group, B: O2(t) final, P buffer free
+  uint64_t* p_ready = p_done + NP;          // [NP] P group -> C: masked bf16 P (hi|lo) packed
+  uint64_t* pv_done = p_ready + NP;         // [NP] C -> O group, B: O2(t) final, P buffer free
   uint64_t* qs_done = pv_done + NP;         // [NSB] A -> S group: Q S(t) done, state copy free
   uint64_t* o1_done = qs_done + NSB;        // A -> O group: O1(t) final
-  uint64_t* o_free = o1_done + 1;           // O group -> A, B: O1 and O2 of tile t read out
+  uint64_t* o_free = o1_done + 1;           // O group -> A, C: O1 and O2 of tile t read out
   uint64_t* s_done = o_free + 1;            // A -> S group: state updated with tile t
   uint64_t* s_ready = s_done + 1;           // S group -> A: bf16 state copy written, S read
-  uint64_t* fin = s_done + 2;               // [2] issuer drains before TMEM release
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(s_done + 4);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(s_done + 5);
+  uint64_t* fin = s_done + 2;               // [3] issuer drains before TMEM release
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(s_done + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(s_done + 6);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -285,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     // a stage is released by both issuers (A: S / Q S, B: P / P V); in the
     // aggregate-only mode issuer A alone consumes the rings
-    const uint32_t kRel = AGG_ONLY ? 1 : 2;
+    const uint32_t kRel = AGG_ONLY ? 1 : 2;  // A + B for Q/K, A + C for V
     for (int i = 0; i < NQK; ++i) {
       mbar_init(&full_qk[i], 1);
       mbar_init(&empty_qk[i], kRel);
@@ -306,6 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(s_ready, kSWarps);
     mbar_init(&fin[0], 1);
     mbar_init(&fin[1], 1);
+    mbar_init(&fin[2], 1);
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -388,13 +390,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait_timeout(&full_v[j % NV], (j / NV) & 1, CP_WAIT_TIMEOUT_NS);
       }
     }
-  } else if (warp == 1 || warp == kBWarp) {
+  } else if (warp == 1 || warp == kBWarp || warp == kCWarp) {
     // ------------------------------------------------------------ MMA issuers
     // Issuer A (warp 1): the state chain S(t) and the inter-tile read-out
-    // Q S(t) into O1.  Issuer B (warp kBWarp): P(t) = Q K^T and the
-    // intra-tile P V(t) into O2.  The two never touch the same accumulator,
-    // so they need no ordering between them; a ring stage is released by a
-    // commit from each.
+    // Q S(t) into O1.  Issuer B (warp kBWarp): P(t) = Q K^T.  Issuer C (warp
+    // kCWarp): the intra-tile P V(t) into O2.  Q S and P V never touch the
+    // same accumulator, so the issuers need no ordering between them beyond
+    // the barriers on P; a ring stage is released by a commit from each of
+    // its two users.
     if (lane == 0 && (warp == 1 || !AGG_ONLY)) {
       constexpr uint32_t idesc_p = idesc_bf16_f32(128, 128, 0, 0);   // Q . K^T
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, MB, 1, 1);    // K^T . V
@@ -498,60 +501,60 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!idle_tick(progressed)) { ok = false; break; }
         }
-      } else {
+      } else if (warp == kBWarp) {
         // issuer B: P(t) needs Q/K(t) landed and P buffer t%NP free (P V of
-        // tile t - NP completed); P V(t) needs P(t) packed, V(t) landed and O2
-        // read out for t - 1.  P runs at most NP - 1 tiles ahead of P V.
-        int nP = 0, nV = 0;
-        while (nV < n_it) {
-          bool progressed = false;
-          if (nP < n_it && nP <= nV + NP - 1 &&
-              mbar_test_wait(&full_qk[nP % NQK], (nP / NQK) & 1) &&
-              (nP < NP || mbar_test_wait(&pv_done[nP % NP], ((nP - NP) / NP) & 1))) {
-            tc_fence_after();
-            const uint32_t q_lo = desc_lo(qk_addr(nP), 16);
-            const uint32_t k_lo = desc_lo(qk_addr(nP) + L::kQBytes, 16);
-            const uint32_t t_p = tmem + L::kColP + (nP % NP) * 128;
-#pragma unroll
-            for (int kk = 0; kk < DP / 16; ++kk) {
-              const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-              mma_ss_lo<kHi, kHi>(t_p, q_lo + off, k_lo + off, idesc_p, kk > 0);
-            }
-            mma_commit(&p_done[nP % NP]);
-            mma_commit(&empty_qk[nP % NQK]);
-            ++nP;
-            progressed = true;
+        // tile t - NP completed)
+        for (int it = 0; it < n_it; ++it) {
+          if (!mbar_wait(&full_qk[it % NQK], (it / NQK) & 1, abort_flag) ||
+              (it >= NP && !mbar_wait(&pv_done[it % NP], ((it - NP) / NP) & 1, abort_flag))) {
+            ok = false;
+            break;
           }
-          if (nV < nP && mbar_test_wait(&p_ready[nV % NP], (nV / NP) & 1) &&
-              mbar_test_wait(&full_v[nV % NV], (nV / NV) & 1) &&
-              (nV == 0 || mbar_test_wait(o_free, (nV - 1) & 1))) {
-            tc_fence_after();
-            const int b = nV % NP;
-            const uint32_t t_p = tmem + L::kColP + b * 128;
-            const uint32_t v_lo = desc_lo(v_addr(nV), kBoxBytes);
-            // O2 = P_hi V + P_lo V (A = packed bf16 P in TMEM, B = V MN-major).
-            // Chunk c of P (columns 32c..32c+31) holds hi in its first 16
-            // TMEM columns and lo in the next 16, two j per column.
+          tc_fence_after();
+          const uint32_t q_lo = desc_lo(qk_addr(it), 16);
+          const uint32_t k_lo = desc_lo(qk_addr(it) + L::kQBytes, 16);
+          const uint32_t t_p = tmem + L::kColP + (it % NP) * 128;
 #pragma unroll
-            for (int part = 0; part < 2; ++part) {
-#pragma unroll
-              for (int kk = 0; kk < kTile / 16; ++kk) {
-                const uint32_t acol = (kk >> 1) * 32 + part * 16 + (kk & 1) * 8;
-                mma_ts_lo<kHi>(t_o2, t_p + acol, v_lo + ((kk * 2048) >> 4), idesc_o,
-                               (part == 0 && kk == 0) ? 0u : 1u);
-              }
-            }
-            mma_commit(&pv_done[b]);
-            mma_commit(&empty_v[nV % NV]);
-            ++nV;
-            progressed = true;
+          for (int kk = 0; kk < DP / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+            mma_ss_lo<kHi, kHi>(t_p, q_lo + off, k_lo + off, idesc_p, kk > 0);
           }
-          if (!idle_tick(progressed)) { ok = false; break; }
+          mma_commit(&p_done[it % NP]);
+          mma_commit(&empty_qk[it % NQK]);
+        }
+      } else {
+        // issuer C: P V(t) needs P(t) packed, V(t) landed and O2 read out
+        // for t - 1
+        for (int it = 0; it < n_it; ++it) {
+          const int b = it % NP;
+          if (!mbar_wait(&p_ready[b], (it / NP) & 1, abort_flag) ||
+              !mbar_wait(&full_v[it % NV], (it / NV) & 1, abort_flag) ||
+              (it > 0 && !mbar_wait(o_free, (it - 1) & 1, abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t t_p = tmem + L::kColP + b * 128;
+          const uint32_t v_lo = desc_lo(v_addr(it), kBoxBytes);
+          // O2 = P_hi V + P_lo V (A = packed bf16 P in TMEM, B = V MN-major).
+          // Chunk c of P (columns 32c..32c+31) holds hi in its first 16
+          // TMEM columns and lo in the next 16, two j per column.
+#pragma unroll
+          for (int part = 0; part < 2; ++part) {
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk) {
+              const uint32_t acol = (kk >> 1) * 32 + part * 16 + (kk & 1) * 8;
+              mma_ts_lo<kHi>(t_o2, t_p + acol, v_lo + ((kk * 2048) >> 4), idesc_o,
+                             (part == 0 && kk == 0) ? 0u : 1u);
+            }
+          }
+          mma_commit(&pv_done[b]);
+          mma_commit(&empty_v[it % NV]);
         }
       }
       if (!ok) record_timeout(a.status, abort_flag);
       // every MMA this thread issued completes before TMEM is released
-      uint64_t* my_fin = &fin[warp == 1 ? 0 : 1];
+      uint64_t* my_fin = &fin[warp == 1 ? 0 : (warp == kBWarp ? 1 : 2)];
       mma_commit(my_fin);
       mbar_wait_timeout(my_fin, 0, CP_WAIT_TIMEOUT_NS);
     }
