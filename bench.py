@@ -40,7 +40,10 @@ UNIT = "Mtok·head/s"
 # DRAM traffic of one launch of the tensor-core kernel measured by ncu
 # (dram__bytes_read.sum + dram__bytes_write.sum) together with the SHA-256 of
 # the kernel source it was measured on; a changed source reports null.
-PROFILED_TRAFFIC = {"source_sha256": None, "bytes_per_launch": None}
+PROFILED_TRAFFIC = {
+    "source_sha256": "8a8a1aa2c768bd353ab7155f915b769d1a0112fa706a8eca1ee728e8e1079f43",
+    "bytes_per_launch": 211614720,  # 201.39 MB read + 10.23 MB written (forward launch)
+}
 
 
 def _env_int(name, default):
@@ -93,7 +96,12 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    """nvidia-smi sampling (every 5 ms) of SM clocks and throttle reasons.
+
+    Each output line is stamped with the host time it arrives; summary()
+    keeps the samples inside [t0, t1] (the timed region) and falls back to
+    the surrounding loaded window when the region is shorter than a few
+    sampling periods."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -102,46 +110,60 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line))
 
     def __enter__(self):
+        import threading
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "5"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._reader, daemon=True)
+            self.thread.start()
         except (OSError, ValueError):
             self.proc = None
         return self
 
     def __exit__(self, *exc):
-        self.out = ""
         if self.proc is not None:
             self.proc.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                self.out, _ = self.proc.communicate()
+            if self.thread is not None:
+                self.thread.join(timeout=5)
 
-    def summary(self):
-        rows = []
-        for r in csv.reader(io.StringIO(self.out or "")):
-            if len(r) < 9:
-                continue
-            try:
-                rows.append([x.strip() for x in r])
-            except Exception:
-                continue
+    def summary(self, t0: float, t1: float, loaded_from: float):
+        def parse(window):
+            rows = []
+            for ts, line in self.lines:
+                if not (window[0] <= ts <= window[1]):
+                    continue
+                r = [x.strip() for x in next(csv.reader(io.StringIO(line)), [])]
+                if len(r) >= 9:
+                    rows.append(r)
+            return rows
+        rows, window = parse((t0, t1 + 0.005)), "timed region"
+        if len(rows) < 3:
+            rows, window = parse((loaded_from, t1 + 0.005)), "timed region + loaded soak before it"
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        num = lambda x: x.replace(".", "", 1).isdigit()
+        sm = [float(r[1]) for r in rows if num(r[1])]
+        smax = [float(r[2]) for r in rows if num(r[2])]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4)
                           if r[5 + i].lower().startswith("active")})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(rows), "window": window}
 
 
 def kernel_sha():
@@ -273,7 +295,13 @@ def run_ours(args, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
-        time.sleep(0.3)  # let the sampler start
+        # keep the GPU loaded for ~0.3 s so the sampler runs and clocks settle
+        soak_from = time.time()
+        while time.time() - soak_from < 0.3:
+            step()
+            torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        t_start = time.time()
         for e0, e1, e2 in ev:
             e0.record(stream)
             cp.causal_product_fwd(qd, kd, vd, out=out, workspace=ws_f, stream=stream)
@@ -281,6 +309,7 @@ def run_ours(args, world, rank, local):
             cp.causal_product_bwd(qd, kd, vd, gd, dq, dk, dv, workspace=ws_b, stream=stream)
             e2.record(stream)
         torch.cuda.synchronize()
+        t_end = time.time()
     barrier(world)
     total_ms = ev[0][0].elapsed_time(ev[-1][2])
     fwd_ms = sum(a.elapsed_time(b) for a, b, _ in ev)
@@ -354,7 +383,7 @@ def run_ours(args, world, rank, local):
                      "peak_source": f"{peak_src} hbm_gbs",
                      "bytes_per_launch": bytes_per_launch, "avg_launch_ms": avg_launch_ms},
         "gpu_launches": launches_per_step * args.steps,
-        "clocks": clocks.summary(),
+        "clocks": clocks.summary(t_start, t_end, soak_from),
         "e2e": e2e,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
