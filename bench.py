@@ -269,9 +269,9 @@ def run_ours(args, world, rank, local):
     qd, kd, vd, gd = (t.to(dev) for t in (q, k, v, g))
     out = torch.empty_like(vd)
     dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
-    ws_f = torch.empty(cp.causal_product_workspace_size(w.B, w.H, w.N, w.D, w.M, w.torch_dtype,
+    ws_f = torch.zeros(cp.causal_product_workspace_size(w.B, w.H, w.N, w.D, w.M, w.torch_dtype,
                                                         False), dtype=torch.uint8, device=dev)
-    ws_b = torch.empty(cp.causal_product_workspace_size(w.B, w.H, w.N, w.D, w.M, w.torch_dtype,
+    ws_b = torch.zeros(cp.causal_product_workspace_size(w.B, w.H, w.N, w.D, w.M, w.torch_dtype,
                                                         True), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 

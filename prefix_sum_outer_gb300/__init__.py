@@ -122,7 +122,8 @@ def causal_product_workspace_size(B: int, H: int, N: int, D: int, M: int,
 
 
 def _workspace(nbytes: int, device) -> torch.Tensor:
-    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    # the status word at its start must begin at zero (it is sticky)
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
 
 def causal_product_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,

@@ -122,7 +122,10 @@ cp_status_t causal_product_fwd(const void* q, const void* k, const void* v, void
   if (st != CP_OK) return st;
   int* status = static_cast<int*>(s.base);
   float* agg = reinterpret_cast<float*>(static_cast<char*>(s.base) + cp::kStatusBytes);
-  if (cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess) return CP_ERR_CUDA;
+  // a fresh allocation starts with a clear status word; a caller's workspace
+  // keeps its (sticky) status until causal_product_status() reads it
+  if (s.owned && cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess)
+    return CP_ERR_CUDA;
   cp::Product p{q, k, v, out, BH, N, D, M, false};
   return cp::run_product(p, dtype, agg, status, stream);
 }
@@ -159,7 +162,10 @@ cp_status_t causal_product_bwd(const void* q, const void* k, const void* v, cons
   if (st != CP_OK) return st;
   int* status = static_cast<int*>(s.base);
   float* agg = reinterpret_cast<float*>(static_cast<char*>(s.base) + cp::kStatusBytes);
-  if (cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess) return CP_ERR_CUDA;
+  // a fresh allocation starts with a clear status word; a caller's workspace
+  // keeps its (sticky) status until causal_product_status() reads it
+  if (s.owned && cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess)
+    return CP_ERR_CUDA;
   // dq_i = sum_{j<=i} (g_i . v_j) k_j
   cp::Product pq{grad_out, v, k, grad_q, BH, N, M, D, false};
   // dv_j = sum_{i>=j} (k_j . q_i) g_i
@@ -251,6 +257,9 @@ extern "C" cp_status_t causal_product_fwd_noalloc(const void* q, const void* k, 
   void* scratch = nullptr;
   st = cp::noalloc_scratch(&scratch);
   if (st != CP_OK) return st;
+  // the shared array keeps the previous call's contents: clear its status word
+  if (cudaMemsetAsync(scratch, 0, sizeof(int), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return CP_ERR_CUDA;
   // With a caller-style workspace the forward entry point allocates nothing.
   return causal_product_fwd(q, k, v, out, B, H, N, D, M, dtype, scratch,
                             CP_NOALLOC_SCRATCH_BYTES, stream);

@@ -26,6 +26,7 @@
 // from the fixed-order sum of its predecessors' aggregates (a two-pass scan
 // across segments, deterministic).
 #include <algorithm>
+#include <atomic>
 #include <cstdio>
 #include <mutex>
 
@@ -791,9 +792,17 @@ cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
                        const CUtensorMap& o, const Args& a, unsigned grid, cudaStream_t st) {
   using L = Layout<DP, MB>;
   auto kern = tc_causal_kernel<DP, MB, AGG>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+  // the shared-memory opt-in is set once per device for each instantiation
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if ((configured.load(std::memory_order_acquire) & bit) == 0) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_release);
+  }
   kern<<<grid, kThreads, L::kSmemBytes, st>>>(q, k, v, o, a);
   return cudaGetLastError();
 }
