@@ -60,6 +60,14 @@
 #include <stddef.h>
 #include <stdint.h>
 
+/* The library is built with hidden visibility; only these entry points are
+ * exported. */
+#if defined(__GNUC__)
+#define CP_API __attribute__((visibility("default")))
+#else
+#define CP_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -86,25 +94,25 @@ typedef enum {
  * causal_product_bwd (backward = 1) needs for this problem; always >= 256
  * (the status word), a multiple of 256.  Pure host computation.  Returns 0
  * for arguments the entry points would reject. */
-size_t causal_product_workspace_size(int64_t B, int64_t H, int64_t N, int64_t D, int64_t M,
-                                     cp_dtype_t dtype, int backward);
+CP_API size_t causal_product_workspace_size(int64_t B, int64_t H, int64_t N, int64_t D, int64_t M,
+                                            cp_dtype_t dtype, int backward);
 
 /* Forward: out[b,h,i,:] = sum_{j<=i} (q[b,h,i,:] . k[b,h,j,:]) v[b,h,j,:].
  * `stream` is a cudaStream_t passed as void*. */
-cp_status_t causal_product_fwd(const void* q, const void* k, const void* v, void* out,
-                               int64_t B, int64_t H, int64_t N, int64_t D, int64_t M,
-                               cp_dtype_t dtype, void* workspace, size_t workspace_bytes,
-                               void* stream);
+CP_API cp_status_t causal_product_fwd(const void* q, const void* k, const void* v, void* out,
+                                      int64_t B, int64_t H, int64_t N, int64_t D, int64_t M,
+                                      cp_dtype_t dtype, void* workspace, size_t workspace_bytes,
+                                      void* stream);
 
 /* Backward: given grad_out = dL/dout, writes grad_q, grad_k, grad_v (the
  * formulas in the header comment).  Three causal products: dq is the
  * forward product of (grad_out, v, k); dv and dk are reverse-order products
  * of (k, q, grad_out) and (v, grad_out, q). */
-cp_status_t causal_product_bwd(const void* q, const void* k, const void* v, const void* grad_out,
-                               void* grad_q, void* grad_k, void* grad_v,
-                               int64_t B, int64_t H, int64_t N, int64_t D, int64_t M,
-                               cp_dtype_t dtype, void* workspace, size_t workspace_bytes,
-                               void* stream);
+CP_API cp_status_t causal_product_bwd(const void* q, const void* k, const void* v, const void* grad_out,
+                                      void* grad_q, void* grad_k, void* grad_v,
+                                      int64_t B, int64_t H, int64_t N, int64_t D, int64_t M,
+                                      cp_dtype_t dtype, void* workspace, size_t workspace_bytes,
+                                      void* stream);
 
 /* Size of the static device scratch array behind causal_product_fwd_noalloc. */
 #define CP_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
@@ -128,17 +136,17 @@ cp_status_t causal_product_bwd(const void* q, const void* k, const void* v, cons
  * every call and keeps the last call's contents: the call clears the status
  * word on `stream` before its kernels run, and calls that overlap on the GPU
  * (different streams, no ordering between them) race on it. */
-cp_status_t causal_product_fwd_noalloc(const void* q, const void* k, const void* v, void* out,
-                                       int64_t B, int64_t H, int64_t N, int64_t D, int64_t M,
-                                       cp_dtype_t dtype, void* stream);
+CP_API cp_status_t causal_product_fwd_noalloc(const void* q, const void* k, const void* v, void* out,
+                                              int64_t B, int64_t H, int64_t N, int64_t D, int64_t M,
+                                              cp_dtype_t dtype, void* stream);
 
 /* Synchronises `stream`, then returns and clears the status word in
  * `workspace` (CP_OK or CP_ERR_TIMEOUT), or CP_ERR_CUDA if the stream
  * reports an error. */
-cp_status_t causal_product_status(void* workspace, void* stream);
+CP_API cp_status_t causal_product_status(void* workspace, void* stream);
 
 /* Static, human-readable name of a status code. */
-const char* causal_product_error_string(cp_status_t status);
+CP_API const char* causal_product_error_string(cp_status_t status);
 
 #ifdef __cplusplus
 }

@@ -33,7 +33,10 @@ def _nvcc() -> str:
 
 
 def _flags():
+    # hidden visibility (and no GNU-unique objects) keeps every internal symbol,
+    # including function-local statics, private to this copy of the library
     return ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+                   "-Xcompiler", "-fvisibility=hidden", "-Xcompiler", "-fno-gnu-unique",
                    "-I", os.path.join(ROOT, "include"), "--expt-relaxed-constexpr"]
 
 
