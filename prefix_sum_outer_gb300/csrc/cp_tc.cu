@@ -14,11 +14,18 @@
 // Q_t S.  P is masked and rounded to bf16 on its way from TMEM to shared
 // memory.
 //
-// CTA = 6 warps:
-//   warp 0       TMA producer: Q/K/V tiles into an NS-deep ring
-//   warp 1       TMEM allocator and single-thread MMA issuer
-//   warps 2..5   epilogue (one thread per TMEM lane = tile row): state and
-//                P conversion, output conversion and TMA store
+// CTA = 16 warps:
+//   warp 0        TMA producer: Q/K tiles and V tiles into two rings
+//   warp 1        TMEM allocator; MMA issuer of the state chain S and of Q S
+//   warps 2..5    state group: fp32 S -> bf16 hi/lo operand copy
+//   warps 6..9    P group: mask P, split into bf16 hi/lo, pack in TMEM
+//   warps 10..13  O group: fp32 O -> bf16, TMA store
+//   warps 14, 15  MMA issuers of P and of P V
+// (the converter groups run one thread per TMEM lane = tile row)
+//
+// Kernels are launched as programmatic dependents: the set-up (barriers,
+// TMEM allocation, descriptor prefetch) overlaps the previous kernel in the
+// stream, and no global memory is touched before it has completed.
 //
 // Long sequences with few problems are split into G segments per problem;
 // a first launch of the same kernel in aggregate-only mode writes each
@@ -284,6 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       !AGG_ONLY && a.agg_in != nullptr && (a.reverse ? (seg < a.G - 1) : (seg > 0));
   auto tile_of = [&](int it) { return a.reverse ? (t_end - 1 - it) : (t_first + it); };
 
+  grid_dep_launch_dependents();
   if (threadIdx.x == 0) {
     // a stage is released by both issuers (A: S / Q S, B: P / P V); in the
     // aggregate-only mode issuer A alone consumes the rings
@@ -328,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  grid_dep_wait();  // inputs written by the previous kernel are visible from here
   const uint32_t tmem = *tmem_holder;
   const int wq = warp & 3;                 // TMEM lane quarter of this warp
   const int row = wq * 32 + lane;          // tile row = TMEM lane
@@ -706,36 +715,65 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      // the store that last read this staging buffer has finished reading it
-      if (o_tid == 0) {
-        if (L::kOBufs == 2)
-          asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-        else
-          tma_store_wait_read_all();
-      }
-      named_barrier_sync(1, kOThreads);
+      auto wait_staging = [&]() {
+        // the store that last read this staging buffer has finished reading it
+        if (o_tid == 0) {
+          if (L::kOBufs == 2)
+            asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+          else
+            tma_store_wait_read_all();
+        }
+        named_barrier_sync(1, kOThreads);
+      };
       // O = O1 (+ its lo half when wide) + O2
-#pragma unroll 1
-      for (int c = 0; c < MB / 32; ++c) {
-        uint32_t r[32], u[32];
-        tmem_ld32(lane_base + L::kColO1 + c * 32, r);
-        tmem_ld32(lane_base + L::kColO2 + c * 32, u);
-        tmem_ld_wait();
+      if constexpr (MB <= 64) {
+        // the whole row fits in registers: release the accumulators before
+        // converting and storing
+        uint32_t r[MB / 32][32];
 #pragma unroll
-        for (int x = 0; x < 32; ++x)
-          r[x] = __float_as_uint(__uint_as_float(r[x]) + __uint_as_float(u[x]));
-        if (L::kWide) {
-          tmem_ld32(lane_base + L::kColO1 + MB + c * 32, u);
+        for (int c = 0; c < MB / 32; ++c) {
+          uint32_t u[32], w[32];
+          tmem_ld32(lane_base + L::kColO1 + c * 32, r[c]);
+          tmem_ld32(lane_base + L::kColO2 + c * 32, u);
+          if (L::kWide) tmem_ld32(lane_base + L::kColO1 + MB + c * 32, w);
+          tmem_ld_wait();
+#pragma unroll
+          for (int x = 0; x < 32; ++x) {
+            float f = __uint_as_float(r[c][x]) + __uint_as_float(u[x]);
+            if (L::kWide) f += __uint_as_float(w[x]);
+            r[c][x] = __float_as_uint(f);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(o_free);
+        wait_staging();
+#pragma unroll
+        for (int c = 0; c < MB / 32; ++c) store_chunk32(ob, row, c * 32, kBoxBytes, r[c]);
+      } else {
+        wait_staging();
+#pragma unroll 1
+        for (int c = 0; c < MB / 32; ++c) {
+          uint32_t r[32], u[32];
+          tmem_ld32(lane_base + L::kColO1 + c * 32, r);
+          tmem_ld32(lane_base + L::kColO2 + c * 32, u);
           tmem_ld_wait();
 #pragma unroll
           for (int x = 0; x < 32; ++x)
             r[x] = __float_as_uint(__uint_as_float(r[x]) + __uint_as_float(u[x]));
+          if (L::kWide) {
+            tmem_ld32(lane_base + L::kColO1 + MB + c * 32, u);
+            tmem_ld_wait();
+#pragma unroll
+            for (int x = 0; x < 32; ++x)
+              r[x] = __float_as_uint(__uint_as_float(r[x]) + __uint_as_float(u[x]));
+          }
+          store_chunk32(ob, row, c * 32, kBoxBytes, r);
         }
-        store_chunk32(ob, row, c * 32, kBoxBytes, r);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(o_free);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(o_free);
       fence_proxy_async_smem();
       named_barrier_sync(1, kOThreads);
       if (o_tid == 0) {
@@ -803,8 +841,17 @@ cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_release);
   }
-  kern<<<grid, kThreads, L::kSmemBytes, st>>>(q, k, v, o, a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = L::kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, q, k, v, o, a);
 }
 
 template <int DP, int MB>
