@@ -63,5 +63,15 @@ struct TcPlan {
 TcPlan tc_plan(int64_t BH, int64_t N, int64_t D, int64_t M);
 cp_status_t tc_launch(const Product& p, const TcPlan& plan, float* agg, int* status,
                       cudaStream_t stream);
+// Only pass 1 of the two-pass scan (a no-op when plan.G == 1).
+cp_status_t tc_aggregate(const Product& p, const TcPlan& plan, float* agg, int* status,
+                         cudaStream_t stream);
+
+// Fused dk and dv of the backward pass (both reverse-order products share
+// the state sum q g^T), for D, M <= 64; `plan` is tc_plan(BH, N, D, M).
+bool tc_dkdv_supported(const TcPlan& plan);
+cp_status_t tc_dkdv_launch(const void* q, const void* k, const void* v, const void* g, void* dk,
+                           void* dv, int64_t BH, int64_t N, int64_t D, int64_t M,
+                           const TcPlan& plan, float* agg, int* status, cudaStream_t stream);
 
 }  // namespace cp

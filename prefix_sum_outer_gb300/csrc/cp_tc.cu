@@ -37,19 +37,14 @@
 #include <cstdio>
 #include <mutex>
 
-#include <cudaTypedefs.h>
-
 #include "cp_internal.h"
-#include "sm103_ptx.cuh"
+#include "cp_tc_common.cuh"
 
 namespace cp {
 namespace tc {
 
 using namespace cp::ptx;
 
-constexpr int kTile = 128;             // rows per tile = MMA M
-constexpr int kBoxCols = 64;           // bf16 columns per TMA box (128 bytes)
-constexpr int kBoxBytes = kTile * 128; // one [128 x 64] bf16 box
 // Warp roles: 0 TMA producer; 1, 14 and 15 MMA issuers (the issuing
 // thread's instruction rate, not the tensor pipe, bounds a single issuer);
 // three converter groups that each own one lane quarter of TMEM per warp.
@@ -61,8 +56,10 @@ constexpr int kOWarp0 = 10, kOWarps = 4;   // O: fp32 -> bf16 -> TMA store
 constexpr int kBWarp = 14;                 // MMA issuer of P
 constexpr int kCWarp = 15;                 // MMA issuer of P V
 constexpr int kThreads = 32 * (kCWarp + 1);
+static_assert(kPWarp0 == kSWarp0 + kSWarps && kOWarp0 == kPWarp0 + kPWarps &&
+                  kBWarp == kOWarp0 + kOWarps,
+              "converter groups of consecutive warps, one per TMEM lane quarter");
 constexpr int kOThreads = 32 * kOWarps;
-constexpr int kSmemLimit = 232448;     // 227 KB opt-in dynamic shared memory
 
 struct Args {
   int64_t N;
@@ -139,104 +136,6 @@ struct Layout {
   static_assert(DP % 64 == 0 && MB % 64 == 0, "64-column boxes");
   static_assert(!kWide || kSplit, "the wide Q S chain reads S_hi and S_lo side by side");
 };
-
-// Byte offset of element (row, col) inside a [rows x 64k] bf16 tile stored
-// as 64-column boxes of `box_stride` bytes with the 128-byte swizzle (the
-// layout TMA writes and tcgen05 descriptors read): 16-byte chunk index
-// XOR row % 8.
-__device__ __forceinline__ uint32_t sw128_offset(int row, int col, int box_stride) {
-  const int box = col >> 6;
-  const int chunk = (col & 63) >> 3;
-  return box * box_stride + row * 128 + ((chunk ^ (row & 7)) << 4) + ((col & 7) << 1);
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-// Convert 32 fp32 values (columns col0..col0+31 of `row`) to bf16 and store
-// them into a swizzled tile; col0 must be a multiple of 32.
-__device__ __forceinline__ void store_chunk32(uint8_t* tile, int row, int col0, int box_stride,
-                                              const uint32_t (&r)[32]) {
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    uint4 w;
-    w.x = pack_bf16x2(__uint_as_float(r[8 * c + 0]), __uint_as_float(r[8 * c + 1]));
-    w.y = pack_bf16x2(__uint_as_float(r[8 * c + 2]), __uint_as_float(r[8 * c + 3]));
-    w.z = pack_bf16x2(__uint_as_float(r[8 * c + 4]), __uint_as_float(r[8 * c + 5]));
-    w.w = pack_bf16x2(__uint_as_float(r[8 * c + 6]), __uint_as_float(r[8 * c + 7]));
-    *reinterpret_cast<uint4*>(tile + sw128_offset(row, col0 + 8 * c, box_stride)) = w;
-  }
-}
-
-// Split 32 fp32 values into hi = bf16(x) and lo = bf16(x - hi) and store
-// both (hi into `hi_tile`, lo into `lo_tile`, same swizzled layout).
-__device__ __forceinline__ void store_chunk32_split(uint8_t* hi_tile, uint8_t* lo_tile, int row,
-                                                    int col0, int box_stride,
-                                                    const uint32_t (&r)[32]) {
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    uint32_t h[4], l[4];
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {
-      const float a = __uint_as_float(r[8 * c + 2 * x]);
-      const float b = __uint_as_float(r[8 * c + 2 * x + 1]);
-      h[x] = pack_bf16x2(a, b);
-      const float ah = __uint_as_float(h[x] << 16);
-      const float bh = __uint_as_float(h[x] & 0xffff0000u);
-      l[x] = pack_bf16x2(a - ah, b - bh);
-    }
-    const uint32_t off = sw128_offset(row, col0 + 8 * c, box_stride);
-    *reinterpret_cast<uint4*>(hi_tile + off) = make_uint4(h[0], h[1], h[2], h[3]);
-    *reinterpret_cast<uint4*>(lo_tile + off) = make_uint4(l[0], l[1], l[2], l[3]);
-  }
-}
-
-__device__ __forceinline__ void store_zero32(uint8_t* tile, int row, int col0, int box_stride) {
-#pragma unroll
-  for (int c = 0; c < 4; ++c)
-    *reinterpret_cast<uint4*>(tile + sw128_offset(row, col0 + 8 * c, box_stride)) =
-        make_uint4(0, 0, 0, 0);
-}
-
-// In place: mask a 32-column chunk of P to the causal triangle (only the
-// diagonal chunk needs it; an entirely masked chunk becomes zero), split
-// each value into bf16 hi + lo and pack: columns 0..15 <- hi pairs,
-// columns 16..31 <- lo pairs.
-__device__ __forceinline__ void split_pack_p(uint32_t (&r)[32], bool zero, bool diag, int lane,
-                                             int reverse) {
-  if (zero) {
-#pragma unroll
-    for (int x = 0; x < 32; ++x) r[x] = 0u;
-    return;
-  }
-  if (diag) {
-#pragma unroll
-    for (int x = 0; x < 32; ++x) {
-      const bool keep = reverse ? (x >= lane) : (x <= lane);
-      if (!keep) r[x] = 0u;
-    }
-  }
-  // hi of pair x goes to r[x] (already consumed), lo waits in a 16-entry
-  // temporary until the pairs it would overwrite are consumed
-  uint32_t lo[16];
-#pragma unroll
-  for (int x = 0; x < 16; ++x) {
-    const float a0 = __uint_as_float(r[2 * x]), a1 = __uint_as_float(r[2 * x + 1]);
-    const uint32_t h = pack_bf16x2(a0, a1);
-    lo[x] = pack_bf16x2(a0 - __uint_as_float(h << 16), a1 - __uint_as_float(h & 0xffff0000u));
-    r[x] = h;
-  }
-#pragma unroll
-  for (int x = 0; x < 16; ++x) r[16 + x] = lo[x];
-}
-
-__device__ __forceinline__ void record_timeout(int* status, volatile int* abort_flag) {
-  *abort_flag = 1;
-  if (status != nullptr) atomicCAS(status, 0, (int)CP_ERR_TIMEOUT);
-}
 
 template <int DP, int MB, bool AGG_ONLY>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -797,34 +696,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ host
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-// [BH][N][cols] bf16, boxes of 64 columns x 128 rows x 1 problem, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* ptr, int64_t BH, int64_t N, int64_t cols) {
-  auto enc = get_encode();
-  if (enc == nullptr) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)N, (cuuint64_t)BH};
-  cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)(N * cols * 2)};
-  cuuint32_t box[3] = {(cuuint32_t)kBoxCols, (cuuint32_t)kTile, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 template <int DP, int MB, bool AGG>
 cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                        const CUtensorMap& o, const Args& a, unsigned grid, cudaStream_t st) {
@@ -857,15 +728,17 @@ cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
 template <int DP, int MB>
 cudaError_t launch_pair(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                         const CUtensorMap& o, Args a, const TcPlan& plan, int64_t problems,
-                        float* agg, cudaStream_t st) {
+                        float* agg, bool agg_only, cudaStream_t st) {
   cudaError_t e = cudaSuccess;
   if (plan.G > 1) {
     Args b = a;
     b.agg_in = nullptr;
     b.agg_out = agg;
     e = launch_one<DP, MB, true>(q, k, v, o, b, (unsigned)(problems * (plan.G - 1)), st);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess || agg_only) return e;
     a.agg_in = agg;
+  } else if (agg_only) {
+    return cudaSuccess;
   }
   return launch_one<DP, MB, false>(q, k, v, o, a, (unsigned)(problems * plan.G), st);
 }
@@ -896,8 +769,9 @@ TcPlan tc_plan(int64_t BH, int64_t N, int64_t D, int64_t M) {
   return p;
 }
 
-cp_status_t tc_launch(const Product& p, const TcPlan& plan, float* agg, int* status,
-                      cudaStream_t stream) {
+namespace {
+cp_status_t tc_run(const Product& p, const TcPlan& plan, float* agg, int* status,
+                   cudaStream_t stream, bool agg_only) {
   if (!plan.ok) return CP_ERR_UNSUPPORTED_SHAPE;
   CUtensorMap mq, mk, mv, mo;
   if (!tc::make_map(&mq, p.q, p.BH, p.N, p.D) || !tc::make_map(&mk, p.k, p.BH, p.N, p.D) ||
@@ -916,7 +790,8 @@ cp_status_t tc_launch(const Product& p, const TcPlan& plan, float* agg, int* sta
   cudaError_t e;
 #define CP_TC_CASE(DP_, MB_)                                                                  \
   if (plan.DP == DP_ && plan.MB == MB_)                                                       \
-    e = tc::launch_pair<DP_, MB_>(mq, mk, mv, mo, a, plan, problems, agg, stream);            \
+    e = tc::launch_pair<DP_, MB_>(mq, mk, mv, mo, a, plan, problems, agg, agg_only,  \
+                                   stream);            \
   else
   CP_TC_CASE(64, 64)
   CP_TC_CASE(64, 128)
@@ -927,6 +802,18 @@ cp_status_t tc_launch(const Product& p, const TcPlan& plan, float* agg, int* sta
   return CP_ERR_UNSUPPORTED_SHAPE;
 #undef CP_TC_CASE
   return e == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+}
+
+}  // namespace
+
+cp_status_t tc_launch(const Product& p, const TcPlan& plan, float* agg, int* status,
+                      cudaStream_t stream) {
+  return tc_run(p, plan, agg, status, stream, false);
+}
+
+cp_status_t tc_aggregate(const Product& p, const TcPlan& plan, float* agg, int* status,
+                         cudaStream_t stream) {
+  return tc_run(p, plan, agg, status, stream, true);
 }
 
 }  // namespace cp

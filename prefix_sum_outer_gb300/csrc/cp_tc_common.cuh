@@ -1,0 +1,149 @@
+// Pieces shared by the tensor-core kernels: tile geometry, the 128-byte
+// swizzled tile layout, bf16 conversion and hi/lo splitting, the in-TMEM
+// packing of the intra-tile matrix P, timeout reporting and TMA maps.
+#pragma once
+#include <cstdint>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "cp_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace cp {
+namespace tc {
+
+constexpr int kTile = 128;             // rows per tile = MMA M
+constexpr int kBoxCols = 64;           // bf16 columns per TMA box (128 bytes)
+constexpr int kBoxBytes = kTile * 128; // one [128 x 64] bf16 box
+constexpr int kSmemLimit = 232448;     // 227 KB opt-in dynamic shared memory
+
+// Byte offset of element (row, col) inside a [rows x 64k] bf16 tile stored
+// as 64-column boxes of `box_stride` bytes with the 128-byte swizzle (the
+// layout TMA writes and tcgen05 descriptors read): 16-byte chunk index
+// XOR row % 8.
+__device__ __forceinline__ uint32_t sw128_offset(int row, int col, int box_stride) {
+  const int box = col >> 6;
+  const int chunk = (col & 63) >> 3;
+  return box * box_stride + row * 128 + ((chunk ^ (row & 7)) << 4) + ((col & 7) << 1);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Convert 32 fp32 values (columns col0..col0+31 of `row`) to bf16 and store
+// them into a swizzled tile; col0 must be a multiple of 32.
+__device__ __forceinline__ void store_chunk32(uint8_t* tile, int row, int col0, int box_stride,
+                                              const uint32_t (&r)[32]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint4 w;
+    w.x = pack_bf16x2(__uint_as_float(r[8 * c + 0]), __uint_as_float(r[8 * c + 1]));
+    w.y = pack_bf16x2(__uint_as_float(r[8 * c + 2]), __uint_as_float(r[8 * c + 3]));
+    w.z = pack_bf16x2(__uint_as_float(r[8 * c + 4]), __uint_as_float(r[8 * c + 5]));
+    w.w = pack_bf16x2(__uint_as_float(r[8 * c + 6]), __uint_as_float(r[8 * c + 7]));
+    *reinterpret_cast<uint4*>(tile + sw128_offset(row, col0 + 8 * c, box_stride)) = w;
+  }
+}
+
+// Split 32 fp32 values into hi = bf16(x) and lo = bf16(x - hi) and store
+// both (hi into `hi_tile`, lo into `lo_tile`, same swizzled layout).
+__device__ __forceinline__ void store_chunk32_split(uint8_t* hi_tile, uint8_t* lo_tile, int row,
+                                                    int col0, int box_stride,
+                                                    const uint32_t (&r)[32]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const float a = __uint_as_float(r[8 * c + 2 * x]);
+      const float b = __uint_as_float(r[8 * c + 2 * x + 1]);
+      h[x] = pack_bf16x2(a, b);
+      const float ah = __uint_as_float(h[x] << 16);
+      const float bh = __uint_as_float(h[x] & 0xffff0000u);
+      l[x] = pack_bf16x2(a - ah, b - bh);
+    }
+    const uint32_t off = sw128_offset(row, col0 + 8 * c, box_stride);
+    *reinterpret_cast<uint4*>(hi_tile + off) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(lo_tile + off) = make_uint4(l[0], l[1], l[2], l[3]);
+  }
+}
+
+__device__ __forceinline__ void store_zero32(uint8_t* tile, int row, int col0, int box_stride) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    *reinterpret_cast<uint4*>(tile + sw128_offset(row, col0 + 8 * c, box_stride)) =
+        make_uint4(0, 0, 0, 0);
+}
+
+// In place: mask a 32-column chunk of P to the causal triangle (only the
+// diagonal chunk needs it; an entirely masked chunk becomes zero), split
+// each value into bf16 hi + lo and pack: columns 0..15 <- hi pairs,
+// columns 16..31 <- lo pairs.
+__device__ __forceinline__ void split_pack_p(uint32_t (&r)[32], bool zero, bool diag, int lane,
+                                             int reverse) {
+  if (zero) {
+#pragma unroll
+    for (int x = 0; x < 32; ++x) r[x] = 0u;
+    return;
+  }
+  if (diag) {
+#pragma unroll
+    for (int x = 0; x < 32; ++x) {
+      const bool keep = reverse ? (x >= lane) : (x <= lane);
+      if (!keep) r[x] = 0u;
+    }
+  }
+  // hi of pair x goes to r[x] (already consumed), lo waits in a 16-entry
+  // temporary until the pairs it would overwrite are consumed
+  uint32_t lo[16];
+#pragma unroll
+  for (int x = 0; x < 16; ++x) {
+    const float a0 = __uint_as_float(r[2 * x]), a1 = __uint_as_float(r[2 * x + 1]);
+    const uint32_t h = pack_bf16x2(a0, a1);
+    lo[x] = pack_bf16x2(a0 - __uint_as_float(h << 16), a1 - __uint_as_float(h & 0xffff0000u));
+    r[x] = h;
+  }
+#pragma unroll
+  for (int x = 0; x < 16; ++x) r[16 + x] = lo[x];
+}
+
+__device__ __forceinline__ void record_timeout(int* status, volatile int* abort_flag) {
+  *abort_flag = 1;
+  if (status != nullptr) atomicCAS(status, 0, (int)CP_ERR_TIMEOUT);
+}
+
+// ------------------------------------------------------------------ host
+inline PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// [BH][N][cols] bf16, boxes of 64 columns x 128 rows x 1 problem, 128-byte swizzle.
+inline bool make_map(CUtensorMap* m, const void* ptr, int64_t BH, int64_t N, int64_t cols) {
+  auto enc = get_encode();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)(N * cols * 2)};
+  cuuint32_t box[3] = {(cuuint32_t)kBoxCols, (cuuint32_t)kTile, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace tc
+}  // namespace cp
