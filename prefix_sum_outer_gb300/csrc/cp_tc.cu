@@ -445,11 +445,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t t_p = tmem + L::kColP + b * 128;
           const uint32_t v_lo = desc_lo(v_addr(it), kBoxBytes);
-          // O2 = P_hi V + P_lo V (A = packed bf16 P in TMEM, B = V MN-major).
-          // Chunk c of P (columns 32c..32c+31) holds hi in its first 16
-          // TMEM columns and lo in the next 16, two j per column.
+          // O2 = P_hi V (+ P_lo V) (A = packed bf16 P in TMEM, B = V
+          // MN-major).  Chunk c of P (columns 32c..32c+31) holds hi in its
+          // first 16 TMEM columns and lo in the next 16, two j per column.
 #pragma unroll
-          for (int part = 0; part < 2; ++part) {
+          for (int part = 0; part < kPParts; ++part) {
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk) {
               const uint32_t acol = (kk >> 1) * 32 + part * 16 + (kk & 1) * 8;
@@ -594,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait();
         }
         split_pack_p(r, z, c == wq, lane, a.reverse);
-        tmem_st32(pc + 32 * c, r);
+        store_packed_p(pc + 32 * c, r);
       }
       tmem_st_wait();
       tc_fence_before();

@@ -79,9 +79,14 @@ __device__ __forceinline__ void store_zero32(uint8_t* tile, int row, int col0, i
         make_uint4(0, 0, 0, 0);
 }
 
-// In place: mask a 32-column chunk of P to the causal triangle (only the
-// diagonal chunk needs it; an entirely masked chunk becomes zero), split
-// each value into bf16 hi + lo and pack: columns 0..15 <- hi pairs,
+// P = Q K^T is rounded to bf16 for the P V product either once (hi) or as
+// hi + lo (lo = bf16(P - hi)), which doubles the P V MMAs.
+constexpr bool kSplitP = true;
+constexpr int kPParts = kSplitP ? 2 : 1;
+
+// In place: mask a 32-column chunk of P to the causal triangle of the tile
+// (only the diagonal chunk needs it; an entirely masked chunk becomes zero)
+// and round to bf16 pairs: columns 0..15 <- hi pairs, and with the split
 // columns 16..31 <- lo pairs.
 __device__ __forceinline__ void split_pack_p(uint32_t (&r)[32], bool zero, bool diag, int lane,
                                              int reverse) {
@@ -104,11 +109,22 @@ __device__ __forceinline__ void split_pack_p(uint32_t (&r)[32], bool zero, bool 
   for (int x = 0; x < 16; ++x) {
     const float a0 = __uint_as_float(r[2 * x]), a1 = __uint_as_float(r[2 * x + 1]);
     const uint32_t h = pack_bf16x2(a0, a1);
-    lo[x] = pack_bf16x2(a0 - __uint_as_float(h << 16), a1 - __uint_as_float(h & 0xffff0000u));
+    if (kSplitP)
+      lo[x] = pack_bf16x2(a0 - __uint_as_float(h << 16), a1 - __uint_as_float(h & 0xffff0000u));
     r[x] = h;
   }
+  if (kSplitP) {
 #pragma unroll
-  for (int x = 0; x < 16; ++x) r[16 + x] = lo[x];
+    for (int x = 0; x < 16; ++x) r[16 + x] = lo[x];
+  }
+}
+
+// Store a packed chunk back to its TMEM columns (16 or 32 of them).
+__device__ __forceinline__ void store_packed_p(uint32_t taddr, const uint32_t (&r)[32]) {
+  if (kSplitP)
+    cp::ptx::tmem_st32(taddr, r);
+  else
+    cp::ptx::tmem_st16(taddr, r);
 }
 
 __device__ __forceinline__ void record_timeout(int* status, volatile int* abort_flag) {

@@ -20,15 +20,15 @@
 //
 // CTA = 16 warps:
 //   warp 0        TMA producer: Q, K, V, G tiles into a 3-stage ring
-//   warp 1        TMEM allocator; MMA issuer of R += Q^T G, K R and V R^T
+//   warp 1        TMEM allocator; MMA issuer of R += Q^T G
 //   warps 2..5    state copy (fp32 R -> bf16 hi/lo) and packing of P2
 //   warps 6..9    packing of P1 (mask, split into bf16 hi/lo, in TMEM)
-//   warps 10..13  dV and dK: fp32 -> bf16 -> global memory
-//   warps 14, 15  MMA issuers of P1, P1 G and of P2, P2 Q
-// The inter-tile term (K R, from warp 1) and the intra-tile term (P G, from
-// warp 14 or 15) accumulate into the same TMEM columns: the intra-tile MMAs
-// are issued only after the inter-tile ones have completed, so the order
-// of the sums is fixed.
+//   warps 10..13  dV and dK: fp32 -> bf16, staged in the stage's K and V
+//                 boxes (no longer read once the output is final), TMA store
+//   warp 14       MMA issuer of dV: P1, then K R and P1 G into one accumulator
+//   warp 15       MMA issuer of dK: P2, then V R^T and P2 Q
+// Each output's inter- and intra-tile terms come from one thread, so they
+// accumulate in issue order.
 #include <algorithm>
 #include <atomic>
 
@@ -72,8 +72,6 @@ struct DkdvArgs {
   int BH;
   int D, M;
   const float* agg_in;  // [BH][G][64][64] per-segment sums of q g^T; null when G == 1
-  uint16_t* dk;         // [BH][N][D] bf16
-  uint16_t* dv;         // [BH][N][M] bf16
   int* status;
 };
 
@@ -89,30 +87,16 @@ __device__ __forceinline__ void pack_p_reverse(uint32_t pc, int wq, int lane) {
       tmem_ld_wait();
     }
     split_pack_p(r, z, c == wq, lane, 1);
-    tmem_st32(pc + 32 * c, r);
+    store_packed_p(pc + 32 * c, r);
   }
   tmem_st_wait();
-}
-
-// Convert one 64-column fp32 row to bf16 and write its first `cols` columns.
-__device__ __forceinline__ void store_row(uint16_t* dst, int cols, const uint32_t (&r)[2][32]) {
-#pragma unroll
-  for (int c8 = 0; c8 < 8; ++c8) {
-    if (c8 * 8 >= cols) break;
-    const uint32_t* x = &r[c8 >> 2][(c8 & 3) * 8];
-    uint4 w;
-    w.x = pack_bf16x2(__uint_as_float(x[0]), __uint_as_float(x[1]));
-    w.y = pack_bf16x2(__uint_as_float(x[2]), __uint_as_float(x[3]));
-    w.z = pack_bf16x2(__uint_as_float(x[4]), __uint_as_float(x[5]));
-    w.w = pack_bf16x2(__uint_as_float(x[6]), __uint_as_float(x[7]));
-    *reinterpret_cast<uint4*>(dst + c8 * 8) = w;
-  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
-                   const DkdvArgs a) {
+                   const __grid_constant__ CUtensorMap tm_dk,
+                   const __grid_constant__ CUtensorMap tm_dv, const DkdvArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -120,16 +104,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* s_tile = ring + kNS * kStageBytes;        // [kNSB] x (hi | lo) bf16 copies of R
   uint64_t* bars = reinterpret_cast<uint64_t*>(s_tile + kNSB * kSBufBytes);
   uint64_t* full = bars;                    // [kNS] TMA -> issuers
-  uint64_t* empty = full + kNS;             // [kNS] issuers (3) -> TMA
-  uint64_t* p_done = empty + kNS;           // [2] issuer 1/2 -> packers: P in TMEM
-  uint64_t* p_ready = p_done + 2;           // [2] packers -> issuer 1/2: P packed
-  uint64_t* inter_done = p_ready + 2;       // [2] state issuer -> issuer 1/2: K R / V R^T done
-  uint64_t* o_done = inter_done + 2;        // [2] issuer 1/2 -> output group: dV / dK final
-  uint64_t* o_free = o_done + 2;            // [2] output group -> state issuer: read out
-  uint64_t* qs_done = o_free + 2;           // [kNSB] state issuer -> state group: copy free
+  uint64_t* empty = full + kNS;             // [kNS] state issuer + output group -> TMA
+  uint64_t* p_done = empty + kNS;           // [2] issuer x -> packers: P in TMEM
+  uint64_t* p_ready = p_done + 2;           // [2] packers -> issuer x: P packed
+  uint64_t* o_done = p_ready + 2;           // [2] issuer x -> output group, issuer x: output final
+  uint64_t* o_free = o_done + 2;            // [2] output group -> issuer x: read out
+  uint64_t* copy_ready = o_free + 2;        // [kNSB] state group -> issuers: copy of R written
+  uint64_t* qs_done = copy_ready + kNSB;    // [kNSB] issuers 1, 2 -> state group: copy read
   uint64_t* s_done = qs_done + kNSB;        // state issuer -> state group: R updated
-  uint64_t* s_ready = s_done + 1;           // state group -> state issuer: R copied
-  uint64_t* fin = s_ready + 1;              // [3]
+  uint64_t* fin = s_done + 1;               // [3]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(fin + 3);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(fin + 4);
 
@@ -148,18 +131,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNS; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 3);
+      mbar_init(&empty[i], 2);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&p_done[x], 1);
       mbar_init(&p_ready[x], 4);
-      mbar_init(&inter_done[x], 1);
       mbar_init(&o_done[x], 1);
       mbar_init(&o_free[x], 4);
     }
-    for (int i = 0; i < kNSB; ++i) mbar_init(&qs_done[i], 1);
+    for (int i = 0; i < kNSB; ++i) {
+      mbar_init(&copy_ready[i], 4);
+      mbar_init(&qs_done[i], 2);
+    }
     mbar_init(s_done, 1);
-    mbar_init(s_ready, 4);
     for (int i = 0; i < 3; ++i) mbar_init(&fin[i], 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -170,6 +154,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_g);
+    tma_prefetch_desc(&tm_dk);
+    tma_prefetch_desc(&tm_dv);
   }
   if (warp == 1) {
     tmem_alloc(tmem_holder, kColsAlloc);
@@ -214,83 +200,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ state issuer
-    // R(t) update needs tile t landed and R copied out (s_ready); K R(t)
-    // needs the update issued (so the copy is written) and the dV
-    // accumulator read out for t - 1; V R^T(t) likewise for dK.
+    // R(t) update needs tile t landed and R copied out for tile t.
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, kW, 1, 1);   // Q^T . G
-      constexpr uint32_t idesc_r = idesc_bf16_f32(128, kW, 0, 1);   // K . R   (R MN-major)
-      constexpr uint32_t idesc_rt = idesc_bf16_f32(128, kW, 0, 0);  // V . R^T (R K-major)
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, kW, 1, 1);  // Q^T . G
       const uint32_t t_s = tmem + kColS;
-      const uint32_t s_addr = smem_u32(s_tile);
       bool ok = true;
-      int nS = 0, n1 = 0, n2 = 0;
-      uint64_t t0 = globaltimer();
-      uint32_t idle = 0;
-      while (n2 < n_it) {
-        bool progressed = false;
-        if (nS < n_it && mbar_test_wait(&full[nS % kNS], (nS / kNS) & 1) &&
-            mbar_test_wait(s_ready, nS & 1)) {
-          tc_fence_after();
-          // R += Q^T G (A = Q^T, B = G, both MN-major)
-          const uint32_t base = stage_addr(nS);
-          const uint32_t qt_lo = desc_lo(base, kBoxBytes);
-          const uint32_t g_lo = desc_lo(base + 3 * kBoxBytes, kBoxBytes);
-          const bool fresh = (nS == 0) && !has_prefix;
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ss_lo<kHi, kHi>(t_s, qt_lo + ((kk * 2048) >> 4), g_lo + ((kk * 2048) >> 4), idesc_s,
-                                (fresh && kk == 0) ? 0u : 1u);
-          mma_commit(s_done);
-          ++nS;
-          progressed = true;
+      for (int it = 0; it < n_it; ++it) {
+        if (!mbar_wait(&full[it % kNS], (it / kNS) & 1, abort_flag) ||
+            !mbar_wait(&copy_ready[it % kNSB], (it / kNSB) & 1, abort_flag)) {
+          ok = false;
+          break;
         }
-        if (n1 < nS && (n1 == 0 || mbar_test_wait(&o_free[0], (n1 - 1) & 1))) {
-          tc_fence_after();
-          // dV = K R_hi + K R_lo
-          const uint32_t k_lo = desc_lo(stage_addr(n1) + kBoxBytes, 16);
-          const uint32_t s_lo = desc_lo(s_addr + (n1 % kNSB) * kSBufBytes, kW * 128);
+        tc_fence_after();
+        // R += Q^T G (A = Q^T, B = G, both MN-major)
+        const uint32_t base = stage_addr(it);
+        const uint32_t qt_lo = desc_lo(base, kBoxBytes);
+        const uint32_t g_lo = desc_lo(base + 3 * kBoxBytes, kBoxBytes);
+        const bool fresh = (it == 0) && !has_prefix;
 #pragma unroll
-          for (int part = 0; part < 2; ++part) {
-#pragma unroll
-            for (int kk = 0; kk < kW / 16; ++kk)
-              mma_ss_lo<kHi, kHi>(tmem + kColO1, k_lo + kk * 2,
-                                  s_lo + ((part * kSOneBytes + kk * 2048) >> 4), idesc_r,
-                                  (part == 0 && kk == 0) ? 0u : 1u);
-          }
-          mma_commit(&inter_done[0]);
-          ++n1;
-          progressed = true;
-        }
-        if (n2 < n1 && (n2 == 0 || mbar_test_wait(&o_free[1], (n2 - 1) & 1))) {
-          tc_fence_after();
-          // dK = V R_hi^T + V R_lo^T: the copy of R read K-major (row d of
-          // R is column d of R^T)
-          const uint32_t v_lo = desc_lo(stage_addr(n2) + 2 * kBoxBytes, 16);
-          const uint32_t rt_lo = desc_lo(s_addr + (n2 % kNSB) * kSBufBytes, 16);
-#pragma unroll
-          for (int part = 0; part < 2; ++part) {
-#pragma unroll
-            for (int kk = 0; kk < kW / 16; ++kk)
-              mma_ss_lo<kHi, kHi>(tmem + kColO2, v_lo + kk * 2,
-                                  rt_lo + ((part * kSOneBytes) >> 4) + kk * 2, idesc_rt,
-                                  (part == 0 && kk == 0) ? 0u : 1u);
-          }
-          mma_commit(&inter_done[1]);
-          mma_commit(&qs_done[n2 % kNSB]);
-          mma_commit(&empty[n2 % kNS]);
-          ++n2;
-          progressed = true;
-        }
-        if (progressed) {
-          idle = 0;
-        } else if ((++idle & 63u) == 0) {
-          if (idle == 64) t0 = globaltimer();
-          if (*abort_flag || globaltimer() - t0 > CP_WAIT_TIMEOUT_NS) {
-            ok = false;
-            break;
-          }
-        }
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ss_lo<kHi, kHi>(t_s, qt_lo + ((kk * 2048) >> 4), g_lo + ((kk * 2048) >> 4), idesc_s,
+                              (fresh && kk == 0) ? 0u : 1u);
+        mma_commit(s_done);
+        mma_commit(&empty[it % kNS]);
       }
       if (!ok) record_timeout(a.status, abort_flag);
       mma_commit(&fin[0]);
@@ -298,17 +230,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kI1Warp || warp == kI2Warp) {
     // ------------------------------------------------------------ product issuers
-    // x = 0: P1 = K Q^T, dV += P1 G;  x = 1: P2 = V G^T, dK += P2 Q.
-    // P(t) overwrites the buffer P(t - 1) was read from, so it waits for
-    // the intra-tile MMAs of t - 1; those wait for P(t) packed and for the
-    // inter-tile term of t, which they accumulate onto.
+    // x = 0: P1 = K Q^T, dV = K R + P1 G;  x = 1: P2 = V G^T, dK = V R^T + P2 Q.
+    // P(t) overwrites the buffer P(t - 1) was read from, so it waits for the
+    // output MMAs of t - 1; the inter-tile term waits for the copy of R and
+    // for the output group to have read the accumulator for t - 1.
     if (lane == 0) {
       const int x = warp == kI1Warp ? 0 : 1;
       constexpr uint32_t idesc_p = idesc_bf16_f32(128, 128, 0, 0);  // [K|V] . [Q|G]^T
-      constexpr uint32_t idesc_o = idesc_bf16_f32(128, kW, 0, 1);   // P . [G|Q]
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, kW, 0, 1);   // P . [G|Q], K . R
+      constexpr uint32_t idesc_ot = idesc_bf16_f32(128, kW, 0, 0);  // V . R^T (R K-major)
       const uint32_t t_p = tmem + (x == 0 ? kColP1 : kColP2);
       const uint32_t t_o = tmem + (x == 0 ? kColO1 : kColO2);
-      // operand boxes within a stage: A of P, B of P, B of P . X
+      const uint32_t s_addr = smem_u32(s_tile);
+      // operand boxes within a stage: A of P (and of the inter-tile term),
+      // B of P, B of P . X
       const uint32_t off_a = (x == 0 ? 1 : 2) * kBoxBytes;  // K or V
       const uint32_t off_b = (x == 0 ? 0 : 3) * kBoxBytes;  // Q or G
       const uint32_t off_x = (x == 0 ? 3 : 0) * kBoxBytes;  // G or Q
@@ -327,16 +262,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < kW / 16; ++kk)
           mma_ss_lo<kHi, kHi>(t_p, a_lo + kk * 2, b_lo + kk * 2, idesc_p, kk > 0 ? 1u : 0u);
         mma_commit(&p_done[x]);
-        if (!mbar_wait(&p_ready[x], it & 1, abort_flag) ||
-            !mbar_wait(&inter_done[x], it & 1, abort_flag)) {
+        if (!mbar_wait(&copy_ready[it % kNSB], (it / kNSB) & 1, abort_flag) ||
+            (it > 0 && !mbar_wait(&o_free[x], (it - 1) & 1, abort_flag))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        // out += P_hi X + P_lo X (A = packed P in TMEM, B = X MN-major)
-        const uint32_t x_lo = desc_lo(base + off_x, kBoxBytes);
+        // inter-tile term from the hi and lo copies of R: K R (R MN-major)
+        // or V R^T (R read K-major: row d of R is column d of R^T)
+        const uint32_t s_buf = s_addr + (it % kNSB) * kSBufBytes;
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
+#pragma unroll
+          for (int kk = 0; kk < kW / 16; ++kk) {
+            const uint32_t acc = (part == 0 && kk == 0) ? 0u : 1u;
+            if (x == 0)
+              mma_ss_lo<kHi, kHi>(t_o, a_lo + kk * 2,
+                                  desc_lo(s_buf + part * kSOneBytes, kW * 128) + ((kk * 2048) >> 4),
+                                  idesc_o, acc);
+            else
+              mma_ss_lo<kHi, kHi>(t_o, a_lo + kk * 2,
+                                  desc_lo(s_buf + part * kSOneBytes, 16) + kk * 2, idesc_ot, acc);
+          }
+        }
+        mma_commit(&qs_done[it % kNSB]);
+        if (!mbar_wait(&p_ready[x], it & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // out += P_hi X (+ P_lo X) (A = packed P in TMEM, B = X MN-major)
+        const uint32_t x_lo = desc_lo(base + off_x, kBoxBytes);
+#pragma unroll
+        for (int part = 0; part < kPParts; ++part) {
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
             const uint32_t acol = (kk >> 1) * 32 + part * 16 + (kk & 1) * 8;
@@ -344,7 +302,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         mma_commit(&o_done[x]);
-        mma_commit(&empty[it % kNS]);
       }
       if (!ok) record_timeout(a.status, abort_flag);
       mma_commit(&fin[1 + x]);
@@ -414,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(s_ready);
+        if (lane == 0) mbar_arrive(&copy_ready[ns % kNSB]);
         ++ns;
         progressed = true;
       }
@@ -457,9 +414,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) record_timeout(a.status, abort_flag);
   } else if (warp < kI1Warp) {
     // ------------------------------------------------------------ output group
+    // dV(t) is staged in the K box of tile t's stage and dK(t) in its V box:
+    // once an output is final, every MMA that read that box has completed.
+    // The stage is released after both stores have read it.
+    const int o_tid = threadIdx.x - 32 * kOWarp0;
     bool ok = true;
     for (int it = 0; it < n_it && ok; ++it) {
-      const int64_t grow = (int64_t)tile_of(it) * kTile + row;
+      const int st = it % kNS;
+      const int row0 = tile_of(it) * kTile;
       for (int x = 0; x < 2; ++x) {
         if (!mbar_wait(&o_done[x], it & 1, abort_flag)) {
           ok = false;
@@ -473,14 +435,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&o_free[x]);
-        if (grow < a.N) {
-          const int cols = x == 0 ? a.M : a.D;
-          uint16_t* dst = (x == 0 ? a.dv : a.dk) + ((int64_t)bh * a.N + grow) * cols;
-          store_row(dst, cols, r);
+        uint8_t* ob = ring + st * kStageBytes + (x == 0 ? 1 : 2) * kBoxBytes;
+        store_chunk32(ob, row, 0, kBoxBytes, r[0]);
+        store_chunk32(ob, row, 32, kBoxBytes, r[1]);
+        fence_proxy_async_smem();
+        named_barrier_sync(1, 128);
+        if (o_tid == 0) {
+          tma_store_3d(x == 0 ? &tm_dv : &tm_dk, ob, 0, row0, bh);
+          tma_store_commit();
         }
+      }
+      if (o_tid == 0 && ok) {
+        tma_store_wait_read_all();
+        mbar_arrive(&empty[st]);
       }
     }
     if (!ok) record_timeout(a.status, abort_flag);
+    if (o_tid == 0) tma_store_wait_all();
   }
 
   tc_fence_before();
@@ -510,9 +481,9 @@ cp_status_t tc_dkdv_launch(const void* q, const void* k, const void* v, const vo
     if (st != CP_OK) return st;
   }
   using namespace tc;
-  CUtensorMap mq, mk, mv, mg;
+  CUtensorMap mq, mk, mv, mg, mdk, mdv;
   if (!make_map(&mq, q, BH, N, D) || !make_map(&mk, k, BH, N, D) || !make_map(&mv, v, BH, N, M) ||
-      !make_map(&mg, g, BH, N, M))
+      !make_map(&mg, g, BH, N, M) || !make_map(&mdk, dk, BH, N, D) || !make_map(&mdv, dv, BH, N, M))
     return CP_ERR_UNSUPPORTED_SHAPE;
   DkdvArgs a{};
   a.N = N;
@@ -523,8 +494,6 @@ cp_status_t tc_dkdv_launch(const void* q, const void* k, const void* v, const vo
   a.D = (int)D;
   a.M = (int)M;
   a.agg_in = plan.G > 1 ? agg : nullptr;
-  a.dk = static_cast<uint16_t*>(dk);
-  a.dv = static_cast<uint16_t*>(dv);
   a.status = status;
   // the shared-memory opt-in is set once per device
   static std::atomic<uint64_t> configured{0};
@@ -548,7 +517,7 @@ cp_status_t tc_dkdv_launch(const void* q, const void* k, const void* v, const vo
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, tc_dkdv_kernel, mq, mk, mv, mg, a);
+  e = cudaLaunchKernelEx(&cfg, tc_dkdv_kernel, mq, mk, mv, mg, mdk, mdv, a);
   return e == cudaSuccess ? CP_OK : CP_ERR_CUDA;
 }
 
