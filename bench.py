@@ -44,6 +44,10 @@ PROFILED_TRAFFIC = {
     "source_sha256": "8a8a1aa2c768bd353ab7155f915b769d1a0112fa706a8eca1ee728e8e1079f43",
     "bytes_per_launch": 211614720,  # 201.39 MB read + 10.23 MB written (forward launch)
 }
+PROFILED_TRAFFIC_DKDV = {
+    "source_sha256": None,
+    "bytes_per_launch": None,
+}
 
 
 def _env_int(name, default):
@@ -166,9 +170,9 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows), "window": window}
 
 
-def kernel_sha():
+def kernel_sha(main="cp_tc.cu"):
     h = hashlib.sha256()
-    for f in ("cp_tc.cu", "sm103_ptx.cuh"):
+    for f in (main, "cp_tc_common.cuh", "sm103_ptx.cuh"):
         with open(os.path.join(ROOT, "prefix_sum_outer_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
@@ -280,8 +284,8 @@ def run_ours(args, world, rank, local):
         cp.causal_product_bwd(qd, kd, vd, gd, dq, dk, dv, workspace=ws_b, stream=stream)
 
     # kernels of ours launched per step (tensor-core path): forward 1 product,
-    # backward 3 products; a product split into segments adds one aggregate launch
-    from ctypes import c_int  # noqa: F401
+    # backward dq plus the fused dk/dv scan (or 2 more products); a scan split
+    # into segments adds one aggregate launch
     launches_per_step = _launches_per_step(w)
 
     for _ in range(max(args.warmup, 0)):
@@ -353,19 +357,37 @@ def run_ours(args, world, rank, local):
         e2e = {"value": w.token_heads * world * n_e2e / (e2e_ms / 1e3) / 1e6, "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e}
 
-    # ---- roofline of the dominant kernel (the tensor-core causal-product kernel)
+    # ---- roofline of the dominant kernel: the causal-product kernel, two
+    # launches per step (forward, and dq in the backward call); the forward
+    # call is exactly one launch of it, timed by its own events
     hbm_gbs, bf16_tf, peak_src = load_peaks()
     s = 2 if w.dtype == "bf16" else 4
-    # every launch is one causal product over (BH, N) with D' + D' + M' + M'
-    # columns moved per row (q', k', v' read, out' written); for D = M all
-    # four products of a step move the same bytes
+    fused = _fused_dkdv(w)
+    segmented = _segmented(w)
+    # one causal product over (BH, N) moves D' + D' + M' + M' columns per row
+    # (q', k', v' read, out' written)
     bytes_per_launch = s * (2 * w.D + 2 * w.M) * w.token_heads
-    n_products = 4
-    avg_launch_ms = (fwd_ms + bwd_ms) / (args.steps * n_products)
+    avg_launch_ms = fwd_ms / args.steps
     achieved = bytes_per_launch / (avg_launch_ms / 1e3) / 1e9
     traffic = None
-    if PROFILED_TRAFFIC["source_sha256"] == kernel_sha():
+    if not segmented and PROFILED_TRAFFIC["source_sha256"] == kernel_sha():
         traffic = PROFILED_TRAFFIC["bytes_per_launch"]
+    kernels = []
+    if fused and not segmented:
+        # the fused dk/dv launch reads q, k, v, g and writes dk, dv; its time
+        # is the backward call minus its causal-product launch (dq, the same
+        # bytes as the forward launch when D = M)
+        dkdv_bytes = s * (3 * w.D + 3 * w.M) * w.token_heads
+        dkdv_ms = (bwd_ms - fwd_ms) / args.steps
+        dkdv_traffic = None
+        if PROFILED_TRAFFIC_DKDV["source_sha256"] == kernel_sha("cp_tc_dkdv.cu"):
+            dkdv_traffic = PROFILED_TRAFFIC_DKDV["bytes_per_launch"]
+        kernels.append({"kernel": "tc_dkdv_kernel", "bound": "hbm",
+                        "bytes_per_launch": dkdv_bytes, "avg_launch_ms": dkdv_ms,
+                        "achieved": dkdv_bytes / (dkdv_ms / 1e3) / 1e9,
+                        "frac": dkdv_bytes / (dkdv_ms / 1e3) / 1e9 / hbm_gbs,
+                        "traffic": dkdv_traffic,
+                        "timing": "backward call minus one forward launch"})
     step_roofline_ms = algorithmic_bytes(w) / (hbm_gbs * 1e9) * 1e3
 
     line = {
@@ -381,7 +403,9 @@ def run_ours(args, world, rank, local):
                      "frac": achieved / hbm_gbs, "traffic": traffic,
                      "kernel": "tc_causal_kernel (one causal product per launch)",
                      "peak_source": f"{peak_src} hbm_gbs",
-                     "bytes_per_launch": bytes_per_launch, "avg_launch_ms": avg_launch_ms},
+                     "bytes_per_launch": bytes_per_launch, "avg_launch_ms": avg_launch_ms,
+                     "timing": "forward call: one launch, CUDA events on its stream",
+                     "other_kernels": kernels},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(t_start, t_end, soak_from),
         "e2e": e2e,
@@ -393,13 +417,25 @@ def run_ours(args, world, rank, local):
     return 0
 
 
-def _launches_per_step(w):
+def _segmented(w):
+    """True when the products are split into segments (an aggregate launch
+    precedes each scan launch): the workspace then holds more than the
+    256-byte status word."""
     import prefix_sum_outer_gb300 as cp
     lib = cp.load_library()
-    # a workspace larger than the status word means a segmented (two-launch) product
-    ws_fwd = lib.causal_product_workspace_size(w.B, w.H, w.N, w.D, w.M, 1, 0)
-    per_product = 2 if ws_fwd > 256 else 1
-    return 4 * per_product
+    return lib.causal_product_workspace_size(w.B, w.H, w.N, w.D, w.M, 1, 0) > 256
+
+
+def _fused_dkdv(w):
+    """bf16 with D, M <= 64: the backward computes dk and dv in one launch."""
+    return w.dtype == "bf16" and w.D <= 64 and w.M <= 64
+
+
+def _launches_per_step(w):
+    per_scan = 2 if _segmented(w) else 1
+    # forward: one product; backward: dq plus either the fused dk/dv scan
+    # or the dv and dk products
+    return per_scan * (1 + 1 + (1 if _fused_dkdv(w) else 2))
 
 
 def main(argv=None):
