@@ -179,7 +179,7 @@ cp_status_t causal_product_bwd(const void* q, const void* k, const void* v, cons
     const cp::TcPlan plan = cp::tc_plan(BH, N, D, M);
     if (cp::tc_dkdv_supported(plan))
       return cp::tc_dkdv_launch(q, k, v, grad_out, grad_k, grad_v, BH, N, D, M, plan, agg, status,
-                                stream);
+                                true, stream);
   }
   st = cp::run_product(pv, dtype, agg, status, stream);
   if (st == CP_OK) st = cp::run_product(pk, dtype, agg, status, stream);

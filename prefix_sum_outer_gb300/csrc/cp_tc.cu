@@ -25,7 +25,8 @@
 //
 // Kernels are launched as programmatic dependents: the set-up (barriers,
 // TMEM allocation, descriptor prefetch) overlaps the previous kernel in the
-// stream, and no global memory is touched before it has completed.
+// stream, and no global memory is touched before it has completed.  The
+// next kernel is allowed to start once every block has passed that wait.
 //
 // Long sequences with few problems are split into G segments per problem;
 // a first launch of the same kernel in aggregate-only mode writes each
@@ -190,7 +191,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       !AGG_ONLY && a.agg_in != nullptr && (a.reverse ? (seg < a.G - 1) : (seg > 0));
   auto tile_of = [&](int it) { return a.reverse ? (t_end - 1 - it) : (t_first + it); };
 
-  grid_dep_launch_dependents();
   if (threadIdx.x == 0) {
     // a stage is released by both issuers (A: S / Q S, B: P / P V); in the
     // aggregate-only mode issuer A alone consumes the rings
@@ -236,6 +236,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   grid_dep_wait();  // inputs written by the previous kernel are visible from here
+  // dependents start only once every block has passed the wait above, so
+  // for them every kernel before this one has completed
+  grid_dep_launch_dependents();
   const uint32_t tmem = *tmem_holder;
   const int wq = warp & 3;                 // TMEM lane quarter of this warp
   const int row = wq * 32 + lane;          // tile row = TMEM lane

@@ -53,9 +53,9 @@ static_assert(kSmemBytes <= kSmemLimit, "shared memory overflow");
 // TMEM columns
 constexpr int kColP1 = 0;
 constexpr int kColP2 = 128;
-constexpr int kColO1 = 256;  // dV accumulator (M columns)
-constexpr int kColO2 = 320;  // dK accumulator (D columns)
-constexpr int kColS = 384;   // state R (D lanes x M columns)
+constexpr int kColO1 = 256;  // dV accumulator, 2 x 64: [K R_hi + P1 G | K R_lo]
+constexpr int kColO2 = 384;  // dK accumulator (D columns)
+constexpr int kColS = 448;   // state R (D lanes x M columns)
 constexpr int kColsAlloc = 512;
 
 constexpr int kSWarp0 = 2, kPWarp0 = 6, kOWarp0 = 10;
@@ -71,6 +71,7 @@ struct DkdvArgs {
   int G;
   int BH;
   int D, M;
+  int overlap_prev;     // the previous kernel in the stream writes nothing this one reads
   const float* agg_in;  // [BH][G][64][64] per-segment sums of q g^T; null when G == 1
   int* status;
 };
@@ -164,7 +165,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  grid_dep_wait();  // inputs written by the previous kernel are visible from here
+  // inputs written by the previous kernel are visible from here (skipped when
+  // that kernel is the dq product of the same backward call: it reads the
+  // same inputs, writes only dq, and started after their writers finished)
+  if (!a.overlap_prev) grid_dep_wait();
   const uint32_t tmem = *tmem_holder;
   const int wq = warp & 3;                 // TMEM lane quarter of this warp
   const int row = wq * 32 + lane;          // tile row = TMEM lane
@@ -239,6 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_p = idesc_bf16_f32(128, 128, 0, 0);  // [K|V] . [Q|G]^T
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, kW, 0, 1);   // P . [G|Q], K . R
       constexpr uint32_t idesc_ot = idesc_bf16_f32(128, kW, 0, 0);  // V . R^T (R K-major)
+      constexpr uint32_t idesc_ow = idesc_bf16_f32(128, 2 * kW, 0, 1);  // K . [R_hi | R_lo]
       const uint32_t t_p = tmem + (x == 0 ? kColP1 : kColP2);
       const uint32_t t_o = tmem + (x == 0 ? kColO1 : kColO2);
       const uint32_t s_addr = smem_u32(s_tile);
@@ -268,21 +273,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        // inter-tile term from the hi and lo copies of R: K R (R MN-major)
-        // or V R^T (R read K-major: row d of R is column d of R^T)
+        // inter-tile term from the hi and lo copies of R.  dV: K [R_hi | R_lo]
+        // in one N = 128 chain (the copies sit side by side as one MN-major
+        // operand; the two halves are summed on read-out).  dK: V R_hi^T +
+        // V R_lo^T, R read K-major (row d of R is column d of R^T).
         const uint32_t s_buf = s_addr + (it % kNSB) * kSBufBytes;
+        if (x == 0) {
+          const uint32_t r_lo = desc_lo(s_buf, kSOneBytes);
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
+          for (int kk = 0; kk < kW / 16; ++kk)
+            mma_ss_lo<kHi, kHi>(t_o, a_lo + kk * 2, r_lo + ((kk * 2048) >> 4), idesc_ow,
+                                kk > 0 ? 1u : 0u);
+        } else {
 #pragma unroll
-          for (int kk = 0; kk < kW / 16; ++kk) {
-            const uint32_t acc = (part == 0 && kk == 0) ? 0u : 1u;
-            if (x == 0)
+          for (int part = 0; part < 2; ++part) {
+#pragma unroll
+            for (int kk = 0; kk < kW / 16; ++kk)
               mma_ss_lo<kHi, kHi>(t_o, a_lo + kk * 2,
-                                  desc_lo(s_buf + part * kSOneBytes, kW * 128) + ((kk * 2048) >> 4),
-                                  idesc_o, acc);
-            else
-              mma_ss_lo<kHi, kHi>(t_o, a_lo + kk * 2,
-                                  desc_lo(s_buf + part * kSOneBytes, 16) + kk * 2, idesc_ot, acc);
+                                  desc_lo(s_buf + part * kSOneBytes, 16) + kk * 2, idesc_ot,
+                                  (part == 0 && kk == 0) ? 0u : 1u);
           }
         }
         mma_commit(&qs_done[it % kNSB]);
@@ -432,6 +441,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(lane_base + (x == 0 ? kColO1 : kColO2), r[0]);
         tmem_ld32(lane_base + (x == 0 ? kColO1 : kColO2) + 32, r[1]);
         tmem_ld_wait();
+        if (x == 0) {
+          // add the K R_lo half
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t u[32];
+            tmem_ld32(lane_base + kColO1 + kW + c * 32, u);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              r[c][e] = __float_as_uint(__uint_as_float(r[c][e]) + __uint_as_float(u[e]));
+          }
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&o_free[x]);
@@ -460,6 +481,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kColsAlloc);
   }
+  // never complete before the previous kernel has (kernels after this one
+  // in the stream rely on that order)
+  if (a.overlap_prev) grid_dep_wait();
 }
 
 }  // namespace
@@ -471,7 +495,8 @@ bool tc_dkdv_supported(const TcPlan& plan) {
 
 cp_status_t tc_dkdv_launch(const void* q, const void* k, const void* v, const void* g, void* dk,
                            void* dv, int64_t BH, int64_t N, int64_t D, int64_t M,
-                           const TcPlan& plan, float* agg, int* status, cudaStream_t stream) {
+                           const TcPlan& plan, float* agg, int* status, bool after_dq,
+                           cudaStream_t stream) {
   if (!tc_dkdv_supported(plan)) return CP_ERR_UNSUPPORTED_SHAPE;
   if (plan.G > 1) {
     // per-segment sums of q g^T: the aggregate pass of the reverse product
@@ -494,6 +519,8 @@ cp_status_t tc_dkdv_launch(const void* q, const void* k, const void* v, const vo
   a.D = (int)D;
   a.M = (int)M;
   a.agg_in = plan.G > 1 ? agg : nullptr;
+  // with a single segment nothing is shared with the dq launch before it
+  a.overlap_prev = (after_dq && plan.G == 1) ? 1 : 0;
   a.status = status;
   // the shared-memory opt-in is set once per device
   static std::atomic<uint64_t> configured{0};
