@@ -172,15 +172,15 @@ cp_status_t causal_product_bwd(const void* q, const void* k, const void* v, cons
   cp::Product pv{k, q, grad_out, grad_v, BH, N, D, M, true};
   // dk_j = sum_{i>=j} (v_j . g_i) q_i
   cp::Product pk{v, grad_out, q, grad_k, BH, N, M, D, true};
-  st = cp::run_product(pq, dtype, agg, status, stream);
-  if (st != CP_OK) return st;
   if (dtype == CP_DTYPE_BF16) {
-    // dv and dk share the reverse state sum q g^T: one pass over q, k, v, g
+    // dv and dk share the reverse state sum q g^T: one scan over q, k, v, g
     const cp::TcPlan plan = cp::tc_plan(BH, N, D, M);
     if (cp::tc_dkdv_supported(plan))
-      return cp::tc_dkdv_launch(q, k, v, grad_out, grad_k, grad_v, BH, N, D, M, plan, agg, status,
-                                true, stream);
+      return cp::tc_bwd_launch(q, k, v, grad_out, grad_q, grad_k, grad_v, BH, N, D, M, plan, agg,
+                               status, stream);
   }
+  st = cp::run_product(pq, dtype, agg, status, stream);
+  if (st != CP_OK) return st;
   st = cp::run_product(pv, dtype, agg, status, stream);
   if (st == CP_OK) st = cp::run_product(pk, dtype, agg, status, stream);
   return st;

@@ -67,14 +67,12 @@ cp_status_t tc_launch(const Product& p, const TcPlan& plan, float* agg, int* sta
 cp_status_t tc_aggregate(const Product& p, const TcPlan& plan, float* agg, int* status,
                          cudaStream_t stream);
 
-// Fused dk and dv of the backward pass (both reverse-order products share
-// the state sum q g^T), for D, M <= 64; `plan` is tc_plan(BH, N, D, M).
+// Backward pass for bf16 with D, M <= 64 (tc_dkdv_supported(plan), plan =
+// tc_plan(BH, N, D, M)): dq is one product launch; dk and dv share the
+// reverse state sum q g^T and are computed in one scan.
 bool tc_dkdv_supported(const TcPlan& plan);
-// `after_dq`: the launch directly follows the dq product of the same call on
-// the same stream, which lets it start while that product still runs.
-cp_status_t tc_dkdv_launch(const void* q, const void* k, const void* v, const void* g, void* dk,
-                           void* dv, int64_t BH, int64_t N, int64_t D, int64_t M,
-                           const TcPlan& plan, float* agg, int* status, bool after_dq,
-                           cudaStream_t stream);
+cp_status_t tc_bwd_launch(const void* q, const void* k, const void* v, const void* g, void* dq,
+                          void* dk, void* dv, int64_t BH, int64_t N, int64_t D, int64_t M,
+                          const TcPlan& plan, float* agg, int* status, cudaStream_t stream);
 
 }  // namespace cp

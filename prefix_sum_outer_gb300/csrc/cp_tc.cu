@@ -1,142 +1,16 @@
-// bf16 causal product on the 5th-generation tensor cores (sm_103a).
-//
-// The recurrence "state += k v^T; out = state^T q" (triton-lang/triton issue
-// #217, the loop listing; the issue's opening comment calls it the prefix
-// sum of Algorithm 1 of "Transformers are RNNs") is regrouped into tiles of
-// 128 rows.  With S the fp32 D x M state before tile t:
-//     P   = Q_t K_t^T            masked to j <= i inside the tile (128x128)
-//     O_t = P V_t + Q_t S        (intra-tile part + inter-tile readout)
-//     S  += K_t^T V_t
-// All four are dense contractions and run as tcgen05.mma with bf16 operands
-// in shared memory and fp32 accumulators in tensor memory (TMEM).  The state
-// never leaves TMEM while a CTA walks its segment; a bf16 copy of it is
-// written to shared memory once per tile to serve as the MMA operand of
-// Q_t S.  P is masked and rounded to bf16 on its way from TMEM to shared
-// memory.
-//
-// CTA = 16 warps:
-//   warp 0        TMA producer: Q/K tiles and V tiles into two rings
-//   warp 1        TMEM allocator; MMA issuer of the state chain S and of Q S
-//   warps 2..5    state group: fp32 S -> bf16 hi/lo operand copy
-//   warps 6..9    P group: mask P, split into bf16 hi/lo, pack in TMEM
-//   warps 10..13  O group: fp32 O -> bf16, TMA store
-//   warps 14, 15  MMA issuers of P and of P V
-// (the converter groups run one thread per TMEM lane = tile row)
-//
-// Kernels are launched as programmatic dependents: the set-up (barriers,
-// TMEM allocation, descriptor prefetch) overlaps the previous kernel in the
-// stream, and no global memory is touched before it has completed.  The
-// next kernel is allowed to start once every block has passed that wait.
-//
-// Long sequences with few problems are split into G segments per problem;
-// a first launch of the same kernel in aggregate-only mode writes each
-// segment's sum of k v^T, and every segment of the second launch starts
-// from the fixed-order sum of its predecessors' aggregates (a two-pass scan
-// across segments, deterministic).
+// bf16 causal product on the 5th-generation tensor cores (sm_103a): the
+// product kernel (one CTA = causal_body of cp_tc_causal.cuh) and its host
+// side (tile plan, tensor maps, launches).
 #include <algorithm>
 #include <atomic>
 #include <cstdio>
 #include <mutex>
 
 #include "cp_internal.h"
-#include "cp_tc_common.cuh"
+#include "cp_tc_causal.cuh"
 
 namespace cp {
 namespace tc {
-
-using namespace cp::ptx;
-
-// Warp roles: 0 TMA producer; 1, 14 and 15 MMA issuers (the issuing
-// thread's instruction rate, not the tensor pipe, bounds a single issuer);
-// three converter groups that each own one lane quarter of TMEM per warp.
-// Sixteen warps keep every sub-partition at four warps, which leaves 128
-// registers per thread.
-constexpr int kSWarp0 = 2, kSWarps = 4;    // state: fp32 S -> bf16 hi/lo operand copy
-constexpr int kPWarp0 = 6, kPWarps = 4;    // P: mask, split hi/lo, pack in TMEM
-constexpr int kOWarp0 = 10, kOWarps = 4;   // O: fp32 -> bf16 -> TMA store
-constexpr int kBWarp = 14;                 // MMA issuer of P
-constexpr int kCWarp = 15;                 // MMA issuer of P V
-constexpr int kThreads = 32 * (kCWarp + 1);
-static_assert(kPWarp0 == kSWarp0 + kSWarps && kOWarp0 == kPWarp0 + kPWarps &&
-                  kBWarp == kOWarp0 + kOWarps,
-              "converter groups of consecutive warps, one per TMEM lane quarter");
-constexpr int kOThreads = 32 * kOWarps;
-
-struct Args {
-  int64_t N;
-  int n_tiles;
-  int seg_tiles;
-  int G;
-  int BH;
-  int n_mb;
-  int reverse;
-  const float* agg_in;   // [P][G][DP][MB]; null when G == 1
-  float* agg_out;        // aggregate-only launch writes here
-  int* status;
-};
-
-template <int DP, int MB>
-struct Layout {
-  static constexpr int kQBoxes = DP / kBoxCols;
-  static constexpr int kVBoxes = MB / kBoxCols;
-  static constexpr int kSBlocks = (DP + 127) / 128;
-  static constexpr int kQBytes = kQBoxes * kBoxBytes;
-  static constexpr int kQKBytes = 2 * kQBytes;               // one Q tile + one K tile
-  static constexpr int kVBytes = kVBoxes * kBoxBytes;
-  static constexpr int kSOneBytes = kVBoxes * DP * 128;      // DP x MB bf16
-  static constexpr int kOBytes = kVBoxes * kBoxBytes;        // 128 x MB bf16
-  static constexpr int kBarBytes = 1024;
-  static constexpr int kAlignSlack = 1024;
-  static constexpr int kAvail = kSmemLimit - kBarBytes - kAlignSlack;
-  // Q/K and V tiles live in two rings: Q and K are released once P, the
-  // state update and Q S have been issued, V only after P V, so the V ring
-  // gets one stage more when it fits.  Returns NQK * 8 + NV.
-  static constexpr int rings(int budget) {
-    for (int n = 4; n >= 1; --n) {
-      if (n * kQKBytes + (n + 1) * kVBytes <= budget) return n * 8 + n + 1;
-      if (n * kQKBytes + n * kVBytes <= budget) return n * 8 + n;
-    }
-    return 0;
-  }
-  // TMEM holds NP buffers of P (128 columns, fp32; later packed bf16 hi|lo),
-  // the Q S accumulator O1, the P V accumulator O2 (MB columns) and the
-  // state (kSBlocks x MB).  O1 is 2 MB wide when it fits: Q [S_hi | S_lo]
-  // in one N = 2 MB chain, the two halves summed on read-out.  A P buffer is
-  // reused only after the P V that read it has completed.
-  static constexpr int cols(int np, bool wide) {
-    return np * 128 + (wide ? 2 : 1) * MB + MB + kSBlocks * MB;
-  }
-  static constexpr int NP = cols(2, false) <= 512 ? 2 : 1;
-  static constexpr bool kWide = cols(NP, true) <= 512 && 2 * MB <= 256;
-  static constexpr int kO1Cols = (kWide ? 2 : 1) * MB;
-  static constexpr int NO = 1;
-  // bf16 copies of the state in shared memory (one per tile in flight, at
-  // most two); the state operand of Q S is split into hi + lo parts when it
-  // fits next to a one-stage ring.
-  static constexpr int NSB =
-      (NP >= 2 && rings(kAvail - 4 * kSOneBytes - 2 * kOBytes) / 8 >= 2) ? 2 : 1;
-  static constexpr bool kSplit = rings(kAvail - NSB * 2 * kSOneBytes - kOBytes) / 8 >= 1;
-  static constexpr int kSBufBytes = (kSplit ? 2 : 1) * kSOneBytes;
-  // output staging: two buffers (one store in flight) when they fit
-  static constexpr int kOBufs =
-      rings(kAvail - NSB * kSBufBytes - 2 * kOBytes) / 8 >= (NSB == 2 ? 2 : 1) ? 2 : 1;
-  static constexpr int kFixed = NSB * kSBufBytes + kOBufs * kOBytes;
-  static constexpr int NQK = rings(kAvail - kFixed) / 8;
-  static constexpr int NV = rings(kAvail - kFixed) % 8;
-  static constexpr int kSmemBytes =
-      NQK * kQKBytes + NV * kVBytes + kFixed + kBarBytes + kAlignSlack;
-  static constexpr int kColP = 0;                        // + b * 128
-  static constexpr int kColO1 = NP * 128;                // Q S (kO1Cols)
-  static constexpr int kColO2 = kColO1 + kO1Cols;        // P V (MB)
-  static constexpr int kColS = kColO2 + MB;              // + sb * MB
-  static constexpr int kColsUsed = kColS + kSBlocks * MB;
-  static constexpr int kColsAlloc = kColsUsed <= 256 ? 256 : 512;
-  static_assert(NQK >= 1 && NV >= 1, "tile does not fit in shared memory");
-  static_assert(kSmemBytes <= kSmemLimit, "shared memory overflow");
-  static_assert(kColsUsed <= 512, "accumulators do not fit in TMEM");
-  static_assert(DP % 64 == 0 && MB % 64 == 0, "64-column boxes");
-  static_assert(!kWide || kSplit, "the wide Q S chain reads S_hi and S_lo side by side");
-};
 
 template <int DP, int MB, bool AGG_ONLY>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -144,558 +18,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_o, const Args a) {
-  using L = Layout<DP, MB>;
-  constexpr int NQK = L::NQK;
-  constexpr int NV = L::NV;
-  constexpr int NP = L::NP;
-  constexpr int NSB = L::NSB;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* qk_ring = smem;                           // [NQK] x (Q tile | K tile)
-  uint8_t* v_ring = qk_ring + NQK * L::kQKBytes;     // [NV] x V tile
-  uint8_t* s_tile = v_ring + NV * L::kVBytes;        // [NSB] x (hi | lo) bf16 state copies
-  uint8_t* o_tile = s_tile + NSB * L::kSBufBytes;    // [kOBufs] output staging
-  uint64_t* bars = reinterpret_cast<uint64_t*>(o_tile + L::kOBufs * L::kOBytes);
-  uint64_t* full_qk = bars;                 // [NQK] TMA -> MMA
-  uint64_t* empty_qk = full_qk + NQK;       // [NQK] MMA -> TMA
-  uint64_t* full_v = empty_qk + NQK;        // [NV]
-  uint64_t* empty_v = full_v + NV;          // [NV]
-  uint64_t* p_done = empty_v + NV;          // [NP] issuer B -> P group: P(t) in TMEM
-  uint64_t* p_ready = p_done + NP;          // [NP] P group -> C: masked bf16 P (hi|lo) packed
-  uint64_t* pv_done = p_ready + NP;         // [NP] C -> O group, B: O2(t) final, P buffer free
-  uint64_t* qs_done = pv_done + NP;         // [NSB] A -> S group: Q S(t) done, state copy free
-  uint64_t* o1_done = qs_done + NSB;        // A -> O group: O1(t) final
-  uint64_t* o_free = o1_done + 1;           // O group -> A, C: O1 and O2 of tile t read out
-  uint64_t* s_done = o_free + 1;            // A -> S group: state updated with tile t
-  uint64_t* s_ready = s_done + 1;           // S group -> A: bf16 state copy written, S read
-  uint64_t* fin = s_done + 2;               // [3] issuer drains before TMEM release
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(s_done + 5);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(s_done + 6);
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-
-  // ---- block -> (segment, problem, value-column block)
-  int idx = blockIdx.x;
-  const int mb = idx % a.n_mb;
-  idx /= a.n_mb;
-  const int bh = idx % a.BH;
-  int seg = idx / a.BH;
-  if (AGG_ONLY && a.reverse) seg += 1;  // the first segment in scan order is never needed
-  const int t_first = seg * a.seg_tiles;
-  const int t_end = min(a.n_tiles, t_first + a.seg_tiles);
-  const int n_it = t_end - t_first;
-  const int pidx = bh * a.n_mb + mb;
-  const bool has_prefix =
-      !AGG_ONLY && a.agg_in != nullptr && (a.reverse ? (seg < a.G - 1) : (seg > 0));
-  auto tile_of = [&](int it) { return a.reverse ? (t_end - 1 - it) : (t_first + it); };
-
-  if (threadIdx.x == 0) {
-    // a stage is released by both issuers (A: S / Q S, B: P / P V); in the
-    // aggregate-only mode issuer A alone consumes the rings
-    const uint32_t kRel = AGG_ONLY ? 1 : 2;  // A + B for Q/K, A + C for V
-    for (int i = 0; i < NQK; ++i) {
-      mbar_init(&full_qk[i], 1);
-      mbar_init(&empty_qk[i], kRel);
-    }
-    for (int i = 0; i < NV; ++i) {
-      mbar_init(&full_v[i], 1);
-      mbar_init(&empty_v[i], kRel);
-    }
-    for (int i = 0; i < NP; ++i) {
-      mbar_init(&p_done[i], 1);
-      mbar_init(&p_ready[i], kPWarps);
-      mbar_init(&pv_done[i], 1);
-    }
-    for (int i = 0; i < NSB; ++i) mbar_init(&qs_done[i], 1);
-    mbar_init(o1_done, 1);
-    mbar_init(o_free, kOWarps);
-    mbar_init(s_done, 1);
-    mbar_init(s_ready, kSWarps);
-    mbar_init(&fin[0], 1);
-    mbar_init(&fin[1], 1);
-    mbar_init(&fin[2], 1);
-    *abort_flag = 0;
-    fence_mbar_init();
-    fence_proxy_async_smem();
-  }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
-    if (!AGG_ONLY) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_o);
-    }
-  }
-  if (warp == 1) {
-    tmem_alloc(tmem_holder, L::kColsAlloc);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  grid_dep_wait();  // inputs written by the previous kernel are visible from here
-  // dependents start only once every block has passed the wait above, so
-  // for them every kernel before this one has completed
-  grid_dep_launch_dependents();
-  const uint32_t tmem = *tmem_holder;
-  const int wq = warp & 3;                 // TMEM lane quarter of this warp
-  const int row = wq * 32 + lane;          // tile row = TMEM lane
-  const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    // Polls both rings and refills whichever has a free stage (V never runs
-    // ahead of Q/K).
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      constexpr uint32_t kQKTx = AGG_ONLY ? L::kQBytes : L::kQKBytes;
-      int nq = 0, nv = 0;
-      uint64_t t0 = globaltimer();
-      uint32_t idle = 0;
-      while (nq < n_it || nv < n_it) {
-        bool progressed = false;
-        if (nq < n_it &&
-            (nq < NQK || mbar_test_wait(&empty_qk[nq % NQK], ((nq / NQK) - 1) & 1))) {
-          const int st = nq % NQK;
-          const int row0 = tile_of(nq) * kTile;
-          uint8_t* q_s = qk_ring + st * L::kQKBytes;
-          uint8_t* k_s = q_s + L::kQBytes;
-          mbar_arrive_expect_tx(&full_qk[st], kQKTx);
-#pragma unroll
-          for (int b = 0; b < L::kQBoxes; ++b) {
-            if (!AGG_ONLY)
-              tma_load_3d(q_s + b * kBoxBytes, &tm_q, &full_qk[st], b * kBoxCols, row0, bh, pol);
-            tma_load_3d(k_s + b * kBoxBytes, &tm_k, &full_qk[st], b * kBoxCols, row0, bh, pol);
-          }
-          ++nq;
-          progressed = true;
-        }
-        if (nv < nq && (nv < NV || mbar_test_wait(&empty_v[nv % NV], ((nv / NV) - 1) & 1))) {
-          const int st = nv % NV;
-          const int row0 = tile_of(nv) * kTile;
-          uint8_t* v_s = v_ring + st * L::kVBytes;
-          mbar_arrive_expect_tx(&full_v[st], L::kVBytes);
-#pragma unroll
-          for (int b = 0; b < L::kVBoxes; ++b)
-            tma_load_3d(v_s + b * kBoxBytes, &tm_v, &full_v[st], mb * MB + b * kBoxCols, row0,
-                        bh, pol);
-          ++nv;
-          progressed = true;
-        }
-        if (progressed) {
-          idle = 0;
-        } else if ((++idle & 63u) == 0) {
-          if (idle == 64) t0 = globaltimer();
-          if (*abort_flag || globaltimer() - t0 > CP_WAIT_TIMEOUT_NS) {
-            record_timeout(a.status, abort_flag);
-            break;
-          }
-        }
-      }
-      if (*abort_flag) {
-        // let the copies already issued land before the CTA's memory goes away
-        for (int j = max(0, nq - NQK); j < nq; ++j)
-          mbar_wait_timeout(&full_qk[j % NQK], (j / NQK) & 1, CP_WAIT_TIMEOUT_NS);
-        for (int j = max(0, nv - NV); j < nv; ++j)
-          mbar_wait_timeout(&full_v[j % NV], (j / NV) & 1, CP_WAIT_TIMEOUT_NS);
-      }
-    }
-  } else if (warp == 1 || warp == kBWarp || warp == kCWarp) {
-    // ------------------------------------------------------------ MMA issuers
-    // Issuer A (warp 1): the state chain S(t) and the inter-tile read-out
-    // Q S(t) into O1.  Issuer B (warp kBWarp): P(t) = Q K^T.  Issuer C (warp
-    // kCWarp): the intra-tile P V(t) into O2.  Q S and P V never touch the
-    // same accumulator, so the issuers need no ordering between them beyond
-    // the barriers on P; a ring stage is released by a commit from each of
-    // its two users.
-    if (lane == 0 && (warp == 1 || !AGG_ONLY)) {
-      constexpr uint32_t idesc_p = idesc_bf16_f32(128, 128, 0, 0);   // Q . K^T
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, MB, 1, 1);    // K^T . V
-      constexpr uint32_t idesc_o = idesc_bf16_f32(128, MB, 0, 1);    // P . V, Q . S
-      constexpr uint32_t idesc_ow = idesc_bf16_f32(128, 2 * MB, 0, 1);  // Q . [S_hi | S_lo]
-      constexpr uint32_t kHi = desc_hi(1024);  // SBO = 1024, 128-byte swizzle
-      const uint32_t t_s = tmem + L::kColS;
-      const uint32_t t_o1 = tmem + L::kColO1;
-      const uint32_t t_o2 = tmem + L::kColO2;
-      const uint32_t s_addr = smem_u32(s_tile);
-      auto qk_addr = [&](int it) { return smem_u32(qk_ring + (it % NQK) * L::kQKBytes); };
-      auto v_addr = [&](int it) { return smem_u32(v_ring + (it % NV) * L::kVBytes); };
-      // Descriptor low words advance by (byte offset >> 4) per K step.
-      auto issue_s = [&](int it) {
-        // S += K^T V (A = K^T and B = V, both MN-major), one 128-row block of
-        // the state per 128 columns of K
-        const uint32_t kt_lo = desc_lo(qk_addr(it) + L::kQBytes, kBoxBytes);
-        const uint32_t v_lo = desc_lo(v_addr(it), kBoxBytes);
-        const bool fresh = (it == 0) && !has_prefix;
-#pragma unroll
-        for (int sb = 0; sb < L::kSBlocks; ++sb) {
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            mma_ss_lo<kHi, kHi>(t_s + sb * MB, kt_lo + ((2 * sb * kBoxBytes + kk * 2048) >> 4),
-                                v_lo + ((kk * 2048) >> 4), idesc_s, (fresh && kk == 0) ? 0u : 1u);
-          }
-        }
-      };
-      bool ok = true;
-      uint64_t t0 = globaltimer();
-      uint32_t idle = 0;
-      auto idle_tick = [&](bool progressed) -> bool {  // false: give up
-        if (progressed) {
-          idle = 0;
-        } else if ((++idle & 63u) == 0) {
-          if (idle == 64) t0 = globaltimer();
-          if (*abort_flag || globaltimer() - t0 > CP_WAIT_TIMEOUT_NS) return false;
-        }
-        return true;
-      };
-      if (AGG_ONLY) {
-        for (int it = 0; it < n_it; ++it) {
-          if (!mbar_wait(&full_qk[it % NQK], (it / NQK) & 1, abort_flag) ||
-              !mbar_wait(&full_v[it % NV], (it / NV) & 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          issue_s(it);
-          mma_commit(&empty_qk[it % NQK]);
-          mma_commit(&empty_v[it % NV]);
-        }
-        if (ok) mma_commit(s_done);
-      } else if (warp == 1) {
-        // issuer A: S(t) needs Q/K(t), V(t) landed and the state copied out
-        // (s_ready); Q S(t) needs S(t) issued and O1 read out for t - 1.
-        int nS = 0, nQ = 0;
-        while (nQ < n_it) {
-          bool progressed = false;
-          if (nS < n_it && mbar_test_wait(&full_qk[nS % NQK], (nS / NQK) & 1) &&
-              mbar_test_wait(&full_v[nS % NV], (nS / NV) & 1) &&
-              mbar_test_wait(s_ready, nS & 1)) {
-            tc_fence_after();
-            issue_s(nS);
-            mma_commit(s_done);
-            mma_commit(&empty_v[nS % NV]);
-            ++nS;
-            progressed = true;
-          }
-          if (nQ < nS && (nQ == 0 || mbar_test_wait(o_free, (nQ - 1) & 1))) {
-            tc_fence_after();
-            const uint32_t q_lo = desc_lo(qk_addr(nQ), 16);
-            const uint32_t s_lo = desc_lo(s_addr + (nQ % NSB) * L::kSBufBytes, DP * 128);
-            if (L::kWide) {
-              // O1 = Q [S_hi | S_lo]: hi and lo copies sit side by side as
-              // one MN-major operand of 2 MB columns
-#pragma unroll
-              for (int kk = 0; kk < DP / 16; ++kk) {
-                const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-                mma_ss_lo<kHi, kHi>(t_o1, q_lo + off, s_lo + ((kk * 2048) >> 4), idesc_ow,
-                                    kk > 0 ? 1u : 0u);
-              }
-            } else {
-              // O1 = Q S_hi (+ Q S_lo)
-#pragma unroll
-              for (int part = 0; part < (L::kSplit ? 2 : 1); ++part) {
-#pragma unroll
-                for (int kk = 0; kk < DP / 16; ++kk) {
-                  const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-                  mma_ss_lo<kHi, kHi>(t_o1, q_lo + off,
-                                      s_lo + ((part * L::kSOneBytes + kk * 2048) >> 4), idesc_o,
-                                      (part == 0 && kk == 0) ? 0u : 1u);
-                }
-              }
-            }
-            mma_commit(&qs_done[nQ % NSB]);
-            mma_commit(o1_done);
-            mma_commit(&empty_qk[nQ % NQK]);
-            ++nQ;
-            progressed = true;
-          }
-          if (!idle_tick(progressed)) { ok = false; break; }
-        }
-      } else if (warp == kBWarp) {
-        // issuer B: P(t) needs Q/K(t) landed and P buffer t%NP free (P V of
-        // tile t - NP completed)
-        for (int it = 0; it < n_it; ++it) {
-          if (!mbar_wait(&full_qk[it % NQK], (it / NQK) & 1, abort_flag) ||
-              (it >= NP && !mbar_wait(&pv_done[it % NP], ((it - NP) / NP) & 1, abort_flag))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t q_lo = desc_lo(qk_addr(it), 16);
-          const uint32_t k_lo = desc_lo(qk_addr(it) + L::kQBytes, 16);
-          const uint32_t t_p = tmem + L::kColP + (it % NP) * 128;
-#pragma unroll
-          for (int kk = 0; kk < DP / 16; ++kk) {
-            const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-            mma_ss_lo<kHi, kHi>(t_p, q_lo + off, k_lo + off, idesc_p, kk > 0);
-          }
-          mma_commit(&p_done[it % NP]);
-          mma_commit(&empty_qk[it % NQK]);
-        }
-      } else {
-        // issuer C: P V(t) needs P(t) packed, V(t) landed and O2 read out
-        // for t - 1
-        for (int it = 0; it < n_it; ++it) {
-          const int b = it % NP;
-          if (!mbar_wait(&p_ready[b], (it / NP) & 1, abort_flag) ||
-              !mbar_wait(&full_v[it % NV], (it / NV) & 1, abort_flag) ||
-              (it > 0 && !mbar_wait(o_free, (it - 1) & 1, abort_flag))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t t_p = tmem + L::kColP + b * 128;
-          const uint32_t v_lo = desc_lo(v_addr(it), kBoxBytes);
-          // O2 = P_hi V (+ P_lo V) (A = packed bf16 P in TMEM, B = V
-          // MN-major).  Chunk c of P (columns 32c..32c+31) holds hi in its
-          // first 16 TMEM columns and lo in the next 16, two j per column.
-#pragma unroll
-          for (int part = 0; part < kPParts; ++part) {
-#pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk) {
-              const uint32_t acol = (kk >> 1) * 32 + part * 16 + (kk & 1) * 8;
-              mma_ts_lo<kHi>(t_o2, t_p + acol, v_lo + ((kk * 2048) >> 4), idesc_o,
-                             (part == 0 && kk == 0) ? 0u : 1u);
-            }
-          }
-          mma_commit(&pv_done[b]);
-          mma_commit(&empty_v[it % NV]);
-        }
-      }
-      if (!ok) record_timeout(a.status, abort_flag);
-      // every MMA this thread issued completes before TMEM is released
-      uint64_t* my_fin = &fin[warp == 1 ? 0 : (warp == kBWarp ? 1 : 2)];
-      mma_commit(my_fin);
-      mbar_wait_timeout(my_fin, 0, CP_WAIT_TIMEOUT_NS);
-    }
-  } else if (warp < kPWarp0) {
-    // ------------------------------------------------------------ state group
-    bool ok = true;
-    if (AGG_ONLY) {
-      if (!mbar_wait(s_done, 0, abort_flag)) {
-        record_timeout(a.status, abort_flag);
-      } else if (n_it > 0) {
-        tc_fence_after();
-        float* dst = a.agg_out + ((size_t)pidx * a.G + seg) * (size_t)DP * MB;
-#pragma unroll
-        for (int sb = 0; sb < L::kSBlocks; ++sb) {
-          if (sb * 128 + wq * 32 >= DP) continue;  // warp-uniform
-          const int d = sb * 128 + row;
-#pragma unroll
-          for (int c = 0; c < MB / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(lane_base + L::kColS + sb * MB + c * 32, r);
-            tmem_ld_wait();
-            float4* o4 = reinterpret_cast<float4*>(dst + (size_t)d * MB + c * 32);
-#pragma unroll
-            for (int x = 0; x < 8; ++x)
-              o4[x] = make_float4(__uint_as_float(r[4 * x]), __uint_as_float(r[4 * x + 1]),
-                                  __uint_as_float(r[4 * x + 2]), __uint_as_float(r[4 * x + 3]));
-          }
-        }
-      }
-    } else {
-      // initial state: fixed-order sum of the preceding segments' aggregates
-      if (has_prefix) {
-        const int lo = a.reverse ? seg + 1 : 0;
-        const int hi = a.reverse ? a.G : seg;
-#pragma unroll
-        for (int sb = 0; sb < L::kSBlocks; ++sb) {
-          if (sb * 128 + wq * 32 >= DP) continue;
-          const int d = sb * 128 + row;
-#pragma unroll
-          for (int c = 0; c < MB / 32; ++c) {
-            float acc[32];
-#pragma unroll
-            for (int x = 0; x < 32; ++x) acc[x] = 0.f;
-            for (int s2 = lo; s2 < hi; ++s2) {
-              const float4* src = reinterpret_cast<const float4*>(
-                  a.agg_in + (((size_t)pidx * a.G + s2) * DP + d) * MB + c * 32);
-#pragma unroll
-              for (int x = 0; x < 8; ++x) {
-                const float4 f = __ldg(src + x);
-                acc[4 * x] += f.x;
-                acc[4 * x + 1] += f.y;
-                acc[4 * x + 2] += f.z;
-                acc[4 * x + 3] += f.w;
-              }
-            }
-            uint32_t r[32];
-#pragma unroll
-            for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(acc[x]);
-            tmem_st32(lane_base + L::kColS + sb * MB + c * 32, r);
-          }
-        }
-        tmem_st_wait();
-      }
-      for (int it = 0; it < n_it && ok; ++it) {
-        const int b = it % NSB;
-        uint8_t* sbuf = s_tile + b * L::kSBufBytes;
-        // the Q S that last read this copy (tile it - NSB) has completed
-        if (it >= NSB && !mbar_wait(&qs_done[b], ((it - NSB) / NSB) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        if (it == 0 && !has_prefix) {
-#pragma unroll
-          for (int sb = 0; sb < L::kSBlocks; ++sb) {
-            if (sb * 128 + wq * 32 >= DP) continue;
-#pragma unroll
-            for (int c = 0; c < MB / 32; ++c) {
-              store_zero32(sbuf, sb * 128 + row, c * 32, DP * 128);
-              if (L::kSplit) store_zero32(sbuf + L::kSOneBytes, sb * 128 + row, c * 32, DP * 128);
-            }
-          }
-        } else {
-          if (it > 0) {
-            if (!mbar_wait(s_done, (it - 1) & 1, abort_flag)) { ok = false; break; }
-            tc_fence_after();
-          }
-#pragma unroll
-          for (int sb = 0; sb < L::kSBlocks; ++sb) {
-            if (sb * 128 + wq * 32 >= DP) continue;
-#pragma unroll
-            for (int c = 0; c < MB / 32; ++c) {
-              uint32_t r[32];
-              tmem_ld32(lane_base + L::kColS + sb * MB + c * 32, r);
-              tmem_ld_wait();
-              if (L::kSplit)
-                store_chunk32_split(sbuf, sbuf + L::kSOneBytes, sb * 128 + row, c * 32, DP * 128,
-                                    r);
-              else
-                store_chunk32(sbuf, sb * 128 + row, c * 32, DP * 128, r);
-            }
-          }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(s_ready);
-      }
-      if (!ok) record_timeout(a.status, abort_flag);
-    }
-  } else if (warp < kOWarp0) {
-    // ------------------------------------------------------------ P group
-    // P of tile it: mask to the causal triangle of the tile, split into bf16
-    // hi + lo and pack back into the chunk's own TMEM columns: chunk c
-    // (j in [32c, 32c+32)) -> hi at 32c + [0,16), lo at 32c + [16,32), two j
-    // per 32-bit column.
-    bool ok = true;
-    for (int it = 0; !AGG_ONLY && it < n_it && ok; ++it) {
-      const int b = it % NP;
-      if (!mbar_wait(&p_done[b], (it / NP) & 1, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t pc = lane_base + L::kColP + b * 128;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        const bool z = a.reverse ? (c < wq) : (c > wq);  // chunk entirely masked
-        uint32_t r[32];
-        if (!z) {
-          tmem_ld32(pc + 32 * c, r);
-          tmem_ld_wait();
-        }
-        split_pack_p(r, z, c == wq, lane, a.reverse);
-        store_packed_p(pc + 32 * c, r);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_ready[b]);
-    }
-    if (!ok) record_timeout(a.status, abort_flag);
-  } else {
-    // ------------------------------------------------------------ O group
-    const int o_tid = threadIdx.x - 32 * kOWarp0;   // 0..kOThreads-1
-    bool ok = true;
-    for (int it = 0; !AGG_ONLY && it < n_it && ok; ++it) {
-      uint8_t* ob = o_tile + (it % L::kOBufs) * L::kOBytes;
-      if (!mbar_wait(o1_done, it & 1, abort_flag) ||
-          !mbar_wait(&pv_done[it % NP], (it / NP) & 1, abort_flag)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      auto wait_staging = [&]() {
-        // the store that last read this staging buffer has finished reading it
-        if (o_tid == 0) {
-          if (L::kOBufs == 2)
-            asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-          else
-            tma_store_wait_read_all();
-        }
-        named_barrier_sync(1, kOThreads);
-      };
-      // O = O1 (+ its lo half when wide) + O2
-      if constexpr (MB <= 64) {
-        // the whole row fits in registers: release the accumulators before
-        // converting and storing
-        uint32_t r[MB / 32][32];
-#pragma unroll
-        for (int c = 0; c < MB / 32; ++c) {
-          uint32_t u[32], w[32];
-          tmem_ld32(lane_base + L::kColO1 + c * 32, r[c]);
-          tmem_ld32(lane_base + L::kColO2 + c * 32, u);
-          if (L::kWide) tmem_ld32(lane_base + L::kColO1 + MB + c * 32, w);
-          tmem_ld_wait();
-#pragma unroll
-          for (int x = 0; x < 32; ++x) {
-            float f = __uint_as_float(r[c][x]) + __uint_as_float(u[x]);
-            if (L::kWide) f += __uint_as_float(w[x]);
-            r[c][x] = __float_as_uint(f);
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(o_free);
-        wait_staging();
-#pragma unroll
-        for (int c = 0; c < MB / 32; ++c) store_chunk32(ob, row, c * 32, kBoxBytes, r[c]);
-      } else {
-        wait_staging();
-#pragma unroll 1
-        for (int c = 0; c < MB / 32; ++c) {
-          uint32_t r[32], u[32];
-          tmem_ld32(lane_base + L::kColO1 + c * 32, r);
-          tmem_ld32(lane_base + L::kColO2 + c * 32, u);
-          tmem_ld_wait();
-#pragma unroll
-          for (int x = 0; x < 32; ++x)
-            r[x] = __float_as_uint(__uint_as_float(r[x]) + __uint_as_float(u[x]));
-          if (L::kWide) {
-            tmem_ld32(lane_base + L::kColO1 + MB + c * 32, u);
-            tmem_ld_wait();
-#pragma unroll
-            for (int x = 0; x < 32; ++x)
-              r[x] = __float_as_uint(__uint_as_float(r[x]) + __uint_as_float(u[x]));
-          }
-          store_chunk32(ob, row, c * 32, kBoxBytes, r);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(o_free);
-      }
-      fence_proxy_async_smem();
-      named_barrier_sync(1, kOThreads);
-      if (o_tid == 0) {
-        const int tile = tile_of(it);
-#pragma unroll
-        for (int bx = 0; bx < L::kVBoxes; ++bx)
-          tma_store_3d(&tm_o, ob + bx * kBoxBytes, mb * MB + bx * kBoxCols, tile * kTile, bh);
-        tma_store_commit();
-      }
-    }
-    if (!ok) record_timeout(a.status, abort_flag);
-    if (o_tid == 0) tma_store_wait_all();
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, L::kColsAlloc);
-  }
+  causal_body<DP, MB, AGG_ONLY>(tm_q, tm_k, tm_v, tm_o, a);
 }
 
 // ------------------------------------------------------------------ host
