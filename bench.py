@@ -40,13 +40,15 @@ UNIT = "Mtok·head/s"
 # DRAM traffic of one launch of the tensor-core kernel measured by ncu
 # (dram__bytes_read.sum + dram__bytes_write.sum) together with the SHA-256 of
 # the kernel source it was measured on; a changed source reports null.
+CAUSAL_SOURCES = ("cp_tc.cu", "cp_tc_causal.cuh", "cp_tc_common.cuh", "sm103_ptx.cuh")
+DKDV_SOURCES = ("cp_tc_dkdv.cu", "cp_tc_dkdv.cuh", "cp_tc_common.cuh", "sm103_ptx.cuh")
 PROFILED_TRAFFIC = {
-    "source_sha256": "8a8a1aa2c768bd353ab7155f915b769d1a0112fa706a8eca1ee728e8e1079f43",
-    "bytes_per_launch": 211614720,  # 201.39 MB read + 10.23 MB written (forward launch)
+    "source_sha256": "a1d4c6d965fbaddad32b2a7d61de45f34e2d1b9ab1ca3a929df55b9e1ef43272",
+    "bytes_per_launch": 211631872,  # 201.39 MB read + 10.24 MB written (forward launch)
 }
 PROFILED_TRAFFIC_DKDV = {
-    "source_sha256": None,
-    "bytes_per_launch": None,
+    "source_sha256": "4c3aaec81f4bb36defef0acfd8aafca2b7d618db36a2c9415427fae2fab10daf",
+    "bytes_per_launch": 342428928,  # 268.53 MB read + 73.90 MB written
 }
 
 
@@ -170,9 +172,9 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows), "window": window}
 
 
-def kernel_sha(main="cp_tc.cu"):
+def kernel_sha(files=CAUSAL_SOURCES):
     h = hashlib.sha256()
-    for f in (main, "cp_tc_common.cuh", "sm103_ptx.cuh"):
+    for f in files:
         with open(os.path.join(ROOT, "prefix_sum_outer_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
@@ -380,7 +382,7 @@ def run_ours(args, world, rank, local):
         dkdv_bytes = s * (3 * w.D + 3 * w.M) * w.token_heads
         dkdv_ms = (bwd_ms - fwd_ms) / args.steps
         dkdv_traffic = None
-        if PROFILED_TRAFFIC_DKDV["source_sha256"] == kernel_sha("cp_tc_dkdv.cu"):
+        if PROFILED_TRAFFIC_DKDV["source_sha256"] == kernel_sha(DKDV_SOURCES):
             dkdv_traffic = PROFILED_TRAFFIC_DKDV["bytes_per_launch"]
         kernels.append({"kernel": "tc_dkdv_kernel", "bound": "hbm",
                         "bytes_per_launch": dkdv_bytes, "avg_launch_ms": dkdv_ms,
