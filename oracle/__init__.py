@@ -12,6 +12,13 @@ it with gcc and exposes it through ctypes:
 
     fwd(q, k, v)        -> out            (float64 [..., N, M])
     bwd(q, k, v, g)     -> (dq, dk, dv)   (float64)
+    fwd_state(q, k, v, state_in=None)
+                        -> (out, state_out)           with carried state
+    bwd_state(q, k, v, g, state_in=None, grad_state_out=None)
+                        -> (dq, dk, dv, grad_state_in)
+
+States are [..., D, M] arrays; they may be float64 (the oracle's own
+states) as well as float32 or bfloat16 values, all exact in double.
 
 Inputs are numpy arrays of shape [B, H, N, D] / [B, H, N, M] (any leading
 shape works; the last two axes are N and the feature axis).  They are
@@ -65,6 +72,11 @@ def _load():
             lib.cpo_fwd.restype = c_int
             lib.cpo_bwd.argtypes = [p, p, p, p, p, p, p, i64, i64, i64, i64, c_int]
             lib.cpo_bwd.restype = c_int
+            lib.cpo_fwd_state.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, c_int]
+            lib.cpo_fwd_state.restype = c_int
+            lib.cpo_bwd_state.argtypes = [p, p, p, p, p, p, p, p, p, p, i64, i64, i64, i64,
+                                          c_int]
+            lib.cpo_bwd_state.restype = c_int
             lib.cpo_threads.argtypes = [c_int]
             lib.cpo_threads.restype = c_int
             _lib = lib
@@ -119,3 +131,53 @@ def bwd(q, k, v, g, nthreads: int = 0):
     if rc != 0:
         raise RuntimeError(f"oracle bwd failed ({rc})")
     return dq, dk, dv
+
+
+def _state(x, lead, D, M, name):
+    if x is None:
+        return None
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    if x.shape != lead + (D, M):
+        raise ValueError(f"{name} shape {x.shape} != {lead + (D, M)}")
+    return x
+
+
+def _ptr(x):
+    return None if x is None else x.ctypes.data
+
+
+def fwd_state(q, k, v, state_in=None, nthreads: int = 0):
+    """(out, state_out) with the scan started from state_in ([..., D, M],
+    None = zero): out_i = (S_0 + sum_{j<=i} k_j v_j^T)^T q_i and
+    state_out = S_0 + sum_j k_j v_j^T, in fp64."""
+    q, k, v = _as_f32(q), _as_f32(k), _as_f32(v)
+    lead, BH, N, D, M = _dims(q, k, v)
+    s0 = _state(state_in, lead, D, M, "state_in")
+    out = np.zeros(lead + (N, M), dtype=np.float64)
+    s_n = np.zeros(lead + (D, M), dtype=np.float64)
+    rc = _load().cpo_fwd_state(q.ctypes.data, k.ctypes.data, v.ctypes.data, out.ctypes.data,
+                               _ptr(s0), s_n.ctypes.data, BH, N, D, M, int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle fwd_state failed ({rc})")
+    return out, s_n
+
+
+def bwd_state(q, k, v, g, state_in=None, grad_state_out=None, nthreads: int = 0):
+    """(dq, dk, dv, grad_state_in) of L = <g, out> + <grad_state_out, S_N>
+    for the scan started from state_in (None = zero), in fp64."""
+    q, k, v, g = _as_f32(q), _as_f32(k), _as_f32(v), _as_f32(g)
+    lead, BH, N, D, M = _dims(q, k, v)
+    if g.shape != v.shape:
+        raise ValueError(f"grad shape {g.shape} != out shape {v.shape}")
+    s0 = _state(state_in, lead, D, M, "state_in")
+    ds_n = _state(grad_state_out, lead, D, M, "grad_state_out")
+    dq = np.zeros(lead + (N, D), dtype=np.float64)
+    dk = np.zeros(lead + (N, D), dtype=np.float64)
+    dv = np.zeros(lead + (N, M), dtype=np.float64)
+    ds0 = np.zeros(lead + (D, M), dtype=np.float64)
+    rc = _load().cpo_bwd_state(q.ctypes.data, k.ctypes.data, v.ctypes.data, g.ctypes.data,
+                               _ptr(s0), _ptr(ds_n), dq.ctypes.data, dk.ctypes.data,
+                               dv.ctypes.data, ds0.ctypes.data, BH, N, D, M, int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle bwd_state failed ({rc})")
+    return dq, dk, dv, ds0

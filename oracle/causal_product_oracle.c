@@ -28,6 +28,15 @@
  *       R_j  = sum_{i>=j} q_i g_i^T            (reverse sweep over j)
  *       dk_j = R_j v_j,    dv_j = R_j^T k_j
  *
+ *   Carried state.  The loop in the issue keeps its state across the
+ *   sequence (the Triton port there takes the state as an argument), so a
+ *   call may start from an initial state S_0 and hand on its final state:
+ *       S_i = S_0 + sum_{j<=i} k_j v_j^T,      S_N = S_0 + sum_j k_j v_j^T.
+ *   With L = sum_i <g_i, out_i> + <dS_N, S_N> the backward becomes
+ *       dq_i = S_i g_i,    R_j = dS_N + sum_{i>=j} q_i g_i^T,
+ *       dk_j = R_j v_j,    dv_j = R_j^T k_j,    dS_0 = R_0
+ *   (S_0 enters every S_i, and dS_N every R_j).  Absent states are zero.
+ *
  * Inputs are float32 arrays holding the exact values the GPU receives
  * (bfloat16 values are exactly representable in float32 and in double);
  * each slice is widened to double before any arithmetic.  Outputs are
@@ -48,10 +57,15 @@ static void widen(const float *src, double *dst, int64_t n) {
     for (int64_t i = 0; i < n; ++i) dst[i] = (double)src[i];
 }
 
-/* Forward recurrence on one (b,h) slice; all arrays double, row-major. */
+/* Forward recurrence on one (b,h) slice; all arrays double, row-major.
+ * S0 (may be NULL: zero) is the initial state; the final state goes to SN
+ * when SN is not NULL. */
 static void fwd_slice(const double *q, const double *k, const double *v,
-                      double *out, double *S, int64_t N, int64_t D, int64_t M) {
-    memset(S, 0, sizeof(double) * (size_t)(D * M));
+                      double *out, double *S, const double *S0, double *SN,
+                      int64_t N, int64_t D, int64_t M) {
+    /* start from the initial state */
+    if (S0) memcpy(S, S0, sizeof(double) * (size_t)(D * M));
+    else memset(S, 0, sizeof(double) * (size_t)(D * M));
     for (int64_t i = 0; i < N; ++i) {
         const double *ki = k + i * D, *vi = v + i * M, *qi = q + i * D;
         /* state update: S += k_i v_i^T */
@@ -69,14 +83,19 @@ static void fwd_slice(const double *q, const double *k, const double *v,
             for (int64_t m = 0; m < M; ++m) oi[m] += qd * Sd[m];
         }
     }
+    if (SN) memcpy(SN, S, sizeof(double) * (size_t)(D * M));
 }
 
-/* Backward on one (b,h) slice. */
+/* Backward on one (b,h) slice.  S0 and dSN (may be NULL: zero) are the
+ * initial state and the gradient of the final state; dS0 (when not NULL)
+ * receives the gradient of the initial state. */
 static void bwd_slice(const double *q, const double *k, const double *v,
                       const double *g, double *dq, double *dk, double *dv,
-                      double *S, int64_t N, int64_t D, int64_t M) {
-    /* forward sweep: S_i = sum_{j<=i} k_j v_j^T ; dq_i = S_i g_i */
-    memset(S, 0, sizeof(double) * (size_t)(D * M));
+                      double *S, const double *S0, const double *dSN, double *dS0,
+                      int64_t N, int64_t D, int64_t M) {
+    /* forward sweep: S_i = S_0 + sum_{j<=i} k_j v_j^T ; dq_i = S_i g_i */
+    if (S0) memcpy(S, S0, sizeof(double) * (size_t)(D * M));
+    else memset(S, 0, sizeof(double) * (size_t)(D * M));
     for (int64_t i = 0; i < N; ++i) {
         const double *ki = k + i * D, *vi = v + i * M, *gi = g + i * M;
         for (int64_t d = 0; d < D; ++d) {
@@ -92,9 +111,10 @@ static void bwd_slice(const double *q, const double *k, const double *v,
             dqi[d] = acc;
         }
     }
-    /* reverse sweep: R_j = sum_{i>=j} q_i g_i^T ; dk_j = R_j v_j ; dv_j = R_j^T k_j */
+    /* reverse sweep: R_j = dS_N + sum_{i>=j} q_i g_i^T ; dk_j = R_j v_j ; dv_j = R_j^T k_j */
     double *R = S;
-    memset(R, 0, sizeof(double) * (size_t)(D * M));
+    if (dSN) memcpy(R, dSN, sizeof(double) * (size_t)(D * M));
+    else memset(R, 0, sizeof(double) * (size_t)(D * M));
     for (int64_t j = N - 1; j >= 0; --j) {
         const double *qj = q + j * D, *gj = g + j * M;
         const double *kj = k + j * D, *vj = v + j * M;
@@ -118,6 +138,8 @@ static void bwd_slice(const double *q, const double *k, const double *v,
             for (int64_t m = 0; m < M; ++m) dvj[m] += kd * Rd[m];
         }
     }
+    /* dS_0 = R_0 */
+    if (dS0) memcpy(dS0, R, sizeof(double) * (size_t)(D * M));
 }
 
 static int set_threads(int nthreads) {
@@ -134,12 +156,15 @@ static int set_threads(int nthreads) {
  * (<= 0 means the OpenMP default). */
 int cpo_threads(int nthreads) { return set_threads(nthreads); }
 
-/* Forward over BH slices.  Returns 0 on success, -1 on a bad argument,
- * -2 when a scratch allocation fails. */
-int cpo_fwd(const float *q, const float *k, const float *v, double *out,
-            int64_t BH, int64_t N, int64_t D, int64_t M, int nthreads) {
+/* Forward over BH slices.  state_in [BH][D][M] (may be NULL: zero) is the
+ * initial state of every slice, state_out [BH][D][M] (may be NULL) receives
+ * the final state.  Returns 0 on success, -1 on a bad argument, -2 when a
+ * scratch allocation fails. */
+int cpo_fwd_state(const float *q, const float *k, const float *v, double *out,
+                  const double *state_in, double *state_out,
+                  int64_t BH, int64_t N, int64_t D, int64_t M, int nthreads) {
     if (BH < 0 || N < 0 || D <= 0 || M <= 0) return -1;
-    if (BH == 0 || N == 0) return 0;
+    if (BH == 0) return 0;
     set_threads(nthreads);
     int err = 0;
 #pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
@@ -150,18 +175,29 @@ int cpo_fwd(const float *q, const float *k, const float *v, double *out,
         widen(q + bh * N * D, qd, N * D);
         widen(k + bh * N * D, kd, N * D);
         widen(v + bh * N * M, vd, N * M);
-        fwd_slice(qd, kd, vd, out + bh * N * M, S, N, D, M);
+        fwd_slice(qd, kd, vd, out + bh * N * M, S, state_in ? state_in + bh * D * M : NULL,
+                  state_out ? state_out + bh * D * M : NULL, N, D, M);
         free(buf);
     }
     return err ? -2 : 0;
 }
 
-/* Backward over BH slices: g is dL/dout; writes dq, dk, dv. */
-int cpo_bwd(const float *q, const float *k, const float *v, const float *g,
-            double *dq, double *dk, double *dv,
+/* Forward over BH slices without carried state. */
+int cpo_fwd(const float *q, const float *k, const float *v, double *out,
             int64_t BH, int64_t N, int64_t D, int64_t M, int nthreads) {
+    if (N == 0) return (BH < 0 || D <= 0 || M <= 0) ? -1 : 0;
+    return cpo_fwd_state(q, k, v, out, NULL, NULL, BH, N, D, M, nthreads);
+}
+
+/* Backward over BH slices: g is dL/dout; writes dq, dk, dv.  state_in and
+ * grad_state_out [BH][D][M] (may be NULL: zero) are the initial state and
+ * dL/dS_N; grad_state_in (may be NULL) receives dL/dS_0. */
+int cpo_bwd_state(const float *q, const float *k, const float *v, const float *g,
+                  const double *state_in, const double *grad_state_out,
+                  double *dq, double *dk, double *dv, double *grad_state_in,
+                  int64_t BH, int64_t N, int64_t D, int64_t M, int nthreads) {
     if (BH < 0 || N < 0 || D <= 0 || M <= 0) return -1;
-    if (BH == 0 || N == 0) return 0;
+    if (BH == 0) return 0;
     set_threads(nthreads);
     int err = 0;
 #pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
@@ -174,9 +210,19 @@ int cpo_bwd(const float *q, const float *k, const float *v, const float *g,
         widen(k + bh * N * D, kd, N * D);
         widen(v + bh * N * M, vd, N * M);
         widen(g + bh * N * M, gd, N * M);
-        bwd_slice(qd, kd, vd, gd, dq + bh * N * D, dk + bh * N * D, dv + bh * N * M,
-                  S, N, D, M);
+        bwd_slice(qd, kd, vd, gd, dq + bh * N * D, dk + bh * N * D, dv + bh * N * M, S,
+                  state_in ? state_in + bh * D * M : NULL,
+                  grad_state_out ? grad_state_out + bh * D * M : NULL,
+                  grad_state_in ? grad_state_in + bh * D * M : NULL, N, D, M);
         free(buf);
     }
     return err ? -2 : 0;
+}
+
+/* Backward over BH slices without carried state. */
+int cpo_bwd(const float *q, const float *k, const float *v, const float *g,
+            double *dq, double *dk, double *dv,
+            int64_t BH, int64_t N, int64_t D, int64_t M, int nthreads) {
+    if (N == 0) return (BH < 0 || D <= 0 || M <= 0) ? -1 : 0;
+    return cpo_bwd_state(q, k, v, g, NULL, NULL, dq, dk, dv, NULL, BH, N, D, M, nthreads);
 }

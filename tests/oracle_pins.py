@@ -1,7 +1,8 @@
 """Pins for the causal-product oracle.
 
-Each pin checks an implementation ``impl`` (an object with ``fwd(q,k,v)``
-and ``bwd(q,k,v,g)`` returning float64 numpy arrays, like ``oracle``)
+Each pin checks an implementation ``impl`` (an object with ``fwd(q,k,v)``,
+``bwd(q,k,v,g)``, ``fwd_state(q,k,v,s0)`` and ``bwd_state(q,k,v,g,s0,ds_n)``
+returning float64 numpy arrays, like ``oracle``)
 against something other than the recurrence itself: hand-worked values,
 a brute-force quadratic form, closed forms, textbook special cases,
 linearity, causality and finite differences.  ``tests/test_oracle.py``
@@ -249,7 +250,93 @@ def pin_bwd_identities(impl):
     assert _rel(dk, f(impl.fwd(f(v), f(g), f(q)))) <= 1e-13, "dk identity"
 
 
+# --------------------------------------------------------------------------
+# carried-state pins: impl.fwd_state(q, k, v, s0) -> (out, s_n) and
+# impl.bwd_state(q, k, v, g, s0, ds_n) -> (dq, dk, dv, ds0)
+# --------------------------------------------------------------------------
+
+def _state_case(seed, shape=(1, 2, 23, 6, 4)):
+    B, H, N, D, M = shape
+    rng = _rng(seed)
+    q, k = _pos(rng, (B, H, N, D)), _pos(rng, (B, H, N, D))
+    v = rng.standard_normal((B, H, N, M)).astype(np.float32)
+    g = rng.standard_normal((B, H, N, M)).astype(np.float32)
+    s0 = rng.standard_normal((B, H, D, M)).astype(np.float32)
+    ds_n = rng.standard_normal((B, H, D, M)).astype(np.float32)
+    return q, k, v, g, s0, ds_n
+
+
+def pin_state_closed_forms(impl):
+    """With an initial state S_0 and a final-state gradient dS_N (numpy
+    products in float64 on the right-hand sides):
+      S_N = S_0 + K^T V;  out(S_0) = out(0) + Q S_0 row by row;
+      dS_0 = dS_N + Q^T G;  dq(S_0) = dq(0) + G S_0^T;
+      dk(dS_N) = dk(0) + V dS_N^T;  dv(dS_N) = dv(0) + K dS_N."""
+    q, k, v, g, s0, ds_n = _state_case(16)
+    f64 = lambda x: x.astype(np.float64)
+    out, s_n = impl.fwd_state(q, k, v, s0)
+    assert _rel(s_n, f64(s0) + np.einsum("bhnd,bhnm->bhdm", f64(k), f64(v))) <= 1e-12, "S_N"
+    assert _rel(out, impl.fwd(q, k, v) + np.einsum("bhnd,bhdm->bhnm", f64(q), f64(s0))) <= 1e-12, \
+        "out with S_0"
+    dq, dk, dv, ds0 = impl.bwd_state(q, k, v, g, s0, ds_n)
+    dq0, dk0, dv0 = impl.bwd(q, k, v, g)
+    assert _rel(ds0, f64(ds_n) + np.einsum("bhnd,bhnm->bhdm", f64(q), f64(g))) <= 1e-12, "dS_0"
+    assert _rel(dq, dq0 + np.einsum("bhnm,bhdm->bhnd", f64(g), f64(s0))) <= 1e-12, "dq with S_0"
+    assert _rel(dk, dk0 + np.einsum("bhdm,bhnm->bhnd", f64(ds_n), f64(v))) <= 1e-12, "dk with dS_N"
+    assert _rel(dv, dv0 + np.einsum("bhdm,bhnd->bhnm", f64(ds_n), f64(k))) <= 1e-12, "dv with dS_N"
+
+
+def pin_state_chunking(impl, cut=16):
+    """Splitting the sequence and handing the state on reproduces the whole
+    sequence exactly: the forward runs chunk 1 then chunk 2 from its final
+    state; the backward runs chunk 2 (final-state gradient dS_N) then chunk
+    1 with chunk 2's dS_0 as its final-state gradient."""
+    q, k, v, g, s0, ds_n = _state_case(17)
+    parts = lambda x: (np.ascontiguousarray(x[..., :cut, :]), np.ascontiguousarray(x[..., cut:, :]))
+    (q1, q2), (k1, k2), (v1, v2), (g1, g2) = parts(q), parts(k), parts(v), parts(g)
+    out, s_n = impl.fwd_state(q, k, v, s0)
+    o1, s1 = impl.fwd_state(q1, k1, v1, s0)
+    o2, s2 = impl.fwd_state(q2, k2, v2, s1)
+    assert np.array_equal(np.concatenate([o1, o2], axis=-2), out), "chunked out"
+    assert np.array_equal(s2, s_n), "chunked S_N"
+    full = impl.bwd_state(q, k, v, g, s0, ds_n)
+    dq2, dk2, dv2, ds_mid = impl.bwd_state(q2, k2, v2, g2, s1, ds_n)
+    dq1, dk1, dv1, ds0 = impl.bwd_state(q1, k1, v1, g1, s0, ds_mid)
+    for name, a, b in (("dq", (dq1, dq2), full[0]), ("dk", (dk1, dk2), full[1]),
+                       ("dv", (dv1, dv2), full[2])):
+        assert np.array_equal(np.concatenate(a, axis=-2), b), ("chunked", name)
+    assert np.array_equal(ds0, full[3]), "chunked dS_0"
+
+
+def pin_state_finite_differences(impl, shape=(1, 1, 6, 3, 2)):
+    """Central differences of L = <g, out> + <dS_N, S_N> in every coordinate
+    of S_0, k and v (L is linear in each, dyadic inputs: exact)."""
+    B, H, N, D, M = shape
+    rng = _rng(18)
+    q, k = _dyadic(rng, (B, H, N, D)), _dyadic(rng, (B, H, N, D))
+    v, g = _dyadic(rng, (B, H, N, M)), _dyadic(rng, (B, H, N, M))
+    s0, ds_n = _dyadic(rng, (B, H, D, M)), _dyadic(rng, (B, H, D, M))
+    dq, dk, dv, ds0 = impl.bwd_state(q, k, v, g, s0, ds_n)
+
+    def loss(kk, vv, ss):
+        out, s_n = impl.fwd_state(q, kk, vv, ss)
+        return float(np.sum(out * g.astype(np.float64)) + np.sum(s_n * ds_n.astype(np.float64)))
+
+    for name, x, grad in (("k", k, dk), ("v", v, dv), ("s0", s0, ds0)):
+        fd = np.zeros(x.shape, np.float64)
+        for idx in np.ndindex(*x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += 1.0
+            xm[idx] -= 1.0
+            args = {"k": k, "v": v, "s0": s0}
+            ap, am = dict(args), dict(args)
+            ap[name], am[name] = xp, xm
+            fd[idx] = (loss(ap["k"], ap["v"], ap["s0"]) - loss(am["k"], am["v"], am["s0"])) / 2.0
+        assert np.allclose(grad, fd, rtol=1e-12, atol=1e-12), ("state finite differences", name)
+
+
 FWD_PINS = [pin_golden, pin_brute_force, pin_first_row_closed_form, pin_last_row_is_noncausal,
             pin_scalar_cumsum, pin_ones_cumsum, pin_zero_value, pin_linearity, pin_causality]
 BWD_PINS = [pin_finite_differences, pin_bwd_brute_force, pin_bwd_identities]
-ALL_PINS = FWD_PINS + BWD_PINS
+STATE_PINS = [pin_state_closed_forms, pin_state_chunking, pin_state_finite_differences]
+ALL_PINS = FWD_PINS + BWD_PINS + STATE_PINS

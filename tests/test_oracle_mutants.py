@@ -30,9 +30,9 @@ MUTANTS = {
     "exclusive_prefix": [
         ("/* readout: out_i = S^T q_i */",
          "for (int64_t d = 0; d < D; ++d) for (int64_t m = 0; m < M; ++m) S[d * M + m] -= ki[d] * vi[m];"),
-        ("for (int64_t m = 0; m < M; ++m) oi[m] += qd * Sd[m];\n        }\n    }\n}",
+        ("for (int64_t m = 0; m < M; ++m) oi[m] += qd * Sd[m];\n        }\n    }\n    if (SN)",
          "for (int64_t m = 0; m < M; ++m) oi[m] += qd * Sd[m];\n        }\n"
-         "        for (int64_t d = 0; d < D; ++d) for (int64_t m = 0; m < M; ++m) S[d * M + m] += ki[d] * vi[m];\n    }\n}")],
+         "        for (int64_t d = 0; d < D; ++d) for (int64_t m = 0; m < M; ++m) S[d * M + m] += ki[d] * vi[m];\n    }\n    if (SN)")],
     # dq with the value instead of the output gradient
     "dq_uses_v": [("acc += Sd[m] * gi[m];", "acc += Sd[m] * vi[m];")],
     # reverse sweep skips row 0
@@ -44,6 +44,22 @@ MUTANTS = {
     # dk reads the state transposed (indices kept in bounds for any D, M)
     "dk_transposed": [("for (int64_t m = 0; m < M; ++m) acc += Rd[m] * vj[m];",
                        "for (int64_t m = 0; m < M; ++m) acc += R[(m % D) * M + (d % M)] * vj[m];")],
+    # the forward ignores the initial state
+    "fwd_ignores_state_in": [("/* start from the initial state */\n    if (S0)",
+                              "/* start from the initial state */\n    if (0)")],
+    # dq's forward sweep ignores the initial state
+    "dq_ignores_state_in": [("dq_i = S_i g_i */\n    if (S0)", "dq_i = S_i g_i */\n    if (0)")],
+    # the reverse sweep ignores the final-state gradient
+    "reverse_ignores_grad_state": [("if (dSN) memcpy(R, dSN,", "if (0) memcpy(R, dSN,")],
+    # the final state is the sum without the initial state
+    "state_out_drops_state_in": [("    if (SN) memcpy(SN, S, sizeof(double) * (size_t)(D * M));",
+                                  "    if (SN) { memcpy(SN, S, sizeof(double) * (size_t)(D * M));"
+                                  " if (S0) for (int64_t e = 0; e < D * M; ++e) SN[e] -= S0[e]; }")],
+    # dS_0 is taken before the last row of the reverse sweep
+    "grad_state_in_misses_row0": [("    /* dS_0 = R_0 */\n    if (dS0) memcpy(dS0, R, sizeof(double) * (size_t)(D * M));",
+                                   "    /* dS_0 = R_0 */\n    if (dS0) { memcpy(dS0, R, sizeof(double) * (size_t)(D * M));"
+                                   " for (int64_t d = 0; d < D; ++d) for (int64_t m = 0; m < M; ++m)"
+                                   " dS0[d * M + m] -= q[d] * g[m]; }")],
 }
 
 
@@ -53,6 +69,8 @@ class _Impl:
         i64, p, c_int = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
         lib.cpo_fwd.argtypes = [p, p, p, p, i64, i64, i64, i64, c_int]
         lib.cpo_bwd.argtypes = [p, p, p, p, p, p, p, i64, i64, i64, i64, c_int]
+        lib.cpo_fwd_state.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, c_int]
+        lib.cpo_bwd_state.argtypes = [p, p, p, p, p, p, p, p, p, p, i64, i64, i64, i64, c_int]
         self.lib = lib
 
     def fwd(self, q, k, v):
@@ -76,6 +94,34 @@ class _Impl:
                               dq.ctypes.data, dk.ctypes.data, dv.ctypes.data, BH, N, D, M, 1)
         assert rc == 0
         return dq, dk, dv
+
+
+    def fwd_state(self, q, k, v, s0):
+        q, k, v = (np.ascontiguousarray(x, np.float32) for x in (q, k, v))
+        lead = q.shape[:-2]
+        BH = int(np.prod(lead)) if lead else 1
+        N, D, M = q.shape[-2], q.shape[-1], v.shape[-1]
+        s0 = np.ascontiguousarray(s0, np.float64)
+        out, s_n = np.zeros(lead + (N, M)), np.zeros(lead + (D, M))
+        rc = self.lib.cpo_fwd_state(q.ctypes.data, k.ctypes.data, v.ctypes.data, out.ctypes.data,
+                                    s0.ctypes.data, s_n.ctypes.data, BH, N, D, M, 1)
+        assert rc == 0
+        return out, s_n
+
+    def bwd_state(self, q, k, v, g, s0, ds_n):
+        q, k, v, g = (np.ascontiguousarray(x, np.float32) for x in (q, k, v, g))
+        lead = q.shape[:-2]
+        BH = int(np.prod(lead)) if lead else 1
+        N, D, M = q.shape[-2], q.shape[-1], v.shape[-1]
+        s0, ds_n = (np.ascontiguousarray(x, np.float64) for x in (s0, ds_n))
+        dq, dk, dv = np.zeros(lead + (N, D)), np.zeros(lead + (N, D)), np.zeros(lead + (N, M))
+        ds0 = np.zeros(lead + (D, M))
+        rc = self.lib.cpo_bwd_state(q.ctypes.data, k.ctypes.data, v.ctypes.data, g.ctypes.data,
+                                    s0.ctypes.data, ds_n.ctypes.data, dq.ctypes.data,
+                                    dk.ctypes.data, dv.ctypes.data, ds0.ctypes.data,
+                                    BH, N, D, M, 1)
+        assert rc == 0
+        return dq, dk, dv, ds0
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
