@@ -114,6 +114,41 @@ CP_API cp_status_t causal_product_bwd(const void* q, const void* k, const void* 
                                       cp_dtype_t dtype, void* workspace, size_t workspace_bytes,
                                       void* stream);
 
+/* Forward with a carried state.  The recurrence of triton-lang/triton issue
+ * #217 keeps its state across the sequence, and the Triton port there takes
+ * that state as an argument; these entry points let a sequence be processed
+ * in pieces (or continue from a cache) by handing the state on:
+ *     S_i = S_0 + sum_{j<=i} k_j v_j^T,   out_i = S_i^T q_i,
+ *     S_N = S_0 + sum_j k_j v_j^T.
+ * state_in  [B,H,D,M] fp32, row-major (d, m): S_0; NULL means zero.
+ * state_out [B,H,D,M] fp32: receives S_N; NULL means not written.
+ * Both are device pointers, 16-byte aligned; state_out must not overlap any
+ * other argument.  Everything else as causal_product_fwd, which is this call
+ * with both states NULL.  With N = 0, state_out = state_in. */
+CP_API cp_status_t causal_product_fwd_state(const void* q, const void* k, const void* v, void* out,
+                                            const float* state_in, float* state_out,
+                                            int64_t B, int64_t H, int64_t N, int64_t D, int64_t M,
+                                            cp_dtype_t dtype, void* workspace,
+                                            size_t workspace_bytes, void* stream);
+
+/* Backward of causal_product_fwd_state.  With L = sum_i <grad_out_i, out_i>
+ * + <grad_state_out, S_N>:
+ *     grad_q_i = S_i grad_out_i,                  (S_i includes S_0)
+ *     R_j = grad_state_out + sum_{i>=j} q_i grad_out_i^T,
+ *     grad_k_j = R_j v_j,   grad_v_j = R_j^T k_j,   grad_state_in = R_0.
+ * state_in is the forward's S_0 (NULL: zero), grad_state_out = dL/dS_N
+ * (NULL: zero), grad_state_in receives dL/dS_0 (NULL: not written); all
+ * [B,H,D,M] fp32 device pointers, 16-byte aligned, outputs overlapping
+ * nothing.  causal_product_bwd is this call with all three NULL.  With
+ * N = 0, grad_state_in = grad_state_out. */
+CP_API cp_status_t causal_product_bwd_state(const void* q, const void* k, const void* v,
+                                            const void* grad_out, const float* state_in,
+                                            const float* grad_state_out, void* grad_q,
+                                            void* grad_k, void* grad_v, float* grad_state_in,
+                                            int64_t B, int64_t H, int64_t N, int64_t D, int64_t M,
+                                            cp_dtype_t dtype, void* workspace,
+                                            size_t workspace_bytes, void* stream);
+
 /* Size of the static device scratch array behind causal_product_fwd_noalloc. */
 #define CP_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 

@@ -67,6 +67,12 @@ def load_library(rebuild: bool = True) -> ctypes.CDLL:
             lib.causal_product_bwd.argtypes = [p, p, p, p, p, p, p, i64, i64, i64, i64, i64, c_int,
                                                p, sz, p]
             lib.causal_product_bwd.restype = c_int
+            lib.causal_product_fwd_state.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, i64,
+                                                     c_int, p, sz, p]
+            lib.causal_product_fwd_state.restype = c_int
+            lib.causal_product_bwd_state.argtypes = [p, p, p, p, p, p, p, p, p, p, i64, i64, i64,
+                                                     i64, i64, c_int, p, sz, p]
+            lib.causal_product_bwd_state.restype = c_int
             lib.causal_product_fwd_noalloc.argtypes = [p, p, p, p, i64, i64, i64, i64, i64, c_int,
                                                        p]
             lib.causal_product_fwd_noalloc.restype = c_int
@@ -126,26 +132,48 @@ def _workspace(nbytes: int, device) -> torch.Tensor:
     return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
 
+def _state_arg(t: Optional[torch.Tensor], shape, device, name: str) -> int:
+    """Device pointer of an optional fp32 [B,H,D,M] state tensor (0 if None)."""
+    if t is None:
+        return 0
+    if t.dtype != torch.float32 or tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must be float32 of shape {tuple(shape)}; "
+                         f"got {t.dtype} {tuple(t.shape)}")
+    if t.device != device or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous tensor on {device}")
+    return t.data_ptr()
+
+
 def causal_product_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                        out: Optional[torch.Tensor] = None,
                        workspace: Optional[torch.Tensor] = None,
-                       stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
-    """out[b,h,i] = sum_{j<=i} (q[b,h,i] . k[b,h,j]) v[b,h,j], enqueued on ``stream``."""
+                       stream: Optional[torch.cuda.Stream] = None,
+                       state_in: Optional[torch.Tensor] = None,
+                       return_state: bool = False):
+    """out[b,h,i] = (S_0 + sum_{j<=i} k[b,h,j] v[b,h,j]^T)^T q[b,h,i], enqueued
+    on ``stream``.  ``state_in`` is S_0 (float32 [B,H,D,M], None = zero);
+    with ``return_state`` the result is (out, S_N), S_N the state after the
+    last row."""
     B, H, N, D, M = _dims(q, k, v)
     code = _dtype_code(q, k, v)
     if out is None:
         out = torch.empty((B, H, N, M), dtype=q.dtype, device=q.device)
     _check_device(q, k, v, out)
+    state_out = (torch.empty((B, H, D, M), dtype=torch.float32, device=q.device)
+                 if return_state else None)
     lib = load_library()
     need = lib.causal_product_workspace_size(B, H, N, D, M, code, 0)
     if workspace is None:
         workspace = _workspace(need, q.device)
-    rc = lib.causal_product_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                                B, H, N, D, M, code, workspace.data_ptr(), workspace.numel(),
-                                _stream_ptr(stream, q.device))
+    rc = lib.causal_product_fwd_state(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+        _state_arg(state_in, (B, H, D, M), q.device, "state_in"),
+        _state_arg(state_out, (B, H, D, M), q.device, "state_out"),
+        B, H, N, D, M, code, workspace.data_ptr(), workspace.numel(),
+        _stream_ptr(stream, q.device))
     if rc != CP_OK:
         raise CausalProductError(rc, "causal_product_fwd")
-    return out
+    return (out, state_out) if return_state else out
 
 
 def causal_product_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
@@ -175,8 +203,13 @@ def causal_product_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, grad_o
                        grad_k: Optional[torch.Tensor] = None,
                        grad_v: Optional[torch.Tensor] = None,
                        workspace: Optional[torch.Tensor] = None,
-                       stream: Optional[torch.cuda.Stream] = None):
-    """(dq, dk, dv) of L = <grad_out, causal_product(q, k, v)>."""
+                       stream: Optional[torch.cuda.Stream] = None,
+                       state_in: Optional[torch.Tensor] = None,
+                       grad_state_out: Optional[torch.Tensor] = None,
+                       return_state_grad: bool = False):
+    """(dq, dk, dv) of L = <grad_out, out> + <grad_state_out, S_N> for the
+    forward from ``state_in`` (S_0; both float32 [B,H,D,M], None = zero).
+    With ``return_state_grad`` the result is (dq, dk, dv, dL/dS_0)."""
     B, H, N, D, M = _dims(q, k, v)
     code = _dtype_code(q, k, v, grad_out)
     if grad_out.shape != v.shape:
@@ -185,16 +218,25 @@ def causal_product_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, grad_o
     grad_k = torch.empty_like(k) if grad_k is None else grad_k
     grad_v = torch.empty_like(v) if grad_v is None else grad_v
     _check_device(q, k, v, grad_out, grad_q, grad_k, grad_v)
+    grad_state_in = (torch.empty((B, H, D, M), dtype=torch.float32, device=q.device)
+                     if return_state_grad else None)
     lib = load_library()
     need = lib.causal_product_workspace_size(B, H, N, D, M, code, 1)
     if workspace is None:
         workspace = _workspace(need, q.device)
-    rc = lib.causal_product_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), grad_out.data_ptr(),
-                                grad_q.data_ptr(), grad_k.data_ptr(), grad_v.data_ptr(),
-                                B, H, N, D, M, code, workspace.data_ptr(), workspace.numel(),
-                                _stream_ptr(stream, q.device))
+    shape = (B, H, D, M)
+    rc = lib.causal_product_bwd_state(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), grad_out.data_ptr(),
+        _state_arg(state_in, shape, q.device, "state_in"),
+        _state_arg(grad_state_out, shape, q.device, "grad_state_out"),
+        grad_q.data_ptr(), grad_k.data_ptr(), grad_v.data_ptr(),
+        _state_arg(grad_state_in, shape, q.device, "grad_state_in"),
+        B, H, N, D, M, code, workspace.data_ptr(), workspace.numel(),
+        _stream_ptr(stream, q.device))
     if rc != CP_OK:
         raise CausalProductError(rc, "causal_product_bwd")
+    if return_state_grad:
+        return grad_q, grad_k, grad_v, grad_state_in
     return grad_q, grad_k, grad_v
 
 
@@ -220,6 +262,35 @@ class CausalProduct(torch.autograd.Function):
         return causal_product_bwd(q, k, v, g.contiguous().to(q.dtype))
 
 
-def causal_product(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor) -> torch.Tensor:
-    """Causal dot product with autograd support (no normaliser, no scale)."""
-    return CausalProduct.apply(q, k, v)
+class CausalProductState(torch.autograd.Function):
+    """Autograd wrapper with a carried state: (q, k, v, S_0) -> (out, S_N)."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, state):
+        q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+        state = None if state is None else state.contiguous()
+        ctx.save_for_backward(q, k, v, state)
+        ctx.has_state = state is not None
+        return causal_product_fwd(q, k, v, state_in=state, return_state=True)
+
+    @staticmethod
+    def backward(ctx, g, g_state):
+        q, k, v, state = ctx.saved_tensors
+        g = torch.zeros_like(v) if g is None else g.contiguous().to(q.dtype)
+        g_state = None if g_state is None else g_state.contiguous().float()
+        dq, dk, dv, ds = causal_product_bwd(q, k, v, g, state_in=state if ctx.has_state else None,
+                                            grad_state_out=g_state, return_state_grad=True)
+        return dq, dk, dv, (ds if ctx.has_state else None)
+
+
+def causal_product(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                   state: Optional[torch.Tensor] = None, return_state: bool = False):
+    """Causal dot product with autograd support (no normaliser, no scale).
+
+    ``state`` (float32 [B,H,D,M]) is the state before the first row; with
+    ``return_state`` the result is (out, state after the last row), both
+    differentiable."""
+    if state is None and not return_state:
+        return CausalProduct.apply(q, k, v)
+    out, s_n = CausalProductState.apply(q, k, v, state)
+    return (out, s_n) if return_state else out

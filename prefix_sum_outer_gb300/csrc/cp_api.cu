@@ -14,7 +14,17 @@ constexpr size_t kAlign = 256;
 
 size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
+// (a null pointer counts as aligned: optional arguments are checked this way)
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// With no rows, the carried state passes through unchanged (zero when absent).
+cp_status_t pass_state(const float* from, float* to, size_t bytes, cudaStream_t stream) {
+  if (to == nullptr) return CP_OK;
+  const cudaError_t e = from != nullptr
+                            ? cudaMemcpyAsync(to, from, bytes, cudaMemcpyDeviceToDevice, stream)
+                            : cudaMemsetAsync(to, 0, bytes, stream);
+  return e == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+}
 
 cp_status_t check_dims(int64_t B, int64_t H, int64_t N, int64_t D, int64_t M, cp_dtype_t dtype) {
   if (B <= 0 || H <= 0 || N < 0) return CP_ERR_INVALID_ARG;
@@ -84,6 +94,7 @@ cp_status_t acquire(Scratch& s, void* workspace, size_t workspace_bytes, size_t 
 }
 
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  if (a == nullptr || b == nullptr || na == 0 || nb == 0) return false;
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
   return x < y + nb && y < x + na;
 }
@@ -99,24 +110,33 @@ size_t causal_product_workspace_size(int64_t B, int64_t H, int64_t N, int64_t D,
   return cp::workspace_bytes(B * H, N, D, M, dtype, backward != 0);
 }
 
-cp_status_t causal_product_fwd(const void* q, const void* k, const void* v, void* out, int64_t B,
-                               int64_t H, int64_t N, int64_t D, int64_t M, cp_dtype_t dtype,
-                               void* workspace, size_t workspace_bytes, void* stream_) {
+cp_status_t causal_product_fwd_state(const void* q, const void* k, const void* v, void* out,
+                                     const float* state_in, float* state_out, int64_t B,
+                                     int64_t H, int64_t N, int64_t D, int64_t M,
+                                     cp_dtype_t dtype, void* workspace, size_t workspace_bytes,
+                                     void* stream_) {
   cp_status_t st = cp::check_dims(B, H, N, D, M, dtype);
   if (st != CP_OK) return st;
-  if (!q || !k || !v || !out) return CP_ERR_INVALID_ARG;
-  if (!cp::aligned16(q) || !cp::aligned16(k) || !cp::aligned16(v) || !cp::aligned16(out))
+  // with no rows nothing is read or written but the states
+  if (N > 0 && (!q || !k || !v || !out)) return CP_ERR_INVALID_ARG;
+  if (!cp::aligned16(q) || !cp::aligned16(k) || !cp::aligned16(v) || !cp::aligned16(out) ||
+      !cp::aligned16(state_in) || !cp::aligned16(state_out))
     return CP_ERR_MISALIGNED;
   const size_t es = dtype == CP_DTYPE_F32 ? 4 : 2;
   const int64_t BH = B * H;
   const size_t nqk = (size_t)BH * N * D * es, nv = (size_t)BH * N * M * es;
+  const size_t nst = (size_t)BH * D * M * sizeof(float);
   if (cp::overlaps(out, nv, q, nqk) || cp::overlaps(out, nv, k, nqk) ||
-      cp::overlaps(out, nv, v, nv))
+      cp::overlaps(out, nv, v, nv) || cp::overlaps(out, nv, state_in, nst))
+    return CP_ERR_INVALID_ARG;
+  if (cp::overlaps(state_out, nst, q, nqk) || cp::overlaps(state_out, nst, k, nqk) ||
+      cp::overlaps(state_out, nst, v, nv) || cp::overlaps(state_out, nst, out, nv) ||
+      cp::overlaps(state_out, nst, state_in, nst))
     return CP_ERR_INVALID_ARG;
   const size_t need = cp::workspace_bytes(BH, N, D, M, dtype, false);
   if (workspace != nullptr && workspace_bytes < need) return CP_ERR_WORKSPACE_TOO_SMALL;
-  if (N == 0) return CP_OK;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (N == 0) return cp::pass_state(state_in, state_out, nst, stream);
   cp::Scratch s;
   st = cp::acquire(s, workspace, workspace_bytes, need, stream);
   if (st != CP_OK) return st;
@@ -127,36 +147,53 @@ cp_status_t causal_product_fwd(const void* q, const void* k, const void* v, void
   if (s.owned && cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess)
     return CP_ERR_CUDA;
   cp::Product p{q, k, v, out, BH, N, D, M, false};
+  p.state_in = state_in;
+  p.state_out = state_out;
+  p.st_ld_r = M;
+  p.st_ld_c = 1;
   return cp::run_product(p, dtype, agg, status, stream);
 }
 
-cp_status_t causal_product_bwd(const void* q, const void* k, const void* v, const void* grad_out,
-                               void* grad_q, void* grad_k, void* grad_v, int64_t B, int64_t H,
-                               int64_t N, int64_t D, int64_t M, cp_dtype_t dtype, void* workspace,
-                               size_t workspace_bytes, void* stream_) {
+cp_status_t causal_product_fwd(const void* q, const void* k, const void* v, void* out, int64_t B,
+                               int64_t H, int64_t N, int64_t D, int64_t M, cp_dtype_t dtype,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  return causal_product_fwd_state(q, k, v, out, nullptr, nullptr, B, H, N, D, M, dtype,
+                                  workspace, workspace_bytes, stream);
+}
+
+cp_status_t causal_product_bwd_state(const void* q, const void* k, const void* v,
+                                     const void* grad_out, const float* state_in,
+                                     const float* grad_state_out, void* grad_q, void* grad_k,
+                                     void* grad_v, float* grad_state_in, int64_t B, int64_t H,
+                                     int64_t N, int64_t D, int64_t M, cp_dtype_t dtype,
+                                     void* workspace, size_t workspace_bytes, void* stream_) {
   cp_status_t st = cp::check_dims(B, H, N, D, M, dtype);
   if (st != CP_OK) return st;
-  if (!q || !k || !v || !grad_out || !grad_q || !grad_k || !grad_v) return CP_ERR_INVALID_ARG;
-  const void* ptrs[7] = {q, k, v, grad_out, grad_q, grad_k, grad_v};
+  if (N > 0 && (!q || !k || !v || !grad_out || !grad_q || !grad_k || !grad_v))
+    return CP_ERR_INVALID_ARG;
+  const void* ptrs[10] = {q, k, v, grad_out, grad_q, grad_k, grad_v,
+                          state_in, grad_state_out, grad_state_in};
   for (const void* p : ptrs)
     if (!cp::aligned16(p)) return CP_ERR_MISALIGNED;
   const size_t es = dtype == CP_DTYPE_F32 ? 4 : 2;
   const int64_t BH = B * H;
   const size_t nqk = (size_t)BH * N * D * es, nv = (size_t)BH * N * M * es;
-  const void* ins[4] = {q, k, v, grad_out};
-  const size_t in_sz[4] = {nqk, nqk, nv, nv};
-  void* outs[3] = {grad_q, grad_k, grad_v};
-  const size_t out_sz[3] = {nqk, nqk, nv};
-  for (int o = 0; o < 3; ++o) {
-    for (int i = 0; i < 4; ++i)
+  const size_t nst = (size_t)BH * D * M * sizeof(float);
+  const void* ins[6] = {q, k, v, grad_out, state_in, grad_state_out};
+  const size_t in_sz[6] = {nqk, nqk, nv, nv, nst, nst};
+  void* outs[4] = {grad_q, grad_k, grad_v, grad_state_in};
+  const size_t out_sz[4] = {nqk, nqk, nv, nst};
+  for (int o = 0; o < 4; ++o) {
+    for (int i = 0; i < 6; ++i)
       if (cp::overlaps(outs[o], out_sz[o], ins[i], in_sz[i])) return CP_ERR_INVALID_ARG;
-    for (int o2 = o + 1; o2 < 3; ++o2)
+    for (int o2 = o + 1; o2 < 4; ++o2)
       if (cp::overlaps(outs[o], out_sz[o], outs[o2], out_sz[o2])) return CP_ERR_INVALID_ARG;
   }
   const size_t need = cp::workspace_bytes(BH, N, D, M, dtype, true);
   if (workspace != nullptr && workspace_bytes < need) return CP_ERR_WORKSPACE_TOO_SMALL;
-  if (N == 0) return CP_OK;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  // no rows: dL/dS_0 = dL/dS_N
+  if (N == 0) return cp::pass_state(grad_state_out, grad_state_in, nst, stream);
   cp::Scratch s;
   st = cp::acquire(s, workspace, workspace_bytes, need, stream);
   if (st != CP_OK) return st;
@@ -166,24 +203,46 @@ cp_status_t causal_product_bwd(const void* q, const void* k, const void* v, cons
   // keeps its (sticky) status until causal_product_status() reads it
   if (s.owned && cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess)
     return CP_ERR_CUDA;
-  // dq_i = sum_{j<=i} (g_i . v_j) k_j
+  // dq_i = (S_0 + sum_{j<=i} k_j v_j^T) g_i: the forward product (g, v, k),
+  // whose state sum v k^T is the transpose of the caller's S_0
   cp::Product pq{grad_out, v, k, grad_q, BH, N, M, D, false};
-  // dv_j = sum_{i>=j} (k_j . q_i) g_i
+  pq.state_in = state_in;
+  pq.st_ld_r = 1;
+  pq.st_ld_c = M;
+  // dv_j = R_j^T k_j with R_j = dS_N + sum_{i>=j} q_i g_i^T: the reverse
+  // product (k, q, g) with state R; it also hands on dS_0 = R_0
   cp::Product pv{k, q, grad_out, grad_v, BH, N, D, M, true};
-  // dk_j = sum_{i>=j} (v_j . g_i) q_i
+  pv.state_in = grad_state_out;
+  pv.state_out = grad_state_in;
+  pv.st_ld_r = M;
+  pv.st_ld_c = 1;
+  // dk_j = R_j v_j: the reverse product (v, g, q), whose state is R^T
   cp::Product pk{v, grad_out, q, grad_k, BH, N, M, D, true};
+  pk.state_in = grad_state_out;
+  pk.st_ld_r = 1;
+  pk.st_ld_c = M;
   if (dtype == CP_DTYPE_BF16) {
-    // dv and dk share the reverse state sum q g^T: one scan over q, k, v, g
+    // dv and dk share the reverse state R: one scan over q, k, v, g
     const cp::TcPlan plan = cp::tc_plan(BH, N, D, M);
     if (cp::tc_dkdv_supported(plan))
-      return cp::tc_bwd_launch(q, k, v, grad_out, grad_q, grad_k, grad_v, BH, N, D, M, plan, agg,
-                               status, stream);
+      return cp::tc_bwd_launch(q, k, v, grad_out, grad_q, grad_k, grad_v, state_in,
+                               grad_state_out, grad_state_in, BH, N, D, M, plan, agg, status,
+                               stream);
   }
   st = cp::run_product(pq, dtype, agg, status, stream);
   if (st != CP_OK) return st;
   st = cp::run_product(pv, dtype, agg, status, stream);
   if (st == CP_OK) st = cp::run_product(pk, dtype, agg, status, stream);
   return st;
+}
+
+cp_status_t causal_product_bwd(const void* q, const void* k, const void* v, const void* grad_out,
+                               void* grad_q, void* grad_k, void* grad_v, int64_t B, int64_t H,
+                               int64_t N, int64_t D, int64_t M, cp_dtype_t dtype, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  return causal_product_bwd_state(q, k, v, grad_out, nullptr, nullptr, grad_q, grad_k, grad_v,
+                                  nullptr, B, H, N, D, M, dtype, workspace, workspace_bytes,
+                                  stream);
 }
 
 cp_status_t causal_product_status(void* workspace, void* stream_) {

@@ -34,6 +34,14 @@ struct Product {
   void* out;
   int64_t BH, N, D, M;
   bool reverse;
+  // Carried state of the scan (fp32, D x M per problem, may be null): the
+  // state before the first row in scan order, and the state after the last.
+  // Element (r, c) of problem p sits at p * D * M + r * st_ld_r + c * st_ld_c,
+  // so a product whose state is the transpose of the caller's reads it
+  // through swapped strides.
+  const float* state_in = nullptr;
+  float* state_out = nullptr;
+  int64_t st_ld_r = 0, st_ld_c = 0;
 };
 
 // ---- fp32 (SIMT FMA) path
@@ -71,8 +79,12 @@ cp_status_t tc_aggregate(const Product& p, const TcPlan& plan, float* agg, int* 
 // tc_plan(BH, N, D, M)): dq is one product launch; dk and dv share the
 // reverse state sum q g^T and are computed in one scan.
 bool tc_dkdv_supported(const TcPlan& plan);
+// state_in (S_0), grad_state_out (dL/dS_N) and grad_state_in (dL/dS_0) are
+// [BH][D][M] fp32 or null.
 cp_status_t tc_bwd_launch(const void* q, const void* k, const void* v, const void* g, void* dq,
-                          void* dk, void* dv, int64_t BH, int64_t N, int64_t D, int64_t M,
-                          const TcPlan& plan, float* agg, int* status, cudaStream_t stream);
+                          void* dk, void* dv, const float* state_in,
+                          const float* grad_state_out, float* grad_state_in, int64_t BH,
+                          int64_t N, int64_t D, int64_t M, const TcPlan& plan, float* agg,
+                          int* status, cudaStream_t stream);
 
 }  // namespace cp

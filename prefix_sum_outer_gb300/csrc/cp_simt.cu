@@ -32,6 +32,11 @@ struct SimtArgs {
   const float* agg_in;  // [P][G][D][Mb] aggregates (pass 2 reads), may be null
   float* agg_out;       // pass 1 writes
   int agg_only;
+  // carried state (see Product): [BH] x D x M, element (d, m) at
+  // d * st_ld_r + m * st_ld_c; may be null
+  const float* state_in;
+  float* state_out;
+  int64_t st_ld_r, st_ld_c;
 };
 
 __global__ void __launch_bounds__(kThreads) simt_kernel(SimtArgs a) {
@@ -66,9 +71,13 @@ __global__ void __launch_bounds__(kThreads) simt_kernel(SimtArgs a) {
   const float* vb = a.v + (int64_t)bh * a.N * a.M;
   float* ob = a.out + (int64_t)bh * a.N * a.M;
 
-  // initial state: aggregates of the segments before this one in scan order
+  // initial state: the carried state plus the aggregates of the segments
+  // before this one in scan order
+  const float* st_in =
+      (!a.agg_only && a.state_in != nullptr) ? a.state_in + (int64_t)bh * D * a.M : nullptr;
   for (int e = threadIdx.x; e < D * Mb; e += kThreads) {
-    float acc = 0.f;
+    const int d0 = e / Mb, m_ = e % Mb;
+    float acc = (st_in != nullptr && m_ < mw) ? st_in[d0 * a.st_ld_r + (m0 + m_) * a.st_ld_c] : 0.f;
     if (!a.agg_only && a.agg_in != nullptr) {
       const int lo = a.reverse ? s + 1 : 0;
       const int hi = a.reverse ? a.G : s;
@@ -135,6 +144,14 @@ __global__ void __launch_bounds__(kThreads) simt_kernel(SimtArgs a) {
     __syncthreads();
     float* dst = a.agg_out + ((int64_t)pidx * a.G + s) * D * Mb;
     for (int e = threadIdx.x; e < D * Mb; e += kThreads) dst[e] = Ss[e];
+  } else if (a.state_out != nullptr && (a.reverse ? s == 0 : s == a.G - 1)) {
+    // the last segment in scan order hands on its final state
+    __syncthreads();
+    float* st = a.state_out + (int64_t)bh * D * a.M;
+    for (int e = threadIdx.x; e < D * Mb; e += kThreads) {
+      const int d0 = e / Mb, m_ = e % Mb;
+      if (m_ < mw) st[d0 * a.st_ld_r + (m0 + m_) * a.st_ld_c] = Ss[e];
+    }
   }
 }
 
@@ -183,10 +200,15 @@ cudaError_t simt_launch(const Product& p, const SimtPlan& plan, float* agg, int*
   a.BH = (int)p.BH;
   a.seg_rows = plan.seg_rows;
   a.reverse = p.reverse ? 1 : 0;
+  a.state_in = p.state_in;
+  a.state_out = p.state_out;
+  a.st_ld_r = p.st_ld_r;
+  a.st_ld_c = p.st_ld_c;
   const int64_t problems = p.BH * plan.n_mb;
   if (plan.G > 1) {
     a.agg_only = 1;
     a.agg_out = agg;
+    // (the aggregate pass ignores the carried state: agg_only is set)
     simt_kernel<<<(unsigned)(problems * (plan.G - 1)), kThreads, smem, stream>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -12,21 +12,21 @@
 namespace cp {
 namespace tc {
 
-template <int DP, int MB, bool AGG_ONLY>
+template <int DP, int MB, bool AGG_ONLY, bool STATE_OUT>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_o, const Args a) {
-  causal_body<DP, MB, AGG_ONLY>(tm_q, tm_k, tm_v, tm_o, a);
+  causal_body<DP, MB, AGG_ONLY, STATE_OUT>(tm_q, tm_k, tm_v, tm_o, a);
 }
 
 // ------------------------------------------------------------------ host
-template <int DP, int MB, bool AGG>
+template <int DP, int MB, bool AGG, bool STATE_OUT = false>
 cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                        const CUtensorMap& o, const Args& a, unsigned grid, cudaStream_t st) {
   using L = Layout<DP, MB>;
-  auto kern = tc_causal_kernel<DP, MB, AGG>;
+  auto kern = tc_causal_kernel<DP, MB, AGG, STATE_OUT>;
   // the shared-memory opt-in is set once per device for each instantiation
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
@@ -60,12 +60,16 @@ cudaError_t launch_pair(const CUtensorMap& q, const CUtensorMap& k, const CUtens
     Args b = a;
     b.agg_in = nullptr;
     b.agg_out = agg;
+    b.state_in = nullptr;   // aggregates are the segments' own sums
+    b.state_out = nullptr;
     e = launch_one<DP, MB, true>(q, k, v, o, b, (unsigned)(problems * (plan.G - 1)), st);
     if (e != cudaSuccess || agg_only) return e;
     a.agg_in = agg;
   } else if (agg_only) {
     return cudaSuccess;
   }
+  if (a.state_out != nullptr)
+    return launch_one<DP, MB, false, true>(q, k, v, o, a, (unsigned)(problems * plan.G), st);
   return launch_one<DP, MB, false>(q, k, v, o, a, (unsigned)(problems * plan.G), st);
 }
 
@@ -112,6 +116,12 @@ cp_status_t tc_run(const Product& p, const TcPlan& plan, float* agg, int* status
   a.n_mb = plan.n_mb;
   a.reverse = p.reverse ? 1 : 0;
   a.status = status;
+  a.state_in = p.state_in;
+  a.state_out = p.state_out;
+  a.st_ld_r = p.st_ld_r;
+  a.st_ld_c = p.st_ld_c;
+  a.Dr = (int)p.D;
+  a.Mc = (int)p.M;
   const int64_t problems = p.BH * plan.n_mb;
   cudaError_t e;
 #define CP_TC_CASE(DP_, MB_)                                                                  \

@@ -69,6 +69,12 @@ struct Args {
   const float* agg_in;   // [P][G][DP][MB]; null when G == 1
   float* agg_out;        // aggregate-only launch writes here
   int* status;
+  // carried state (see Product): read by every segment, written by the last
+  // one in scan order; Dr x Mc per problem
+  const float* state_in;
+  float* state_out;
+  int64_t st_ld_r, st_ld_c;
+  int Dr, Mc;
 };
 
 template <int DP, int MB>
@@ -135,8 +141,10 @@ struct Layout {
 };
 
 // One CTA's work: the scan of one (segment, problem, value block).  The
-// tensor maps are the kernel's __grid_constant__ parameters.
-template <int DP, int MB, bool AGG_ONLY>
+// tensor maps are the kernel's __grid_constant__ parameters.  STATE_OUT:
+// the launch writes the final state (a separate instantiation: the write,
+// though it runs once, costs the whole kernel registers).
+template <int DP, int MB, bool AGG_ONLY, bool STATE_OUT>
 __device__ __forceinline__ void causal_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                             const CUtensorMap& tm_v, const CUtensorMap& tm_o,
                                             const Args& a) {
@@ -185,6 +193,9 @@ __device__ __forceinline__ void causal_body(const CUtensorMap& tm_q, const CUten
   const int pidx = bh * a.n_mb + mb;
   const bool has_prefix =
       !AGG_ONLY && a.agg_in != nullptr && (a.reverse ? (seg < a.G - 1) : (seg > 0));
+  // the state does not start at zero: earlier segments or a carried state
+  const bool has_init = has_prefix || (!AGG_ONLY && a.state_in != nullptr);
+  const bool last_seg = a.reverse ? (seg == 0) : (seg == a.G - 1);
   auto tile_of = [&](int it) { return a.reverse ? (t_end - 1 - it) : (t_first + it); };
 
   if (threadIdx.x == 0) {
@@ -324,7 +335,7 @@ __device__ __forceinline__ void causal_body(const CUtensorMap& tm_q, const CUten
         // the state per 128 columns of K
         const uint32_t kt_lo = desc_lo(qk_addr(it) + L::kQBytes, kBoxBytes);
         const uint32_t v_lo = desc_lo(v_addr(it), kBoxBytes);
-        const bool fresh = (it == 0) && !has_prefix;
+        const bool fresh = (it == 0) && !has_init;
 #pragma unroll
         for (int sb = 0; sb < L::kSBlocks; ++sb) {
 #pragma unroll
@@ -493,10 +504,12 @@ __device__ __forceinline__ void causal_body(const CUtensorMap& tm_q, const CUten
         }
       }
     } else {
-      // initial state: fixed-order sum of the preceding segments' aggregates
-      if (has_prefix) {
-        const int lo = a.reverse ? seg + 1 : 0;
-        const int hi = a.reverse ? a.G : seg;
+      // initial state: the carried state plus the fixed-order sum of the
+      // preceding segments' aggregates
+      if (has_init) {
+        const int lo = has_prefix ? (a.reverse ? seg + 1 : 0) : 0;
+        const int hi = has_prefix ? (a.reverse ? a.G : seg) : 0;
+        const float* st = a.state_in != nullptr ? a.state_in + (int64_t)bh * a.Dr * a.Mc : nullptr;
 #pragma unroll
         for (int sb = 0; sb < L::kSBlocks; ++sb) {
           if (sb * 128 + wq * 32 >= DP) continue;
@@ -504,8 +517,12 @@ __device__ __forceinline__ void causal_body(const CUtensorMap& tm_q, const CUten
 #pragma unroll
           for (int c = 0; c < MB / 32; ++c) {
             float acc[32];
+            // columns m0 + x of row d of the carried state
+            const int m0 = mb * MB + c * 32;
+            const int nm = (st != nullptr && d < a.Dr) ? min(32, a.Mc - m0) : 0;
+            const float* src = st + d * a.st_ld_r + m0 * a.st_ld_c;
 #pragma unroll
-            for (int x = 0; x < 32; ++x) acc[x] = 0.f;
+            for (int x = 0; x < 32; ++x) acc[x] = x < nm ? src[x * a.st_ld_c] : 0.f;
             for (int s2 = lo; s2 < hi; ++s2) {
               const float4* src = reinterpret_cast<const float4*>(
                   a.agg_in + (((size_t)pidx * a.G + s2) * DP + d) * MB + c * 32);
@@ -534,7 +551,7 @@ __device__ __forceinline__ void causal_body(const CUtensorMap& tm_q, const CUten
           ok = false;
           break;
         }
-        if (it == 0 && !has_prefix) {
+        if (it == 0 && !has_init) {
 #pragma unroll
           for (int sb = 0; sb < L::kSBlocks; ++sb) {
             if (sb * 128 + wq * 32 >= DP) continue;
@@ -569,6 +586,32 @@ __device__ __forceinline__ void causal_body(const CUtensorMap& tm_q, const CUten
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(s_ready);
+      }
+      // the last segment in scan order hands on the state after its last tile
+      if (STATE_OUT && ok && last_seg && n_it > 0) {
+        if (!mbar_wait(s_done, (n_it - 1) & 1, abort_flag)) {
+          ok = false;
+        } else {
+          tc_fence_after();
+          float* st = a.state_out + (int64_t)bh * a.Dr * a.Mc;
+#pragma unroll
+          for (int sb = 0; sb < L::kSBlocks; ++sb) {
+            if (sb * 128 + wq * 32 >= DP) continue;  // warp-uniform
+            const int d = sb * 128 + row;
+#pragma unroll 1
+            for (int c = 0; c < MB / 32; ++c) {
+              uint32_t r[32];
+              tmem_ld32(lane_base + L::kColS + sb * MB + c * 32, r);
+              tmem_ld_wait();
+              const int m0 = mb * MB + c * 32;
+              const int nm = d < a.Dr ? min(32, a.Mc - m0) : 0;
+              float* dst = st + d * a.st_ld_r + m0 * a.st_ld_c;
+#pragma unroll
+              for (int x = 0; x < 32; ++x)
+                if (x < nm) dst[x * a.st_ld_c] = __uint_as_float(r[x]);
+            }
+          }
+        }
       }
       if (!ok) record_timeout(a.status, abort_flag);
     }

@@ -16,12 +16,13 @@ namespace cp {
 namespace tc {
 namespace {
 
+template <bool STATE_OUT>
 __global__ void __launch_bounds__(dkdv::kThreads, 1)
     tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                    const __grid_constant__ CUtensorMap tm_dk,
                    const __grid_constant__ CUtensorMap tm_dv, const dkdv::DkdvArgs a) {
-  dkdv::dkdv_body(tm_q, tm_k, tm_v, tm_g, tm_dk, tm_dv, a);
+  dkdv::dkdv_body<STATE_OUT>(tm_q, tm_k, tm_v, tm_g, tm_dk, tm_dv, a);
 }
 
 template <typename Kernel>
@@ -67,8 +68,10 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), unsigned grid, int smem, cudaStre
 }  // namespace
 
 cp_status_t tc_bwd_launch(const void* q, const void* k, const void* v, const void* g, void* dq,
-                          void* dk, void* dv, int64_t BH, int64_t N, int64_t D, int64_t M,
-                          const TcPlan& plan, float* agg, int* status, cudaStream_t stream) {
+                          void* dk, void* dv, const float* state_in,
+                          const float* grad_state_out, float* grad_state_in, int64_t BH,
+                          int64_t N, int64_t D, int64_t M, const TcPlan& plan, float* agg,
+                          int* status, cudaStream_t stream) {
   using namespace tc;
   if (!tc_dkdv_supported(plan)) return CP_ERR_UNSUPPORTED_SHAPE;
   CUtensorMap mq, mk, mv, mg, mdk, mdv;
@@ -84,12 +87,18 @@ cp_status_t tc_bwd_launch(const void* q, const void* k, const void* v, const voi
   a.D = (int)D;
   a.M = (int)M;
   a.agg_in = plan.G > 1 ? agg : nullptr;
+  a.state_in = grad_state_out;
+  a.state_out = grad_state_in;
   a.status = status;
   cudaError_t e;
   // dq_i = sum_{j<=i} (g_i . v_j) k_j: the forward product (g, v, k); then
   // (split problems) the aggregate pass of the state sum q g^T, i.e. of the
   // reverse product with k' = q and v' = g; then the fused dk/dv scan
-  const Product pq{g, v, k, dq, BH, N, M, D, false};
+  Product pq{g, v, k, dq, BH, N, M, D, false};
+  // its state is sum v k^T: the transpose of the caller's S_0
+  pq.state_in = state_in;
+  pq.st_ld_r = 1;
+  pq.st_ld_c = M;
   cp_status_t st = tc_launch(pq, tc_plan(BH, N, M, D), agg, status, stream);
   if (st != CP_OK) return st;
   if (plan.G > 1) {
@@ -97,11 +106,20 @@ cp_status_t tc_bwd_launch(const void* q, const void* k, const void* v, const voi
     st = tc_aggregate(pa, plan, agg, status, stream);
     if (st != CP_OK) return st;
   }
-  static std::atomic<uint64_t> configured{0};
-  e = set_smem_once(tc_dkdv_kernel, dkdv::kSmemBytes, configured);
-  if (e == cudaSuccess)
-    e = launch_pdl(tc_dkdv_kernel, (unsigned)(BH * plan.G), dkdv::kSmemBytes, stream, mq, mk, mv,
-                   mg, mdk, mdv, a);
+  const unsigned grid = (unsigned)(BH * plan.G);
+  if (grad_state_in != nullptr) {
+    static std::atomic<uint64_t> configured{0};
+    e = set_smem_once(tc_dkdv_kernel<true>, dkdv::kSmemBytes, configured);
+    if (e == cudaSuccess)
+      e = launch_pdl(tc_dkdv_kernel<true>, grid, dkdv::kSmemBytes, stream, mq, mk, mv, mg, mdk,
+                     mdv, a);
+  } else {
+    static std::atomic<uint64_t> configured{0};
+    e = set_smem_once(tc_dkdv_kernel<false>, dkdv::kSmemBytes, configured);
+    if (e == cudaSuccess)
+      e = launch_pdl(tc_dkdv_kernel<false>, grid, dkdv::kSmemBytes, stream, mq, mk, mv, mg, mdk,
+                     mdv, a);
+  }
   return e == cudaSuccess ? CP_OK : CP_ERR_CUDA;
 }
 

@@ -69,6 +69,8 @@ struct DkdvArgs {
   int BH;
   int D, M;
   const float* agg_in;  // [BH][G][64][64] per-segment sums of q g^T; null when G == 1
+  const float* state_in;  // [BH][D][M] dL/dS_N seeding R (null: zero)
+  float* state_out;       // [BH][D][M] receives dL/dS_0 = R after row 0 (null: not written)
   int* status;
 };
 
@@ -90,7 +92,9 @@ __device__ __forceinline__ void pack_p_reverse(uint32_t pc, int wq, int lane) {
 }
 
 // One CTA's work: the fused reverse scan of one (segment, problem).  The
-// tensor maps are the kernel's __grid_constant__ parameters.
+// tensor maps are the kernel's __grid_constant__ parameters.  STATE_OUT: the
+// launch writes dL/dS_0 (a separate instantiation, as for the product).
+template <bool STATE_OUT>
 __device__ __forceinline__ void dkdv_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                           const CUtensorMap& tm_v, const CUtensorMap& tm_g,
                                           const CUtensorMap& tm_dk, const CUtensorMap& tm_dv,
@@ -123,6 +127,8 @@ __device__ __forceinline__ void dkdv_body(const CUtensorMap& tm_q, const CUtenso
   const int t_end = min(a.n_tiles, t_first + a.seg_tiles);
   const int n_it = t_end - t_first;
   const bool has_prefix = a.agg_in != nullptr && seg < a.G - 1;
+  // R does not start at zero: later segments or a carried final-state gradient
+  const bool has_init = has_prefix || a.state_in != nullptr;
   auto tile_of = [&](int it) { return t_end - 1 - it; };  // reverse order
 
   if (threadIdx.x == 0) {
@@ -215,7 +221,7 @@ __device__ __forceinline__ void dkdv_body(const CUtensorMap& tm_q, const CUtenso
         const uint32_t base = stage_addr(it);
         const uint32_t qt_lo = desc_lo(base, kBoxBytes);
         const uint32_t g_lo = desc_lo(base + 3 * kBoxBytes, kBoxBytes);
-        const bool fresh = (it == 0) && !has_prefix;
+        const bool fresh = (it == 0) && !has_init;
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           mma_ss_lo<kHi, kHi>(t_s, qt_lo + ((kk * 2048) >> 4), g_lo + ((kk * 2048) >> 4), idesc_s,
@@ -315,15 +321,20 @@ __device__ __forceinline__ void dkdv_body(const CUtensorMap& tm_q, const CUtenso
     // ------------------------------------------------------------ state group
     // Two independent sequences, taken whichever is ready: the bf16 copy of
     // R before each tile, and the packing of P2.
-    if (has_prefix) {
-      // initial state: fixed-order sum of the later segments' aggregates
+    if (has_init) {
+      // initial state: the carried dL/dS_N plus the fixed-order sum of the
+      // later segments' aggregates
       if (wq < 2) {
+        const float* st = a.state_in != nullptr ? a.state_in + (int64_t)bh * a.D * a.M : nullptr;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           float acc[32];
 #pragma unroll
-          for (int x = 0; x < 32; ++x) acc[x] = 0.f;
-          for (int s2 = seg + 1; s2 < a.G; ++s2) {
+          for (int x = 0; x < 32; ++x) {
+            const int m = c * 32 + x;
+            acc[x] = (st != nullptr && row < a.D && m < a.M) ? st[row * a.M + m] : 0.f;
+          }
+          for (int s2 = seg + 1; has_prefix && s2 < a.G; ++s2) {
             const float4* src = reinterpret_cast<const float4*>(
                 a.agg_in + (((size_t)bh * a.G + s2) * kW + row) * kW + c * 32);
 #pragma unroll
@@ -361,7 +372,7 @@ __device__ __forceinline__ void dkdv_body(const CUtensorMap& tm_q, const CUtenso
         if (wq < 2) {  // rows d of R (D <= 64 lanes)
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
-            if (ns == 0 && !has_prefix) {
+            if (ns == 0 && !has_init) {
               store_zero32(sbuf, row, c * 32, kW * 128);
               store_zero32(sbuf + kSOneBytes, row, c * 32, kW * 128);
             } else {
@@ -397,6 +408,26 @@ __device__ __forceinline__ void dkdv_body(const CUtensorMap& tm_q, const CUtenso
         if (*abort_flag || globaltimer() - t0 > CP_WAIT_TIMEOUT_NS) {
           ok = false;
           break;
+        }
+      }
+    }
+    // the first segment (last in scan order) hands on R after row 0: dL/dS_0
+    if (STATE_OUT && ok && seg == 0 && n_it > 0) {
+      if (!mbar_wait(s_done, (n_it - 1) & 1, abort_flag)) {
+        ok = false;
+      } else if (wq < 2) {
+        tc_fence_after();
+        float* st = a.state_out + (int64_t)bh * a.D * a.M;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t r[32];
+          tmem_ld32(lane_base + kColS + c * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int x = 0; x < 32; ++x) {
+            const int m = c * 32 + x;
+            if (row < a.D && m < a.M) st[row * a.M + m] = __uint_as_float(r[x]);
+          }
         }
       }
     }

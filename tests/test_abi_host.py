@@ -133,3 +133,42 @@ def test_python_binding_refuses_cpu_tensors():
     q = torch.ones(1, 1, 4, 16)
     with pytest.raises(RuntimeError):
         cp.causal_product_fwd(q, q, q)
+
+
+def test_state_argument_checks(lib):
+    def fwd_state(**kw):
+        args = dict(q=A, k=2 * A, v=3 * A, out=4 * A, s_in=None, s_out=None, B=1, H=1, N=16,
+                    D=16, M=16, dtype=F32)
+        args.update(kw)
+        return lib.causal_product_fwd_state(args["q"], args["k"], args["v"], args["out"],
+                                            args["s_in"], args["s_out"], args["B"], args["H"],
+                                            args["N"], args["D"], args["M"], args["dtype"],
+                                            None, 0, None)
+    assert fwd_state(s_in=5 * A + 4) == MISALIGNED
+    assert fwd_state(s_out=5 * A + 8) == MISALIGNED
+    # the final state may not overlap an input, the output or the initial state
+    assert fwd_state(s_out=A + 64) == INVALID_ARG
+    assert fwd_state(s_out=4 * A + 64) == INVALID_ARG
+    assert fwd_state(s_in=5 * A, s_out=5 * A + 256) == INVALID_ARG
+    # the output may not overlap the initial state
+    assert fwd_state(s_in=4 * A + 512) == INVALID_ARG
+    assert fwd_state(N=0) == OK
+
+    def bwd_state(**kw):
+        args = dict(q=A, k=2 * A, v=3 * A, g=4 * A, s_in=None, gs_out=None, dq=5 * A, dk=6 * A,
+                    dv=7 * A, gs_in=None, B=1, H=1, N=16, D=16, M=16, dtype=F32)
+        args.update(kw)
+        return lib.causal_product_bwd_state(args["q"], args["k"], args["v"], args["g"],
+                                            args["s_in"], args["gs_out"], args["dq"], args["dk"],
+                                            args["dv"], args["gs_in"], args["B"], args["H"],
+                                            args["N"], args["D"], args["M"], args["dtype"],
+                                            None, 0, None)
+    assert bwd_state(gs_in=8 * A + 4) == MISALIGNED
+    assert bwd_state(s_in=8 * A + 12) == MISALIGNED
+    # dL/dS_0 may not overlap a gradient or any input state
+    assert bwd_state(gs_in=5 * A + 16) == INVALID_ARG
+    assert bwd_state(s_in=8 * A, gs_in=8 * A + 32) == INVALID_ARG
+    assert bwd_state(gs_out=8 * A, gs_in=8 * A) == INVALID_ARG
+    # a gradient may not overlap an input state
+    assert bwd_state(s_in=6 * A + 128) == INVALID_ARG
+    assert bwd_state(N=0) == OK
