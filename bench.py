@@ -431,6 +431,33 @@ def run_ours(args, world, rank, local):
                "chunks": n_chunks,
                "timing": "CUDA events; copies and compute of successive chunks overlap"}
 
+    # ---- the same step with a carried state: S_0 in, S_N out, dL/dS_N in,
+    # dL/dS_0 out (the scans seed and hand on fp32 [B,H,D,M] states)
+    st_shape = (w.B, w.H, w.D, w.M)
+    s0 = torch.randn(st_shape, device=dev)
+    ds_n = torch.randn(st_shape, device=dev)
+    s_n = torch.empty(st_shape, device=dev)
+    ds_0 = torch.empty(st_shape, device=dev)
+
+    def state_step():
+        cp.causal_product_fwd(qd, kd, vd, out=out, workspace=ws_f, stream=stream, state_in=s0,
+                              return_state=True, state_out=s_n)
+        cp.causal_product_bwd(qd, kd, vd, gd, dq, dk, dv, workspace=ws_b, stream=stream,
+                              state_in=s0, grad_state_out=ds_n, return_state_grad=True,
+                              grad_state_in=ds_0)
+
+    for _ in range(3):
+        state_step()
+    torch.cuda.synchronize()
+    n_st = max(3, min(args.steps, 10))
+    st0, st1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    st0.record(stream)
+    for _ in range(n_st):
+        state_step()
+    st1.record(stream)
+    torch.cuda.synchronize()
+    state_ms = max_over_ranks(st0.elapsed_time(st1), world) / n_st
+
     # ---- roofline of the dominant kernel: the causal-product kernel, two
     # launches per step (forward, and dq in the backward call); the forward
     # call is exactly one launch of it, timed by its own events
@@ -483,6 +510,9 @@ def run_ours(args, world, rank, local):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(t_start, t_end, soak_from),
         "e2e": e2e,
+        "carried_state": {"ms_per_step": state_ms,
+                          "value": w.token_heads * world / (state_ms / 1e3) / 1e6, "unit": UNIT,
+                          "note": "fwd with S_0 in and S_N out, bwd with dS_N in and dS_0 out"},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)

@@ -149,18 +149,19 @@ def causal_product_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                        workspace: Optional[torch.Tensor] = None,
                        stream: Optional[torch.cuda.Stream] = None,
                        state_in: Optional[torch.Tensor] = None,
-                       return_state: bool = False):
+                       return_state: bool = False,
+                       state_out: Optional[torch.Tensor] = None):
     """out[b,h,i] = (S_0 + sum_{j<=i} k[b,h,j] v[b,h,j]^T)^T q[b,h,i], enqueued
     on ``stream``.  ``state_in`` is S_0 (float32 [B,H,D,M], None = zero);
     with ``return_state`` the result is (out, S_N), S_N the state after the
-    last row."""
+    last row (written into ``state_out`` when given)."""
     B, H, N, D, M = _dims(q, k, v)
     code = _dtype_code(q, k, v)
     if out is None:
         out = torch.empty((B, H, N, M), dtype=q.dtype, device=q.device)
     _check_device(q, k, v, out)
-    state_out = (torch.empty((B, H, D, M), dtype=torch.float32, device=q.device)
-                 if return_state else None)
+    if return_state and state_out is None:
+        state_out = torch.empty((B, H, D, M), dtype=torch.float32, device=q.device)
     lib = load_library()
     need = lib.causal_product_workspace_size(B, H, N, D, M, code, 0)
     if workspace is None:
@@ -206,10 +207,12 @@ def causal_product_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, grad_o
                        stream: Optional[torch.cuda.Stream] = None,
                        state_in: Optional[torch.Tensor] = None,
                        grad_state_out: Optional[torch.Tensor] = None,
-                       return_state_grad: bool = False):
+                       return_state_grad: bool = False,
+                       grad_state_in: Optional[torch.Tensor] = None):
     """(dq, dk, dv) of L = <grad_out, out> + <grad_state_out, S_N> for the
     forward from ``state_in`` (S_0; both float32 [B,H,D,M], None = zero).
-    With ``return_state_grad`` the result is (dq, dk, dv, dL/dS_0)."""
+    With ``return_state_grad`` the result is (dq, dk, dv, dL/dS_0), the last
+    written into ``grad_state_in`` when given."""
     B, H, N, D, M = _dims(q, k, v)
     code = _dtype_code(q, k, v, grad_out)
     if grad_out.shape != v.shape:
@@ -218,8 +221,8 @@ def causal_product_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, grad_o
     grad_k = torch.empty_like(k) if grad_k is None else grad_k
     grad_v = torch.empty_like(v) if grad_v is None else grad_v
     _check_device(q, k, v, grad_out, grad_q, grad_k, grad_v)
-    grad_state_in = (torch.empty((B, H, D, M), dtype=torch.float32, device=q.device)
-                     if return_state_grad else None)
+    if return_state_grad and grad_state_in is None:
+        grad_state_in = torch.empty((B, H, D, M), dtype=torch.float32, device=q.device)
     lib = load_library()
     need = lib.causal_product_workspace_size(B, H, N, D, M, code, 1)
     if workspace is None:
