@@ -458,6 +458,36 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     state_ms = max_over_ranks(st0.elapsed_time(st1), world) / n_st
 
+    # ---- decoding step (one new row per (b,h), state updated in place) on a
+    # serving-size batch whose fp32 state (128 MiB) exceeds L2
+    dec = None
+    if w.dtype == "bf16" and not args.no_decode:
+        dB, dH = 512, w.H
+        g_ = torch.Generator(device="cpu").manual_seed(77)
+        dq_ = torch.randn((dB, dH, w.D), generator=g_).to(dev, w.torch_dtype)
+        dk_ = torch.randn((dB, dH, w.D), generator=g_).to(dev, w.torch_dtype)
+        dv_ = torch.randn((dB, dH, w.M), generator=g_).to(dev, w.torch_dtype)
+        dst = torch.zeros((dB, dH, w.D, w.M), dtype=torch.float32, device=dev)
+        dout = torch.empty((dB, dH, w.M), dtype=w.torch_dtype, device=dev)
+        for _ in range(3):
+            cp.causal_product_decode(dq_, dk_, dv_, dst, out=dout, stream=stream)
+        torch.cuda.synchronize()
+        n_dec = 20
+        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        d0.record(stream)
+        for _ in range(n_dec):
+            cp.causal_product_decode(dq_, dk_, dv_, dst, out=dout, stream=stream)
+        d1.record(stream)
+        torch.cuda.synchronize()
+        dec_ms = max_over_ranks(d0.elapsed_time(d1), world) / n_dec
+        s_ = 2
+        dec_bytes = dB * dH * (8 * w.D * w.M + s_ * (2 * w.D + 2 * w.M))
+        dec = {"B": dB, "H": dH, "D": w.D, "M": w.M, "us_per_step": dec_ms * 1e3,
+               "tokens_per_s": dB * dH * world / (dec_ms / 1e3),
+               "bytes_per_step": dec_bytes, "achieved_gbs": dec_bytes / (dec_ms / 1e3) / 1e9,
+               "frac": dec_bytes / (dec_ms / 1e3) / 1e9 / load_peaks()[0],
+               "kernel": "decode_kernel", "bound": "hbm"}
+
     # ---- roofline of the dominant kernel: the causal-product kernel, two
     # launches per step (forward, and dq in the backward call); the forward
     # call is exactly one launch of it, timed by its own events
@@ -510,6 +540,7 @@ def run_ours(args, world, rank, local):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(t_start, t_end, soak_from),
         "e2e": e2e,
+        "decode": dec,
         "carried_state": {"ms_per_step": state_ms,
                           "value": w.token_heads * world / (state_ms / 1e3) / 1e6, "unit": UNIT,
                           "note": "fwd with S_0 in and S_N out, bwd with dS_N in and dS_0 out"},
@@ -551,6 +582,7 @@ def main(argv=None):
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-chunks", type=int, default=2)
+    ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     args = ap.parse_args(argv)

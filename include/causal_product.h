@@ -149,6 +149,18 @@ CP_API cp_status_t causal_product_bwd_state(const void* q, const void* k, const 
                                             cp_dtype_t dtype, void* workspace,
                                             size_t workspace_bytes, void* stream);
 
+/* One decoding step for every (b,h): the loop body of triton-lang/triton
+ * issue #217 applied to one new row,
+ *     S <- S + k v^T,   out = S^T q        (readout after the update),
+ * i.e. causal_product_fwd_state with N = 1, updating the state in place.
+ * q, k: [B,H,D], v, out: [B,H,M] in `dtype`; state: [B,H,D,M] fp32 (row d,
+ * column m), read and written.  Device pointers, 16-byte aligned; out and
+ * state overlap nothing.  fp32 arithmetic; out rounded to nearest-even for
+ * bf16.  No workspace, no status word (nothing waits). */
+CP_API cp_status_t causal_product_decode(const void* q, const void* k, const void* v, void* out,
+                                         float* state, int64_t B, int64_t H, int64_t D, int64_t M,
+                                         cp_dtype_t dtype, void* stream);
+
 /* Size of the static device scratch array behind causal_product_fwd_noalloc. */
 #define CP_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 

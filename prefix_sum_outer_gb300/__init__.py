@@ -73,6 +73,8 @@ def load_library(rebuild: bool = True) -> ctypes.CDLL:
             lib.causal_product_bwd_state.argtypes = [p, p, p, p, p, p, p, p, p, p, i64, i64, i64,
                                                      i64, i64, c_int, p, sz, p]
             lib.causal_product_bwd_state.restype = c_int
+            lib.causal_product_decode.argtypes = [p, p, p, p, p, i64, i64, i64, i64, c_int, p]
+            lib.causal_product_decode.restype = c_int
             lib.causal_product_fwd_noalloc.argtypes = [p, p, p, p, i64, i64, i64, i64, i64, c_int,
                                                        p]
             lib.causal_product_fwd_noalloc.restype = c_int
@@ -241,6 +243,30 @@ def causal_product_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, grad_o
     if return_state_grad:
         return grad_q, grad_k, grad_v, grad_state_in
     return grad_q, grad_k, grad_v
+
+
+def causal_product_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                          state: torch.Tensor, out: Optional[torch.Tensor] = None,
+                          stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """One decoding step: state <- state + k v^T (in place), out = state^T q.
+
+    q, k: [B,H,D]; v: [B,H,M]; state: float32 [B,H,D,M]."""
+    if q.dim() != 3 or k.shape != q.shape or v.dim() != 3 or v.shape[:2] != q.shape[:2]:
+        raise ValueError(f"expected q,k [B,H,D] and v [B,H,M]; got {tuple(q.shape)}, "
+                         f"{tuple(k.shape)}, {tuple(v.shape)}")
+    B, H, D = q.shape
+    M = v.shape[2]
+    code = _dtype_code(q, k, v)
+    if out is None:
+        out = torch.empty((B, H, M), dtype=q.dtype, device=q.device)
+    _check_device(q, k, v, out, state)
+    _state_arg(state, (B, H, D, M), q.device, "state")
+    rc = load_library().causal_product_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                              out.data_ptr(), state.data_ptr(), B, H, D, M, code,
+                                              _stream_ptr(stream, q.device))
+    if rc != CP_OK:
+        raise CausalProductError(rc, "causal_product_decode")
+    return out
 
 
 def causal_product_status(workspace: torch.Tensor,

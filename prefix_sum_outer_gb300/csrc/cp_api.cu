@@ -245,6 +245,31 @@ cp_status_t causal_product_bwd(const void* q, const void* k, const void* v, cons
                                   stream);
 }
 
+cp_status_t causal_product_decode(const void* q, const void* k, const void* v, void* out,
+                                  float* state, int64_t B, int64_t H, int64_t D, int64_t M,
+                                  cp_dtype_t dtype, void* stream_) {
+  cp_status_t st = cp::check_dims(B, H, 1, D, M, dtype);
+  if (st != CP_OK) return st;
+  if (!q || !k || !v || !out || !state) return CP_ERR_INVALID_ARG;
+  if (!cp::aligned16(q) || !cp::aligned16(k) || !cp::aligned16(v) || !cp::aligned16(out) ||
+      !cp::aligned16(state))
+    return CP_ERR_MISALIGNED;
+  const size_t es = dtype == CP_DTYPE_F32 ? 4 : 2;
+  const int64_t BH = B * H;
+  const size_t nq = (size_t)BH * D * es, nv = (size_t)BH * M * es;
+  const size_t nst = (size_t)BH * D * M * sizeof(float);
+  const void* ins[3] = {q, k, v};
+  const size_t in_sz[3] = {nq, nq, nv};
+  for (int i = 0; i < 3; ++i)
+    if (cp::overlaps(out, nv, ins[i], in_sz[i]) || cp::overlaps(state, nst, ins[i], in_sz[i]))
+      return CP_ERR_INVALID_ARG;
+  if (cp::overlaps(out, nv, state, nst)) return CP_ERR_INVALID_ARG;
+  return cp::decode_launch(q, k, v, out, state, BH, D, M, dtype,
+                           static_cast<cudaStream_t>(stream_)) == cudaSuccess
+             ? CP_OK
+             : CP_ERR_CUDA;
+}
+
 cp_status_t causal_product_status(void* workspace, void* stream_) {
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   if (cudaStreamSynchronize(stream) != cudaSuccess) return CP_ERR_CUDA;

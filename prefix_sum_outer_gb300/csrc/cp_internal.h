@@ -87,4 +87,9 @@ cp_status_t tc_bwd_launch(const void* q, const void* k, const void* v, const voi
                           int64_t N, int64_t D, int64_t M, const TcPlan& plan, float* agg,
                           int* status, cudaStream_t stream);
 
+// ---- decoding step (SIMT): S += k v^T, out = S^T q for every problem;
+// M <= 256
+cudaError_t decode_launch(const void* q, const void* k, const void* v, void* out, float* state,
+                          int64_t BH, int64_t D, int64_t M, cp_dtype_t dtype, cudaStream_t stream);
+
 }  // namespace cp

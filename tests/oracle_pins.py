@@ -338,5 +338,20 @@ def pin_state_finite_differences(impl, shape=(1, 1, 6, 3, 2)):
 FWD_PINS = [pin_golden, pin_brute_force, pin_first_row_closed_form, pin_last_row_is_noncausal,
             pin_scalar_cumsum, pin_ones_cumsum, pin_zero_value, pin_linearity, pin_causality]
 BWD_PINS = [pin_finite_differences, pin_bwd_brute_force, pin_bwd_identities]
-STATE_PINS = [pin_state_closed_forms, pin_state_chunking, pin_state_finite_differences]
+def pin_state_token_by_token(impl, n=9):
+    """Feeding the rows one at a time (N = 1 per call, the decoding step)
+    and handing the state on reproduces the whole sequence exactly."""
+    q, k, v, g, s0, ds_n = _state_case(19, shape=(1, 2, n, 5, 3))
+    out, s_n = impl.fwd_state(q, k, v, s0)
+    state = s0.astype(np.float64)
+    rows = []
+    for i in range(n):
+        o, state = impl.fwd_state(q[..., i:i + 1, :], k[..., i:i + 1, :], v[..., i:i + 1, :], state)
+        rows.append(o)
+    assert np.array_equal(np.concatenate(rows, axis=-2), out), "token-by-token out"
+    assert np.array_equal(state, s_n), "token-by-token state"
+
+
+STATE_PINS = [pin_state_closed_forms, pin_state_chunking, pin_state_finite_differences,
+              pin_state_token_by_token]
 ALL_PINS = FWD_PINS + BWD_PINS + STATE_PINS

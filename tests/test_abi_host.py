@@ -172,3 +172,22 @@ def test_state_argument_checks(lib):
     # a gradient may not overlap an input state
     assert bwd_state(s_in=6 * A + 128) == INVALID_ARG
     assert bwd_state(N=0) == OK
+
+
+def test_decode_argument_checks(lib):
+    def dec(**kw):
+        args = dict(q=A, k=2 * A, v=3 * A, out=4 * A, st=5 * A, B=1, H=1, D=16, M=16, dtype=F32)
+        args.update(kw)
+        return lib.causal_product_decode(args["q"], args["k"], args["v"], args["out"], args["st"],
+                                         args["B"], args["H"], args["D"], args["M"],
+                                         args["dtype"], None)
+    assert dec(st=None) == INVALID_ARG
+    assert dec(q=None) == INVALID_ARG
+    assert dec(st=5 * A + 4) == MISALIGNED
+    assert dec(D=12, dtype=BF16) == UNSUPPORTED_SHAPE
+    assert dec(M=300) == UNSUPPORTED_SHAPE
+    assert dec(dtype=7) == UNSUPPORTED_DTYPE
+    # the state or the output may not overlap an input or each other
+    assert dec(st=A + 32) == INVALID_ARG
+    assert dec(out=3 * A + 16) == INVALID_ARG
+    assert dec(out=5 * A + 64) == INVALID_ARG
