@@ -18,7 +18,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_o, const Args a) {
-  causal_body<DP, MB, AGG_ONLY, STATE_OUT>(tm_q, tm_k, tm_v, tm_o, a);
+  causal_body<DP, MB, AGG_ONLY, STATE_OUT>(tm_q, tm_k, tm_v, tm_o, a,
+                                           Phase{(int)blockIdx.x, true, true});
 }
 
 // ------------------------------------------------------------------ host

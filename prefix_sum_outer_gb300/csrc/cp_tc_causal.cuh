@@ -144,10 +144,11 @@ struct Layout {
 // tensor maps are the kernel's __grid_constant__ parameters.  STATE_OUT:
 // the launch writes the final state (a separate instantiation: the write,
 // though it runs once, costs the whole kernel registers).
+// Returns false when a wait gave up.
 template <int DP, int MB, bool AGG_ONLY, bool STATE_OUT>
-__device__ __forceinline__ void causal_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+__device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                             const CUtensorMap& tm_v, const CUtensorMap& tm_o,
-                                            const Args& a) {
+                                            const Args& a, const Phase ph) {
   using L = Layout<DP, MB>;
   constexpr int NQK = L::NQK;
   constexpr int NV = L::NV;
@@ -181,7 +182,7 @@ __device__ __forceinline__ void causal_body(const CUtensorMap& tm_q, const CUten
   const int lane = threadIdx.x & 31;
 
   // ---- block -> (segment, problem, value-column block)
-  int idx = blockIdx.x;
+  int idx = ph.work;
   const int mb = idx % a.n_mb;
   idx /= a.n_mb;
   const int bh = idx % a.BH;
@@ -237,15 +238,17 @@ __device__ __forceinline__ void causal_body(const CUtensorMap& tm_q, const CUten
   }
   if (warp == 1) {
     tmem_alloc(tmem_holder, L::kColsAlloc);
-    tmem_relinquish();
+    if (ph.last) tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  grid_dep_wait();  // inputs written by the previous kernel are visible from here
-  // dependents start only once every block has passed the wait above, so
-  // for them every kernel before this one has completed
-  grid_dep_launch_dependents();
+  if (ph.first) {
+    grid_dep_wait();  // inputs written by the previous kernel are visible from here
+    // dependents start only once every block has passed the wait above, so
+    // for them every kernel before this one has completed
+    grid_dep_launch_dependents();
+  }
   const uint32_t tmem = *tmem_holder;
   const int wq = warp & 3;                 // TMEM lane quarter of this warp
   const int row = wq * 32 + lane;          // tile row = TMEM lane
@@ -735,6 +738,15 @@ __device__ __forceinline__ void causal_body(const CUtensorMap& tm_q, const CUten
     tc_fence_after();
     tmem_dealloc(tmem, L::kColsAlloc);
   }
+  const bool completed = *abort_flag == 0;
+  if (!ph.last) {
+    // a later scan of this CTA reuses the barriers' memory
+    __syncthreads();
+    if (threadIdx.x == 0)
+      for (uint64_t* b = bars; b < fin + 3; ++b) mbar_inval(b);
+    __syncthreads();
+  }
+  return completed;
 }
 
 }  // namespace tc

@@ -18,6 +18,17 @@ constexpr int kBoxCols = 64;           // bf16 columns per TMA box (128 bytes)
 constexpr int kBoxBytes = kTile * 128; // one [128 x 64] bf16 box
 constexpr int kSmemLimit = 232448;     // 227 KB opt-in dynamic shared memory
 
+// One scan a CTA runs.  A CTA may run several scans one after another (the
+// backward kernel does); `work` replaces the block index, `first` makes the
+// scan wait for the previous kernel in the stream (and then let dependents
+// start), `last` gives up the CTA's permit to allocate tensor memory and
+// skips the barrier clean-up that lets a later scan reuse the memory.
+struct Phase {
+  int work;
+  bool first;
+  bool last;
+};
+
 // Byte offset of element (row, col) inside a [rows x 64k] bf16 tile stored
 // as 64-column boxes of `box_stride` bytes with the 128-byte swizzle (the
 // layout TMA writes and tcgen05 descriptors read): 16-byte chunk index

@@ -1,15 +1,20 @@
-// Backward pass for bf16 with D, M <= 64: dq as one causal-product launch,
-// then the fused dk/dv reverse scan (cp_tc_dkdv.cuh), preceded by its
-// aggregate pass when the problems are split into segments.
+// Backward pass for bf16 with D, M <= 64: the fused dk/dv reverse scan
+// (cp_tc_dkdv.cuh) and dq, a forward causal product.
 //
-// (Running both scans of a problem in one CTA, dk/dv and then dq, was
-// measured: no faster than two launches, since each scan's pipeline fill and
-// drain stay on the critical path either way.)
+// Unsplit problems on fewer problems than SMs run as one launch with a
+// static schedule (tc_bwd_kernel): CTA p < BH runs the dk/dv scan of problem
+// p, and the SMs that would otherwise idle run dq scans, two each; the
+// remaining dq scans follow the dk/dv scan of their own problem on the same
+// CTA, whose first tiles that scan has just read.  Per problem the dk/dv
+// scan takes about 1.6 times a dq scan, so two dq scans per spare SM keep
+// those SMs busy about as long as a dk/dv + dq CTA.  Split problems run
+// dq as a product launch, then the aggregate pass and the fused scan.
 #include <algorithm>
 #include <atomic>
 #include <utility>
 
 #include "cp_internal.h"
+#include "cp_tc_causal.cuh"
 #include "cp_tc_dkdv.cuh"
 
 namespace cp {
@@ -22,8 +27,43 @@ __global__ void __launch_bounds__(dkdv::kThreads, 1)
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                    const __grid_constant__ CUtensorMap tm_dk,
                    const __grid_constant__ CUtensorMap tm_dv, const dkdv::DkdvArgs a) {
-  dkdv::dkdv_body<STATE_OUT>(tm_q, tm_k, tm_v, tm_g, tm_dk, tm_dv, a);
+  dkdv::dkdv_body<STATE_OUT>(tm_q, tm_k, tm_v, tm_g, tm_dk, tm_dv, a,
+                             Phase{(int)blockIdx.x, true, true});
 }
+
+constexpr int kDqPerSpare = 2;
+
+// CTA c < BH: the dk/dv scan of problem c, then dq of problem c when c <
+// n_main_dq.  CTA BH + e: dq of problems n_main_dq + kDqPerSpare * e + j.
+template <bool STATE_OUT>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+                  const __grid_constant__ CUtensorMap tm_dk,
+                  const __grid_constant__ CUtensorMap tm_dv,
+                  const __grid_constant__ CUtensorMap tm_dq, const dkdv::DkdvArgs a, const Args aq,
+                  int n_main_dq) {
+  const int c = (int)blockIdx.x;
+  if (c < a.BH) {
+    const bool more = c < n_main_dq;
+    if (dkdv::dkdv_body<STATE_OUT>(tm_q, tm_k, tm_v, tm_g, tm_dk, tm_dv, a, Phase{c, true, !more}) &&
+        more)
+      causal_body<dkdv::kW, dkdv::kW, false, false>(tm_g, tm_v, tm_k, tm_dq, aq,
+                                                    Phase{c, false, true});
+    return;
+  }
+  // dq_i = sum_{j<=i} (g_i . v_j) k_j: the forward product (g, v, k)
+  const int p0 = n_main_dq + kDqPerSpare * (c - a.BH);
+  const int n = min(kDqPerSpare, a.BH - p0);
+  for (int j = 0; j < n; ++j)
+    if (!causal_body<dkdv::kW, dkdv::kW, false, false>(tm_g, tm_v, tm_k, tm_dq, aq,
+                                                       Phase{p0 + j, j == 0, j == n - 1}))
+      return;
+}
+
+static_assert(dkdv::kThreads == kThreads, "both scans run on the same CTA");
+static_assert(dkdv::kSmemBytes == Layout<dkdv::kW, dkdv::kW>::kSmemBytes,
+              "both scans use the same shared-memory size");
 
 template <typename Kernel>
 cudaError_t set_smem_once(Kernel kern, int bytes, std::atomic<uint64_t>& configured) {
@@ -91,6 +131,49 @@ cp_status_t tc_bwd_launch(const void* q, const void* k, const void* v, const voi
   a.state_out = grad_state_in;
   a.status = status;
   cudaError_t e;
+  int dev = 0, n_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return CP_ERR_CUDA;
+  if (plan.G == 1 && BH < n_sm) {
+    // one launch: dk/dv scans on BH CTAs, dq scans on the spare SMs first
+    CUtensorMap mdq;
+    if (!make_map(&mdq, dq, BH, N, D)) return CP_ERR_UNSUPPORTED_SHAPE;
+    Args aq{};
+    aq.N = N;
+    aq.n_tiles = plan.n_tiles;
+    aq.seg_tiles = plan.n_tiles;
+    aq.G = 1;
+    aq.BH = (int)BH;
+    aq.n_mb = 1;
+    aq.reverse = 0;
+    aq.status = status;
+    // the product's state sum v k^T is the transpose of the caller's S_0
+    aq.state_in = state_in;
+    aq.st_ld_r = 1;
+    aq.st_ld_c = M;
+    aq.Dr = (int)M;
+    aq.Mc = (int)D;
+    const int64_t spare = n_sm - BH;
+    const int64_t n_spare_dq = std::min<int64_t>(BH, spare * kDqPerSpare);
+    const int n_main_dq = (int)(BH - n_spare_dq);
+    const unsigned grid = (unsigned)(BH + (n_spare_dq + kDqPerSpare - 1) / kDqPerSpare);
+    constexpr int kSmem = dkdv::kSmemBytes;
+    if (grad_state_in != nullptr) {
+      static std::atomic<uint64_t> configured{0};
+      e = set_smem_once(tc_bwd_kernel<true>, kSmem, configured);
+      if (e == cudaSuccess)
+        e = launch_pdl(tc_bwd_kernel<true>, grid, kSmem, stream, mq, mk, mv, mg, mdk, mdv, mdq, a,
+                       aq, n_main_dq);
+    } else {
+      static std::atomic<uint64_t> configured{0};
+      e = set_smem_once(tc_bwd_kernel<false>, kSmem, configured);
+      if (e == cudaSuccess)
+        e = launch_pdl(tc_bwd_kernel<false>, grid, kSmem, stream, mq, mk, mv, mg, mdk, mdv, mdq,
+                       a, aq, n_main_dq);
+    }
+    return e == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+  }
   // dq_i = sum_{j<=i} (g_i . v_j) k_j: the forward product (g, v, k); then
   // (split problems) the aggregate pass of the state sum q g^T, i.e. of the
   // reverse product with k' = q and v' = g; then the fused dk/dv scan

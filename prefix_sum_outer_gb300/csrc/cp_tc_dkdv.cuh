@@ -94,11 +94,12 @@ __device__ __forceinline__ void pack_p_reverse(uint32_t pc, int wq, int lane) {
 // One CTA's work: the fused reverse scan of one (segment, problem).  The
 // tensor maps are the kernel's __grid_constant__ parameters.  STATE_OUT: the
 // launch writes dL/dS_0 (a separate instantiation, as for the product).
+// Returns false when a wait gave up.
 template <bool STATE_OUT>
-__device__ __forceinline__ void dkdv_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+__device__ __forceinline__ bool dkdv_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                           const CUtensorMap& tm_v, const CUtensorMap& tm_g,
                                           const CUtensorMap& tm_dk, const CUtensorMap& tm_dv,
-                                          const DkdvArgs& a) {
+                                          const DkdvArgs& a, const Phase ph) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -121,8 +122,8 @@ __device__ __forceinline__ void dkdv_body(const CUtensorMap& tm_q, const CUtenso
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  const int bh = blockIdx.x % a.BH;
-  const int seg = blockIdx.x / a.BH;
+  const int bh = ph.work % a.BH;
+  const int seg = ph.work / a.BH;
   const int t_first = seg * a.seg_tiles;
   const int t_end = min(a.n_tiles, t_first + a.seg_tiles);
   const int n_it = t_end - t_first;
@@ -162,14 +163,16 @@ __device__ __forceinline__ void dkdv_body(const CUtensorMap& tm_q, const CUtenso
   }
   if (warp == 1) {
     tmem_alloc(tmem_holder, kColsAlloc);
-    tmem_relinquish();
+    if (ph.last) tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  grid_dep_wait();  // inputs written by the previous kernel are visible from here
-  // dependents start only once every block has passed the wait above
-  grid_dep_launch_dependents();
+  if (ph.first) {
+    grid_dep_wait();  // inputs written by the previous kernel are visible from here
+    // dependents start only once every block has passed the wait above
+    grid_dep_launch_dependents();
+  }
   const uint32_t tmem = *tmem_holder;
   const int wq = warp & 3;                 // TMEM lane quarter of this warp
   const int row = wq * 32 + lane;          // tile row = TMEM lane
@@ -507,6 +510,15 @@ __device__ __forceinline__ void dkdv_body(const CUtensorMap& tm_q, const CUtenso
     tc_fence_after();
     tmem_dealloc(tmem, kColsAlloc);
   }
+  const bool completed = *abort_flag == 0;
+  if (!ph.last) {
+    // a later scan of this CTA reuses the barriers' memory
+    __syncthreads();
+    if (threadIdx.x == 0)
+      for (uint64_t* b = bars; b < fin + 3; ++b) mbar_inval(b);
+    __syncthreads();
+  }
+  return completed;
 }
 
 }  // namespace dkdv

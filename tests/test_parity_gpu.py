@@ -122,11 +122,14 @@ def test_segmented_scan(N, dtype):
 
 
 @pytest.mark.parametrize("shape", [(1, 1, 3000, 48, 32), (1, 3, 1111, 64, 40), (3, 5, 257, 8, 64),
-                                   (2, 2, 640, 64, 64)], ids=lambda s: "x".join(map(str, s)))
+                                   (2, 2, 640, 64, 64), (10, 13, 300, 64, 64),
+                                   (1, 151, 256, 48, 64), (10, 16, 300, 64, 56)],
+                         ids=lambda s: "x".join(map(str, s)))
 def test_fused_dkdv_shapes(shape):
     """bf16 backward with D, M <= 64 computes dk and dv in one pass over a
-    shared reverse state: D != M, ragged tails, a single segment and the
-    two-pass scan across segments."""
+    shared reverse state: D != M, ragged tails, the two-pass scan across
+    segments, and unsplit problems in one launch with dq scans on the
+    spare SMs (130 and 151 problems) or as separate launches (160)."""
     B, H, N, D, M = shape
     q, k, v, g = make_inputs(B, H, N, D, M, torch.bfloat16, seed=N + D)
     check_bwd(q, k, v, g, "bf16")
