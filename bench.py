@@ -41,14 +41,15 @@ UNIT = "Mtok·head/s"
 # (dram__bytes_read.sum + dram__bytes_write.sum) together with the SHA-256 of
 # the kernel source it was measured on; a changed source reports null.
 CAUSAL_SOURCES = ("cp_tc.cu", "cp_tc_causal.cuh", "cp_tc_common.cuh", "sm103_ptx.cuh")
-DKDV_SOURCES = ("cp_tc_dkdv.cu", "cp_tc_dkdv.cuh", "cp_tc_common.cuh", "sm103_ptx.cuh")
+BWD_SOURCES = ("cp_tc_dkdv.cu", "cp_tc_dkdv.cuh", "cp_tc_causal.cuh", "cp_tc_common.cuh",
+               "sm103_ptx.cuh")
 PROFILED_TRAFFIC = {
     "source_sha256": "a1d4c6d965fbaddad32b2a7d61de45f34e2d1b9ab1ca3a929df55b9e1ef43272",
     "bytes_per_launch": 211631872,  # 201.39 MB read + 10.24 MB written (forward launch)
 }
-PROFILED_TRAFFIC_DKDV = {
-    "source_sha256": "4c3aaec81f4bb36defef0acfd8aafca2b7d618db36a2c9415427fae2fab10daf",
-    "bytes_per_launch": 342428928,  # 268.53 MB read + 73.90 MB written
+PROFILED_TRAFFIC_BWD = {
+    "source_sha256": None,
+    "bytes_per_launch": None,
 }
 
 
@@ -285,9 +286,10 @@ def run_ours(args, world, rank, local):
         cp.causal_product_fwd(qd, kd, vd, out=out, workspace=ws_f, stream=stream)
         cp.causal_product_bwd(qd, kd, vd, gd, dq, dk, dv, workspace=ws_b, stream=stream)
 
-    # kernels of ours launched per step (tensor-core path): forward 1 product,
-    # backward dq plus the fused dk/dv scan (or 2 more products); a scan split
-    # into segments adds one aggregate launch
+    # kernels of ours launched per step (tensor-core path): forward 1 product;
+    # backward 1 launch (dk/dv and dq scans) for unsplit problems on fewer
+    # than the SMs, else dq plus the fused dk/dv scan (or 2 more products);
+    # a scan split into segments adds one aggregate launch
     launches_per_step = _launches_per_step(w)
 
     for _ in range(max(args.warmup, 0)):
@@ -446,22 +448,24 @@ def run_ours(args, world, rank, local):
                               state_in=s0, grad_state_out=ds_n, return_state_grad=True,
                               grad_state_in=ds_0)
 
-    for _ in range(3):
-        state_step()
-    torch.cuda.synchronize()
-    n_st = max(3, min(args.steps, 10))
-    st0, st1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    st0.record(stream)
-    for _ in range(n_st):
-        state_step()
-    st1.record(stream)
-    torch.cuda.synchronize()
-    state_ms = max_over_ranks(st0.elapsed_time(st1), world) / n_st
+    state_ms = None
+    if not args.no_extras:
+        for _ in range(3):
+            state_step()
+        torch.cuda.synchronize()
+        n_st = max(3, min(args.steps, 10))
+        st0, st1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        st0.record(stream)
+        for _ in range(n_st):
+            state_step()
+        st1.record(stream)
+        torch.cuda.synchronize()
+        state_ms = max_over_ranks(st0.elapsed_time(st1), world) / n_st
 
     # ---- decoding step (one new row per (b,h), state updated in place) on a
     # serving-size batch whose fp32 state (128 MiB) exceeds L2
     dec = None
-    if w.dtype == "bf16" and not args.no_decode:
+    if w.dtype == "bf16" and not args.no_extras:
         dB, dH = 512, w.H
         g_ = torch.Generator(device="cpu").manual_seed(77)
         dq_ = torch.randn((dB, dH, w.D), generator=g_).to(dev, w.torch_dtype)
@@ -505,20 +509,26 @@ def run_ours(args, world, rank, local):
         traffic = PROFILED_TRAFFIC["bytes_per_launch"]
     kernels = []
     if fused and not segmented:
-        # the fused dk/dv launch reads q, k, v, g and writes dk, dv; its time
-        # is the backward call minus its causal-product launch (dq, the same
-        # bytes as the forward launch when D = M)
-        dkdv_bytes = s * (3 * w.D + 3 * w.M) * w.token_heads
-        dkdv_ms = (bwd_ms - fwd_ms) / args.steps
-        dkdv_traffic = None
-        if PROFILED_TRAFFIC_DKDV["source_sha256"] == kernel_sha(DKDV_SOURCES):
-            dkdv_traffic = PROFILED_TRAFFIC_DKDV["bytes_per_launch"]
-        kernels.append({"kernel": "tc_dkdv_kernel", "bound": "hbm",
-                        "bytes_per_launch": dkdv_bytes, "avg_launch_ms": dkdv_ms,
-                        "achieved": dkdv_bytes / (dkdv_ms / 1e3) / 1e9,
-                        "frac": dkdv_bytes / (dkdv_ms / 1e3) / 1e9 / hbm_gbs,
-                        "traffic": dkdv_traffic,
-                        "timing": "backward call minus one forward launch"})
+        bwd_traffic = None
+        if PROFILED_TRAFFIC_BWD["source_sha256"] == kernel_sha(BWD_SOURCES):
+            bwd_traffic = PROFILED_TRAFFIC_BWD["bytes_per_launch"]
+        if _single_launch_bwd(w):
+            # one launch: the fused dk/dv scans (read q, k, v, g; write dk,
+            # dv) and the dq scans (read g, v, k; write dq)
+            b_bytes = s * (5 * w.D + 5 * w.M) * w.token_heads
+            b_ms = bwd_ms / args.steps
+            name, timing = "tc_bwd_kernel", "backward call: one launch, CUDA events on its stream"
+        else:
+            # the fused dk/dv launch, timed as the backward call minus its
+            # causal-product launch (dq, the same bytes as the forward when D = M)
+            b_bytes = s * (3 * w.D + 3 * w.M) * w.token_heads
+            b_ms = (bwd_ms - fwd_ms) / args.steps
+            name, timing = "tc_dkdv_kernel", "backward call minus one forward launch"
+        kernels.append({"kernel": name, "bound": "hbm", "bytes_per_launch": b_bytes,
+                        "avg_launch_ms": b_ms, "achieved": b_bytes / (b_ms / 1e3) / 1e9,
+                        "frac": b_bytes / (b_ms / 1e3) / 1e9 / hbm_gbs,
+                        "traffic": bwd_traffic if name == "tc_bwd_kernel" else None,
+                        "timing": timing})
     step_roofline_ms = algorithmic_bytes(w) / (hbm_gbs * 1e9) * 1e3
 
     line = {
@@ -541,9 +551,9 @@ def run_ours(args, world, rank, local):
         "clocks": clocks.summary(t_start, t_end, soak_from),
         "e2e": e2e,
         "decode": dec,
-        "carried_state": {"ms_per_step": state_ms,
-                          "value": w.token_heads * world / (state_ms / 1e3) / 1e6, "unit": UNIT,
-                          "note": "fwd with S_0 in and S_N out, bwd with dS_N in and dS_0 out"},
+        "carried_state": None if state_ms is None else {
+            "ms_per_step": state_ms, "value": w.token_heads * world / (state_ms / 1e3) / 1e6,
+            "unit": UNIT, "note": "fwd with S_0 in and S_N out, bwd with dS_N in and dS_0 out"},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
@@ -566,7 +576,16 @@ def _fused_dkdv(w):
     return w.dtype == "bf16" and w.D <= 64 and w.M <= 64
 
 
+def _single_launch_bwd(w):
+    """Unsplit problems, fewer than the SMs: the backward is one launch."""
+    import torch
+    n_sm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return _fused_dkdv(w) and not _segmented(w) and w.B * w.H < n_sm
+
+
 def _launches_per_step(w):
+    if _single_launch_bwd(w):
+        return 2
     per_scan = 2 if _segmented(w) else 1
     # forward: one product; backward: dq plus either the fused dk/dv scan
     # or the dv and dk products
@@ -582,7 +601,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-chunks", type=int, default=2)
-    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the carried-state and decoding measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     args = ap.parse_args(argv)
