@@ -6,7 +6,8 @@
 // sum of Algorithm 1 of "Transformers are RNNs") is regrouped into tiles of
 // 128 rows.  With S the fp32 D x M state before tile t:
 //     P   = Q_t K_t^T            masked to j <= i inside the tile (128x128)
-//     O_t = P V_t + Q_t S        (intra-tile part + inter-tile readout)
+//     O_t = Q_t S + P V_t        (inter-tile readout, then the intra-tile part
+//                                 accumulated onto it)
 //     S  += K_t^T V_t
 // All four are dense contractions and run as tcgen05.mma with bf16 operands
 // in shared memory and fp32 accumulators in tensor memory (TMEM).  The state
@@ -101,17 +102,13 @@ struct Layout {
     return 0;
   }
   // TMEM holds NP buffers of P (128 columns, fp32; later packed bf16 hi|lo),
-  // the Q S accumulator O1, the P V accumulator O2 (MB columns) and the
-  // state (kSBlocks x MB).  O1 is 2 MB wide when it fits: Q [S_hi | S_lo]
-  // in one N = 2 MB chain, the two halves summed on read-out.  A P buffer is
-  // reused only after the P V that read it has completed.
-  static constexpr int cols(int np, bool wide) {
-    return np * 128 + (wide ? 2 : 1) * MB + MB + kSBlocks * MB;
-  }
-  static constexpr int NP = cols(2, false) <= 512 ? 2 : 1;
-  static constexpr bool kWide = cols(NP, true) <= 512 && 2 * MB <= 256;
-  static constexpr int kO1Cols = (kWide ? 2 : 1) * MB;
-  static constexpr int NO = 1;
+  // NO output accumulators of MB columns (Q S, then P V accumulated on top)
+  // and the state (kSBlocks x MB).  A P buffer is reused only after the P V
+  // that read it has completed, an output buffer only after the output
+  // group has read it out.
+  static constexpr int cols(int np, int no) { return np * 128 + no * MB + kSBlocks * MB; }
+  static constexpr int NP = cols(2, 1) <= 512 ? 2 : 1;
+  static constexpr int NO = cols(NP, 3) <= 512 ? 3 : (cols(NP, 2) <= 512 ? 2 : 1);
   // bf16 copies of the state in shared memory (one per tile in flight, at
   // most two); the state operand of Q S is split into hi + lo parts when it
   // fits next to a one-stage ring.
@@ -128,16 +125,14 @@ struct Layout {
   static constexpr int kSmemBytes =
       NQK * kQKBytes + NV * kVBytes + kFixed + kBarBytes + kAlignSlack;
   static constexpr int kColP = 0;                        // + b * 128
-  static constexpr int kColO1 = NP * 128;                // Q S (kO1Cols)
-  static constexpr int kColO2 = kColO1 + kO1Cols;        // P V (MB)
-  static constexpr int kColS = kColO2 + MB;              // + sb * MB
+  static constexpr int kColO = NP * 128;                 // + o * MB
+  static constexpr int kColS = kColO + NO * MB;          // + sb * MB
   static constexpr int kColsUsed = kColS + kSBlocks * MB;
   static constexpr int kColsAlloc = kColsUsed <= 256 ? 256 : 512;
   static_assert(NQK >= 1 && NV >= 1, "tile does not fit in shared memory");
   static_assert(kSmemBytes <= kSmemLimit, "shared memory overflow");
   static_assert(kColsUsed <= 512, "accumulators do not fit in TMEM");
   static_assert(DP % 64 == 0 && MB % 64 == 0, "64-column boxes");
-  static_assert(!kWide || kSplit, "the wide Q S chain reads S_hi and S_lo side by side");
 };
 
 // One CTA's work: the scan of one (segment, problem, value block).  The
@@ -154,6 +149,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
   constexpr int NV = L::NV;
   constexpr int NP = L::NP;
   constexpr int NSB = L::NSB;
+  constexpr int NO = L::NO;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -168,11 +164,12 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
   uint64_t* empty_v = full_v + NV;          // [NV]
   uint64_t* p_done = empty_v + NV;          // [NP] issuer B -> P group: P(t) in TMEM
   uint64_t* p_ready = p_done + NP;          // [NP] P group -> C: masked bf16 P (hi|lo) packed
-  uint64_t* pv_done = p_ready + NP;         // [NP] C -> O group, B: O2(t) final, P buffer free
+  uint64_t* pv_done = p_ready + NP;         // [NP] C -> B: P V(t) done, P buffer free
   uint64_t* qs_done = pv_done + NP;         // [NSB] A -> S group: Q S(t) done, state copy free
-  uint64_t* o1_done = qs_done + NSB;        // A -> O group: O1(t) final
-  uint64_t* o_free = o1_done + 1;           // O group -> A, C: O1 and O2 of tile t read out
-  uint64_t* s_done = o_free + 1;            // A -> S group: state updated with tile t
+  uint64_t* o_qs = qs_done + NSB;           // [NO] A -> C: Q S(t) in output buffer t % NO
+  uint64_t* o_done = o_qs + NO;             // [NO] C -> O group: O(t) final
+  uint64_t* o_free = o_done + NO;           // [NO] O group -> A: output buffer read out
+  uint64_t* s_done = o_free + NO;           // A -> S group: state updated with tile t
   uint64_t* s_ready = s_done + 1;           // S group -> A: bf16 state copy written, S read
   uint64_t* fin = s_done + 2;               // [3] issuer drains before TMEM release
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(s_done + 5);
@@ -217,8 +214,11 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
       mbar_init(&pv_done[i], 1);
     }
     for (int i = 0; i < NSB; ++i) mbar_init(&qs_done[i], 1);
-    mbar_init(o1_done, 1);
-    mbar_init(o_free, kOWarps);
+    for (int i = 0; i < NO; ++i) {
+      mbar_init(&o_qs[i], 1);
+      mbar_init(&o_done[i], 1);
+      mbar_init(&o_free[i], kOWarps);
+    }
     mbar_init(s_done, 1);
     mbar_init(s_ready, kSWarps);
     mbar_init(&fin[0], 1);
@@ -315,20 +315,18 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
   } else if (warp == 1 || warp == kBWarp || warp == kCWarp) {
     // ------------------------------------------------------------ MMA issuers
     // Issuer A (warp 1): the state chain S(t) and the inter-tile read-out
-    // Q S(t) into O1.  Issuer B (warp kBWarp): P(t) = Q K^T.  Issuer C (warp
-    // kCWarp): the intra-tile P V(t) into O2.  Q S and P V never touch the
-    // same accumulator, so the issuers need no ordering between them beyond
-    // the barriers on P; a ring stage is released by a commit from each of
-    // its two users.
+    // Q S(t) into output buffer t % NO.  Issuer B (warp kBWarp): P(t) =
+    // Q K^T.  Issuer C (warp kCWarp): the intra-tile P V(t), accumulated onto
+    // Q S(t) once that has completed, so the order of the sums is fixed.
+    // With NO buffers the read-out of a tile never holds up the next one.  A
+    // ring stage is released by a commit from each of its two users.
     if (lane == 0 && (warp == 1 || !AGG_ONLY)) {
       constexpr uint32_t idesc_p = idesc_bf16_f32(128, 128, 0, 0);   // Q . K^T
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, MB, 1, 1);    // K^T . V
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, MB, 0, 1);    // P . V, Q . S
-      constexpr uint32_t idesc_ow = idesc_bf16_f32(128, 2 * MB, 0, 1);  // Q . [S_hi | S_lo]
       constexpr uint32_t kHi = desc_hi(1024);  // SBO = 1024, 128-byte swizzle
       const uint32_t t_s = tmem + L::kColS;
-      const uint32_t t_o1 = tmem + L::kColO1;
-      const uint32_t t_o2 = tmem + L::kColO2;
+      auto t_out = [&](int it) { return tmem + L::kColO + (it % NO) * MB; };
       const uint32_t s_addr = smem_u32(s_tile);
       auto qk_addr = [&](int it) { return smem_u32(qk_ring + (it % NQK) * L::kQKBytes); };
       auto v_addr = [&](int it) { return smem_u32(v_ring + (it % NV) * L::kVBytes); };
@@ -375,7 +373,8 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
         if (ok) mma_commit(s_done);
       } else if (warp == 1) {
         // issuer A: S(t) needs Q/K(t), V(t) landed and the state copied out
-        // (s_ready); Q S(t) needs S(t) issued and O1 read out for t - 1.
+        // (s_ready); Q S(t) needs S(t) issued and output buffer t % NO read
+        // out for t - NO.
         int nS = 0, nQ = 0;
         while (nQ < n_it) {
           bool progressed = false;
@@ -389,34 +388,25 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
             ++nS;
             progressed = true;
           }
-          if (nQ < nS && (nQ == 0 || mbar_test_wait(o_free, (nQ - 1) & 1))) {
+          if (nQ < nS &&
+              (nQ < NO || mbar_test_wait(&o_free[nQ % NO], ((nQ - NO) / NO) & 1))) {
             tc_fence_after();
             const uint32_t q_lo = desc_lo(qk_addr(nQ), 16);
             const uint32_t s_lo = desc_lo(s_addr + (nQ % NSB) * L::kSBufBytes, DP * 128);
-            if (L::kWide) {
-              // O1 = Q [S_hi | S_lo]: hi and lo copies sit side by side as
-              // one MN-major operand of 2 MB columns
+            // O(t) = Q S_hi (+ Q S_lo) into a free output buffer; P V(t)
+            // accumulates on top once this has completed
+#pragma unroll
+            for (int part = 0; part < (L::kSplit ? 2 : 1); ++part) {
 #pragma unroll
               for (int kk = 0; kk < DP / 16; ++kk) {
                 const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-                mma_ss_lo<kHi, kHi>(t_o1, q_lo + off, s_lo + ((kk * 2048) >> 4), idesc_ow,
-                                    kk > 0 ? 1u : 0u);
-              }
-            } else {
-              // O1 = Q S_hi (+ Q S_lo)
-#pragma unroll
-              for (int part = 0; part < (L::kSplit ? 2 : 1); ++part) {
-#pragma unroll
-                for (int kk = 0; kk < DP / 16; ++kk) {
-                  const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-                  mma_ss_lo<kHi, kHi>(t_o1, q_lo + off,
-                                      s_lo + ((part * L::kSOneBytes + kk * 2048) >> 4), idesc_o,
-                                      (part == 0 && kk == 0) ? 0u : 1u);
-                }
+                mma_ss_lo<kHi, kHi>(t_out(nQ), q_lo + off,
+                                    s_lo + ((part * L::kSOneBytes + kk * 2048) >> 4), idesc_o,
+                                    (part == 0 && kk == 0) ? 0u : 1u);
               }
             }
             mma_commit(&qs_done[nQ % NSB]);
-            mma_commit(o1_done);
+            mma_commit(&o_qs[nQ % NO]);
             mma_commit(&empty_qk[nQ % NQK]);
             ++nQ;
             progressed = true;
@@ -445,20 +435,20 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
           mma_commit(&empty_qk[it % NQK]);
         }
       } else {
-        // issuer C: P V(t) needs P(t) packed, V(t) landed and O2 read out
-        // for t - 1
+        // issuer C: P V(t) needs P(t) packed, V(t) landed and Q S(t)
+        // completed in the output buffer it accumulates onto
         for (int it = 0; it < n_it; ++it) {
           const int b = it % NP;
           if (!mbar_wait(&p_ready[b], (it / NP) & 1, abort_flag) ||
               !mbar_wait(&full_v[it % NV], (it / NV) & 1, abort_flag) ||
-              (it > 0 && !mbar_wait(o_free, (it - 1) & 1, abort_flag))) {
+              !mbar_wait(&o_qs[it % NO], (it / NO) & 1, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t t_p = tmem + L::kColP + b * 128;
           const uint32_t v_lo = desc_lo(v_addr(it), kBoxBytes);
-          // O2 = P_hi V (+ P_lo V) (A = packed bf16 P in TMEM, B = V
+          // O(t) += P_hi V (+ P_lo V) (A = packed bf16 P in TMEM, B = V
           // MN-major).  Chunk c of P (columns 32c..32c+31) holds hi in its
           // first 16 TMEM columns and lo in the next 16, two j per column.
 #pragma unroll
@@ -466,11 +456,11 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk) {
               const uint32_t acol = (kk >> 1) * 32 + part * 16 + (kk & 1) * 8;
-              mma_ts_lo<kHi>(t_o2, t_p + acol, v_lo + ((kk * 2048) >> 4), idesc_o,
-                             (part == 0 && kk == 0) ? 0u : 1u);
+              mma_ts_lo<kHi>(t_out(it), t_p + acol, v_lo + ((kk * 2048) >> 4), idesc_o, 1u);
             }
           }
           mma_commit(&pv_done[b]);
+          mma_commit(&o_done[it % NO]);
           mma_commit(&empty_v[it % NV]);
         }
       }
@@ -653,12 +643,12 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
     bool ok = true;
     for (int it = 0; !AGG_ONLY && it < n_it && ok; ++it) {
       uint8_t* ob = o_tile + (it % L::kOBufs) * L::kOBytes;
-      if (!mbar_wait(o1_done, it & 1, abort_flag) ||
-          !mbar_wait(&pv_done[it % NP], (it / NP) & 1, abort_flag)) {
+      if (!mbar_wait(&o_done[it % NO], (it / NO) & 1, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      const uint32_t t_o = lane_base + L::kColO + (it % NO) * MB;
       auto wait_staging = [&]() {
         // the store that last read this staging buffer has finished reading it
         if (o_tid == 0) {
@@ -669,28 +659,16 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
         }
         named_barrier_sync(1, kOThreads);
       };
-      // O = O1 (+ its lo half when wide) + O2
       if constexpr (MB <= 64) {
-        // the whole row fits in registers: release the accumulators before
+        // the whole row fits in registers: release the buffer before
         // converting and storing
         uint32_t r[MB / 32][32];
 #pragma unroll
-        for (int c = 0; c < MB / 32; ++c) {
-          uint32_t u[32], w[32];
-          tmem_ld32(lane_base + L::kColO1 + c * 32, r[c]);
-          tmem_ld32(lane_base + L::kColO2 + c * 32, u);
-          if (L::kWide) tmem_ld32(lane_base + L::kColO1 + MB + c * 32, w);
-          tmem_ld_wait();
-#pragma unroll
-          for (int x = 0; x < 32; ++x) {
-            float f = __uint_as_float(r[c][x]) + __uint_as_float(u[x]);
-            if (L::kWide) f += __uint_as_float(w[x]);
-            r[c][x] = __float_as_uint(f);
-          }
-        }
+        for (int c = 0; c < MB / 32; ++c) tmem_ld32(t_o + c * 32, r[c]);
+        tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(o_free);
+        if (lane == 0) mbar_arrive(&o_free[it % NO]);
         wait_staging();
 #pragma unroll
         for (int c = 0; c < MB / 32; ++c) store_chunk32(ob, row, c * 32, kBoxBytes, r[c]);
@@ -698,25 +676,14 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
         wait_staging();
 #pragma unroll 1
         for (int c = 0; c < MB / 32; ++c) {
-          uint32_t r[32], u[32];
-          tmem_ld32(lane_base + L::kColO1 + c * 32, r);
-          tmem_ld32(lane_base + L::kColO2 + c * 32, u);
+          uint32_t r[32];
+          tmem_ld32(t_o + c * 32, r);
           tmem_ld_wait();
-#pragma unroll
-          for (int x = 0; x < 32; ++x)
-            r[x] = __float_as_uint(__uint_as_float(r[x]) + __uint_as_float(u[x]));
-          if (L::kWide) {
-            tmem_ld32(lane_base + L::kColO1 + MB + c * 32, u);
-            tmem_ld_wait();
-#pragma unroll
-            for (int x = 0; x < 32; ++x)
-              r[x] = __float_as_uint(__uint_as_float(r[x]) + __uint_as_float(u[x]));
-          }
           store_chunk32(ob, row, c * 32, kBoxBytes, r);
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(o_free);
+        if (lane == 0) mbar_arrive(&o_free[it % NO]);
       }
       fence_proxy_async_smem();
       named_barrier_sync(1, kOThreads);
