@@ -44,12 +44,12 @@ CAUSAL_SOURCES = ("cp_tc.cu", "cp_tc_causal.cuh", "cp_tc_common.cuh", "sm103_ptx
 BWD_SOURCES = ("cp_tc_dkdv.cu", "cp_tc_dkdv.cuh", "cp_tc_causal.cuh", "cp_tc_common.cuh",
                "sm103_ptx.cuh")
 PROFILED_TRAFFIC = {
-    "source_sha256": "a1d4c6d965fbaddad32b2a7d61de45f34e2d1b9ab1ca3a929df55b9e1ef43272",
-    "bytes_per_launch": 211631872,  # 201.39 MB read + 10.24 MB written (forward launch)
+    "source_sha256": "4adf80f4cd33d34fa9578a9b9f9e8fb024ee57a48ee7c26674c974b04558cf36",
+    "bytes_per_launch": 211895040,  # 201.40 MB read + 10.50 MB written (forward launch)
 }
 PROFILED_TRAFFIC_BWD = {
-    "source_sha256": None,
-    "bytes_per_launch": None,
+    "source_sha256": "00783b015ef4ec96a917a56cacbeeb9bf5417314201285f15ce96e59605b3d02",
+    "bytes_per_launch": 605915136,  # 463.80 MB read + 142.11 MB written (one backward launch)
 }
 
 
@@ -436,10 +436,11 @@ def run_ours(args, world, rank, local):
     # ---- the same step with a carried state: S_0 in, S_N out, dL/dS_N in,
     # dL/dS_0 out (the scans seed and hand on fp32 [B,H,D,M] states)
     st_shape = (w.B, w.H, w.D, w.M)
-    s0 = torch.randn(st_shape, device=dev)
-    ds_n = torch.randn(st_shape, device=dev)
-    s_n = torch.empty(st_shape, device=dev)
-    ds_0 = torch.empty(st_shape, device=dev)
+    if not args.no_extras:
+        s0 = torch.randn(st_shape, device=dev)
+        ds_n = torch.randn(st_shape, device=dev)
+        s_n = torch.empty(st_shape, device=dev)
+        ds_0 = torch.empty(st_shape, device=dev)
 
     def state_step():
         cp.causal_product_fwd(qd, kd, vd, out=out, workspace=ws_f, stream=stream, state_in=s0,
@@ -492,43 +493,53 @@ def run_ours(args, world, rank, local):
                "frac": dec_bytes / (dec_ms / 1e3) / 1e9 / load_peaks()[0],
                "kernel": "decode_kernel", "bound": "hbm"}
 
-    # ---- roofline of the dominant kernel: the causal-product kernel, two
-    # launches per step (forward, and dq in the backward call); the forward
-    # call is exactly one launch of it, timed by its own events
+    # ---- roofline of the dominant kernel.  Unsplit problems on fewer than
+    # the SMs: the single backward launch (dk/dv and dq scans; the backward
+    # call is exactly that launch, timed by its own events); otherwise the
+    # causal-product kernel (two launches per step, the forward call is one).
     hbm_gbs, bf16_tf, peak_src = load_peaks()
     s = 2 if w.dtype == "bf16" else 4
     fused = _fused_dkdv(w)
     segmented = _segmented(w)
     # one causal product over (BH, N) moves D' + D' + M' + M' columns per row
     # (q', k', v' read, out' written)
-    bytes_per_launch = s * (2 * w.D + 2 * w.M) * w.token_heads
-    avg_launch_ms = fwd_ms / args.steps
-    achieved = bytes_per_launch / (avg_launch_ms / 1e3) / 1e9
-    traffic = None
+    fwd_bytes = s * (2 * w.D + 2 * w.M) * w.token_heads
+    fwd_ms_launch = fwd_ms / args.steps
+    fwd_traffic = None
     if not segmented and PROFILED_TRAFFIC["source_sha256"] == kernel_sha():
-        traffic = PROFILED_TRAFFIC["bytes_per_launch"]
-    kernels = []
+        fwd_traffic = PROFILED_TRAFFIC["bytes_per_launch"]
+    fwd_entry = {"kernel": "tc_causal_kernel (one causal product per launch)", "bound": "hbm",
+                 "bytes_per_launch": fwd_bytes, "avg_launch_ms": fwd_ms_launch,
+                 "achieved": fwd_bytes / (fwd_ms_launch / 1e3) / 1e9,
+                 "frac": fwd_bytes / (fwd_ms_launch / 1e3) / 1e9 / hbm_gbs,
+                 "traffic": fwd_traffic,
+                 "timing": "forward call: one launch, CUDA events on its stream"}
+    bwd_entry = None
     if fused and not segmented:
-        bwd_traffic = None
-        if PROFILED_TRAFFIC_BWD["source_sha256"] == kernel_sha(BWD_SOURCES):
-            bwd_traffic = PROFILED_TRAFFIC_BWD["bytes_per_launch"]
         if _single_launch_bwd(w):
             # one launch: the fused dk/dv scans (read q, k, v, g; write dk,
             # dv) and the dq scans (read g, v, k; write dq)
             b_bytes = s * (5 * w.D + 5 * w.M) * w.token_heads
             b_ms = bwd_ms / args.steps
+            b_traffic = None
+            if PROFILED_TRAFFIC_BWD["source_sha256"] == kernel_sha(BWD_SOURCES):
+                b_traffic = PROFILED_TRAFFIC_BWD["bytes_per_launch"]
             name, timing = "tc_bwd_kernel", "backward call: one launch, CUDA events on its stream"
         else:
             # the fused dk/dv launch, timed as the backward call minus its
             # causal-product launch (dq, the same bytes as the forward when D = M)
             b_bytes = s * (3 * w.D + 3 * w.M) * w.token_heads
             b_ms = (bwd_ms - fwd_ms) / args.steps
+            b_traffic = None
             name, timing = "tc_dkdv_kernel", "backward call minus one forward launch"
-        kernels.append({"kernel": name, "bound": "hbm", "bytes_per_launch": b_bytes,
-                        "avg_launch_ms": b_ms, "achieved": b_bytes / (b_ms / 1e3) / 1e9,
-                        "frac": b_bytes / (b_ms / 1e3) / 1e9 / hbm_gbs,
-                        "traffic": bwd_traffic if name == "tc_bwd_kernel" else None,
-                        "timing": timing})
+        bwd_entry = {"kernel": name, "bound": "hbm", "bytes_per_launch": b_bytes,
+                     "avg_launch_ms": b_ms, "achieved": b_bytes / (b_ms / 1e3) / 1e9,
+                     "frac": b_bytes / (b_ms / 1e3) / 1e9 / hbm_gbs, "traffic": b_traffic,
+                     "timing": timing}
+    if bwd_entry is not None and bwd_entry["kernel"] == "tc_bwd_kernel":
+        dominant, kernels = bwd_entry, [fwd_entry]
+    else:
+        dominant, kernels = fwd_entry, [bwd_entry] if bwd_entry is not None else []
     step_roofline_ms = algorithmic_bytes(w) / (hbm_gbs * 1e9) * 1e3
 
     line = {
@@ -540,12 +551,11 @@ def run_ours(args, world, rank, local):
                    "fwd_ms": fwd_ms / args.steps, "bwd_ms": bwd_ms / args.steps,
                    "step_hbm_roofline_frac": step_roofline_ms / ms_per_step,
                    "parallelism": f"replicas x{world} (b,h)-sharded, no collective"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
-                     "frac": achieved / hbm_gbs, "traffic": traffic,
-                     "kernel": "tc_causal_kernel (one causal product per launch)",
-                     "peak_source": f"{peak_src} hbm_gbs",
-                     "bytes_per_launch": bytes_per_launch, "avg_launch_ms": avg_launch_ms,
-                     "timing": "forward call: one launch, CUDA events on its stream",
+        "roofline": {"bound": "hbm", "achieved": dominant["achieved"], "peak": hbm_gbs,
+                     "unit": "GB/s", "frac": dominant["frac"], "traffic": dominant["traffic"],
+                     "kernel": dominant["kernel"], "peak_source": f"{peak_src} hbm_gbs",
+                     "bytes_per_launch": dominant["bytes_per_launch"],
+                     "avg_launch_ms": dominant["avg_launch_ms"], "timing": dominant["timing"],
                      "other_kernels": kernels},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(t_start, t_end, soak_from),
