@@ -187,6 +187,15 @@ CP_API cp_status_t causal_product_fwd_noalloc(const void* q, const void* k, cons
                                               int64_t B, int64_t H, int64_t N, int64_t D, int64_t M,
                                               cp_dtype_t dtype, void* stream);
 
+/* Self-test of the failure path (no counterpart on the pages): one block
+ * waits on a barrier that nothing arrives at, gives up after `wait_ns`
+ * nanoseconds (1 ns .. 1 s) and records CP_ERR_TIMEOUT in the status word of
+ * `workspace` (at least 256 bytes, 16-byte aligned), exactly as a kernel
+ * whose bounded wait runs out.  No fault, no trap; the context stays usable.
+ * Read the result with causal_product_status. */
+CP_API cp_status_t causal_product_selftest_timeout(void* workspace, uint64_t wait_ns,
+                                                   void* stream);
+
 /* Synchronises `stream`, then returns and clears the status word in
  * `workspace` (CP_OK or CP_ERR_TIMEOUT), or CP_ERR_CUDA if the stream
  * reports an error. */

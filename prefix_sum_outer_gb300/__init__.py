@@ -34,6 +34,7 @@ __all__ = [
 
 CP_DTYPE_F32, CP_DTYPE_BF16 = 0, 1
 CP_OK = 0
+CP_ERR_TIMEOUT = 7
 _DTYPES = {torch.float32: CP_DTYPE_F32, torch.bfloat16: CP_DTYPE_BF16}
 
 _lib = None
@@ -73,6 +74,8 @@ def load_library(rebuild: bool = True) -> ctypes.CDLL:
             lib.causal_product_bwd_state.argtypes = [p, p, p, p, p, p, p, p, p, p, i64, i64, i64,
                                                      i64, i64, c_int, p, sz, p]
             lib.causal_product_bwd_state.restype = c_int
+            lib.causal_product_selftest_timeout.argtypes = [p, ctypes.c_uint64, p]
+            lib.causal_product_selftest_timeout.restype = c_int
             lib.causal_product_decode.argtypes = [p, p, p, p, p, i64, i64, i64, i64, c_int, p]
             lib.causal_product_decode.restype = c_int
             lib.causal_product_fwd_noalloc.argtypes = [p, p, p, p, i64, i64, i64, i64, i64, c_int,
@@ -267,6 +270,17 @@ def causal_product_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     if rc != CP_OK:
         raise CausalProductError(rc, "causal_product_decode")
     return out
+
+
+def causal_product_selftest_timeout(workspace: torch.Tensor, wait_ns: int = 20_000_000,
+                                    stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Enqueue the failure-path self-test: a bounded wait that runs out and
+    records CP_ERR_TIMEOUT in ``workspace``'s status word (read it with
+    causal_product_status)."""
+    rc = load_library().causal_product_selftest_timeout(workspace.data_ptr(), int(wait_ns),
+                                                        _stream_ptr(stream, workspace.device))
+    if rc != CP_OK:
+        raise CausalProductError(rc, "causal_product_selftest_timeout")
 
 
 def causal_product_status(workspace: torch.Tensor,

@@ -270,6 +270,16 @@ cp_status_t causal_product_decode(const void* q, const void* k, const void* v, v
              : CP_ERR_CUDA;
 }
 
+cp_status_t causal_product_selftest_timeout(void* workspace, uint64_t wait_ns, void* stream_) {
+  if (workspace == nullptr) return CP_ERR_INVALID_ARG;
+  if (!cp::aligned16(workspace)) return CP_ERR_MISALIGNED;
+  if (wait_ns == 0 || wait_ns > 1000000000ull) return CP_ERR_INVALID_ARG;
+  return cp::selftest_timeout_launch(static_cast<int*>(workspace), wait_ns,
+                                     static_cast<cudaStream_t>(stream_)) == cudaSuccess
+             ? CP_OK
+             : CP_ERR_CUDA;
+}
+
 cp_status_t causal_product_status(void* workspace, void* stream_) {
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   if (cudaStreamSynchronize(stream) != cudaSuccess) return CP_ERR_CUDA;

@@ -92,4 +92,7 @@ cp_status_t tc_bwd_launch(const void* q, const void* k, const void* v, const voi
 cudaError_t decode_launch(const void* q, const void* k, const void* v, void* out, float* state,
                           int64_t BH, int64_t D, int64_t M, cp_dtype_t dtype, cudaStream_t stream);
 
+// ---- failure-path self-test: records CP_ERR_TIMEOUT after `wait_ns`
+cudaError_t selftest_timeout_launch(int* status, uint64_t wait_ns, cudaStream_t stream);
+
 }  // namespace cp

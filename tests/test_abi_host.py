@@ -191,3 +191,11 @@ def test_decode_argument_checks(lib):
     assert dec(st=A + 32) == INVALID_ARG
     assert dec(out=3 * A + 16) == INVALID_ARG
     assert dec(out=5 * A + 64) == INVALID_ARG
+
+
+def test_selftest_argument_checks(lib):
+    st = lib.causal_product_selftest_timeout
+    assert st(None, 1000, None) == INVALID_ARG
+    assert st(A + 8, 1000, None) == MISALIGNED
+    assert st(A, 0, None) == INVALID_ARG
+    assert st(A, 2_000_000_000, None) == INVALID_ARG
