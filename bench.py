@@ -493,6 +493,51 @@ def run_ours(args, world, rank, local):
                "frac": dec_bytes / (dec_ms / 1e3) / 1e9 / load_peaks()[0],
                "kernel": "decode_kernel", "bound": "hbm"}
 
+    # ---- normaliser z_i = q_i . sum_{j<=i} k_j of the same q, k, and its
+    # backward (dq, dk from dL/dz); vector scans, bound by HBM
+    norm = None
+    if not args.no_extras:
+        gz = torch.randn((w.B, w.H, w.N), generator=torch.Generator().manual_seed(78)).to(dev)
+        zb = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+        nq, nk = torch.empty_like(qd), torch.empty_like(kd)
+        ws_n = torch.zeros(cp.load_library().causal_product_normalizer_workspace_size(
+            w.B, w.H, w.N, w.D, 1 if w.dtype == "bf16" else 0), dtype=torch.uint8, device=dev)
+
+        def norm_fwd():
+            cp.causal_product_normalizer(qd, kd, z=zb, workspace=ws_n, stream=stream)
+
+        def norm_bwd():
+            cp.causal_product_normalizer_bwd(qd, kd, gz, nq, nk, workspace=ws_n, stream=stream)
+
+        def timed(fn, n=20):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(n):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return max_over_ranks(e0.elapsed_time(e1), world) / n
+
+        nf_ms, nb_ms = timed(norm_fwd), timed(norm_bwd)
+        s_ = 2 if w.dtype == "bf16" else 4
+        # forward reads q and k, writes z (fp32); backward reads k, q and
+        # dL/dz twice and writes dq and dk
+        nf_bytes = (2 * s_ * w.D + 4) * w.token_heads
+        nb_bytes = (4 * s_ * w.D + 8) * w.token_heads
+        peak = load_peaks()[0]
+        norm = {"kernel": "norm_lb_kernel (single pass, look-back)", "bound": "hbm",
+                "fwd": {"us": nf_ms * 1e3, "bytes": nf_bytes,
+                        "achieved_gbs": nf_bytes / (nf_ms / 1e3) / 1e9,
+                        "frac": nf_bytes / (nf_ms / 1e3) / 1e9 / peak},
+                "bwd": {"us": nb_ms * 1e3, "bytes": nb_bytes,
+                        "achieved_gbs": nb_bytes / (nb_ms / 1e3) / 1e9,
+                        "frac": nb_bytes / (nb_ms / 1e3) / 1e9 / peak},
+                "timing": "CUDA events over 20 calls each; a call is a workspace fill and "
+                          "one launch per output (z; dq then dk)"}
+
     # ---- roofline of the dominant kernel.  Unsplit problems on fewer than
     # the SMs: the single backward launch (dk/dv and dq scans; the backward
     # call is exactly that launch, timed by its own events); otherwise the
@@ -561,6 +606,7 @@ def run_ours(args, world, rank, local):
         "clocks": clocks.summary(t_start, t_end, soak_from),
         "e2e": e2e,
         "decode": dec,
+        "normalizer": norm,
         "carried_state": None if state_ms is None else {
             "ms_per_step": state_ms, "value": w.token_heads * world / (state_ms / 1e3) / 1e6,
             "unit": UNIT, "note": "fwd with S_0 in and S_N out, bwd with dS_N in and dS_0 out"},

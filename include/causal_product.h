@@ -161,6 +161,36 @@ CP_API cp_status_t causal_product_decode(const void* q, const void* k, const voi
                                          float* state, int64_t B, int64_t H, int64_t D, int64_t M,
                                          cp_dtype_t dtype, void* stream);
 
+/* Normaliser of causal linear attention ("Transformers are RNNs", the
+ * denominator of its causal attention; the pages of triton-lang/triton issue
+ * #217 cite that paper for the recurrence but their loop leaves it out):
+ *     z_i = q_i . sum_{j<=i} k_j,
+ * the causal product with a value of 1 (M = 1, v_j = 1).  For every (b,h):
+ * q, k [B,H,N,D] in `dtype` (same rules as causal_product_fwd: device
+ * pointers, 16-byte aligned, D in [1, 256], bf16 needs D % 8 == 0);
+ * z [B,H,N] fp32, written.  fp32 accumulation; sums run in a fixed order,
+ * so results are bitwise reproducible.  Workspace as for the other entry
+ * points, sized by causal_product_normalizer_workspace_size (nothing in
+ * these kernels waits, so they never write the status word).  N = 0
+ * enqueues nothing. */
+CP_API size_t causal_product_normalizer_workspace_size(int64_t B, int64_t H, int64_t N, int64_t D,
+                                                       cp_dtype_t dtype);
+CP_API cp_status_t causal_product_normalizer(const void* q, const void* k, float* z, int64_t B,
+                                             int64_t H, int64_t N, int64_t D, cp_dtype_t dtype,
+                                             void* workspace, size_t workspace_bytes,
+                                             void* stream);
+
+/* Backward of causal_product_normalizer: with grad_z = dL/dz [B,H,N] fp32,
+ *     grad_q_i = grad_z_i sum_{j<=i} k_j,
+ *     grad_k_j = sum_{i>=j} grad_z_i q_i,
+ * written in `dtype` ([B,H,N,D], overlapping nothing).  Two launches on
+ * `stream`; same workspace size as the forward. */
+CP_API cp_status_t causal_product_normalizer_bwd(const void* q, const void* k, const float* grad_z,
+                                                 void* grad_q, void* grad_k, int64_t B, int64_t H,
+                                                 int64_t N, int64_t D, cp_dtype_t dtype,
+                                                 void* workspace, size_t workspace_bytes,
+                                                 void* stream);
+
 /* Size of the static device scratch array behind causal_product_fwd_noalloc. */
 #define CP_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 

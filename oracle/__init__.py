@@ -16,6 +16,8 @@ it with gcc and exposes it through ctypes:
                         -> (out, state_out)           with carried state
     bwd_state(q, k, v, g, state_in=None, grad_state_out=None)
                         -> (dq, dk, dv, grad_state_in)
+    norm(q, k)          -> z = q_i . sum_{j<=i} k_j   (float64 [..., N])
+    norm_bwd(q, k, g)   -> (dq, dk)                   (g = dL/dz, [..., N])
 
 States are [..., D, M] arrays; they may be float64 (the oracle's own
 states) as well as float32 or bfloat16 values, all exact in double.
@@ -77,6 +79,10 @@ def _load():
             lib.cpo_bwd_state.argtypes = [p, p, p, p, p, p, p, p, p, p, i64, i64, i64, i64,
                                           c_int]
             lib.cpo_bwd_state.restype = c_int
+            lib.cpo_norm.argtypes = [p, p, p, i64, i64, i64, c_int]
+            lib.cpo_norm.restype = c_int
+            lib.cpo_norm_bwd.argtypes = [p, p, p, p, p, i64, i64, i64, c_int]
+            lib.cpo_norm_bwd.restype = c_int
             lib.cpo_threads.argtypes = [c_int]
             lib.cpo_threads.restype = c_int
             _lib = lib
@@ -181,3 +187,38 @@ def bwd_state(q, k, v, g, state_in=None, grad_state_out=None, nthreads: int = 0)
     if rc != 0:
         raise RuntimeError(f"oracle bwd_state failed ({rc})")
     return dq, dk, dv, ds0
+
+
+def _qk_dims(q, k):
+    if q.ndim < 2 or q.shape != k.shape:
+        raise ValueError(f"shape mismatch: q{q.shape} k{k.shape}")
+    lead = q.shape[:-2]
+    BH = int(np.prod(lead)) if lead else 1
+    return lead, BH, q.shape[-2], q.shape[-1]
+
+
+def norm(q, k, nthreads: int = 0) -> np.ndarray:
+    """Normaliser z_i = q_i . sum_{j<=i} k_j per leading slice, in fp64."""
+    q, k = _as_f32(q), _as_f32(k)
+    lead, BH, N, D = _qk_dims(q, k)
+    z = np.zeros(lead + (N,), dtype=np.float64)
+    rc = _load().cpo_norm(q.ctypes.data, k.ctypes.data, z.ctypes.data, BH, N, D, int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle norm failed ({rc})")
+    return z
+
+
+def norm_bwd(q, k, g, nthreads: int = 0):
+    """(dq, dk) of L = sum_i g_i z_i: dq_i = g_i sum_{j<=i} k_j,
+    dk_j = sum_{i>=j} g_i q_i, in fp64."""
+    q, k, g = _as_f32(q), _as_f32(k), _as_f32(g)
+    lead, BH, N, D = _qk_dims(q, k)
+    if g.shape != lead + (N,):
+        raise ValueError(f"grad shape {g.shape} != z shape {lead + (N,)}")
+    dq = np.zeros(lead + (N, D), dtype=np.float64)
+    dk = np.zeros(lead + (N, D), dtype=np.float64)
+    rc = _load().cpo_norm_bwd(q.ctypes.data, k.ctypes.data, g.ctypes.data, dq.ctypes.data,
+                              dk.ctypes.data, BH, N, D, int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle norm_bwd failed ({rc})")
+    return dq, dk

@@ -37,6 +37,13 @@
  *       dk_j = R_j v_j,    dv_j = R_j^T k_j,    dS_0 = R_0
  *   (S_0 enters every S_i, and dS_N every R_j).  Absent states are zero.
  *
+ *   Normaliser.  Causal linear attention ("Transformers are RNNs", the
+ *   paper the issue cites for the recurrence) divides each output row by
+ *       z_i = q_i . c_i,       c_i = sum_{j<=i} k_j
+ *   (the issue's loop leaves it out).  Its backward, from the definition
+ *   with L = sum_i g_i z_i:
+ *       dq_i = g_i c_i,        dk_j = sum_{i>=j} g_i q_i.
+ *
  * Inputs are float32 arrays holding the exact values the GPU receives
  * (bfloat16 values are exactly representable in float32 and in double);
  * each slice is widened to double before any arithmetic.  Outputs are
@@ -225,4 +232,61 @@ int cpo_bwd(const float *q, const float *k, const float *v, const float *g,
             int64_t BH, int64_t N, int64_t D, int64_t M, int nthreads) {
     if (N == 0) return (BH < 0 || D <= 0 || M <= 0) ? -1 : 0;
     return cpo_bwd_state(q, k, v, g, NULL, NULL, dq, dk, dv, NULL, BH, N, D, M, nthreads);
+}
+
+/* Normaliser over BH slices: z [BH][N] (double) = q_i . sum_{j<=i} k_j. */
+int cpo_norm(const float *q, const float *k, double *z, int64_t BH, int64_t N, int64_t D,
+             int nthreads) {
+    if (BH < 0 || N < 0 || D <= 0) return -1;
+    if (BH == 0 || N == 0) return 0;
+    set_threads(nthreads);
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+    for (int64_t bh = 0; bh < BH; ++bh) {
+        double *c = (double *)calloc((size_t)D, sizeof(double));
+        if (!c) { err |= 1; continue; }
+        const float *qs = q + bh * N * D, *ks = k + bh * N * D;
+        for (int64_t i = 0; i < N; ++i) {
+            /* c += k_i, then z_i = q_i . c */
+            for (int64_t d = 0; d < D; ++d) c[d] += (double)ks[i * D + d];
+            double acc = 0.0;
+            for (int64_t d = 0; d < D; ++d) acc += (double)qs[i * D + d] * c[d];
+            z[bh * N + i] = acc;
+        }
+        free(c);
+    }
+    return err ? -2 : 0;
+}
+
+/* Backward of the normaliser: g [BH][N] is dL/dz; writes dq, dk [BH][N][D]. */
+int cpo_norm_bwd(const float *q, const float *k, const float *g, double *dq, double *dk,
+                 int64_t BH, int64_t N, int64_t D, int nthreads) {
+    if (BH < 0 || N < 0 || D <= 0) return -1;
+    if (BH == 0 || N == 0) return 0;
+    set_threads(nthreads);
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+    for (int64_t bh = 0; bh < BH; ++bh) {
+        double *c = (double *)calloc((size_t)D, sizeof(double));
+        if (!c) { err |= 1; continue; }
+        const float *qs = q + bh * N * D, *ks = k + bh * N * D, *gs = g + bh * N;
+        double *dqs = dq + bh * N * D, *dks = dk + bh * N * D;
+        /* forward sweep: c_i = sum_{j<=i} k_j ; dq_i = g_i c_i */
+        for (int64_t i = 0; i < N; ++i) {
+            for (int64_t d = 0; d < D; ++d) {
+                c[d] += (double)ks[i * D + d];
+                dqs[i * D + d] = (double)gs[i] * c[d];
+            }
+        }
+        /* reverse sweep: r_j = sum_{i>=j} g_i q_i ; dk_j = r_j */
+        memset(c, 0, sizeof(double) * (size_t)D);
+        for (int64_t j = N - 1; j >= 0; j--) {
+            for (int64_t d = 0; d < D; ++d) {
+                c[d] += (double)gs[j] * (double)qs[j * D + d];
+                dks[j * D + d] = c[d];
+            }
+        }
+        free(c);
+    }
+    return err ? -2 : 0;
 }

@@ -27,7 +27,8 @@ from . import build as _build
 
 __all__ = [
     "CP_OK", "CausalProductError", "causal_product", "causal_product_fwd", "causal_product_bwd",
-    "causal_product_fwd_noalloc",
+    "causal_product_fwd_noalloc", "causal_product_decode",
+    "causal_product_normalizer", "causal_product_normalizer_bwd", "normalizer",
     "causal_product_workspace_size", "causal_product_status", "causal_product_error_string",
     "library_path", "load_library",
 ]
@@ -81,6 +82,13 @@ def load_library(rebuild: bool = True) -> ctypes.CDLL:
             lib.causal_product_fwd_noalloc.argtypes = [p, p, p, p, i64, i64, i64, i64, i64, c_int,
                                                        p]
             lib.causal_product_fwd_noalloc.restype = c_int
+            lib.causal_product_normalizer_workspace_size.argtypes = [i64, i64, i64, i64, c_int]
+            lib.causal_product_normalizer_workspace_size.restype = sz
+            lib.causal_product_normalizer.argtypes = [p, p, p, i64, i64, i64, i64, c_int, p, sz, p]
+            lib.causal_product_normalizer.restype = c_int
+            lib.causal_product_normalizer_bwd.argtypes = [p, p, p, p, p, i64, i64, i64, i64, c_int,
+                                                          p, sz, p]
+            lib.causal_product_normalizer_bwd.restype = c_int
             lib.causal_product_status.argtypes = [p, p]
             lib.causal_product_status.restype = c_int
             lib.causal_product_error_string.argtypes = [c_int]
@@ -272,6 +280,64 @@ def causal_product_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     return out
 
 
+def _qk_dims(q: torch.Tensor, k: torch.Tensor):
+    if q.dim() != 4 or k.shape != q.shape:
+        raise ValueError(f"expected q,k [B,H,N,D]; got {tuple(q.shape)}, {tuple(k.shape)}")
+    return tuple(q.shape)
+
+
+def causal_product_normalizer(q: torch.Tensor, k: torch.Tensor,
+                              z: Optional[torch.Tensor] = None,
+                              workspace: Optional[torch.Tensor] = None,
+                              stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """z[b,h,i] = q[b,h,i] . sum_{j<=i} k[b,h,j] (float32 [B,H,N]): the
+    denominator of causal linear attention."""
+    B, H, N, D = _qk_dims(q, k)
+    code = _dtype_code(q, k)
+    if z is None:
+        z = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if z.dtype != torch.float32 or tuple(z.shape) != (B, H, N):
+        raise ValueError(f"z must be float32 of shape {(B, H, N)}")
+    _check_device(q, k, z)
+    lib = load_library()
+    need = lib.causal_product_normalizer_workspace_size(B, H, N, D, code)
+    if workspace is None:
+        workspace = _workspace(need, q.device)
+    rc = lib.causal_product_normalizer(q.data_ptr(), k.data_ptr(), z.data_ptr(), B, H, N, D, code,
+                                       workspace.data_ptr(), workspace.numel(),
+                                       _stream_ptr(stream, q.device))
+    if rc != CP_OK:
+        raise CausalProductError(rc, "causal_product_normalizer")
+    return z
+
+
+def causal_product_normalizer_bwd(q: torch.Tensor, k: torch.Tensor, grad_z: torch.Tensor,
+                                  grad_q: Optional[torch.Tensor] = None,
+                                  grad_k: Optional[torch.Tensor] = None,
+                                  workspace: Optional[torch.Tensor] = None,
+                                  stream: Optional[torch.cuda.Stream] = None):
+    """(dq, dk) of L = <grad_z, z>: dq_i = grad_z_i sum_{j<=i} k_j,
+    dk_j = sum_{i>=j} grad_z_i q_i, in q's dtype."""
+    B, H, N, D = _qk_dims(q, k)
+    code = _dtype_code(q, k)
+    if grad_z.dtype != torch.float32 or tuple(grad_z.shape) != (B, H, N):
+        raise ValueError(f"grad_z must be float32 of shape {(B, H, N)}")
+    grad_q = torch.empty_like(q) if grad_q is None else grad_q
+    grad_k = torch.empty_like(k) if grad_k is None else grad_k
+    _check_device(q, k, grad_z, grad_q, grad_k)
+    lib = load_library()
+    need = lib.causal_product_normalizer_workspace_size(B, H, N, D, code)
+    if workspace is None:
+        workspace = _workspace(need, q.device)
+    rc = lib.causal_product_normalizer_bwd(q.data_ptr(), k.data_ptr(), grad_z.data_ptr(),
+                                           grad_q.data_ptr(), grad_k.data_ptr(), B, H, N, D, code,
+                                           workspace.data_ptr(), workspace.numel(),
+                                           _stream_ptr(stream, q.device))
+    if rc != CP_OK:
+        raise CausalProductError(rc, "causal_product_normalizer_bwd")
+    return grad_q, grad_k
+
+
 def causal_product_selftest_timeout(workspace: torch.Tensor, wait_ns: int = 20_000_000,
                                     stream: Optional[torch.cuda.Stream] = None) -> None:
     """Enqueue the failure-path self-test: a bounded wait that runs out and
@@ -303,6 +369,26 @@ class CausalProduct(torch.autograd.Function):
     def backward(ctx, g):
         q, k, v = ctx.saved_tensors
         return causal_product_bwd(q, k, v, g.contiguous().to(q.dtype))
+
+
+class Normalizer(torch.autograd.Function):
+    """Autograd wrapper of the normaliser: (q, k) -> z."""
+
+    @staticmethod
+    def forward(ctx, q, k):
+        q, k = q.contiguous(), k.contiguous()
+        ctx.save_for_backward(q, k)
+        return causal_product_normalizer(q, k)
+
+    @staticmethod
+    def backward(ctx, gz):
+        q, k = ctx.saved_tensors
+        return causal_product_normalizer_bwd(q, k, gz.contiguous().float())
+
+
+def normalizer(q: torch.Tensor, k: torch.Tensor) -> torch.Tensor:
+    """z_i = q_i . sum_{j<=i} k_j (float32 [B,H,N]) with autograd support."""
+    return Normalizer.apply(q, k)
 
 
 class CausalProductState(torch.autograd.Function):

@@ -99,6 +99,19 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 
+cp_status_t check_norm_dims(int64_t B, int64_t H, int64_t N, int64_t D, cp_dtype_t dtype) {
+  if (B <= 0 || H <= 0 || N < 0) return CP_ERR_INVALID_ARG;
+  if (dtype != CP_DTYPE_F32 && dtype != CP_DTYPE_BF16) return CP_ERR_UNSUPPORTED_DTYPE;
+  if (D < 1 || D > 256) return CP_ERR_UNSUPPORTED_SHAPE;
+  if (dtype == CP_DTYPE_BF16 && (D % 8) != 0) return CP_ERR_UNSUPPORTED_SHAPE;
+  if (B * H > (int64_t)1 << 24 || N > (int64_t)1 << 31) return CP_ERR_UNSUPPORTED_SHAPE;
+  return CP_OK;
+}
+
+size_t norm_workspace_bytes(int64_t BH, int64_t N, int64_t D, cp_dtype_t dtype) {
+  return kStatusBytes + round_up(norm_scratch_bytes(BH, N, D, dtype));
+}
+
 }  // namespace
 }  // namespace cp
 
@@ -266,6 +279,81 @@ cp_status_t causal_product_decode(const void* q, const void* k, const void* v, v
   if (cp::overlaps(out, nv, state, nst)) return CP_ERR_INVALID_ARG;
   return cp::decode_launch(q, k, v, out, state, BH, D, M, dtype,
                            static_cast<cudaStream_t>(stream_)) == cudaSuccess
+             ? CP_OK
+             : CP_ERR_CUDA;
+}
+
+size_t causal_product_normalizer_workspace_size(int64_t B, int64_t H, int64_t N, int64_t D,
+                                                cp_dtype_t dtype) {
+  if (cp::check_norm_dims(B, H, N, D, dtype) != CP_OK) return 0;
+  return cp::norm_workspace_bytes(B * H, N, D, dtype);
+}
+
+cp_status_t causal_product_normalizer(const void* q, const void* k, float* z, int64_t B, int64_t H,
+                                      int64_t N, int64_t D, cp_dtype_t dtype, void* workspace,
+                                      size_t workspace_bytes, void* stream_) {
+  cp_status_t st = cp::check_norm_dims(B, H, N, D, dtype);
+  if (st != CP_OK) return st;
+  if (N > 0 && (!q || !k || !z)) return CP_ERR_INVALID_ARG;
+  if (!cp::aligned16(q) || !cp::aligned16(k) || !cp::aligned16(z)) return CP_ERR_MISALIGNED;
+  const size_t es = dtype == CP_DTYPE_F32 ? 4 : 2;
+  const int64_t BH = B * H;
+  const size_t nqk = (size_t)BH * N * D * es, nz = (size_t)BH * N * sizeof(float);
+  if (cp::overlaps(z, nz, q, nqk) || cp::overlaps(z, nz, k, nqk)) return CP_ERR_INVALID_ARG;
+  const size_t need = cp::norm_workspace_bytes(BH, N, D, dtype);
+  if (workspace != nullptr && workspace_bytes < need) return CP_ERR_WORKSPACE_TOO_SMALL;
+  if (N == 0) return CP_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  cp::Scratch s;
+  st = cp::acquire(s, workspace, workspace_bytes, need, stream);
+  if (st != CP_OK) return st;
+  int* status = static_cast<int*>(s.base);
+  void* scratch = static_cast<char*>(s.base) + cp::kStatusBytes;
+  if (s.owned && cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess)
+    return CP_ERR_CUDA;
+  return cp::norm_launch(0, q, k, nullptr, z, nullptr, BH, N, D, dtype, scratch, status,
+                         stream) == cudaSuccess
+             ? CP_OK
+             : CP_ERR_CUDA;
+}
+
+cp_status_t causal_product_normalizer_bwd(const void* q, const void* k, const float* grad_z,
+                                          void* grad_q, void* grad_k, int64_t B, int64_t H,
+                                          int64_t N, int64_t D, cp_dtype_t dtype, void* workspace,
+                                          size_t workspace_bytes, void* stream_) {
+  cp_status_t st = cp::check_norm_dims(B, H, N, D, dtype);
+  if (st != CP_OK) return st;
+  if (N > 0 && (!q || !k || !grad_z || !grad_q || !grad_k)) return CP_ERR_INVALID_ARG;
+  const void* ptrs[5] = {q, k, grad_z, grad_q, grad_k};
+  for (const void* p : ptrs)
+    if (!cp::aligned16(p)) return CP_ERR_MISALIGNED;
+  const size_t es = dtype == CP_DTYPE_F32 ? 4 : 2;
+  const int64_t BH = B * H;
+  const size_t nqk = (size_t)BH * N * D * es, nz = (size_t)BH * N * sizeof(float);
+  const void* ins[3] = {q, k, grad_z};
+  const size_t in_sz[3] = {nqk, nqk, nz};
+  for (int i = 0; i < 3; ++i)
+    if (cp::overlaps(grad_q, nqk, ins[i], in_sz[i]) || cp::overlaps(grad_k, nqk, ins[i], in_sz[i]))
+      return CP_ERR_INVALID_ARG;
+  if (cp::overlaps(grad_q, nqk, grad_k, nqk)) return CP_ERR_INVALID_ARG;
+  const size_t need = cp::norm_workspace_bytes(BH, N, D, dtype);
+  if (workspace != nullptr && workspace_bytes < need) return CP_ERR_WORKSPACE_TOO_SMALL;
+  if (N == 0) return CP_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  cp::Scratch s;
+  st = cp::acquire(s, workspace, workspace_bytes, need, stream);
+  if (st != CP_OK) return st;
+  int* status = static_cast<int*>(s.base);
+  void* scratch = static_cast<char*>(s.base) + cp::kStatusBytes;
+  if (s.owned && cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess)
+    return CP_ERR_CUDA;
+  // dq scans k forwards, dk scans g q backwards; they share the scratch
+  // area one after the other on the stream
+  if (cp::norm_launch(1, q, k, grad_z, nullptr, grad_q, BH, N, D, dtype, scratch, status,
+                      stream) != cudaSuccess)
+    return CP_ERR_CUDA;
+  return cp::norm_launch(2, q, k, grad_z, nullptr, grad_k, BH, N, D, dtype, scratch, status,
+                         stream) == cudaSuccess
              ? CP_OK
              : CP_ERR_CUDA;
 }

@@ -92,6 +92,16 @@ cp_status_t tc_bwd_launch(const void* q, const void* k, const void* v, const voi
 cudaError_t decode_launch(const void* q, const void* k, const void* v, void* out, float* state,
                           int64_t BH, int64_t D, int64_t M, cp_dtype_t dtype, cudaStream_t stream);
 
+// ---- normaliser (SIMT): mode 0: z_i = q_i . sum_{j<=i} k_j (fp32 z);
+// mode 1: dq_i = g_i sum_{j<=i} k_j; mode 2: dk_j = sum_{i>=j} g_i q_i
+// (dq, dk in the input dtype; g fp32).  `scratch` (256-byte aligned) holds
+// norm_scratch_bytes(...); a bounded wait that runs out records
+// CP_ERR_TIMEOUT in *status.
+size_t norm_scratch_bytes(int64_t BH, int64_t N, int64_t D, cp_dtype_t dtype);
+cudaError_t norm_launch(int mode, const void* q, const void* k, const float* grad_z, float* z,
+                        void* out, int64_t BH, int64_t N, int64_t D, cp_dtype_t dtype,
+                        void* scratch, int* status, cudaStream_t stream);
+
 // ---- failure-path self-test: records CP_ERR_TIMEOUT after `wait_ns`
 cudaError_t selftest_timeout_launch(int* status, uint64_t wait_ns, cudaStream_t stream);
 

@@ -99,6 +99,19 @@ def make_inputs(B: int, H: int, N: int, D: int, M: int, dtype: torch.dtype, seed
     return cast(q), cast(k), cast(v), cast(g)
 
 
+def make_norm_inputs(B: int, H: int, N: int, D: int, dtype: torch.dtype, seed: int,
+                     feature: str = "elu", x_std: float = 1.0):
+    """Inputs of the normaliser: CPU tensors q, k [B,H,N,D] in ``dtype`` (the
+    same draw as ``make_inputs`` with M = 1) and grad_z ~ N(0, 1), float32
+    [B,H,N], from a second generator seeded ``seed + 7919``."""
+    q, k, _, _ = make_inputs(B, H, N, D, 1, dtype, seed, feature=feature, x_std=x_std,
+                             backward=False)
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(int(seed) + 7919)
+    gz = torch.randn((B, H, N), generator=gen, dtype=torch.float32)
+    return q, k, gz
+
+
 def workload_inputs(w: Workload, N: Optional[int] = None, BH_limit: Optional[int] = None):
     """Inputs of a named workload; ``N``/``BH_limit`` shrink it for quick checks
     (the draw is then of the smaller shape, same seed and distributions)."""

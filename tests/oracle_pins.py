@@ -1,8 +1,9 @@
 """Pins for the causal-product oracle.
 
 Each pin checks an implementation ``impl`` (an object with ``fwd(q,k,v)``,
-``bwd(q,k,v,g)``, ``fwd_state(q,k,v,s0)`` and ``bwd_state(q,k,v,g,s0,ds_n)``
-returning float64 numpy arrays, like ``oracle``)
+``bwd(q,k,v,g)``, ``fwd_state(q,k,v,s0)``, ``bwd_state(q,k,v,g,s0,ds_n)``,
+``norm(q,k)`` and ``norm_bwd(q,k,g)`` returning float64 numpy arrays, like
+``oracle``)
 against something other than the recurrence itself: hand-worked values,
 a brute-force quadratic form, closed forms, textbook special cases,
 linearity, causality and finite differences.  ``tests/test_oracle.py``
@@ -354,4 +355,82 @@ def pin_state_token_by_token(impl, n=9):
 
 STATE_PINS = [pin_state_closed_forms, pin_state_chunking, pin_state_finite_differences,
               pin_state_token_by_token]
-ALL_PINS = FWD_PINS + BWD_PINS + STATE_PINS
+
+
+# --------------------------------------------------------------------------
+# normaliser pins: z_i = q_i . sum_{j<=i} k_j and its backward
+# --------------------------------------------------------------------------
+
+def _norm_case(seed, shape=(2, 2, 13, 5)):
+    rng = _rng(seed)
+    q = _dyadic(rng, shape, -2, 2, 8)
+    k = _dyadic(rng, shape, -2, 2, 8)
+    g = _dyadic(rng, shape[:-1], -2, 2, 8)
+    return q, k, g
+
+
+def pin_norm_quadratic_form(impl):
+    """z = rowsum(tril(Q K^T)) and, for L = g . z, dq = diag(g) A K and
+    dk = A^T diag(g) Q with A the lower-triangular matrix of ones: the
+    quadratic form written with dense matrices (exact for dyadic inputs)."""
+    for seed, shape in ((31, (2, 2, 13, 5)), (32, (1, 1, 1, 1)), (33, (1, 3, 40, 8))):
+        q, k, g = _norm_case(seed, shape)
+        N = shape[-2]
+        A = np.tril(np.ones((N, N)))
+        qd, kd, gd = (x.astype(np.float64) for x in (q, k, g))
+        z_ref = np.einsum("...ij,...ij->...i", A * (qd @ np.swapaxes(kd, -1, -2)), np.ones((N, N)))
+        assert np.array_equal(impl.norm(q, k), z_ref), "norm quadratic form"
+        dq, dk = impl.norm_bwd(q, k, g)
+        assert np.array_equal(dq, gd[..., None] * (A @ kd)), "norm dq quadratic form"
+        assert np.array_equal(dk, A.T @ (gd[..., None] * qd)), "norm dk quadratic form"
+
+
+def pin_norm_is_product_with_ones(impl):
+    """The normaliser is the causal product with a single value column of
+    ones, and its gradients are the product's with grad_out = g."""
+    q, k, g = _norm_case(34, (2, 3, 21, 6))
+    ones = np.ones(q.shape[:-1] + (1,), np.float32)
+    assert np.array_equal(impl.norm(q, k), impl.fwd(q, k, ones)[..., 0]), "norm vs product"
+    dq, dk = impl.norm_bwd(q, k, g)
+    pq, pk, _ = impl.bwd(q, k, ones, g[..., None])
+    assert np.array_equal(dq, pq) and np.array_equal(dk, pk), "norm bwd vs product bwd"
+
+
+def pin_norm_closed_forms(impl):
+    """Row 0 is q_0 . k_0, the last row is q_{N-1} . sum_j k_j; dk of the
+    first row is sum_i g_i q_i, of the last row g_{N-1} q_{N-1}; dq of the
+    last row is g_{N-1} sum_j k_j."""
+    q, k, g = _norm_case(35, (1, 2, 17, 7))
+    qd, kd, gd = (x.astype(np.float64) for x in (q, k, g))
+    z = impl.norm(q, k)
+    assert np.array_equal(z[..., 0], np.sum(qd[..., 0, :] * kd[..., 0, :], -1)), "norm row 0"
+    assert np.array_equal(z[..., -1], np.sum(qd[..., -1, :] * kd.sum(-2), -1)), "norm last row"
+    dq, dk = impl.norm_bwd(q, k, g)
+    assert np.array_equal(dk[..., 0, :], (gd[..., None] * qd).sum(-2)), "norm dk row 0"
+    assert np.array_equal(dk[..., -1, :], gd[..., -1, None] * qd[..., -1, :]), "norm dk last row"
+    assert np.array_equal(dq[..., -1, :], gd[..., -1, None] * kd.sum(-2)), "norm dq last row"
+
+
+def pin_norm_finite_differences(impl, shape=(1, 1, 6, 3)):
+    """L = g . z is linear in q for fixed k (and in k for fixed q), so a
+    central difference with a unit step is exact for dyadic inputs."""
+    q, k, g = _norm_case(36, shape)
+    gd = g.astype(np.float64)
+    dq, dk = impl.norm_bwd(q, k, g)
+    for name, x, grad in (("q", q, dq), ("k", k, dk)):
+        fd = np.zeros(x.shape)
+        for idx in np.ndindex(*x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += 1.0
+            xm[idx] -= 1.0
+            if name == "q":
+                lp, lm = (np.sum(gd * impl.norm(a, k)) for a in (xp, xm))
+            else:
+                lp, lm = (np.sum(gd * impl.norm(q, a)) for a in (xp, xm))
+            fd[idx] = (lp - lm) / 2.0
+        assert np.allclose(grad, fd, rtol=1e-12, atol=1e-12), ("norm finite differences", name)
+
+
+NORM_PINS = [pin_norm_quadratic_form, pin_norm_is_product_with_ones, pin_norm_closed_forms,
+             pin_norm_finite_differences]
+ALL_PINS = FWD_PINS + BWD_PINS + STATE_PINS + NORM_PINS

@@ -199,3 +199,44 @@ def test_selftest_argument_checks(lib):
     assert st(A + 8, 1000, None) == MISALIGNED
     assert st(A, 0, None) == INVALID_ARG
     assert st(A, 2_000_000_000, None) == INVALID_ARG
+
+
+def test_normalizer_argument_checks(lib):
+    ws = lib.causal_product_normalizer_workspace_size
+    assert ws(8, 16, 4096, 64, BF16) >= 256 and ws(8, 16, 4096, 64, BF16) % 256 == 0
+    assert ws(1, 1, 65536, 64, BF16) > 256      # few long problems: segment sums
+    assert ws(8, 16, 0, 64, BF16) == 256
+    assert ws(0, 16, 4096, 64, BF16) == 0
+    assert ws(1, 1, 16, 12, BF16) == 0
+    assert ws(1, 1, 16, 257, F32) == 0
+
+    def fwd(**kw):
+        a = dict(q=A, k=2 * A, z=3 * A, B=1, H=2, N=64, D=16, dtype=F32, ws=None, wsb=0)
+        a.update(kw)
+        return lib.causal_product_normalizer(a["q"], a["k"], a["z"], a["B"], a["H"], a["N"],
+                                             a["D"], a["dtype"], a["ws"], a["wsb"], None)
+
+    assert fwd(z=None) == INVALID_ARG
+    assert fwd(q=A + 8) == MISALIGNED
+    assert fwd(D=0) == UNSUPPORTED_SHAPE
+    assert fwd(D=12, dtype=BF16) == UNSUPPORTED_SHAPE
+    assert fwd(dtype=3) == UNSUPPORTED_DTYPE
+    assert fwd(B=-1) == INVALID_ARG
+    assert fwd(z=A + 64) == INVALID_ARG                 # z inside q
+    assert fwd(ws=8 * A, wsb=16) == WS_TOO_SMALL
+    assert fwd(N=0) == OK and fwd(N=0, q=None, k=None, z=None) == OK
+
+    def bwd(**kw):
+        a = dict(q=A, k=2 * A, g=3 * A, dq=4 * A, dk=5 * A, B=1, H=2, N=64, D=16, dtype=F32)
+        a.update(kw)
+        return lib.causal_product_normalizer_bwd(a["q"], a["k"], a["g"], a["dq"], a["dk"],
+                                                 a["B"], a["H"], a["N"], a["D"], a["dtype"],
+                                                 None, 0, None)
+
+    assert bwd(dk=None) == INVALID_ARG
+    assert bwd(g=3 * A + 4) == MISALIGNED
+    assert bwd(D=300) == UNSUPPORTED_SHAPE
+    assert bwd(dq=5 * A) == INVALID_ARG                 # dq and dk alias
+    assert bwd(dk=3 * A + 16) == INVALID_ARG            # dk over grad_z
+    assert bwd(dq=2 * A + 32) == INVALID_ARG            # dq over k
+    assert bwd(N=0) == OK

@@ -60,6 +60,26 @@ MUTANTS = {
                                    "    /* dS_0 = R_0 */\n    if (dS0) { memcpy(dS0, R, sizeof(double) * (size_t)(D * M));"
                                    " for (int64_t d = 0; d < D; ++d) for (int64_t m = 0; m < M; ++m)"
                                    " dS0[d * M + m] -= q[d] * g[m]; }")],
+    # the normaliser reads the running sum before adding row i (exclusive)
+    "norm_exclusive": [("/* c += k_i, then z_i = q_i . c */\n"
+                        "            for (int64_t d = 0; d < D; ++d) c[d] += (double)ks[i * D + d];\n"
+                        "            double acc = 0.0;\n"
+                        "            for (int64_t d = 0; d < D; ++d) acc += (double)qs[i * D + d] * c[d];",
+                        "double acc = 0.0;\n"
+                        "            for (int64_t d = 0; d < D; ++d) acc += (double)qs[i * D + d] * c[d];\n"
+                        "            for (int64_t d = 0; d < D; ++d) c[d] += (double)ks[i * D + d];")],
+    # the normaliser's readout uses k instead of q
+    "norm_reads_k": [("acc += (double)qs[i * D + d] * c[d];", "acc += (double)ks[i * D + d] * c[d];")],
+    # dq of the normaliser without the gradient factor
+    "norm_dq_drops_g": [("dqs[i * D + d] = (double)gs[i] * c[d];", "dqs[i * D + d] = c[d];")],
+    # dk of the normaliser summed forwards instead of backwards
+    "norm_dk_forward": [("for (int64_t j = N - 1; j >= 0; j--) {\n            for (int64_t d = 0; d < D; ++d) {\n"
+                         "                c[d] += (double)gs[j]",
+                         "for (int64_t j = 0; j < N; ++j) {\n            for (int64_t d = 0; d < D; ++d) {\n"
+                         "                c[d] += (double)gs[j]")],
+    # dk of the normaliser uses k instead of q
+    "norm_dk_uses_k": [("c[d] += (double)gs[j] * (double)qs[j * D + d];",
+                        "c[d] += (double)gs[j] * (double)ks[j * D + d];")],
 }
 
 
@@ -71,7 +91,28 @@ class _Impl:
         lib.cpo_bwd.argtypes = [p, p, p, p, p, p, p, i64, i64, i64, i64, c_int]
         lib.cpo_fwd_state.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, c_int]
         lib.cpo_bwd_state.argtypes = [p, p, p, p, p, p, p, p, p, p, i64, i64, i64, i64, c_int]
+        lib.cpo_norm.argtypes = [p, p, p, i64, i64, i64, c_int]
+        lib.cpo_norm_bwd.argtypes = [p, p, p, p, p, i64, i64, i64, c_int]
         self.lib = lib
+
+    def norm(self, q, k):
+        q, k = (np.ascontiguousarray(x, np.float32) for x in (q, k))
+        lead = q.shape[:-2]
+        BH = int(np.prod(lead)) if lead else 1
+        N, D = q.shape[-2], q.shape[-1]
+        z = np.zeros(lead + (N,))
+        assert self.lib.cpo_norm(q.ctypes.data, k.ctypes.data, z.ctypes.data, BH, N, D, 1) == 0
+        return z
+
+    def norm_bwd(self, q, k, g):
+        q, k, g = (np.ascontiguousarray(x, np.float32) for x in (q, k, g))
+        lead = q.shape[:-2]
+        BH = int(np.prod(lead)) if lead else 1
+        N, D = q.shape[-2], q.shape[-1]
+        dq, dk = np.zeros(lead + (N, D)), np.zeros(lead + (N, D))
+        assert self.lib.cpo_norm_bwd(q.ctypes.data, k.ctypes.data, g.ctypes.data, dq.ctypes.data,
+                                     dk.ctypes.data, BH, N, D, 1) == 0
+        return dq, dk
 
     def fwd(self, q, k, v):
         q, k, v = (np.ascontiguousarray(x, np.float32) for x in (q, k, v))
