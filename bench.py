@@ -538,6 +538,31 @@ def run_ours(args, world, rank, local):
                 "timing": "CUDA events over 20 calls each; a call is a workspace fill and "
                           "one launch per output (z; dq then dk)"}
 
+    # ---- the forward with the feature map phi(x) = elu(x) + 1 applied to raw
+    # x_q, x_k ~ N(0, 1) inside the product kernel (both branches of phi
+    # taken); it moves the same bytes as the plain forward
+    feat = None
+    if not args.no_extras:
+        xq_, xk_, _, _ = make_inputs(w.B, w.H, w.N, w.D, 1, w.torch_dtype, seed=79,
+                                     feature="normal", backward=False)
+        xq_, xk_ = xq_.to(dev), xk_.to(dev)
+        fo = torch.empty_like(vd)
+
+        def feat_fwd():
+            cp.causal_product_fwd_feature(xq_, xk_, vd, "elu1", out=fo, workspace=ws_f,
+                                          stream=stream)
+
+        ff_ms = timed(feat_fwd)
+        s_ = 2 if w.dtype == "bf16" else 4
+        fb = s_ * (2 * w.D + 2 * w.M) * w.token_heads
+        feat = {"kernel": "tc_causal_kernel, phi = elu + 1 applied in shared memory",
+                "bound": "hbm", "us": ff_ms * 1e3, "bytes": fb,
+                "achieved_gbs": fb / (ff_ms / 1e3) / 1e9,
+                "frac": fb / (ff_ms / 1e3) / 1e9 / load_peaks()[0],
+                "plain_fwd_us": fwd_ms / args.steps * 1e3,
+                "timing": "CUDA events over 20 calls"}
+        del xq_, xk_, fo
+
     # ---- roofline of the dominant kernel.  Unsplit problems on fewer than
     # the SMs: the single backward launch (dk/dv and dq scans; the backward
     # call is exactly that launch, timed by its own events); otherwise the
@@ -607,6 +632,7 @@ def run_ours(args, world, rank, local):
         "e2e": e2e,
         "decode": dec,
         "normalizer": norm,
+        "feature_map": feat,
         "carried_state": None if state_ms is None else {
             "ms_per_step": state_ms, "value": w.token_heads * world / (state_ms / 1e3) / 1e6,
             "unit": UNIT, "note": "fwd with S_0 in and S_N out, bwd with dS_N in and dS_0 out"},

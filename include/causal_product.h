@@ -77,6 +77,13 @@ typedef enum {
   CP_DTYPE_BF16 = 1  /* bf16 in/out; bf16 tensor-core products, fp32 accumulate */
 } cp_dtype_t;
 
+/* Feature map applied to q and k before the product (causal linear
+ * attention, "Transformers are RNNs": phi(x) = elu(x) + 1). */
+typedef enum {
+  CP_FEATURE_NONE = 0,  /* q, k used as given */
+  CP_FEATURE_ELU1 = 1   /* phi(x) = x + 1 for x > 0, e^x otherwise */
+} cp_feature_t;
+
 typedef enum {
   CP_OK = 0,
   CP_ERR_INVALID_ARG = 1,        /* null pointer, negative size, aliasing outputs */
@@ -190,6 +197,41 @@ CP_API cp_status_t causal_product_normalizer_bwd(const void* q, const void* k, c
                                                  int64_t N, int64_t D, cp_dtype_t dtype,
                                                  void* workspace, size_t workspace_bytes,
                                                  void* stream);
+
+/* Forward with the feature map applied on load: out_i = sum_{j<=i}
+ * (phi(q_i) . phi(k_j)) v_j for raw inputs q, k (the linear-attention
+ * features phi(x) of "Transformers are RNNs"; the pages of
+ * triton-lang/triton issue #217 feed the product such features).  phi is
+ * computed inside the product kernels (on the tensor-core path, in shared
+ * memory after the tile is loaded; bf16 operands are phi rounded to bf16), so
+ * phi(q) and phi(k) are never written to memory.  Arguments, layout and
+ * workspace as causal_product_fwd (its workspace size serves);
+ * feature = CP_FEATURE_NONE is causal_product_fwd. */
+CP_API cp_status_t causal_product_fwd_feature(const void* q, const void* k, const void* v,
+                                              void* out, cp_feature_t feature, int64_t B,
+                                              int64_t H, int64_t N, int64_t D, int64_t M,
+                                              cp_dtype_t dtype, void* workspace,
+                                              size_t workspace_bytes, void* stream);
+
+/* Backward of causal_product_fwd_feature: grad_q = phi'(q) * dL/dphi(q),
+ * grad_k = phi'(k) * dL/dphi(k) (elementwise), grad_v as causal_product_bwd,
+ * with phi'(x) = 1 for x > 0 and e^x otherwise.  Runs phi(q) and phi(k)
+ * into the workspace, the product backward on them, then the elementwise
+ * chain rule in place on grad_q and grad_k.  Workspace: at least
+ * causal_product_feature_workspace_size(..., backward = 1) bytes (NULL:
+ * allocated and freed on `stream`). */
+CP_API cp_status_t causal_product_bwd_feature(const void* q, const void* k, const void* v,
+                                              const void* grad_out, void* grad_q, void* grad_k,
+                                              void* grad_v, cp_feature_t feature, int64_t B,
+                                              int64_t H, int64_t N, int64_t D, int64_t M,
+                                              cp_dtype_t dtype, void* workspace,
+                                              size_t workspace_bytes, void* stream);
+
+/* Workspace bytes of causal_product_fwd_feature (backward = 0, the same as
+ * causal_product_fwd) or causal_product_bwd_feature (backward = 1: the
+ * backward's workspace plus phi(q) and phi(k)); 0 for rejected arguments. */
+CP_API size_t causal_product_feature_workspace_size(int64_t B, int64_t H, int64_t N, int64_t D,
+                                                    int64_t M, cp_dtype_t dtype, int backward);
 
 /* Size of the static device scratch array behind causal_product_fwd_noalloc. */
 #define CP_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)

@@ -18,6 +18,8 @@ it with gcc and exposes it through ctypes:
                         -> (dq, dk, dv, grad_state_in)
     norm(q, k)          -> z = q_i . sum_{j<=i} k_j   (float64 [..., N])
     norm_bwd(q, k, g)   -> (dq, dk)                   (g = dL/dz, [..., N])
+    fwd_feature(q, k, v, feature="elu1")   -> out of phi(q), phi(k), v
+    bwd_feature(q, k, v, g, feature="elu1") -> (dq, dk, dv) w.r.t. raw q, k, v
 
 States are [..., D, M] arrays; they may be float64 (the oracle's own
 states) as well as float32 or bfloat16 values, all exact in double.
@@ -58,7 +60,7 @@ def build(force: bool = False) -> str:
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fopenmp",
-           "-shared", "-fPIC", "-std=c11", "-o", tmp, _SRC]
+           "-shared", "-fPIC", "-std=c11", "-o", tmp, _SRC, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -83,6 +85,11 @@ def _load():
             lib.cpo_norm.restype = c_int
             lib.cpo_norm_bwd.argtypes = [p, p, p, p, p, i64, i64, i64, c_int]
             lib.cpo_norm_bwd.restype = c_int
+            lib.cpo_fwd_feature.argtypes = [p, p, p, p, c_int, i64, i64, i64, i64, c_int]
+            lib.cpo_fwd_feature.restype = c_int
+            lib.cpo_bwd_feature.argtypes = [p, p, p, p, p, p, p, c_int, i64, i64, i64, i64,
+                                            c_int]
+            lib.cpo_bwd_feature.restype = c_int
             lib.cpo_threads.argtypes = [c_int]
             lib.cpo_threads.restype = c_int
             _lib = lib
@@ -222,3 +229,37 @@ def norm_bwd(q, k, g, nthreads: int = 0):
     if rc != 0:
         raise RuntimeError(f"oracle norm_bwd failed ({rc})")
     return dq, dk
+
+
+_FEATURES = {"none": 0, "elu1": 1}
+
+
+def fwd_feature(q, k, v, feature: str = "elu1", nthreads: int = 0) -> np.ndarray:
+    """out_i = sum_{j<=i} (phi(q_i) . phi(k_j)) v_j with phi(x) = elu(x) + 1
+    evaluated in fp64 from the raw q, k."""
+    q, k, v = _as_f32(q), _as_f32(k), _as_f32(v)
+    lead, BH, N, D, M = _dims(q, k, v)
+    out = np.zeros(lead + (N, M), dtype=np.float64)
+    rc = _load().cpo_fwd_feature(q.ctypes.data, k.ctypes.data, v.ctypes.data, out.ctypes.data,
+                                 _FEATURES[feature], BH, N, D, M, int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle fwd_feature failed ({rc})")
+    return out
+
+
+def bwd_feature(q, k, v, g, feature: str = "elu1", nthreads: int = 0):
+    """(dq, dk, dv) of L = <g, out> for fwd_feature, with respect to the raw
+    q, k and v, in fp64."""
+    q, k, v, g = _as_f32(q), _as_f32(k), _as_f32(v), _as_f32(g)
+    lead, BH, N, D, M = _dims(q, k, v)
+    if g.shape != v.shape:
+        raise ValueError(f"grad shape {g.shape} != out shape {v.shape}")
+    dq = np.zeros(lead + (N, D), dtype=np.float64)
+    dk = np.zeros(lead + (N, D), dtype=np.float64)
+    dv = np.zeros(lead + (N, M), dtype=np.float64)
+    rc = _load().cpo_bwd_feature(q.ctypes.data, k.ctypes.data, v.ctypes.data, g.ctypes.data,
+                                 dq.ctypes.data, dk.ctypes.data, dv.ctypes.data,
+                                 _FEATURES[feature], BH, N, D, M, int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle bwd_feature failed ({rc})")
+    return dq, dk, dv

@@ -44,6 +44,12 @@
  *   with L = sum_i g_i z_i:
  *       dq_i = g_i c_i,        dk_j = sum_{i>=j} g_i q_i.
  *
+ *   Feature map.  Causal linear attention feeds the product phi(q) and
+ *   phi(k), with phi(x) = elu(x) + 1 (x + 1 for x > 0, e^x otherwise) in
+ *   "Transformers are RNNs".  The feature entry points take the raw q, k,
+ *   map them in double, run the same recurrences, and apply the chain rule
+ *   dL/dx = dL/dphi * phi'(x), phi'(x) = 1 for x > 0, e^x otherwise.
+ *
  * Inputs are float32 arrays holding the exact values the GPU receives
  * (bfloat16 values are exactly representable in float32 and in double);
  * each slice is widened to double before any arithmetic.  Outputs are
@@ -52,6 +58,7 @@
  * Parallelism: OpenMP over the independent (b,h) slices only; the sweep
  * inside a slice is the plain serial loop, in sequence order.
  */
+#include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -62,6 +69,22 @@
 /* Widen one [N][C] float slice to double. */
 static void widen(const float *src, double *dst, int64_t n) {
     for (int64_t i = 0; i < n; ++i) dst[i] = (double)src[i];
+}
+
+/* The feature map (feature 1: elu + 1) and its derivative. */
+static double phi(int feature, double x) {
+    if (feature == 1) return x > 0.0 ? x + 1.0 : exp(x);
+    return x;
+}
+
+static double dphi(int feature, double x) {
+    if (feature == 1) return x > 0.0 ? 1.0 : exp(x);
+    return 1.0;
+}
+
+/* Widen one [N][C] float slice to double, mapped by the feature map. */
+static void widen_phi(const float *src, double *dst, int64_t n, int feature) {
+    for (int64_t i = 0; i < n; ++i) dst[i] = phi(feature, (double)src[i]);
 }
 
 /* Forward recurrence on one (b,h) slice; all arrays double, row-major.
@@ -287,6 +310,59 @@ int cpo_norm_bwd(const float *q, const float *k, const float *g, double *dq, dou
             }
         }
         free(c);
+    }
+    return err ? -2 : 0;
+}
+
+/* Forward of the causal product of phi(q), phi(k) and v (feature 0: q, k
+ * as given, feature 1: elu + 1). */
+int cpo_fwd_feature(const float *q, const float *k, const float *v, double *out, int feature,
+                    int64_t BH, int64_t N, int64_t D, int64_t M, int nthreads) {
+    if (BH < 0 || N < 0 || D <= 0 || M <= 0 || feature < 0 || feature > 1) return -1;
+    if (BH == 0 || N == 0) return 0;
+    set_threads(nthreads);
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+    for (int64_t bh = 0; bh < BH; ++bh) {
+        double *buf = (double *)malloc(sizeof(double) * (size_t)(N * (2 * D + M) + D * M));
+        if (!buf) { err |= 1; continue; }
+        double *qd = buf, *kd = qd + N * D, *vd = kd + N * D, *S = vd + N * M;
+        widen_phi(q + bh * N * D, qd, N * D, feature);
+        widen_phi(k + bh * N * D, kd, N * D, feature);
+        widen(v + bh * N * M, vd, N * M);
+        fwd_slice(qd, kd, vd, out + bh * N * M, S, NULL, NULL, N, D, M);
+        free(buf);
+    }
+    return err ? -2 : 0;
+}
+
+/* Backward of cpo_fwd_feature with respect to the raw q, k and v. */
+int cpo_bwd_feature(const float *q, const float *k, const float *v, const float *g, double *dq,
+                    double *dk, double *dv, int feature, int64_t BH, int64_t N, int64_t D,
+                    int64_t M, int nthreads) {
+    if (BH < 0 || N < 0 || D <= 0 || M <= 0 || feature < 0 || feature > 1) return -1;
+    if (BH == 0 || N == 0) return 0;
+    set_threads(nthreads);
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+    for (int64_t bh = 0; bh < BH; ++bh) {
+        double *buf = (double *)malloc(sizeof(double) * (size_t)(N * (2 * D + 2 * M) + D * M));
+        if (!buf) { err |= 1; continue; }
+        double *qd = buf, *kd = qd + N * D, *vd = kd + N * D, *gd = vd + N * M;
+        double *S = gd + N * M;
+        const float *qs = q + bh * N * D, *ks = k + bh * N * D;
+        widen_phi(qs, qd, N * D, feature);
+        widen_phi(ks, kd, N * D, feature);
+        widen(v + bh * N * M, vd, N * M);
+        widen(g + bh * N * M, gd, N * M);
+        double *dqs = dq + bh * N * D, *dks = dk + bh * N * D;
+        bwd_slice(qd, kd, vd, gd, dqs, dks, dv + bh * N * M, S, NULL, NULL, NULL, N, D, M);
+        /* chain rule through phi */
+        for (int64_t e = 0; e < N * D; ++e) {
+            dqs[e] *= dphi(feature, (double)qs[e]);
+            dks[e] *= dphi(feature, (double)ks[e]);
+        }
+        free(buf);
     }
     return err ? -2 : 0;
 }

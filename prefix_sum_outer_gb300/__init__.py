@@ -29,6 +29,7 @@ __all__ = [
     "CP_OK", "CausalProductError", "causal_product", "causal_product_fwd", "causal_product_bwd",
     "causal_product_fwd_noalloc", "causal_product_decode",
     "causal_product_normalizer", "causal_product_normalizer_bwd", "normalizer",
+    "causal_product_fwd_feature", "causal_product_bwd_feature", "FEATURES",
     "causal_product_workspace_size", "causal_product_status", "causal_product_error_string",
     "library_path", "load_library",
 ]
@@ -37,6 +38,14 @@ CP_DTYPE_F32, CP_DTYPE_BF16 = 0, 1
 CP_OK = 0
 CP_ERR_TIMEOUT = 7
 _DTYPES = {torch.float32: CP_DTYPE_F32, torch.bfloat16: CP_DTYPE_BF16}
+# feature maps applied to q and k inside the kernels (cp_feature_t)
+FEATURES = {None: 0, "none": 0, "elu1": 1}
+
+
+def _feature_code(feature) -> int:
+    if feature not in FEATURES:
+        raise ValueError(f"unknown feature map {feature!r}; expected one of {list(FEATURES)}")
+    return FEATURES[feature]
 
 _lib = None
 _lock = threading.Lock()
@@ -89,6 +98,15 @@ def load_library(rebuild: bool = True) -> ctypes.CDLL:
             lib.causal_product_normalizer_bwd.argtypes = [p, p, p, p, p, i64, i64, i64, i64, c_int,
                                                           p, sz, p]
             lib.causal_product_normalizer_bwd.restype = c_int
+            lib.causal_product_fwd_feature.argtypes = [p, p, p, p, c_int, i64, i64, i64, i64, i64,
+                                                       c_int, p, sz, p]
+            lib.causal_product_fwd_feature.restype = c_int
+            lib.causal_product_bwd_feature.argtypes = [p, p, p, p, p, p, p, c_int, i64, i64, i64,
+                                                       i64, i64, c_int, p, sz, p]
+            lib.causal_product_bwd_feature.restype = c_int
+            lib.causal_product_feature_workspace_size.argtypes = [i64, i64, i64, i64, i64, c_int,
+                                                                  c_int]
+            lib.causal_product_feature_workspace_size.restype = sz
             lib.causal_product_status.argtypes = [p, p]
             lib.causal_product_status.restype = c_int
             lib.causal_product_error_string.argtypes = [c_int]
@@ -188,6 +206,62 @@ def causal_product_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     if rc != CP_OK:
         raise CausalProductError(rc, "causal_product_fwd")
     return (out, state_out) if return_state else out
+
+
+def causal_product_fwd_feature(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                               feature: str = "elu1", out: Optional[torch.Tensor] = None,
+                               workspace: Optional[torch.Tensor] = None,
+                               stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """out_i = sum_{j<=i} (phi(q_i) . phi(k_j)) v_j with phi applied inside the
+    kernels (``feature="elu1"``: phi(x) = elu(x) + 1); q and k are the raw
+    inputs."""
+    B, H, N, D, M = _dims(q, k, v)
+    code = _dtype_code(q, k, v)
+    if out is None:
+        out = torch.empty((B, H, N, M), dtype=q.dtype, device=q.device)
+    _check_device(q, k, v, out)
+    lib = load_library()
+    need = lib.causal_product_feature_workspace_size(B, H, N, D, M, code, 0)
+    if workspace is None:
+        workspace = _workspace(need, q.device)
+    rc = lib.causal_product_fwd_feature(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                        _feature_code(feature), B, H, N, D, M, code,
+                                        workspace.data_ptr(), workspace.numel(),
+                                        _stream_ptr(stream, q.device))
+    if rc != CP_OK:
+        raise CausalProductError(rc, "causal_product_fwd_feature")
+    return out
+
+
+def causal_product_bwd_feature(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                               grad_out: torch.Tensor, feature: str = "elu1",
+                               grad_q: Optional[torch.Tensor] = None,
+                               grad_k: Optional[torch.Tensor] = None,
+                               grad_v: Optional[torch.Tensor] = None,
+                               workspace: Optional[torch.Tensor] = None,
+                               stream: Optional[torch.cuda.Stream] = None):
+    """(dq, dk, dv) of L = <grad_out, out> for causal_product_fwd_feature,
+    with respect to the raw q, k and v."""
+    B, H, N, D, M = _dims(q, k, v)
+    code = _dtype_code(q, k, v, grad_out)
+    if grad_out.shape != v.shape:
+        raise ValueError("grad_out must have v's shape")
+    grad_q = torch.empty_like(q) if grad_q is None else grad_q
+    grad_k = torch.empty_like(k) if grad_k is None else grad_k
+    grad_v = torch.empty_like(v) if grad_v is None else grad_v
+    _check_device(q, k, v, grad_out, grad_q, grad_k, grad_v)
+    lib = load_library()
+    need = lib.causal_product_feature_workspace_size(B, H, N, D, M, code, 1)
+    if workspace is None:
+        workspace = _workspace(need, q.device)
+    rc = lib.causal_product_bwd_feature(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                        grad_out.data_ptr(), grad_q.data_ptr(), grad_k.data_ptr(),
+                                        grad_v.data_ptr(), _feature_code(feature), B, H, N, D, M,
+                                        code, workspace.data_ptr(), workspace.numel(),
+                                        _stream_ptr(stream, q.device))
+    if rc != CP_OK:
+        raise CausalProductError(rc, "causal_product_bwd_feature")
+    return grad_q, grad_k, grad_v
 
 
 def causal_product_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
@@ -391,6 +465,23 @@ def normalizer(q: torch.Tensor, k: torch.Tensor) -> torch.Tensor:
     return Normalizer.apply(q, k)
 
 
+class CausalProductFeature(torch.autograd.Function):
+    """Autograd wrapper with the feature map applied inside the kernels."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, feature):
+        q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+        ctx.save_for_backward(q, k, v)
+        ctx.feature = feature
+        return causal_product_fwd_feature(q, k, v, feature)
+
+    @staticmethod
+    def backward(ctx, g):
+        q, k, v = ctx.saved_tensors
+        dq, dk, dv = causal_product_bwd_feature(q, k, v, g.contiguous().to(q.dtype), ctx.feature)
+        return dq, dk, dv, None
+
+
 class CausalProductState(torch.autograd.Function):
     """Autograd wrapper with a carried state: (q, k, v, S_0) -> (out, S_N)."""
 
@@ -413,12 +504,18 @@ class CausalProductState(torch.autograd.Function):
 
 
 def causal_product(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
-                   state: Optional[torch.Tensor] = None, return_state: bool = False):
+                   state: Optional[torch.Tensor] = None, return_state: bool = False,
+                   feature: Optional[str] = None):
     """Causal dot product with autograd support (no normaliser, no scale).
 
     ``state`` (float32 [B,H,D,M]) is the state before the first row; with
     ``return_state`` the result is (out, state after the last row), both
-    differentiable."""
+    differentiable.  ``feature="elu1"`` applies phi(x) = elu(x) + 1 to q and
+    k inside the kernels (no carried state in that mode)."""
+    if _feature_code(feature) != 0:
+        if state is not None or return_state:
+            raise ValueError("a feature map is not combined with a carried state")
+        return CausalProductFeature.apply(q, k, v, feature)
     if state is None and not return_state:
         return CausalProduct.apply(q, k, v)
     out, s_n = CausalProductState.apply(q, k, v, state)

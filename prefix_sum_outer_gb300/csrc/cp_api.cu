@@ -108,6 +108,12 @@ cp_status_t check_norm_dims(int64_t B, int64_t H, int64_t N, int64_t D, cp_dtype
   return CP_OK;
 }
 
+// phi(q), phi(k) in the feature backward's workspace, after the backward's area
+size_t feature_copy_bytes(int64_t BH, int64_t N, int64_t D, cp_dtype_t dtype) {
+  const size_t es = dtype == CP_DTYPE_F32 ? 4 : 2;
+  return (size_t)BH * N * D * es;
+}
+
 size_t norm_workspace_bytes(int64_t BH, int64_t N, int64_t D, cp_dtype_t dtype) {
   return kStatusBytes + round_up(norm_scratch_bytes(BH, N, D, dtype));
 }
@@ -165,6 +171,105 @@ cp_status_t causal_product_fwd_state(const void* q, const void* k, const void* v
   p.st_ld_r = M;
   p.st_ld_c = 1;
   return cp::run_product(p, dtype, agg, status, stream);
+}
+
+size_t causal_product_feature_workspace_size(int64_t B, int64_t H, int64_t N, int64_t D,
+                                             int64_t M, cp_dtype_t dtype, int backward) {
+  if (cp::check_dims(B, H, N, D, M, dtype) != CP_OK) return 0;
+  size_t ws = cp::workspace_bytes(B * H, N, D, M, dtype, backward != 0);
+  if (backward) ws += 2 * cp::round_up(cp::feature_copy_bytes(B * H, N, D, dtype));
+  return ws;
+}
+
+cp_status_t causal_product_fwd_feature(const void* q, const void* k, const void* v, void* out,
+                                       cp_feature_t feature, int64_t B, int64_t H, int64_t N,
+                                       int64_t D, int64_t M, cp_dtype_t dtype, void* workspace,
+                                       size_t workspace_bytes, void* stream_) {
+  if (feature != CP_FEATURE_NONE && feature != CP_FEATURE_ELU1) return CP_ERR_INVALID_ARG;
+  cp_status_t st = cp::check_dims(B, H, N, D, M, dtype);
+  if (st != CP_OK) return st;
+  if (N > 0 && (!q || !k || !v || !out)) return CP_ERR_INVALID_ARG;
+  if (!cp::aligned16(q) || !cp::aligned16(k) || !cp::aligned16(v) || !cp::aligned16(out))
+    return CP_ERR_MISALIGNED;
+  const size_t es = dtype == CP_DTYPE_F32 ? 4 : 2;
+  const int64_t BH = B * H;
+  const size_t nqk = (size_t)BH * N * D * es, nv = (size_t)BH * N * M * es;
+  if (cp::overlaps(out, nv, q, nqk) || cp::overlaps(out, nv, k, nqk) || cp::overlaps(out, nv, v, nv))
+    return CP_ERR_INVALID_ARG;
+  const size_t need = cp::workspace_bytes(BH, N, D, M, dtype, false);
+  if (workspace != nullptr && workspace_bytes < need) return CP_ERR_WORKSPACE_TOO_SMALL;
+  if (N == 0) return CP_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  cp::Scratch s;
+  st = cp::acquire(s, workspace, workspace_bytes, need, stream);
+  if (st != CP_OK) return st;
+  int* status = static_cast<int*>(s.base);
+  float* agg = reinterpret_cast<float*>(static_cast<char*>(s.base) + cp::kStatusBytes);
+  if (s.owned && cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess)
+    return CP_ERR_CUDA;
+  cp::Product p{q, k, v, out, BH, N, D, M, false};
+  p.feature = feature;
+  return cp::run_product(p, dtype, agg, status, stream);
+}
+
+cp_status_t causal_product_bwd_feature(const void* q, const void* k, const void* v,
+                                       const void* grad_out, void* grad_q, void* grad_k,
+                                       void* grad_v, cp_feature_t feature, int64_t B, int64_t H,
+                                       int64_t N, int64_t D, int64_t M, cp_dtype_t dtype,
+                                       void* workspace, size_t workspace_bytes, void* stream_) {
+  if (feature == CP_FEATURE_NONE)
+    return causal_product_bwd(q, k, v, grad_out, grad_q, grad_k, grad_v, B, H, N, D, M, dtype,
+                              workspace, workspace_bytes, stream_);
+  if (feature != CP_FEATURE_ELU1) return CP_ERR_INVALID_ARG;
+  cp_status_t st = cp::check_dims(B, H, N, D, M, dtype);
+  if (st != CP_OK) return st;
+  if (N > 0 && (!q || !k || !v || !grad_out || !grad_q || !grad_k || !grad_v))
+    return CP_ERR_INVALID_ARG;
+  const void* ptrs[7] = {q, k, v, grad_out, grad_q, grad_k, grad_v};
+  for (const void* p : ptrs)
+    if (!cp::aligned16(p)) return CP_ERR_MISALIGNED;
+  const int64_t BH = B * H;
+  {
+    const size_t es = dtype == CP_DTYPE_F32 ? 4 : 2;
+    const size_t nqk = (size_t)BH * N * D * es, nv = (size_t)BH * N * M * es;
+    const void* ins[4] = {q, k, v, grad_out};
+    const size_t in_sz[4] = {nqk, nqk, nv, nv};
+    void* outs[3] = {grad_q, grad_k, grad_v};
+    const size_t out_sz[3] = {nqk, nqk, nv};
+    for (int o = 0; o < 3; ++o) {
+      for (int i = 0; i < 4; ++i)
+        if (cp::overlaps(outs[o], out_sz[o], ins[i], in_sz[i])) return CP_ERR_INVALID_ARG;
+      for (int o2 = o + 1; o2 < 3; ++o2)
+        if (cp::overlaps(outs[o], out_sz[o], outs[o2], out_sz[o2])) return CP_ERR_INVALID_ARG;
+    }
+  }
+  const size_t bwd_ws = cp::workspace_bytes(BH, N, D, M, dtype, true);
+  const size_t copy = cp::round_up(cp::feature_copy_bytes(BH, N, D, dtype));
+  const size_t need = bwd_ws + 2 * copy;
+  if (workspace != nullptr && workspace_bytes < need) return CP_ERR_WORKSPACE_TOO_SMALL;
+  if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return CP_ERR_MISALIGNED;
+  if (N == 0) return CP_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  cp::Scratch s;
+  st = cp::acquire(s, workspace, workspace_bytes, need, stream);
+  if (st != CP_OK) return st;
+  if (s.owned && cudaMemsetAsync(s.base, 0, sizeof(int), stream) != cudaSuccess)
+    return CP_ERR_CUDA;
+  char* fq = static_cast<char*>(s.base) + bwd_ws;
+  char* fk = fq + copy;
+  const int64_t n = BH * N * D;
+  if (cp::feature_map_launch(feature, q, fq, n, dtype, stream) != cudaSuccess ||
+      cp::feature_map_launch(feature, k, fk, n, dtype, stream) != cudaSuccess)
+    return CP_ERR_CUDA;
+  // the product backward on phi(q), phi(k)
+  st = causal_product_bwd(fq, fk, v, grad_out, grad_q, grad_k, grad_v, B, H, N, D, M, dtype,
+                          s.base, bwd_ws, stream_);
+  if (st != CP_OK) return st;
+  if (cp::feature_grad_launch(feature, q, grad_q, n, dtype, stream) != cudaSuccess ||
+      cp::feature_grad_launch(feature, k, grad_k, n, dtype, stream) != cudaSuccess)
+    return CP_ERR_CUDA;
+  return CP_OK;
 }
 
 cp_status_t causal_product_fwd(const void* q, const void* k, const void* v, void* out, int64_t B,

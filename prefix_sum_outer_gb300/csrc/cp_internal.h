@@ -42,6 +42,8 @@ struct Product {
   const float* state_in = nullptr;
   float* state_out = nullptr;
   int64_t st_ld_r = 0, st_ld_c = 0;
+  // feature map applied to q and k as they are loaded (cp_feature_t)
+  int feature = 0;
 };
 
 // ---- fp32 (SIMT FMA) path
@@ -101,6 +103,13 @@ size_t norm_scratch_bytes(int64_t BH, int64_t N, int64_t D, cp_dtype_t dtype);
 cudaError_t norm_launch(int mode, const void* q, const void* k, const float* grad_z, float* z,
                         void* out, int64_t BH, int64_t N, int64_t D, cp_dtype_t dtype,
                         void* scratch, int* status, cudaStream_t stream);
+
+// ---- feature map, elementwise over n elements of `dtype`:
+// feature_map: y = phi(x); feature_grad: g *= phi'(x) in place
+cudaError_t feature_map_launch(int feature, const void* x, void* y, int64_t n, cp_dtype_t dtype,
+                               cudaStream_t stream);
+cudaError_t feature_grad_launch(int feature, const void* x, void* g, int64_t n,
+                                cp_dtype_t dtype, cudaStream_t stream);
 
 // ---- failure-path self-test: records CP_ERR_TIMEOUT after `wait_ns`
 cudaError_t selftest_timeout_launch(int* status, uint64_t wait_ns, cudaStream_t stream);

@@ -37,7 +37,10 @@ struct SimtArgs {
   const float* state_in;
   float* state_out;
   int64_t st_ld_r, st_ld_c;
+  int feature;  // 1: phi(x) = elu(x) + 1 applied to q and k on load
 };
+
+__device__ __forceinline__ float elu1(float x) { return x > 0.f ? x + 1.f : expf(x); }
 
 __global__ void __launch_bounds__(kThreads) simt_kernel(SimtArgs a) {
   extern __shared__ float smem[];
@@ -95,8 +98,14 @@ __global__ void __launch_bounds__(kThreads) simt_kernel(SimtArgs a) {
       const int r = e / D, d = e % D;
       const int64_t row = r0 + r;
       const bool in = row < seg_hi;
-      Ks[r * ldq + d] = in ? kb[row * D + d] : 0.f;
-      if (!a.agg_only) Qs[r * ldq + d] = in ? qb[row * D + d] : 0.f;
+      float kx = in ? kb[row * D + d] : 0.f;
+      if (a.feature && in) kx = elu1(kx);
+      Ks[r * ldq + d] = kx;
+      if (!a.agg_only) {
+        float qx = in ? qb[row * D + d] : 0.f;
+        if (a.feature && in) qx = elu1(qx);
+        Qs[r * ldq + d] = qx;
+      }
     }
     for (int e = threadIdx.x; e < kC * Mb; e += kThreads) {
       const int r = e / Mb, m = e % Mb;
@@ -204,6 +213,7 @@ cudaError_t simt_launch(const Product& p, const SimtPlan& plan, float* agg, int*
   a.state_out = p.state_out;
   a.st_ld_r = p.st_ld_r;
   a.st_ld_c = p.st_ld_c;
+  a.feature = p.feature;
   const int64_t problems = p.BH * plan.n_mb;
   if (plan.G > 1) {
     a.agg_only = 1;

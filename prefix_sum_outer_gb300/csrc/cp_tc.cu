@@ -12,22 +12,22 @@
 namespace cp {
 namespace tc {
 
-template <int DP, int MB, bool AGG_ONLY, bool STATE_OUT>
+template <int DP, int MB, bool AGG_ONLY, bool STATE_OUT, bool FEAT>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_o, const Args a) {
-  causal_body<DP, MB, AGG_ONLY, STATE_OUT>(tm_q, tm_k, tm_v, tm_o, a,
-                                           Phase{(int)blockIdx.x, true, true});
+  causal_body<DP, MB, AGG_ONLY, STATE_OUT, FEAT>(tm_q, tm_k, tm_v, tm_o, a,
+                                                 Phase{(int)blockIdx.x, true, true});
 }
 
 // ------------------------------------------------------------------ host
-template <int DP, int MB, bool AGG, bool STATE_OUT = false>
+template <int DP, int MB, bool AGG, bool STATE_OUT = false, bool FEAT = false>
 cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                        const CUtensorMap& o, const Args& a, unsigned grid, cudaStream_t st) {
   using L = Layout<DP, MB>;
-  auto kern = tc_causal_kernel<DP, MB, AGG, STATE_OUT>;
+  auto kern = tc_causal_kernel<DP, MB, AGG, STATE_OUT, FEAT>;
   // the shared-memory opt-in is set once per device for each instantiation
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
@@ -63,15 +63,19 @@ cudaError_t launch_pair(const CUtensorMap& q, const CUtensorMap& k, const CUtens
     b.agg_out = agg;
     b.state_in = nullptr;   // aggregates are the segments' own sums
     b.state_out = nullptr;
-    e = launch_one<DP, MB, true>(q, k, v, o, b, (unsigned)(problems * (plan.G - 1)), st);
+    const unsigned g1 = (unsigned)(problems * (plan.G - 1));
+    e = a.feature ? launch_one<DP, MB, true, false, true>(q, k, v, o, b, g1, st)
+                  : launch_one<DP, MB, true>(q, k, v, o, b, g1, st);
     if (e != cudaSuccess || agg_only) return e;
     a.agg_in = agg;
   } else if (agg_only) {
     return cudaSuccess;
   }
-  if (a.state_out != nullptr)
-    return launch_one<DP, MB, false, true>(q, k, v, o, a, (unsigned)(problems * plan.G), st);
-  return launch_one<DP, MB, false>(q, k, v, o, a, (unsigned)(problems * plan.G), st);
+  const unsigned g2 = (unsigned)(problems * plan.G);
+  // (a feature map is never combined with a carried state)
+  if (a.feature) return launch_one<DP, MB, false, false, true>(q, k, v, o, a, g2, st);
+  if (a.state_out != nullptr) return launch_one<DP, MB, false, true>(q, k, v, o, a, g2, st);
+  return launch_one<DP, MB, false>(q, k, v, o, a, g2, st);
 }
 
 }  // namespace tc
@@ -123,6 +127,7 @@ cp_status_t tc_run(const Product& p, const TcPlan& plan, float* agg, int* status
   a.st_ld_c = p.st_ld_c;
   a.Dr = (int)p.D;
   a.Mc = (int)p.M;
+  a.feature = p.feature;
   const int64_t problems = p.BH * plan.n_mb;
   cudaError_t e;
 #define CP_TC_CASE(DP_, MB_)                                                                  \

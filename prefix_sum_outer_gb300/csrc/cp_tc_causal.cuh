@@ -30,6 +30,11 @@
 // stream, and no global memory is touched before it has completed.  The
 // next kernel is allowed to start once every block has passed that wait.
 //
+// With a feature map (the FEAT instantiation), the loaded Q and K tiles are
+// raw inputs x: the state and O groups map them in shared memory, phi(x) =
+// elu(x) + 1 (x + 1 for x > 0, e^x otherwise, rounded to bf16), before any
+// MMA reads them, so phi(q) and phi(k) never exist in global memory.
+//
 // Long sequences with few problems are split into G segments per problem;
 // a first launch of the same kernel in aggregate-only mode writes each
 // segment's sum of k v^T, and every segment of the second launch starts
@@ -76,7 +81,27 @@ struct Args {
   float* state_out;
   int64_t st_ld_r, st_ld_c;
   int Dr, Mc;
+  int feature;  // 0: q, k used as given; 1: phi = elu + 1 (FEAT instantiation)
 };
+
+// phi(x) = elu(x) + 1 on a pair of bf16 values, in packed bf16x2
+// arithmetic: phi(x) = e^min(x, 0) + max(x, 0), with min and max exact
+// (NaN-propagating) and e^n = 2^(n log2 e) by the change of base.  log2 e
+// is split into two bf16 parts (0x3fb9 = 1.4453125 and 0xbb2c =
+// -0.00262451171875, together within 5e-6 of it) so the product n log2 e
+// is rounded once, by the FMA; 2^y is the hardware base-2 exponential on
+// bf16 pairs, and the sum is rounded to bf16 once.
+__device__ __forceinline__ uint32_t elu1_bf16x2(uint32_t w) {
+  constexpr uint32_t kLog2eHi = 0x3fb93fb9u, kLog2eLo = 0xbb2cbb2cu;
+  uint32_t mn, mx, t, y, e, r;
+  asm("min.NaN.bf16x2 %0, %1, %2;" : "=r"(mn) : "r"(w), "r"(0u));
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(mx) : "r"(w), "r"(0u));
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(t) : "r"(mn), "r"(kLog2eLo));
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(y) : "r"(mn), "r"(kLog2eHi), "r"(t));
+  asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(e) : "r"(y));
+  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(e), "r"(mx));
+  return r;
+}
 
 template <int DP, int MB>
 struct Layout {
@@ -139,8 +164,9 @@ struct Layout {
 // tensor maps are the kernel's __grid_constant__ parameters.  STATE_OUT:
 // the launch writes the final state (a separate instantiation: the write,
 // though it runs once, costs the whole kernel registers).
+// FEAT: q and k are raw inputs mapped by phi = elu + 1 in shared memory.
 // Returns false when a wait gave up.
-template <int DP, int MB, bool AGG_ONLY, bool STATE_OUT>
+template <int DP, int MB, bool AGG_ONLY, bool STATE_OUT, bool FEAT = false>
 __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                             const CUtensorMap& tm_v, const CUtensorMap& tm_o,
                                             const Args& a, const Phase ph) {
@@ -174,6 +200,16 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
   uint64_t* fin = s_done + 2;               // [3] issuer drains before TMEM release
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(s_done + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(s_done + 6);
+  uint64_t* qk_ready = s_done + 7;          // [NQK] S, O groups -> MMA: Q/K(t) mapped (FEAT)
+  // the barrier the MMA issuers wait on before reading a Q/K stage
+  uint64_t* const qk_bar = FEAT ? qk_ready : full_qk;
+  // FEAT: warps that map a tile (the state group; the O group too when
+  // there are outputs) and their threads
+  constexpr int kMapWarps = AGG_ONLY ? kSWarps : kSWarps + kOWarps;
+  // a group maps tile it + kAhead during its iteration it: as far ahead as
+  // the Q/K ring allows, off the MMA chain (mapping tile it + kAhead needs
+  // only the stage tile it - 1 releases)
+  constexpr int kAhead = NQK - 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -203,6 +239,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
     for (int i = 0; i < NQK; ++i) {
       mbar_init(&full_qk[i], 1);
       mbar_init(&empty_qk[i], kRel);
+      if (FEAT) mbar_init(&qk_ready[i], kMapWarps);
     }
     for (int i = 0; i < NV; ++i) {
       mbar_init(&full_v[i], 1);
@@ -253,6 +290,30 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
   const int wq = warp & 3;                 // TMEM lane quarter of this warp
   const int row = wq * 32 + lane;          // tile row = TMEM lane
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+
+  // FEAT: phi applied in place to the landed Q/K tiles of tile it (K only in
+  // the aggregate-only mode, which loads no Q) by the kMapWarps mapping
+  // warps, each thread taking every (32 kMapWarps)-th 16-byte chunk from
+  // mtid on; the issuers wait on qk_ready for all of them
+  auto map_qk = [&](int it, int mtid) -> bool {
+    if (!mbar_wait(&full_qk[it % NQK], (it / NQK) & 1, abort_flag)) return false;
+    uint8_t* q_s = qk_ring + (it % NQK) * L::kQKBytes;
+    uint4* p = reinterpret_cast<uint4*>(AGG_ONLY ? q_s + L::kQBytes : q_s);
+    constexpr int kChunks = (AGG_ONLY ? 1 : 2) * L::kQBytes / 16;
+#pragma unroll 2
+    for (int i = mtid; i < kChunks; i += 32 * kMapWarps) {
+      uint4 w = p[i];
+      w.x = elu1_bf16x2(w.x);
+      w.y = elu1_bf16x2(w.y);
+      w.z = elu1_bf16x2(w.z);
+      w.w = elu1_bf16x2(w.w);
+      p[i] = w;
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&qk_ready[it % NQK]);
+    return true;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -360,7 +421,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
       };
       if (AGG_ONLY) {
         for (int it = 0; it < n_it; ++it) {
-          if (!mbar_wait(&full_qk[it % NQK], (it / NQK) & 1, abort_flag) ||
+          if (!mbar_wait(&qk_bar[it % NQK], (it / NQK) & 1, abort_flag) ||
               !mbar_wait(&full_v[it % NV], (it / NV) & 1, abort_flag)) {
             ok = false;
             break;
@@ -378,7 +439,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
         int nS = 0, nQ = 0;
         while (nQ < n_it) {
           bool progressed = false;
-          if (nS < n_it && mbar_test_wait(&full_qk[nS % NQK], (nS / NQK) & 1) &&
+          if (nS < n_it && mbar_test_wait(&qk_bar[nS % NQK], (nS / NQK) & 1) &&
               mbar_test_wait(&full_v[nS % NV], (nS / NV) & 1) &&
               mbar_test_wait(s_ready, nS & 1)) {
             tc_fence_after();
@@ -417,7 +478,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
         // issuer B: P(t) needs Q/K(t) landed and P buffer t%NP free (P V of
         // tile t - NP completed)
         for (int it = 0; it < n_it; ++it) {
-          if (!mbar_wait(&full_qk[it % NQK], (it / NQK) & 1, abort_flag) ||
+          if (!mbar_wait(&qk_bar[it % NQK], (it / NQK) & 1, abort_flag) ||
               (it >= NP && !mbar_wait(&pv_done[it % NP], ((it - NP) / NP) & 1, abort_flag))) {
             ok = false;
             break;
@@ -474,7 +535,10 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
     // ------------------------------------------------------------ state group
     bool ok = true;
     if (AGG_ONLY) {
-      if (!mbar_wait(s_done, 0, abort_flag)) {
+      for (int it = 0; FEAT && it < n_it && ok; ++it) ok = map_qk(it, threadIdx.x - 32 * kSWarp0);
+      if (!ok) {
+        record_timeout(a.status, abort_flag);
+      } else if (!mbar_wait(s_done, 0, abort_flag)) {
         record_timeout(a.status, abort_flag);
       } else if (n_it > 0) {
         tc_fence_after();
@@ -536,7 +600,13 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
         }
         tmem_st_wait();
       }
+      const int mtid = threadIdx.x - 32 * kSWarp0;  // state group: mapping threads 0..127
+      for (int j = 0; FEAT && j < kAhead && j < n_it && ok; ++j) ok = map_qk(j, mtid);
       for (int it = 0; it < n_it && ok; ++it) {
+        if (FEAT && kAhead == 0 && !map_qk(it, mtid)) {
+          ok = false;
+          break;
+        }
         const int b = it % NSB;
         uint8_t* sbuf = s_tile + b * L::kSBufBytes;
         // the Q S that last read this copy (tile it - NSB) has completed
@@ -579,6 +649,8 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(s_ready);
+        // map a later tile's Q/K while this tile's MMAs run
+        if (FEAT && kAhead > 0 && it + kAhead < n_it) ok = map_qk(it + kAhead, mtid);
       }
       // the last segment in scan order hands on the state after its last tile
       if (STATE_OUT && ok && last_seg && n_it > 0) {
@@ -641,7 +713,15 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
     // ------------------------------------------------------------ O group
     const int o_tid = threadIdx.x - 32 * kOWarp0;   // 0..kOThreads-1
     bool ok = true;
+    // FEAT: the O group maps the other half of every tile, tile it + kAhead
+    // before the read-out of tile it
+    for (int j = 0; FEAT && !AGG_ONLY && j < kAhead && j < n_it && ok; ++j)
+      ok = map_qk(j, 32 * kSWarps + o_tid);
     for (int it = 0; !AGG_ONLY && it < n_it && ok; ++it) {
+      if (FEAT && it + kAhead < n_it && !map_qk(it + kAhead, 32 * kSWarps + o_tid)) {
+        ok = false;
+        break;
+      }
       uint8_t* ob = o_tile + (it % L::kOBufs) * L::kOBytes;
       if (!mbar_wait(&o_done[it % NO], (it / NO) & 1, abort_flag)) {
         ok = false;
@@ -709,8 +789,11 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
   if (!ph.last) {
     // a later scan of this CTA reuses the barriers' memory
     __syncthreads();
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0) {
       for (uint64_t* b = bars; b < fin + 3; ++b) mbar_inval(b);
+      if (FEAT)
+        for (int i = 0; i < NQK; ++i) mbar_inval(&qk_ready[i]);
+    }
     __syncthreads();
   }
   return completed;

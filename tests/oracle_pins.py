@@ -2,8 +2,8 @@
 
 Each pin checks an implementation ``impl`` (an object with ``fwd(q,k,v)``,
 ``bwd(q,k,v,g)``, ``fwd_state(q,k,v,s0)``, ``bwd_state(q,k,v,g,s0,ds_n)``,
-``norm(q,k)`` and ``norm_bwd(q,k,g)`` returning float64 numpy arrays, like
-``oracle``)
+``norm(q,k)``, ``norm_bwd(q,k,g)``, ``fwd_feature(q,k,v)`` and
+``bwd_feature(q,k,v,g)`` returning float64 numpy arrays, like ``oracle``)
 against something other than the recurrence itself: hand-worked values,
 a brute-force quadratic form, closed forms, textbook special cases,
 linearity, causality and finite differences.  ``tests/test_oracle.py``
@@ -433,4 +433,87 @@ def pin_norm_finite_differences(impl, shape=(1, 1, 6, 3)):
 
 NORM_PINS = [pin_norm_quadratic_form, pin_norm_is_product_with_ones, pin_norm_closed_forms,
              pin_norm_finite_differences]
-ALL_PINS = FWD_PINS + BWD_PINS + STATE_PINS + NORM_PINS
+
+
+# --------------------------------------------------------------------------
+# feature-map pins: phi(x) = elu(x) + 1 applied to q and k
+# --------------------------------------------------------------------------
+
+def _elu1(x):
+    return np.where(x > 0, x + 1.0, np.exp(np.minimum(x, 0.0)))
+
+
+def pin_feature_positive_is_shift(impl):
+    """For x > 0, phi(x) = x + 1 (exact in float32 for these dyadic values)
+    and phi'(x) = 1: the feature forward and backward equal the plain ones on
+    x + 1."""
+    rng = _rng(41)
+    shape = (1, 2, 19, 5)
+    q = _dyadic(rng, shape, 0, 4, 16) + np.float32(1 / 16)
+    k = _dyadic(rng, shape, 0, 4, 16) + np.float32(1 / 16)
+    v = _dyadic(rng, shape[:-1] + (3,), -2, 2, 16)
+    g = _dyadic(rng, shape[:-1] + (3,), -2, 2, 16)
+    assert np.array_equal(impl.fwd_feature(q, k, v), impl.fwd(q + 1, k + 1, v)), "feature fwd shift"
+    a = impl.bwd_feature(q, k, v, g)
+    b = impl.bwd(q + 1, k + 1, v, g)
+    for x, y, name in zip(a, b, ("dq", "dk", "dv")):
+        assert np.array_equal(x, y), ("feature bwd shift", name)
+
+
+def pin_feature_quadratic_form(impl):
+    """out = tril(phi(Q) phi(K)^T) V with phi from numpy in fp64; the
+    gradients from the same dense form: dphi(Q) = tril(G V^T) phi(K),
+    dphi(K) = tril(G V^T)^T phi(Q), dV = tril(phi(Q) phi(K)^T)^T G, and
+    dQ = dphi(Q) * phi'(Q), dK = dphi(K) * phi'(K)."""
+    rng = _rng(42)
+    shape = (2, 1, 23, 6)
+    q = rng.standard_normal(shape).astype(np.float32)
+    k = rng.standard_normal(shape).astype(np.float32)
+    v = rng.standard_normal(shape[:-1] + (4,)).astype(np.float32)
+    g = rng.standard_normal(shape[:-1] + (4,)).astype(np.float32)
+    qd, kd, vd, gd = (x.astype(np.float64) for x in (q, k, v, g))
+    fq, fk = _elu1(qd), _elu1(kd)
+    A = np.tril(np.ones((shape[-2], shape[-2])))
+    T = lambda x: np.swapaxes(x, -1, -2)
+    P = A * (fq @ T(fk))
+    out = P @ vd
+    assert _rel(impl.fwd_feature(q, k, v), out) < 1e-12, "feature fwd dense form"
+    GV = A * (gd @ T(vd))
+    dfq, dfk, dv = GV @ fk, T(GV) @ fq, T(P) @ gd
+    dq = dfq * np.where(qd > 0, 1.0, np.exp(np.minimum(qd, 0.0)))
+    dk = dfk * np.where(kd > 0, 1.0, np.exp(np.minimum(kd, 0.0)))
+    got = impl.bwd_feature(q, k, v, g)
+    for x, y, name in zip(got, (dq, dk, dv), ("dq", "dk", "dv")):
+        assert _rel(x, y) < 1e-12, ("feature bwd dense form", name)
+
+
+def pin_feature_finite_differences(impl, shape=(1, 1, 5, 3)):
+    """Central differences of L = <g, out> with respect to the raw q and k
+    (step 2^-12, exact in float32 for these inputs) agree with the feature
+    backward to the O(h^2) truncation error.  The inputs are odd multiples of
+    1/32, away from the kink of phi'' at 0."""
+    rng = _rng(43)
+    q = _dyadic(rng, shape, -2, 2, 16) + np.float32(1 / 32)
+    k = _dyadic(rng, shape, -2, 2, 16) + np.float32(1 / 32)
+    v = _dyadic(rng, shape[:-1] + (2,), -2, 2, 16)
+    g = _dyadic(rng, shape[:-1] + (2,), -2, 2, 16)
+    gd = g.astype(np.float64)
+    dq, dk, _ = impl.bwd_feature(q, k, v, g)
+    h = np.float32(2.0 ** -12)
+    for name, x, grad in (("q", q, dq), ("k", k, dk)):
+        fd = np.zeros(x.shape)
+        for idx in np.ndindex(*x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args_p = (xp, k) if name == "q" else (q, xp)
+            args_m = (xm, k) if name == "q" else (q, xm)
+            lp = np.sum(gd * impl.fwd_feature(*args_p, v))
+            lm = np.sum(gd * impl.fwd_feature(*args_m, v))
+            fd[idx] = (lp - lm) / (2.0 * float(h))
+        assert np.allclose(grad, fd, rtol=1e-5, atol=1e-6), ("feature finite differences", name)
+
+
+FEATURE_PINS = [pin_feature_positive_is_shift, pin_feature_quadratic_form,
+                pin_feature_finite_differences]
+ALL_PINS = FWD_PINS + BWD_PINS + STATE_PINS + NORM_PINS + FEATURE_PINS

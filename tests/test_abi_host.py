@@ -240,3 +240,42 @@ def test_normalizer_argument_checks(lib):
     assert bwd(dk=3 * A + 16) == INVALID_ARG            # dk over grad_z
     assert bwd(dq=2 * A + 32) == INVALID_ARG            # dq over k
     assert bwd(N=0) == OK
+
+
+def test_feature_argument_checks(lib):
+    ws = lib.causal_product_feature_workspace_size
+    plain_f = lib.causal_product_workspace_size(8, 16, 4096, 64, 64, BF16, 0)
+    plain_b = lib.causal_product_workspace_size(8, 16, 4096, 64, 64, BF16, 1)
+    assert ws(8, 16, 4096, 64, 64, BF16, 0) == plain_f
+    # the backward keeps phi(q) and phi(k) next to its own workspace
+    assert ws(8, 16, 4096, 64, 64, BF16, 1) == plain_b + 2 * 8 * 16 * 4096 * 64 * 2
+    assert ws(8, 16, 4096, 12, 64, BF16, 1) == 0
+
+    def fwd(**kw):
+        a = dict(q=A, k=2 * A, v=3 * A, out=4 * A, feat=1, B=1, H=2, N=64, D=16, M=16, dtype=F32)
+        a.update(kw)
+        return lib.causal_product_fwd_feature(a["q"], a["k"], a["v"], a["out"], a["feat"], a["B"],
+                                              a["H"], a["N"], a["D"], a["M"], a["dtype"], None, 0,
+                                              None)
+
+    assert fwd(feat=7) == INVALID_ARG
+    assert fwd(q=A + 4) == MISALIGNED
+    assert fwd(out=2 * A + 64) == INVALID_ARG          # out over k
+    assert fwd(D=12, dtype=BF16) == UNSUPPORTED_SHAPE
+    assert fwd(N=0) == OK
+
+    def bwd(**kw):
+        a = dict(q=A, k=2 * A, v=3 * A, g=4 * A, dq=5 * A, dk=6 * A, dv=7 * A, feat=1, B=1, H=2,
+                 N=64, D=16, M=16, dtype=F32, ws=None, wsb=0)
+        a.update(kw)
+        return lib.causal_product_bwd_feature(a["q"], a["k"], a["v"], a["g"], a["dq"], a["dk"],
+                                              a["dv"], a["feat"], a["B"], a["H"], a["N"], a["D"],
+                                              a["M"], a["dtype"], a["ws"], a["wsb"], None)
+
+    assert bwd(feat=7) == INVALID_ARG
+    assert bwd(dq=None) == INVALID_ARG
+    assert bwd(k=2 * A + 8) == MISALIGNED
+    assert bwd(dq=A + 256) == INVALID_ARG              # dq over q
+    assert bwd(dk=5 * A) == INVALID_ARG                # dq and dk alias
+    assert bwd(ws=8 * A, wsb=1024) == WS_TOO_SMALL
+    assert bwd(N=0) == OK

@@ -80,6 +80,14 @@ MUTANTS = {
     # dk of the normaliser uses k instead of q
     "norm_dk_uses_k": [("c[d] += (double)gs[j] * (double)qs[j * D + d];",
                         "c[d] += (double)gs[j] * (double)ks[j * D + d];")],
+    # the feature map without its exponential branch
+    "feature_no_exp": [("if (feature == 1) return x > 0.0 ? x + 1.0 : exp(x);",
+                        "if (feature == 1) return x + 1.0;")],
+    # the backward without the chain rule through phi
+    "feature_no_chain_rule": [("dqs[e] *= dphi(feature, (double)qs[e]);", "(void)0;")],
+    # phi' taken as phi
+    "feature_dphi_is_phi": [("if (feature == 1) return x > 0.0 ? 1.0 : exp(x);",
+                             "if (feature == 1) return x > 0.0 ? x + 1.0 : exp(x);")],
 }
 
 
@@ -92,8 +100,31 @@ class _Impl:
         lib.cpo_fwd_state.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, c_int]
         lib.cpo_bwd_state.argtypes = [p, p, p, p, p, p, p, p, p, p, i64, i64, i64, i64, c_int]
         lib.cpo_norm.argtypes = [p, p, p, i64, i64, i64, c_int]
+        lib.cpo_fwd_feature.argtypes = [p, p, p, p, c_int, i64, i64, i64, i64, c_int]
+        lib.cpo_bwd_feature.argtypes = [p, p, p, p, p, p, p, c_int, i64, i64, i64, i64, c_int]
         lib.cpo_norm_bwd.argtypes = [p, p, p, p, p, i64, i64, i64, c_int]
         self.lib = lib
+
+    def fwd_feature(self, q, k, v):
+        q, k, v = (np.ascontiguousarray(x, np.float32) for x in (q, k, v))
+        lead = q.shape[:-2]
+        BH = int(np.prod(lead)) if lead else 1
+        N, D, M = q.shape[-2], q.shape[-1], v.shape[-1]
+        out = np.zeros(lead + (N, M))
+        assert self.lib.cpo_fwd_feature(q.ctypes.data, k.ctypes.data, v.ctypes.data,
+                                        out.ctypes.data, 1, BH, N, D, M, 1) == 0
+        return out
+
+    def bwd_feature(self, q, k, v, g):
+        q, k, v, g = (np.ascontiguousarray(x, np.float32) for x in (q, k, v, g))
+        lead = q.shape[:-2]
+        BH = int(np.prod(lead)) if lead else 1
+        N, D, M = q.shape[-2], q.shape[-1], v.shape[-1]
+        dq, dk, dv = np.zeros(lead + (N, D)), np.zeros(lead + (N, D)), np.zeros(lead + (N, M))
+        assert self.lib.cpo_bwd_feature(q.ctypes.data, k.ctypes.data, v.ctypes.data, g.ctypes.data,
+                                        dq.ctypes.data, dk.ctypes.data, dv.ctypes.data, 1, BH, N,
+                                        D, M, 1) == 0
+        return dq, dk, dv
 
     def norm(self, q, k):
         q, k = (np.ascontiguousarray(x, np.float32) for x in (q, k))
@@ -175,7 +206,7 @@ def test_mutant_is_caught(name, tmp_path):
     mpath.write_text(src)
     lib = tmp_path / f"lib{name}.so"
     subprocess.run(["gcc", "-O1", "-fopenmp", "-shared", "-fPIC", "-std=c11", "-o", str(lib),
-                    str(mpath)], check=True)
+                    str(mpath), "-lm"], check=True)
     impl = _Impl(str(lib))
     caught = []
     for pin in pins.ALL_PINS:
