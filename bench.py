@@ -44,12 +44,12 @@ CAUSAL_SOURCES = ("cp_tc.cu", "cp_tc_causal.cuh", "cp_tc_common.cuh", "sm103_ptx
 BWD_SOURCES = ("cp_tc_dkdv.cu", "cp_tc_dkdv.cuh", "cp_tc_causal.cuh", "cp_tc_common.cuh",
                "sm103_ptx.cuh")
 PROFILED_TRAFFIC = {
-    "source_sha256": "4adf80f4cd33d34fa9578a9b9f9e8fb024ee57a48ee7c26674c974b04558cf36",
-    "bytes_per_launch": 211895040,  # 201.40 MB read + 10.50 MB written (forward launch)
+    "source_sha256": "bab58d028a38bb878e9b57afbc34fcd0561e36e31c3ecc3d8bbcff9daa1c9a65",
+    "bytes_per_launch": 211835136,  # 201.40 MB read + 10.43 MB written (forward launch)
 }
 PROFILED_TRAFFIC_BWD = {
-    "source_sha256": "00783b015ef4ec96a917a56cacbeeb9bf5417314201285f15ce96e59605b3d02",
-    "bytes_per_launch": 605915136,  # 463.80 MB read + 142.11 MB written (one backward launch)
+    "source_sha256": "45fa6e84f0d222971fa1707c4d1f9fbead602a2ae98416215a59f0b05c21a6db",
+    "bytes_per_launch": 605403904,  # 463.64 MB read + 141.77 MB written (one backward launch)
 }
 
 
