@@ -46,7 +46,8 @@
  *
  * Supported shapes: B, H >= 1; N >= 0 (N = 0 returns CP_OK and enqueues
  * nothing); 1 <= D, M <= 256.  bf16 additionally needs D and M to be
- * multiples of 8 (16-byte rows for the tensor-memory-access engine).
+ * multiples of 8 (16-byte rows for the tensor-memory-access engine); the
+ * normaliser needs D a multiple of 8 for bf16 and fp16.
  *
  * Errors are reported before anything is enqueued (argument checks) or as
  * CP_ERR_CUDA for a failed launch.  A kernel that finds one of its internal
@@ -74,7 +75,9 @@ extern "C" {
 
 typedef enum {
   CP_DTYPE_F32 = 0,  /* fp32 in/out; fp32 FMA arithmetic (no TF32 rounding) */
-  CP_DTYPE_BF16 = 1  /* bf16 in/out; bf16 tensor-core products, fp32 accumulate */
+  CP_DTYPE_BF16 = 1, /* bf16 in/out; bf16 tensor-core products, fp32 accumulate */
+  CP_DTYPE_F16 = 2   /* fp16 in/out; widened on load, fp32 FMA arithmetic (the fp32
+                        path, CUDA cores), rounded to nearest-even once on store */
 } cp_dtype_t;
 
 /* Feature map applied to q and k before the product (causal linear

@@ -9,7 +9,8 @@ the library's CUDA kernels.  PyTorch supplies device memory and streams.
     causal_product_bwd(q, k, v, g, dq, dk, dv) #   as the C ABI
 
 q, k: [B, H, N, D]; v: [B, H, N, M]; all contiguous, on one CUDA device,
-dtype float32 or bfloat16.  out_i = sum_{j<=i} (q_i . k_j) v_j.
+dtype float32, bfloat16 or float16 (fp16 runs on the fp32 path, widened on
+load).  out_i = sum_{j<=i} (q_i . k_j) v_j.
 
 There is no fallback: if the library cannot be built or loaded, every call
 raises.
@@ -34,10 +35,11 @@ __all__ = [
     "library_path", "load_library",
 ]
 
-CP_DTYPE_F32, CP_DTYPE_BF16 = 0, 1
+CP_DTYPE_F32, CP_DTYPE_BF16, CP_DTYPE_F16 = 0, 1, 2
 CP_OK = 0
 CP_ERR_TIMEOUT = 7
-_DTYPES = {torch.float32: CP_DTYPE_F32, torch.bfloat16: CP_DTYPE_BF16}
+_DTYPES = {torch.float32: CP_DTYPE_F32, torch.bfloat16: CP_DTYPE_BF16,
+           torch.float16: CP_DTYPE_F16}
 # feature maps applied to q and k inside the kernels (cp_feature_t)
 FEATURES = {None: 0, "none": 0, "elu1": 1}
 

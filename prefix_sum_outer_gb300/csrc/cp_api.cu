@@ -28,7 +28,8 @@ cp_status_t pass_state(const float* from, float* to, size_t bytes, cudaStream_t 
 
 cp_status_t check_dims(int64_t B, int64_t H, int64_t N, int64_t D, int64_t M, cp_dtype_t dtype) {
   if (B <= 0 || H <= 0 || N < 0) return CP_ERR_INVALID_ARG;
-  if (dtype != CP_DTYPE_F32 && dtype != CP_DTYPE_BF16) return CP_ERR_UNSUPPORTED_DTYPE;
+  if (dtype != CP_DTYPE_F32 && dtype != CP_DTYPE_BF16 && dtype != CP_DTYPE_F16)
+    return CP_ERR_UNSUPPORTED_DTYPE;
   if (D < 1 || D > 256 || M < 1 || M > 256) return CP_ERR_UNSUPPORTED_SHAPE;
   if (dtype == CP_DTYPE_BF16 && ((D % 8) != 0 || (M % 8) != 0)) return CP_ERR_UNSUPPORTED_SHAPE;
   // index arithmetic inside the kernels uses 32-bit tile and problem counts
@@ -39,7 +40,7 @@ cp_status_t check_dims(int64_t B, int64_t H, int64_t N, int64_t D, int64_t M, cp
 // Aggregate bytes one product of shape (BH, N, D', M') needs.
 size_t product_agg_bytes(int64_t BH, int64_t N, int64_t D, int64_t M, cp_dtype_t dtype) {
   if (N == 0) return 0;
-  if (dtype == CP_DTYPE_F32) return simt_plan(BH, N, D, M).agg_bytes;
+  if (dtype != CP_DTYPE_BF16) return simt_plan(BH, N, D, M).agg_bytes;
   return tc_plan(BH, N, D, M).agg_bytes;
 }
 
@@ -55,9 +56,11 @@ size_t workspace_bytes(int64_t BH, int64_t N, int64_t D, int64_t M, cp_dtype_t d
   return kStatusBytes + round_up(agg);
 }
 
-cp_status_t run_product(const Product& p, cp_dtype_t dtype, float* agg, int* status,
+cp_status_t run_product(Product p, cp_dtype_t dtype, float* agg, int* status,
                         cudaStream_t stream) {
-  if (dtype == CP_DTYPE_F32) {
+  if (dtype != CP_DTYPE_BF16) {
+    // fp32, and fp16 widened on load: the SIMT kernel
+    p.dtype = dtype;
     const SimtPlan plan = simt_plan(p.BH, p.N, p.D, p.M);
     return simt_launch(p, plan, agg, status, stream) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
   }
@@ -101,9 +104,11 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 cp_status_t check_norm_dims(int64_t B, int64_t H, int64_t N, int64_t D, cp_dtype_t dtype) {
   if (B <= 0 || H <= 0 || N < 0) return CP_ERR_INVALID_ARG;
-  if (dtype != CP_DTYPE_F32 && dtype != CP_DTYPE_BF16) return CP_ERR_UNSUPPORTED_DTYPE;
+  if (dtype != CP_DTYPE_F32 && dtype != CP_DTYPE_BF16 && dtype != CP_DTYPE_F16)
+    return CP_ERR_UNSUPPORTED_DTYPE;
   if (D < 1 || D > 256) return CP_ERR_UNSUPPORTED_SHAPE;
-  if (dtype == CP_DTYPE_BF16 && (D % 8) != 0) return CP_ERR_UNSUPPORTED_SHAPE;
+  // 16-bit rows move in 16-byte vectors
+  if (dtype != CP_DTYPE_F32 && (D % 8) != 0) return CP_ERR_UNSUPPORTED_SHAPE;
   if (B * H > (int64_t)1 << 24 || N > (int64_t)1 << 31) return CP_ERR_UNSUPPORTED_SHAPE;
   return CP_OK;
 }

@@ -9,6 +9,7 @@
 #include <algorithm>
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "cp_internal.h"
 
@@ -23,6 +24,8 @@ template <>
 __device__ __forceinline__ float to_f32<float>(float x) { return x; }
 template <>
 __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <>
+__device__ __forceinline__ float to_f32<__half>(__half x) { return __half2float(x); }
 
 template <typename T>
 __device__ __forceinline__ T from_f32(float x);
@@ -30,6 +33,8 @@ template <>
 __device__ __forceinline__ float from_f32<float>(float x) { return x; }
 template <>
 __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+template <>
+__device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(x); }
 
 template <typename T>
 __global__ void __launch_bounds__(kDecThreads)
@@ -152,6 +157,10 @@ cudaError_t decode_launch(const void* q, const void* k, const void* v, void* out
           static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
           static_cast<const __nv_bfloat16*>(v), static_cast<__nv_bfloat16*>(out), state, (int)D,
           (int)M);
+    else if (dtype == CP_DTYPE_F16)
+      decode_kernel_v4<__half><<<(unsigned)BH, kDecThreads, smem, stream>>>(
+          static_cast<const __half*>(q), static_cast<const __half*>(k),
+          static_cast<const __half*>(v), static_cast<__half*>(out), state, (int)D, (int)M);
     else
       decode_kernel_v4<float><<<(unsigned)BH, kDecThreads, smem, stream>>>(
           static_cast<const float*>(q), static_cast<const float*>(k),
@@ -164,6 +173,10 @@ cudaError_t decode_launch(const void* q, const void* k, const void* v, void* out
         static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
         static_cast<const __nv_bfloat16*>(v), static_cast<__nv_bfloat16*>(out), state, (int)D,
         (int)M);
+  else if (dtype == CP_DTYPE_F16)
+    decode_kernel<__half><<<(unsigned)BH, kDecThreads, smem, stream>>>(
+        static_cast<const __half*>(q), static_cast<const __half*>(k),
+        static_cast<const __half*>(v), static_cast<__half*>(out), state, (int)D, (int)M);
   else
     decode_kernel<float><<<(unsigned)BH, kDecThreads, smem, stream>>>(
         static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),

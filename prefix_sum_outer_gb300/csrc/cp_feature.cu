@@ -11,6 +11,7 @@
 #include <algorithm>
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "cp_internal.h"
 
@@ -60,6 +61,39 @@ struct Chunk<__nv_bfloat16> {
     static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(x);
   }
 };
+template <>
+struct Chunk<__half> {
+  static constexpr int kN = 8;
+  static __device__ __forceinline__ void from_word(const uint4& w, float* f) {
+    const __half2* h = reinterpret_cast<const __half2*>(&w);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 t = __half22float2(h[j]);
+      f[2 * j] = t.x;
+      f[2 * j + 1] = t.y;
+    }
+  }
+  static __device__ __forceinline__ void load(const void* p, int64_t c, float* f) {
+    from_word(__ldg(static_cast<const uint4*>(p) + c), f);
+  }
+  static __device__ __forceinline__ void load_rw(const void* p, int64_t c, float* f) {
+    from_word(static_cast<const uint4*>(p)[c], f);
+  }
+  static __device__ __forceinline__ void store(void* p, int64_t c, const float* f) {
+    uint4 w;
+    __half2* h = reinterpret_cast<__half2*>(&w);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) h[j] = __floats2half2_rn(f[2 * j], f[2 * j + 1]);
+    static_cast<uint4*>(p)[c] = w;
+  }
+  static __device__ __forceinline__ float elem(const void* p, int64_t i) {
+    return __half2float(static_cast<const __half*>(p)[i]);
+  }
+  static __device__ __forceinline__ void set(void* p, int64_t i, float x) {
+    static_cast<__half*>(p)[i] = __float2half_rn(x);
+  }
+};
+
 template <>
 struct Chunk<float> {
   static constexpr int kN = 4;
@@ -116,11 +150,13 @@ cudaError_t feature_run(const void* x, void* y, int64_t n, cp_dtype_t dtype, cud
   int dev = 0, n_sm = kPlanSMs;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t per = dtype == CP_DTYPE_BF16 ? 8 : 4;
+  const int64_t per = dtype == CP_DTYPE_F32 ? 4 : 8;
   const int64_t want = (n / per + kFeatThreads - 1) / kFeatThreads;
   const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, 8LL * n_sm));
   if (dtype == CP_DTYPE_BF16)
     feature_kernel<__nv_bfloat16, GRAD><<<grid, kFeatThreads, 0, st>>>(x, y, n);
+  else if (dtype == CP_DTYPE_F16)
+    feature_kernel<__half, GRAD><<<grid, kFeatThreads, 0, st>>>(x, y, n);
   else
     feature_kernel<float, GRAD><<<grid, kFeatThreads, 0, st>>>(x, y, n);
   return cudaGetLastError();

@@ -44,9 +44,11 @@ struct Product {
   int64_t st_ld_r = 0, st_ld_c = 0;
   // feature map applied to q and k as they are loaded (cp_feature_t)
   int feature = 0;
+  // element type of q, k, v and out (the fp32 SIMT path also takes fp16)
+  cp_dtype_t dtype = CP_DTYPE_F32;
 };
 
-// ---- fp32 (SIMT FMA) path
+// ---- fp32 (SIMT FMA) path, also for fp16 inputs (widened on load)
 struct SimtPlan {
   int C;        // rows per tile
   int Mb;       // value columns per CTA

@@ -36,6 +36,7 @@
 #include <mutex>
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "cp_internal.h"
 #include "sm103_ptx.cuh"
@@ -110,6 +111,27 @@ struct VecIO<__nv_bfloat16, 8> {
 #pragma unroll
     for (int j = 0; j < 4; ++j) h[j] = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
     *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p) + e) = r;
+  }
+};
+
+template <>
+struct VecIO<__half, 8> {
+  using R = uint4;
+  static __device__ __forceinline__ R zero() { return make_uint4(0u, 0u, 0u, 0u); }
+  static __device__ __forceinline__ R lds(const uint8_t* p, int64_t e) {
+    return *reinterpret_cast<const uint4*>(p + e * 2);
+  }
+  static __device__ __forceinline__ void unpack2(const R& r, float2* f) {
+    const __half2* h = reinterpret_cast<const __half2*>(&r);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) f[j] = __half22float2(h[j]);
+  }
+  static __device__ __forceinline__ void store2(void* p, int64_t e, const float2* f) {
+    uint4 r;
+    __half2* h = reinterpret_cast<__half2*>(&r);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) h[j] = __floats2half2_rn(f[j].x, f[j].y);
+    *reinterpret_cast<uint4*>(static_cast<__half*>(p) + e) = r;
   }
 };
 
@@ -658,7 +680,7 @@ struct NormShape {
 
 NormShape norm_shape(int64_t D, cp_dtype_t dtype, int warps, int rows_per_thread) {
   NormShape sh{};
-  sh.V = dtype == CP_DTYPE_BF16 ? 8 : (D % 4 == 0 ? 4 : 1);
+  sh.V = dtype != CP_DTYPE_F32 ? 8 : (D % 4 == 0 ? 4 : 1);
   const int64_t per_row = (D + sh.V - 1) / sh.V;  // accesses per row
   int K = 1;
   while ((per_row + K - 1) / K > 32) K <<= 1;
@@ -838,6 +860,7 @@ cudaError_t norm_launch(int mode, const void* q, const void* k, const float* gra
     a.status = status;
     uint8_t* ws = static_cast<uint8_t*>(scratch);
     if (dtype == CP_DTYPE_BF16) return lb_modes<__nv_bfloat16, 8, 1>(mode, a, pl, ws, stream);
+    if (dtype == CP_DTYPE_F16) return lb_modes<__half, 8, 1>(mode, a, pl, ws, stream);
     if (pl.sh.K == 1) return lb_modes<float, 4, 1>(mode, a, pl, ws, stream);
     return lb_modes<float, 4, 2>(mode, a, pl, ws, stream);
   }

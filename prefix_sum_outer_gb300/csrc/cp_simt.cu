@@ -1,7 +1,8 @@
 // fp32 causal product on the CUDA cores (FFMA), chunked over the sequence.
 //
 // TF32 tensor-core rounding (10-bit mantissa) would not hold fp32 accuracy,
-// so the fp32 path uses plain fp32 FMA.  One CTA owns one (problem,
+// so the fp32 path uses plain fp32 FMA.  fp16 inputs take the same kernel:
+// elements are widened to fp32 on load and the outputs rounded to fp16 once.  One CTA owns one (problem,
 // value-column block, segment).  It walks its segment in tiles of C rows:
 //     P      = Q_t K_t^T, masked to the causal triangle of the tile
 //     O_t    = Q_t S + P V_t            (S = state before the tile)
@@ -10,6 +11,8 @@
 // triton-lang/triton issue #217 regrouped by tiles: within a tile the
 // prefix is the masked product, across tiles it is the carried state.
 #include <algorithm>
+
+#include <cuda_fp16.h>
 
 #include "cp_internal.h"
 
@@ -21,10 +24,10 @@ constexpr int kThreads = 256;
 constexpr int kMaxMb = 64;
 
 struct SimtArgs {
-  const float* q;
-  const float* k;
-  const float* v;
-  float* out;
+  const void* q;    // element type T of the kernel
+  const void* k;
+  const void* v;
+  void* out;
   int64_t N;
   int D, M, Mb, n_mb, G, BH;
   int64_t seg_rows;
@@ -42,6 +45,16 @@ struct SimtArgs {
 
 __device__ __forceinline__ float elu1(float x) { return x > 0.f ? x + 1.f : expf(x); }
 
+__device__ __forceinline__ float widen(float x) { return x; }
+__device__ __forceinline__ float widen(__half x) { return __half2float(x); }
+template <typename T>
+__device__ __forceinline__ T narrow(float x);
+template <>
+__device__ __forceinline__ float narrow<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __half narrow<__half>(float x) { return __float2half_rn(x); }
+
+template <typename T>
 __global__ void __launch_bounds__(kThreads) simt_kernel(SimtArgs a) {
   extern __shared__ float smem[];
   const int D = a.D, Mb = a.Mb;
@@ -69,10 +82,10 @@ __global__ void __launch_bounds__(kThreads) simt_kernel(SimtArgs a) {
   const int64_t n_rows = seg_hi - seg_lo;
   const int n_t = (int)((n_rows + kC - 1) / kC);
 
-  const float* qb = a.q + (int64_t)bh * a.N * D;
-  const float* kb = a.k + (int64_t)bh * a.N * D;
-  const float* vb = a.v + (int64_t)bh * a.N * a.M;
-  float* ob = a.out + (int64_t)bh * a.N * a.M;
+  const T* qb = static_cast<const T*>(a.q) + (int64_t)bh * a.N * D;
+  const T* kb = static_cast<const T*>(a.k) + (int64_t)bh * a.N * D;
+  const T* vb = static_cast<const T*>(a.v) + (int64_t)bh * a.N * a.M;
+  T* ob = static_cast<T*>(a.out) + (int64_t)bh * a.N * a.M;
 
   // initial state: the carried state plus the aggregates of the segments
   // before this one in scan order
@@ -98,11 +111,11 @@ __global__ void __launch_bounds__(kThreads) simt_kernel(SimtArgs a) {
       const int r = e / D, d = e % D;
       const int64_t row = r0 + r;
       const bool in = row < seg_hi;
-      float kx = in ? kb[row * D + d] : 0.f;
+      float kx = in ? widen(kb[row * D + d]) : 0.f;
       if (a.feature && in) kx = elu1(kx);
       Ks[r * ldq + d] = kx;
       if (!a.agg_only) {
-        float qx = in ? qb[row * D + d] : 0.f;
+        float qx = in ? widen(qb[row * D + d]) : 0.f;
         if (a.feature && in) qx = elu1(qx);
         Qs[r * ldq + d] = qx;
       }
@@ -110,7 +123,7 @@ __global__ void __launch_bounds__(kThreads) simt_kernel(SimtArgs a) {
     for (int e = threadIdx.x; e < kC * Mb; e += kThreads) {
       const int r = e / Mb, m = e % Mb;
       const int64_t row = r0 + r;
-      Vs[e] = (row < seg_hi && m < mw) ? vb[row * a.M + m0 + m] : 0.f;
+      Vs[e] = (row < seg_hi && m < mw) ? widen(vb[row * a.M + m0 + m]) : 0.f;
     }
     __syncthreads();
     if (!a.agg_only) {
@@ -137,7 +150,7 @@ __global__ void __launch_bounds__(kThreads) simt_kernel(SimtArgs a) {
         for (int d = 0; d < D; ++d) acc = fmaf(qi[d], Ss[d * Mb + m], acc);
         const float* pi = Ps + i * (kC + 1);
         for (int j = 0; j < kC; ++j) acc = fmaf(pi[j], Vs[j * Mb + m], acc);
-        ob[row * a.M + m0 + m] = acc;
+        ob[row * a.M + m0 + m] = narrow<T>(acc);
       }
       __syncthreads();
     }
@@ -192,14 +205,15 @@ cudaError_t simt_launch(const Product& p, const SimtPlan& plan, float* agg, int*
                         cudaStream_t stream) {
   (void)status;
   const size_t smem = simt_smem_bytes((int)p.D, plan.Mb);
-  cudaError_t e = cudaFuncSetAttribute(simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto kern = p.dtype == CP_DTYPE_F16 ? simt_kernel<__half> : simt_kernel<float>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
   SimtArgs a{};
-  a.q = static_cast<const float*>(p.q);
-  a.k = static_cast<const float*>(p.k);
-  a.v = static_cast<const float*>(p.v);
-  a.out = static_cast<float*>(p.out);
+  a.q = p.q;
+  a.k = p.k;
+  a.v = p.v;
+  a.out = p.out;
   a.N = p.N;
   a.D = (int)p.D;
   a.M = (int)p.M;
@@ -219,14 +233,14 @@ cudaError_t simt_launch(const Product& p, const SimtPlan& plan, float* agg, int*
     a.agg_only = 1;
     a.agg_out = agg;
     // (the aggregate pass ignores the carried state: agg_only is set)
-    simt_kernel<<<(unsigned)(problems * (plan.G - 1)), kThreads, smem, stream>>>(a);
+    kern<<<(unsigned)(problems * (plan.G - 1)), kThreads, smem, stream>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     a.agg_only = 0;
     a.agg_in = agg;
     a.agg_out = nullptr;
   }
-  simt_kernel<<<(unsigned)(problems * plan.G), kThreads, smem, stream>>>(a);
+  kern<<<(unsigned)(problems * plan.G), kThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -279,3 +279,15 @@ def test_feature_argument_checks(lib):
     assert bwd(dk=5 * A) == INVALID_ARG                # dq and dk alias
     assert bwd(ws=8 * A, wsb=1024) == WS_TOO_SMALL
     assert bwd(N=0) == OK
+
+
+def test_f16_dtype_checks(lib):
+    F16 = 2
+    # fp16 runs on the fp32 path: any D, M in [1, 256]
+    assert lib.causal_product_workspace_size(1, 2, 64, 12, 7, F16, 1) >= 256
+    assert lib.causal_product_workspace_size(1, 2, 64, 257, 7, F16, 0) == 0
+    # the normaliser moves 16-bit rows in 16-byte vectors
+    assert lib.causal_product_normalizer_workspace_size(1, 2, 64, 16, F16) >= 256
+    assert lib.causal_product_normalizer_workspace_size(1, 2, 64, 12, F16) == 0
+    assert lib.causal_product_fwd(A, 2 * A, 3 * A, 4 * A, 1, 1, 64, 16, 16, 3, None, 0,
+                                  None) == UNSUPPORTED_DTYPE
