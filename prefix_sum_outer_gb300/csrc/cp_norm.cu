@@ -345,7 +345,7 @@ constexpr int kLbWarps = 4;
 constexpr int kLbThreads = 32 * kLbWarps;
 constexpr int kLbMaxStages = 8;
 constexpr int kLbRowsPerThread = 8;           // divided by K
-constexpr uint32_t kLbRingBytes = 64 * 1024;  // shared memory of a CTA's ring
+constexpr uint32_t kLbRingBytes = 32 * 1024;  // shared memory of a CTA's ring
 constexpr int kMaxDev = 64;
 
 struct LbArgs {
@@ -781,7 +781,7 @@ cudaError_t lb_run(LbArgs a, const LbPlan& pl, uint8_t* ws, cudaStream_t st) {
       (uint32_t)((pl.sh.rows * (size_t)a.D * sizeof(T) + 127) / 128 * 128);
   const uint32_t stage = kIn * in_bytes;
   int S = (int)(kLbRingBytes / stage);
-  S = std::max(2, std::min(kLbMaxStages, S));
+  S = std::max(1, std::min(kLbMaxStages, S));
   const size_t aux = sizeof(float) * ((2 * kLbWarps + 1) * (size_t)a.D +
                                       std::max<size_t>(kLbThreads, a.D));
   const size_t smem = (size_t)S * stage + aux;
