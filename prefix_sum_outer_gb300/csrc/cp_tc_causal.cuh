@@ -25,10 +25,11 @@
 //   warps 14, 15  MMA issuers of P and of P V
 // (the converter groups run one thread per TMEM lane = tile row)
 //
-// Kernels are launched as programmatic dependents: the set-up (barriers,
-// TMEM allocation, descriptor prefetch) overlaps the previous kernel in the
-// stream, and no global memory is touched before it has completed.  The
-// next kernel is allowed to start once every block has passed that wait.
+// Product kernels are launched as programmatic dependents: the set-up
+// (barriers, TMEM allocation, descriptor prefetch) overlaps the previous
+// kernel in the stream, and no global memory is touched before it has
+// completed.  A CTA lets the next kernel be scheduled only when its own
+// work is done.
 //
 // With a feature map (the FEAT instantiation), the loaded Q and K tiles are
 // raw inputs x: the state and O groups map them in shared memory, phi(x) =
@@ -280,12 +281,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (ph.first) {
-    grid_dep_wait();  // inputs written by the previous kernel are visible from here
-    // dependents start only once every block has passed the wait above, so
-    // for them every kernel before this one has completed
-    grid_dep_launch_dependents();
-  }
+  if (ph.first) grid_dep_wait();  // inputs written by the previous kernel are visible from here
   const uint32_t tmem = *tmem_holder;
   const int wq = warp & 3;                 // TMEM lane quarter of this warp
   const int row = wq * 32 + lane;          // tile row = TMEM lane
@@ -781,6 +777,12 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
 
   tc_fence_before();
   __syncthreads();
+  // this CTA's work is done: the next kernel in the stream may be scheduled
+  // once every CTA has got here (its blocks still wait in grid_dep_wait for
+  // this whole grid).  Triggering at the start instead let the next kernel's
+  // CTAs take the SMs this grid's blocks freed, which cost up to 80 us when
+  // the forward and backward kernels alternate.
+  if (ph.last) grid_dep_launch_dependents();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, L::kColsAlloc);

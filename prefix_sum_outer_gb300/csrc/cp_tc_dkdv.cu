@@ -89,19 +89,19 @@ bool tc_dkdv_supported(const TcPlan& plan) {
 
 namespace {
 
+// The backward kernels are launched in plain stream order, not as
+// programmatic dependents of the kernel before them: measured on the
+// B=8 H=16 N=4096 D=M=64 step, a dependent backward launch saved 2-3 us
+// after another backward but cost about 35 us after a forward that writes
+// its final state, so the backward waits for its predecessor to complete.
 template <typename... KArgs, typename... Act>
-cudaError_t launch_pdl(void (*kern)(KArgs...), unsigned grid, int smem, cudaStream_t stream,
+cudaError_t launch_bwd(void (*kern)(KArgs...), unsigned grid, int smem, cudaStream_t stream,
                        Act&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(tc::dkdv::kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Act>(args)...);
 }
 
@@ -163,13 +163,13 @@ cp_status_t tc_bwd_launch(const void* q, const void* k, const void* v, const voi
       static std::atomic<uint64_t> configured{0};
       e = set_smem_once(tc_bwd_kernel<true>, kSmem, configured);
       if (e == cudaSuccess)
-        e = launch_pdl(tc_bwd_kernel<true>, grid, kSmem, stream, mq, mk, mv, mg, mdk, mdv, mdq, a,
+        e = launch_bwd(tc_bwd_kernel<true>, grid, kSmem, stream, mq, mk, mv, mg, mdk, mdv, mdq, a,
                        aq, n_main_dq);
     } else {
       static std::atomic<uint64_t> configured{0};
       e = set_smem_once(tc_bwd_kernel<false>, kSmem, configured);
       if (e == cudaSuccess)
-        e = launch_pdl(tc_bwd_kernel<false>, grid, kSmem, stream, mq, mk, mv, mg, mdk, mdv, mdq,
+        e = launch_bwd(tc_bwd_kernel<false>, grid, kSmem, stream, mq, mk, mv, mg, mdk, mdv, mdq,
                        a, aq, n_main_dq);
     }
     return e == cudaSuccess ? CP_OK : CP_ERR_CUDA;
@@ -194,13 +194,13 @@ cp_status_t tc_bwd_launch(const void* q, const void* k, const void* v, const voi
     static std::atomic<uint64_t> configured{0};
     e = set_smem_once(tc_dkdv_kernel<true>, dkdv::kSmemBytes, configured);
     if (e == cudaSuccess)
-      e = launch_pdl(tc_dkdv_kernel<true>, grid, dkdv::kSmemBytes, stream, mq, mk, mv, mg, mdk,
+      e = launch_bwd(tc_dkdv_kernel<true>, grid, dkdv::kSmemBytes, stream, mq, mk, mv, mg, mdk,
                      mdv, a);
   } else {
     static std::atomic<uint64_t> configured{0};
     e = set_smem_once(tc_dkdv_kernel<false>, dkdv::kSmemBytes, configured);
     if (e == cudaSuccess)
-      e = launch_pdl(tc_dkdv_kernel<false>, grid, dkdv::kSmemBytes, stream, mq, mk, mv, mg, mdk,
+      e = launch_bwd(tc_dkdv_kernel<false>, grid, dkdv::kSmemBytes, stream, mq, mk, mv, mg, mdk,
                      mdv, a);
   }
   return e == cudaSuccess ? CP_OK : CP_ERR_CUDA;

@@ -168,11 +168,7 @@ __device__ __forceinline__ bool dkdv_body(const CUtensorMap& tm_q, const CUtenso
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (ph.first) {
-    grid_dep_wait();  // inputs written by the previous kernel are visible from here
-    // dependents start only once every block has passed the wait above
-    grid_dep_launch_dependents();
-  }
+  if (ph.first) grid_dep_wait();  // inputs written by the previous kernel are visible from here
   const uint32_t tmem = *tmem_holder;
   const int wq = warp & 3;                 // TMEM lane quarter of this warp
   const int row = wq * 32 + lane;          // tile row = TMEM lane
@@ -506,6 +502,12 @@ __device__ __forceinline__ bool dkdv_body(const CUtensorMap& tm_q, const CUtenso
 
   tc_fence_before();
   __syncthreads();
+  // this CTA's work is done: the next kernel in the stream may be scheduled
+  // once every CTA has got here (its blocks still wait in grid_dep_wait for
+  // this whole grid).  Triggering at the start instead let the next kernel's
+  // CTAs take the SMs this grid's blocks freed, which cost up to 80 us when
+  // the forward and backward kernels alternate.
+  if (ph.last) grid_dep_launch_dependents();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kColsAlloc);
