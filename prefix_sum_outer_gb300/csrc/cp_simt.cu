@@ -19,7 +19,6 @@
 namespace cp {
 namespace {
 
-constexpr int kC = 32;          // rows per tile
 constexpr int kThreads = 256;
 constexpr int kMaxMb = 64;
 
@@ -30,6 +29,7 @@ struct SimtArgs {
   void* out;
   int64_t N;
   int D, M, Mb, n_mb, G, BH;
+  int C;            // rows per tile (a multiple of 4)
   int64_t seg_rows;
   int reverse;
   const float* agg_in;  // [P][G][D][Mb] aggregates (pass 2 reads), may be null
@@ -54,16 +54,51 @@ __device__ __forceinline__ float narrow<float>(float x) { return x; }
 template <>
 __device__ __forceinline__ __half narrow<__half>(float x) { return __float2half_rn(x); }
 
+__device__ __forceinline__ int round4(int x) { return (x + 3) & ~3; }
+
+// acc[i][j] += sum_{k in [k0, k1)} A[r0 + i][k] * B[k][c0 + j] for a 4 x 4
+// block: A and B row-major in shared memory (lda, ldb multiples of 4), k0
+// and k1 multiples of 4.  Sixteen FMAs per two 16-byte loads of each
+// operand row; the k order is fixed, so results are reproducible.
+__device__ __forceinline__ void mm4x4(float (&acc)[4][4], const float* A, int lda,
+                                      const float* B, int ldb, int r0, int c0, int k0, int k1) {
+  for (int k = k0; k < k1; k += 4) {
+    float a[4][4], b[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 t = *reinterpret_cast<const float4*>(A + (r0 + i) * lda + k);
+      a[i][0] = t.x;
+      a[i][1] = t.y;
+      a[i][2] = t.z;
+      a[i][3] = t.w;
+    }
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const float4 t = *reinterpret_cast<const float4*>(B + (k + kk) * ldb + c0);
+      b[kk][0] = t.x;
+      b[kk][1] = t.y;
+      b[kk][2] = t.z;
+      b[kk][3] = t.w;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i][kk], b[kk][j], acc[i][j]);
+  }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads) simt_kernel(SimtArgs a) {
-  extern __shared__ float smem[];
-  const int D = a.D, Mb = a.Mb;
-  const int ldq = D + 1;
-  float* Qs = smem;                  // [C][D+1]
-  float* Ks = Qs + kC * ldq;         // [C][D+1]
-  float* Vs = Ks + kC * ldq;         // [C][Mb]
-  float* Ps = Vs + kC * Mb;          // [C][C+1]
-  float* Ss = Ps + kC * (kC + 1);    // [D][Mb]
+  extern __shared__ __align__(16) float smem[];
+  const int D = a.D, Mb = a.Mb, C = a.C;
+  const int Dp = round4(D), Mbp = round4(Mb);
+  float* Qs = smem;                  // [C][Dp]   q tile, row-major
+  float* Kt = Qs + C * Dp;           // [Dp][C]   k tile, transposed
+  float* Vs = Kt + Dp * C;           // [C][Mbp]
+  float* Ps = Vs + C * Mbp;          // [C][C]    masked Q K^T
+  float* Ss = Ps + C * C;            // [Dp][Mbp] state (padding stays zero)
 
   // block -> (segment, problem, value block); pass 1 skips the one segment
   // whose aggregate nobody reads.
@@ -80,7 +115,7 @@ __global__ void __launch_bounds__(kThreads) simt_kernel(SimtArgs a) {
   const int64_t seg_lo = (int64_t)s * a.seg_rows;
   const int64_t seg_hi = min(a.N, seg_lo + a.seg_rows);
   const int64_t n_rows = seg_hi - seg_lo;
-  const int n_t = (int)((n_rows + kC - 1) / kC);
+  const int n_t = (int)((n_rows + C - 1) / C);
 
   const T* qb = static_cast<const T*>(a.q) + (int64_t)bh * a.N * D;
   const T* kb = static_cast<const T*>(a.k) + (int64_t)bh * a.N * D;
@@ -91,111 +126,184 @@ __global__ void __launch_bounds__(kThreads) simt_kernel(SimtArgs a) {
   // before this one in scan order
   const float* st_in =
       (!a.agg_only && a.state_in != nullptr) ? a.state_in + (int64_t)bh * D * a.M : nullptr;
-  for (int e = threadIdx.x; e < D * Mb; e += kThreads) {
-    const int d0 = e / Mb, m_ = e % Mb;
-    float acc = (st_in != nullptr && m_ < mw) ? st_in[d0 * a.st_ld_r + (m0 + m_) * a.st_ld_c] : 0.f;
-    if (!a.agg_only && a.agg_in != nullptr) {
-      const int lo = a.reverse ? s + 1 : 0;
-      const int hi = a.reverse ? a.G : s;
-      for (int s2 = lo; s2 < hi; ++s2)
-        acc += a.agg_in[((int64_t)pidx * a.G + s2) * D * Mb + e];
+  for (int e = threadIdx.x; e < Dp * Mbp; e += kThreads) {
+    const int d0 = e / Mbp, m_ = e % Mbp;
+    float acc = 0.f;
+    if (d0 < D && m_ < mw) {
+      if (st_in != nullptr) acc = st_in[d0 * a.st_ld_r + (m0 + m_) * a.st_ld_c];
+      if (!a.agg_only && a.agg_in != nullptr) {
+        const int lo = a.reverse ? s + 1 : 0;
+        const int hi = a.reverse ? a.G : s;
+        for (int s2 = lo; s2 < hi; ++s2)
+          acc += a.agg_in[((int64_t)pidx * a.G + s2) * D * Mb + d0 * Mb + m_];
+      }
     }
     Ss[e] = acc;
   }
 
+  const int tc_p = C / 4, tc_o = Mbp / 4;
   for (int it = 0; it < n_t; ++it) {
     const int t = a.reverse ? (n_t - 1 - it) : it;
-    const int64_t r0 = seg_lo + (int64_t)t * kC;
+    const int64_t r0 = seg_lo + (int64_t)t * C;
     __syncthreads();
-    for (int e = threadIdx.x; e < kC * D; e += kThreads) {
-      const int r = e / D, d = e % D;
-      const int64_t row = r0 + r;
-      const bool in = row < seg_hi;
-      float kx = in ? widen(kb[row * D + d]) : 0.f;
-      if (a.feature && in) kx = elu1(kx);
-      Ks[r * ldq + d] = kx;
-      if (!a.agg_only) {
-        float qx = in ? widen(qb[row * D + d]) : 0.f;
-        if (a.feature && in) qx = elu1(qx);
-        Qs[r * ldq + d] = qx;
+    // ---- load: q row-major, k transposed (consecutive threads on
+    // consecutive rows, so the transposed stores hit distinct banks), v.
+    // Each thread issues kBatch loads before it stores any of them.
+    constexpr int kBatch = 8;
+    for (int b0 = threadIdx.x; b0 < Dp * C; b0 += kBatch * kThreads) {
+      float r_[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int e = b0 + u * kThreads;
+        const int d = e / C, r = e % C;
+        const int64_t row = r0 + r;
+        const bool in = e < Dp * C && row < seg_hi && d < D;
+        float x = in ? widen(kb[row * D + d]) : 0.f;
+        if (a.feature && in) x = elu1(x);
+        r_[u] = x;
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int e = b0 + u * kThreads;
+        if (e < Dp * C) Kt[e] = r_[u];  // e = d * C + r
       }
     }
-    for (int e = threadIdx.x; e < kC * Mb; e += kThreads) {
-      const int r = e / Mb, m = e % Mb;
-      const int64_t row = r0 + r;
-      Vs[e] = (row < seg_hi && m < mw) ? widen(vb[row * a.M + m0 + m]) : 0.f;
+    if (!a.agg_only) {
+      for (int b0 = threadIdx.x; b0 < C * Dp; b0 += kBatch * kThreads) {
+        float r_[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int e = b0 + u * kThreads;
+          const int r = e / Dp, d = e % Dp;
+          const int64_t row = r0 + r;
+          const bool in = e < C * Dp && row < seg_hi && d < D;
+          float x = in ? widen(qb[row * D + d]) : 0.f;
+          if (a.feature && in) x = elu1(x);
+          r_[u] = x;
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int e = b0 + u * kThreads;
+          if (e < C * Dp) Qs[e] = r_[u];
+        }
+      }
+    }
+    for (int b0 = threadIdx.x; b0 < C * Mbp; b0 += kBatch * kThreads) {
+      float r_[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int e = b0 + u * kThreads;
+        const int r = e / Mbp, m = e % Mbp;
+        const int64_t row = r0 + r;
+        r_[u] = (e < C * Mbp && row < seg_hi && m < mw) ? widen(vb[row * a.M + m0 + m]) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int e = b0 + u * kThreads;
+        if (e < C * Mbp) Vs[e] = r_[u];
+      }
     }
     __syncthreads();
     if (!a.agg_only) {
-      // P = Q K^T restricted to the causal triangle of the tile
-      for (int e = threadIdx.x; e < kC * kC; e += kThreads) {
-        const int i = e / kC, j = e % kC;
-        float acc = 0.f;
-        const bool keep = a.reverse ? (j >= i) : (j <= i);
-        if (keep) {
-          const float* qi = Qs + i * ldq;
-          const float* kj = Ks + j * ldq;
-          for (int d = 0; d < D; ++d) acc = fmaf(qi[d], kj[d], acc);
+      // ---- P = Q K^T restricted to the causal triangle of the tile
+      for (int tt = threadIdx.x; tt < tc_p * tc_p; tt += kThreads) {
+        const int i0 = (tt / tc_p) * 4, j0 = (tt % tc_p) * 4;
+        float acc[4][4] = {};
+        const bool none = a.reverse ? (j0 + 3 < i0) : (j0 > i0 + 3);
+        if (!none) mm4x4(acc, Qs, Dp, Kt, C, i0, j0, 0, Dp);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float o[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const bool keep = a.reverse ? (j0 + j >= i0 + i) : (j0 + j <= i0 + i);
+            o[j] = keep ? acc[i][j] : 0.f;
+          }
+          *reinterpret_cast<float4*>(Ps + (i0 + i) * C + j0) = make_float4(o[0], o[1], o[2], o[3]);
         }
-        Ps[i * (kC + 1) + j] = acc;
       }
       __syncthreads();
-      // O = Q S + P V
-      for (int e = threadIdx.x; e < kC * Mb; e += kThreads) {
-        const int i = e / Mb, m = e % Mb;
-        const int64_t row = r0 + i;
-        if (row >= seg_hi || m >= mw) continue;
-        float acc = 0.f;
-        const float* qi = Qs + i * ldq;
-        for (int d = 0; d < D; ++d) acc = fmaf(qi[d], Ss[d * Mb + m], acc);
-        const float* pi = Ps + i * (kC + 1);
-        for (int j = 0; j < kC; ++j) acc = fmaf(pi[j], Vs[j * Mb + m], acc);
-        ob[row * a.M + m0 + m] = narrow<T>(acc);
+      // ---- O = Q S + P V (P is zero outside the triangle: only the
+      // columns j a row can see are visited)
+      for (int tt = threadIdx.x; tt < tc_p * tc_o; tt += kThreads) {
+        const int i0 = (tt / tc_o) * 4, c0 = (tt % tc_o) * 4;
+        float acc[4][4] = {};
+        mm4x4(acc, Qs, Dp, Ss, Mbp, i0, c0, 0, Dp);
+        if (a.reverse)
+          mm4x4(acc, Ps, C, Vs, Mbp, i0, c0, i0, C);
+        else
+          mm4x4(acc, Ps, C, Vs, Mbp, i0, c0, 0, i0 + 4);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int64_t row = r0 + i0 + i;
+          if (row >= seg_hi) continue;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (c0 + j < mw) ob[row * a.M + m0 + c0 + j] = narrow<T>(acc[i][j]);
+        }
       }
       __syncthreads();
     }
-    // S += K^T V
-    for (int e = threadIdx.x; e < D * Mb; e += kThreads) {
-      const int d = e / Mb, m = e % Mb;
-      float acc = Ss[e];
-      for (int j = 0; j < kC; ++j) acc = fmaf(Ks[j * ldq + d], Vs[j * Mb + m], acc);
-      Ss[e] = acc;
+    // ---- S += K^T V
+    for (int tt = threadIdx.x; tt < (Dp / 4) * tc_o; tt += kThreads) {
+      const int d0 = (tt / tc_o) * 4, c0 = (tt % tc_o) * 4;
+      float acc[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 t4 = *reinterpret_cast<const float4*>(Ss + (d0 + i) * Mbp + c0);
+        acc[i][0] = t4.x;
+        acc[i][1] = t4.y;
+        acc[i][2] = t4.z;
+        acc[i][3] = t4.w;
+      }
+      mm4x4(acc, Kt, C, Vs, Mbp, d0, c0, 0, C);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<float4*>(Ss + (d0 + i) * Mbp + c0) =
+            make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
     }
   }
+  __syncthreads();
   if (a.agg_only) {
-    __syncthreads();
     float* dst = a.agg_out + ((int64_t)pidx * a.G + s) * D * Mb;
-    for (int e = threadIdx.x; e < D * Mb; e += kThreads) dst[e] = Ss[e];
+    for (int e = threadIdx.x; e < D * Mb; e += kThreads) {
+      const int d0 = e / Mb, m_ = e % Mb;
+      dst[e] = Ss[d0 * Mbp + m_];
+    }
   } else if (a.state_out != nullptr && (a.reverse ? s == 0 : s == a.G - 1)) {
     // the last segment in scan order hands on its final state
-    __syncthreads();
     float* st = a.state_out + (int64_t)bh * D * a.M;
     for (int e = threadIdx.x; e < D * Mb; e += kThreads) {
       const int d0 = e / Mb, m_ = e % Mb;
-      if (m_ < mw) st[d0 * a.st_ld_r + (m0 + m_) * a.st_ld_c] = Ss[e];
+      if (m_ < mw) st[d0 * a.st_ld_r + (m0 + m_) * a.st_ld_c] = Ss[d0 * Mbp + m_];
     }
   }
 }
 
-size_t simt_smem_bytes(int D, int Mb) {
-  return sizeof(float) *
-         (size_t)(2 * kC * (D + 1) + kC * Mb + kC * (kC + 1) + D * Mb);
+// rows per tile: 32 keeps a CTA's shared memory small enough for four CTAs
+// per SM at D = M = 64 (and the quadratic in-tile part of the work small);
+// a sequence of at most 64 rows with narrow operands is one tile of 64
+int simt_rows(int64_t N, int64_t D) { return (N <= 64 && D <= 64) ? 64 : 32; }
+
+size_t simt_smem_bytes(int C_, int D, int Mb) {
+  const size_t C = C_, Dp = (D + 3) / 4 * 4, Mbp = (Mb + 3) / 4 * 4;
+  return sizeof(float) * (2 * C * Dp + C * Mbp + C * C + Dp * Mbp);
 }
 
 }  // namespace
 
 SimtPlan simt_plan(int64_t BH, int64_t N, int64_t D, int64_t M) {
   SimtPlan p{};
-  p.C = kC;
+  p.C = simt_rows(N, D);
   p.Mb = (int)std::min<int64_t>(M, kMaxMb);
   p.n_mb = (int)((M + p.Mb - 1) / p.Mb);
   const int64_t problems = BH * p.n_mb;
-  const int64_t n_tiles = (N + kC - 1) / kC;
-  // aim for about two CTAs per SM; every segment holds at least 4 tiles
-  int64_t G = std::max<int64_t>(1, (2 * kPlanSMs) / std::max<int64_t>(problems, 1));
-  G = std::min<int64_t>(G, std::max<int64_t>(1, n_tiles / 4));
+  const int64_t n_tiles = (N + p.C - 1) / p.C;
+  // aim for about four CTAs per SM; every segment holds at least 2 tiles
+  int64_t G = std::max<int64_t>(1, (4 * kPlanSMs) / std::max<int64_t>(problems, 1));
+  G = std::min<int64_t>(G, std::max<int64_t>(1, n_tiles / 2));
   const int64_t tiles_per_seg = (n_tiles + G - 1) / std::max<int64_t>(G, 1);
-  p.seg_rows = std::max<int64_t>(1, tiles_per_seg) * kC;
+  p.seg_rows = std::max<int64_t>(1, tiles_per_seg) * p.C;
   p.G = (int)std::max<int64_t>(1, (N + p.seg_rows - 1) / p.seg_rows);
   p.agg_bytes = p.G > 1 ? sizeof(float) * (size_t)problems * p.G * D * p.Mb : 0;
   return p;
@@ -204,7 +312,7 @@ SimtPlan simt_plan(int64_t BH, int64_t N, int64_t D, int64_t M) {
 cudaError_t simt_launch(const Product& p, const SimtPlan& plan, float* agg, int* status,
                         cudaStream_t stream) {
   (void)status;
-  const size_t smem = simt_smem_bytes((int)p.D, plan.Mb);
+  const size_t smem = simt_smem_bytes(plan.C, (int)p.D, plan.Mb);
   auto kern = p.dtype == CP_DTYPE_F16 ? simt_kernel<__half> : simt_kernel<float>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
@@ -222,6 +330,7 @@ cudaError_t simt_launch(const Product& p, const SimtPlan& plan, float* agg, int*
   a.G = plan.G;
   a.BH = (int)p.BH;
   a.seg_rows = plan.seg_rows;
+  a.C = plan.C;
   a.reverse = p.reverse ? 1 : 0;
   a.state_in = p.state_in;
   a.state_out = p.state_out;
