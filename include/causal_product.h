@@ -236,6 +236,29 @@ CP_API cp_status_t causal_product_bwd_feature(const void* q, const void* k, cons
 CP_API size_t causal_product_feature_workspace_size(int64_t B, int64_t H, int64_t N, int64_t D,
                                                     int64_t M, cp_dtype_t dtype, int backward);
 
+/* The normaliser of mapped features from raw inputs: z_i = phi(q_i) .
+ * sum_{j<=i} phi(k_j) with phi applied inside the kernel, and its backward
+ * with respect to the raw q, k (grad_q = phi'(q) * grad_z sum phi(k),
+ * grad_k = phi'(k) * sum grad_z phi(q)), so that causal linear attention
+ * from raw inputs, causal_product_fwd_feature(...) / z, never writes phi(q)
+ * or phi(k) to memory.  Arguments as causal_product_normalizer /
+ * causal_product_normalizer_bwd (same workspace size); feature =
+ * CP_FEATURE_NONE is those calls.  A feature map needs rows of 16-byte
+ * multiples (D % 8 == 0 for bf16 and fp16, D % 4 == 0 for fp32);
+ * CP_ERR_UNSUPPORTED_SHAPE otherwise. */
+CP_API cp_status_t causal_product_normalizer_feature(const void* q, const void* k, float* z,
+                                                     cp_feature_t feature, int64_t B, int64_t H,
+                                                     int64_t N, int64_t D, cp_dtype_t dtype,
+                                                     void* workspace, size_t workspace_bytes,
+                                                     void* stream);
+CP_API cp_status_t causal_product_normalizer_bwd_feature(const void* q, const void* k,
+                                                         const float* grad_z, void* grad_q,
+                                                         void* grad_k, cp_feature_t feature,
+                                                         int64_t B, int64_t H, int64_t N,
+                                                         int64_t D, cp_dtype_t dtype,
+                                                         void* workspace, size_t workspace_bytes,
+                                                         void* stream);
+
 /* Size of the static device scratch array behind causal_product_fwd_noalloc. */
 #define CP_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 

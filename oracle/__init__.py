@@ -19,6 +19,8 @@ it with gcc and exposes it through ctypes:
     norm(q, k)          -> z = q_i . sum_{j<=i} k_j   (float64 [..., N])
     norm_bwd(q, k, g)   -> (dq, dk)                   (g = dL/dz, [..., N])
     fwd_feature(q, k, v, feature="elu1")   -> out of phi(q), phi(k), v
+    norm_feature(q, k, feature="elu1")     -> z of phi(q), phi(k)
+    norm_bwd_feature(q, k, g, feature="elu1") -> (dq, dk) w.r.t. raw q, k
     bwd_feature(q, k, v, g, feature="elu1") -> (dq, dk, dv) w.r.t. raw q, k, v
 
 States are [..., D, M] arrays; they may be float64 (the oracle's own
@@ -90,6 +92,10 @@ def _load():
             lib.cpo_bwd_feature.argtypes = [p, p, p, p, p, p, p, c_int, i64, i64, i64, i64,
                                             c_int]
             lib.cpo_bwd_feature.restype = c_int
+            lib.cpo_norm_feature.argtypes = [p, p, p, c_int, i64, i64, i64, c_int]
+            lib.cpo_norm_feature.restype = c_int
+            lib.cpo_norm_bwd_feature.argtypes = [p, p, p, p, p, c_int, i64, i64, i64, c_int]
+            lib.cpo_norm_bwd_feature.restype = c_int
             lib.cpo_threads.argtypes = [c_int]
             lib.cpo_threads.restype = c_int
             _lib = lib
@@ -263,3 +269,32 @@ def bwd_feature(q, k, v, g, feature: str = "elu1", nthreads: int = 0):
     if rc != 0:
         raise RuntimeError(f"oracle bwd_feature failed ({rc})")
     return dq, dk, dv
+
+
+def norm_feature(q, k, feature: str = "elu1", nthreads: int = 0) -> np.ndarray:
+    """z_i = phi(q_i) . sum_{j<=i} phi(k_j) from the raw q, k, in fp64."""
+    q, k = _as_f32(q), _as_f32(k)
+    lead, BH, N, D = _qk_dims(q, k)
+    z = np.zeros(lead + (N,), dtype=np.float64)
+    rc = _load().cpo_norm_feature(q.ctypes.data, k.ctypes.data, z.ctypes.data,
+                                  _FEATURES[feature], BH, N, D, int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle norm_feature failed ({rc})")
+    return z
+
+
+def norm_bwd_feature(q, k, g, feature: str = "elu1", nthreads: int = 0):
+    """(dq, dk) of L = sum_i g_i z_i for norm_feature, with respect to the
+    raw q and k, in fp64."""
+    q, k, g = _as_f32(q), _as_f32(k), _as_f32(g)
+    lead, BH, N, D = _qk_dims(q, k)
+    if g.shape != lead + (N,):
+        raise ValueError(f"grad shape {g.shape} != z shape {lead + (N,)}")
+    dq = np.zeros(lead + (N, D), dtype=np.float64)
+    dk = np.zeros(lead + (N, D), dtype=np.float64)
+    rc = _load().cpo_norm_bwd_feature(q.ctypes.data, k.ctypes.data, g.ctypes.data,
+                                      dq.ctypes.data, dk.ctypes.data, _FEATURES[feature], BH, N,
+                                      D, int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle norm_bwd_feature failed ({rc})")
+    return dq, dk

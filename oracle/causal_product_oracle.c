@@ -366,3 +366,62 @@ int cpo_bwd_feature(const float *q, const float *k, const float *v, const float 
     }
     return err ? -2 : 0;
 }
+
+/* Normaliser of mapped features: z_i = phi(q_i) . sum_{j<=i} phi(k_j) from
+ * the raw q, k (feature 0: as given, 1: elu + 1). */
+int cpo_norm_feature(const float *q, const float *k, double *z, int feature, int64_t BH,
+                     int64_t N, int64_t D, int nthreads) {
+    if (BH < 0 || N < 0 || D <= 0 || feature < 0 || feature > 1) return -1;
+    if (BH == 0 || N == 0) return 0;
+    set_threads(nthreads);
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+    for (int64_t bh = 0; bh < BH; ++bh) {
+        double *c = (double *)calloc((size_t)D, sizeof(double));
+        if (!c) { err |= 1; continue; }
+        const float *qs = q + bh * N * D, *ks = k + bh * N * D;
+        for (int64_t i = 0; i < N; ++i) {
+            /* c += phi(k_i), then z_i = phi(q_i) . c */
+            for (int64_t d = 0; d < D; ++d) c[d] += phi(feature, (double)ks[i * D + d]);
+            double acc = 0.0;
+            for (int64_t d = 0; d < D; ++d) acc += phi(feature, (double)qs[i * D + d]) * c[d];
+            z[bh * N + i] = acc;
+        }
+        free(c);
+    }
+    return err ? -2 : 0;
+}
+
+/* Backward of cpo_norm_feature with respect to the raw q, k:
+ *   dq_i = phi'(q_i) * g_i sum_{j<=i} phi(k_j),
+ *   dk_j = phi'(k_j) * sum_{i>=j} g_i phi(q_i). */
+int cpo_norm_bwd_feature(const float *q, const float *k, const float *g, double *dq, double *dk,
+                         int feature, int64_t BH, int64_t N, int64_t D, int nthreads) {
+    if (BH < 0 || N < 0 || D <= 0 || feature < 0 || feature > 1) return -1;
+    if (BH == 0 || N == 0) return 0;
+    set_threads(nthreads);
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+    for (int64_t bh = 0; bh < BH; ++bh) {
+        double *c = (double *)calloc((size_t)D, sizeof(double));
+        if (!c) { err |= 1; continue; }
+        const float *qs = q + bh * N * D, *ks = k + bh * N * D, *gs = g + bh * N;
+        double *dqs = dq + bh * N * D, *dks = dk + bh * N * D;
+        for (int64_t i = 0; i < N; ++i) {
+            for (int64_t d = 0; d < D; ++d) {
+                const double qx = (double)qs[i * D + d];
+                c[d] += phi(feature, (double)ks[i * D + d]);
+                dqs[i * D + d] = dphi(feature, qx) * ((double)gs[i] * c[d]);
+            }
+        }
+        memset(c, 0, sizeof(double) * (size_t)D);
+        for (int64_t j = N - 1; j >= 0; j -= 1) {
+            for (int64_t d = 0; d < D; ++d) {
+                c[d] += (double)gs[j] * phi(feature, (double)qs[j * D + d]);
+                dks[j * D + d] = dphi(feature, (double)ks[j * D + d]) * c[d];
+            }
+        }
+        free(c);
+    }
+    return err ? -2 : 0;
+}

@@ -109,6 +109,12 @@ def load_library(rebuild: bool = True) -> ctypes.CDLL:
             lib.causal_product_feature_workspace_size.argtypes = [i64, i64, i64, i64, i64, c_int,
                                                                   c_int]
             lib.causal_product_feature_workspace_size.restype = sz
+            lib.causal_product_normalizer_feature.argtypes = [p, p, p, c_int, i64, i64, i64, i64,
+                                                              c_int, p, sz, p]
+            lib.causal_product_normalizer_feature.restype = c_int
+            lib.causal_product_normalizer_bwd_feature.argtypes = [p, p, p, p, p, c_int, i64, i64,
+                                                                  i64, i64, c_int, p, sz, p]
+            lib.causal_product_normalizer_bwd_feature.restype = c_int
             lib.causal_product_status.argtypes = [p, p]
             lib.causal_product_status.restype = c_int
             lib.causal_product_error_string.argtypes = [c_int]
@@ -365,9 +371,11 @@ def _qk_dims(q: torch.Tensor, k: torch.Tensor):
 def causal_product_normalizer(q: torch.Tensor, k: torch.Tensor,
                               z: Optional[torch.Tensor] = None,
                               workspace: Optional[torch.Tensor] = None,
-                              stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+                              stream: Optional[torch.cuda.Stream] = None,
+                              feature: Optional[str] = None) -> torch.Tensor:
     """z[b,h,i] = q[b,h,i] . sum_{j<=i} k[b,h,j] (float32 [B,H,N]): the
-    denominator of causal linear attention."""
+    denominator of causal linear attention.  With ``feature="elu1"`` q and k
+    are raw inputs mapped by phi(x) = elu(x) + 1 inside the kernel."""
     B, H, N, D = _qk_dims(q, k)
     code = _dtype_code(q, k)
     if z is None:
@@ -379,9 +387,10 @@ def causal_product_normalizer(q: torch.Tensor, k: torch.Tensor,
     need = lib.causal_product_normalizer_workspace_size(B, H, N, D, code)
     if workspace is None:
         workspace = _workspace(need, q.device)
-    rc = lib.causal_product_normalizer(q.data_ptr(), k.data_ptr(), z.data_ptr(), B, H, N, D, code,
-                                       workspace.data_ptr(), workspace.numel(),
-                                       _stream_ptr(stream, q.device))
+    rc = lib.causal_product_normalizer_feature(q.data_ptr(), k.data_ptr(), z.data_ptr(),
+                                               _feature_code(feature), B, H, N, D, code,
+                                               workspace.data_ptr(), workspace.numel(),
+                                               _stream_ptr(stream, q.device))
     if rc != CP_OK:
         raise CausalProductError(rc, "causal_product_normalizer")
     return z
@@ -391,9 +400,11 @@ def causal_product_normalizer_bwd(q: torch.Tensor, k: torch.Tensor, grad_z: torc
                                   grad_q: Optional[torch.Tensor] = None,
                                   grad_k: Optional[torch.Tensor] = None,
                                   workspace: Optional[torch.Tensor] = None,
-                                  stream: Optional[torch.cuda.Stream] = None):
+                                  stream: Optional[torch.cuda.Stream] = None,
+                                  feature: Optional[str] = None):
     """(dq, dk) of L = <grad_z, z>: dq_i = grad_z_i sum_{j<=i} k_j,
-    dk_j = sum_{i>=j} grad_z_i q_i, in q's dtype."""
+    dk_j = sum_{i>=j} grad_z_i q_i, in q's dtype (with ``feature``, with
+    respect to the raw q, k: times phi')."""
     B, H, N, D = _qk_dims(q, k)
     code = _dtype_code(q, k)
     if grad_z.dtype != torch.float32 or tuple(grad_z.shape) != (B, H, N):
@@ -405,10 +416,11 @@ def causal_product_normalizer_bwd(q: torch.Tensor, k: torch.Tensor, grad_z: torc
     need = lib.causal_product_normalizer_workspace_size(B, H, N, D, code)
     if workspace is None:
         workspace = _workspace(need, q.device)
-    rc = lib.causal_product_normalizer_bwd(q.data_ptr(), k.data_ptr(), grad_z.data_ptr(),
-                                           grad_q.data_ptr(), grad_k.data_ptr(), B, H, N, D, code,
-                                           workspace.data_ptr(), workspace.numel(),
-                                           _stream_ptr(stream, q.device))
+    rc = lib.causal_product_normalizer_bwd_feature(q.data_ptr(), k.data_ptr(), grad_z.data_ptr(),
+                                                   grad_q.data_ptr(), grad_k.data_ptr(),
+                                                   _feature_code(feature), B, H, N, D, code,
+                                                   workspace.data_ptr(), workspace.numel(),
+                                                   _stream_ptr(stream, q.device))
     if rc != CP_OK:
         raise CausalProductError(rc, "causal_product_normalizer_bwd")
     return grad_q, grad_k
@@ -451,20 +463,23 @@ class Normalizer(torch.autograd.Function):
     """Autograd wrapper of the normaliser: (q, k) -> z."""
 
     @staticmethod
-    def forward(ctx, q, k):
+    def forward(ctx, q, k, feature):
         q, k = q.contiguous(), k.contiguous()
         ctx.save_for_backward(q, k)
-        return causal_product_normalizer(q, k)
+        ctx.feature = feature
+        return causal_product_normalizer(q, k, feature=feature)
 
     @staticmethod
     def backward(ctx, gz):
         q, k = ctx.saved_tensors
-        return causal_product_normalizer_bwd(q, k, gz.contiguous().float())
+        dq, dk = causal_product_normalizer_bwd(q, k, gz.contiguous().float(), feature=ctx.feature)
+        return dq, dk, None
 
 
-def normalizer(q: torch.Tensor, k: torch.Tensor) -> torch.Tensor:
-    """z_i = q_i . sum_{j<=i} k_j (float32 [B,H,N]) with autograd support."""
-    return Normalizer.apply(q, k)
+def normalizer(q: torch.Tensor, k: torch.Tensor, feature: Optional[str] = None) -> torch.Tensor:
+    """z_i = q_i . sum_{j<=i} k_j (float32 [B,H,N]) with autograd support;
+    ``feature="elu1"`` maps raw q, k by phi(x) = elu(x) + 1 in the kernel."""
+    return Normalizer.apply(q, k, feature)
 
 
 class CausalProductFeature(torch.autograd.Function):

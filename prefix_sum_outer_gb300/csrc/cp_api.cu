@@ -399,11 +399,16 @@ size_t causal_product_normalizer_workspace_size(int64_t B, int64_t H, int64_t N,
   return cp::norm_workspace_bytes(B * H, N, D, dtype);
 }
 
-cp_status_t causal_product_normalizer(const void* q, const void* k, float* z, int64_t B, int64_t H,
-                                      int64_t N, int64_t D, cp_dtype_t dtype, void* workspace,
-                                      size_t workspace_bytes, void* stream_) {
+cp_status_t causal_product_normalizer_feature(const void* q, const void* k, float* z,
+                                              cp_feature_t feature, int64_t B, int64_t H,
+                                              int64_t N, int64_t D, cp_dtype_t dtype,
+                                              void* workspace, size_t workspace_bytes,
+                                              void* stream_) {
+  if (feature != CP_FEATURE_NONE && feature != CP_FEATURE_ELU1) return CP_ERR_INVALID_ARG;
   cp_status_t st = cp::check_norm_dims(B, H, N, D, dtype);
   if (st != CP_OK) return st;
+  if (feature != CP_FEATURE_NONE && !cp::norm_feature_supported(D, dtype))
+    return CP_ERR_UNSUPPORTED_SHAPE;
   if (N > 0 && (!q || !k || !z)) return CP_ERR_INVALID_ARG;
   if (!cp::aligned16(q) || !cp::aligned16(k) || !cp::aligned16(z)) return CP_ERR_MISALIGNED;
   const size_t es = dtype == CP_DTYPE_F32 ? 4 : 2;
@@ -421,18 +426,30 @@ cp_status_t causal_product_normalizer(const void* q, const void* k, float* z, in
   void* scratch = static_cast<char*>(s.base) + cp::kStatusBytes;
   if (s.owned && cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess)
     return CP_ERR_CUDA;
-  return cp::norm_launch(0, q, k, nullptr, z, nullptr, BH, N, D, dtype, scratch, status,
-                         stream) == cudaSuccess
+  return cp::norm_launch(0, q, k, nullptr, z, nullptr, BH, N, D, dtype, scratch, status, stream,
+                         feature) == cudaSuccess
              ? CP_OK
              : CP_ERR_CUDA;
 }
 
-cp_status_t causal_product_normalizer_bwd(const void* q, const void* k, const float* grad_z,
-                                          void* grad_q, void* grad_k, int64_t B, int64_t H,
-                                          int64_t N, int64_t D, cp_dtype_t dtype, void* workspace,
-                                          size_t workspace_bytes, void* stream_) {
+cp_status_t causal_product_normalizer(const void* q, const void* k, float* z, int64_t B, int64_t H,
+                                      int64_t N, int64_t D, cp_dtype_t dtype, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+  return causal_product_normalizer_feature(q, k, z, CP_FEATURE_NONE, B, H, N, D, dtype, workspace,
+                                           workspace_bytes, stream);
+}
+
+cp_status_t causal_product_normalizer_bwd_feature(const void* q, const void* k,
+                                                  const float* grad_z, void* grad_q, void* grad_k,
+                                                  cp_feature_t feature, int64_t B, int64_t H,
+                                                  int64_t N, int64_t D, cp_dtype_t dtype,
+                                                  void* workspace, size_t workspace_bytes,
+                                                  void* stream_) {
+  if (feature != CP_FEATURE_NONE && feature != CP_FEATURE_ELU1) return CP_ERR_INVALID_ARG;
   cp_status_t st = cp::check_norm_dims(B, H, N, D, dtype);
   if (st != CP_OK) return st;
+  if (feature != CP_FEATURE_NONE && !cp::norm_feature_supported(D, dtype))
+    return CP_ERR_UNSUPPORTED_SHAPE;
   if (N > 0 && (!q || !k || !grad_z || !grad_q || !grad_k)) return CP_ERR_INVALID_ARG;
   const void* ptrs[5] = {q, k, grad_z, grad_q, grad_k};
   for (const void* p : ptrs)
@@ -459,13 +476,21 @@ cp_status_t causal_product_normalizer_bwd(const void* q, const void* k, const fl
     return CP_ERR_CUDA;
   // dq scans k forwards, dk scans g q backwards; they share the scratch
   // area one after the other on the stream
-  if (cp::norm_launch(1, q, k, grad_z, nullptr, grad_q, BH, N, D, dtype, scratch, status,
-                      stream) != cudaSuccess)
+  if (cp::norm_launch(1, q, k, grad_z, nullptr, grad_q, BH, N, D, dtype, scratch, status, stream,
+                      feature) != cudaSuccess)
     return CP_ERR_CUDA;
   return cp::norm_launch(2, q, k, grad_z, nullptr, grad_k, BH, N, D, dtype, scratch, status,
-                         stream) == cudaSuccess
+                         stream, feature) == cudaSuccess
              ? CP_OK
              : CP_ERR_CUDA;
+}
+
+cp_status_t causal_product_normalizer_bwd(const void* q, const void* k, const float* grad_z,
+                                          void* grad_q, void* grad_k, int64_t B, int64_t H,
+                                          int64_t N, int64_t D, cp_dtype_t dtype, void* workspace,
+                                          size_t workspace_bytes, void* stream) {
+  return causal_product_normalizer_bwd_feature(q, k, grad_z, grad_q, grad_k, CP_FEATURE_NONE, B, H,
+                                               N, D, dtype, workspace, workspace_bytes, stream);
 }
 
 cp_status_t causal_product_selftest_timeout(void* workspace, uint64_t wait_ns, void* stream_) {

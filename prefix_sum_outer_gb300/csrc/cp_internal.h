@@ -101,10 +101,13 @@ cudaError_t decode_launch(const void* q, const void* k, const void* v, void* out
 // (dq, dk in the input dtype; g fp32).  `scratch` (256-byte aligned) holds
 // norm_scratch_bytes(...); a bounded wait that runs out records
 // CP_ERR_TIMEOUT in *status.
+// With feature != 0, q and k are raw inputs mapped by phi = elu + 1 (rows of
+// 16-byte multiples only: norm_feature_supported).
 size_t norm_scratch_bytes(int64_t BH, int64_t N, int64_t D, cp_dtype_t dtype);
+bool norm_feature_supported(int64_t D, cp_dtype_t dtype);
 cudaError_t norm_launch(int mode, const void* q, const void* k, const float* grad_z, float* z,
                         void* out, int64_t BH, int64_t N, int64_t D, cp_dtype_t dtype,
-                        void* scratch, int* status, cudaStream_t stream);
+                        void* scratch, int* status, cudaStream_t stream, int feature = 0);
 
 // ---- feature map, elementwise over n elements of `dtype`:
 // feature_map: y = phi(x); feature_grad: g *= phi'(x) in place

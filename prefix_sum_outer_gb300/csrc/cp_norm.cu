@@ -387,11 +387,22 @@ __device__ __forceinline__ void lb_record_timeout(int* status, volatile int* abo
   atomicCAS(status, 0, (int)CP_ERR_TIMEOUT);
 }
 
-template <typename T, int V, int K, int MODE>
+// Feature map phi(x) = elu(x) + 1 of causal linear attention on a pair:
+// with e = e^min(x, 0), phi(x) = e + max(x, 0) and phi'(x) = e.
+__device__ __forceinline__ void elu1_pair(float2 x, float2& phi, float2& dphi) {
+  dphi = make_float2(__expf(fminf(x.x, 0.f)), __expf(fminf(x.y, 0.f)));
+  phi = __fadd2_rn(dphi, make_float2(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)));
+}
+
+// FEAT: q and k are raw inputs x mapped by phi on load; dq and dk are then
+// taken through phi' (dq = phi'(x_q) g sum phi(k), dk = phi'(x_k) sum g phi(q)),
+// so every mode streams both q and k.
+template <typename T, int V, int K, int MODE, bool FEAT>
 __global__ void __launch_bounds__(kLbThreads, 3) norm_lb_kernel(const LbArgs a) {
   constexpr int RPT = kLbRowsPerThread / K;
   constexpr bool kRev = MODE == kDK;
-  constexpr int kIn = MODE == kZ ? 2 : 1;  // inputs streamed per tile
+  constexpr bool kTwo = MODE == kZ || FEAT;  // a second input per tile
+  constexpr int kIn = kTwo ? 2 : 1;          // inputs streamed per tile
   constexpr int V2 = V / 2;
   using IO = VecIO<T, V>;
   using R = typename IO::R;
@@ -413,6 +424,7 @@ __global__ void __launch_bounds__(kLbThreads, 3) norm_lb_kernel(const LbArgs a) 
   const int tile_rows = RPT * kLbWarps * gpw;
   const int sp0 = (warp * gpw + gw) * RPT;
   const void* src = MODE == kDK ? a.q : a.k;
+  const void* other = MODE == kDK ? a.k : a.q;  // the second input (z, FEAT)
   // look-back work of this thread: column lb_d of run lb_pt (D <= 128: the
   // runs split the tiles between nparts thread groups; else one run)
   const int nparts = D <= kLbThreads ? kLbThreads / D : 1;
@@ -443,7 +455,8 @@ __global__ void __launch_bounds__(kLbThreads, 3) norm_lb_kernel(const LbArgs a) 
     const int64_t e0 = ((int64_t)p * a.N + lo) * D;
     ptx::mbar_arrive_expect_tx(&full[s], kIn * bytes);
     ptx::bulk_load(st, static_cast<const T*>(src) + e0, bytes, &full[s]);
-    if (kIn == 2) ptx::bulk_load(st + a.in_bytes, static_cast<const T*>(a.q) + e0, bytes, &full[s]);
+    if (kIn == 2)
+      ptx::bulk_load(st + a.in_bytes, static_cast<const T*>(other) + e0, bytes, &full[s]);
   };
 
   if (tid == 0) {
@@ -480,7 +493,7 @@ __global__ void __launch_bounds__(kLbThreads, 3) norm_lb_kernel(const LbArgs a) 
     // ---- this thread's rows, from the stage (scan order); rl = row - lo
     const uint8_t* st = lsm + (size_t)s * a.stage_bytes;
     R xs[RPT][K];
-    R qs[MODE == kZ ? RPT : 1][K];
+    R qs[kTwo ? RPT : 1][K];
     float gz[RPT];
     int rl[RPT];
     bool valid[RPT];
@@ -493,7 +506,7 @@ __global__ void __launch_bounds__(kLbThreads, 3) norm_lb_kernel(const LbArgs a) 
       for (int kk = 0; kk < K; ++kk) {
         const bool ok = valid[i] && colv[kk];
         xs[i][kk] = ok ? IO::lds(st, e0 + col[kk]) : IO::zero();
-        if constexpr (MODE == kZ) qs[i][kk] = ok ? IO::lds(st + a.in_bytes, e0 + col[kk]) : IO::zero();
+        if constexpr (kTwo) qs[i][kk] = ok ? IO::lds(st + a.in_bytes, e0 + col[kk]) : IO::zero();
       }
       gz[i] = (MODE != kZ && valid[i]) ? __ldg(a.grad_z + base + lo + rl[i]) : 0.f;
     }
@@ -512,6 +525,16 @@ __global__ void __launch_bounds__(kLbThreads, 3) norm_lb_kernel(const LbArgs a) 
       for (int kk = 0; kk < K; ++kk) {
         float2 f[V2];
         IO::unpack2(xs[i][kk], f);
+        if constexpr (FEAT) {
+          // phi of the padding would be 1: map real elements only
+          if (valid[i] && colv[kk]) {
+#pragma unroll
+            for (int j = 0; j < V2; ++j) {
+              float2 d_;
+              elu1_pair(f[j], f[j], d_);
+            }
+          }
+        }
 #pragma unroll
         for (int j = 0; j < V2; ++j)
           sum[kk][j] = MODE == kDK ? __ffma2_rn(g2, f[j], sum[kk][j]) : __fadd2_rn(sum[kk][j], f[j]);
@@ -640,18 +663,47 @@ __global__ void __launch_bounds__(kLbThreads, 3) norm_lb_kernel(const LbArgs a) 
       for (int kk = 0; kk < K; ++kk) {
         float2 f[V2];
         IO::unpack2(xs[i][kk], f);
+        if constexpr (FEAT) {
+          if (valid[i] && colv[kk]) {
+#pragma unroll
+            for (int j = 0; j < V2; ++j) {
+              float2 d_;
+              elu1_pair(f[j], f[j], d_);
+            }
+          }
+        }
 #pragma unroll
         for (int j = 0; j < V2; ++j)
           c[kk][j] = MODE == kDK ? __ffma2_rn(g2, f[j], c[kk][j]) : __fadd2_rn(c[kk][j], f[j]);
         if constexpr (MODE == kZ) {
           float2 qf[V2];
           IO::unpack2(qs[i][kk], qf);
+          if constexpr (FEAT) {
+            if (valid[i] && colv[kk]) {
+#pragma unroll
+              for (int j = 0; j < V2; ++j) {
+                float2 d_;
+                elu1_pair(qf[j], qf[j], d_);
+              }
+            }
+          }
 #pragma unroll
           for (int j = 0; j < V2; ++j) zp = __ffma2_rn(qf[j], c[kk][j], zp);
         } else {
           float2 o[V2];
 #pragma unroll
           for (int j = 0; j < V2; ++j) o[j] = MODE == kDQ ? __fmul2_rn(g2, c[kk][j]) : c[kk][j];
+          if constexpr (FEAT) {
+            // chain rule through phi of the output's own raw input
+            float2 xo[V2];
+            IO::unpack2(qs[i][kk], xo);
+#pragma unroll
+            for (int j = 0; j < V2; ++j) {
+              float2 p_, d_;
+              elu1_pair(xo[j], p_, d_);
+              o[j] = __fmul2_rn(o[j], d_);
+            }
+          }
           if (valid[i] && colv[kk]) IO::store2(a.out, gb + rl[i] * D + col[kk], o);
         }
       }
@@ -774,9 +826,9 @@ cudaError_t norm_modes(int mode, const NormArgs& a, int64_t BH, const NormPlan& 
   return norm_run<T, V, K, kDK>(a, BH, pl, agg, st);
 }
 
-template <typename T, int V, int K, int MODE>
+template <typename T, int V, int K, int MODE, bool FEAT>
 cudaError_t lb_run(LbArgs a, const LbPlan& pl, uint8_t* ws, cudaStream_t st) {
-  constexpr int kIn = MODE == kZ ? 2 : 1;
+  constexpr int kIn = (MODE == kZ || FEAT) ? 2 : 1;
   const uint32_t in_bytes =
       (uint32_t)((pl.sh.rows * (size_t)a.D * sizeof(T) + 127) / 128 * 128);
   const uint32_t stage = kIn * in_bytes;
@@ -785,7 +837,7 @@ cudaError_t lb_run(LbArgs a, const LbPlan& pl, uint8_t* ws, cudaStream_t st) {
   const size_t aux = sizeof(float) * ((2 * kLbWarps + 1) * (size_t)a.D +
                                       std::max<size_t>(kLbThreads, a.D));
   const size_t smem = (size_t)S * stage + aux;
-  auto kern = norm_lb_kernel<T, V, K, MODE>;
+  auto kern = norm_lb_kernel<T, V, K, MODE, FEAT>;
   // the dynamic shared-memory opt-in of this kernel on each device: raised
   // when a launch needs more than any before it
   static std::mutex mu;
@@ -829,10 +881,16 @@ cudaError_t lb_run(LbArgs a, const LbPlan& pl, uint8_t* ws, cudaStream_t st) {
 }
 
 template <typename T, int V, int K>
-cudaError_t lb_modes(int mode, const LbArgs& a, const LbPlan& pl, uint8_t* ws, cudaStream_t st) {
-  if (mode == kZ) return lb_run<T, V, K, kZ>(a, pl, ws, st);
-  if (mode == kDQ) return lb_run<T, V, K, kDQ>(a, pl, ws, st);
-  return lb_run<T, V, K, kDK>(a, pl, ws, st);
+cudaError_t lb_modes(int mode, bool feat, const LbArgs& a, const LbPlan& pl, uint8_t* ws,
+                     cudaStream_t st) {
+  if (feat) {
+    if (mode == kZ) return lb_run<T, V, K, kZ, true>(a, pl, ws, st);
+    if (mode == kDQ) return lb_run<T, V, K, kDQ, true>(a, pl, ws, st);
+    return lb_run<T, V, K, kDK, true>(a, pl, ws, st);
+  }
+  if (mode == kZ) return lb_run<T, V, K, kZ, false>(a, pl, ws, st);
+  if (mode == kDQ) return lb_run<T, V, K, kDQ, false>(a, pl, ws, st);
+  return lb_run<T, V, K, kDK, false>(a, pl, ws, st);
 }
 
 }  // namespace
@@ -843,9 +901,12 @@ size_t norm_scratch_bytes(int64_t BH, int64_t N, int64_t D, cp_dtype_t dtype) {
   return norm_plan(BH, N, D, dtype).agg_bytes;
 }
 
+bool norm_feature_supported(int64_t D, cp_dtype_t dtype) { return single_pass(D, dtype); }
+
 cudaError_t norm_launch(int mode, const void* q, const void* k, const float* grad_z, float* z,
                         void* out, int64_t BH, int64_t N, int64_t D, cp_dtype_t dtype,
-                        void* scratch, int* status, cudaStream_t stream) {
+                        void* scratch, int* status, cudaStream_t stream, int feature) {
+  const bool feat = feature != 0;
   if (single_pass(D, dtype)) {
     const LbPlan pl = lb_plan(BH, N, D, dtype);
     LbArgs a{};
@@ -859,11 +920,13 @@ cudaError_t norm_launch(int mode, const void* q, const void* k, const float* gra
     a.BH = (int)BH;
     a.status = status;
     uint8_t* ws = static_cast<uint8_t*>(scratch);
-    if (dtype == CP_DTYPE_BF16) return lb_modes<__nv_bfloat16, 8, 1>(mode, a, pl, ws, stream);
-    if (dtype == CP_DTYPE_F16) return lb_modes<__half, 8, 1>(mode, a, pl, ws, stream);
-    if (pl.sh.K == 1) return lb_modes<float, 4, 1>(mode, a, pl, ws, stream);
-    return lb_modes<float, 4, 2>(mode, a, pl, ws, stream);
+    if (dtype == CP_DTYPE_BF16)
+      return lb_modes<__nv_bfloat16, 8, 1>(mode, feat, a, pl, ws, stream);
+    if (dtype == CP_DTYPE_F16) return lb_modes<__half, 8, 1>(mode, feat, a, pl, ws, stream);
+    if (pl.sh.K == 1) return lb_modes<float, 4, 1>(mode, feat, a, pl, ws, stream);
+    return lb_modes<float, 4, 2>(mode, feat, a, pl, ws, stream);
   }
+  if (feat) return cudaErrorInvalidValue;  // the feature map needs 16-byte rows
   const NormPlan pl = norm_plan(BH, N, D, dtype);
   NormArgs a{};
   a.q = q;

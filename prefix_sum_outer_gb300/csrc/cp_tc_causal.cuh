@@ -296,14 +296,28 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
     uint8_t* q_s = qk_ring + (it % NQK) * L::kQKBytes;
     uint4* p = reinterpret_cast<uint4*>(AGG_ONLY ? q_s + L::kQBytes : q_s);
     constexpr int kChunks = (AGG_ONLY ? 1 : 2) * L::kQBytes / 16;
-#pragma unroll 2
-    for (int i = mtid; i < kChunks; i += 32 * kMapWarps) {
+    constexpr int kTileChunks = L::kQBytes / 16, kBoxChunks = kBoxBytes / 16;
+    auto map_chunk = [&](int i) {
       uint4 w = p[i];
       w.x = elu1_bf16x2(w.x);
       w.y = elu1_bf16x2(w.y);
       w.z = elu1_bf16x2(w.z);
       w.w = elu1_bf16x2(w.w);
       p[i] = w;
+    };
+    if (a.Dr == DP) {
+#pragma unroll 2
+      for (int i = mtid; i < kChunks; i += 32 * kMapWarps) map_chunk(i);
+    } else {
+      // columns D..DP-1 of the boxes are zero padding, and phi(0) would be
+      // 1: leave them.  A box row is 128 bytes (8 chunks of 8 columns)
+      // stored with the 128-byte swizzle, so chunk c of row r holds
+      // logical chunk c ^ (r % 8).
+      for (int i = mtid; i < kChunks; i += 32 * kMapWarps) {
+        const int local = i % kTileChunks, b = local / kBoxChunks, rc = local % kBoxChunks;
+        const int col0 = b * kBoxCols + (((rc & 7) ^ ((rc >> 3) & 7)) << 3);
+        if (col0 < a.Dr) map_chunk(i);
+      }
     }
     fence_proxy_async_smem();
     __syncwarp();

@@ -2,8 +2,9 @@
 
 Each pin checks an implementation ``impl`` (an object with ``fwd(q,k,v)``,
 ``bwd(q,k,v,g)``, ``fwd_state(q,k,v,s0)``, ``bwd_state(q,k,v,g,s0,ds_n)``,
-``norm(q,k)``, ``norm_bwd(q,k,g)``, ``fwd_feature(q,k,v)`` and
-``bwd_feature(q,k,v,g)`` returning float64 numpy arrays, like ``oracle``)
+``norm(q,k)``, ``norm_bwd(q,k,g)``, ``fwd_feature(q,k,v)``,
+``bwd_feature(q,k,v,g)``, ``norm_feature(q,k)`` and ``norm_bwd_feature(q,k,g)``
+returning float64 numpy arrays, like ``oracle``)
 against something other than the recurrence itself: hand-worked values,
 a brute-force quadratic form, closed forms, textbook special cases,
 linearity, causality and finite differences.  ``tests/test_oracle.py``
@@ -514,6 +515,33 @@ def pin_feature_finite_differences(impl, shape=(1, 1, 5, 3)):
         assert np.allclose(grad, fd, rtol=1e-5, atol=1e-6), ("feature finite differences", name)
 
 
+def pin_norm_feature(impl):
+    """The normaliser of mapped features: for x > 0 it is the plain
+    normaliser of x + 1 (exact); in general z = rowsum(tril(phi(Q) phi(K)^T))
+    with numpy's fp64 exp, and the gradients are the dense forms times
+    phi' (dq = phi'(Q) * diag(g) A phi(K), dk = phi'(K) * A^T diag(g) phi(Q))."""
+    rng = _rng(44)
+    shape = (1, 2, 17, 6)
+    qp = _dyadic(rng, shape, 0, 3, 16) + np.float32(1 / 16)
+    kp = _dyadic(rng, shape, 0, 3, 16) + np.float32(1 / 16)
+    g = _dyadic(rng, shape[:-1], -2, 2, 8)
+    assert np.array_equal(impl.norm_feature(qp, kp), impl.norm(qp + 1, kp + 1)), "norm feature shift"
+    a, b = impl.norm_bwd_feature(qp, kp, g), impl.norm_bwd(qp + 1, kp + 1, g)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1]), "norm feature bwd shift"
+    q = rng.standard_normal(shape).astype(np.float32)
+    k = rng.standard_normal(shape).astype(np.float32)
+    qd, kd, gd = (x.astype(np.float64) for x in (q, k, g))
+    fq, fk = _elu1(qd), _elu1(kd)
+    dfq = np.where(qd > 0, 1.0, np.exp(np.minimum(qd, 0.0)))
+    dfk = np.where(kd > 0, 1.0, np.exp(np.minimum(kd, 0.0)))
+    A = np.tril(np.ones((shape[-2], shape[-2])))
+    z = np.sum(A * (fq @ np.swapaxes(fk, -1, -2)), axis=-1)
+    assert _rel(impl.norm_feature(q, k), z) < 1e-12, "norm feature dense form"
+    dq, dk = impl.norm_bwd_feature(q, k, g)
+    assert _rel(dq, dfq * (gd[..., None] * (A @ fk))) < 1e-12, "norm feature dq"
+    assert _rel(dk, dfk * (A.T @ (gd[..., None] * fq))) < 1e-12, "norm feature dk"
+
+
 FEATURE_PINS = [pin_feature_positive_is_shift, pin_feature_quadratic_form,
-                pin_feature_finite_differences]
+                pin_feature_finite_differences, pin_norm_feature]
 ALL_PINS = FWD_PINS + BWD_PINS + STATE_PINS + NORM_PINS + FEATURE_PINS

@@ -291,3 +291,21 @@ def test_f16_dtype_checks(lib):
     assert lib.causal_product_normalizer_workspace_size(1, 2, 64, 12, F16) == 0
     assert lib.causal_product_fwd(A, 2 * A, 3 * A, 4 * A, 1, 1, 64, 16, 16, 3, None, 0,
                                   None) == UNSUPPORTED_DTYPE
+
+
+def test_normalizer_feature_argument_checks(lib):
+    f = lib.causal_product_normalizer_feature
+    args = lambda **kw: dict(dict(q=A, k=2 * A, z=3 * A, feat=1, B=1, H=2, N=64, D=16, dtype=F32), **kw)
+
+    def call(**kw):
+        a = args(**kw)
+        return f(a["q"], a["k"], a["z"], a["feat"], a["B"], a["H"], a["N"], a["D"], a["dtype"],
+                 None, 0, None)
+
+    assert call(feat=5) == INVALID_ARG
+    assert call(D=7) == UNSUPPORTED_SHAPE        # fp32 rows of 28 bytes: no feature map
+    assert call(N=0) == OK
+    assert call(N=0, D=7, feat=0) == OK          # the plain normaliser takes any fp32 D
+    b = lib.causal_product_normalizer_bwd_feature
+    assert b(A, 2 * A, 3 * A, 4 * A, 5 * A, 5, 1, 2, 64, 16, F32, None, 0, None) == INVALID_ARG
+    assert b(A, 2 * A, 3 * A, 4 * A, 5 * A, 1, 1, 2, 64, 12, BF16, None, 0, None) == UNSUPPORTED_SHAPE

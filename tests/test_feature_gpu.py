@@ -25,6 +25,8 @@ FWD_SHAPES = [
     (1, 2, 700, 256, 64, "bf16"),
     (2, 2, 300, 192, 64, "bf16"),
     (3, 5, 129, 64, 128, "bf16"),
+    (2, 3, 500, 48, 64, "bf16"),      # D below the 64-column box: padded columns
+    (1, 2, 333, 96, 64, "bf16"),
     (2, 3, 200, 16, 16, "f32"),
     (1, 2, 513, 36, 20, "f32"),
 ]
@@ -32,6 +34,7 @@ BWD_SHAPES = [
     (2, 4, 1000, 64, 64, "bf16"),
     (8, 16, 1024, 64, 64, "bf16"),
     (1, 2, 777, 128, 128, "bf16"),
+    (2, 2, 400, 40, 64, "bf16"),
     (2, 3, 200, 16, 16, "f32"),
 ]
 

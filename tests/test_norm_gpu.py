@@ -119,3 +119,59 @@ def test_normalised_attention_composes():
     torch.cuda.synchronize()
     ref = oracle.fwd(to_np(q), to_np(k), to_np(v)) / oracle.norm(to_np(q), to_np(k))[..., None]
     assert row_rel_err(to_np(att), ref) <= TOL["bf16"]
+
+
+# ---- the normaliser of mapped features from raw inputs (phi = elu + 1 in the
+# kernel); phi > 0, so z itself is the scale of its summation error
+FEAT_SHAPES = [
+    (2, 3, 1000, 64, "bf16"),
+    (1, 1, 20000, 128, "bf16"),
+    (2, 2, 300, 256, "f32"),
+    (2, 3, 500, 36, "f32"),
+]
+
+
+@pytest.mark.parametrize("shape", FEAT_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_normalizer_feature_against_oracle(shape):
+    B, H, N, D, dt = shape
+    q, k, gz = make_norm_inputs(B, H, N, D, DT[dt], seed=N + D, feature="normal")
+    z = cp.causal_product_normalizer(q.to(DEV), k.to(DEV), feature="elu1")
+    dq, dk = cp.causal_product_normalizer_bwd(q.to(DEV), k.to(DEV), gz.to(DEV), feature="elu1")
+    torch.cuda.synchronize()
+    ref = oracle.norm_feature(to_np(q), to_np(k))
+    assert float(np.max(np.abs(to_np(z) - ref) / ref)) <= Z_TOL
+    r_dq, r_dk = oracle.norm_bwd_feature(to_np(q), to_np(k), gz.numpy())
+    assert row_rel_err(to_np(dq), r_dq) <= TOL[dt]
+    assert row_rel_err(to_np(dk), r_dk) <= TOL[dt]
+
+
+def test_normalised_attention_from_raw_inputs():
+    """out / z with phi applied inside both the product and the normaliser."""
+    B, H, N, D, M = 2, 4, 700, 64, 64
+    from prefix_sum_outer_gb300.workloads import make_inputs
+    x_q, x_k, v, _ = make_inputs(B, H, N, D, M, torch.bfloat16, seed=21, feature="normal",
+                                 backward=False)
+    xq, xk, vd = x_q.to(DEV), x_k.to(DEV), v.to(DEV)
+    att = (cp.causal_product(xq, xk, vd, feature="elu1").float()
+           / cp.normalizer(xq, xk, feature="elu1")[..., None])
+    torch.cuda.synchronize()
+    ref = (oracle.fwd_feature(to_np(x_q), to_np(x_k), to_np(v))
+           / oracle.norm_feature(to_np(x_q), to_np(x_k))[..., None])
+    assert row_rel_err(to_np(att), ref) <= TOL["bf16"]
+
+
+def test_normalizer_feature_autograd():
+    q, k, gz = make_norm_inputs(2, 2, 400, 64, torch.bfloat16, seed=4, feature="normal")
+    qd, kd = q.to(DEV).requires_grad_(), k.to(DEV).requires_grad_()
+    z = cp.normalizer(qd, kd, feature="elu1")
+    z.backward(gz.to(DEV))
+    torch.cuda.synchronize()
+    r_dq, r_dk = oracle.norm_bwd_feature(to_np(q), to_np(k), gz.numpy())
+    assert row_rel_err(to_np(qd.grad), r_dq) <= TOL["bf16"]
+    assert row_rel_err(to_np(kd.grad), r_dk) <= TOL["bf16"]
+
+
+def test_normalizer_feature_needs_16_byte_rows():
+    q = torch.zeros((1, 1, 16, 7), device=DEV)
+    with pytest.raises(cp.CausalProductError):
+        cp.causal_product_normalizer(q, q.clone(), feature="elu1")

@@ -88,6 +88,12 @@ MUTANTS = {
     # phi' taken as phi
     "feature_dphi_is_phi": [("if (feature == 1) return x > 0.0 ? 1.0 : exp(x);",
                              "if (feature == 1) return x > 0.0 ? x + 1.0 : exp(x);")],
+    # the normaliser of mapped features without phi' on dq
+    "norm_feature_dq_no_dphi": [("dqs[i * D + d] = dphi(feature, qx) * ((double)gs[i] * c[d]);",
+                                 "dqs[i * D + d] = (double)gs[i] * c[d];")],
+    # the normaliser of mapped features reading phi(k) for the readout
+    "norm_feature_reads_k": [("acc += phi(feature, (double)qs[i * D + d]) * c[d];",
+                              "acc += phi(feature, (double)ks[i * D + d]) * c[d];")],
 }
 
 
@@ -101,6 +107,8 @@ class _Impl:
         lib.cpo_bwd_state.argtypes = [p, p, p, p, p, p, p, p, p, p, i64, i64, i64, i64, c_int]
         lib.cpo_norm.argtypes = [p, p, p, i64, i64, i64, c_int]
         lib.cpo_fwd_feature.argtypes = [p, p, p, p, c_int, i64, i64, i64, i64, c_int]
+        lib.cpo_norm_feature.argtypes = [p, p, p, c_int, i64, i64, i64, c_int]
+        lib.cpo_norm_bwd_feature.argtypes = [p, p, p, p, p, c_int, i64, i64, i64, c_int]
         lib.cpo_bwd_feature.argtypes = [p, p, p, p, p, p, p, c_int, i64, i64, i64, i64, c_int]
         lib.cpo_norm_bwd.argtypes = [p, p, p, p, p, i64, i64, i64, c_int]
         self.lib = lib
@@ -125,6 +133,26 @@ class _Impl:
                                         dq.ctypes.data, dk.ctypes.data, dv.ctypes.data, 1, BH, N,
                                         D, M, 1) == 0
         return dq, dk, dv
+
+    def norm_feature(self, q, k):
+        q, k = (np.ascontiguousarray(x, np.float32) for x in (q, k))
+        lead = q.shape[:-2]
+        BH = int(np.prod(lead)) if lead else 1
+        N, D = q.shape[-2], q.shape[-1]
+        z = np.zeros(lead + (N,))
+        assert self.lib.cpo_norm_feature(q.ctypes.data, k.ctypes.data, z.ctypes.data, 1, BH, N,
+                                         D, 1) == 0
+        return z
+
+    def norm_bwd_feature(self, q, k, g):
+        q, k, g = (np.ascontiguousarray(x, np.float32) for x in (q, k, g))
+        lead = q.shape[:-2]
+        BH = int(np.prod(lead)) if lead else 1
+        N, D = q.shape[-2], q.shape[-1]
+        dq, dk = np.zeros(lead + (N, D)), np.zeros(lead + (N, D))
+        assert self.lib.cpo_norm_bwd_feature(q.ctypes.data, k.ctypes.data, g.ctypes.data,
+                                             dq.ctypes.data, dk.ctypes.data, 1, BH, N, D, 1) == 0
+        return dq, dk
 
     def norm(self, q, k):
         q, k = (np.ascontiguousarray(x, np.float32) for x in (q, k))
