@@ -548,6 +548,22 @@ def run_ours(args, world, rank, local):
                         "frac": nb_bytes / (nb_ms / 1e3) / 1e9 / peak},
                 "timing": "CUDA events over 20 calls each; a call is a workspace fill and "
                           "one launch per output (z; dq then dk)"}
+        # the same with phi = elu + 1 applied to raw x ~ N(0, 1) in the kernel;
+        # its backward streams q and k in both launches
+        rq, rk, _, _ = make_inputs(w.B, w.H, w.N, w.D, 1, w.torch_dtype, seed=80,
+                                   feature="normal", backward=False)
+        rq, rk = rq.to(dev), rk.to(dev)
+        ff_ms = timed(lambda: cp.causal_product_normalizer(rq, rk, z=zb, workspace=ws_n,
+                                                           stream=stream, feature="elu1"))
+        fb_ms = timed(lambda: cp.causal_product_normalizer_bwd(rq, rk, gz, nq, nk, workspace=ws_n,
+                                                               stream=stream, feature="elu1"))
+        fb_bytes = (6 * s_ * w.D + 8) * w.token_heads
+        norm["feature_elu1"] = {
+            "fwd": {"us": ff_ms * 1e3, "bytes": nf_bytes,
+                    "frac": nf_bytes / (ff_ms / 1e3) / 1e9 / peak},
+            "bwd": {"us": fb_ms * 1e3, "bytes": fb_bytes,
+                    "frac": fb_bytes / (fb_ms / 1e3) / 1e9 / peak}}
+        del rq, rk
 
     # ---- the forward with the feature map phi(x) = elu(x) + 1 applied to raw
     # x_q, x_k ~ N(0, 1) inside the product kernel (both branches of phi
