@@ -32,9 +32,10 @@
 // work is done.
 //
 // With a feature map (the FEAT instantiation), the loaded Q and K tiles are
-// raw inputs x: the state and O groups map them in shared memory, phi(x) =
-// elu(x) + 1 (x + 1 for x > 0, e^x otherwise, rounded to bf16), before any
-// MMA reads them, so phi(q) and phi(k) never exist in global memory.
+// raw inputs x: the O group (the state group in the aggregate-only mode)
+// maps them in shared memory, phi(x) = elu(x) + 1 (x + 1 for x > 0, e^x
+// otherwise, rounded to bf16), before any MMA reads them, so phi(q) and
+// phi(k) never exist in global memory.
 //
 // Long sequences with few problems are split into G segments per problem;
 // a first launch of the same kernel in aggregate-only mode writes each
@@ -204,9 +205,10 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
   uint64_t* qk_ready = s_done + 7;          // [NQK] S, O groups -> MMA: Q/K(t) mapped (FEAT)
   // the barrier the MMA issuers wait on before reading a Q/K stage
   uint64_t* const qk_bar = FEAT ? qk_ready : full_qk;
-  // FEAT: warps that map a tile (the state group; the O group too when
-  // there are outputs) and their threads
-  constexpr int kMapWarps = AGG_ONLY ? kSWarps : kSWarps + kOWarps;
+  // FEAT: warps that map a tile: the O group, whose read-out has slack (NO
+  // accumulators), not the state group, which sits on the state chain; the
+  // state group only in the aggregate-only mode, which has no read-out
+  constexpr int kMapWarps = AGG_ONLY ? kSWarps : kOWarps;
   // a group maps tile it + kAhead during its iteration it: as far ahead as
   // the Q/K ring allows, off the MMA chain (mapping tile it + kAhead needs
   // only the stage tile it - 1 releases)
@@ -610,13 +612,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
         }
         tmem_st_wait();
       }
-      const int mtid = threadIdx.x - 32 * kSWarp0;  // state group: mapping threads 0..127
-      for (int j = 0; FEAT && j < kAhead && j < n_it && ok; ++j) ok = map_qk(j, mtid);
       for (int it = 0; it < n_it && ok; ++it) {
-        if (FEAT && kAhead == 0 && !map_qk(it, mtid)) {
-          ok = false;
-          break;
-        }
         const int b = it % NSB;
         uint8_t* sbuf = s_tile + b * L::kSBufBytes;
         // the Q S that last read this copy (tile it - NSB) has completed
@@ -659,8 +655,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(s_ready);
-        // map a later tile's Q/K while this tile's MMAs run
-        if (FEAT && kAhead > 0 && it + kAhead < n_it) ok = map_qk(it + kAhead, mtid);
+
       }
       // the last segment in scan order hands on the state after its last tile
       if (STATE_OUT && ok && last_seg && n_it > 0) {
@@ -723,12 +718,12 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
     // ------------------------------------------------------------ O group
     const int o_tid = threadIdx.x - 32 * kOWarp0;   // 0..kOThreads-1
     bool ok = true;
-    // FEAT: the O group maps the other half of every tile, tile it + kAhead
-    // before the read-out of tile it
+    // FEAT: the O group maps every tile, tile it + kAhead before the
+    // read-out of tile it
     for (int j = 0; FEAT && !AGG_ONLY && j < kAhead && j < n_it && ok; ++j)
-      ok = map_qk(j, 32 * kSWarps + o_tid);
+      ok = map_qk(j, o_tid);
     for (int it = 0; !AGG_ONLY && it < n_it && ok; ++it) {
-      if (FEAT && it + kAhead < n_it && !map_qk(it + kAhead, 32 * kSWarps + o_tid)) {
+      if (FEAT && it + kAhead < n_it && !map_qk(it + kAhead, o_tid)) {
         ok = false;
         break;
       }
