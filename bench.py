@@ -44,12 +44,12 @@ CAUSAL_SOURCES = ("cp_tc.cu", "cp_tc_causal.cuh", "cp_tc_common.cuh", "sm103_ptx
 BWD_SOURCES = ("cp_tc_dkdv.cu", "cp_tc_dkdv.cuh", "cp_tc_causal.cuh", "cp_tc_common.cuh",
                "sm103_ptx.cuh")
 PROFILED_TRAFFIC = {
-    "source_sha256": "cbe78c64def120300af7bd0c63a0e21af2369b7acd55d5195ed9824ece264a9d",
-    "bytes_per_launch": 211525120,  # 201.40 MB read + 10.12 MB written (forward launch)
+    "source_sha256": "02f99ab66a117d082bbb60d661bc0c797ba40fdc24dcab8efa975f6072c137d0",
+    "bytes_per_launch": 212234496,  # 201.40 MB read + 10.84 MB written (forward launch)
 }
 PROFILED_TRAFFIC_BWD = {
-    "source_sha256": "50ce47de8a6d4a1f5da6f1aed3f09151f737e66e6d6ceb400b7e6cd58835cbe1",
-    "bytes_per_launch": 605446656,  # 463.57 MB read + 141.88 MB written (one backward launch)
+    "source_sha256": "6c513e1788c825a297bae150ac46c4a727dc0d4ebaad7853ab477d928e6a4028",
+    "bytes_per_launch": 605719296,  # 463.78 MB read + 141.94 MB written (one backward launch)
 }
 
 
