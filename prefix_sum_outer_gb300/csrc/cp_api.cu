@@ -93,6 +93,9 @@ cp_status_t acquire(Scratch& s, void* workspace, size_t workspace_bytes, size_t 
     return CP_ERR_CUDA;
   }
   s.owned = true;
+  // a fresh allocation starts with a clear status word; a caller's workspace
+  // keeps its (sticky) status until causal_product_status() reads it
+  if (cudaMemsetAsync(s.base, 0, sizeof(int), stream) != cudaSuccess) return CP_ERR_CUDA;
   return CP_OK;
 }
 
@@ -166,10 +169,6 @@ cp_status_t causal_product_fwd_state(const void* q, const void* k, const void* v
   if (st != CP_OK) return st;
   int* status = static_cast<int*>(s.base);
   float* agg = reinterpret_cast<float*>(static_cast<char*>(s.base) + cp::kStatusBytes);
-  // a fresh allocation starts with a clear status word; a caller's workspace
-  // keeps its (sticky) status until causal_product_status() reads it
-  if (s.owned && cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess)
-    return CP_ERR_CUDA;
   cp::Product p{q, k, v, out, BH, N, D, M, false};
   p.state_in = state_in;
   p.state_out = state_out;
@@ -210,8 +209,6 @@ cp_status_t causal_product_fwd_feature(const void* q, const void* k, const void*
   if (st != CP_OK) return st;
   int* status = static_cast<int*>(s.base);
   float* agg = reinterpret_cast<float*>(static_cast<char*>(s.base) + cp::kStatusBytes);
-  if (s.owned && cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess)
-    return CP_ERR_CUDA;
   cp::Product p{q, k, v, out, BH, N, D, M, false};
   p.feature = feature;
   return cp::run_product(p, dtype, agg, status, stream);
@@ -259,8 +256,6 @@ cp_status_t causal_product_bwd_feature(const void* q, const void* k, const void*
   cp::Scratch s;
   st = cp::acquire(s, workspace, workspace_bytes, need, stream);
   if (st != CP_OK) return st;
-  if (s.owned && cudaMemsetAsync(s.base, 0, sizeof(int), stream) != cudaSuccess)
-    return CP_ERR_CUDA;
   char* fq = static_cast<char*>(s.base) + bwd_ws;
   char* fk = fq + copy;
   const int64_t n = BH * N * D;
@@ -322,10 +317,6 @@ cp_status_t causal_product_bwd_state(const void* q, const void* k, const void* v
   if (st != CP_OK) return st;
   int* status = static_cast<int*>(s.base);
   float* agg = reinterpret_cast<float*>(static_cast<char*>(s.base) + cp::kStatusBytes);
-  // a fresh allocation starts with a clear status word; a caller's workspace
-  // keeps its (sticky) status until causal_product_status() reads it
-  if (s.owned && cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess)
-    return CP_ERR_CUDA;
   // dq_i = (S_0 + sum_{j<=i} k_j v_j^T) g_i: the forward product (g, v, k),
   // whose state sum v k^T is the transpose of the caller's S_0
   cp::Product pq{grad_out, v, k, grad_q, BH, N, M, D, false};
@@ -424,8 +415,6 @@ cp_status_t causal_product_normalizer_feature(const void* q, const void* k, floa
   if (st != CP_OK) return st;
   int* status = static_cast<int*>(s.base);
   void* scratch = static_cast<char*>(s.base) + cp::kStatusBytes;
-  if (s.owned && cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess)
-    return CP_ERR_CUDA;
   return cp::norm_launch(0, q, k, nullptr, z, nullptr, BH, N, D, dtype, scratch, status, stream,
                          feature) == cudaSuccess
              ? CP_OK
@@ -472,8 +461,6 @@ cp_status_t causal_product_normalizer_bwd_feature(const void* q, const void* k,
   if (st != CP_OK) return st;
   int* status = static_cast<int*>(s.base);
   void* scratch = static_cast<char*>(s.base) + cp::kStatusBytes;
-  if (s.owned && cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess)
-    return CP_ERR_CUDA;
   // dq scans k forwards, dk scans g q backwards; they share the scratch
   // area one after the other on the stream
   if (cp::norm_launch(1, q, k, grad_z, nullptr, grad_q, BH, N, D, dtype, scratch, status, stream,
