@@ -90,7 +90,7 @@ __device__ __forceinline__ void mm4x4(float (&acc)[4][4], const float* A, int ld
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads) simt_kernel(SimtArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) simt_kernel(SimtArgs a) {
   extern __shared__ __align__(16) float smem[];
   const int D = a.D, Mb = a.Mb, C = a.C;
   const int Dp = round4(D), Mbp = round4(Mb);
@@ -146,61 +146,78 @@ __global__ void __launch_bounds__(kThreads) simt_kernel(SimtArgs a) {
     const int t = a.reverse ? (n_t - 1 - it) : it;
     const int64_t r0 = seg_lo + (int64_t)t * C;
     __syncthreads();
-    // ---- load: q row-major, k transposed (consecutive threads on
-    // consecutive rows, so the transposed stores hit distinct banks), v.
-    // Each thread issues kBatch loads before it stores any of them.
-    constexpr int kBatch = 8;
-    for (int b0 = threadIdx.x; b0 < Dp * C; b0 += kBatch * kThreads) {
-      float r_[kBatch];
+    // ---- load, as two-dimensional loops (rows by warp, columns by lane: no
+    // index division).  q and v rows are read along their columns
+    // (coalesced); k is stored transposed with consecutive lanes on
+    // consecutive rows, so its shared-memory stores hit distinct banks.
+    // Each thread issues all its loads of a row block before storing them.
+    {
+      const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+      constexpr int kW = kThreads / 32;
+      // k: Kt[d][r] for d = warp + kW i, r = lane + 32 j
+      for (int d0 = warp; d0 < Dp; d0 += 4 * kW) {
+        float r_[4][2];
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int e = b0 + u * kThreads;
-        const int d = e / C, r = e % C;
-        const int64_t row = r0 + r;
-        const bool in = e < Dp * C && row < seg_hi && d < D;
-        float x = in ? widen(kb[row * D + d]) : 0.f;
-        if (a.feature && in) x = elu1(x);
-        r_[u] = x;
-      }
+        for (int u = 0; u < 4; ++u) {
+          const int d = d0 + u * kW;
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int e = b0 + u * kThreads;
-        if (e < Dp * C) Kt[e] = r_[u];  // e = d * C + r
-      }
-    }
-    if (!a.agg_only) {
-      for (int b0 = threadIdx.x; b0 < C * Dp; b0 += kBatch * kThreads) {
-        float r_[kBatch];
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          const int e = b0 + u * kThreads;
-          const int r = e / Dp, d = e % Dp;
-          const int64_t row = r0 + r;
-          const bool in = e < C * Dp && row < seg_hi && d < D;
-          float x = in ? widen(qb[row * D + d]) : 0.f;
-          if (a.feature && in) x = elu1(x);
-          r_[u] = x;
+          for (int jj = 0; jj < 2; ++jj) {
+            const int r = lane + 32 * jj;
+            const int64_t row = r0 + r;
+            const bool in = d < D && r < C && row < seg_hi;
+            float x = in ? widen(kb[row * D + d]) : 0.f;
+            if (a.feature && in) x = elu1(x);
+            r_[u][jj] = x;
+          }
         }
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          const int e = b0 + u * kThreads;
-          if (e < C * Dp) Qs[e] = r_[u];
+        for (int u = 0; u < 4; ++u) {
+          const int d = d0 + u * kW;
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj) {
+            const int r = lane + 32 * jj;
+            if (d < Dp && r < C) Kt[d * C + r] = r_[u][jj];
+          }
         }
       }
-    }
-    for (int b0 = threadIdx.x; b0 < C * Mbp; b0 += kBatch * kThreads) {
-      float r_[kBatch];
+      // q: Qs[r][d] and v: Vs[r][m], in 32-column blocks (column lane + 32 cb),
+      // four rows r = r1 + kW u of a block in flight per thread
+      for (int cb = 0; !a.agg_only && cb * 32 < Dp; ++cb) {
+        const int d = lane + 32 * cb;
+        for (int r1 = warp; r1 < C; r1 += 4 * kW) {
+          float r_[4];
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int e = b0 + u * kThreads;
-        const int r = e / Mbp, m = e % Mbp;
-        const int64_t row = r0 + r;
-        r_[u] = (e < C * Mbp && row < seg_hi && m < mw) ? widen(vb[row * a.M + m0 + m]) : 0.f;
+          for (int u = 0; u < 4; ++u) {
+            const int r = r1 + u * kW;
+            const int64_t row = r0 + r;
+            const bool in = r < C && row < seg_hi && d < D;
+            float x = in ? widen(qb[row * D + d]) : 0.f;
+            if (a.feature && in) x = elu1(x);
+            r_[u] = x;
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int r = r1 + u * kW;
+            if (r < C && d < Dp) Qs[r * Dp + d] = r_[u];
+          }
+        }
       }
+      for (int cb = 0; cb * 32 < Mbp; ++cb) {
+        const int m = lane + 32 * cb;
+        for (int r1 = warp; r1 < C; r1 += 4 * kW) {
+          float r_[4];
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int e = b0 + u * kThreads;
-        if (e < C * Mbp) Vs[e] = r_[u];
+          for (int u = 0; u < 4; ++u) {
+            const int r = r1 + u * kW;
+            const int64_t row = r0 + r;
+            r_[u] = (r < C && row < seg_hi && m < mw) ? widen(vb[row * a.M + m0 + m]) : 0.f;
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int r = r1 + u * kW;
+            if (r < C && m < Mbp) Vs[r * Mbp + m] = r_[u];
+          }
+        }
       }
     }
     __syncthreads();
