@@ -286,10 +286,8 @@ def run_ours(args, world, rank, local):
         cp.causal_product_fwd(qd, kd, vd, out=out, workspace=ws_f, stream=stream)
         cp.causal_product_bwd(qd, kd, vd, gd, dq, dk, dv, workspace=ws_b, stream=stream)
 
-    # kernels of ours launched per step (tensor-core path): forward 1 product;
-    # backward 1 launch (dk/dv and dq scans) for unsplit problems on fewer
-    # than the SMs, else dq plus the fused dk/dv scan (or 2 more products);
-    # a scan split into segments adds one aggregate launch
+    # kernels of ours launched per step: the library's own count for the
+    # forward and the backward call of this shape
     launches_per_step = _launches_per_step(w)
 
     for _ in range(max(args.warmup, 0)):
@@ -674,34 +672,34 @@ def run_ours(args, world, rank, local):
     return 0
 
 
-def _segmented(w):
-    """True when the products are split into segments (an aggregate launch
-    precedes each scan launch): the workspace then holds more than the
-    256-byte status word."""
-    import prefix_sum_outer_gb300 as cp
-    lib = cp.load_library()
-    return lib.causal_product_workspace_size(w.B, w.H, w.N, w.D, w.M, 1, 0) > 256
-
-
 def _fused_dkdv(w):
-    """bf16 with D, M <= 64: the backward computes dk and dv in one launch."""
+    """bf16 with D, M <= 64: the backward computes dk and dv in one scan."""
     return w.dtype == "bf16" and w.D <= 64 and w.M <= 64
 
 
+def _launch_count(w, backward):
+    import prefix_sum_outer_gb300 as cp
+    c = cp.causal_product_launch_count(w.B, w.H, w.N, w.D, w.M, w.torch_dtype, backward)
+    if c < 0:
+        raise RuntimeError(f"shape of {w.name} rejected by the library")
+    return c
+
+
+def _segmented(w):
+    """The forward scan is split into segments (sums, prefix, scan)."""
+    return _launch_count(w, False) > 1
+
+
 def _single_launch_bwd(w):
-    """Unsplit problems, fewer than the SMs: the backward is one launch."""
-    import torch
-    n_sm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    return _fused_dkdv(w) and not _segmented(w) and w.B * w.H < n_sm
+    """The whole backward (dk/dv and dq scans) is one launch."""
+    return _fused_dkdv(w) and _launch_count(w, True) == 1
 
 
 def _launches_per_step(w):
-    if _single_launch_bwd(w):
-        return 2
-    per_scan = 2 if _segmented(w) else 1
-    # forward: one product; backward: dq plus either the fused dk/dv scan
-    # or the dv and dk products
-    return per_scan * (1 + 1 + (1 if _fused_dkdv(w) else 2))
+    """Kernels one fwd + bwd step launches, as the library plans them (one per
+    unsplit scan, three per split scan, one for the whole backward when it
+    fits a single launch)."""
+    return _launch_count(w, False) + _launch_count(w, True)
 
 
 def main(argv=None):

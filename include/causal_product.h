@@ -107,6 +107,16 @@ typedef enum {
 CP_API size_t causal_product_workspace_size(int64_t B, int64_t H, int64_t N, int64_t D, int64_t M,
                                             cp_dtype_t dtype, int backward);
 
+/* Number of kernels one causal_product_fwd (backward = 0) or
+ * causal_product_bwd (backward = 1) call launches for this problem, with no
+ * carried state: 1 per unsplit scan, 3 per scan split into segments (the
+ * segment sums, their prefix, the scan), and 1 for the whole backward when
+ * bf16 with D, M <= 64 runs unsplit on fewer problems than SMs.  Pure host
+ * computation (the SM count of the current device, else 152).  Returns -1
+ * for arguments the entry points would reject, 0 when N = 0. */
+CP_API int causal_product_launch_count(int64_t B, int64_t H, int64_t N, int64_t D, int64_t M,
+                                       cp_dtype_t dtype, int backward);
+
 /* Forward: out[b,h,i,:] = sum_{j<=i} (q[b,h,i,:] . k[b,h,j,:]) v[b,h,j,:].
  * `stream` is a cudaStream_t passed as void*. */
 CP_API cp_status_t causal_product_fwd(const void* q, const void* k, const void* v, void* out,

@@ -31,8 +31,8 @@ __all__ = [
     "causal_product_fwd_noalloc", "causal_product_decode",
     "causal_product_normalizer", "causal_product_normalizer_bwd", "normalizer",
     "causal_product_fwd_feature", "causal_product_bwd_feature", "FEATURES",
-    "causal_product_workspace_size", "causal_product_status", "causal_product_error_string",
-    "library_path", "load_library",
+    "causal_product_workspace_size", "causal_product_launch_count", "causal_product_status",
+    "causal_product_error_string", "library_path", "load_library",
 ]
 
 CP_DTYPE_F32, CP_DTYPE_BF16, CP_DTYPE_F16 = 0, 1, 2
@@ -75,6 +75,8 @@ def load_library(rebuild: bool = True) -> ctypes.CDLL:
             p, i64, c_int, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
             lib.causal_product_workspace_size.argtypes = [i64, i64, i64, i64, i64, c_int, c_int]
             lib.causal_product_workspace_size.restype = sz
+            lib.causal_product_launch_count.argtypes = [i64, i64, i64, i64, i64, c_int, c_int]
+            lib.causal_product_launch_count.restype = c_int
             lib.causal_product_fwd.argtypes = [p, p, p, p, i64, i64, i64, i64, i64, c_int, p, sz, p]
             lib.causal_product_fwd.restype = c_int
             lib.causal_product_bwd.argtypes = [p, p, p, p, p, p, p, i64, i64, i64, i64, i64, c_int,
@@ -164,6 +166,15 @@ def causal_product_workspace_size(B: int, H: int, N: int, D: int, M: int,
                                   backward: bool = False) -> int:
     return int(load_library().causal_product_workspace_size(B, H, N, D, M, _DTYPES[dtype],
                                                             int(bool(backward))))
+
+
+def causal_product_launch_count(B: int, H: int, N: int, D: int, M: int,
+                                dtype: torch.dtype = torch.bfloat16,
+                                backward: bool = False) -> int:
+    """Kernels one causal_product_fwd (or, with ``backward``, _bwd) call
+    launches for this shape; -1 for a shape the entry points reject."""
+    return int(load_library().causal_product_launch_count(B, H, N, D, M, _DTYPES[dtype],
+                                                          int(bool(backward))))
 
 
 def _workspace(nbytes: int, device) -> torch.Tensor:

@@ -137,6 +137,36 @@ size_t causal_product_workspace_size(int64_t B, int64_t H, int64_t N, int64_t D,
   return cp::workspace_bytes(B * H, N, D, M, dtype, backward != 0);
 }
 
+int causal_product_launch_count(int64_t B, int64_t H, int64_t N, int64_t D, int64_t M,
+                                cp_dtype_t dtype, int backward) {
+  if (cp::check_dims(B, H, N, D, M, dtype) != CP_OK) return -1;
+  if (N == 0) return 0;
+  const int64_t BH = B * H;
+  // a split scan is three launches: segment sums, their prefix, the scan
+  auto product = [&](int64_t d, int64_t m) {
+    const int G = dtype == CP_DTYPE_BF16 ? cp::tc_plan(BH, N, d, m).G
+                                         : cp::simt_plan(BH, N, d, m).G;
+    return G > 1 ? 3 : 1;
+  };
+  if (!backward) return product(D, M);
+  if (dtype == CP_DTYPE_BF16) {
+    const cp::TcPlan plan = cp::tc_plan(BH, N, D, M);
+    if (cp::tc_dkdv_supported(plan)) {
+      int dev = 0, n_sm = 0;
+      if (cudaGetDevice(&dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();  // no device here: plan for the 152-SM part
+        n_sm = cp::kPlanSMs;
+      }
+      if (plan.G == 1 && BH < n_sm) return 1;
+      // dq product, the reverse segment sums and their prefix, the dk/dv scan
+      return product(M, D) + (plan.G > 1 ? 2 : 0) + 1;
+    }
+  }
+  // dq (g, v, k), dv (k, q, g), dk (v, g, q)
+  return product(M, D) + product(D, M) + product(M, D);
+}
+
 cp_status_t causal_product_fwd_state(const void* q, const void* k, const void* v, void* out,
                                      const float* state_in, float* state_out, int64_t B,
                                      int64_t H, int64_t N, int64_t D, int64_t M,

@@ -75,9 +75,17 @@ struct TcPlan {
 TcPlan tc_plan(int64_t BH, int64_t N, int64_t D, int64_t M);
 cp_status_t tc_launch(const Product& p, const TcPlan& plan, float* agg, int* status,
                       cudaStream_t stream);
-// Only pass 1 of the two-pass scan (a no-op when plan.G == 1).
+// Only pass 1 of the two-pass scan (a no-op when plan.G == 1).  On return
+// agg holds each segment's starting state (seg_prefix_launch has run).
 cp_status_t tc_aggregate(const Product& p, const TcPlan& plan, float* agg, int* status,
                          cudaStream_t stream);
+
+// Between the passes of a split scan: agg [P][G][E] fp32 per-segment
+// aggregates become, in place, the exclusive prefix in scan order (slot s
+// holds the sum of the slots before it: s' < s forward, s' > s reverse).
+// The slot last in scan order is only written.  A no-op when G <= 1.
+cudaError_t seg_prefix_launch(float* agg, int64_t P, int G, int64_t E, bool reverse,
+                              cudaStream_t stream);
 
 // Backward pass for bf16 with D, M <= 64 (tc_dkdv_supported(plan), plan =
 // tc_plan(BH, N, D, M)): dq is one product launch; dk and dv share the

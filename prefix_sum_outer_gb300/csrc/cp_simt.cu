@@ -131,12 +131,9 @@ __global__ void __launch_bounds__(kThreads, 4) simt_kernel(SimtArgs a) {
     float acc = 0.f;
     if (d0 < D && m_ < mw) {
       if (st_in != nullptr) acc = st_in[d0 * a.st_ld_r + (m0 + m_) * a.st_ld_c];
-      if (!a.agg_only && a.agg_in != nullptr) {
-        const int lo = a.reverse ? s + 1 : 0;
-        const int hi = a.reverse ? a.G : s;
-        for (int s2 = lo; s2 < hi; ++s2)
-          acc += a.agg_in[((int64_t)pidx * a.G + s2) * D * Mb + d0 * Mb + m_];
-      }
+      // slot s of agg_in: the sum of the preceding segments' aggregates
+      if (!a.agg_only && a.agg_in != nullptr && (a.reverse ? s < a.G - 1 : s > 0))
+        acc += a.agg_in[((int64_t)pidx * a.G + s) * D * Mb + d0 * Mb + m_];
     }
     Ss[e] = acc;
   }
@@ -361,6 +358,9 @@ cudaError_t simt_launch(const Product& p, const SimtPlan& plan, float* agg, int*
     // (the aggregate pass ignores the carried state: agg_only is set)
     kern<<<(unsigned)(problems * (plan.G - 1)), kThreads, smem, stream>>>(a);
     e = cudaGetLastError();
+    // each segment's starting state: one slot per second-pass CTA
+    if (e == cudaSuccess)
+      e = seg_prefix_launch(agg, problems, plan.G, (int64_t)p.D * plan.Mb, p.reverse, stream);
     if (e != cudaSuccess) return e;
     a.agg_only = 0;
     a.agg_in = agg;

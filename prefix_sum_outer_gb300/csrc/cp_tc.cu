@@ -66,6 +66,9 @@ cudaError_t launch_pair(const CUtensorMap& q, const CUtensorMap& k, const CUtens
     const unsigned g1 = (unsigned)(problems * (plan.G - 1));
     e = a.feature ? launch_one<DP, MB, true, false, true>(q, k, v, o, b, g1, st)
                   : launch_one<DP, MB, true>(q, k, v, o, b, g1, st);
+    // each segment's starting state: one slot per second-pass CTA
+    if (e == cudaSuccess)
+      e = seg_prefix_launch(agg, problems, plan.G, (int64_t)DP * MB, a.reverse != 0, st);
     if (e != cudaSuccess || agg_only) return e;
     a.agg_in = agg;
   } else if (agg_only) {

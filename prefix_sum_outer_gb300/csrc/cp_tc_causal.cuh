@@ -573,11 +573,11 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
         }
       }
     } else {
-      // initial state: the carried state plus the fixed-order sum of the
-      // preceding segments' aggregates
+      // initial state: the carried state plus the sum of the preceding
+      // segments' aggregates (slot seg of agg_in, prefixed between passes)
       if (has_init) {
-        const int lo = has_prefix ? (a.reverse ? seg + 1 : 0) : 0;
-        const int hi = has_prefix ? (a.reverse ? a.G : seg) : 0;
+        const int lo = has_prefix ? seg : 0;
+        const int hi = has_prefix ? seg + 1 : 0;
         const float* st = a.state_in != nullptr ? a.state_in + (int64_t)bh * a.Dr * a.Mc : nullptr;
 #pragma unroll
         for (int sb = 0; sb < L::kSBlocks; ++sb) {

@@ -333,9 +333,10 @@ __device__ __forceinline__ bool dkdv_body(const CUtensorMap& tm_q, const CUtenso
             const int m = c * 32 + x;
             acc[x] = (st != nullptr && row < a.D && m < a.M) ? st[row * a.M + m] : 0.f;
           }
-          for (int s2 = seg + 1; has_prefix && s2 < a.G; ++s2) {
+          // slot seg holds the sum of the later segments' aggregates
+          if (has_prefix) {
             const float4* src = reinterpret_cast<const float4*>(
-                a.agg_in + (((size_t)bh * a.G + s2) * kW + row) * kW + c * 32);
+                a.agg_in + (((size_t)bh * a.G + seg) * kW + row) * kW + c * 32);
 #pragma unroll
             for (int x = 0; x < 8; ++x) {
               const float4 f = __ldg(src + x);

@@ -82,6 +82,38 @@ def test_workspace_size(lib):
     assert ws(1, 1, 16, 16, 16, 5, 0) == 0
 
 
+def test_launch_count(lib):
+    """The plan's launch counts for the five workloads (152 SMs when no GPU
+    is present, as on the target part)."""
+    import torch
+    if torch.cuda.is_available():
+        n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+        if n_sm != 152:
+            pytest.skip("counts below are for a 152-SM device")
+    lc = lib.causal_product_launch_count
+    # B=8 H=16 N=4096 D=M=64: 128 unsplit problems, fwd 1 launch, the
+    # whole backward in 1
+    assert lc(8, 16, 4096, 64, 64, BF16, 0) == 1
+    assert lc(8, 16, 4096, 64, 64, BF16, 1) == 1
+    # 16 problems of 32768 rows: every scan split (sums, prefix, scan),
+    # three products in the backward
+    assert lc(2, 8, 32768, 128, 128, BF16, 0) == 3
+    assert lc(2, 8, 32768, 128, 128, BF16, 1) == 9
+    assert lc(4, 8, 8229, 256, 64, BF16, 0) == 3
+    assert lc(4, 8, 8229, 256, 64, BF16, 1) == 9
+    # fp32: 32 problems of 32 tiles split 16 ways; one 64-row tile unsplit
+    assert lc(4, 8, 1024, 64, 64, F32, 0) == 3
+    assert lc(4, 8, 1024, 64, 64, F32, 1) == 9
+    assert lc(1, 2, 64, 16, 16, F32, 0) == 1
+    assert lc(1, 2, 64, 16, 16, F32, 1) == 3
+    # bf16 D = M = 64 split: dq product (3), reverse sums + prefix, dk/dv scan
+    assert lc(1, 2, 8192, 64, 64, BF16, 1) == 6
+    # many problems: fused dk/dv scan on its own launch after dq
+    assert lc(16, 16, 1024, 64, 64, BF16, 1) == 2
+    assert lc(1, 1, 0, 64, 64, BF16, 1) == 0
+    assert lc(1, 1, 16, 12, 16, BF16, 0) == -1
+
+
 A = 1 << 20  # a 16-byte-aligned fake device address; never dereferenced here
 
 

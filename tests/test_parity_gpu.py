@@ -112,6 +112,31 @@ def test_shapes_fwd_bwd(shape, dtype):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("shape", [(1, 1, 300, 256, 256), (1, 2, 200, 64, 256),
+                                   (1, 1, 150, 256, 8)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_widest_shapes(shape, dtype):
+    """D = M = 256 is the widest the boundary takes: four 64-column value
+    blocks on the tensor-core path, 256-row states on the fp32 path."""
+    B, H, N, D, M = shape
+    q, k, v, g = make_inputs(B, H, N, D, M, DT[dtype], seed=N + D + M)
+    check_fwd(q, k, v, "bf16" if dtype == "bf16" else "f32")
+    check_bwd(q, k, v, g, "bf16" if dtype == "bf16" else "f32")
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 100, 1, 1), (2, 1, 333, 3, 5), (1, 1, 257, 33, 130)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_fp32_odd_widths(shape):
+    """fp32 takes any width from 1 to 256: widths that are not a multiple of
+    4 pad the shared-memory tiles with zeros, and M = 130 leaves a value block
+    two columns wide."""
+    B, H, N, D, M = shape
+    q, k, v, g = make_inputs(B, H, N, D, M, torch.float32, seed=N + 31 * D + M)
+    check_fwd(q, k, v, "f32")
+    check_bwd(q, k, v, g, "f32")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("N", [1000, 4096, 5000])
 def test_segmented_scan(N, dtype):
     """Few problems, long sequences: the sequence is split into segments and
