@@ -26,7 +26,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int DP, int MB, bool AGG, bool STATE_OUT = false, bool FEAT = false>
 cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                        const CUtensorMap& o, const Args& a, unsigned grid, cudaStream_t st) {
-  using L = Layout<DP, MB>;
+  using L = Layout<DP, MB, AGG>;
   auto kern = tc_causal_kernel<DP, MB, AGG, STATE_OUT, FEAT>;
   // the shared-memory opt-in is set once per device for each instantiation
   static std::atomic<uint64_t> configured{0};

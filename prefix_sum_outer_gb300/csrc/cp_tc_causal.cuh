@@ -105,13 +105,19 @@ __device__ __forceinline__ uint32_t elu1_bf16x2(uint32_t w) {
   return r;
 }
 
-template <int DP, int MB>
+// AGG: the aggregate-only pass.  It loads no Q and keeps neither state
+// copies nor output staging, so its Q/K stages hold K alone and the whole
+// budget goes to the rings (at DP = MB = 128: 3 K and 4 V stages instead of
+// one of each).
+template <int DP, int MB, bool AGG = false>
 struct Layout {
   static constexpr int kQBoxes = DP / kBoxCols;
   static constexpr int kVBoxes = MB / kBoxCols;
   static constexpr int kSBlocks = (DP + 127) / 128;
   static constexpr int kQBytes = kQBoxes * kBoxBytes;
   static constexpr int kQKBytes = 2 * kQBytes;               // one Q tile + one K tile
+  static constexpr int kQKStage = AGG ? kQBytes : kQKBytes;  // a Q/K ring stage
+  static constexpr int kKOff = AGG ? 0 : kQBytes;            // K within a stage
   static constexpr int kVBytes = kVBoxes * kBoxBytes;
   static constexpr int kSOneBytes = kVBoxes * DP * 128;      // DP x MB bf16
   static constexpr int kOBytes = kVBoxes * kBoxBytes;        // 128 x MB bf16
@@ -123,8 +129,8 @@ struct Layout {
   // gets one stage more when it fits.  Returns NQK * 8 + NV.
   static constexpr int rings(int budget) {
     for (int n = 4; n >= 1; --n) {
-      if (n * kQKBytes + (n + 1) * kVBytes <= budget) return n * 8 + n + 1;
-      if (n * kQKBytes + n * kVBytes <= budget) return n * 8 + n;
+      if (n * kQKStage + (n + 1) * kVBytes <= budget) return n * 8 + n + 1;
+      if (n * kQKStage + n * kVBytes <= budget) return n * 8 + n;
     }
     return 0;
   }
@@ -146,11 +152,13 @@ struct Layout {
   // output staging: two buffers (one store in flight) when they fit
   static constexpr int kOBufs =
       rings(kAvail - NSB * kSBufBytes - 2 * kOBytes) / 8 >= (NSB == 2 ? 2 : 1) ? 2 : 1;
-  static constexpr int kFixed = NSB * kSBufBytes + kOBufs * kOBytes;
+  static constexpr int kSRegion = AGG ? 0 : NSB * kSBufBytes;
+  static constexpr int kORegion = AGG ? 0 : kOBufs * kOBytes;
+  static constexpr int kFixed = kSRegion + kORegion;
   static constexpr int NQK = rings(kAvail - kFixed) / 8;
   static constexpr int NV = rings(kAvail - kFixed) % 8;
   static constexpr int kSmemBytes =
-      NQK * kQKBytes + NV * kVBytes + kFixed + kBarBytes + kAlignSlack;
+      NQK * kQKStage + NV * kVBytes + kFixed + kBarBytes + kAlignSlack;
   static constexpr int kColP = 0;                        // + b * 128
   static constexpr int kColO = NP * 128;                 // + o * MB
   static constexpr int kColS = kColO + NO * MB;          // + sb * MB
@@ -172,7 +180,7 @@ template <int DP, int MB, bool AGG_ONLY, bool STATE_OUT, bool FEAT = false>
 __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                             const CUtensorMap& tm_v, const CUtensorMap& tm_o,
                                             const Args& a, const Phase ph) {
-  using L = Layout<DP, MB>;
+  using L = Layout<DP, MB, AGG_ONLY>;
   constexpr int NQK = L::NQK;
   constexpr int NV = L::NV;
   constexpr int NP = L::NP;
@@ -181,11 +189,11 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* qk_ring = smem;                           // [NQK] x (Q tile | K tile)
-  uint8_t* v_ring = qk_ring + NQK * L::kQKBytes;     // [NV] x V tile
+  uint8_t* qk_ring = smem;                           // [NQK] x (Q tile | K tile), K alone (AGG)
+  uint8_t* v_ring = qk_ring + NQK * L::kQKStage;     // [NV] x V tile
   uint8_t* s_tile = v_ring + NV * L::kVBytes;        // [NSB] x (hi | lo) bf16 state copies
-  uint8_t* o_tile = s_tile + NSB * L::kSBufBytes;    // [kOBufs] output staging
-  uint64_t* bars = reinterpret_cast<uint64_t*>(o_tile + L::kOBufs * L::kOBytes);
+  uint8_t* o_tile = s_tile + L::kSRegion;            // [kOBufs] output staging
+  uint64_t* bars = reinterpret_cast<uint64_t*>(o_tile + L::kORegion);
   uint64_t* full_qk = bars;                 // [NQK] TMA -> MMA
   uint64_t* empty_qk = full_qk + NQK;       // [NQK] MMA -> TMA
   uint64_t* full_v = empty_qk + NQK;        // [NV]
@@ -295,8 +303,8 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
   // mtid on; the issuers wait on qk_ready for all of them
   auto map_qk = [&](int it, int mtid) -> bool {
     if (!mbar_wait(&full_qk[it % NQK], (it / NQK) & 1, abort_flag)) return false;
-    uint8_t* q_s = qk_ring + (it % NQK) * L::kQKBytes;
-    uint4* p = reinterpret_cast<uint4*>(AGG_ONLY ? q_s + L::kQBytes : q_s);
+    uint8_t* q_s = qk_ring + (it % NQK) * L::kQKStage;
+    uint4* p = reinterpret_cast<uint4*>(AGG_ONLY ? q_s + L::kKOff : q_s);
     constexpr int kChunks = (AGG_ONLY ? 1 : 2) * L::kQBytes / 16;
     constexpr int kTileChunks = L::kQBytes / 16, kBoxChunks = kBoxBytes / 16;
     auto map_chunk = [&](int i) {
@@ -343,8 +351,8 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
             (nq < NQK || mbar_test_wait(&empty_qk[nq % NQK], ((nq / NQK) - 1) & 1))) {
           const int st = nq % NQK;
           const int row0 = tile_of(nq) * kTile;
-          uint8_t* q_s = qk_ring + st * L::kQKBytes;
-          uint8_t* k_s = q_s + L::kQBytes;
+          uint8_t* q_s = qk_ring + st * L::kQKStage;
+          uint8_t* k_s = q_s + L::kKOff;
           mbar_arrive_expect_tx(&full_qk[st], kQKTx);
 #pragma unroll
           for (int b = 0; b < L::kQBoxes; ++b) {
@@ -401,13 +409,13 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
       const uint32_t t_s = tmem + L::kColS;
       auto t_out = [&](int it) { return tmem + L::kColO + (it % NO) * MB; };
       const uint32_t s_addr = smem_u32(s_tile);
-      auto qk_addr = [&](int it) { return smem_u32(qk_ring + (it % NQK) * L::kQKBytes); };
+      auto qk_addr = [&](int it) { return smem_u32(qk_ring + (it % NQK) * L::kQKStage); };
       auto v_addr = [&](int it) { return smem_u32(v_ring + (it % NV) * L::kVBytes); };
       // Descriptor low words advance by (byte offset >> 4) per K step.
       auto issue_s = [&](int it) {
         // S += K^T V (A = K^T and B = V, both MN-major), one 128-row block of
         // the state per 128 columns of K
-        const uint32_t kt_lo = desc_lo(qk_addr(it) + L::kQBytes, kBoxBytes);
+        const uint32_t kt_lo = desc_lo(qk_addr(it) + L::kKOff, kBoxBytes);
         const uint32_t v_lo = desc_lo(v_addr(it), kBoxBytes);
         const bool fresh = (it == 0) && !has_init;
 #pragma unroll
@@ -497,7 +505,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
           }
           tc_fence_after();
           const uint32_t q_lo = desc_lo(qk_addr(it), 16);
-          const uint32_t k_lo = desc_lo(qk_addr(it) + L::kQBytes, 16);
+          const uint32_t k_lo = desc_lo(qk_addr(it) + L::kKOff, 16);
           const uint32_t t_p = tmem + L::kColP + (it % NP) * 128;
 #pragma unroll
           for (int kk = 0; kk < DP / 16; ++kk) {
