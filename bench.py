@@ -43,13 +43,16 @@ UNIT = "Mtok·head/s"
 CAUSAL_SOURCES = ("cp_tc.cu", "cp_tc_causal.cuh", "cp_tc_common.cuh", "sm103_ptx.cuh")
 BWD_SOURCES = ("cp_tc_dkdv.cu", "cp_tc_dkdv.cuh", "cp_tc_causal.cuh", "cp_tc_common.cuh",
                "sm103_ptx.cuh")
+# Both figures are means over the 7 launches of each kernel in the launch
+# list of `bench.py --steps 1 --warmup 3 --no-e2e --no-cpu-baseline
+# --no-extras` taken with the two DRAM counters beside gpu__time_duration.
 PROFILED_TRAFFIC = {
-    "source_sha256": "02f99ab66a117d082bbb60d661bc0c797ba40fdc24dcab8efa975f6072c137d0",
-    "bytes_per_launch": 212234496,  # 201.40 MB read + 10.84 MB written (forward launch)
+    "source_sha256": "3d5d33e7c17edb559a1a30ac7ab4d7a58fd3f92ba8e1fc823574e9b95bebcad0",
+    "bytes_per_launch": 208765659,  # 201.40 MB read + 7.36 MB written (forward launch)
 }
 PROFILED_TRAFFIC_BWD = {
-    "source_sha256": "6c513e1788c825a297bae150ac46c4a727dc0d4ebaad7853ab477d928e6a4028",
-    "bytes_per_launch": 605719296,  # 463.78 MB read + 141.94 MB written (one backward launch)
+    "source_sha256": "63ea8432cd63a61ff28feca23246b9482aadb9b6451afaf09990251ccf8c3b9c",
+    "bytes_per_launch": 602030921,  # 463.22 MB read + 138.81 MB written (one backward launch)
 }
 
 
