@@ -99,6 +99,7 @@ __global__ void __launch_bounds__(kThreads, 4) simt_kernel(SimtArgs a) {
   float* Vs = Kt + Dp * C;           // [C][Mbp]
   float* Ps = Vs + C * Mbp;          // [C][C]    masked Q K^T
   float* Ss = Ps + C * C;            // [Dp][Mbp] state (padding stays zero)
+  float* Os = Ss + Dp * Mbp;         // [C][Mbp]  Q S of the tile (phase 1 -> phase 2)
 
   // block -> (segment, problem, value block); pass 1 skips the one segment
   // whose aggregate nobody reads.
@@ -218,31 +219,59 @@ __global__ void __launch_bounds__(kThreads, 4) simt_kernel(SimtArgs a) {
       }
     }
     __syncthreads();
+    // Two compute phases per tile.  Q S reads the state before this tile's
+    // update and does not need P, so it runs beside P; P V and the state
+    // update touch disjoint data, so they run side by side after it.
     if (!a.agg_only) {
-      // ---- P = Q K^T restricted to the causal triangle of the tile
-      for (int tt = threadIdx.x; tt < tc_p * tc_p; tt += kThreads) {
-        const int i0 = (tt / tc_p) * 4, j0 = (tt % tc_p) * 4;
+      // ---- phase 1: P = Q K^T on the causal triangle of the tile, and
+      // Q S into Os
+      const int nP = tc_p * tc_p, nO = tc_p * tc_o;
+      for (int tt = threadIdx.x; tt < nP + nO; tt += kThreads) {
         float acc[4][4] = {};
-        const bool none = a.reverse ? (j0 + 3 < i0) : (j0 > i0 + 3);
-        if (!none) mm4x4(acc, Qs, Dp, Kt, C, i0, j0, 0, Dp);
+        if (tt < nP) {
+          const int i0 = (tt / tc_p) * 4, j0 = (tt % tc_p) * 4;
+          const bool none = a.reverse ? (j0 + 3 < i0) : (j0 > i0 + 3);
+          if (!none) mm4x4(acc, Qs, Dp, Kt, C, i0, j0, 0, Dp);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float o[4];
+          for (int i = 0; i < 4; ++i) {
+            float o[4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const bool keep = a.reverse ? (j0 + j >= i0 + i) : (j0 + j <= i0 + i);
-            o[j] = keep ? acc[i][j] : 0.f;
+            for (int j = 0; j < 4; ++j) {
+              const bool keep = a.reverse ? (j0 + j >= i0 + i) : (j0 + j <= i0 + i);
+              o[j] = keep ? acc[i][j] : 0.f;
+            }
+            *reinterpret_cast<float4*>(Ps + (i0 + i) * C + j0) =
+                make_float4(o[0], o[1], o[2], o[3]);
           }
-          *reinterpret_cast<float4*>(Ps + (i0 + i) * C + j0) = make_float4(o[0], o[1], o[2], o[3]);
+        } else {
+          const int u = tt - nP;
+          const int i0 = (u / tc_o) * 4, c0 = (u % tc_o) * 4;
+          mm4x4(acc, Qs, Dp, Ss, Mbp, i0, c0, 0, Dp);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<float4*>(Os + (i0 + i) * Mbp + c0) =
+                make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
         }
       }
       __syncthreads();
-      // ---- O = Q S + P V (P is zero outside the triangle: only the
-      // columns j a row can see are visited)
-      for (int tt = threadIdx.x; tt < tc_p * tc_o; tt += kThreads) {
+    }
+    // ---- phase 2: O = Q S + P V and its store (P is zero outside the
+    // triangle: only the columns j a row can see are visited), and
+    // S += K^T V
+    const int nO2 = a.agg_only ? 0 : tc_p * tc_o;
+    const int nS = (Dp / 4) * tc_o;
+    for (int tt = threadIdx.x; tt < nO2 + nS; tt += kThreads) {
+      float acc[4][4];
+      if (tt < nO2) {
         const int i0 = (tt / tc_o) * 4, c0 = (tt % tc_o) * 4;
-        float acc[4][4] = {};
-        mm4x4(acc, Qs, Dp, Ss, Mbp, i0, c0, 0, Dp);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 t4 = *reinterpret_cast<const float4*>(Os + (i0 + i) * Mbp + c0);
+          acc[i][0] = t4.x;
+          acc[i][1] = t4.y;
+          acc[i][2] = t4.z;
+          acc[i][3] = t4.w;
+        }
         if (a.reverse)
           mm4x4(acc, Ps, C, Vs, Mbp, i0, c0, i0, C);
         else
@@ -255,26 +284,23 @@ __global__ void __launch_bounds__(kThreads, 4) simt_kernel(SimtArgs a) {
           for (int j = 0; j < 4; ++j)
             if (c0 + j < mw) ob[row * a.M + m0 + c0 + j] = narrow<T>(acc[i][j]);
         }
-      }
-      __syncthreads();
-    }
-    // ---- S += K^T V
-    for (int tt = threadIdx.x; tt < (Dp / 4) * tc_o; tt += kThreads) {
-      const int d0 = (tt / tc_o) * 4, c0 = (tt % tc_o) * 4;
-      float acc[4][4];
+      } else {
+        const int u = tt - nO2;
+        const int d0 = (u / tc_o) * 4, c0 = (u % tc_o) * 4;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float4 t4 = *reinterpret_cast<const float4*>(Ss + (d0 + i) * Mbp + c0);
-        acc[i][0] = t4.x;
-        acc[i][1] = t4.y;
-        acc[i][2] = t4.z;
-        acc[i][3] = t4.w;
-      }
-      mm4x4(acc, Kt, C, Vs, Mbp, d0, c0, 0, C);
+        for (int i = 0; i < 4; ++i) {
+          const float4 t4 = *reinterpret_cast<const float4*>(Ss + (d0 + i) * Mbp + c0);
+          acc[i][0] = t4.x;
+          acc[i][1] = t4.y;
+          acc[i][2] = t4.z;
+          acc[i][3] = t4.w;
+        }
+        mm4x4(acc, Kt, C, Vs, Mbp, d0, c0, 0, C);
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        *reinterpret_cast<float4*>(Ss + (d0 + i) * Mbp + c0) =
-            make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        for (int i = 0; i < 4; ++i)
+          *reinterpret_cast<float4*>(Ss + (d0 + i) * Mbp + c0) =
+              make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+      }
     }
   }
   __syncthreads();
@@ -301,7 +327,7 @@ int simt_rows(int64_t N, int64_t D) { return (N <= 64 && D <= 64) ? 64 : 32; }
 
 size_t simt_smem_bytes(int C_, int D, int Mb) {
   const size_t C = C_, Dp = (D + 3) / 4 * 4, Mbp = (Mb + 3) / 4 * 4;
-  return sizeof(float) * (2 * C * Dp + C * Mbp + C * C + Dp * Mbp);
+  return sizeof(float) * (2 * C * Dp + 2 * C * Mbp + C * C + Dp * Mbp);
 }
 
 }  // namespace
