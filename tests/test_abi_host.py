@@ -161,10 +161,28 @@ def test_bwd_argument_checks(lib):
 
 
 def test_python_binding_refuses_cpu_tensors():
+    """Every compute entry point of the binding refuses host tensors with an
+    error: there is no CPU path to fall back to."""
     import torch
     q = torch.ones(1, 1, 4, 16)
-    with pytest.raises(RuntimeError):
-        cp.causal_product_fwd(q, q, q)
+    z = torch.ones(1, 1, 4)
+    q1 = torch.ones(1, 1, 16)
+    st = torch.zeros(1, 1, 16, 16)
+    calls = [
+        lambda: cp.causal_product_fwd(q, q, q),
+        lambda: cp.causal_product_bwd(q, q, q, q),
+        lambda: cp.causal_product_fwd_noalloc(q, q, q, torch.empty_like(q)),
+        lambda: cp.causal_product_fwd_feature(q, q, q),
+        lambda: cp.causal_product_bwd_feature(q, q, q, q),
+        lambda: cp.causal_product_normalizer(q, q),
+        lambda: cp.causal_product_normalizer_bwd(q, q, z),
+        lambda: cp.causal_product_decode(q1, q1, q1, st),
+        lambda: cp.causal_product(q, q, q),
+        lambda: cp.normalizer(q, q),
+    ]
+    for call in calls:
+        with pytest.raises(RuntimeError, match="CUDA tensors only"):
+            call()
 
 
 def test_state_argument_checks(lib):
