@@ -72,6 +72,16 @@ def test_fp32_workloads(name):
     check_fwd(q, k, v, w.dtype)
 
 
+@pytest.mark.parametrize("name", ["tiny_f32_fwd", "mid_f32_fwd"])
+def test_fp32_workloads_backward(name):
+    """The fp32 workloads' backward, on the inputs the bench's fwd + bwd step
+    uses (the same draw with g)."""
+    w = WORKLOADS[name]
+    q, k, v, g = make_inputs(w.B, w.H, w.N, w.D, w.M, w.torch_dtype, w.seed,
+                             feature=w.feature, x_std=w.x_std, backward=True)
+    check_bwd(q, k, v, g, w.dtype)
+
+
 @pytest.mark.parametrize("name", ["bf16_b8h16_n4096_d64", "bf16_long_n32768_d128",
                                   "bf16_favor_n8229_d256_m64"])
 def test_bf16_workloads_full_size(name):
