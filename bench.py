@@ -210,13 +210,20 @@ def cpu_baseline(w, budget_s=10.0):
     q, k, v, g = make_inputs(1, n, w.N, w.D, w.M, w.torch_dtype, seed=w.seed, feature=w.feature,
                              x_std=w.x_std)
     qn, kn, vn, gn = f(q), f(k), f(v), f(g)
-    t0 = time.perf_counter()
-    oracle.fwd(qn, kn, vn)
-    oracle.bwd(qn, kn, vn, gn)
-    dt = time.perf_counter() - t0
-    return {"value": n * w.N / dt / 1e6, "unit": UNIT, "cores": cores, "kind": "oracle",
+    # when the whole workload is shorter than the budget, repeat it (at most
+    # 20 passes) so the figure rests on seconds of CPU work, not one short pass
+    reps, dt = 0, 0.0
+    while True:
+        t0 = time.perf_counter()
+        oracle.fwd(qn, kn, vn)
+        oracle.bwd(qn, kn, vn, gn)
+        dt += time.perf_counter() - t0
+        reps += 1
+        if dt >= 0.5 * budget_s or reps >= 20:
+            break
+    return {"value": reps * n * w.N / dt / 1e6, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{n} of {w.B * w.H} (b,h) slices x N={w.N}, fwd+bwd, fp64 C oracle, "
-                      f"{dt:.1f} s"}
+                      f"{reps} pass(es), {dt:.1f} s"}
 
 
 def run_reference(args, world, rank):
