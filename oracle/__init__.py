@@ -22,6 +22,9 @@ it with gcc and exposes it through ctypes:
     norm_feature(q, k, feature="elu1")     -> z of phi(q), phi(k)
     norm_bwd_feature(q, k, g, feature="elu1") -> (dq, dk) w.r.t. raw q, k
     bwd_feature(q, k, v, g, feature="elu1") -> (dq, dk, dv) w.r.t. raw q, k, v
+    fwd_favor(xq, xk, v, W)    -> out of phi(xq), phi(xk), v with positive
+                                  random features phi(x) = exp(W x - |x|^2/2)/sqrt(D)
+    bwd_favor(xq, xk, v, W, g) -> (dxq, dxk, dv) w.r.t. xq, xk, v (W fixed)
 
 States are [..., D, M] arrays; they may be float64 (the oracle's own
 states) as well as float32 or bfloat16 values, all exact in double.
@@ -96,6 +99,11 @@ def _load():
             lib.cpo_norm_feature.restype = c_int
             lib.cpo_norm_bwd_feature.argtypes = [p, p, p, p, p, c_int, i64, i64, i64, c_int]
             lib.cpo_norm_bwd_feature.restype = c_int
+            lib.cpo_fwd_favor.argtypes = [p, p, p, p, p, i64, i64, i64, i64, i64, c_int]
+            lib.cpo_fwd_favor.restype = c_int
+            lib.cpo_bwd_favor.argtypes = [p, p, p, p, p, p, p, p, i64, i64, i64, i64, i64,
+                                          c_int]
+            lib.cpo_bwd_favor.restype = c_int
             lib.cpo_threads.argtypes = [c_int]
             lib.cpo_threads.restype = c_int
             _lib = lib
@@ -298,3 +306,45 @@ def norm_bwd_feature(q, k, g, feature: str = "elu1", nthreads: int = 0):
     if rc != 0:
         raise RuntimeError(f"oracle norm_bwd_feature failed ({rc})")
     return dq, dk
+
+
+def _favor_dims(xq, xk, v, W):
+    if (xq.ndim < 2 or xq.shape != xk.shape or xq.shape[:-1] != v.shape[:-1] or W.ndim != 2
+            or W.shape[1] != xq.shape[-1]):
+        raise ValueError(f"shape mismatch: xq{xq.shape} xk{xk.shape} v{v.shape} W{W.shape}")
+    lead = xq.shape[:-2]
+    BH = int(np.prod(lead)) if lead else 1
+    return lead, BH, xq.shape[-2], xq.shape[-1], W.shape[0], v.shape[-1]
+
+
+def fwd_favor(xq, xk, v, W, nthreads: int = 0) -> np.ndarray:
+    """out_i = sum_{j<=i} (phi(xq_i) . phi(xk_j)) v_j with the positive random
+    features phi(x)_d = exp(w_d . x - |x|^2 / 2) / sqrt(D), evaluated in fp64.
+    xq, xk: [..., N, r]; W: [D, r] (one projection for every slice);
+    v: [..., N, M]."""
+    xq, xk, v, W = _as_f32(xq), _as_f32(xk), _as_f32(v), _as_f32(W)
+    lead, BH, N, r, D, M = _favor_dims(xq, xk, v, W)
+    out = np.zeros(lead + (N, M), dtype=np.float64)
+    rc = _load().cpo_fwd_favor(xq.ctypes.data, xk.ctypes.data, v.ctypes.data, W.ctypes.data,
+                               out.ctypes.data, BH, N, r, D, M, int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle fwd_favor failed ({rc})")
+    return out
+
+
+def bwd_favor(xq, xk, v, W, g, nthreads: int = 0):
+    """(dxq, dxk, dv) of L = <g, out> for fwd_favor, with respect to xq, xk
+    and v (W is fixed), in fp64."""
+    xq, xk, v, W, g = _as_f32(xq), _as_f32(xk), _as_f32(v), _as_f32(W), _as_f32(g)
+    lead, BH, N, r, D, M = _favor_dims(xq, xk, v, W)
+    if g.shape != v.shape:
+        raise ValueError(f"grad shape {g.shape} != out shape {v.shape}")
+    dxq = np.zeros(lead + (N, r), dtype=np.float64)
+    dxk = np.zeros(lead + (N, r), dtype=np.float64)
+    dv = np.zeros(lead + (N, M), dtype=np.float64)
+    rc = _load().cpo_bwd_favor(xq.ctypes.data, xk.ctypes.data, v.ctypes.data, W.ctypes.data,
+                               g.ctypes.data, dxq.ctypes.data, dxk.ctypes.data, dv.ctypes.data,
+                               BH, N, r, D, M, int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle bwd_favor failed ({rc})")
+    return dxq, dxk, dv

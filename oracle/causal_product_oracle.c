@@ -50,6 +50,16 @@
  *   map them in double, run the same recurrences, and apply the chain rule
  *   dL/dx = dL/dphi * phi'(x), phi'(x) = 1 for x > 0, e^x otherwise.
  *
+ *   Positive random features.  The issue names Performer-style models as
+ *   users of the kernel.  Their feature map (positive random features of
+ *   the softmax kernel) takes a raw row x in R^r and one projection W in
+ *   R^{D x r}, shared by every row and slice, and gives a D-vector:
+ *       phi(x)_d = exp(w_d . x - |x|^2 / 2) / sqrt(D).
+ *   The product of phi(xq), phi(xk) and v runs the same recurrences.  With
+ *   a = dL/dphi(x) for one row, the chain rule gives
+ *       dL/dx = sum_d a_d phi_d (w_d - x) = W^T (a * phi) - x (a . phi).
+ *   W is an input, not a trained parameter: no gradient is formed for it.
+ *
  * Inputs are float32 arrays holding the exact values the GPU receives
  * (bfloat16 values are exactly representable in float32 and in double);
  * each slice is widened to double before any arithmetic.  Outputs are
@@ -362,6 +372,90 @@ int cpo_bwd_feature(const float *q, const float *k, const float *v, const float 
             dqs[e] *= dphi(feature, (double)qs[e]);
             dks[e] *= dphi(feature, (double)ks[e]);
         }
+        free(buf);
+    }
+    return err ? -2 : 0;
+}
+
+/* phi of every row of one [N][r] slice into [N][D] (positive random
+ * features, W row-major [D][r]). */
+static void favor_slice(const float *x, const float *W, int64_t N, int64_t r, int64_t D,
+                        double *phi) {
+    const double scale = 1.0 / sqrt((double)D);
+    for (int64_t i = 0; i < N; ++i) {
+        const float *xi = x + i * r;
+        double n2 = 0.0;
+        for (int64_t t = 0; t < r; ++t) n2 += (double)xi[t] * (double)xi[t];
+        for (int64_t d = 0; d < D; ++d) {
+            double wx = 0.0;
+            for (int64_t t = 0; t < r; ++t) wx += (double)W[d * r + t] * (double)xi[t];
+            phi[i * D + d] = exp(wx - 0.5 * n2) * scale;
+        }
+    }
+}
+
+/* dL/dx of one slice from a = dL/dphi: W^T (a * phi) - x (a . phi) per row. */
+static void favor_grad(const float *x, const float *W, const double *phi, const double *a,
+                       int64_t N, int64_t r, int64_t D, double *dx) {
+    for (int64_t i = 0; i < N; ++i) {
+        const double *pi = phi + i * D, *ai = a + i * D;
+        double s = 0.0;
+        for (int64_t d = 0; d < D; ++d) s += ai[d] * pi[d];
+        for (int64_t t = 0; t < r; ++t) {
+            double acc = 0.0;
+            for (int64_t d = 0; d < D; ++d) acc += (double)W[d * r + t] * (ai[d] * pi[d]);
+            dx[i * r + t] = acc - (double)x[i * r + t] * s;
+        }
+    }
+}
+
+/* Forward of the causal product of phi(xq), phi(xk) and v with positive
+ * random features: xq, xk [BH][N][r], W [D][r], v [BH][N][M] -> out
+ * [BH][N][M]. */
+int cpo_fwd_favor(const float *xq, const float *xk, const float *v, const float *W, double *out,
+                  int64_t BH, int64_t N, int64_t r, int64_t D, int64_t M, int nthreads) {
+    if (BH < 0 || N < 0 || r <= 0 || D <= 0 || M <= 0) return -1;
+    if (BH == 0 || N == 0) return 0;
+    set_threads(nthreads);
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+    for (int64_t bh = 0; bh < BH; ++bh) {
+        double *buf = (double *)malloc(sizeof(double) * (size_t)(N * (2 * D + M) + D * M));
+        if (!buf) { err |= 1; continue; }
+        double *qd = buf, *kd = qd + N * D, *vd = kd + N * D, *S = vd + N * M;
+        favor_slice(xq + bh * N * r, W, N, r, D, qd);
+        favor_slice(xk + bh * N * r, W, N, r, D, kd);
+        widen(v + bh * N * M, vd, N * M);
+        fwd_slice(qd, kd, vd, out + bh * N * M, S, NULL, NULL, N, D, M);
+        free(buf);
+    }
+    return err ? -2 : 0;
+}
+
+/* Backward of cpo_fwd_favor with respect to xq, xk and v (W fixed):
+ * dxq, dxk [BH][N][r], dv [BH][N][M]. */
+int cpo_bwd_favor(const float *xq, const float *xk, const float *v, const float *W,
+                  const float *g, double *dxq, double *dxk, double *dv, int64_t BH, int64_t N,
+                  int64_t r, int64_t D, int64_t M, int nthreads) {
+    if (BH < 0 || N < 0 || r <= 0 || D <= 0 || M <= 0) return -1;
+    if (BH == 0 || N == 0) return 0;
+    set_threads(nthreads);
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+    for (int64_t bh = 0; bh < BH; ++bh) {
+        double *buf = (double *)malloc(sizeof(double) * (size_t)(N * (4 * D + 2 * M) + D * M));
+        if (!buf) { err |= 1; continue; }
+        double *qd = buf, *kd = qd + N * D, *aq = kd + N * D, *ak = aq + N * D;
+        double *vd = ak + N * D, *gd = vd + N * M, *S = gd + N * M;
+        const float *xqs = xq + bh * N * r, *xks = xk + bh * N * r;
+        favor_slice(xqs, W, N, r, D, qd);
+        favor_slice(xks, W, N, r, D, kd);
+        widen(v + bh * N * M, vd, N * M);
+        widen(g + bh * N * M, gd, N * M);
+        /* dL/dphi(q), dL/dphi(k) and dv from the plain recurrences */
+        bwd_slice(qd, kd, vd, gd, aq, ak, dv + bh * N * M, S, NULL, NULL, NULL, N, D, M);
+        favor_grad(xqs, W, qd, aq, N, r, D, dxq + bh * N * r);
+        favor_grad(xks, W, kd, ak, N, r, D, dxk + bh * N * r);
         free(buf);
     }
     return err ? -2 : 0;

@@ -3,8 +3,9 @@
 Each pin checks an implementation ``impl`` (an object with ``fwd(q,k,v)``,
 ``bwd(q,k,v,g)``, ``fwd_state(q,k,v,s0)``, ``bwd_state(q,k,v,g,s0,ds_n)``,
 ``norm(q,k)``, ``norm_bwd(q,k,g)``, ``fwd_feature(q,k,v)``,
-``bwd_feature(q,k,v,g)``, ``norm_feature(q,k)`` and ``norm_bwd_feature(q,k,g)``
-returning float64 numpy arrays, like ``oracle``)
+``bwd_feature(q,k,v,g)``, ``norm_feature(q,k)``, ``norm_bwd_feature(q,k,g)``,
+``fwd_favor(xq,xk,v,W)`` and ``bwd_favor(xq,xk,v,W,g)`` returning float64
+numpy arrays, like ``oracle``)
 against something other than the recurrence itself: hand-worked values,
 a brute-force quadratic form, closed forms, textbook special cases,
 linearity, causality and finite differences.  ``tests/test_oracle.py``
@@ -544,4 +545,85 @@ def pin_norm_feature(impl):
 
 FEATURE_PINS = [pin_feature_positive_is_shift, pin_feature_quadratic_form,
                 pin_feature_finite_differences, pin_norm_feature]
-ALL_PINS = FWD_PINS + BWD_PINS + STATE_PINS + NORM_PINS + FEATURE_PINS
+
+
+# --------------------------------------------------------------------------
+# positive random features: phi(x)_d = exp(w_d . x - |x|^2 / 2) / sqrt(D)
+# --------------------------------------------------------------------------
+
+def pin_favor_zero_projection(impl):
+    """W = 0 makes every feature exp(-|x|^2 / 2) / sqrt(D), so
+    phi(x) . phi(y) = exp(-(|x|^2 + |y|^2) / 2) whatever D is: with
+    a_i = exp(-|xq_i|^2 / 2) and b_j = exp(-|xk_j|^2 / 2) the product is the
+    scaled cumulative sum out_i = a_i sum_{j<=i} b_j v_j.  Its gradients in
+    closed form: dxq_i = -xq_i a_i (g_i . c_i) with c_i = sum_{j<=i} b_j v_j;
+    with e_j = sum_{i>=j} a_i g_i, dv_j = b_j e_j and dxk_j = -xk_j b_j (v_j . e_j)."""
+    rng = _rng(51)
+    lead, N, r, D, M = (2, 1), 11, 3, 6, 4
+    xq = (rng.standard_normal(lead + (N, r)) * 0.7).astype(np.float32)
+    xk = (rng.standard_normal(lead + (N, r)) * 0.7).astype(np.float32)
+    v = rng.standard_normal(lead + (N, M)).astype(np.float32)
+    g = rng.standard_normal(lead + (N, M)).astype(np.float32)
+    W = np.zeros((D, r), np.float32)
+    qd, kd, vd, gd = (x.astype(np.float64) for x in (xq, xk, v, g))
+    a = np.exp(-0.5 * np.sum(qd * qd, axis=-1))
+    b = np.exp(-0.5 * np.sum(kd * kd, axis=-1))
+    c = np.cumsum(b[..., None] * vd, axis=-2)
+    assert _rel(impl.fwd_favor(xq, xk, v, W), a[..., None] * c) < 1e-12, "favor W=0 fwd"
+    e = np.flip(np.cumsum(np.flip(a[..., None] * gd, axis=-2), axis=-2), axis=-2)
+    dxq = -qd * (a * np.sum(gd * c, axis=-1))[..., None]
+    dxk = -kd * (b * np.sum(vd * e, axis=-1))[..., None]
+    dv = b[..., None] * e
+    got = impl.bwd_favor(xq, xk, v, W, g)
+    for x, y, name in zip(got, (dxq, dxk, dv), ("dxq", "dxk", "dv")):
+        assert _rel(x, y) < 1e-12, ("favor W=0 bwd", name)
+
+
+def pin_favor_unbiased(impl):
+    """Positive random features estimate the softmax kernel without bias:
+    for w ~ N(0, I), E[exp(w.x - |x|^2/2) exp(w.y - |y|^2/2)] = exp(x . y).
+    With D = 2^15 Gaussian rows of W and v = 1, out_i = sum_{j<=i}
+    phi(xq_i) . phi(xk_j) must come within a few standard errors (about 1 %
+    here) of sum_{j<=i} exp(xq_i . xk_j)."""
+    rng = _rng(52)
+    N, r, D = 4, 4, 1 << 15
+    xq = (rng.standard_normal((1, 1, N, r)) * 0.25).astype(np.float32)
+    xk = (rng.standard_normal((1, 1, N, r)) * 0.25).astype(np.float32)
+    W = rng.standard_normal((D, r)).astype(np.float32)
+    v = np.ones((1, 1, N, 1), np.float32)
+    got = impl.fwd_favor(xq, xk, v, W)[0, 0, :, 0]
+    K = np.exp(xq[0, 0].astype(np.float64) @ xk[0, 0].astype(np.float64).T)
+    want = np.array([np.sum(K[i, :i + 1]) for i in range(N)])
+    assert np.all(np.abs(got / want - 1.0) < 0.05), ("favor unbiased", got, want)
+
+
+def pin_favor_finite_differences(impl, shape=(1, 1, 5, 3)):
+    """Central differences of L = <g, out> with respect to xq and xk (step
+    2^-12, exact in float32 for these dyadic inputs) agree with the backward
+    to the O(h^2) truncation error."""
+    rng = _rng(53)
+    D, M = 4, 2
+    xq = _dyadic(rng, shape, -2, 2, 16) / np.float32(2)
+    xk = _dyadic(rng, shape, -2, 2, 16) / np.float32(2)
+    W = _dyadic(rng, (D, shape[-1]), -2, 2, 8)
+    v = _dyadic(rng, shape[:-1] + (M,), -2, 2, 16)
+    g = _dyadic(rng, shape[:-1] + (M,), -2, 2, 16)
+    gd = g.astype(np.float64)
+    dxq, dxk, _ = impl.bwd_favor(xq, xk, v, W, g)
+    h = np.float32(2.0 ** -12)
+    for name, x, grad in (("xq", xq, dxq), ("xk", xk, dxk)):
+        fd = np.zeros(x.shape)
+        for idx in np.ndindex(*x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args_p = (xp, xk) if name == "xq" else (xq, xp)
+            args_m = (xm, xk) if name == "xq" else (xq, xm)
+            lp = np.sum(gd * impl.fwd_favor(*args_p, v, W))
+            lm = np.sum(gd * impl.fwd_favor(*args_m, v, W))
+            fd[idx] = (lp - lm) / (2.0 * float(h))
+        assert np.allclose(grad, fd, rtol=1e-5, atol=1e-6), ("favor finite differences", name)
+
+
+FAVOR_PINS = [pin_favor_zero_projection, pin_favor_unbiased, pin_favor_finite_differences]
+ALL_PINS = FWD_PINS + BWD_PINS + STATE_PINS + NORM_PINS + FEATURE_PINS + FAVOR_PINS

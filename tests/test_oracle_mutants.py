@@ -94,6 +94,20 @@ MUTANTS = {
     # the normaliser of mapped features reading phi(k) for the readout
     "norm_feature_reads_k": [("acc += phi(feature, (double)qs[i * D + d]) * c[d];",
                               "acc += phi(feature, (double)ks[i * D + d]) * c[d];")],
+    # positive random features with the norm term's sign flipped
+    "favor_norm_sign": [("phi[i * D + d] = exp(wx - 0.5 * n2) * scale;",
+                         "phi[i * D + d] = exp(wx + 0.5 * n2) * scale;")],
+    # positive random features without the 1/sqrt(D) normalisation
+    "favor_no_scale": [("const double scale = 1.0 / sqrt((double)D);", "const double scale = 1.0;")],
+    # the projection read transposed (still in bounds: t < r, d < D)
+    "favor_w_transposed": [("wx += (double)W[d * r + t] * (double)xi[t];",
+                            "wx += (double)W[t * D + d] * (double)xi[t];")],
+    # the chain rule without the -x (a . phi) term of the norm
+    "favor_grad_drops_norm_term": [("dx[i * r + t] = acc - (double)x[i * r + t] * s;",
+                                    "dx[i * r + t] = acc;")],
+    # the chain rule without the phi factor on the projection term
+    "favor_grad_unweighted": [("acc += (double)W[d * r + t] * (ai[d] * pi[d]);",
+                               "acc += (double)W[d * r + t] * ai[d];")],
 }
 
 
@@ -111,7 +125,30 @@ class _Impl:
         lib.cpo_norm_bwd_feature.argtypes = [p, p, p, p, p, c_int, i64, i64, i64, c_int]
         lib.cpo_bwd_feature.argtypes = [p, p, p, p, p, p, p, c_int, i64, i64, i64, i64, c_int]
         lib.cpo_norm_bwd.argtypes = [p, p, p, p, p, i64, i64, i64, c_int]
+        lib.cpo_fwd_favor.argtypes = [p, p, p, p, p, i64, i64, i64, i64, i64, c_int]
+        lib.cpo_bwd_favor.argtypes = [p, p, p, p, p, p, p, p, i64, i64, i64, i64, i64, c_int]
         self.lib = lib
+
+    def fwd_favor(self, xq, xk, v, W):
+        xq, xk, v, W = (np.ascontiguousarray(x, np.float32) for x in (xq, xk, v, W))
+        lead = xq.shape[:-2]
+        BH = int(np.prod(lead)) if lead else 1
+        N, r, D, M = xq.shape[-2], xq.shape[-1], W.shape[0], v.shape[-1]
+        out = np.zeros(lead + (N, M))
+        assert self.lib.cpo_fwd_favor(xq.ctypes.data, xk.ctypes.data, v.ctypes.data,
+                                      W.ctypes.data, out.ctypes.data, BH, N, r, D, M, 1) == 0
+        return out
+
+    def bwd_favor(self, xq, xk, v, W, g):
+        xq, xk, v, W, g = (np.ascontiguousarray(x, np.float32) for x in (xq, xk, v, W, g))
+        lead = xq.shape[:-2]
+        BH = int(np.prod(lead)) if lead else 1
+        N, r, D, M = xq.shape[-2], xq.shape[-1], W.shape[0], v.shape[-1]
+        dxq, dxk, dv = np.zeros(lead + (N, r)), np.zeros(lead + (N, r)), np.zeros(lead + (N, M))
+        assert self.lib.cpo_bwd_favor(xq.ctypes.data, xk.ctypes.data, v.ctypes.data,
+                                      W.ctypes.data, g.ctypes.data, dxq.ctypes.data,
+                                      dxk.ctypes.data, dv.ctypes.data, BH, N, r, D, M, 1) == 0
+        return dxq, dxk, dv
 
     def fwd_feature(self, q, k, v):
         q, k, v = (np.ascontiguousarray(x, np.float32) for x in (q, k, v))
