@@ -68,6 +68,26 @@ def _elu_plus_one(x: torch.Tensor) -> torch.Tensor:
     return torch.where(x > 0, x + 1.0, torch.exp(x))
 
 
+def _favor_draw(gen: torch.Generator, B: int, H: int, N: int, D: int):
+    """The random part of the "favor" inputs, in draw order: W [D, r], then
+    x_q and x_k [B, H, N, r] (float32)."""
+    r = FAVOR_INPUT_FEATURES
+    f32 = torch.float32
+    W = torch.randn((D, r), generator=gen, dtype=f32)
+    scale = 1.0 / (r ** 0.25)
+    xq = torch.randn((B, H, N, r), generator=gen, dtype=f32) * scale
+    xk = torch.randn((B, H, N, r), generator=gen, dtype=f32) * scale
+    return W, xq, xk
+
+
+def favor_raw_inputs(B: int, H: int, N: int, D: int, seed: int):
+    """(W, x_q, x_k) behind make_inputs(..., feature="favor") with the same
+    seed: the projection and the raw rows before the feature map."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(int(seed))
+    return _favor_draw(gen, B, H, N, D)
+
+
 def make_inputs(B: int, H: int, N: int, D: int, M: int, dtype: torch.dtype, seed: int,
                 feature: str = "elu", x_std: float = 1.0, backward: bool = True,
                 v_std: float = 1.0):
@@ -81,11 +101,7 @@ def make_inputs(B: int, H: int, N: int, D: int, M: int, dtype: torch.dtype, seed
         q = _elu_plus_one(xq)
         k = _elu_plus_one(xk)
     elif feature == "favor":
-        r = FAVOR_INPUT_FEATURES
-        W = torch.randn((D, r), generator=gen, dtype=f32)
-        scale = 1.0 / (r ** 0.25)
-        xq = torch.randn((B, H, N, r), generator=gen, dtype=f32) * scale
-        xk = torch.randn((B, H, N, r), generator=gen, dtype=f32) * scale
+        W, xq, xk = _favor_draw(gen, B, H, N, D)
         q = torch.exp(xq @ W.t() - 0.5 * (xq * xq).sum(-1, keepdim=True)) / math.sqrt(D)
         k = torch.exp(xk @ W.t() - 0.5 * (xk * xk).sum(-1, keepdim=True)) / math.sqrt(D)
     elif feature == "normal":
