@@ -25,6 +25,8 @@ it with gcc and exposes it through ctypes:
     fwd_favor(xq, xk, v, W)    -> out of phi(xq), phi(xk), v with positive
                                   random features phi(x) = exp(W x - |x|^2/2)/sqrt(D)
     bwd_favor(xq, xk, v, W, g) -> (dxq, dxk, dv) w.r.t. xq, xk, v (W fixed)
+    norm_favor(xq, xk, W)      -> z of phi(xq), phi(xk)
+    norm_bwd_favor(xq, xk, W, g) -> (dxq, dxk) w.r.t. xq, xk (g = dL/dz)
 
 States are [..., D, M] arrays; they may be float64 (the oracle's own
 states) as well as float32 or bfloat16 values, all exact in double.
@@ -104,6 +106,10 @@ def _load():
             lib.cpo_bwd_favor.argtypes = [p, p, p, p, p, p, p, p, i64, i64, i64, i64, i64,
                                           c_int]
             lib.cpo_bwd_favor.restype = c_int
+            lib.cpo_norm_favor.argtypes = [p, p, p, p, i64, i64, i64, i64, c_int]
+            lib.cpo_norm_favor.restype = c_int
+            lib.cpo_norm_bwd_favor.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, c_int]
+            lib.cpo_norm_bwd_favor.restype = c_int
             lib.cpo_threads.argtypes = [c_int]
             lib.cpo_threads.restype = c_int
             _lib = lib
@@ -348,3 +354,39 @@ def bwd_favor(xq, xk, v, W, g, nthreads: int = 0):
     if rc != 0:
         raise RuntimeError(f"oracle bwd_favor failed ({rc})")
     return dxq, dxk, dv
+
+
+def _favor_qk_dims(xq, xk, W):
+    if xq.ndim < 2 or xq.shape != xk.shape or W.ndim != 2 or W.shape[1] != xq.shape[-1]:
+        raise ValueError(f"shape mismatch: xq{xq.shape} xk{xk.shape} W{W.shape}")
+    lead = xq.shape[:-2]
+    BH = int(np.prod(lead)) if lead else 1
+    return lead, BH, xq.shape[-2], xq.shape[-1], W.shape[0]
+
+
+def norm_favor(xq, xk, W, nthreads: int = 0) -> np.ndarray:
+    """z_i = phi(xq_i) . sum_{j<=i} phi(xk_j) with the positive random
+    features of fwd_favor, in fp64."""
+    xq, xk, W = _as_f32(xq), _as_f32(xk), _as_f32(W)
+    lead, BH, N, r, D = _favor_qk_dims(xq, xk, W)
+    z = np.zeros(lead + (N,), dtype=np.float64)
+    rc = _load().cpo_norm_favor(xq.ctypes.data, xk.ctypes.data, W.ctypes.data, z.ctypes.data,
+                                BH, N, r, D, int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle norm_favor failed ({rc})")
+    return z
+
+
+def norm_bwd_favor(xq, xk, W, g, nthreads: int = 0):
+    """(dxq, dxk) of L = sum_i g_i z_i for norm_favor (W fixed), in fp64."""
+    xq, xk, W, g = _as_f32(xq), _as_f32(xk), _as_f32(W), _as_f32(g)
+    lead, BH, N, r, D = _favor_qk_dims(xq, xk, W)
+    if g.shape != lead + (N,):
+        raise ValueError(f"grad shape {g.shape} != z shape {lead + (N,)}")
+    dxq = np.zeros(lead + (N, r), dtype=np.float64)
+    dxk = np.zeros(lead + (N, r), dtype=np.float64)
+    rc = _load().cpo_norm_bwd_favor(xq.ctypes.data, xk.ctypes.data, W.ctypes.data, g.ctypes.data,
+                                    dxq.ctypes.data, dxk.ctypes.data, BH, N, r, D, int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle norm_bwd_favor failed ({rc})")
+    return dxq, dxk

@@ -461,6 +461,70 @@ int cpo_bwd_favor(const float *xq, const float *xk, const float *v, const float 
     return err ? -2 : 0;
 }
 
+/* Normaliser of positive random features: z_i = phi(xq_i) . sum_{j<=i}
+ * phi(xk_j), xq, xk [BH][N][r], W [D][r] -> z [BH][N]. */
+int cpo_norm_favor(const float *xq, const float *xk, const float *W, double *z, int64_t BH,
+                   int64_t N, int64_t r, int64_t D, int nthreads) {
+    if (BH < 0 || N < 0 || r <= 0 || D <= 0) return -1;
+    if (BH == 0 || N == 0) return 0;
+    set_threads(nthreads);
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+    for (int64_t bh = 0; bh < BH; ++bh) {
+        double *buf = (double *)malloc(sizeof(double) * (size_t)(2 * N * D + D));
+        if (!buf) { err |= 1; continue; }
+        double *pq = buf, *pk = pq + N * D, *c = pk + N * D;
+        favor_slice(xq + bh * N * r, W, N, r, D, pq);
+        favor_slice(xk + bh * N * r, W, N, r, D, pk);
+        memset(c, 0, sizeof(double) * (size_t)D);
+        for (int64_t i = 0; i < N; ++i) {
+            /* c += phi(k_i), then z_i = phi(q_i) . c */
+            for (int64_t d = 0; d < D; ++d) c[d] += pk[i * D + d];
+            double acc = 0.0;
+            for (int64_t d = 0; d < D; ++d) acc += pq[i * D + d] * c[d];
+            z[bh * N + i] = acc;
+        }
+        free(buf);
+    }
+    return err ? -2 : 0;
+}
+
+/* Backward of cpo_norm_favor with respect to xq and xk (W fixed), from
+ * g = dL/dz [BH][N]: dL/dphi(q_i) = g_i c_i, dL/dphi(k_j) = sum_{i>=j}
+ * g_i phi(q_i), then the chain rule through phi. */
+int cpo_norm_bwd_favor(const float *xq, const float *xk, const float *W, const float *g,
+                       double *dxq, double *dxk, int64_t BH, int64_t N, int64_t r, int64_t D,
+                       int nthreads) {
+    if (BH < 0 || N < 0 || r <= 0 || D <= 0) return -1;
+    if (BH == 0 || N == 0) return 0;
+    set_threads(nthreads);
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+    for (int64_t bh = 0; bh < BH; ++bh) {
+        double *buf = (double *)malloc(sizeof(double) * (size_t)(4 * N * D + D));
+        if (!buf) { err |= 1; continue; }
+        double *pq = buf, *pk = pq + N * D, *aq = pk + N * D, *ak = aq + N * D;
+        double *c = ak + N * D;
+        const float *xqs = xq + bh * N * r, *xks = xk + bh * N * r, *gs = g + bh * N;
+        favor_slice(xqs, W, N, r, D, pq);
+        favor_slice(xks, W, N, r, D, pk);
+        memset(c, 0, sizeof(double) * (size_t)D);
+        for (int64_t i = 0; i < N; ++i) {
+            for (int64_t d = 0; d < D; ++d) c[d] += pk[i * D + d];
+            for (int64_t d = 0; d < D; ++d) aq[i * D + d] = (double)gs[i] * c[d];
+        }
+        memset(c, 0, sizeof(double) * (size_t)D);
+        for (int64_t j = N - 1; j >= 0; j -= 1) {
+            for (int64_t d = 0; d < D; ++d) c[d] += (double)gs[j] * pq[j * D + d];
+            for (int64_t d = 0; d < D; ++d) ak[j * D + d] = c[d];
+        }
+        favor_grad(xqs, W, pq, aq, N, r, D, dxq + bh * N * r);
+        favor_grad(xks, W, pk, ak, N, r, D, dxk + bh * N * r);
+        free(buf);
+    }
+    return err ? -2 : 0;
+}
+
 /* Normaliser of mapped features: z_i = phi(q_i) . sum_{j<=i} phi(k_j) from
  * the raw q, k (feature 0: as given, 1: elu + 1). */
 int cpo_norm_feature(const float *q, const float *k, double *z, int feature, int64_t BH,

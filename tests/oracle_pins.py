@@ -4,8 +4,9 @@ Each pin checks an implementation ``impl`` (an object with ``fwd(q,k,v)``,
 ``bwd(q,k,v,g)``, ``fwd_state(q,k,v,s0)``, ``bwd_state(q,k,v,g,s0,ds_n)``,
 ``norm(q,k)``, ``norm_bwd(q,k,g)``, ``fwd_feature(q,k,v)``,
 ``bwd_feature(q,k,v,g)``, ``norm_feature(q,k)``, ``norm_bwd_feature(q,k,g)``,
-``fwd_favor(xq,xk,v,W)`` and ``bwd_favor(xq,xk,v,W,g)`` returning float64
-numpy arrays, like ``oracle``)
+``fwd_favor(xq,xk,v,W)``, ``bwd_favor(xq,xk,v,W,g)``, ``norm_favor(xq,xk,W)``
+and ``norm_bwd_favor(xq,xk,W,g)`` returning float64 numpy arrays, like
+``oracle``)
 against something other than the recurrence itself: hand-worked values,
 a brute-force quadratic form, closed forms, textbook special cases,
 linearity, causality and finite differences.  ``tests/test_oracle.py``
@@ -625,5 +626,37 @@ def pin_favor_finite_differences(impl, shape=(1, 1, 5, 3)):
         assert np.allclose(grad, fd, rtol=1e-5, atol=1e-6), ("favor finite differences", name)
 
 
-FAVOR_PINS = [pin_favor_zero_projection, pin_favor_unbiased, pin_favor_finite_differences]
+def pin_norm_favor(impl):
+    """The normaliser of positive random features.  With W = 0 (features
+    exp(-|x|^2 / 2) / sqrt(D)) it is a scaled cumulative sum, z_i = a_i
+    sum_{j<=i} b_j, with gradients dxq_i = -xq_i a_i g_i sum_{j<=i} b_j and
+    dxk_j = -xk_j b_j sum_{i>=j} g_i a_i.  For a random W it is the product
+    with v = 1, forward and backward (the product is pinned above)."""
+    rng = _rng(54)
+    lead, N, r, D = (1, 2), 13, 3, 5
+    xq = (rng.standard_normal(lead + (N, r)) * 0.7).astype(np.float32)
+    xk = (rng.standard_normal(lead + (N, r)) * 0.7).astype(np.float32)
+    g = rng.standard_normal(lead + (N,)).astype(np.float32)
+    qd, kd, gd = (x.astype(np.float64) for x in (xq, xk, g))
+    W0 = np.zeros((D, r), np.float32)
+    a = np.exp(-0.5 * np.sum(qd * qd, axis=-1))
+    b = np.exp(-0.5 * np.sum(kd * kd, axis=-1))
+    cb = np.cumsum(b, axis=-1)
+    ea = np.flip(np.cumsum(np.flip(a * gd, axis=-1), axis=-1), axis=-1)
+    assert _rel(impl.norm_favor(xq, xk, W0), a * cb) < 1e-12, "norm favor W=0"
+    dxq, dxk = impl.norm_bwd_favor(xq, xk, W0, g)
+    assert _rel(dxq, -qd * (a * gd * cb)[..., None]) < 1e-12, "norm favor W=0 dxq"
+    assert _rel(dxk, -kd * (b * ea)[..., None]) < 1e-12, "norm favor W=0 dxk"
+    W = rng.standard_normal((D, r)).astype(np.float32)
+    ones = np.ones(lead + (N, 1), np.float32)
+    assert _rel(impl.norm_favor(xq, xk, W), impl.fwd_favor(xq, xk, ones, W)[..., 0]) < 1e-12, \
+        "norm favor = product with v = 1"
+    got = impl.norm_bwd_favor(xq, xk, W, g)
+    ref = impl.bwd_favor(xq, xk, ones, W, g[..., None])
+    assert _rel(got[0], ref[0]) < 1e-12 and _rel(got[1], ref[1]) < 1e-12, \
+        "norm favor bwd = product bwd with v = 1"
+
+
+FAVOR_PINS = [pin_favor_zero_projection, pin_favor_unbiased, pin_favor_finite_differences,
+              pin_norm_favor]
 ALL_PINS = FWD_PINS + BWD_PINS + STATE_PINS + NORM_PINS + FEATURE_PINS + FAVOR_PINS

@@ -108,6 +108,10 @@ MUTANTS = {
     # the chain rule without the phi factor on the projection term
     "favor_grad_unweighted": [("acc += (double)W[d * r + t] * (ai[d] * pi[d]);",
                                "acc += (double)W[d * r + t] * ai[d];")],
+    # the normaliser of positive random features reading phi(k) for the readout
+    "norm_favor_reads_k": [("acc += pq[i * D + d] * c[d];", "acc += pk[i * D + d] * c[d];")],
+    # its backward without the gradient factor on dq
+    "norm_bwd_favor_drops_g": [("aq[i * D + d] = (double)gs[i] * c[d];", "aq[i * D + d] = c[d];")],
 }
 
 
@@ -127,7 +131,30 @@ class _Impl:
         lib.cpo_norm_bwd.argtypes = [p, p, p, p, p, i64, i64, i64, c_int]
         lib.cpo_fwd_favor.argtypes = [p, p, p, p, p, i64, i64, i64, i64, i64, c_int]
         lib.cpo_bwd_favor.argtypes = [p, p, p, p, p, p, p, p, i64, i64, i64, i64, i64, c_int]
+        lib.cpo_norm_favor.argtypes = [p, p, p, p, i64, i64, i64, i64, c_int]
+        lib.cpo_norm_bwd_favor.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, c_int]
         self.lib = lib
+
+    def norm_favor(self, xq, xk, W):
+        xq, xk, W = (np.ascontiguousarray(x, np.float32) for x in (xq, xk, W))
+        lead = xq.shape[:-2]
+        BH = int(np.prod(lead)) if lead else 1
+        N, r, D = xq.shape[-2], xq.shape[-1], W.shape[0]
+        z = np.zeros(lead + (N,))
+        assert self.lib.cpo_norm_favor(xq.ctypes.data, xk.ctypes.data, W.ctypes.data,
+                                       z.ctypes.data, BH, N, r, D, 1) == 0
+        return z
+
+    def norm_bwd_favor(self, xq, xk, W, g):
+        xq, xk, W, g = (np.ascontiguousarray(x, np.float32) for x in (xq, xk, W, g))
+        lead = xq.shape[:-2]
+        BH = int(np.prod(lead)) if lead else 1
+        N, r, D = xq.shape[-2], xq.shape[-1], W.shape[0]
+        dxq, dxk = np.zeros(lead + (N, r)), np.zeros(lead + (N, r))
+        assert self.lib.cpo_norm_bwd_favor(xq.ctypes.data, xk.ctypes.data, W.ctypes.data,
+                                           g.ctypes.data, dxq.ctypes.data, dxk.ctypes.data, BH,
+                                           N, r, D, 1) == 0
+        return dxq, dxk
 
     def fwd_favor(self, xq, xk, v, W):
         xq, xk, v, W = (np.ascontiguousarray(x, np.float32) for x in (xq, xk, v, W))
