@@ -598,6 +598,17 @@ def run_ours(args, world, rank, local):
                 "timing": "CUDA events over 20 calls"}
         del xq_, xk_, fo
 
+    # ---- the other four workloads, each as a step of its own pass (forward
+    # for the fp32 ones, whose workload is forward only, with their
+    # fwd + bwd beside it), same steps and warm-up, CUDA events
+    others = None
+    if not args.no_others:
+        others = {}
+        for name, w2 in WORKLOADS.items():
+            if name == w.name:
+                continue
+            others[name] = time_workload(cp, w2, dev, stream, args.steps, args.warmup, world)
+
     # ---- roofline of the dominant kernel.  Unsplit problems on fewer than
     # the SMs: the single backward launch (dk/dv and dq scans; the backward
     # call is exactly that launch, timed by its own events); otherwise the
@@ -623,8 +634,11 @@ def run_ours(args, world, rank, local):
     if fused and not segmented:
         if _single_launch_bwd(w):
             # one launch: the fused dk/dv scans (read q, k, v, g; write dk,
-            # dv) and the dq scans (read g, v, k; write dq)
-            b_bytes = s * (5 * w.D + 5 * w.M) * w.token_heads
+            # dv) and the dq scans (read g, v, k; write dq).  The roofline
+            # counts the backward's algorithmic bytes (read q, k, v, g once,
+            # write dq, dk, dv); the kernel's own reads are reported beside it
+            b_bytes = s * (4 * w.D + 3 * w.M) * w.token_heads
+            impl_bytes = s * (5 * w.D + 5 * w.M) * w.token_heads
             b_ms = bwd_ms / args.steps
             b_traffic = None
             if PROFILED_TRAFFIC_BWD["source_sha256"] == kernel_sha(BWD_SOURCES):
@@ -634,10 +648,12 @@ def run_ours(args, world, rank, local):
             # the fused dk/dv launch, timed as the backward call minus its
             # causal-product launch (dq, the same bytes as the forward when D = M)
             b_bytes = s * (3 * w.D + 3 * w.M) * w.token_heads
+            impl_bytes = b_bytes
             b_ms = (bwd_ms - fwd_ms) / args.steps
             b_traffic = None
             name, timing = "tc_dkdv_kernel", "backward call minus one forward launch"
         bwd_entry = {"kernel": name, "bound": "hbm", "bytes_per_launch": b_bytes,
+                     "implementation_bytes_per_launch": impl_bytes,
                      "avg_launch_ms": b_ms, "achieved": b_bytes / (b_ms / 1e3) / 1e9,
                      "frac": b_bytes / (b_ms / 1e3) / 1e9 / hbm_gbs, "traffic": b_traffic,
                      "timing": timing}
@@ -663,6 +679,10 @@ def run_ours(args, world, rank, local):
                      "unit": "GB/s", "frac": dominant["frac"], "traffic": dominant["traffic"],
                      "kernel": dominant["kernel"], "peak_source": f"{peak_src} hbm_gbs",
                      "bytes_per_launch": dominant["bytes_per_launch"],
+                     "implementation_bytes_per_launch": dominant.get(
+                         "implementation_bytes_per_launch", dominant["bytes_per_launch"]),
+                     "bytes_basis": "algorithmic bytes per launch: forward s(2D+2M), "
+                                    "backward s(4D+3M) per token-head",
                      "avg_launch_ms": dominant["avg_launch_ms"], "timing": dominant["timing"],
                      "other_kernels": kernels},
         "gpu_launches": launches_per_step * args.steps,
@@ -671,6 +691,7 @@ def run_ours(args, world, rank, local):
         "decode": dec,
         "normalizer": norm,
         "feature_map": feat,
+        "other_workloads": others,
         "carried_state": None if state_ms is None else {
             "ms_per_step": state_ms, "value": w.token_heads * world / (state_ms / 1e3) / 1e6,
             "unit": UNIT, "note": "fwd with S_0 in and S_N out, bwd with dS_N in and dS_0 out"},
@@ -680,6 +701,98 @@ def run_ours(args, world, rank, local):
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+def step_bytes(w, backward=True):
+    """Algorithmic bytes of one step: forward s(2D+2M), backward s(4D+3M)
+    per token-head."""
+    s = 2 if w.dtype == "bf16" else 4
+    per_th = s * (2 * w.D + 2 * w.M) + (s * (4 * w.D + 3 * w.M) if backward else 0)
+    return per_th * w.token_heads
+
+
+def step_flops(w, backward=True):
+    """Algorithmic flops of one step with the chunk convention C = 64:
+    forward 4DM + C(D+M), backward 10DM + C(3D+2M) per token-head."""
+    C = 64
+    per_th = 4 * w.D * w.M + C * (w.D + w.M)
+    if backward:
+        per_th += 10 * w.D * w.M + C * (3 * w.D + 2 * w.M)
+    return per_th * w.token_heads
+
+
+def fp32_fma_peak_tflops():
+    """FP32 FMA peak derived from unit counts and the clock (not measured):
+    152 SMs x 128 lanes x 2 flop x the maximum SM clock."""
+    mhz = 2070.0
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            mhz = float(json.load(f).get("sm_max_mhz", mhz))
+    return 152 * 128 * 2 * mhz * 1e6 / 1e12
+
+
+def time_workload(cp, w, dev, stream, steps, warmup, world):
+    """Time one workload's step (its own pass) and its fwd + bwd step with
+    CUDA events on `stream`, and report the step roofline."""
+    import torch
+    from prefix_sum_outer_gb300.workloads import make_inputs
+    q, k, v, g = make_inputs(w.B, w.H, w.N, w.D, w.M, w.torch_dtype, seed=w.seed,
+                             feature=w.feature, x_std=w.x_std, backward=True)
+    qd, kd, vd, gd = (t.to(dev) for t in (q, k, v, g))
+    out = torch.empty_like(vd)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws_f = torch.zeros(cp.causal_product_workspace_size(w.B, w.H, w.N, w.D, w.M, w.torch_dtype,
+                                                        False), dtype=torch.uint8, device=dev)
+    ws_b = torch.zeros(cp.causal_product_workspace_size(w.B, w.H, w.N, w.D, w.M, w.torch_dtype,
+                                                        True), dtype=torch.uint8, device=dev)
+
+    def fwd():
+        cp.causal_product_fwd(qd, kd, vd, out=out, workspace=ws_f, stream=stream)
+
+    def fwd_bwd():
+        fwd()
+        cp.causal_product_bwd(qd, kd, vd, gd, dq, dk, dv, workspace=ws_b, stream=stream)
+
+    def timed(fn):
+        for _ in range(max(warmup, 3)):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return max_over_ranks(e0.elapsed_time(e1), world) / steps
+
+    hbm_gbs = load_peaks()[0]
+    res = {"B": w.B, "H": w.H, "N": w.N, "D": w.D, "M": w.M, "dtype": w.dtype,
+           "features": w.feature, "pass": "fwd+bwd" if w.backward else "fwd"}
+    for label, fn, bwd in (("fwd", fwd, False), ("fwd_bwd", fwd_bwd, True)):
+        ms = timed(fn)
+        nbytes, flops = step_bytes(w, bwd), step_flops(w, bwd)
+        entry = {"ms_per_step": ms, "value": w.token_heads * world / (ms / 1e3) / 1e6,
+                 "unit": UNIT, "bytes_per_step": nbytes,
+                 "step_hbm_roofline_frac": nbytes / (hbm_gbs * 1e9) / (ms / 1e3),
+                 "flops_per_step": flops}
+        if w.dtype == "f32":
+            peak = fp32_fma_peak_tflops()
+            entry["bound"] = "alu"
+            entry["step_alu_roofline_frac"] = flops / (peak * 1e12) / (ms / 1e3)
+            entry["alu_peak_tflops"] = peak
+            entry["alu_peak_source"] = "derived: 152 SMs x 128 FP32 lanes x 2 x max SM clock"
+        else:
+            entry["bound"] = "hbm"
+        entry["launches"] = _launch_count(w, False) + (_launch_count(w, True) if bwd else 0)
+        res[label] = entry
+    if cp.causal_product_status(ws_f) != cp.CP_OK or cp.causal_product_status(ws_b) != cp.CP_OK:
+        raise RuntimeError(f"kernel status word reports an error on {w.name}")
+    res["timing"] = (f"CUDA events over {steps} back-to-back steps after "
+                     f"{max(warmup, 3)} warm-up steps")
+    del qd, kd, vd, gd, out, dq, dk, dv, ws_f, ws_b
+    torch.cuda.empty_cache()
+    return res
 
 
 def _fused_dkdv(w):
@@ -723,6 +836,8 @@ def main(argv=None):
     ap.add_argument("--e2e-chunks", type=int, default=2)
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the carried-state and decoding measurements")
+    ap.add_argument("--no-others", action="store_true",
+                    help="skip timing the other four workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     args = ap.parse_args(argv)

@@ -288,12 +288,24 @@ CP_API cp_status_t causal_product_normalizer_bwd_feature(const void* q, const vo
  * (cudaGetSymbolAddress) and caches it; make that first call before any
  * stream capture.  Problems whose scratch would exceed the array return
  * CP_ERR_NOALLOC_LIMIT before enqueuing anything.  The array is shared by
- * every call and keeps the last call's contents: the call clears the status
- * word on `stream` before its kernels run, and calls that overlap on the GPU
- * (different streams, no ordering between them) race on it. */
+ * every call and keeps the last call's contents; calls that overlap on the
+ * GPU (different streams, no ordering between them) race on it.  Its first
+ * bytes hold a status word shared by every call on the device: it starts
+ * clear when the library's module is loaded, a kernel whose bounded wait runs
+ * out writes CP_ERR_TIMEOUT into it (the outputs of that call are then
+ * undefined), and it stays set until causal_product_noalloc_status reads it. */
 CP_API cp_status_t causal_product_fwd_noalloc(const void* q, const void* k, const void* v, void* out,
                                               int64_t B, int64_t H, int64_t N, int64_t D, int64_t M,
                                               cp_dtype_t dtype, void* stream);
+
+/* Synchronises `stream`, then returns and clears the status word of the
+ * static scratch array behind causal_product_fwd_noalloc on the current
+ * device: CP_OK, CP_ERR_TIMEOUT if any call since the last read recorded a
+ * timeout, or CP_ERR_CUDA if the stream reports an error.  Allocates
+ * nothing.  (No counterpart in the paper; it completes the allocation-free
+ * entry point, whose callers have no workspace to pass to
+ * causal_product_status.) */
+CP_API cp_status_t causal_product_noalloc_status(void* stream);
 
 /* Self-test of the failure path (no counterpart on the pages): one block
  * waits on a barrier that nothing arrives at, gives up after `wait_ns`

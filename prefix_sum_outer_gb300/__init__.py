@@ -28,7 +28,7 @@ from . import build as _build
 
 __all__ = [
     "CP_OK", "CausalProductError", "causal_product", "causal_product_fwd", "causal_product_bwd",
-    "causal_product_fwd_noalloc", "causal_product_decode",
+    "causal_product_fwd_noalloc", "causal_product_noalloc_status", "causal_product_decode",
     "causal_product_normalizer", "causal_product_normalizer_bwd", "normalizer",
     "causal_product_fwd_feature", "causal_product_bwd_feature", "FEATURES",
     "causal_product_workspace_size", "causal_product_launch_count", "causal_product_status",
@@ -95,6 +95,8 @@ def load_library(rebuild: bool = True) -> ctypes.CDLL:
             lib.causal_product_fwd_noalloc.argtypes = [p, p, p, p, i64, i64, i64, i64, i64, c_int,
                                                        p]
             lib.causal_product_fwd_noalloc.restype = c_int
+            lib.causal_product_noalloc_status.argtypes = [p]
+            lib.causal_product_noalloc_status.restype = c_int
             lib.causal_product_normalizer_workspace_size.argtypes = [i64, i64, i64, i64, c_int]
             lib.causal_product_normalizer_workspace_size.restype = sz
             lib.causal_product_normalizer.argtypes = [p, p, p, i64, i64, i64, i64, c_int, p, sz, p]
@@ -156,6 +158,15 @@ def _check_device(*ts: torch.Tensor):
             raise ValueError("all tensors must be contiguous")
 
 
+def _check_like(t: torch.Tensor, shape, dtype: torch.dtype, name: str):
+    """A caller-provided output must have exactly the shape and dtype the
+    kernels write: the C ABI receives only its pointer, so a smaller buffer
+    would be written past its end."""
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype} of shape {tuple(shape)}; "
+                         f"got {t.dtype} {tuple(t.shape)}")
+
+
 def _stream_ptr(stream: Optional[torch.cuda.Stream], device) -> int:
     s = stream if stream is not None else torch.cuda.current_stream(device)
     return int(s.cuda_stream)
@@ -209,6 +220,7 @@ def causal_product_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     code = _dtype_code(q, k, v)
     if out is None:
         out = torch.empty((B, H, N, M), dtype=q.dtype, device=q.device)
+    _check_like(out, (B, H, N, M), q.dtype, "out")
     _check_device(q, k, v, out)
     if return_state and state_out is None:
         state_out = torch.empty((B, H, D, M), dtype=torch.float32, device=q.device)
@@ -238,6 +250,7 @@ def causal_product_fwd_feature(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor
     code = _dtype_code(q, k, v)
     if out is None:
         out = torch.empty((B, H, N, M), dtype=q.dtype, device=q.device)
+    _check_like(out, (B, H, N, M), q.dtype, "out")
     _check_device(q, k, v, out)
     lib = load_library()
     need = lib.causal_product_feature_workspace_size(B, H, N, D, M, code, 0)
@@ -268,6 +281,8 @@ def causal_product_bwd_feature(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor
     grad_q = torch.empty_like(q) if grad_q is None else grad_q
     grad_k = torch.empty_like(k) if grad_k is None else grad_k
     grad_v = torch.empty_like(v) if grad_v is None else grad_v
+    for t, ref, name in ((grad_q, q, "grad_q"), (grad_k, k, "grad_k"), (grad_v, v, "grad_v")):
+        _check_like(t, ref.shape, ref.dtype, name)
     _check_device(q, k, v, grad_out, grad_q, grad_k, grad_v)
     lib = load_library()
     need = lib.causal_product_feature_workspace_size(B, H, N, D, M, code, 1)
@@ -296,6 +311,7 @@ def causal_product_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor
     """
     B, H, N, D, M = _dims(q, k, v)
     code = _dtype_code(q, k, v, out)
+    _check_like(out, (B, H, N, M), q.dtype, "out")
     _check_device(q, k, v, out)
     rc = load_library().causal_product_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(),
                                                    out.data_ptr(), B, H, N, D, M, code,
@@ -326,6 +342,8 @@ def causal_product_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, grad_o
     grad_q = torch.empty_like(q) if grad_q is None else grad_q
     grad_k = torch.empty_like(k) if grad_k is None else grad_k
     grad_v = torch.empty_like(v) if grad_v is None else grad_v
+    for t, ref, name in ((grad_q, q, "grad_q"), (grad_k, k, "grad_k"), (grad_v, v, "grad_v")):
+        _check_like(t, ref.shape, ref.dtype, name)
     _check_device(q, k, v, grad_out, grad_q, grad_k, grad_v)
     if return_state_grad and grad_state_in is None:
         grad_state_in = torch.empty((B, H, D, M), dtype=torch.float32, device=q.device)
@@ -363,6 +381,7 @@ def causal_product_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     code = _dtype_code(q, k, v)
     if out is None:
         out = torch.empty((B, H, M), dtype=q.dtype, device=q.device)
+    _check_like(out, (B, H, M), q.dtype, "out")
     _check_device(q, k, v, out, state)
     _state_arg(state, (B, H, D, M), q.device, "state")
     rc = load_library().causal_product_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(),
@@ -422,6 +441,8 @@ def causal_product_normalizer_bwd(q: torch.Tensor, k: torch.Tensor, grad_z: torc
         raise ValueError(f"grad_z must be float32 of shape {(B, H, N)}")
     grad_q = torch.empty_like(q) if grad_q is None else grad_q
     grad_k = torch.empty_like(k) if grad_k is None else grad_k
+    for t, ref, name in ((grad_q, q, "grad_q"), (grad_k, k, "grad_k")):
+        _check_like(t, ref.shape, ref.dtype, name)
     _check_device(q, k, grad_z, grad_q, grad_k)
     lib = load_library()
     need = lib.causal_product_normalizer_workspace_size(B, H, N, D, code)
@@ -453,6 +474,14 @@ def causal_product_status(workspace: torch.Tensor,
     """Synchronise ``stream`` and return (and clear) the workspace status word."""
     return int(load_library().causal_product_status(workspace.data_ptr(),
                                                     _stream_ptr(stream, workspace.device)))
+
+
+def causal_product_noalloc_status(stream: Optional[torch.cuda.Stream] = None,
+                                  device=None) -> int:
+    """Synchronise ``stream`` and return (and clear) the status word that
+    every causal_product_fwd_noalloc call on the current device shares."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    return int(load_library().causal_product_noalloc_status(_stream_ptr(stream, dev)))
 
 
 class CausalProduct(torch.autograd.Function):

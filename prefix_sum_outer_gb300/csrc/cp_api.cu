@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <mutex>
 
+#include <cuda.h>
+
 #include "cp_internal.h"
 
 namespace cp {
@@ -558,7 +560,7 @@ const char* causal_product_error_string(cp_status_t s) {
 // ---------------------------------------------------------------------------
 // Forward pass without any allocation.  Its scratch is a file-scope device
 // array; host code only ever passes the array's device address (looked up
-// once per device), never the host-side symbol itself.
+// once per device and context), never the host-side symbol itself.
 namespace cp {
 namespace {
 
@@ -567,18 +569,46 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[CP_NOALLOC_SCRA
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mutex;
 void* g_noalloc_ptr[kMaxDevices] = {};
+// the context the cached address belongs to: after cudaDeviceReset the
+// runtime creates a new primary context and loads the module again, so the
+// address is looked up afresh
+CUcontext g_noalloc_ctx[kMaxDevices] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
 
 // Device address of the scratch array on the current device.
 cp_status_t noalloc_scratch(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return CP_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return CP_ERR_NO_DEVICE;
+  const CtxGetCurrentFn get = ctx_get_current();
+  if (get == nullptr) return CP_ERR_CUDA;
+  CUcontext ctx = nullptr;
+  if (get(&ctx) != CUDA_SUCCESS) return CP_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (g_noalloc_ptr[dev] == nullptr) {
+  if (g_noalloc_ptr[dev] == nullptr || ctx == nullptr || g_noalloc_ctx[dev] != ctx) {
+    // the lookup makes the device's primary context current (and loads the
+    // module into it) when nothing has yet
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
       return CP_ERR_CUDA;
+    if (get(&ctx) != CUDA_SUCCESS || ctx == nullptr) return CP_ERR_CUDA;
     g_noalloc_ptr[dev] = p;
+    g_noalloc_ctx[dev] = ctx;
   }
   *out = g_noalloc_ptr[dev];
   return CP_OK;
@@ -599,10 +629,17 @@ extern "C" cp_status_t causal_product_fwd_noalloc(const void* q, const void* k, 
   void* scratch = nullptr;
   st = cp::noalloc_scratch(&scratch);
   if (st != CP_OK) return st;
-  // the shared array keeps the previous call's contents: clear its status word
-  if (cudaMemsetAsync(scratch, 0, sizeof(int), static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return CP_ERR_CUDA;
-  // With a caller-style workspace the forward entry point allocates nothing.
+  // The array starts zeroed when the module loads, so its status word starts
+  // clear; like a caller's workspace it is sticky until
+  // causal_product_noalloc_status reads it.  With a caller-style workspace
+  // the forward entry point allocates nothing.
   return causal_product_fwd(q, k, v, out, B, H, N, D, M, dtype, scratch,
                             CP_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+extern "C" cp_status_t causal_product_noalloc_status(void* stream) {
+  void* scratch = nullptr;
+  const cp_status_t st = cp::noalloc_scratch(&scratch);
+  if (st != CP_OK) return st;
+  return causal_product_status(scratch, stream);
 }

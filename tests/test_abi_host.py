@@ -185,6 +185,34 @@ def test_python_binding_refuses_cpu_tensors():
             call()
 
 
+def test_python_binding_refuses_misshaped_outputs():
+    """A caller's output buffer must match the shape and dtype the kernels
+    write; the C ABI only sees its pointer, so the binding checks it before
+    anything else (here on host tensors, which are refused later anyway)."""
+    import torch
+    q = torch.ones(1, 1, 4, 16)
+    short = torch.empty(1, 1, 3, 16)
+    wrong = torch.empty(1, 1, 4, 16, dtype=torch.float16)
+    z = torch.ones(1, 1, 4)
+    q1 = torch.ones(1, 1, 16)
+    st = torch.zeros(1, 1, 16, 16)
+    calls = [
+        lambda: cp.causal_product_fwd(q, q, q, out=short),
+        lambda: cp.causal_product_fwd(q, q, q, out=wrong),
+        lambda: cp.causal_product_fwd_noalloc(q, q, q, short),
+        lambda: cp.causal_product_fwd_feature(q, q, q, out=short),
+        lambda: cp.causal_product_bwd(q, q, q, q, grad_q=short),
+        lambda: cp.causal_product_bwd(q, q, q, q, grad_k=short),
+        lambda: cp.causal_product_bwd(q, q, q, q, grad_v=wrong),
+        lambda: cp.causal_product_bwd_feature(q, q, q, q, grad_v=short),
+        lambda: cp.causal_product_normalizer_bwd(q, q, z, grad_k=short),
+        lambda: cp.causal_product_decode(q1, q1, q1, st, out=torch.empty(1, 1, 8)),
+    ]
+    for call in calls:
+        with pytest.raises(ValueError):
+            call()
+
+
 def test_state_argument_checks(lib):
     def fwd_state(**kw):
         args = dict(q=A, k=2 * A, v=3 * A, out=4 * A, s_in=None, s_out=None, B=1, H=1, N=16,
