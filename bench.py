@@ -1,7 +1,9 @@
 #!/usr/bin/env python3
 """Benchmark of the causal dot product (forward + backward) on GB300.
 
-One step = causal_product_fwd + causal_product_bwd over one batch of the
+One step = causal_product_fwd_ckpt + causal_product_bwd_ckpt (the forward
+leaves checkpoints of its state for the backward's dq scans, as the autograd
+wrapper does) over one batch of the
 bf16 workload B=8, H=16, N=4096, D=M=64 (inputs resident in HBM when the
 timed region starts; every input is larger than the 129 MB L2, so no flush
 is needed between iterations).  Prints ONE JSON line (rank 0).
@@ -292,9 +294,21 @@ def run_ours(args, world, rank, local):
                                                         True), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    # the forward leaves checkpoints of its state for the backward's dq scans
+    ckpt = torch.empty(max(cp.causal_product_checkpoint_size(w.B, w.H, w.N, w.D, w.M,
+                                                             w.torch_dtype) // 4, 1),
+                       dtype=torch.float32, device=dev)
+
+    def fwd_call():
+        cp.causal_product_fwd_ckpt(qd, kd, vd, out=out, ckpt=ckpt, workspace=ws_f, stream=stream)
+
+    def bwd_call():
+        cp.causal_product_bwd_ckpt(qd, kd, vd, gd, ckpt, dq, dk, dv, workspace=ws_b,
+                                   stream=stream)
+
     def step():
-        cp.causal_product_fwd(qd, kd, vd, out=out, workspace=ws_f, stream=stream)
-        cp.causal_product_bwd(qd, kd, vd, gd, dq, dk, dv, workspace=ws_b, stream=stream)
+        fwd_call()
+        bwd_call()
 
     # kernels of ours launched per step: the library's own count for the
     # forward and the backward call of this shape
@@ -332,9 +346,9 @@ def run_ours(args, world, rank, local):
         # step time)
         for e0, e1, e2 in ev:
             e0.record(stream)
-            cp.causal_product_fwd(qd, kd, vd, out=out, workspace=ws_f, stream=stream)
+            fwd_call()
             e1.record(stream)
-            cp.causal_product_bwd(qd, kd, vd, gd, dq, dk, dv, workspace=ws_b, stream=stream)
+            bwd_call()
             e2.record(stream)
         torch.cuda.synchronize()
     barrier(world)
@@ -372,6 +386,11 @@ def run_ours(args, world, rank, local):
                                                              False), dtype=torch.uint8, device=dev)
         ws_bc = torch.zeros(cp.causal_product_workspace_size(1, cb, w.N, w.D, w.M, w.torch_dtype,
                                                              True), dtype=torch.uint8, device=dev)
+        # one checkpoint buffer per chunk would let chunks overlap; the
+        # compute of the chunks runs on one stream, so they share one
+        ckpt_c = torch.empty(max(cp.causal_product_checkpoint_size(1, cb, w.N, w.D, w.M,
+                                                                   w.torch_dtype) // 4, 1),
+                             dtype=torch.float32, device=dev)
 
         # cross-step hazards: a chunk's inputs are overwritten only after the
         # previous step's compute of that chunk, and its outputs only after
@@ -401,9 +420,10 @@ def run_ours(args, world, rank, local):
                     s_cmp.wait_event(e)
                 cq, ck, cv, cg = (t[sl].view(1, cb, w.N, -1) for t in dev_in)
                 co, cdq, cdk, cdv = (t[sl].view(1, cb, w.N, -1) for t in dev_out)
-                cp.causal_product_fwd(cq, ck, cv, out=co, workspace=ws_fc, stream=s_cmp)
-                cp.causal_product_bwd(cq, ck, cv, cg, cdq, cdk, cdv, workspace=ws_bc,
-                                      stream=s_cmp)
+                cp.causal_product_fwd_ckpt(cq, ck, cv, out=co, ckpt=ckpt_c, workspace=ws_fc,
+                                           stream=s_cmp)
+                cp.causal_product_bwd_ckpt(cq, ck, cv, cg, ckpt_c, cdq, cdk, cdv, workspace=ws_bc,
+                                           stream=s_cmp)
                 e = torch.cuda.Event()
                 e.record(s_cmp)
                 prev_cmp[c] = e
@@ -747,12 +767,18 @@ def time_workload(cp, w, dev, stream, steps, warmup, world):
     ws_b = torch.zeros(cp.causal_product_workspace_size(w.B, w.H, w.N, w.D, w.M, w.torch_dtype,
                                                         True), dtype=torch.uint8, device=dev)
 
+    ckpt = torch.empty(max(cp.causal_product_checkpoint_size(w.B, w.H, w.N, w.D, w.M,
+                                                             w.torch_dtype) // 4, 1),
+                       dtype=torch.float32, device=dev)
+
     def fwd():
         cp.causal_product_fwd(qd, kd, vd, out=out, workspace=ws_f, stream=stream)
 
     def fwd_bwd():
-        fwd()
-        cp.causal_product_bwd(qd, kd, vd, gd, dq, dk, dv, workspace=ws_b, stream=stream)
+        # the training step: the forward leaves checkpoints for the backward
+        cp.causal_product_fwd_ckpt(qd, kd, vd, out=out, ckpt=ckpt, workspace=ws_f, stream=stream)
+        cp.causal_product_bwd_ckpt(qd, kd, vd, gd, ckpt, dq, dk, dv, workspace=ws_b,
+                                   stream=stream)
 
     def timed(fn):
         for _ in range(max(warmup, 3)):
@@ -784,7 +810,8 @@ def time_workload(cp, w, dev, stream, steps, warmup, world):
             entry["alu_peak_source"] = "derived: 152 SMs x 128 FP32 lanes x 2 x max SM clock"
         else:
             entry["bound"] = "hbm"
-        entry["launches"] = _launch_count(w, False) + (_launch_count(w, True) if bwd else 0)
+        entry["launches"] = (_launch_count(w, True, ckpt=True) + _launch_count(w, False, ckpt=True)
+                             if bwd else _launch_count(w, False))
         res[label] = entry
     if cp.causal_product_status(ws_f) != cp.CP_OK or cp.causal_product_status(ws_b) != cp.CP_OK:
         raise RuntimeError(f"kernel status word reports an error on {w.name}")
@@ -800,9 +827,10 @@ def _fused_dkdv(w):
     return w.dtype == "bf16" and w.D <= 64 and w.M <= 64
 
 
-def _launch_count(w, backward):
+def _launch_count(w, backward, ckpt=False):
     import prefix_sum_outer_gb300 as cp
-    c = cp.causal_product_launch_count(w.B, w.H, w.N, w.D, w.M, w.torch_dtype, backward)
+    c = cp.causal_product_launch_count(w.B, w.H, w.N, w.D, w.M, w.torch_dtype, backward,
+                                       ckpt=ckpt)
     if c < 0:
         raise RuntimeError(f"shape of {w.name} rejected by the library")
     return c
@@ -815,14 +843,14 @@ def _segmented(w):
 
 def _single_launch_bwd(w):
     """The whole backward (dk/dv and dq scans) is one launch."""
-    return _fused_dkdv(w) and _launch_count(w, True) == 1
+    return _fused_dkdv(w) and _launch_count(w, True, ckpt=True) == 1
 
 
 def _launches_per_step(w):
     """Kernels one fwd + bwd step launches, as the library plans them (one per
     unsplit scan, three per split scan, one for the whole backward when it
     fits a single launch)."""
-    return _launch_count(w, False) + _launch_count(w, True)
+    return _launch_count(w, False, ckpt=True) + _launch_count(w, True, ckpt=True)
 
 
 def main(argv=None):

@@ -35,7 +35,8 @@
  *   - `workspace` is device scratch of at least
  *     causal_product_workspace_size(...) bytes, owned by the caller, used
  *     only until the enqueued work completes; it holds the per-segment fp32
- *     state aggregates of the two-pass scan and a status word.  The status
+ *     state aggregates of the two-pass scan, a status word and two counters
+ *     of the one-launch backward (which leaves them at zero).  The status
  *     word is sticky: kernels only ever write an error code into it, and
  *     causal_product_status() reads and clears it.  Zero the first 256 bytes
  *     of a new workspace once before its first use.  Passing
@@ -107,13 +108,16 @@ typedef enum {
 CP_API size_t causal_product_workspace_size(int64_t B, int64_t H, int64_t N, int64_t D, int64_t M,
                                             cp_dtype_t dtype, int backward);
 
-/* Number of kernels one causal_product_fwd (backward = 0) or
- * causal_product_bwd (backward = 1) call launches for this problem, with no
- * carried state: 1 per unsplit scan, 3 per scan split into segments (the
- * segment sums, their prefix, the scan), and 1 for the whole backward when
- * bf16 with D, M <= 64 runs unsplit on fewer problems than SMs.  Pure host
- * computation (the SM count of the current device, else 152).  Returns -1
- * for arguments the entry points would reject, 0 when N = 0. */
+/* Number of kernels one causal_product_fwd (backward = 0),
+ * causal_product_bwd (backward = 1), causal_product_fwd_ckpt (backward = 2)
+ * or causal_product_bwd_ckpt (backward = 3) call launches for this problem,
+ * with no carried state: 1 per unsplit scan, 3 per scan split into segments
+ * (the segment sums, their prefix, the scan), 1 for a scan seeded from
+ * precomputed states (dq from checkpoints; bf16 dk from dv's segment
+ * prefixes), and 1 for the whole backward when bf16 with D, M <= 64 runs
+ * unsplit on fewer problems than SMs.  Pure host computation (the SM count
+ * of the current device, else 152).  Returns -1 for arguments the entry
+ * points would reject, 0 when N = 0. */
 CP_API int causal_product_launch_count(int64_t B, int64_t H, int64_t N, int64_t D, int64_t M,
                                        cp_dtype_t dtype, int backward);
 
@@ -133,6 +137,41 @@ CP_API cp_status_t causal_product_bwd(const void* q, const void* k, const void* 
                                       int64_t B, int64_t H, int64_t N, int64_t D, int64_t M,
                                       cp_dtype_t dtype, void* workspace, size_t workspace_bytes,
                                       void* stream);
+
+/* Forward and backward with checkpoints of the state.  The backward's dq is
+ * the forward product of (grad_out, v, k), whose running state sum_j v_j k_j^T
+ * is the transpose of the forward's S_i; causal_product_fwd_ckpt writes that
+ * state at fixed row boundaries (every few 128-row tiles) into `ckpt`, so
+ * causal_product_bwd_ckpt can split every dq scan into segments that start
+ * from a checkpoint, with no pass of its own over k and v to find the
+ * segments' starting states (a two-pass scan whose first pass the forward
+ * has already done; the pages of triton-lang/triton issue #217 ask for the
+ * prefix sum over the sequence to be parallel).
+ *
+ * causal_product_checkpoint_size returns the bytes of `ckpt` (fp32; layout
+ * private to the library), a pure function of the shape and dtype; 0 means
+ * no checkpoints are used for this problem (fp32 and fp16 inputs, short
+ * sequences, or a backward that does not split dq), and then `ckpt` may be
+ * NULL and the two calls are causal_product_fwd and causal_product_bwd.
+ * Otherwise `ckpt` is a caller-owned device buffer of at least that many
+ * bytes, 16-byte aligned, overlapping no other argument; the forward writes
+ * it and the backward reads it, so pass the backward the buffer of the
+ * forward on the same q, k, v (a stale or foreign buffer gives a wrong
+ * grad_q, undetected).  All other arguments, errors and workspaces as
+ * causal_product_fwd / causal_product_bwd; CP_ERR_WORKSPACE_TOO_SMALL if
+ * ckpt_bytes is below the size.  No carried state in this mode. */
+CP_API size_t causal_product_checkpoint_size(int64_t B, int64_t H, int64_t N, int64_t D,
+                                             int64_t M, cp_dtype_t dtype);
+CP_API cp_status_t causal_product_fwd_ckpt(const void* q, const void* k, const void* v, void* out,
+                                           float* ckpt, size_t ckpt_bytes, int64_t B, int64_t H,
+                                           int64_t N, int64_t D, int64_t M, cp_dtype_t dtype,
+                                           void* workspace, size_t workspace_bytes, void* stream);
+CP_API cp_status_t causal_product_bwd_ckpt(const void* q, const void* k, const void* v,
+                                           const void* grad_out, const float* ckpt,
+                                           size_t ckpt_bytes, void* grad_q, void* grad_k,
+                                           void* grad_v, int64_t B, int64_t H, int64_t N,
+                                           int64_t D, int64_t M, cp_dtype_t dtype,
+                                           void* workspace, size_t workspace_bytes, void* stream);
 
 /* Forward with a carried state.  The recurrence of triton-lang/triton issue
  * #217 keeps its state across the sequence, and the Triton port there takes

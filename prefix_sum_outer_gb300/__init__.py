@@ -32,6 +32,7 @@ __all__ = [
     "causal_product_normalizer", "causal_product_normalizer_bwd", "normalizer",
     "causal_product_fwd_feature", "causal_product_bwd_feature", "FEATURES",
     "causal_product_workspace_size", "causal_product_launch_count", "causal_product_status",
+    "causal_product_checkpoint_size", "causal_product_fwd_ckpt", "causal_product_bwd_ckpt",
     "causal_product_error_string", "library_path", "load_library",
 ]
 
@@ -82,6 +83,14 @@ def load_library(rebuild: bool = True) -> ctypes.CDLL:
             lib.causal_product_bwd.argtypes = [p, p, p, p, p, p, p, i64, i64, i64, i64, i64, c_int,
                                                p, sz, p]
             lib.causal_product_bwd.restype = c_int
+            lib.causal_product_checkpoint_size.argtypes = [i64, i64, i64, i64, i64, c_int]
+            lib.causal_product_checkpoint_size.restype = sz
+            lib.causal_product_fwd_ckpt.argtypes = [p, p, p, p, p, sz, i64, i64, i64, i64, i64,
+                                                    c_int, p, sz, p]
+            lib.causal_product_fwd_ckpt.restype = c_int
+            lib.causal_product_bwd_ckpt.argtypes = [p, p, p, p, p, sz, p, p, p, i64, i64, i64,
+                                                    i64, i64, c_int, p, sz, p]
+            lib.causal_product_bwd_ckpt.restype = c_int
             lib.causal_product_fwd_state.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, i64,
                                                      c_int, p, sz, p]
             lib.causal_product_fwd_state.restype = c_int
@@ -181,11 +190,90 @@ def causal_product_workspace_size(B: int, H: int, N: int, D: int, M: int,
 
 def causal_product_launch_count(B: int, H: int, N: int, D: int, M: int,
                                 dtype: torch.dtype = torch.bfloat16,
-                                backward: bool = False) -> int:
-    """Kernels one causal_product_fwd (or, with ``backward``, _bwd) call
-    launches for this shape; -1 for a shape the entry points reject."""
-    return int(load_library().causal_product_launch_count(B, H, N, D, M, _DTYPES[dtype],
-                                                          int(bool(backward))))
+                                backward: bool = False, ckpt: bool = False) -> int:
+    """Kernels one causal_product_fwd (or, with ``backward``, _bwd; with
+    ``ckpt``, the checkpoint calls) launches for this shape; -1 for a shape
+    the entry points reject."""
+    mode = int(bool(backward)) + (2 if ckpt else 0)
+    return int(load_library().causal_product_launch_count(B, H, N, D, M, _DTYPES[dtype], mode))
+
+
+def causal_product_checkpoint_size(B: int, H: int, N: int, D: int, M: int,
+                                   dtype: torch.dtype = torch.bfloat16) -> int:
+    """Bytes of the checkpoint buffer of causal_product_fwd_ckpt (0: none)."""
+    return int(load_library().causal_product_checkpoint_size(B, H, N, D, M, _DTYPES[dtype]))
+
+
+def _ckpt_buffer(B, H, N, D, M, dtype, device, ckpt):
+    n = causal_product_checkpoint_size(B, H, N, D, M, dtype)
+    if ckpt is None:
+        ckpt = torch.empty(max(n // 4, 1), dtype=torch.float32, device=device)
+    if ckpt.dtype != torch.float32 or ckpt.numel() * 4 < n or not ckpt.is_contiguous():
+        raise ValueError(f"ckpt must be a contiguous float32 tensor of at least {n} bytes")
+    return ckpt
+
+
+def causal_product_fwd_ckpt(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                            out: Optional[torch.Tensor] = None,
+                            ckpt: Optional[torch.Tensor] = None,
+                            workspace: Optional[torch.Tensor] = None,
+                            stream: Optional[torch.cuda.Stream] = None):
+    """The forward that also writes checkpoints of the state for the
+    backward (causal_product_bwd_ckpt); returns (out, ckpt)."""
+    B, H, N, D, M = _dims(q, k, v)
+    code = _dtype_code(q, k, v)
+    if out is None:
+        out = torch.empty((B, H, N, M), dtype=q.dtype, device=q.device)
+    _check_like(out, (B, H, N, M), q.dtype, "out")
+    _check_device(q, k, v, out)
+    ckpt = _ckpt_buffer(B, H, N, D, M, q.dtype, q.device, ckpt)
+    _check_device(q, ckpt)
+    lib = load_library()
+    need = lib.causal_product_workspace_size(B, H, N, D, M, code, 0)
+    if workspace is None:
+        workspace = _workspace(need, q.device)
+    rc = lib.causal_product_fwd_ckpt(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                     ckpt.data_ptr(), ckpt.numel() * 4, B, H, N, D, M, code,
+                                     workspace.data_ptr(), workspace.numel(),
+                                     _stream_ptr(stream, q.device))
+    if rc != CP_OK:
+        raise CausalProductError(rc, "causal_product_fwd_ckpt")
+    return out, ckpt
+
+
+def causal_product_bwd_ckpt(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                            grad_out: torch.Tensor, ckpt: torch.Tensor,
+                            grad_q: Optional[torch.Tensor] = None,
+                            grad_k: Optional[torch.Tensor] = None,
+                            grad_v: Optional[torch.Tensor] = None,
+                            workspace: Optional[torch.Tensor] = None,
+                            stream: Optional[torch.cuda.Stream] = None):
+    """(dq, dk, dv) of L = <grad_out, out>, the dq scans seeded from the
+    checkpoints causal_product_fwd_ckpt wrote for the same q, k, v."""
+    B, H, N, D, M = _dims(q, k, v)
+    code = _dtype_code(q, k, v, grad_out)
+    if grad_out.shape != v.shape:
+        raise ValueError("grad_out must have v's shape")
+    grad_q = torch.empty_like(q) if grad_q is None else grad_q
+    grad_k = torch.empty_like(k) if grad_k is None else grad_k
+    grad_v = torch.empty_like(v) if grad_v is None else grad_v
+    for t, ref, name in ((grad_q, q, "grad_q"), (grad_k, k, "grad_k"), (grad_v, v, "grad_v")):
+        _check_like(t, ref.shape, ref.dtype, name)
+    _check_device(q, k, v, grad_out, grad_q, grad_k, grad_v)
+    ckpt = _ckpt_buffer(B, H, N, D, M, q.dtype, q.device, ckpt)
+    _check_device(q, ckpt)
+    lib = load_library()
+    need = lib.causal_product_workspace_size(B, H, N, D, M, code, 1)
+    if workspace is None:
+        workspace = _workspace(need, q.device)
+    rc = lib.causal_product_bwd_ckpt(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                     grad_out.data_ptr(), ckpt.data_ptr(), ckpt.numel() * 4,
+                                     grad_q.data_ptr(), grad_k.data_ptr(), grad_v.data_ptr(),
+                                     B, H, N, D, M, code, workspace.data_ptr(),
+                                     workspace.numel(), _stream_ptr(stream, q.device))
+    if rc != CP_OK:
+        raise CausalProductError(rc, "causal_product_bwd_ckpt")
+    return grad_q, grad_k, grad_v
 
 
 def _workspace(nbytes: int, device) -> torch.Tensor:
@@ -485,18 +573,20 @@ def causal_product_noalloc_status(stream: Optional[torch.cuda.Stream] = None,
 
 
 class CausalProduct(torch.autograd.Function):
-    """Autograd wrapper: forward and backward both call the C ABI."""
+    """Autograd wrapper: forward and backward both call the C ABI; the
+    forward keeps checkpoints of the state for the backward's dq scans."""
 
     @staticmethod
     def forward(ctx, q, k, v):
         q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
-        ctx.save_for_backward(q, k, v)
-        return causal_product_fwd(q, k, v)
+        out, ckpt = causal_product_fwd_ckpt(q, k, v)
+        ctx.save_for_backward(q, k, v, ckpt)
+        return out
 
     @staticmethod
     def backward(ctx, g):
-        q, k, v = ctx.saved_tensors
-        return causal_product_bwd(q, k, v, g.contiguous().to(q.dtype))
+        q, k, v, ckpt = ctx.saved_tensors
+        return causal_product_bwd_ckpt(q, k, v, g.contiguous().to(q.dtype), ckpt)
 
 
 class Normalizer(torch.autograd.Function):

@@ -95,9 +95,10 @@ cp_status_t acquire(Scratch& s, void* workspace, size_t workspace_bytes, size_t 
     return CP_ERR_CUDA;
   }
   s.owned = true;
-  // a fresh allocation starts with a clear status word; a caller's workspace
-  // keeps its (sticky) status until causal_product_status() reads it
-  if (cudaMemsetAsync(s.base, 0, sizeof(int), stream) != cudaSuccess) return CP_ERR_CUDA;
+  // a fresh allocation starts with a clear status word and ticket counters;
+  // a caller's workspace keeps its (sticky) status until
+  // causal_product_status() reads it
+  if (cudaMemsetAsync(s.base, 0, 4 * sizeof(int), stream) != cudaSuccess) return CP_ERR_CUDA;
   return CP_OK;
 }
 
@@ -128,6 +129,14 @@ size_t norm_workspace_bytes(int64_t BH, int64_t N, int64_t D, cp_dtype_t dtype) 
   return kStatusBytes + round_up(norm_scratch_bytes(BH, N, D, dtype));
 }
 
+// Checkpoint plan of a call (none for fp32 and fp16, or without rows).
+CkptPlan call_ckpt_plan(int64_t B, int64_t H, int64_t N, int64_t D, int64_t M,
+                        cp_dtype_t dtype) {
+  if (dtype != CP_DTYPE_BF16 || N <= 0) return CkptPlan{};
+  return ckpt_plan(B * H, N, D, M);
+}
+
+
 }  // namespace
 }  // namespace cp
 
@@ -150,7 +159,12 @@ int causal_product_launch_count(int64_t B, int64_t H, int64_t N, int64_t D, int6
                                          : cp::simt_plan(BH, N, d, m).G;
     return G > 1 ? 3 : 1;
   };
-  if (!backward) return product(D, M);
+  if (backward < 0 || backward > 3) return -1;
+  // modes 2 and 3 are the checkpoint calls (forward and backward); with
+  // checkpoints the dq product is one launch, seeded from them
+  const bool ckpt = backward >= 2 && cp::call_ckpt_plan(B, H, N, D, M, dtype).G > 1;
+  if (backward == 0 || backward == 2) return product(D, M);
+  const int dq_launches = ckpt ? 1 : product(M, D);
   if (dtype == CP_DTYPE_BF16) {
     const cp::TcPlan plan = cp::tc_plan(BH, N, D, M);
     if (cp::tc_dkdv_supported(plan)) {
@@ -162,19 +176,40 @@ int causal_product_launch_count(int64_t B, int64_t H, int64_t N, int64_t D, int6
       }
       if (plan.G == 1 && BH < n_sm) return 1;
       // dq product, the reverse segment sums and their prefix, the dk/dv scan
-      return product(M, D) + (plan.G > 1 ? 2 : 0) + 1;
+      return dq_launches + (plan.G > 1 ? 2 : 0) + 1;
     }
   }
-  // dq (g, v, k), dv (k, q, g), dk (v, g, q)
-  return product(M, D) + product(D, M) + product(M, D);
+  // dq (g, v, k), dv (k, q, g), dk (v, g, q); bf16 dk starts from dv's
+  // segment prefixes when dv's scan is split with one value block
+  int dk_launches = product(M, D);
+  if (dtype == CP_DTYPE_BF16) {
+    const cp::TcPlan pvp = cp::tc_plan(BH, N, D, M);
+    if (pvp.ok && pvp.G > 1 && pvp.n_mb == 1) dk_launches = 1;
+  }
+  return dq_launches + product(D, M) + dk_launches;
 }
 
-cp_status_t causal_product_fwd_state(const void* q, const void* k, const void* v, void* out,
-                                     const float* state_in, float* state_out, int64_t B,
-                                     int64_t H, int64_t N, int64_t D, int64_t M,
-                                     cp_dtype_t dtype, void* workspace, size_t workspace_bytes,
-                                     void* stream_) {
+}  // extern "C"
+
+namespace cp {
+namespace {
+
+cp_status_t check_ckpt(const CkptPlan& ck, const void* ckpt, size_t ckpt_bytes) {
+  if (ck.G < 2) return CP_OK;
+  if (ckpt == nullptr) return CP_ERR_INVALID_ARG;
+  if (ckpt_bytes < ck.bytes) return CP_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned16(ckpt)) return CP_ERR_MISALIGNED;
+  return CP_OK;
+}
+
+cp_status_t fwd_impl(const void* q, const void* k, const void* v, void* out,
+                     const float* state_in, float* state_out, float* ckpt, size_t ckpt_bytes,
+                     int64_t B, int64_t H, int64_t N, int64_t D, int64_t M, cp_dtype_t dtype,
+                     void* workspace, size_t workspace_bytes, void* stream_, bool use_ckpt) {
   cp_status_t st = cp::check_dims(B, H, N, D, M, dtype);
+  if (st != CP_OK) return st;
+  const CkptPlan ck = use_ckpt ? call_ckpt_plan(B, H, N, D, M, dtype) : CkptPlan{};
+  st = check_ckpt(ck, ckpt, ckpt_bytes);
   if (st != CP_OK) return st;
   // with no rows nothing is read or written but the states
   if (N > 0 && (!q || !k || !v || !out)) return CP_ERR_INVALID_ARG;
@@ -192,6 +227,12 @@ cp_status_t causal_product_fwd_state(const void* q, const void* k, const void* v
       cp::overlaps(state_out, nst, v, nv) || cp::overlaps(state_out, nst, out, nv) ||
       cp::overlaps(state_out, nst, state_in, nst))
     return CP_ERR_INVALID_ARG;
+  if (ck.G > 1) {
+    const void* others[4] = {q, k, v, out};
+    const size_t sz[4] = {nqk, nqk, nv, nv};
+    for (int i = 0; i < 4; ++i)
+      if (cp::overlaps(ckpt, ck.bytes, others[i], sz[i])) return CP_ERR_INVALID_ARG;
+  }
   const size_t need = cp::workspace_bytes(BH, N, D, M, dtype, false);
   if (workspace != nullptr && workspace_bytes < need) return CP_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
@@ -206,7 +247,39 @@ cp_status_t causal_product_fwd_state(const void* q, const void* k, const void* v
   p.state_out = state_out;
   p.st_ld_r = M;
   p.st_ld_c = 1;
+  if (ck.G > 1) {
+    p.ck = ck;
+    p.ckpt = ckpt;
+  }
   return cp::run_product(p, dtype, agg, status, stream);
+}
+
+}  // namespace
+}  // namespace cp
+
+extern "C" {
+
+cp_status_t causal_product_fwd_state(const void* q, const void* k, const void* v, void* out,
+                                     const float* state_in, float* state_out, int64_t B,
+                                     int64_t H, int64_t N, int64_t D, int64_t M,
+                                     cp_dtype_t dtype, void* workspace, size_t workspace_bytes,
+                                     void* stream) {
+  return cp::fwd_impl(q, k, v, out, state_in, state_out, nullptr, 0, B, H, N, D, M, dtype,
+                      workspace, workspace_bytes, stream, false);
+}
+
+size_t causal_product_checkpoint_size(int64_t B, int64_t H, int64_t N, int64_t D, int64_t M,
+                                      cp_dtype_t dtype) {
+  if (cp::check_dims(B, H, N, D, M, dtype) != CP_OK) return 0;
+  return cp::call_ckpt_plan(B, H, N, D, M, dtype).bytes;
+}
+
+cp_status_t causal_product_fwd_ckpt(const void* q, const void* k, const void* v, void* out,
+                                    float* ckpt, size_t ckpt_bytes, int64_t B, int64_t H,
+                                    int64_t N, int64_t D, int64_t M, cp_dtype_t dtype,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+  return cp::fwd_impl(q, k, v, out, nullptr, nullptr, ckpt, ckpt_bytes, B, H, N, D, M, dtype,
+                      workspace, workspace_bytes, stream, true);
 }
 
 size_t causal_product_feature_workspace_size(int64_t B, int64_t H, int64_t N, int64_t D,
@@ -311,13 +384,21 @@ cp_status_t causal_product_fwd(const void* q, const void* k, const void* v, void
                                   workspace, workspace_bytes, stream);
 }
 
-cp_status_t causal_product_bwd_state(const void* q, const void* k, const void* v,
-                                     const void* grad_out, const float* state_in,
-                                     const float* grad_state_out, void* grad_q, void* grad_k,
-                                     void* grad_v, float* grad_state_in, int64_t B, int64_t H,
-                                     int64_t N, int64_t D, int64_t M, cp_dtype_t dtype,
-                                     void* workspace, size_t workspace_bytes, void* stream_) {
+}  // extern "C"
+
+namespace cp {
+namespace {
+
+cp_status_t bwd_impl(const void* q, const void* k, const void* v, const void* grad_out,
+                     const float* state_in, const float* grad_state_out, const float* ckpt,
+                     size_t ckpt_bytes, void* grad_q, void* grad_k, void* grad_v,
+                     float* grad_state_in, int64_t B, int64_t H, int64_t N, int64_t D, int64_t M,
+                     cp_dtype_t dtype, void* workspace, size_t workspace_bytes, void* stream_,
+                     bool use_ckpt) {
   cp_status_t st = cp::check_dims(B, H, N, D, M, dtype);
+  if (st != CP_OK) return st;
+  const CkptPlan ck = use_ckpt ? call_ckpt_plan(B, H, N, D, M, dtype) : CkptPlan{};
+  st = check_ckpt(ck, ckpt, ckpt_bytes);
   if (st != CP_OK) return st;
   if (N > 0 && (!q || !k || !v || !grad_out || !grad_q || !grad_k || !grad_v))
     return CP_ERR_INVALID_ARG;
@@ -338,6 +419,10 @@ cp_status_t causal_product_bwd_state(const void* q, const void* k, const void* v
       if (cp::overlaps(outs[o], out_sz[o], ins[i], in_sz[i])) return CP_ERR_INVALID_ARG;
     for (int o2 = o + 1; o2 < 4; ++o2)
       if (cp::overlaps(outs[o], out_sz[o], outs[o2], out_sz[o2])) return CP_ERR_INVALID_ARG;
+  }
+  if (ck.G > 1) {
+    for (int o = 0; o < 4; ++o)
+      if (cp::overlaps(outs[o], out_sz[o], ckpt, ck.bytes)) return CP_ERR_INVALID_ARG;
   }
   const size_t need = cp::workspace_bytes(BH, N, D, M, dtype, true);
   if (workspace != nullptr && workspace_bytes < need) return CP_ERR_WORKSPACE_TOO_SMALL;
@@ -373,13 +458,57 @@ cp_status_t causal_product_bwd_state(const void* q, const void* k, const void* v
     if (cp::tc_dkdv_supported(plan))
       return cp::tc_bwd_launch(q, k, v, grad_out, grad_q, grad_k, grad_v, state_in,
                                grad_state_out, grad_state_in, BH, N, D, M, plan, agg, status,
-                               stream);
+                               ck.G > 1 ? ckpt : nullptr, ck, stream);
+    // dq: every segment seeded from the forward's checkpoints
+    if (ck.G > 1) cp::seed_from_ckpt(pq, ckpt, ck);
+    // dk's reverse state R^T is the transpose of dv's R: when dv's scan is
+    // split with one value block, dk's segments start from dv's segment
+    // prefixes (left in the aggregate area, read transposed) instead of
+    // running a segment-sum pass of their own
+    const cp::TcPlan pvp = cp::tc_plan(BH, N, D, M);
+    if (pvp.ok && pvp.G > 1 && pvp.n_mb == 1 && grad_state_out == nullptr) {
+      pk.seed = agg;
+      pk.seed_G = pvp.G;
+      pk.seed_tiles = pvp.seg_tiles;
+      pk.seed_bh = (int64_t)pvp.G * pvp.DP * pvp.MB;
+      pk.seed_seg = (int64_t)pvp.DP * pvp.MB;
+      pk.seed_seg_off = 0;
+      pk.state_in = nullptr;
+      pk.st_ld_r = 1;
+      pk.st_ld_c = pvp.MB;
+    }
   }
   st = cp::run_product(pq, dtype, agg, status, stream);
   if (st != CP_OK) return st;
   st = cp::run_product(pv, dtype, agg, status, stream);
   if (st == CP_OK) st = cp::run_product(pk, dtype, agg, status, stream);
   return st;
+}
+
+}  // namespace
+}  // namespace cp
+
+extern "C" {
+
+cp_status_t causal_product_bwd_state(const void* q, const void* k, const void* v,
+                                     const void* grad_out, const float* state_in,
+                                     const float* grad_state_out, void* grad_q, void* grad_k,
+                                     void* grad_v, float* grad_state_in, int64_t B, int64_t H,
+                                     int64_t N, int64_t D, int64_t M, cp_dtype_t dtype,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+  return cp::bwd_impl(q, k, v, grad_out, state_in, grad_state_out, nullptr, 0, grad_q, grad_k,
+                      grad_v, grad_state_in, B, H, N, D, M, dtype, workspace, workspace_bytes,
+                      stream, false);
+}
+
+cp_status_t causal_product_bwd_ckpt(const void* q, const void* k, const void* v,
+                                    const void* grad_out, const float* ckpt, size_t ckpt_bytes,
+                                    void* grad_q, void* grad_k, void* grad_v, int64_t B,
+                                    int64_t H, int64_t N, int64_t D, int64_t M, cp_dtype_t dtype,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+  return cp::bwd_impl(q, k, v, grad_out, nullptr, nullptr, ckpt, ckpt_bytes, grad_q, grad_k,
+                      grad_v, nullptr, B, H, N, D, M, dtype, workspace, workspace_bytes, stream,
+                      true);
 }
 
 cp_status_t causal_product_bwd(const void* q, const void* k, const void* v, const void* grad_out,

@@ -27,6 +27,17 @@ namespace cp {
 constexpr int kPlanSMs = 152;
 constexpr size_t kStatusBytes = 256;
 
+// Checkpoints a bf16 forward product leaves for the backward's dq product:
+// the state before every `tiles`-th 128-row tile, G - 1 of them per
+// problem, fp32 [BH][G - 1][D][M] (the carried-state layout).  The dq
+// product runs in G segments of `tiles` tiles, segment s > 0 seeded from
+// checkpoint s.  G < 2: no checkpoints.
+struct CkptPlan {
+  int tiles = 0;
+  int G = 1;
+  size_t bytes = 0;
+};
+
 struct Product {
   const void* q;
   const void* k;
@@ -46,7 +57,31 @@ struct Product {
   int feature = 0;
   // element type of q, k, v and out (the fp32 SIMT path also takes fp16)
   cp_dtype_t dtype = CP_DTYPE_F32;
+  // bf16 forward: write checkpoints (ck geometry) into ckpt
+  CkptPlan ck;
+  float* ckpt = nullptr;
+  // bf16: run in seed_G segments of seed_tiles tiles, every segment but the
+  // first in scan order starting from a precomputed state (instead of a
+  // segment-sum pass): element (r, c) of the start of segment s of problem
+  // p at seed[p * seed_bh + (s + seed_seg_off) * seed_seg + r * st_ld_r +
+  // c * st_ld_c]; no carried state besides
+  const float* seed = nullptr;
+  int seed_G = 0, seed_tiles = 0;
+  int64_t seed_bh = 0, seed_seg = 0;
+  int seed_seg_off = 0;
 };
+
+// The dq product (g, v, k) of a backward seeded from a forward's checkpoints
+// (fp32 [BH][G - 1][D][M] with D = p.M, M = p.D: checkpoint s is the state
+// before segment s, read transposed through the product's strides).
+inline void seed_from_ckpt(Product& p, const float* ckpt, const CkptPlan& ck) {
+  p.seed = ckpt;
+  p.seed_G = ck.G;
+  p.seed_tiles = ck.tiles;
+  p.seed_bh = (int64_t)(ck.G - 1) * p.D * p.M;
+  p.seed_seg = p.D * p.M;
+  p.seed_seg_off = -1;
+}
 
 // ---- fp32 (SIMT FMA) path, also for fp16 inputs (widened on load)
 struct SimtPlan {
@@ -73,6 +108,8 @@ struct TcPlan {
   bool ok;
 };
 TcPlan tc_plan(int64_t BH, int64_t N, int64_t D, int64_t M);
+// Checkpoint plan of a bf16 problem (pure host computation, 152-SM part).
+CkptPlan ckpt_plan(int64_t BH, int64_t N, int64_t D, int64_t M);
 cp_status_t tc_launch(const Product& p, const TcPlan& plan, float* agg, int* status,
                       cudaStream_t stream);
 // Only pass 1 of the two-pass scan (a no-op when plan.G == 1).  On return
@@ -89,7 +126,10 @@ cudaError_t seg_prefix_launch(float* agg, int64_t P, int G, int64_t E, bool reve
 
 // Backward pass for bf16 with D, M <= 64 (tc_dkdv_supported(plan), plan =
 // tc_plan(BH, N, D, M)): dq is one product launch; dk and dv share the
-// reverse state sum q g^T and are computed in one scan.
+// reverse state sum q g^T and are computed in one scan.  With checkpoints
+// (ckpt non-null, ck.G > 1, no S_0) the dq scans are segments seeded from
+// them.  `status` is the workspace header: its word 0 is the status word and
+// words 2 and 3 the dq ticket counters of the one-launch backward.
 bool tc_dkdv_supported(const TcPlan& plan);
 // state_in (S_0), grad_state_out (dL/dS_N) and grad_state_in (dL/dS_0) are
 // [BH][D][M] fp32 or null.
@@ -97,7 +137,8 @@ cp_status_t tc_bwd_launch(const void* q, const void* k, const void* v, const voi
                           void* dk, void* dv, const float* state_in,
                           const float* grad_state_out, float* grad_state_in, int64_t BH,
                           int64_t N, int64_t D, int64_t M, const TcPlan& plan, float* agg,
-                          int* status, cudaStream_t stream);
+                          int* status, const float* ckpt, const CkptPlan& ck,
+                          cudaStream_t stream);
 
 // ---- decoding step (SIMT): S += k v^T, out = S^T q for every problem;
 // M <= 256

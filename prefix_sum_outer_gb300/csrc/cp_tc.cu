@@ -12,22 +12,22 @@
 namespace cp {
 namespace tc {
 
-template <int DP, int MB, bool AGG_ONLY, bool STATE_OUT, bool FEAT>
+template <int DP, int MB, bool AGG_ONLY, bool STATE_OUT, bool FEAT, bool CKPT>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_o, const Args a) {
-  causal_body<DP, MB, AGG_ONLY, STATE_OUT, FEAT>(tm_q, tm_k, tm_v, tm_o, a,
-                                                 Phase{(int)blockIdx.x, true, true});
+  causal_body<DP, MB, AGG_ONLY, STATE_OUT, FEAT, CKPT>(tm_q, tm_k, tm_v, tm_o, a,
+                                                       Phase{(int)blockIdx.x, true, true});
 }
 
 // ------------------------------------------------------------------ host
-template <int DP, int MB, bool AGG, bool STATE_OUT = false, bool FEAT = false>
+template <int DP, int MB, bool AGG, bool STATE_OUT = false, bool FEAT = false, bool CKPT = false>
 cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                        const CUtensorMap& o, const Args& a, unsigned grid, cudaStream_t st) {
   using L = Layout<DP, MB, AGG>;
-  auto kern = tc_causal_kernel<DP, MB, AGG, STATE_OUT, FEAT>;
+  auto kern = tc_causal_kernel<DP, MB, AGG, STATE_OUT, FEAT, CKPT>;
   // the shared-memory opt-in is set once per device for each instantiation
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
@@ -75,10 +75,21 @@ cudaError_t launch_pair(const CUtensorMap& q, const CUtensorMap& k, const CUtens
     return cudaSuccess;
   }
   const unsigned g2 = (unsigned)(problems * plan.G);
-  // (a feature map is never combined with a carried state)
+  // (a feature map, a carried state and checkpoints are never combined)
   if (a.feature) return launch_one<DP, MB, false, false, true>(q, k, v, o, a, g2, st);
   if (a.state_out != nullptr) return launch_one<DP, MB, false, true>(q, k, v, o, a, g2, st);
+  if (a.ckpt != nullptr) return launch_one<DP, MB, false, false, false, true>(q, k, v, o, a, g2, st);
   return launch_one<DP, MB, false>(q, k, v, o, a, g2, st);
+}
+
+// The scan pass alone, every segment seeded from a precomputed slot
+// (checkpoints a forward product left): agg_in holds [P][G][DP][MB] with
+// slot s the state before segment s.
+template <int DP, int MB>
+cudaError_t launch_seeded(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                          const CUtensorMap& o, const Args& a, int64_t problems,
+                          cudaStream_t st) {
+  return launch_one<DP, MB, false>(q, k, v, o, a, (unsigned)(problems * a.G), st);
 }
 
 }  // namespace tc
@@ -107,6 +118,29 @@ TcPlan tc_plan(int64_t BH, int64_t N, int64_t D, int64_t M) {
   return p;
 }
 
+CkptPlan ckpt_plan(int64_t BH, int64_t N, int64_t D, int64_t M) {
+  CkptPlan c;
+  const TcPlan fp = tc_plan(BH, N, D, M);
+  const TcPlan qp = tc_plan(BH, N, M, D);  // the dq product (g, v, k)
+  if (!fp.ok || !qp.ok || qp.n_tiles < 2) return c;
+  int tiles = 0;
+  if (qp.G > 1) {
+    // dq is split into segments anyway: the checkpoints replace its
+    // segment-sum pass and the prefix between the passes.  (The one-launch
+    // backward keeps whole dq scans: measured on B=8 H=16 N=4096 D=M=64, a
+    // dq scan cut into 2, 4 or 8 seeded segments made that launch 8, 8 and
+    // 31 us slower, each extra scan start and drain costing about 7 us.)
+    tiles = qp.seg_tiles;
+  }
+  if (tiles < 1) return c;
+  const int G = (qp.n_tiles + tiles - 1) / tiles;
+  if (G < 2) return c;
+  c.tiles = tiles;
+  c.G = G;
+  c.bytes = sizeof(float) * (size_t)BH * (G - 1) * D * M;
+  return c;
+}
+
 namespace {
 cp_status_t tc_run(const Product& p, const TcPlan& plan, float* agg, int* status,
                    cudaStream_t stream, bool agg_only) {
@@ -131,12 +165,31 @@ cp_status_t tc_run(const Product& p, const TcPlan& plan, float* agg, int* status
   a.Dr = (int)p.D;
   a.Mc = (int)p.M;
   a.feature = p.feature;
+  a.ckpt = p.ckpt;
+  a.ck_tiles = p.ck.tiles;
+  a.ck_G = p.ck.G;
   const int64_t problems = p.BH * plan.n_mb;
+  const bool seeded = p.seed != nullptr;
+  if (seeded) {
+    // segments each seeded from a precomputed state (read through the
+    // carried-state strides; no carried state besides)
+    if (agg_only || p.seed_G < 2 || p.seed_tiles < 1 || p.state_in != nullptr || p.feature ||
+        (int64_t)(p.seed_G - 1) * p.seed_tiles >= plan.n_tiles)
+      return CP_ERR_INVALID_ARG;
+    a.G = p.seed_G;
+    a.seg_tiles = p.seed_tiles;
+    a.agg_in = nullptr;
+    a.seed = p.seed;
+    a.seed_bh = p.seed_bh;
+    a.seed_seg = p.seed_seg;
+    a.seed_seg_off = p.seed_seg_off;
+  }
   cudaError_t e;
 #define CP_TC_CASE(DP_, MB_)                                                                  \
   if (plan.DP == DP_ && plan.MB == MB_)                                                       \
-    e = tc::launch_pair<DP_, MB_>(mq, mk, mv, mo, a, plan, problems, agg, agg_only,  \
-                                   stream);            \
+    e = seeded ? tc::launch_seeded<DP_, MB_>(mq, mk, mv, mo, a, problems, stream)             \
+               : tc::launch_pair<DP_, MB_>(mq, mk, mv, mo, a, plan, problems, agg, agg_only,  \
+                                           stream);                                           \
   else
   CP_TC_CASE(64, 64)
   CP_TC_CASE(64, 128)

@@ -84,6 +84,20 @@ struct Args {
   int64_t st_ld_r, st_ld_c;
   int Dr, Mc;
   int feature;  // 0: q, k used as given; 1: phi = elu + 1 (FEAT instantiation)
+  // Checkpoints of the state every ck_tiles tiles, in the caller's state
+  // layout: ckpt[((bh * (ck_G - 1) + s - 1) * Dr + d) * Mc + m] is element
+  // (d, m) of the state before tile s * ck_tiles, s = 1 .. ck_G - 1.  A
+  // forward product with ckpt set (CKPT instantiation) writes them.
+  float* ckpt;
+  int ck_tiles, ck_G;
+  // Seeded segments: with seed set, every segment but the first in scan
+  // order starts from a precomputed state instead of a segment-sum pass:
+  // element (r, c) of the start of segment seg of problem bh is
+  // seed[bh * seed_bh + (seg + seed_seg_off) * seed_seg + r * st_ld_r + c * st_ld_c]
+  // (the carried-state strides; no carried state besides).
+  const float* seed;
+  int64_t seed_bh, seed_seg;
+  int seed_seg_off;
 };
 
 // phi(x) = elu(x) + 1 on a pair of bf16 values, in packed bf16x2
@@ -175,8 +189,9 @@ struct Layout {
 // the launch writes the final state (a separate instantiation: the write,
 // though it runs once, costs the whole kernel registers).
 // FEAT: q and k are raw inputs mapped by phi = elu + 1 in shared memory.
+// CKPT: a forward product writes its state at every checkpoint boundary.
 // Returns false when a wait gave up.
-template <int DP, int MB, bool AGG_ONLY, bool STATE_OUT, bool FEAT = false>
+template <int DP, int MB, bool AGG_ONLY, bool STATE_OUT, bool FEAT = false, bool CKPT = false>
 __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                             const CUtensorMap& tm_v, const CUtensorMap& tm_o,
                                             const Args& a, const Phase ph) {
@@ -238,8 +253,12 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
   const int pidx = bh * a.n_mb + mb;
   const bool has_prefix =
       !AGG_ONLY && a.agg_in != nullptr && (a.reverse ? (seg < a.G - 1) : (seg > 0));
-  // the state does not start at zero: earlier segments or a carried state
-  const bool has_init = has_prefix || (!AGG_ONLY && a.state_in != nullptr);
+  // a segment seeded from a precomputed state
+  const bool seeded =
+      !AGG_ONLY && a.seed != nullptr && (a.reverse ? (seg < a.G - 1) : (seg > 0));
+  // the state does not start at zero: earlier segments, a checkpoint or a
+  // carried state
+  const bool has_init = has_prefix || seeded || (!AGG_ONLY && a.state_in != nullptr);
   const bool last_seg = a.reverse ? (seg == 0) : (seg == a.G - 1);
   auto tile_of = [&](int it) { return a.reverse ? (t_end - 1 - it) : (t_first + it); };
 
@@ -296,6 +315,17 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
   const int wq = warp & 3;                 // TMEM lane quarter of this warp
   const int row = wq * 32 + lane;          // tile row = TMEM lane
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+
+  // CKPT: checkpoint s (>= 1) is the state before tile s * ck_tiles; 0
+  // when the boundary before `tile` holds none (the start of the sequence)
+  auto ckpt_slot = [&](int tile) -> int {
+    if (!CKPT || a.reverse || tile <= 0 || tile >= a.n_tiles) return 0;
+    return tile % a.ck_tiles == 0 ? tile / a.ck_tiles : 0;
+  };
+  // CKPT: row d of checkpoint s, columns m0 .. m0 + 31 of this value block
+  auto ckpt_row = [&](int s_slot, int d, int m0) -> float* {
+    return a.ckpt + (((size_t)bh * (a.ck_G - 1) + s_slot - 1) * a.Dr + d) * a.Mc + m0;
+  };
 
   // FEAT: phi applied in place to the landed Q/K tiles of tile it (K only in
   // the aggregate-only mode, which loads no Q) by the kMapWarps mapping
@@ -586,7 +616,9 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
       if (has_init) {
         const int lo = has_prefix ? seg : 0;
         const int hi = has_prefix ? seg + 1 : 0;
-        const float* st = a.state_in != nullptr ? a.state_in + (int64_t)bh * a.Dr * a.Mc : nullptr;
+        const float* st =
+            seeded ? a.seed + (int64_t)bh * a.seed_bh + (int64_t)(seg + a.seed_seg_off) * a.seed_seg
+                   : (a.state_in != nullptr ? a.state_in + (int64_t)bh * a.Dr * a.Mc : nullptr);
 #pragma unroll
         for (int sb = 0; sb < L::kSBlocks; ++sb) {
           if (sb * 128 + wq * 32 >= DP) continue;
@@ -663,7 +695,73 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(s_ready);
+        // CKPT: the state before this tile is a checkpoint.  It is written
+        // off the state chain, after the copy is handed on, from the hi + lo
+        // copy this thread wrote (hi + lo carries 16 significant bits: the
+        // precision the Q S operands use), which stays put until the copy
+        // after the next NSB - 1 tiles.
+        if (CKPT && L::kSplit && it > 0) {
+          const int slot = ckpt_slot(tile_of(it));
+          if (slot > 0) {
+#pragma unroll 1
+            for (int sb = 0; sb < L::kSBlocks; ++sb) {
+              const int d = sb * 128 + row;
+              if (sb * 128 + wq * 32 >= DP || d >= a.Dr) continue;
+#pragma unroll 1
+              for (int c8 = 0; c8 < MB / 8; ++c8) {
+                const int m0 = mb * MB + c8 * 8;
+                if (m0 + 8 > a.Mc) break;
+                const uint32_t off = sw128_offset(d, c8 * 8, DP * 128);
+                const uint4 h = *reinterpret_cast<const uint4*>(sbuf + off);
+                const uint4 l = *reinterpret_cast<const uint4*>(sbuf + L::kSOneBytes + off);
+                const uint32_t hw[4] = {h.x, h.y, h.z, h.w}, lw[4] = {l.x, l.y, l.z, l.w};
+                float f[8];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  f[2 * u] = __uint_as_float(hw[u] << 16) + __uint_as_float(lw[u] << 16);
+                  f[2 * u + 1] = __uint_as_float(hw[u] & 0xffff0000u) +
+                                 __uint_as_float(lw[u] & 0xffff0000u);
+                }
+                float4* dst = reinterpret_cast<float4*>(ckpt_row(slot, d, m0));
+                dst[0] = make_float4(f[0], f[1], f[2], f[3]);
+                dst[1] = make_float4(f[4], f[5], f[6], f[7]);
+              }
+            }
+          }
+        }
 
+      }
+      // CKPT: a checkpoint boundary right after this segment's last tile
+      // (the state is exact here: no copy follows it)
+      if (CKPT && ok && n_it > 0 && ckpt_slot(tile_of(n_it - 1) + 1) > 0) {
+        if (!mbar_wait(s_done, (n_it - 1) & 1, abort_flag)) {
+          ok = false;
+        } else {
+          tc_fence_after();
+          const int slot = ckpt_slot(tile_of(n_it - 1) + 1);
+#pragma unroll 1
+          for (int sb = 0; sb < L::kSBlocks; ++sb) {
+            const int d = sb * 128 + row;
+            if (sb * 128 + wq * 32 >= DP) continue;  // warp-uniform
+#pragma unroll 1
+            for (int c = 0; c < MB / 32; ++c) {
+              uint32_t r[32];
+              tmem_ld32(lane_base + L::kColS + sb * MB + c * 32, r);
+              tmem_ld_wait();
+              const int m0 = mb * MB + c * 32;
+              if (d >= a.Dr) continue;
+#pragma unroll
+              for (int x8 = 0; x8 < 4; ++x8) {
+                if (m0 + 8 * x8 + 8 > a.Mc) break;
+                float4* dst = reinterpret_cast<float4*>(ckpt_row(slot, d, m0 + 8 * x8));
+                dst[0] = make_float4(__uint_as_float(r[8 * x8]), __uint_as_float(r[8 * x8 + 1]),
+                                     __uint_as_float(r[8 * x8 + 2]), __uint_as_float(r[8 * x8 + 3]));
+                dst[1] = make_float4(__uint_as_float(r[8 * x8 + 4]), __uint_as_float(r[8 * x8 + 5]),
+                                     __uint_as_float(r[8 * x8 + 6]), __uint_as_float(r[8 * x8 + 7]));
+              }
+            }
+          }
+        }
       }
       // the last segment in scan order hands on the state after its last tile
       if (STATE_OUT && ok && last_seg && n_it > 0) {

@@ -96,18 +96,26 @@ def test_launch_count(lib):
     assert lc(8, 16, 4096, 64, 64, BF16, 0) == 1
     assert lc(8, 16, 4096, 64, 64, BF16, 1) == 1
     # 16 problems of 32768 rows: every scan split (sums, prefix, scan),
-    # three products in the backward
+    # three products in the backward, dk seeded from dv's segment prefixes
+    # (one launch); with checkpoints dq is one seeded launch too
     assert lc(2, 8, 32768, 128, 128, BF16, 0) == 3
-    assert lc(2, 8, 32768, 128, 128, BF16, 1) == 9
+    assert lc(2, 8, 32768, 128, 128, BF16, 1) == 7
+    assert lc(2, 8, 32768, 128, 128, BF16, 2) == 3
+    assert lc(2, 8, 32768, 128, 128, BF16, 3) == 5
     assert lc(4, 8, 8229, 256, 64, BF16, 0) == 3
-    assert lc(4, 8, 8229, 256, 64, BF16, 1) == 9
+    assert lc(4, 8, 8229, 256, 64, BF16, 1) == 7
+    assert lc(4, 8, 8229, 256, 64, BF16, 3) == 5
+    assert lc(8, 16, 4096, 64, 64, BF16, 3) == 1
+    assert lc(8, 16, 4096, 64, 64, BF16, 4) == -1
     # fp32: 32 problems of 32 tiles split 16 ways; one 64-row tile unsplit
     assert lc(4, 8, 1024, 64, 64, F32, 0) == 3
     assert lc(4, 8, 1024, 64, 64, F32, 1) == 9
     assert lc(1, 2, 64, 16, 16, F32, 0) == 1
     assert lc(1, 2, 64, 16, 16, F32, 1) == 3
-    # bf16 D = M = 64 split: dq product (3), reverse sums + prefix, dk/dv scan
+    # bf16 D = M = 64 split: dq product (3), reverse sums + prefix, dk/dv scan;
+    # with checkpoints dq is one seeded launch
     assert lc(1, 2, 8192, 64, 64, BF16, 1) == 6
+    assert lc(1, 2, 8192, 64, 64, BF16, 3) == 4
     # many problems: fused dk/dv scan on its own launch after dq
     assert lc(16, 16, 1024, 64, 64, BF16, 1) == 2
     assert lc(1, 1, 0, 64, 64, BF16, 1) == 0
@@ -120,6 +128,32 @@ A = 1 << 20  # a 16-byte-aligned fake device address; never dereferenced here
 def fwd(lib, q=A, k=2 * A, v=3 * A, out=4 * A, B=1, H=1, N=16, D=16, M=16, dtype=F32,
         ws=None, ws_bytes=0):
     return lib.causal_product_fwd(q, k, v, out, B, H, N, D, M, dtype, ws, ws_bytes, None)
+
+
+def test_checkpoint_calls(lib):
+    """Checkpoint sizes and the argument checks of the checkpoint calls."""
+    size = lib.causal_product_checkpoint_size
+    # split dq (16 problems of 256 tiles, 9 segments): 8 checkpoints of D x M
+    assert size(2, 8, 32768, 128, 128, BF16) == 4 * 16 * 8 * 128 * 128
+    # the one-launch backward keeps whole dq scans; fp32 has none; rejects: 0
+    assert size(8, 16, 4096, 64, 64, BF16) == 0
+    assert size(1, 2, 8192, 64, 64, F32) == 0
+    assert size(1, 1, 16, 12, 16, BF16) == 0
+    n = size(1, 2, 8192, 64, 64, BF16)
+    assert n > 0 and n % (4 * 2 * 64 * 64) == 0
+    fck, bck = lib.causal_product_fwd_ckpt, lib.causal_product_bwd_ckpt
+    args = (1, 2, 8192, 64, 64, BF16, None, 0, None)
+    assert fck(A, 2 * A, 3 * A, 4 * A, None, 0, *args) == INVALID_ARG
+    assert fck(A, 2 * A, 3 * A, 4 * A, 5 * A, n - 16, *args) == WS_TOO_SMALL
+    assert fck(A, 2 * A, 3 * A, 4 * A, 5 * A + 4, n, *args) == MISALIGNED
+    # the checkpoints may not overlap the output
+    assert fck(A, 2 * A, 3 * A, 4 * A, 4 * A + 64, n, *args) == INVALID_ARG
+    assert bck(A, 2 * A, 3 * A, 4 * A, None, 0, 5 * A, 6 * A, 7 * A, *args) == INVALID_ARG
+    assert bck(A, 2 * A, 3 * A, 4 * A, 8 * A, n - 16, 5 * A, 6 * A, 7 * A, *args) == WS_TOO_SMALL
+    # ... nor a gradient
+    assert bck(A, 2 * A, 3 * A, 4 * A, 5 * A, n, 5 * A, 6 * A, 7 * A, *args) == INVALID_ARG
+    # without rows nothing is needed
+    assert fck(A, 2 * A, 3 * A, 4 * A, None, 0, 1, 2, 0, 64, 64, BF16, None, 0, None) == OK
 
 
 def test_fwd_argument_checks(lib):
