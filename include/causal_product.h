@@ -308,6 +308,39 @@ CP_API cp_status_t causal_product_normalizer_bwd_feature(const void* q, const vo
                                                          void* workspace, size_t workspace_bytes,
                                                          void* stream);
 
+/* Positive random features (the Performer feature map "FAVOR+"; the pages
+ * of triton-lang/triton issue #217 offer the causal product as a drop-in for
+ * the Performers code):
+ *     phi(x)_d = exp(w_d . x - |x|^2 / 2) / sqrt(D),   d = 0 .. D-1,
+ *     out_i    = sum_{j<=i} (phi(xq_i) . phi(xk_j)) v_j,
+ * from the raw rows xq, xk [B][H][N][R] and one projection W [D][R] (row d is
+ * w_d) shared by every row and (b,h).  bf16 only: xq, xk, v, W, out (and the
+ * gradients) are bf16 device pointers, 16-byte aligned; R in 8 .. 64 (a
+ * multiple of 8), D in 64 .. 256 (a multiple of 64), M as for
+ * causal_product_fwd.  The features are computed on the tensor cores (X W^T,
+ * fp32 accumulation), exponentiated in fp32 and rounded to bf16 once.
+ * causal_product_bwd_favor writes dL/dxq, dL/dxk (with respect to the raw
+ * rows, W fixed: dL/dx = sum_d a_d phi_d (w_d - x), a = dL/dphi) and dL/dv.
+ * Workspace: causal_product_favor_workspace_size(..., backward) bytes (NULL:
+ * allocated on `stream`); it holds phi(xq), phi(xk) (and, backward, their
+ * gradients).  CP_ERR_UNSUPPORTED_DTYPE for fp32/fp16,
+ * CP_ERR_UNSUPPORTED_SHAPE for R or D out of range; otherwise errors as
+ * causal_product_fwd.  N = 0 enqueues nothing. */
+CP_API size_t causal_product_favor_workspace_size(int64_t B, int64_t H, int64_t N, int64_t R,
+                                                  int64_t D, int64_t M, cp_dtype_t dtype,
+                                                  int backward);
+CP_API cp_status_t causal_product_fwd_favor(const void* xq, const void* xk, const void* v,
+                                            const void* W, void* out, int64_t B, int64_t H,
+                                            int64_t N, int64_t R, int64_t D, int64_t M,
+                                            cp_dtype_t dtype, void* workspace,
+                                            size_t workspace_bytes, void* stream);
+CP_API cp_status_t causal_product_bwd_favor(const void* xq, const void* xk, const void* v,
+                                            const void* W, const void* grad_out, void* grad_xq,
+                                            void* grad_xk, void* grad_v, int64_t B, int64_t H,
+                                            int64_t N, int64_t R, int64_t D, int64_t M,
+                                            cp_dtype_t dtype, void* workspace,
+                                            size_t workspace_bytes, void* stream);
+
 /* Size of the static device scratch array behind causal_product_fwd_noalloc. */
 #define CP_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 

@@ -33,6 +33,7 @@ __all__ = [
     "causal_product_fwd_feature", "causal_product_bwd_feature", "FEATURES",
     "causal_product_workspace_size", "causal_product_launch_count", "causal_product_status",
     "causal_product_checkpoint_size", "causal_product_fwd_ckpt", "causal_product_bwd_ckpt",
+    "causal_product_fwd_favor", "causal_product_bwd_favor", "causal_product_favor",
     "causal_product_error_string", "library_path", "load_library",
 ]
 
@@ -128,6 +129,15 @@ def load_library(rebuild: bool = True) -> ctypes.CDLL:
             lib.causal_product_normalizer_bwd_feature.argtypes = [p, p, p, p, p, c_int, i64, i64,
                                                                   i64, i64, c_int, p, sz, p]
             lib.causal_product_normalizer_bwd_feature.restype = c_int
+            lib.causal_product_favor_workspace_size.argtypes = [i64, i64, i64, i64, i64, i64,
+                                                                c_int, c_int]
+            lib.causal_product_favor_workspace_size.restype = sz
+            lib.causal_product_fwd_favor.argtypes = [p, p, p, p, p, i64, i64, i64, i64, i64, i64,
+                                                     c_int, p, sz, p]
+            lib.causal_product_fwd_favor.restype = c_int
+            lib.causal_product_bwd_favor.argtypes = [p, p, p, p, p, p, p, p, i64, i64, i64, i64,
+                                                     i64, i64, c_int, p, sz, p]
+            lib.causal_product_bwd_favor.restype = c_int
             lib.causal_product_status.argtypes = [p, p]
             lib.causal_product_status.restype = c_int
             lib.causal_product_error_string.argtypes = [c_int]
@@ -409,6 +419,74 @@ def causal_product_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor
     return out
 
 
+def _favor_dims(xq: torch.Tensor, xk: torch.Tensor, v: torch.Tensor, W: torch.Tensor):
+    if (xq.dim() != 4 or xk.shape != xq.shape or v.dim() != 4 or v.shape[:3] != xq.shape[:3]
+            or W.dim() != 2 or W.shape[1] != xq.shape[3]):
+        raise ValueError(f"expected xq, xk [B,H,N,R], v [B,H,N,M], W [D,R]; got {tuple(xq.shape)}, "
+                         f"{tuple(xk.shape)}, {tuple(v.shape)}, {tuple(W.shape)}")
+    B, H, N, R = xq.shape
+    return B, H, N, R, W.shape[0], v.shape[3]
+
+
+def causal_product_fwd_favor(xq: torch.Tensor, xk: torch.Tensor, v: torch.Tensor,
+                             W: torch.Tensor, out: Optional[torch.Tensor] = None,
+                             workspace: Optional[torch.Tensor] = None,
+                             stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """out_i = sum_{j<=i} (phi(xq_i) . phi(xk_j)) v_j with the positive random
+    features phi(x) = exp(W x - |x|^2 / 2) / sqrt(D), computed in the kernels
+    from the raw rows xq, xk [B,H,N,R] and the projection W [D,R] (bf16)."""
+    B, H, N, R, D, M = _favor_dims(xq, xk, v, W)
+    code = _dtype_code(xq, xk, v, W)
+    if out is None:
+        out = torch.empty((B, H, N, M), dtype=v.dtype, device=v.device)
+    _check_like(out, (B, H, N, M), v.dtype, "out")
+    _check_device(xq, xk, v, W, out)
+    lib = load_library()
+    need = lib.causal_product_favor_workspace_size(B, H, N, R, D, M, code, 0)
+    if workspace is None:
+        workspace = _workspace(need, v.device)
+    rc = lib.causal_product_fwd_favor(xq.data_ptr(), xk.data_ptr(), v.data_ptr(), W.data_ptr(),
+                                      out.data_ptr(), B, H, N, R, D, M, code,
+                                      workspace.data_ptr(), workspace.numel(),
+                                      _stream_ptr(stream, v.device))
+    if rc != CP_OK:
+        raise CausalProductError(rc, "causal_product_fwd_favor")
+    return out
+
+
+def causal_product_bwd_favor(xq: torch.Tensor, xk: torch.Tensor, v: torch.Tensor,
+                             W: torch.Tensor, grad_out: torch.Tensor,
+                             grad_xq: Optional[torch.Tensor] = None,
+                             grad_xk: Optional[torch.Tensor] = None,
+                             grad_v: Optional[torch.Tensor] = None,
+                             workspace: Optional[torch.Tensor] = None,
+                             stream: Optional[torch.cuda.Stream] = None):
+    """(dxq, dxk, dv) of L = <grad_out, out> for causal_product_fwd_favor (W
+    fixed)."""
+    B, H, N, R, D, M = _favor_dims(xq, xk, v, W)
+    code = _dtype_code(xq, xk, v, W, grad_out)
+    if grad_out.shape != v.shape:
+        raise ValueError("grad_out must have v's shape")
+    grad_xq = torch.empty_like(xq) if grad_xq is None else grad_xq
+    grad_xk = torch.empty_like(xk) if grad_xk is None else grad_xk
+    grad_v = torch.empty_like(v) if grad_v is None else grad_v
+    for t, ref, name in ((grad_xq, xq, "grad_xq"), (grad_xk, xk, "grad_xk"), (grad_v, v, "grad_v")):
+        _check_like(t, ref.shape, ref.dtype, name)
+    _check_device(xq, xk, v, W, grad_out, grad_xq, grad_xk, grad_v)
+    lib = load_library()
+    need = lib.causal_product_favor_workspace_size(B, H, N, R, D, M, code, 1)
+    if workspace is None:
+        workspace = _workspace(need, v.device)
+    rc = lib.causal_product_bwd_favor(xq.data_ptr(), xk.data_ptr(), v.data_ptr(), W.data_ptr(),
+                                      grad_out.data_ptr(), grad_xq.data_ptr(), grad_xk.data_ptr(),
+                                      grad_v.data_ptr(), B, H, N, R, D, M, code,
+                                      workspace.data_ptr(), workspace.numel(),
+                                      _stream_ptr(stream, v.device))
+    if rc != CP_OK:
+        raise CausalProductError(rc, "causal_product_bwd_favor")
+    return grad_xq, grad_xk, grad_v
+
+
 def causal_product_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, grad_out: torch.Tensor,
                        grad_q: Optional[torch.Tensor] = None,
                        grad_k: Optional[torch.Tensor] = None,
@@ -648,6 +726,31 @@ class CausalProductState(torch.autograd.Function):
         dq, dk, dv, ds = causal_product_bwd(q, k, v, g, state_in=state if ctx.has_state else None,
                                             grad_state_out=g_state, return_state_grad=True)
         return dq, dk, dv, (ds if ctx.has_state else None)
+
+
+class CausalProductFavor(torch.autograd.Function):
+    """Autograd wrapper of the positive-random-feature product: (xq, xk, v)
+    -> out for a fixed projection W (no gradient for W)."""
+
+    @staticmethod
+    def forward(ctx, xq, xk, v, W):
+        xq, xk, v, W = xq.contiguous(), xk.contiguous(), v.contiguous(), W.contiguous()
+        ctx.save_for_backward(xq, xk, v, W)
+        return causal_product_fwd_favor(xq, xk, v, W)
+
+    @staticmethod
+    def backward(ctx, g):
+        xq, xk, v, W = ctx.saved_tensors
+        dxq, dxk, dv = causal_product_bwd_favor(xq, xk, v, W, g.contiguous().to(v.dtype))
+        return dxq, dxk, dv, None
+
+
+def causal_product_favor(xq: torch.Tensor, xk: torch.Tensor, v: torch.Tensor,
+                         W: torch.Tensor) -> torch.Tensor:
+    """Causal product of the positive random features phi(x) = exp(W x -
+    |x|^2 / 2) / sqrt(D) of the raw rows xq, xk, with autograd support for
+    xq, xk and v (W is treated as a constant)."""
+    return CausalProductFavor.apply(xq, xk, v, W)
 
 
 def causal_product(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,

@@ -641,6 +641,150 @@ cp_status_t causal_product_normalizer_bwd(const void* q, const void* k, const fl
                                                N, D, dtype, workspace, workspace_bytes, stream);
 }
 
+}  // extern "C"
+
+namespace cp {
+namespace {
+
+cp_status_t check_favor(int64_t B, int64_t H, int64_t N, int64_t R, int64_t D, int64_t M,
+                        cp_dtype_t dtype) {
+  if (dtype != CP_DTYPE_BF16) return CP_ERR_UNSUPPORTED_DTYPE;
+  cp_status_t st = check_dims(B, H, N, D, M, dtype);
+  if (st != CP_OK) return st;
+  if (!favor_supported(R, D)) return CP_ERR_UNSUPPORTED_SHAPE;
+  return CP_OK;
+}
+
+// Workspace of the positive-random-feature calls: a header and the segment
+// sums of the products, then the features and (backward) their gradients.
+// Forward: phi(xq), phi(xk) as bf16 [BH][N][D].  Backward: [hi | lo] rows
+// of both features ([BH][N][2D]) and the gradients against them
+// ([BH][N][2D]).
+size_t favor_feat_bytes(int64_t BH, int64_t N, int64_t D, bool backward) {
+  return round_up((size_t)BH * N * D * 2 * (backward ? 2 : 1));
+}
+
+size_t favor_agg_bytes(int64_t BH, int64_t N, int64_t D, int64_t M, bool backward) {
+  if (!backward) return round_up(tc_plan(BH, N, D, M).agg_bytes);
+  return round_up(std::max(tc_plan(BH, N, M, 2 * D).agg_bytes, tc_plan(BH, N, D, M).agg_bytes));
+}
+
+size_t favor_ws_bytes(int64_t BH, int64_t N, int64_t D, int64_t M, bool backward) {
+  return kStatusBytes + favor_agg_bytes(BH, N, D, M, backward) +
+         (backward ? 4 : 2) * favor_feat_bytes(BH, N, D, backward);
+}
+
+}  // namespace
+}  // namespace cp
+
+extern "C" {
+
+size_t causal_product_favor_workspace_size(int64_t B, int64_t H, int64_t N, int64_t R, int64_t D,
+                                           int64_t M, cp_dtype_t dtype, int backward) {
+  if (cp::check_favor(B, H, N, R, D, M, dtype) != CP_OK) return 0;
+  return cp::favor_ws_bytes(B * H, N, D, M, backward != 0);
+}
+
+cp_status_t causal_product_fwd_favor(const void* xq, const void* xk, const void* v, const void* W,
+                                     void* out, int64_t B, int64_t H, int64_t N, int64_t R,
+                                     int64_t D, int64_t M, cp_dtype_t dtype, void* workspace,
+                                     size_t workspace_bytes, void* stream_) {
+  cp_status_t st = cp::check_favor(B, H, N, R, D, M, dtype);
+  if (st != CP_OK) return st;
+  if (N > 0 && (!xq || !xk || !v || !W || !out)) return CP_ERR_INVALID_ARG;
+  const void* ptrs[5] = {xq, xk, v, W, out};
+  for (const void* p : ptrs)
+    if (!cp::aligned16(p)) return CP_ERR_MISALIGNED;
+  const int64_t BH = B * H;
+  const size_t nx = (size_t)BH * N * R * 2, nv = (size_t)BH * N * M * 2, nw = (size_t)D * R * 2;
+  if (cp::overlaps(out, nv, xq, nx) || cp::overlaps(out, nv, xk, nx) ||
+      cp::overlaps(out, nv, v, nv) || cp::overlaps(out, nv, W, nw))
+    return CP_ERR_INVALID_ARG;
+  const size_t need = cp::favor_ws_bytes(BH, N, D, M, false);
+  if (workspace != nullptr && workspace_bytes < need) return CP_ERR_WORKSPACE_TOO_SMALL;
+  if (N == 0) return CP_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  cp::Scratch s;
+  st = cp::acquire(s, workspace, workspace_bytes, need, stream);
+  if (st != CP_OK) return st;
+  int* status = static_cast<int*>(s.base);
+  float* agg = reinterpret_cast<float*>(static_cast<char*>(s.base) + cp::kStatusBytes);
+  const size_t feat = cp::favor_feat_bytes(BH, N, D, false);
+  char* fq = static_cast<char*>(s.base) + cp::kStatusBytes + cp::favor_agg_bytes(BH, N, D, M, false);
+  char* fk = fq + feat;
+  st = cp::favor_map_launch(xq, W, fq, BH, N, R, D, false, status, stream);
+  if (st == CP_OK) st = cp::favor_map_launch(xk, W, fk, BH, N, R, D, false, status, stream);
+  if (st != CP_OK) return st;
+  cp::Product p{fq, fk, v, out, BH, N, D, M, false};
+  return cp::run_product(p, CP_DTYPE_BF16, agg, status, stream);
+}
+
+cp_status_t causal_product_bwd_favor(const void* xq, const void* xk, const void* v, const void* W,
+                                     const void* grad_out, void* grad_xq, void* grad_xk,
+                                     void* grad_v, int64_t B, int64_t H, int64_t N, int64_t R,
+                                     int64_t D, int64_t M, cp_dtype_t dtype, void* workspace,
+                                     size_t workspace_bytes, void* stream_) {
+  cp_status_t st = cp::check_favor(B, H, N, R, D, M, dtype);
+  if (st != CP_OK) return st;
+  if (N > 0 && (!xq || !xk || !v || !W || !grad_out || !grad_xq || !grad_xk || !grad_v))
+    return CP_ERR_INVALID_ARG;
+  const void* ptrs[8] = {xq, xk, v, W, grad_out, grad_xq, grad_xk, grad_v};
+  for (const void* p : ptrs)
+    if (!cp::aligned16(p)) return CP_ERR_MISALIGNED;
+  const int64_t BH = B * H;
+  const size_t nx = (size_t)BH * N * R * 2, nv = (size_t)BH * N * M * 2, nw = (size_t)D * R * 2;
+  const void* ins[5] = {xq, xk, v, W, grad_out};
+  const size_t in_sz[5] = {nx, nx, nv, nw, nv};
+  void* outs[3] = {grad_xq, grad_xk, grad_v};
+  const size_t out_sz[3] = {nx, nx, nv};
+  for (int o = 0; o < 3; ++o) {
+    for (int i = 0; i < 5; ++i)
+      if (cp::overlaps(outs[o], out_sz[o], ins[i], in_sz[i])) return CP_ERR_INVALID_ARG;
+    for (int o2 = o + 1; o2 < 3; ++o2)
+      if (cp::overlaps(outs[o], out_sz[o], outs[o2], out_sz[o2])) return CP_ERR_INVALID_ARG;
+  }
+  const size_t need = cp::favor_ws_bytes(BH, N, D, M, true);
+  if (workspace != nullptr && workspace_bytes < need) return CP_ERR_WORKSPACE_TOO_SMALL;
+  if (N == 0) return CP_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  cp::Scratch s;
+  st = cp::acquire(s, workspace, workspace_bytes, need, stream);
+  if (st != CP_OK) return st;
+  int* status = static_cast<int*>(s.base);
+  float* agg = reinterpret_cast<float*>(static_cast<char*>(s.base) + cp::kStatusBytes);
+  const size_t feat = cp::favor_feat_bytes(BH, N, D, true);
+  char* fq = static_cast<char*>(s.base) + cp::kStatusBytes + cp::favor_agg_bytes(BH, N, D, M, true);
+  char* fk = fq + feat;
+  char* aq = fk + feat;
+  char* ak = aq + feat;
+  // Features as [hi | lo] bf16 parts.  The gradient of x flows through
+  // differences between the a_d = dL/dphi_d of one row (the common part of
+  // a_d multiplies sum_d phi_d, nearly independent of x), so each a is
+  // taken against both parts of the other side's features: a bf16 feature
+  // alone put up to a quarter of a row's scale into dL/dx on the D = 256
+  // workload (emulated on the CPU against the fp64 oracle); hi + lo brings it
+  // to the bf16 output floor.
+  st = cp::favor_map_launch(xq, W, fq, BH, N, R, D, true, status, stream);
+  if (st == CP_OK) st = cp::favor_map_launch(xk, W, fk, BH, N, R, D, true, status, stream);
+  if (st != CP_OK) return st;
+  // dL/dphi(xq)_i = sum_{j<=i} (g_i . v_j) phi(xk)_j: the forward product
+  // (g, v, [hi | lo] of phi(xk)), both halves in one launch
+  cp::Product pq{grad_out, v, fk, aq, BH, N, M, 2 * D, false};
+  // dL/dphi(xk)_j = sum_{i>=j} (v_j . g_i) phi(xq)_i: the reverse product
+  cp::Product pk{v, grad_out, fq, ak, BH, N, M, 2 * D, true};
+  // dv_j = sum_{i>=j} (phi(xq)_i . phi(xk)_j) g_i on the hi parts
+  cp::Product pv{fk, fq, grad_out, grad_v, BH, N, D, M, true};
+  pv.ld_qk = 2 * D;
+  st = cp::run_product(pq, CP_DTYPE_BF16, agg, status, stream);
+  if (st == CP_OK) st = cp::run_product(pk, CP_DTYPE_BF16, agg, status, stream);
+  if (st == CP_OK) st = cp::run_product(pv, CP_DTYPE_BF16, agg, status, stream);
+  if (st != CP_OK) return st;
+  st = cp::favor_chain_launch(xq, W, aq, fq, 2 * D, grad_xq, BH, N, R, D, status, stream);
+  if (st == CP_OK)
+    st = cp::favor_chain_launch(xk, W, ak, fk, 2 * D, grad_xk, BH, N, R, D, status, stream);
+  return st;
+}
+
 cp_status_t causal_product_selftest_timeout(void* workspace, uint64_t wait_ns, void* stream_) {
   if (workspace == nullptr) return CP_ERR_INVALID_ARG;
   if (!cp::aligned16(workspace)) return CP_ERR_MISALIGNED;

@@ -69,6 +69,9 @@ struct Product {
   int seed_G = 0, seed_tiles = 0;
   int64_t seed_bh = 0, seed_seg = 0;
   int seed_seg_off = 0;
+  // bf16: row pitch (elements) of q, k (ld_qk) and of v, out (ld_v, ld_o);
+  // 0: dense rows of D or M elements
+  int64_t ld_qk = 0, ld_v = 0, ld_o = 0;
 };
 
 // The dq product (g, v, k) of a backward seeded from a forward's checkpoints
@@ -164,6 +167,22 @@ cudaError_t feature_map_launch(int feature, const void* x, void* y, int64_t n, c
                                cudaStream_t stream);
 cudaError_t feature_grad_launch(int feature, const void* x, void* g, int64_t n,
                                 cp_dtype_t dtype, cudaStream_t stream);
+
+// ---- positive random features (bf16, tensor cores): rows x of R input
+// features ([BH][N][R]), one projection W [D][R]; R in 8..64 (multiple of
+// 8), D in 64..256 (multiple of 64).
+// map:   y = phi(x) = exp(W x - |x|^2 / 2) / sqrt(D): rows of bf16(phi)
+//        ([BH][N][D]), or with `lo` rows [bf16(phi) | bf16(phi - bf16(phi))]
+//        ([BH][N][2D]).
+// chain: dx = sum_d a_d phi_d (w_d - x) for a = dL/dphi given as rows
+//        [a_1 | a_2] ([BH][N][2D] bf16, a = a_1 + a_2) and phi the first D
+//        columns of rows `phi_pitch` elements apart.
+bool favor_supported(int64_t R, int64_t D);
+cp_status_t favor_map_launch(const void* x, const void* W, void* y, int64_t BH, int64_t N,
+                             int64_t R, int64_t D, bool lo, int* status, cudaStream_t stream);
+cp_status_t favor_chain_launch(const void* x, const void* W, const void* a, const void* phi,
+                               int64_t phi_pitch, void* dx, int64_t BH, int64_t N, int64_t R,
+                               int64_t D, int* status, cudaStream_t stream);
 
 // ---- failure-path self-test: records CP_ERR_TIMEOUT after `wait_ns`
 cudaError_t selftest_timeout_launch(int* status, uint64_t wait_ns, cudaStream_t stream);

@@ -571,6 +571,9 @@ __global__ void __launch_bounds__(kLbThreads, 3) norm_lb_kernel(const LbArgs a) 
           for (int j = 0; j < V2; ++j)
             *reinterpret_cast<float2*>(wt + warp * D + col[kk] + 2 * j) = sum[kk][j];
     }
+    // every thread has its rows (read with ordinary loads): order those reads
+    // before the bulk copy that refills the stage (async proxy)
+    ptx::fence_proxy_async_smem();
     __syncthreads();  // wt complete; every thread has its rows: refill the stage
     if (tid == 0) {
       issue(s, next);

@@ -114,7 +114,9 @@ TcPlan tc_plan(int64_t BH, int64_t N, int64_t D, int64_t M) {
   p.G = p.seg_tiles > 0 ? (p.n_tiles + p.seg_tiles - 1) / p.seg_tiles : 1;
   if (p.G < 1) p.G = 1;
   p.agg_bytes = p.G > 1 ? sizeof(float) * (size_t)problems * p.G * p.DP * p.MB : 0;
-  p.ok = p.DP <= 256 && Mpad <= 256;
+  // the entry points allow M <= 256; internal products (the gradients of the
+  // positive random features, with hi | lo value halves) go to 512
+  p.ok = p.DP <= 256 && Mpad <= 512;
   return p;
 }
 
@@ -146,8 +148,10 @@ cp_status_t tc_run(const Product& p, const TcPlan& plan, float* agg, int* status
                    cudaStream_t stream, bool agg_only) {
   if (!plan.ok) return CP_ERR_UNSUPPORTED_SHAPE;
   CUtensorMap mq, mk, mv, mo;
-  if (!tc::make_map(&mq, p.q, p.BH, p.N, p.D) || !tc::make_map(&mk, p.k, p.BH, p.N, p.D) ||
-      !tc::make_map(&mv, p.v, p.BH, p.N, p.M) || !tc::make_map(&mo, p.out, p.BH, p.N, p.M))
+  if (!tc::make_map(&mq, p.q, p.BH, p.N, p.D, p.ld_qk) ||
+      !tc::make_map(&mk, p.k, p.BH, p.N, p.D, p.ld_qk) ||
+      !tc::make_map(&mv, p.v, p.BH, p.N, p.M, p.ld_v) ||
+      !tc::make_map(&mo, p.out, p.BH, p.N, p.M, p.ld_o))
     return CP_ERR_UNSUPPORTED_SHAPE;
   tc::Args a{};
   a.N = p.N;

@@ -158,12 +158,17 @@ inline PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-// [BH][N][cols] bf16, boxes of 64 columns x 128 rows x 1 problem, 128-byte swizzle.
-inline bool make_map(CUtensorMap* m, const void* ptr, int64_t BH, int64_t N, int64_t cols) {
+// [BH][N][cols] bf16, boxes of 64 columns x 128 rows x 1 problem, 128-byte
+// swizzle.  `pitch` (elements between rows, 0: cols) lets the map cover the
+// first `cols` columns of wider rows.
+inline bool make_map(CUtensorMap* m, const void* ptr, int64_t BH, int64_t N, int64_t cols,
+                     int64_t pitch = 0) {
   auto enc = get_encode();
   if (enc == nullptr) return false;
+  if (pitch == 0) pitch = cols;
+  if (pitch < cols) return false;
   cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)N, (cuuint64_t)BH};
-  cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)(N * cols * 2)};
+  cuuint64_t strides[2] = {(cuuint64_t)pitch * 2, (cuuint64_t)(N * pitch * 2)};
   cuuint32_t box[3] = {(cuuint32_t)kBoxCols, (cuuint32_t)kTile, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
