@@ -665,7 +665,9 @@ size_t favor_feat_bytes(int64_t BH, int64_t N, int64_t D, bool backward) {
 }
 
 size_t favor_agg_bytes(int64_t BH, int64_t N, int64_t D, int64_t M, bool backward) {
-  if (!backward) return round_up(tc_plan(BH, N, D, M).agg_bytes);
+  if (!backward)
+    return round_up(std::max(tc_plan(BH, N, D, M).agg_bytes,
+                             favor_fused_plan(BH, N, D, M).agg_bytes));
   return round_up(std::max(tc_plan(BH, N, M, 2 * D).agg_bytes, tc_plan(BH, N, D, M).agg_bytes));
 }
 
@@ -709,6 +711,9 @@ cp_status_t causal_product_fwd_favor(const void* xq, const void* xk, const void*
   if (st != CP_OK) return st;
   int* status = static_cast<int*>(s.base);
   float* agg = reinterpret_cast<float*>(static_cast<char*>(s.base) + cp::kStatusBytes);
+  // D = 128 or 256: the feature map inside the product kernel
+  if (cp::favor_fused_supported(R, D))
+    return cp::favor_fused_fwd_launch(xq, xk, v, W, out, BH, N, R, D, M, agg, status, stream);
   const size_t feat = cp::favor_feat_bytes(BH, N, D, false);
   char* fq = static_cast<char*>(s.base) + cp::kStatusBytes + cp::favor_agg_bytes(BH, N, D, M, false);
   char* fk = fq + feat;

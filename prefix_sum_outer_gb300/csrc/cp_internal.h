@@ -184,6 +184,20 @@ cp_status_t favor_chain_launch(const void* x, const void* W, const void* a, cons
                                int64_t phi_pitch, void* dx, int64_t BH, int64_t N, int64_t R,
                                int64_t D, int* status, cudaStream_t stream);
 
+// The feature map fused into the product kernel (D = 128 or 256, value
+// blocks of 64 columns): out = causal product of phi(xq), phi(xk), v, with
+// phi never leaving the CTA.  Split problems run an aggregate pass (phi(xk)
+// only) and the segment prefix first; `agg` holds favor_fused_plan(...).agg_bytes.
+struct FavorPlan {
+  int n_mb, n_tiles, seg_tiles, G;
+  size_t agg_bytes;
+};
+bool favor_fused_supported(int64_t R, int64_t D);
+FavorPlan favor_fused_plan(int64_t BH, int64_t N, int64_t D, int64_t M);
+cp_status_t favor_fused_fwd_launch(const void* xq, const void* xk, const void* v, const void* W,
+                                   void* out, int64_t BH, int64_t N, int64_t R, int64_t D,
+                                   int64_t M, float* agg, int* status, cudaStream_t stream);
+
 // ---- failure-path self-test: records CP_ERR_TIMEOUT after `wait_ns`
 cudaError_t selftest_timeout_launch(int* status, uint64_t wait_ns, cudaStream_t stream);
 
