@@ -19,13 +19,16 @@
 // the next pair overwrites it.  A whole [128 x 256] feature tile of q and k
 // (128 KB) would not fit beside the state copy and the rings.
 //
-// CTA = 14 warps:
+// CTA = 16 warps:
 //   warp 0        TMA producer: W once, the X tile pair (xq | xk), V ring
-//   warp 1        TMEM allocator; the one MMA issuer (F, P, phi(Q) S, S, P V)
+//   warp 1        TMEM allocator; MMA issuer A: per pair, P, phi(Q) S and S
 //   warps 2..5    state group: bf16 hi/lo copy of S per tile, read-out of O
 //                 (TMA store), the segment aggregates of the first pass
 //   warps 6..9    P group: mask P, split into bf16 hi + lo, pack in TMEM
 //   warps 10..13  mapping group: |x|^2, F -> phi into the pair stage
+//   warp 14       MMA issuer F: the F chunks, as far ahead as TMEM allows
+//   warp 15       MMA issuer C: P V, once P is packed
+// The aggregate pass (phi(K) and S only) double-buffers the pair stage.
 // Every wait is bounded and records CP_ERR_TIMEOUT in the status word.
 #include <algorithm>
 #include <atomic>
@@ -42,8 +45,8 @@ namespace ffwd {
 using namespace cp::ptx;
 
 constexpr int kMB = 64;                       // value columns per CTA
-constexpr int kSWarp0 = 2, kPWarp0 = 6, kMWarp0 = 10;
-constexpr int kThreads = 32 * 14;
+constexpr int kSWarp0 = 2, kPWarp0 = 6, kMWarp0 = 10, kFWarp = 14, kCWarp = 15;
+constexpr int kThreads = 32 * 16;
 constexpr int kFSlots = 3;                    // F chunks in TMEM (64 columns each)
 constexpr float kLog2e = 1.4426950408889634f;
 // TMEM columns
@@ -68,11 +71,12 @@ struct FLayout {
   static constexpr int kWBytes = D * 128;                    // W [D][64] bf16
   static constexpr int kXBytes = (AGG ? 1 : 2) * kBoxBytes;  // xk (| xq)
   static constexpr int kKOff = AGG ? 0 : 2 * kBoxBytes;      // phi(K) pair within the stage
-  static constexpr int kPhiBytes = (AGG ? 2 : 4) * kBoxBytes;
+  static constexpr int kPhiBytes = (AGG ? 2 : 4) * kBoxBytes;  // one pair stage
+  static constexpr int NPHI = AGG ? 2 : 1;                      // pair stages
   static constexpr int kSOneBytes = D * 128;                 // D x 64 bf16
   static constexpr int kSBytes = AGG ? 0 : 2 * kSOneBytes;   // hi | lo
   static constexpr int kOBytes = AGG ? 0 : kBoxBytes;
-  static constexpr int kFixed = kWBytes + kXBytes + kPhiBytes + kSBytes + kOBytes;
+  static constexpr int kFixed = kWBytes + kXBytes + NPHI * kPhiBytes + kSBytes + kOBytes;
   static constexpr int kAvail = kSmemLimit - 2048;
   static constexpr int NV = std::min(3, (kAvail - kFixed) / kBoxBytes);
   static constexpr int kSmemBytes = kFixed + NV * kBoxBytes + 2048;
@@ -111,7 +115,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap tm_v,
                         const __grid_constant__ CUtensorMap tm_o, const FArgs a) {
   using L = FLayout<D, AGG>;
-  constexpr int NPAIR = L::NPAIR, NV = L::NV;
+  constexpr int NPAIR = L::NPAIR, NV = L::NV, NPHI = L::NPHI;
   constexpr int kChunks = AGG ? 2 : 4;  // F chunks per pair: (q0, q1,) k0, k1
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -119,7 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* w_s = smem;
   uint8_t* x_s = w_s + L::kWBytes;        // [xq box |] xk box (xk last)
   uint8_t* phi_s = x_s + L::kXBytes;      // [phi(Q) pair (2 boxes) |] phi(K) pair
-  uint8_t* s_tile = phi_s + L::kPhiBytes; // hi | lo state copy
+  uint8_t* s_tile = phi_s + NPHI * L::kPhiBytes; // hi | lo state copy
   uint8_t* o_tile = s_tile + L::kSBytes;
   uint8_t* v_ring = o_tile + L::kOBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(v_ring + NV * kBoxBytes);
@@ -130,18 +134,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* v_empty = v_full + NV;     // [NV]
   uint64_t* f_full = v_empty + NV;     // [kFSlots] issuer -> mapping
   uint64_t* f_free = f_full + kFSlots; // [kFSlots] mapping -> issuer
-  uint64_t* pair_mapped = f_free + kFSlots;  // mapping -> issuer
-  uint64_t* pair_done = pair_mapped + 1;     // issuer -> mapping: stage read
-  uint64_t* p_done = pair_done + 1;          // issuer -> P group
+  uint64_t* pair_mapped = f_free + kFSlots;  // [NPHI] mapping -> issuer A
+  uint64_t* pair_done = pair_mapped + NPHI;  // [NPHI] issuer A -> mapping: stage read
+  uint64_t* p_done = pair_done + NPHI;       // issuer A -> P group
   uint64_t* p_ready = p_done + 1;            // P group -> issuer
   uint64_t* s_done = p_ready + 1;            // issuer -> state group: S updated
   uint64_t* s_ready = s_done + 1;            // state group -> issuer: copy written
   uint64_t* o_done = s_ready + 1;            // issuer -> state group: O final
   uint64_t* o_free = o_done + 1;             // state group -> issuer: O read out
   uint64_t* pv_done = o_free + 1;            // issuer -> issuer: P buffer free
-  uint64_t* fin = pv_done + 1;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(fin + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(fin + 2);
+  uint64_t* fin = pv_done + 1;               // [3] issuers A, F, C drain
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(fin + 3);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(fin + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -168,8 +172,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&f_full[i], 1);
       mbar_init(&f_free[i], 4);
     }
-    mbar_init(pair_mapped, 4);
-    mbar_init(pair_done, 1);
+    for (int i = 0; i < NPHI; ++i) {
+      mbar_init(&pair_mapped[i], 4);
+      mbar_init(&pair_done[i], 1);
+    }
     mbar_init(p_done, 1);
     mbar_init(p_ready, 4);
     mbar_init(s_done, 1);
@@ -177,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(o_done, 1);
     mbar_init(o_free, 4);
     mbar_init(pv_done, 1);
-    mbar_init(fin, 1);
+    for (int i = 0; i < 3; ++i) mbar_init(&fin[i], 1);
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -247,32 +253,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_timeout(w_full, 0, CP_WAIT_TIMEOUT_NS);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == kFWarp) {
+    // ------------------------------------------------------------ MMA issuer F
+    // F = X W_b^T per 64-column chunk b, into the next free F slot
     if (lane == 0) {
       constexpr uint32_t kHi = desc_hi(1024);
-      constexpr uint32_t idesc_f = idesc_bf16_f32(128, 64, 0, 0);    // X . W_b^T
-      constexpr uint32_t idesc_p = idesc_bf16_f32(128, 128, 0, 0);   // phi(Q) phi(K)^T
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, kMB, 1, 1);   // phi(K)^T V
-      constexpr uint32_t idesc_o = idesc_bf16_f32(128, kMB, 0, 1);   // phi(Q) S, P V
+      constexpr uint32_t idesc_f = idesc_bf16_f32(128, 64, 0, 0);  // X . W_b^T
       const uint32_t w_lo = desc_lo(smem_u32(w_s), 16);
-      const uint32_t s_lo = desc_lo(smem_u32(s_tile), D * 128);
-      const uint32_t phq_lo = desc_lo(smem_u32(phi_s), 16);                // K-major
-      const uint32_t phk_lo = desc_lo(smem_u32(phi_s + L::kKOff), 16);     // K-major
-      const uint32_t phk_mn = desc_lo(smem_u32(phi_s + L::kKOff), kBoxBytes);  // MN-major
       bool ok = mbar_wait(w_full, 0, abort_flag);
       int gc = 0;  // F chunks issued
       for (int it = 0; ok && it < n_it; ++it) {
-        const bool fresh_state = it == 0 && !has_prefix;
-        const int vs = it % NV;
-        const uint32_t v_lo = desc_lo(smem_u32(v_ring + vs * kBoxBytes), kBoxBytes);
         if (!mbar_wait(x_full, it & 1, abort_flag)) { ok = false; break; }
         for (int pp = 0; ok && pp < NPAIR; ++pp) {
-          const int gp = it * NPAIR + pp;  // pairs so far
-          // F chunks of this pair: (xq box 2pp, 2pp+1,) xk box 2pp, 2pp+1
           for (int c = 0; c < kChunks; ++c, ++gc) {
             const int slot = gc % kFSlots;
-            if (gc >= kFSlots && !mbar_wait(&f_free[slot], ((gc / kFSlots) - 1) & 1, abort_flag)) {
+            if (gc >= kFSlots &&
+                !mbar_wait(&f_free[slot], ((gc / kFSlots) - 1) & 1, abort_flag)) {
               ok = false;
               break;
             }
@@ -288,9 +284,68 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   kk > 0 ? 1u : 0u);
             mma_commit(&f_full[slot]);
           }
-          if (!ok) break;
-          if (pp == NPAIR - 1) mma_commit(x_empty);  // the tile's X is read
-          if (!mbar_wait(pair_mapped, gp & 1, abort_flag)) { ok = false; break; }
+        }
+        if (ok) mma_commit(x_empty);  // the tile's X is read by the MMAs
+      }
+      if (!ok) record_timeout(a.status, abort_flag);
+      mma_commit(fin + 1);
+      mbar_wait_timeout(fin + 1, 0, CP_WAIT_TIMEOUT_NS);
+    }
+  } else if (warp == kCWarp) {
+    // ------------------------------------------------------------ MMA issuer C
+    // O += P_hi V + P_lo V once P is packed (after phi(Q) S: p_done follows
+    // every MMA of issuer A for the tile)
+    if (lane == 0 && !AGG) {
+      constexpr uint32_t kHi = desc_hi(1024);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, kMB, 0, 1);
+      bool ok = true;
+      for (int it = 0; it < n_it; ++it) {
+        const int vs = it % NV;
+        if (!mbar_wait(p_ready, it & 1, abort_flag) ||
+            !mbar_wait(&v_full[vs], (it / NV) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t v_lo = desc_lo(smem_u32(v_ring + vs * kBoxBytes), kBoxBytes);
+#pragma unroll
+        for (int part = 0; part < kPParts; ++part) {
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            const uint32_t acol = (kk >> 1) * 32 + part * 16 + (kk & 1) * 8;
+            mma_ts_lo<kHi>(tmem + kColO, tmem + kColP + acol, v_lo + ((kk * 2048) >> 4), idesc_o,
+                           1u);
+          }
+        }
+        mma_commit(o_done);
+        mma_commit(pv_done);
+        mma_commit(&v_empty[vs]);
+      }
+      if (!ok) record_timeout(a.status, abort_flag);
+      mma_commit(fin + 2);
+      mbar_wait_timeout(fin + 2, 0, CP_WAIT_TIMEOUT_NS);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer A
+    if (lane == 0) {
+      constexpr uint32_t kHi = desc_hi(1024);
+      constexpr uint32_t idesc_p = idesc_bf16_f32(128, 128, 0, 0);   // phi(Q) phi(K)^T
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, kMB, 1, 1);   // phi(K)^T V
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, kMB, 0, 1);   // phi(Q) S
+      const uint32_t s_lo = desc_lo(smem_u32(s_tile), D * 128);
+      bool ok = true;
+      for (int it = 0; ok && it < n_it; ++it) {
+        const bool fresh_state = it == 0 && !has_prefix;
+        const int vs = it % NV;
+        const uint32_t v_lo = desc_lo(smem_u32(v_ring + vs * kBoxBytes), kBoxBytes);
+        for (int pp = 0; ok && pp < NPAIR; ++pp) {
+          const int gp = it * NPAIR + pp;  // pairs so far
+          const int st = gp % NPHI;
+          uint8_t* stage = phi_s + st * L::kPhiBytes;
+          const uint32_t phq_lo = desc_lo(smem_u32(stage), 16);                     // K-major
+          const uint32_t phk_lo = desc_lo(smem_u32(stage + L::kKOff), 16);          // K-major
+          const uint32_t phk_mn = desc_lo(smem_u32(stage + L::kKOff), kBoxBytes);   // MN-major
+          if (!mbar_wait(&pair_mapped[st], (gp / NPHI) & 1, abort_flag)) { ok = false; break; }
           if (pp == 0) {
             if (!mbar_wait(&v_full[vs], (it / NV) & 1, abort_flag)) { ok = false; break; }
             if (!AGG) {
@@ -332,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ss_lo<kHi, kHi>(tmem + kColS + pp * kMB, phk_mn + ((kk * 2048) >> 4),
                                 v_lo + ((kk * 2048) >> 4), idesc_s,
                                 (fresh_state && kk == 0) ? 0u : 1u);
-          mma_commit(pair_done);  // the pair stage may be overwritten
+          mma_commit(&pair_done[st]);  // the pair stage may be overwritten
         }
         if (!ok) break;
         if (AGG) {
@@ -341,21 +396,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(s_done);
         mma_commit(p_done);
-        if (!mbar_wait(p_ready, it & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        // O += P_hi V + P_lo V (A = packed P in TMEM)
-#pragma unroll
-        for (int part = 0; part < kPParts; ++part) {
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            const uint32_t acol = (kk >> 1) * 32 + part * 16 + (kk & 1) * 8;
-            mma_ts_lo<kHi>(tmem + kColO, tmem + kColP + acol, v_lo + ((kk * 2048) >> 4), idesc_o,
-                           1u);
-          }
-        }
-        mma_commit(o_done);
-        mma_commit(pv_done);
-        mma_commit(&v_empty[vs]);
       }
       // the aggregate pass hands its state on once, after the last tile
       if (AGG && ok) mma_commit(s_done);
@@ -379,8 +419,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(x_empty);
       for (int pp = 0; ok && pp < NPAIR; ++pp) {
         const int gp = it * NPAIR + pp;
-        // the previous pair's MMAs have read the stage
-        if (gp > 0 && !mbar_wait(pair_done, (gp - 1) & 1, abort_flag)) { ok = false; break; }
+        const int st = gp % NPHI;
+        uint8_t* stage = phi_s + st * L::kPhiBytes;
+        // the MMAs of the pair that last used this stage have read it
+        if (gp >= NPHI && !mbar_wait(&pair_done[st], ((gp / NPHI) - 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
         for (int c = 0; c < kChunks; ++c, ++gc) {
           const int slot = gc % kFSlots;
           if (!mbar_wait(&f_full[slot], (gc / kFSlots) & 1, abort_flag)) { ok = false; break; }
@@ -399,14 +444,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int x = 0; x < 32; ++x)
               r[h][x] = __float_as_uint(ex2_approx(fmaf(__uint_as_float(r[h][x]), kLog2e, cst)));
-          uint8_t* box = phi_s + (is_q ? 0 : L::kKOff) + (c & 1) * kBoxBytes;
+          uint8_t* box = stage + (is_q ? 0 : L::kKOff) + (c & 1) * kBoxBytes;
           store_chunk32(box, row, 0, kBoxBytes, r[0]);
           store_chunk32(box, row, 32, kBoxBytes, r[1]);
         }
         if (!ok) break;
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(pair_mapped);
+        if (lane == 0) mbar_arrive(&pair_mapped[st]);
       }
     }
     if (!ok) record_timeout(a.status, abort_flag);
