@@ -618,6 +618,13 @@ def run_ours(args, world, rank, local):
                 "timing": "CUDA events over 20 calls"}
         del xq_, xk_, fo
 
+    # ---- positive random features (the D = 256 workload's feature map) from
+    # the raw rows: the forward with the map inside the product kernel, the
+    # backward through the feature map kernels
+    favor = None
+    if not args.no_extras:
+        favor = time_favor(cp, dev, stream, args.steps, args.warmup, world)
+
     # ---- the other four workloads, each as a step of its own pass (forward
     # for the fp32 ones, whose workload is forward only, with their
     # fwd + bwd beside it), same steps and warm-up, CUDA events
@@ -712,6 +719,7 @@ def run_ours(args, world, rank, local):
         "normalizer": norm,
         "feature_map": feat,
         "other_workloads": others,
+        "favor": favor,
         "carried_state": None if state_ms is None else {
             "ms_per_step": state_ms, "value": w.token_heads * world / (state_ms / 1e3) / 1e6,
             "unit": UNIT, "note": "fwd with S_0 in and S_N out, bwd with dS_N in and dS_0 out"},
@@ -820,6 +828,61 @@ def time_workload(cp, w, dev, stream, steps, warmup, world):
     del qd, kd, vd, gd, out, dq, dk, dv, ws_f, ws_b
     torch.cuda.empty_cache()
     return res
+
+
+def time_favor(cp, dev, stream, steps, warmup, world):
+    """Positive random features phi(x) = exp(W x - |x|^2/2)/sqrt(D) computed
+    in the kernels from raw rows (B=4 H=8 N=8229, R=64, D=256, M=64: the
+    D = 256 workload before its feature map), forward and backward."""
+    import torch
+    from prefix_sum_outer_gb300.workloads import favor_raw_inputs
+    B, H, N, D, M = 4, 8, 8229, 256, 64
+    W, xq, xk = favor_raw_inputs(B, H, N, D, 5)
+    R = W.shape[1]
+    gen = torch.Generator().manual_seed(6)
+    v = torch.randn((B, H, N, M), generator=gen)
+    g = torch.randn((B, H, N, M), generator=gen)
+    xq, xk, v, g, W = (t.to(torch.bfloat16).to(dev) for t in (xq, xk, v, g, W))
+    out, dxq, dxk, dv = (torch.empty_like(t) for t in (v, xq, xk, v))
+    lib = cp.load_library()
+    ws_f = torch.zeros(lib.causal_product_favor_workspace_size(B, H, N, R, D, M, 1, 0),
+                       dtype=torch.uint8, device=dev)
+    ws_b = torch.zeros(lib.causal_product_favor_workspace_size(B, H, N, R, D, M, 1, 1),
+                       dtype=torch.uint8, device=dev)
+
+    def fwd():
+        cp.causal_product_fwd_favor(xq, xk, v, W, out=out, workspace=ws_f, stream=stream)
+
+    def bwd():
+        cp.causal_product_bwd_favor(xq, xk, v, W, g, dxq, dxk, dv, workspace=ws_b, stream=stream)
+
+    def timed(fn):
+        for _ in range(max(warmup, 3)):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return max_over_ranks(e0.elapsed_time(e1), world) / steps
+
+    f_ms, b_ms = timed(fwd), timed(bwd)
+    if cp.causal_product_status(ws_f) != cp.CP_OK or cp.causal_product_status(ws_b) != cp.CP_OK:
+        raise RuntimeError("kernel status word reports an error in the feature-map run")
+    th = B * H * N
+    # algorithmic bytes: forward reads xq, xk (R), v (M) and writes out (M);
+    # backward reads xq, xk, v, g and writes dxq, dxk, dv
+    fb, bb = 2 * (2 * R + 2 * M) * th, 2 * (4 * R + 3 * M) * th
+    peak = load_peaks()[0]
+    return {"B": B, "H": H, "N": N, "R": R, "D": D, "M": M,
+            "fwd": {"us": f_ms * 1e3, "kernel": "favor_causal_kernel (map fused into the product)",
+                    "bytes": fb, "frac": fb / (f_ms / 1e3) / 1e9 / peak},
+            "bwd": {"us": b_ms * 1e3, "bytes": bb, "frac": bb / (b_ms / 1e3) / 1e9 / peak,
+                    "kernel": "favor_map_kernel, three products, favor_chain_kernel"},
+            "value_fwd_bwd": th * world / ((f_ms + b_ms) / 1e3) / 1e6, "unit": UNIT,
+            "timing": f"CUDA events over {steps} calls each"}
 
 
 def _fused_dkdv(w):

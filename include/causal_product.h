@@ -35,8 +35,7 @@
  *   - `workspace` is device scratch of at least
  *     causal_product_workspace_size(...) bytes, owned by the caller, used
  *     only until the enqueued work completes; it holds the per-segment fp32
- *     state aggregates of the two-pass scan, a status word and two counters
- *     of the one-launch backward (which leaves them at zero).  The status
+ *     state aggregates of the two-pass scan and a status word.  The status
  *     word is sticky: kernels only ever write an error code into it, and
  *     causal_product_status() reads and clears it.  Zero the first 256 bytes
  *     of a new workspace once before its first use.  Passing

@@ -95,10 +95,9 @@ cp_status_t acquire(Scratch& s, void* workspace, size_t workspace_bytes, size_t 
     return CP_ERR_CUDA;
   }
   s.owned = true;
-  // a fresh allocation starts with a clear status word and ticket counters;
-  // a caller's workspace keeps its (sticky) status until
-  // causal_product_status() reads it
-  if (cudaMemsetAsync(s.base, 0, 4 * sizeof(int), stream) != cudaSuccess) return CP_ERR_CUDA;
+  // a fresh allocation starts with a clear status word; a caller's workspace
+  // keeps its (sticky) status until causal_product_status() reads it
+  if (cudaMemsetAsync(s.base, 0, sizeof(int), stream) != cudaSuccess) return CP_ERR_CUDA;
   return CP_OK;
 }
 

@@ -131,8 +131,7 @@ cudaError_t seg_prefix_launch(float* agg, int64_t P, int G, int64_t E, bool reve
 // tc_plan(BH, N, D, M)): dq is one product launch; dk and dv share the
 // reverse state sum q g^T and are computed in one scan.  With checkpoints
 // (ckpt non-null, ck.G > 1, no S_0) the dq scans are segments seeded from
-// them.  `status` is the workspace header: its word 0 is the status word and
-// words 2 and 3 the dq ticket counters of the one-launch backward.
+// them (on split problems; the one-launch backward keeps whole dq scans).
 bool tc_dkdv_supported(const TcPlan& plan);
 // state_in (S_0), grad_state_out (dL/dS_N) and grad_state_in (dL/dS_0) are
 // [BH][D][M] fp32 or null.

@@ -5,6 +5,7 @@
 #include <atomic>
 #include <cstdio>
 #include <mutex>
+#include <type_traits>
 
 #include "cp_internal.h"
 #include "cp_tc_causal.cuh"
@@ -12,22 +13,28 @@
 namespace cp {
 namespace tc {
 
-template <int DP, int MB, bool AGG_ONLY, bool STATE_OUT, bool FEAT, bool CKPT>
+template <bool EXT>
+using KArgs = std::conditional_t<EXT, ArgsX, Args>;
+
+template <int DP, int MB, bool AGG_ONLY, bool STATE_OUT, bool FEAT, bool CKPT, bool SEED>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
-                     const __grid_constant__ CUtensorMap tm_o, const Args a) {
-  causal_body<DP, MB, AGG_ONLY, STATE_OUT, FEAT, CKPT>(tm_q, tm_k, tm_v, tm_o, a,
-                                                       Phase{(int)blockIdx.x, true, true});
+                     const __grid_constant__ CUtensorMap tm_o, const KArgs<CKPT || SEED> a) {
+  causal_body<DP, MB, AGG_ONLY, STATE_OUT, FEAT, CKPT, SEED, KArgs<CKPT || SEED>>(
+      tm_q, tm_k, tm_v, tm_o, a, Phase{(int)blockIdx.x, true, true});
 }
 
 // ------------------------------------------------------------------ host
-template <int DP, int MB, bool AGG, bool STATE_OUT = false, bool FEAT = false, bool CKPT = false>
+template <int DP, int MB, bool AGG, bool STATE_OUT = false, bool FEAT = false, bool CKPT = false,
+          bool SEED = false>
 cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                       const CUtensorMap& o, const Args& a, unsigned grid, cudaStream_t st) {
+                       const CUtensorMap& o, const ArgsX& ax, unsigned grid, cudaStream_t st) {
+  // the plain kernels get the plain arguments (a copy of the base part)
+  const KArgs<CKPT || SEED> a = ax;
   using L = Layout<DP, MB, AGG>;
-  auto kern = tc_causal_kernel<DP, MB, AGG, STATE_OUT, FEAT, CKPT>;
+  auto kern = tc_causal_kernel<DP, MB, AGG, STATE_OUT, FEAT, CKPT, SEED>;
   // the shared-memory opt-in is set once per device for each instantiation
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
@@ -54,11 +61,11 @@ cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
 
 template <int DP, int MB>
 cudaError_t launch_pair(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                        const CUtensorMap& o, Args a, const TcPlan& plan, int64_t problems,
+                        const CUtensorMap& o, ArgsX a, const TcPlan& plan, int64_t problems,
                         float* agg, bool agg_only, cudaStream_t st) {
   cudaError_t e = cudaSuccess;
   if (plan.G > 1) {
-    Args b = a;
+    ArgsX b = a;
     b.agg_in = nullptr;
     b.agg_out = agg;
     b.state_in = nullptr;   // aggregates are the segments' own sums
@@ -87,9 +94,10 @@ cudaError_t launch_pair(const CUtensorMap& q, const CUtensorMap& k, const CUtens
 // slot s the state before segment s.
 template <int DP, int MB>
 cudaError_t launch_seeded(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                          const CUtensorMap& o, const Args& a, int64_t problems,
+                          const CUtensorMap& o, const ArgsX& a, int64_t problems,
                           cudaStream_t st) {
-  return launch_one<DP, MB, false>(q, k, v, o, a, (unsigned)(problems * a.G), st);
+  return launch_one<DP, MB, false, false, false, false, true>(q, k, v, o, a,
+                                                             (unsigned)(problems * a.G), st);
 }
 
 }  // namespace tc
@@ -153,7 +161,7 @@ cp_status_t tc_run(const Product& p, const TcPlan& plan, float* agg, int* status
       !tc::make_map(&mv, p.v, p.BH, p.N, p.M, p.ld_v) ||
       !tc::make_map(&mo, p.out, p.BH, p.N, p.M, p.ld_o))
     return CP_ERR_UNSUPPORTED_SHAPE;
-  tc::Args a{};
+  tc::ArgsX a{};
   a.N = p.N;
   a.n_tiles = plan.n_tiles;
   a.seg_tiles = plan.seg_tiles;

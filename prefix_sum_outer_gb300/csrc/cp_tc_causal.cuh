@@ -84,15 +84,23 @@ struct Args {
   int64_t st_ld_r, st_ld_c;
   int Dr, Mc;
   int feature;  // 0: q, k used as given; 1: phi = elu + 1 (FEAT instantiation)
+};
+
+// The arguments of the checkpoint-writing (CKPT) and seeded (SEED)
+// instantiations.  The plain kernels take Args alone: measured on
+// B=8 H=16 N=4096 D=M=64, these fields in every kernel's parameters made the
+// plain forward launch 3.5 us slower (44.4 -> 48.0 us) through code
+// generation, with the same code path at run time.
+struct ArgsX : Args {
   // Checkpoints of the state every ck_tiles tiles, in the caller's state
   // layout: ckpt[((bh * (ck_G - 1) + s - 1) * Dr + d) * Mc + m] is element
   // (d, m) of the state before tile s * ck_tiles, s = 1 .. ck_G - 1.  A
   // forward product with ckpt set (CKPT instantiation) writes them.
   float* ckpt;
   int ck_tiles, ck_G;
-  // Seeded segments: with seed set, every segment but the first in scan
-  // order starts from a precomputed state instead of a segment-sum pass:
-  // element (r, c) of the start of segment seg of problem bh is
+  // Seeded segments (SEED instantiation): every segment but the first in
+  // scan order starts from a precomputed state instead of a segment-sum
+  // pass: element (r, c) of the start of segment seg of problem bh is
   // seed[bh * seed_bh + (seg + seed_seg_off) * seed_seg + r * st_ld_r + c * st_ld_c]
   // (the carried-state strides; no carried state besides).
   const float* seed;
@@ -190,11 +198,16 @@ struct Layout {
 // though it runs once, costs the whole kernel registers).
 // FEAT: q and k are raw inputs mapped by phi = elu + 1 in shared memory.
 // CKPT: a forward product writes its state at every checkpoint boundary.
+// SEED: segments start from precomputed states (a.seed) instead of the
+// prefix of a segment-sum pass (separate instantiations: both cost the
+// plain scan registers and time when compiled in).
 // Returns false when a wait gave up.
-template <int DP, int MB, bool AGG_ONLY, bool STATE_OUT, bool FEAT = false, bool CKPT = false>
+template <int DP, int MB, bool AGG_ONLY, bool STATE_OUT, bool FEAT = false, bool CKPT = false,
+          bool SEED = false, typename A = Args>
 __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                             const CUtensorMap& tm_v, const CUtensorMap& tm_o,
-                                            const Args& a, const Phase ph) {
+                                            const A& a, const Phase ph) {
+  static_assert(!(CKPT || SEED) || sizeof(A) == sizeof(ArgsX), "CKPT and SEED take ArgsX");
   using L = Layout<DP, MB, AGG_ONLY>;
   constexpr int NQK = L::NQK;
   constexpr int NV = L::NV;
@@ -254,8 +267,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
   const bool has_prefix =
       !AGG_ONLY && a.agg_in != nullptr && (a.reverse ? (seg < a.G - 1) : (seg > 0));
   // a segment seeded from a precomputed state
-  const bool seeded =
-      !AGG_ONLY && a.seed != nullptr && (a.reverse ? (seg < a.G - 1) : (seg > 0));
+  const bool seeded = SEED && !AGG_ONLY && (a.reverse ? (seg < a.G - 1) : (seg > 0));
   // the state does not start at zero: earlier segments, a checkpoint or a
   // carried state
   const bool has_init = has_prefix || seeded || (!AGG_ONLY && a.state_in != nullptr);
@@ -319,12 +331,19 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
   // CKPT: checkpoint s (>= 1) is the state before tile s * ck_tiles; 0
   // when the boundary before `tile` holds none (the start of the sequence)
   auto ckpt_slot = [&](int tile) -> int {
-    if (!CKPT || a.reverse || tile <= 0 || tile >= a.n_tiles) return 0;
-    return tile % a.ck_tiles == 0 ? tile / a.ck_tiles : 0;
+    if constexpr (CKPT) {
+      if (a.reverse || tile <= 0 || tile >= a.n_tiles) return 0;
+      return tile % a.ck_tiles == 0 ? tile / a.ck_tiles : 0;
+    } else {
+      return 0;
+    }
   };
   // CKPT: row d of checkpoint s, columns m0 .. m0 + 31 of this value block
   auto ckpt_row = [&](int s_slot, int d, int m0) -> float* {
-    return a.ckpt + (((size_t)bh * (a.ck_G - 1) + s_slot - 1) * a.Dr + d) * a.Mc + m0;
+    if constexpr (CKPT)
+      return a.ckpt + (((size_t)bh * (a.ck_G - 1) + s_slot - 1) * a.Dr + d) * a.Mc + m0;
+    else
+      return nullptr;
   };
 
   // FEAT: phi applied in place to the landed Q/K tiles of tile it (K only in
@@ -616,9 +635,11 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
       if (has_init) {
         const int lo = has_prefix ? seg : 0;
         const int hi = has_prefix ? seg + 1 : 0;
-        const float* st =
-            seeded ? a.seed + (int64_t)bh * a.seed_bh + (int64_t)(seg + a.seed_seg_off) * a.seed_seg
-                   : (a.state_in != nullptr ? a.state_in + (int64_t)bh * a.Dr * a.Mc : nullptr);
+        const float* st = a.state_in != nullptr ? a.state_in + (int64_t)bh * a.Dr * a.Mc : nullptr;
+        if constexpr (SEED) {
+          if (seeded)
+            st = a.seed + (int64_t)bh * a.seed_bh + (int64_t)(seg + a.seed_seg_off) * a.seed_seg;
+        }
 #pragma unroll
         for (int sb = 0; sb < L::kSBlocks; ++sb) {
           if (sb * 128 + wq * 32 >= DP) continue;

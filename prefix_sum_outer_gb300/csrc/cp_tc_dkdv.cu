@@ -1,14 +1,17 @@
 // Backward pass for bf16 with D, M <= 64: the fused dk/dv reverse scan
 // (cp_tc_dkdv.cuh) and dq, a forward causal product.
 //
-// Unsplit problems on fewer problems than SMs run as one launch
-// (tc_bwd_kernel): CTA p < BH runs the dk/dv scan of problem p, the other
-// SMs start on dq scans at once, and every CTA takes dq scans from a shared
-// ticket counter until none is left, so the SMs finish together whatever
-// the two scans' speeds.  With checkpoints of the forward's state, a dq scan
-// is one segment of a problem, seeded from its checkpoint, and CTA p first
-// runs segment 0 of problem p, whose first tiles its dk/dv scan has just
-// read.  Split problems run dq as a product launch, then the aggregate pass
+// Unsplit problems on fewer problems than SMs run as one launch with a
+// static schedule (tc_bwd_kernel): CTA p < BH runs the dk/dv scan of problem
+// p, and the SMs that would otherwise idle run dq scans, two each; the
+// remaining dq scans follow the dk/dv scan of their own problem on the same
+// CTA, whose first tiles that scan has just read.  Per problem the dk/dv
+// scan takes about 1.6 times a dq scan, so two dq scans per spare SM keep
+// those SMs busy about as long as a dk/dv + dq CTA.  (Cutting the dq scans
+// into segments seeded from forward checkpoints, handed out from a ticket
+// pool, measured slower: each extra scan start and drain cost about 7 us.)
+// Split problems run dq as a product launch (its segments seeded from the
+// forward's checkpoints when the caller has them), then the aggregate pass
 // and the fused scan.
 #include <algorithm>
 #include <atomic>
@@ -32,12 +35,10 @@ __global__ void __launch_bounds__(dkdv::kThreads, 1)
                              Phase{(int)blockIdx.x, true, true});
 }
 
-// The one-launch backward.  aq describes the dq product (g, v, k) with aq.G
-// segments per problem (aq.G > 1: seeded from checkpoints in aq.agg_in).
-// tickets[0] counts the dq scans handed out from the shared pool and
-// tickets[1] the CTAs that have finished; the last CTA to finish sets both
-// back to zero, so every launch starts from a clear pair (the caller zeroes
-// them once, with the rest of the workspace header).
+constexpr int kDqPerSpare = 2;
+
+// CTA c < BH: the dk/dv scan of problem c, then dq of problem c when c <
+// n_main_dq.  CTA BH + e: dq of problems n_main_dq + kDqPerSpare * e + j.
 template <bool STATE_OUT>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -45,43 +46,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tm_dk,
                   const __grid_constant__ CUtensorMap tm_dv,
                   const __grid_constant__ CUtensorMap tm_dq, const dkdv::DkdvArgs a, const Args aq,
-                  int* tickets) {
-  __shared__ int s_ticket;
+                  int n_main_dq) {
   const int c = (int)blockIdx.x;
-  const int BH = a.BH;
-  // dq scans in the pool: with segments, segment 0 of every problem runs on
-  // the dk/dv CTA of its problem and segments 1.. are pooled (segment major);
-  // without, every problem's whole scan is pooled
-  const int G = aq.G;
-  const int n_pool = G > 1 ? BH * (G - 1) : BH;
-  auto dq_work = [&](int t) { return G > 1 ? BH + t : t; };  // work = seg * BH + problem
-  bool ok = true;
-  bool first = true;
-  if (c < BH) {
-    ok = dkdv::dkdv_body<STATE_OUT>(tm_q, tm_k, tm_v, tm_g, tm_dk, tm_dv, a, Phase{c, true, false});
-    first = false;
-    if (ok && G > 1)
-      ok = causal_body<dkdv::kW, dkdv::kW, false, false>(tm_g, tm_v, tm_k, tm_dq, aq,
-                                                         Phase{c, false, false});
+  if (c < a.BH) {
+    const bool more = c < n_main_dq;
+    if (dkdv::dkdv_body<STATE_OUT>(tm_q, tm_k, tm_v, tm_g, tm_dk, tm_dv, a, Phase{c, true, !more}) &&
+        more)
+      causal_body<dkdv::kW, dkdv::kW, false, false>(tm_g, tm_v, tm_k, tm_dq, aq,
+                                                    Phase{c, false, true});
+    return;
   }
-  while (ok) {
-    if (threadIdx.x == 0) s_ticket = atomicAdd(&tickets[0], 1);
-    __syncthreads();
-    const int t = s_ticket;
-    __syncthreads();
-    if (t >= n_pool) break;
-    // dq_i = sum_{j<=i} (g_i . v_j) k_j: the forward product (g, v, k)
-    ok = causal_body<dkdv::kW, dkdv::kW, false, false>(tm_g, tm_v, tm_k, tm_dq, aq,
-                                                       Phase{dq_work(t), first, false});
-    first = false;
-  }
-  if (threadIdx.x == 0) {
-    __threadfence();
-    if (atomicAdd(&tickets[1], 1) == (int)gridDim.x - 1) {
-      atomicExch(&tickets[0], 0);
-      atomicExch(&tickets[1], 0);
-    }
-  }
+  // dq_i = sum_{j<=i} (g_i . v_j) k_j: the forward product (g, v, k)
+  const int p0 = n_main_dq + kDqPerSpare * (c - a.BH);
+  const int n = min(kDqPerSpare, a.BH - p0);
+  for (int j = 0; j < n; ++j)
+    if (!causal_body<dkdv::kW, dkdv::kW, false, false>(tm_g, tm_v, tm_k, tm_dq, aq,
+                                                       Phase{p0 + j, j == 0, j == n - 1}))
+      return;
 }
 
 static_assert(dkdv::kThreads == kThreads, "both scans run on the same CTA");
@@ -163,22 +144,15 @@ cp_status_t tc_bwd_launch(const void* q, const void* k, const void* v, const voi
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return CP_ERR_CUDA;
-  if (plan.G == 1 && BH < n_sm) {
+  if (plan.G == 1 && BH < n_sm && !seeded) {
     // one launch: dk/dv scans on BH CTAs, dq scans on the spare SMs first
     CUtensorMap mdq;
     if (!make_map(&mdq, dq, BH, N, D)) return CP_ERR_UNSUPPORTED_SHAPE;
     Args aq{};
     aq.N = N;
     aq.n_tiles = plan.n_tiles;
-    aq.seg_tiles = seeded ? ck.tiles : plan.n_tiles;
-    aq.G = seeded ? ck.G : 1;
-    if (seeded) {
-      // segment s > 0 starts from checkpoint s (fp32 [BH][G - 1][D][M])
-      aq.seed = ckpt;
-      aq.seed_bh = (int64_t)(ck.G - 1) * D * M;
-      aq.seed_seg = D * M;
-      aq.seed_seg_off = -1;
-    }
+    aq.seg_tiles = plan.n_tiles;
+    aq.G = 1;
     aq.BH = (int)BH;
     aq.n_mb = 1;
     aq.reverse = 0;
@@ -189,23 +163,23 @@ cp_status_t tc_bwd_launch(const void* q, const void* k, const void* v, const voi
     aq.st_ld_c = M;
     aq.Dr = (int)M;
     aq.Mc = (int)D;
-    // every SM: BH dk/dv CTAs and the rest on dq scans from the pool
-    const int64_t n_pool = aq.G > 1 ? BH * (aq.G - 1) : BH;
-    const unsigned grid = (unsigned)std::min<int64_t>(n_sm, BH + n_pool);
-    int* tickets = status + 2;  // two counters in the workspace header
+    const int64_t spare = n_sm - BH;
+    const int64_t n_spare_dq = std::min<int64_t>(BH, spare * kDqPerSpare);
+    const int n_main_dq = (int)(BH - n_spare_dq);
+    const unsigned grid = (unsigned)(BH + (n_spare_dq + kDqPerSpare - 1) / kDqPerSpare);
     constexpr int kSmem = dkdv::kSmemBytes;
     if (grad_state_in != nullptr) {
       static std::atomic<uint64_t> configured{0};
       e = set_smem_once(tc_bwd_kernel<true>, kSmem, configured);
       if (e == cudaSuccess)
         e = launch_bwd(tc_bwd_kernel<true>, grid, kSmem, stream, mq, mk, mv, mg, mdk, mdv, mdq, a,
-                       aq, tickets);
+                       aq, n_main_dq);
     } else {
       static std::atomic<uint64_t> configured{0};
       e = set_smem_once(tc_bwd_kernel<false>, kSmem, configured);
       if (e == cudaSuccess)
         e = launch_bwd(tc_bwd_kernel<false>, grid, kSmem, stream, mq, mk, mv, mg, mdk, mdv, mdq,
-                       a, aq, tickets);
+                       a, aq, n_main_dq);
     }
     return e == cudaSuccess ? CP_OK : CP_ERR_CUDA;
   }

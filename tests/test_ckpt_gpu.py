@@ -107,9 +107,8 @@ def test_ckpt_forward_is_the_forward_and_states_are_exact(shape):
 
 
 def test_ckpt_backward_is_deterministic_and_matches_plain():
-    """Repeats give the same bits (the dq pool hands segments to whichever
-    CTA is free, but each segment's arithmetic is fixed); dk and dv equal the
-    plain backward's, dq agrees with it to rounding."""
+    """Repeats give the same bits; dk and dv equal the plain backward's, dq
+    agrees with it to rounding."""
     B, H, N, D, M = 8, 16, 2048, 64, 64
     q, k, v, g = make_inputs(B, H, N, D, M, torch.bfloat16, seed=11)
     qd, kd, vd, gd = (t.to(DEV) for t in (q, k, v, g))
@@ -127,9 +126,8 @@ def test_ckpt_backward_is_deterministic_and_matches_plain():
 
 
 def test_ckpt_status_and_launch_counts():
-    """A caller workspace stays clear across calls (the ticket counters are
-    left at zero); the library reports one launch for the one-launch
-    backward and a seeded dq launch elsewhere."""
+    """A caller workspace stays clear across calls; the library reports one
+    launch for the one-launch backward and a seeded dq launch elsewhere."""
     w = WORKLOADS["bf16_b8h16_n4096_d64"]
     assert cp.causal_product_launch_count(w.B, w.H, w.N, w.D, w.M, backward=True, ckpt=True) == 1
     B, H, N, D, M = 1, 2, 4100, 128, 64
@@ -144,7 +142,6 @@ def test_ckpt_status_and_launch_counts():
     for _ in range(3):
         cp.causal_product_bwd_ckpt(qd, kd, vd, gd, ckpt, workspace=ws)
     assert cp.causal_product_status(ws) == cp.CP_OK
-    assert int(ws[:16].view(torch.int32)[2]) == 0 and int(ws[:16].view(torch.int32)[3]) == 0
 
 
 def test_autograd_uses_checkpoints():
