@@ -45,16 +45,19 @@ UNIT = "Mtok·head/s"
 CAUSAL_SOURCES = ("cp_tc.cu", "cp_tc_causal.cuh", "cp_tc_common.cuh", "sm103_ptx.cuh")
 BWD_SOURCES = ("cp_tc_dkdv.cu", "cp_tc_dkdv.cuh", "cp_tc_causal.cuh", "cp_tc_common.cuh",
                "sm103_ptx.cuh")
-# Both figures are means over the 7 launches of each kernel in the launch
-# list of `bench.py --steps 1 --warmup 3 --no-e2e --no-cpu-baseline
-# --no-extras` taken with the two DRAM counters beside gpu__time_duration.
+# Both figures are means over 2 launches of each kernel, from
+# `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
+# --clock-control none -k regex:"tc_bwd_kernel|tc_causal_kernel" -s 6 -c 4` of
+# `bench.py --steps 2 --warmup 3 --no-e2e --no-extras --no-others
+# --no-cpu-baseline` (the outputs a launch writes partly stay in the 126 MB
+# L2 when it ends, so its write bytes undercount them).
 PROFILED_TRAFFIC = {
-    "source_sha256": "3d5d33e7c17edb559a1a30ac7ab4d7a58fd3f92ba8e1fc823574e9b95bebcad0",
-    "bytes_per_launch": 208765659,  # 201.40 MB read + 7.36 MB written (forward launch)
+    "source_sha256": "0d2be64cf466d332f23585e36112161e6982031325f1fb1319c667a16009d75c",
+    "bytes_per_launch": 210026880,  # 201.39 MB read + 8.63 MB written (forward launch)
 }
 PROFILED_TRAFFIC_BWD = {
-    "source_sha256": "63ea8432cd63a61ff28feca23246b9482aadb9b6451afaf09990251ccf8c3b9c",
-    "bytes_per_launch": 602030921,  # 463.22 MB read + 138.81 MB written (one backward launch)
+    "source_sha256": "5dee0023019c8fc6d282e28ca8ad92f98221efaf795218f696f58c43f851356f",
+    "bytes_per_launch": 601887488,  # 463.09 MB read + 138.79 MB written (one backward launch)
 }
 
 
