@@ -189,6 +189,21 @@ def kernel_sha(files=CAUSAL_SOURCES):
     return h.hexdigest()
 
 
+def back_to_back(fn, n, stream):
+    """Total milliseconds of ``n`` calls of ``fn`` issued back to back on
+    ``stream``, CUDA events at the two ends of the run only."""
+    import torch
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(n):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
 def algorithmic_bytes(w):
     """Bytes the method must move per step: forward reads q, k, v and writes
     out; backward reads q, k, v, g and writes dq, dk, dv."""
@@ -323,8 +338,6 @@ def run_ours(args, world, rank, local):
     if cp.causal_product_status(ws_f) != cp.CP_OK or cp.causal_product_status(ws_b) != cp.CP_OK:
         raise RuntimeError("kernel status word reports an error after warm-up")
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
@@ -344,9 +357,16 @@ def run_ours(args, world, rank, local):
         t1_ev.record(stream)
         torch.cuda.synchronize()
         t_end = time.time()
-        # then the per-launch split for the roofline objects: events around
-        # each call (they separate the launches, so this loop is not the
-        # step time)
+        # then the per-launch figures for the roofline objects: K forward
+        # calls back to back, then K backward calls back to back, events at
+        # both ends of each run (an event between two launches would cut the
+        # overlap of one launch's tail with the next one's start)
+        fwd_ms = back_to_back(fwd_call, args.steps, stream)
+        bwd_ms = back_to_back(bwd_call, args.steps, stream)
+        # the same calls one at a time, each between its own events, for
+        # comparison: a launch's start-up and drain are then not hidden
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+               torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
         for e0, e1, e2 in ev:
             e0.record(stream)
             fwd_call()
@@ -356,9 +376,10 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
     barrier(world)
     total_ms = t0_ev.elapsed_time(t1_ev)
-    fwd_ms = sum(a.elapsed_time(b) for a, b, _ in ev)
-    bwd_ms = sum(b.elapsed_time(c) for _, b, c in ev)
+    fwd_iso_ms = sum(a.elapsed_time(b) for a, b, _ in ev)
+    bwd_iso_ms = sum(b.elapsed_time(c) for _, b, c in ev)
     total_ms = max_over_ranks(total_ms, world)
+    fwd_ms, bwd_ms = max_over_ranks(fwd_ms, world), max_over_ranks(bwd_ms, world)
     ms_per_step = total_ms / args.steps
     value = w.token_heads * world * args.steps / (total_ms / 1e3) / 1e6
 
@@ -659,7 +680,8 @@ def run_ours(args, world, rank, local):
                  "achieved": fwd_bytes / (fwd_ms_launch / 1e3) / 1e9,
                  "frac": fwd_bytes / (fwd_ms_launch / 1e3) / 1e9 / hbm_gbs,
                  "traffic": fwd_traffic,
-                 "timing": "forward call: one launch, CUDA events on its stream"}
+                 "timing": "K forward calls (one launch each) back to back, CUDA events "
+                           "on their stream at both ends"}
     bwd_entry = None
     if fused and not segmented:
         if _single_launch_bwd(w):
@@ -673,7 +695,8 @@ def run_ours(args, world, rank, local):
             b_traffic = None
             if PROFILED_TRAFFIC_BWD["source_sha256"] == kernel_sha(BWD_SOURCES):
                 b_traffic = PROFILED_TRAFFIC_BWD["bytes_per_launch"]
-            name, timing = "tc_bwd_kernel", "backward call: one launch, CUDA events on its stream"
+            name, timing = ("tc_bwd_kernel", "K backward calls (one launch each) back to back, "
+                            "CUDA events on their stream at both ends")
         else:
             # the fused dk/dv launch, timed as the backward call minus its
             # causal-product launch (dq, the same bytes as the forward when D = M)
@@ -700,9 +723,12 @@ def run_ours(args, world, rank, local):
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "M": w.M,
                    "features": w.feature, "l2": "inputs larger than L2 (no flush)",
                    "fwd_ms": fwd_ms / args.steps, "bwd_ms": bwd_ms / args.steps,
+                   "fwd_isolated_ms": fwd_iso_ms / args.steps,
+                   "bwd_isolated_ms": bwd_iso_ms / args.steps,
                    "step_timing": "K back-to-back fwd+bwd steps, CUDA events at both ends; "
-                                  "fwd_ms / bwd_ms from a second loop with events around "
-                                  "each call",
+                                  "fwd_ms / bwd_ms: K forward calls back to back, then K "
+                                  "backward calls, events at both ends of each run; "
+                                  "*_isolated_ms: events around every call",
                    "step_hbm_roofline_frac": step_roofline_ms / ms_per_step,
                    "parallelism": f"replicas x{world} (b,h)-sharded, no collective"},
         "roofline": {"bound": "hbm", "achieved": dominant["achieved"], "peak": hbm_gbs,
