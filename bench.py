@@ -52,12 +52,12 @@ BWD_SOURCES = ("cp_tc_dkdv.cu", "cp_tc_dkdv.cuh", "cp_tc_causal.cuh", "cp_tc_com
 # --no-cpu-baseline` (the outputs a launch writes partly stay in the 126 MB
 # L2 when it ends, so its write bytes undercount them).
 PROFILED_TRAFFIC = {
-    "source_sha256": "0d2be64cf466d332f23585e36112161e6982031325f1fb1319c667a16009d75c",
-    "bytes_per_launch": 210026880,  # 201.39 MB read + 8.63 MB written (forward launch)
+    "source_sha256": "98bc186908cfe4841eae7f6c6ceb3ca983e7483c772fd5d68f4faf8697e66771",
+    "bytes_per_launch": 209961088,  # 201.41 MB read + 8.55 MB written (forward launch)
 }
 PROFILED_TRAFFIC_BWD = {
-    "source_sha256": "5dee0023019c8fc6d282e28ca8ad92f98221efaf795218f696f58c43f851356f",
-    "bytes_per_launch": 601887488,  # 463.09 MB read + 138.79 MB written (one backward launch)
+    "source_sha256": "63a4bb5949e45944f0e4937520636b26e7033e969b21d4008f94b86865010618",
+    "bytes_per_launch": 601913472,  # 463.05 MB read + 138.87 MB written (one backward launch)
 }
 
 
@@ -616,6 +616,24 @@ def run_ours(args, world, rank, local):
             "bwd": {"us": fb_ms * 1e3, "bytes": fb_bytes,
                     "frac": fb_bytes / (fb_ms / 1e3) / 1e9 / peak}}
         del rq, rk
+        # out and z from one call: the product kernel writes z too where it
+        # can (reads q, k, v once; writes out and z)
+        fo_n = torch.empty_like(vd)
+        ws_fn = torch.zeros(cp.load_library().causal_product_fwd_norm_workspace_size(
+            w.B, w.H, w.N, w.D, w.M, cp._DTYPES[w.torch_dtype]), dtype=torch.uint8, device=dev)
+        fn_ms = timed(lambda: cp.causal_product_fwd_norm(qd, kd, vd, out=fo_n, z=zb,
+                                                         workspace=ws_fn, stream=stream))
+        fn_bytes = (s_ * (2 * w.D + 2 * w.M) + 4) * w.token_heads
+        norm["fused_with_forward"] = {
+            "call": "causal_product_fwd_norm (out and z)",
+            "launches": cp.causal_product_launch_count(w.B, w.H, w.N, w.D, w.M, w.torch_dtype,
+                                                       norm=True),
+            "us": fn_ms * 1e3, "bytes": fn_bytes,
+            "achieved_gbs": fn_bytes / (fn_ms / 1e3) / 1e9,
+            "frac": fn_bytes / (fn_ms / 1e3) / 1e9 / peak,
+            "forward_alone_us": fwd_ms / args.steps * 1e3,
+            "forward_then_normalizer_us": fwd_ms / args.steps * 1e3 + nf_ms * 1e3}
+        del fo_n, ws_fn
 
     # ---- the forward with the feature map phi(x) = elu(x) + 1 applied to raw
     # x_q, x_k ~ N(0, 1) inside the product kernel (both branches of phi

@@ -108,8 +108,9 @@ CP_API size_t causal_product_workspace_size(int64_t B, int64_t H, int64_t N, int
                                             cp_dtype_t dtype, int backward);
 
 /* Number of kernels one causal_product_fwd (backward = 0),
- * causal_product_bwd (backward = 1), causal_product_fwd_ckpt (backward = 2)
- * or causal_product_bwd_ckpt (backward = 3) call launches for this problem,
+ * causal_product_bwd (backward = 1), causal_product_fwd_ckpt (backward = 2),
+ * causal_product_bwd_ckpt (backward = 3) or causal_product_fwd_norm
+ * (backward = 4) call launches for this problem,
  * with no carried state: 1 per unsplit scan, 3 per scan split into segments
  * (the segment sums, their prefix, the scan), 1 for a scan seeded from
  * precomputed states (dq from checkpoints; bf16 dk from dv's segment
@@ -237,6 +238,35 @@ CP_API cp_status_t causal_product_normalizer(const void* q, const void* k, float
                                              int64_t H, int64_t N, int64_t D, cp_dtype_t dtype,
                                              void* workspace, size_t workspace_bytes,
                                              void* stream);
+
+/* The forward product and its normaliser in one call: out as
+ * causal_product_fwd and z as causal_product_normalizer, from the same q, k
+ * and v (the numerator and the denominator of causal linear attention,
+ * "Transformers are RNNs", section 3.2 with the causal masking of section
+ * 3.3).  z_i = q_i . sum_{j<=i} k_j is the product with a value of ones.
+ *
+ * bf16 problems whose forward is one launch with one 64-column box of q, k
+ * and v (D, M <= 64, unsplit problems: causal_product_launch_count(...,
+ * backward = 4) reports 1) compute z inside that launch.  The intra-tile
+ * terms are the row sums of the masked fp32 q k^T tile, and the earlier
+ * tiles' terms are q_i . (sum of their k) in fp32.  q, k and v are read
+ * once.  Other shapes and dtypes run the product, then the normaliser
+ * kernel.
+ *
+ * Arguments:
+ *   q, k, v, out  as causal_product_fwd;
+ *   z             [B,H,N] fp32, 16-byte aligned, overlapping no other
+ *                 argument; written.
+ * out is bitwise the output of causal_product_fwd on the same inputs.
+ * Workspace: causal_product_fwd_norm_workspace_size (or null: allocated on
+ * the stream).  Errors as causal_product_fwd and causal_product_normalizer;
+ * N = 0 enqueues nothing. */
+CP_API size_t causal_product_fwd_norm_workspace_size(int64_t B, int64_t H, int64_t N, int64_t D,
+                                                     int64_t M, cp_dtype_t dtype);
+CP_API cp_status_t causal_product_fwd_norm(const void* q, const void* k, const void* v, void* out,
+                                           float* z, int64_t B, int64_t H, int64_t N, int64_t D,
+                                           int64_t M, cp_dtype_t dtype, void* workspace,
+                                           size_t workspace_bytes, void* stream);
 
 /* Backward of causal_product_normalizer: with grad_z = dL/dz [B,H,N] fp32,
  *     grad_q_i = grad_z_i sum_{j<=i} k_j,

@@ -30,6 +30,7 @@ __all__ = [
     "CP_OK", "CausalProductError", "causal_product", "causal_product_fwd", "causal_product_bwd",
     "causal_product_fwd_noalloc", "causal_product_noalloc_status", "causal_product_decode",
     "causal_product_normalizer", "causal_product_normalizer_bwd", "normalizer",
+    "causal_product_fwd_norm",
     "causal_product_fwd_feature", "causal_product_bwd_feature", "FEATURES",
     "causal_product_workspace_size", "causal_product_launch_count", "causal_product_status",
     "causal_product_checkpoint_size", "causal_product_fwd_ckpt", "causal_product_bwd_ckpt",
@@ -109,6 +110,11 @@ def load_library(rebuild: bool = True) -> ctypes.CDLL:
             lib.causal_product_noalloc_status.restype = c_int
             lib.causal_product_normalizer_workspace_size.argtypes = [i64, i64, i64, i64, c_int]
             lib.causal_product_normalizer_workspace_size.restype = sz
+            lib.causal_product_fwd_norm_workspace_size.argtypes = [i64, i64, i64, i64, i64, c_int]
+            lib.causal_product_fwd_norm_workspace_size.restype = sz
+            lib.causal_product_fwd_norm.argtypes = [p, p, p, p, p, i64, i64, i64, i64, i64, c_int,
+                                                    p, sz, p]
+            lib.causal_product_fwd_norm.restype = c_int
             lib.causal_product_normalizer.argtypes = [p, p, p, i64, i64, i64, i64, c_int, p, sz, p]
             lib.causal_product_normalizer.restype = c_int
             lib.causal_product_normalizer_bwd.argtypes = [p, p, p, p, p, i64, i64, i64, i64, c_int,
@@ -200,11 +206,12 @@ def causal_product_workspace_size(B: int, H: int, N: int, D: int, M: int,
 
 def causal_product_launch_count(B: int, H: int, N: int, D: int, M: int,
                                 dtype: torch.dtype = torch.bfloat16,
-                                backward: bool = False, ckpt: bool = False) -> int:
+                                backward: bool = False, ckpt: bool = False,
+                                norm: bool = False) -> int:
     """Kernels one causal_product_fwd (or, with ``backward``, _bwd; with
-    ``ckpt``, the checkpoint calls) launches for this shape; -1 for a shape
-    the entry points reject."""
-    mode = int(bool(backward)) + (2 if ckpt else 0)
+    ``ckpt``, the checkpoint calls; with ``norm``, causal_product_fwd_norm)
+    launches for this shape; -1 for a shape the entry points reject."""
+    mode = 4 if norm else int(bool(backward)) + (2 if ckpt else 0)
     return int(load_library().causal_product_launch_count(B, H, N, D, M, _DTYPES[dtype], mode))
 
 
@@ -590,6 +597,35 @@ def causal_product_normalizer(q: torch.Tensor, k: torch.Tensor,
     if rc != CP_OK:
         raise CausalProductError(rc, "causal_product_normalizer")
     return z
+
+
+def causal_product_fwd_norm(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                            out: Optional[torch.Tensor] = None,
+                            z: Optional[torch.Tensor] = None,
+                            workspace: Optional[torch.Tensor] = None,
+                            stream: Optional[torch.cuda.Stream] = None):
+    """(out, z): the causal product and its normaliser z[b,h,i] = q[b,h,i] .
+    sum_{j<=i} k[b,h,j] (float32 [B,H,N]) in one call; one kernel launch for
+    bf16 with D, M <= 64 on unsplit problems."""
+    B, H, N, D, M = _dims(q, k, v)
+    code = _dtype_code(q, k, v)
+    if out is None:
+        out = torch.empty((B, H, N, M), dtype=q.dtype, device=q.device)
+    _check_like(out, (B, H, N, M), q.dtype, "out")
+    if z is None:
+        z = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check_like(z, (B, H, N), torch.float32, "z")
+    _check_device(q, k, v, out, z)
+    lib = load_library()
+    need = lib.causal_product_fwd_norm_workspace_size(B, H, N, D, M, code)
+    if workspace is None:
+        workspace = _workspace(need, q.device)
+    rc = lib.causal_product_fwd_norm(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                     z.data_ptr(), B, H, N, D, M, code, workspace.data_ptr(),
+                                     workspace.numel(), _stream_ptr(stream, q.device))
+    if rc != CP_OK:
+        raise CausalProductError(rc, "causal_product_fwd_norm")
+    return out, z
 
 
 def causal_product_normalizer_bwd(q: torch.Tensor, k: torch.Tensor, grad_z: torch.Tensor,

@@ -158,7 +158,12 @@ int causal_product_launch_count(int64_t B, int64_t H, int64_t N, int64_t D, int6
                                          : cp::simt_plan(BH, N, d, m).G;
     return G > 1 ? 3 : 1;
   };
-  if (backward < 0 || backward > 3) return -1;
+  if (backward < 0 || backward > 4) return -1;
+  // mode 4: the forward with the normaliser (one launch when fused)
+  if (backward == 4) {
+    if (dtype == CP_DTYPE_BF16 && cp::tc_norm_fused(cp::tc_plan(BH, N, D, M))) return 1;
+    return product(D, M) + cp::norm_launch_count(BH, N, D, dtype);
+  }
   // modes 2 and 3 are the checkpoint calls (forward and backward); with
   // checkpoints the dq product is one launch, seeded from them
   const bool ckpt = backward >= 2 && cp::call_ckpt_plan(B, H, N, D, M, dtype).G > 1;
@@ -586,6 +591,64 @@ cp_status_t causal_product_normalizer(const void* q, const void* k, float* z, in
                                       size_t workspace_bytes, void* stream) {
   return causal_product_normalizer_feature(q, k, z, CP_FEATURE_NONE, B, H, N, D, dtype, workspace,
                                            workspace_bytes, stream);
+}
+
+size_t causal_product_fwd_norm_workspace_size(int64_t B, int64_t H, int64_t N, int64_t D,
+                                              int64_t M, cp_dtype_t dtype) {
+  if (cp::check_dims(B, H, N, D, M, dtype) != CP_OK ||
+      cp::check_norm_dims(B, H, N, D, dtype) != CP_OK)
+    return 0;
+  // the product and the separate normaliser run one after the other and
+  // share the area
+  return std::max(cp::workspace_bytes(B * H, N, D, M, dtype, false),
+                  cp::norm_workspace_bytes(B * H, N, D, dtype));
+}
+
+cp_status_t causal_product_fwd_norm(const void* q, const void* k, const void* v, void* out,
+                                    float* z, int64_t B, int64_t H, int64_t N, int64_t D,
+                                    int64_t M, cp_dtype_t dtype, void* workspace,
+                                    size_t workspace_bytes, void* stream_) {
+  cp_status_t st = cp::check_dims(B, H, N, D, M, dtype);
+  if (st == CP_OK) st = cp::check_norm_dims(B, H, N, D, dtype);
+  if (st != CP_OK) return st;
+  if (N > 0 && (!q || !k || !v || !out || !z)) return CP_ERR_INVALID_ARG;
+  if (!cp::aligned16(q) || !cp::aligned16(k) || !cp::aligned16(v) || !cp::aligned16(out) ||
+      !cp::aligned16(z))
+    return CP_ERR_MISALIGNED;
+  const size_t es = dtype == CP_DTYPE_F32 ? 4 : 2;
+  const int64_t BH = B * H;
+  const size_t nqk = (size_t)BH * N * D * es, nv = (size_t)BH * N * M * es;
+  const size_t nz = (size_t)BH * N * sizeof(float);
+  const void* ins[3] = {q, k, v};
+  const size_t in_sz[3] = {nqk, nqk, nv};
+  for (int i = 0; i < 3; ++i)
+    if (cp::overlaps(out, nv, ins[i], in_sz[i]) || cp::overlaps(z, nz, ins[i], in_sz[i]))
+      return CP_ERR_INVALID_ARG;
+  if (cp::overlaps(z, nz, out, nv)) return CP_ERR_INVALID_ARG;
+  const size_t need = std::max(cp::workspace_bytes(BH, N, D, M, dtype, false),
+                               cp::norm_workspace_bytes(BH, N, D, dtype));
+  if (workspace != nullptr && workspace_bytes < need) return CP_ERR_WORKSPACE_TOO_SMALL;
+  if (N == 0) return CP_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  cp::Scratch s;
+  st = cp::acquire(s, workspace, workspace_bytes, need, stream);
+  if (st != CP_OK) return st;
+  int* status = static_cast<int*>(s.base);
+  void* scratch = static_cast<char*>(s.base) + cp::kStatusBytes;
+  cp::Product p{q, k, v, out, BH, N, D, M, false};
+  p.st_ld_r = M;
+  p.st_ld_c = 1;
+  if (dtype == CP_DTYPE_BF16 && cp::tc_norm_fused(cp::tc_plan(BH, N, D, M))) {
+    // one launch: the product kernel also writes z
+    p.z = z;
+    return cp::run_product(p, dtype, static_cast<float*>(scratch), status, stream);
+  }
+  st = cp::run_product(p, dtype, static_cast<float*>(scratch), status, stream);
+  if (st != CP_OK) return st;
+  return cp::norm_launch(0, q, k, nullptr, z, nullptr, BH, N, D, dtype, scratch, status, stream,
+                         0) == cudaSuccess
+             ? CP_OK
+             : CP_ERR_CUDA;
 }
 
 cp_status_t causal_product_normalizer_bwd_feature(const void* q, const void* k,

@@ -74,19 +74,6 @@ __device__ __forceinline__ float row_sumsq(const uint8_t* box, int row) {
   return s;
 }
 
-// Hand a shared-memory stage this thread has read with ordinary loads back
-// to the TMA engine, which will overwrite it: every reading thread orders
-// its loads before the async proxy's later writes (fence.proxy.async) and
-// arrives itself (the barrier counts every reader).  `v` is a value computed
-// from the loads, so they have returned before the fence.  (A single lane
-// arriving after __syncwarp let the next tile's TMA load overwrite rows some
-// lanes were still reading.)
-__device__ __forceinline__ void release_to_tma(uint64_t* bar, float v) {
-  asm volatile("" ::"f"(v));
-  fence_proxy_async_smem();
-  mbar_arrive(bar);
-}
-
 struct TileWalk {
   int tiles_per_problem;
   int n_tiles;  // BH * tiles_per_problem

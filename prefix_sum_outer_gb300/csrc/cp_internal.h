@@ -72,6 +72,9 @@ struct Product {
   // bf16: row pitch (elements) of q, k (ld_qk) and of v, out (ld_v, ld_o);
   // 0: dense rows of D or M elements
   int64_t ld_qk = 0, ld_v = 0, ld_o = 0;
+  // bf16 forward of an unsplit problem with D, M <= 64 (tc_norm_fused):
+  // also write the normaliser z = q_i . sum_{j<=i} k_j, [BH][N] fp32
+  float* z = nullptr;
 };
 
 // The dq product (g, v, k) of a backward seeded from a forward's checkpoints
@@ -111,6 +114,11 @@ struct TcPlan {
   bool ok;
 };
 TcPlan tc_plan(int64_t BH, int64_t N, int64_t D, int64_t M);
+// The forward of this plan can write the normaliser in the same launch
+// (Product::z): one 64-column box of q, k and of v, one segment per problem.
+inline bool tc_norm_fused(const TcPlan& p) {
+  return p.ok && p.DP == 64 && p.MB == 64 && p.n_mb == 1 && p.G == 1;
+}
 // Checkpoint plan of a bf16 problem (pure host computation, 152-SM part).
 CkptPlan ckpt_plan(int64_t BH, int64_t N, int64_t D, int64_t M);
 cp_status_t tc_launch(const Product& p, const TcPlan& plan, float* agg, int* status,
@@ -156,6 +164,8 @@ cudaError_t decode_launch(const void* q, const void* k, const void* v, void* out
 // 16-byte multiples only: norm_feature_supported).
 size_t norm_scratch_bytes(int64_t BH, int64_t N, int64_t D, cp_dtype_t dtype);
 bool norm_feature_supported(int64_t D, cp_dtype_t dtype);
+// kernels one forward normaliser call (mode 0) launches
+int norm_launch_count(int64_t BH, int64_t N, int64_t D, cp_dtype_t dtype);
 cudaError_t norm_launch(int mode, const void* q, const void* k, const float* grad_z, float* z,
                         void* out, int64_t BH, int64_t N, int64_t D, cp_dtype_t dtype,
                         void* scratch, int* status, cudaStream_t stream, int feature = 0);

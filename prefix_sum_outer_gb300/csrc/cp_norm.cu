@@ -906,6 +906,12 @@ size_t norm_scratch_bytes(int64_t BH, int64_t N, int64_t D, cp_dtype_t dtype) {
 
 bool norm_feature_supported(int64_t D, cp_dtype_t dtype) { return single_pass(D, dtype); }
 
+int norm_launch_count(int64_t BH, int64_t N, int64_t D, cp_dtype_t dtype) {
+  if (N == 0) return 0;
+  if (single_pass(D, dtype)) return 1;
+  return norm_plan(BH, N, D, dtype).G > 1 ? 2 : 1;
+}
+
 cudaError_t norm_launch(int mode, const void* q, const void* k, const float* grad_z, float* z,
                         void* out, int64_t BH, int64_t N, int64_t D, cp_dtype_t dtype,
                         void* scratch, int* status, cudaStream_t stream, int feature) {

@@ -16,25 +16,29 @@ namespace tc {
 template <bool EXT>
 using KArgs = std::conditional_t<EXT, ArgsX, Args>;
 
-template <int DP, int MB, bool AGG_ONLY, bool STATE_OUT, bool FEAT, bool CKPT, bool SEED>
+template <int DP, int MB, bool AGG_ONLY, bool STATE_OUT, bool FEAT, bool CKPT, bool SEED,
+          bool NORM>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
-                     const __grid_constant__ CUtensorMap tm_o, const KArgs<CKPT || SEED> a) {
-  causal_body<DP, MB, AGG_ONLY, STATE_OUT, FEAT, CKPT, SEED, KArgs<CKPT || SEED>>(
+                     const __grid_constant__ CUtensorMap tm_o,
+                     const KArgs<CKPT || SEED || NORM> a) {
+  causal_body<DP, MB, AGG_ONLY, STATE_OUT, FEAT, CKPT, SEED, NORM, KArgs<CKPT || SEED || NORM>>(
       tm_q, tm_k, tm_v, tm_o, a, Phase{(int)blockIdx.x, true, true});
 }
 
 // ------------------------------------------------------------------ host
 template <int DP, int MB, bool AGG, bool STATE_OUT = false, bool FEAT = false, bool CKPT = false,
-          bool SEED = false>
+          bool SEED = false, bool NORM = false>
 cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                        const CUtensorMap& o, const ArgsX& ax, unsigned grid, cudaStream_t st) {
   // the plain kernels get the plain arguments (a copy of the base part)
-  const KArgs<CKPT || SEED> a = ax;
+  const KArgs<CKPT || SEED || NORM> a = ax;
   using L = Layout<DP, MB, AGG>;
-  auto kern = tc_causal_kernel<DP, MB, AGG, STATE_OUT, FEAT, CKPT, SEED>;
+  constexpr int kSmem = L::kSmemBytes + (NORM ? kNormBytes<DP> : 0);
+  static_assert(kSmem <= kSmemLimit, "shared memory overflow");
+  auto kern = tc_causal_kernel<DP, MB, AGG, STATE_OUT, FEAT, CKPT, SEED, NORM>;
   // the shared-memory opt-in is set once per device for each instantiation
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
@@ -42,14 +46,14 @@ cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if ((configured.load(std::memory_order_acquire) & bit) == 0) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = L::kSmemBytes;
+  cfg.dynamicSmemBytes = kSmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -82,7 +86,17 @@ cudaError_t launch_pair(const CUtensorMap& q, const CUtensorMap& k, const CUtens
     return cudaSuccess;
   }
   const unsigned g2 = (unsigned)(problems * plan.G);
-  // (a feature map, a carried state and checkpoints are never combined)
+  // (a feature map, a carried state, checkpoints and the normaliser are
+  // never combined)
+  if constexpr (DP == 64 && MB == 64) {
+    if (a.z != nullptr) {
+      if (plan.G != 1 || a.feature || a.state_out != nullptr || a.state_in != nullptr ||
+          a.ckpt != nullptr || a.reverse)
+        return cudaErrorInvalidValue;
+      return launch_one<DP, MB, false, false, false, false, false, true>(q, k, v, o, a, g2, st);
+    }
+  }
+  if (a.z != nullptr) return cudaErrorInvalidValue;
   if (a.feature) return launch_one<DP, MB, false, false, true>(q, k, v, o, a, g2, st);
   if (a.state_out != nullptr) return launch_one<DP, MB, false, true>(q, k, v, o, a, g2, st);
   if (a.ckpt != nullptr) return launch_one<DP, MB, false, false, false, true>(q, k, v, o, a, g2, st);
@@ -180,6 +194,7 @@ cp_status_t tc_run(const Product& p, const TcPlan& plan, float* agg, int* status
   a.ckpt = p.ckpt;
   a.ck_tiles = p.ck.tiles;
   a.ck_G = p.ck.G;
+  a.z = p.z;
   const int64_t problems = p.BH * plan.n_mb;
   const bool seeded = p.seed != nullptr;
   if (seeded) {

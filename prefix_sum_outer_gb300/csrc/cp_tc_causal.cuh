@@ -37,6 +37,14 @@
 // otherwise, rounded to bf16), before any MMA reads them, so phi(q) and
 // phi(k) never exist in global memory.
 //
+// With the normaliser (the NORM instantiation, forward, D <= 64, one
+// segment per problem) the CTA also writes z_i = q_i . sum_{j<=i} k_j.  The
+// state group, whose warps of lane quarters 2 and 3 hold no state rows at
+// D <= 64 and whose chain has slack, computes q_i . s_k for the tile (s_k =
+// the sum of k over the earlier tiles, in shared memory) and the tile's
+// column sums of k, off the P chain; the P group sums each masked fp32 row
+// of P while packing it (the terms j of the tile) and writes z.
+//
 // Long sequences with few problems are split into G segments per problem;
 // a first launch of the same kernel in aggregate-only mode writes each
 // segment's sum of k v^T, and every segment of the second launch starts
@@ -106,7 +114,15 @@ struct ArgsX : Args {
   const float* seed;
   int64_t seed_bh, seed_seg;
   int seed_seg_off;
+  // NORM instantiation: z [BH][N] fp32, z_i = q_i . sum_{j<=i} k_j
+  float* z;
 };
+
+// Shared memory of the NORM instantiation beyond the layout: q_i . s_k for
+// the tile's 128 rows, s_k and one half of a tile's column sums of k (DP
+// fp32 each).
+template <int DP>
+constexpr int kNormBytes = 128 * 4 + 2 * DP * 4;
 
 // phi(x) = elu(x) + 1 on a pair of bf16 values, in packed bf16x2
 // arithmetic: phi(x) = e^min(x, 0) + max(x, 0), with min and max exact
@@ -201,13 +217,18 @@ struct Layout {
 // SEED: segments start from precomputed states (a.seed) instead of the
 // prefix of a segment-sum pass (separate instantiations: both cost the
 // plain scan registers and time when compiled in).
+// NORM: the forward scan of an unsplit problem also writes z (a.z).
 // Returns false when a wait gave up.
 template <int DP, int MB, bool AGG_ONLY, bool STATE_OUT, bool FEAT = false, bool CKPT = false,
-          bool SEED = false, typename A = Args>
+          bool SEED = false, bool NORM = false, typename A = Args>
 __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                             const CUtensorMap& tm_v, const CUtensorMap& tm_o,
                                             const A& a, const Phase ph) {
-  static_assert(!(CKPT || SEED) || sizeof(A) == sizeof(ArgsX), "CKPT and SEED take ArgsX");
+  static_assert(!(CKPT || SEED || NORM) || sizeof(A) == sizeof(ArgsX),
+                "CKPT, SEED and NORM take ArgsX");
+  static_assert(!NORM || !(AGG_ONLY || STATE_OUT || FEAT || CKPT || SEED),
+                "the normaliser is written by the plain forward scan alone");
+  static_assert(!NORM || DP == 64, "the normaliser uses the state group's two idle warps");
   using L = Layout<DP, MB, AGG_ONLY>;
   constexpr int NQK = L::NQK;
   constexpr int NV = L::NV;
@@ -239,6 +260,13 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(s_done + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(s_done + 6);
   uint64_t* qk_ready = s_done + 7;          // [NQK] S, O groups -> MMA: Q/K(t) mapped (FEAT)
+  // NORM, after the barriers: q_i . s_k of the tile's rows, s_k, half a
+  // tile's column sums
+  float* z_q = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + L::kBarBytes);
+  float* z_sk = z_q + 128;
+  float* z_part = z_sk + DP;
+  uint64_t* zq_ready = qk_ready + NQK;      // NORM: state group -> P group: z_q of tile t written
+  uint64_t* zq_free = zq_ready + 1;         // NORM: P group -> state group: z_q read
   // the barrier the MMA issuers wait on before reading a Q/K stage
   uint64_t* const qk_bar = FEAT ? qk_ready : full_qk;
   // FEAT: warps that map a tile: the O group, whose read-out has slack (NO
@@ -280,8 +308,13 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
     const uint32_t kRel = AGG_ONLY ? 1 : 2;  // A + B for Q/K, A + C for V
     for (int i = 0; i < NQK; ++i) {
       mbar_init(&full_qk[i], 1);
-      mbar_init(&empty_qk[i], kRel);
+      // NORM: every state-group warp also reads Q (and two of them K)
+      mbar_init(&empty_qk[i], kRel + (NORM ? kSWarps : 0));
       if (FEAT) mbar_init(&qk_ready[i], kMapWarps);
+    }
+    if (NORM) {
+      mbar_init(zq_ready, kSWarps);
+      mbar_init(zq_free, kPWarps);
     }
     for (int i = 0; i < NV; ++i) {
       mbar_init(&full_v[i], 1);
@@ -673,6 +706,10 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
         }
         tmem_st_wait();
       }
+      if (NORM) {
+        for (int d = threadIdx.x - 32 * kSWarp0; d < DP; d += 32 * kSWarps) z_sk[d] = 0.f;
+        named_barrier_sync(2, 32 * kSWarps);
+      }
       for (int it = 0; it < n_it && ok; ++it) {
         const int b = it % NSB;
         uint8_t* sbuf = s_tile + b * L::kSBufBytes;
@@ -716,6 +753,72 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(s_ready);
+        if constexpr (NORM) {
+          // q_i . s_k for the tile's rows (thread = row), then s_k takes the
+          // tile's k: column sums over 64 rows each by the warps of lane
+          // quarters 2 and 3 (no state rows at D <= 64), lane l owning
+          // columns 2l, 2l + 1, four interleaved partial sums; fixed order
+          const int st = it % NQK;
+          if (!mbar_wait(&full_qk[st], (it / NQK) & 1, abort_flag) ||
+              (it > 0 && !mbar_wait(zq_free, (it - 1) & 1, abort_flag))) {
+            ok = false;
+            break;
+          }
+          const uint8_t* q_s = qk_ring + st * L::kQKStage;
+          const uint8_t* k_s = q_s + L::kKOff;
+          float qd[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8) {
+            const uint4 w =
+                *reinterpret_cast<const uint4*>(q_s + sw128_offset(row, 8 * c8, kBoxBytes));
+            const float4* skc = reinterpret_cast<const float4*>(z_sk + 8 * c8);
+            const float4 s0 = skc[0], s1 = skc[1];
+            qd[0] = fmaf(__uint_as_float(w.x << 16), s0.x, qd[0]);
+            qd[1] = fmaf(__uint_as_float(w.x & 0xffff0000u), s0.y, qd[1]);
+            qd[2] = fmaf(__uint_as_float(w.y << 16), s0.z, qd[2]);
+            qd[3] = fmaf(__uint_as_float(w.y & 0xffff0000u), s0.w, qd[3]);
+            qd[0] = fmaf(__uint_as_float(w.z << 16), s1.x, qd[0]);
+            qd[1] = fmaf(__uint_as_float(w.z & 0xffff0000u), s1.y, qd[1]);
+            qd[2] = fmaf(__uint_as_float(w.w << 16), s1.z, qd[2]);
+            qd[3] = fmaf(__uint_as_float(w.w & 0xffff0000u), s1.w, qd[3]);
+          }
+          const float qdot = (qd[0] + qd[1]) + (qd[2] + qd[3]);
+          z_q[row] = qdot;
+          float cs0 = 0.f, cs1 = 0.f;
+          if (wq >= 2) {  // warp-uniform
+            float acc[4][2] = {};
+#pragma unroll 4
+            for (int r = 64 * (wq - 2); r < 64 * (wq - 2) + 64; r += 4) {
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const uint32_t w = *reinterpret_cast<const uint32_t*>(
+                    k_s + sw128_offset(r + u, 2 * lane, kBoxBytes));
+                acc[u][0] += __uint_as_float(w << 16);
+                acc[u][1] += __uint_as_float(w & 0xffff0000u);
+              }
+            }
+            cs0 = (acc[0][0] + acc[1][0]) + (acc[2][0] + acc[3][0]);
+            cs1 = (acc[0][1] + acc[1][1]) + (acc[2][1] + acc[3][1]);
+            if (wq == 3) {  // rows 64..127, for quarter 2 to add
+              z_part[2 * lane] = cs0;
+              z_part[2 * lane + 1] = cs1;
+            }
+          }
+          // this warp's reads of the stage are done: hand it back
+          asm volatile("" ::"f"(qdot + cs0 + cs1));
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&empty_qk[st]);
+            mbar_arrive(zq_ready);
+          }
+          named_barrier_sync(2, 32 * kSWarps);  // every read of s_k done; rows 64..127 summed
+          if (wq == 2) {
+            z_sk[2 * lane] += cs0 + z_part[2 * lane];
+            z_sk[2 * lane + 1] += cs1 + z_part[2 * lane + 1];
+          }
+          named_barrier_sync(2, 32 * kSWarps);  // s_k advanced before the next tile reads it
+        }
         // CKPT: the state before this tile is a checkpoint.  It is written
         // off the state chain, after the copy is handed on, from the hi + lo
         // copy this thread wrote (hi + lo carries 16 significant bits: the
@@ -824,6 +927,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
       if (!mbar_wait(&p_done[b], (it / NP) & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
       const uint32_t pc = lane_base + L::kColP + b * 128;
+      float zrow = 0.f;  // NORM: sum over the row's unmasked fp32 entries, in column order
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         const bool z = a.reverse ? (c < wq) : (c > wq);  // chunk entirely masked
@@ -831,6 +935,26 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
         if (!z) {
           tmem_ld32(pc + 32 * c, r);
           tmem_ld_wait();
+          if (NORM) {
+            // the chunk's kept entries summed as a pairwise tree (forward
+            // mask: all of a chunk left of the diagonal, columns x <= lane of
+            // the diagonal chunk)
+            float t[16];
+            if (c == wq) {  // warp-uniform
+#pragma unroll
+              for (int x = 0; x < 16; ++x)
+                t[x] = (2 * x <= lane ? __uint_as_float(r[2 * x]) : 0.f) +
+                       (2 * x + 1 <= lane ? __uint_as_float(r[2 * x + 1]) : 0.f);
+            } else {
+#pragma unroll
+              for (int x = 0; x < 16; ++x) t[x] = __uint_as_float(r[2 * x]) + __uint_as_float(r[2 * x + 1]);
+            }
+#pragma unroll
+            for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+              for (int x = 0; x < w; ++x) t[x] += t[x + w];
+            zrow += t[0];
+          }
         }
         split_pack_p(r, z, c == wq, lane, a.reverse);
         store_packed_p(pc + 32 * c, r);
@@ -839,6 +963,18 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_ready[b]);
+      if constexpr (NORM) {
+        // z_i = (row sum of P: the terms j of this tile) + q_i . s_k
+        if (!mbar_wait(zq_ready, it & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const float zval = zrow + z_q[row];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(zq_free);
+        const int64_t grow = (int64_t)tile_of(it) * kTile + row;
+        if (grow < a.N) a.z[(int64_t)bh * a.N + grow] = zval;
+      }
     }
     if (!ok) record_timeout(a.status, abort_flag);
   } else {
@@ -931,6 +1067,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
       for (uint64_t* b = bars; b < fin + 3; ++b) mbar_inval(b);
       if (FEAT)
         for (int i = 0; i < NQK; ++i) mbar_inval(&qk_ready[i]);
+
     }
     __syncthreads();
   }

@@ -138,6 +138,19 @@ __device__ __forceinline__ void store_packed_p(uint32_t taddr, const uint32_t (&
     cp::ptx::tmem_st16(taddr, r);
 }
 
+// Hand a shared-memory stage this thread has read with ordinary loads back
+// to the TMA engine, which will overwrite it: every reading thread orders
+// its loads before the async proxy's later writes (fence.proxy.async) and
+// arrives itself (the barrier counts every reader).  `v` is a value computed
+// from the loads, so they have returned before the fence.  (A single lane
+// arriving after __syncwarp let the next tile's TMA load overwrite rows some
+// lanes were still reading.)
+__device__ __forceinline__ void release_to_tma(uint64_t* bar, float v) {
+  asm volatile("" ::"f"(v));
+  cp::ptx::fence_proxy_async_smem();
+  cp::ptx::mbar_arrive(bar);
+}
+
 __device__ __forceinline__ void record_timeout(int* status, volatile int* abort_flag) {
   *abort_flag = 1;
   if (status != nullptr) atomicCAS(status, 0, (int)CP_ERR_TIMEOUT);

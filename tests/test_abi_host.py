@@ -106,7 +106,11 @@ def test_launch_count(lib):
     assert lc(4, 8, 8229, 256, 64, BF16, 1) == 7
     assert lc(4, 8, 8229, 256, 64, BF16, 3) == 5
     assert lc(8, 16, 4096, 64, 64, BF16, 3) == 1
-    assert lc(8, 16, 4096, 64, 64, BF16, 4) == -1
+    # the forward with the normaliser: one launch on the fused shapes, else
+    # the product and the normaliser kernel
+    assert lc(8, 16, 4096, 64, 64, BF16, 4) == 1
+    assert lc(2, 8, 32768, 128, 128, BF16, 4) == 4
+    assert lc(8, 16, 4096, 64, 64, BF16, 5) == -1
     # fp32: 32 problems of 32 tiles split 16 ways; one 64-row tile unsplit
     assert lc(4, 8, 1024, 64, 64, F32, 0) == 3
     assert lc(4, 8, 1024, 64, 64, F32, 1) == 9
