@@ -300,7 +300,14 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
   // carried state
   const bool has_init = has_prefix || seeded || (!AGG_ONLY && a.state_in != nullptr);
   const bool last_seg = a.reverse ? (seg == 0) : (seg == a.G - 1);
-  auto tile_of = [&](int it) { return a.reverse ? (t_end - 1 - it) : (t_first + it); };
+  // The aggregate-only pass walks each segment against the order of the
+  // scan pass that follows it, and keeps what it loads in L2: the scan pass
+  // then starts on the tiles the aggregate pass read last (a segment's sum
+  // is the same in either order; the order is fixed, so it is
+  // deterministic).
+  auto tile_of = [&](int it) {
+    return (a.reverse != 0) != AGG_ONLY ? (t_end - 1 - it) : (t_first + it);
+  };
 
   if (threadIdx.x == 0) {
     // a stage is released by both issuers (A: S / Q S, B: P / P V); in the
@@ -422,7 +429,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
     // Polls both rings and refills whichever has a free stage (V never runs
     // ahead of Q/K).
     if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
+      const uint64_t pol = AGG_ONLY ? policy_evict_last() : policy_evict_first();
       constexpr uint32_t kQKTx = AGG_ONLY ? L::kQBytes : L::kQKBytes;
       int nq = 0, nv = 0;
       uint64_t t0 = globaltimer();
