@@ -658,6 +658,30 @@ def run_ours(args, world, rank, local):
                 "frac": fb / (ff_ms / 1e3) / 1e9 / load_peaks()[0],
                 "plain_fwd_us": fwd_ms / args.steps * 1e3,
                 "timing": "CUDA events over 20 calls"}
+        if w.backward:
+            # the backward with respect to the raw rows: phi on the loaded
+            # tiles, phi' on the stored gradients; the plain backward's bytes
+            fdq, fdk, fdv = torch.empty_like(xq_), torch.empty_like(xk_), torch.empty_like(vd)
+            ws_fb = torch.empty(cp.causal_product_feature_workspace_size(
+                w.B, w.H, w.N, w.D, w.M, w.torch_dtype, backward=True), dtype=torch.uint8,
+                device=dev)
+
+            def feat_bwd():
+                cp.causal_product_bwd_feature(xq_, xk_, vd, gd, "elu1", grad_q=fdq, grad_k=fdk,
+                                              grad_v=fdv, workspace=ws_fb, stream=stream)
+
+            fbw_ms = timed(feat_bwd)
+            bb = s_ * (4 * w.D + 3 * w.M) * w.token_heads
+            feat.update({"bwd_us": fbw_ms * 1e3, "bwd_bytes": bb,
+                         "bwd_achieved_gbs": bb / (fbw_ms / 1e3) / 1e9,
+                         "bwd_frac": bb / (fbw_ms / 1e3) / 1e9 / load_peaks()[0],
+                         "plain_bwd_us": bwd_ms / args.steps * 1e3,
+                         "bwd_kernels": "three tc_causal_kernel products (dq, dv, dk), "
+                                        "no phi workspace"
+                                        if w.dtype == "bf16" else "map, backward, chain rule"})
+            if int(cp.causal_product_status(ws_fb, stream)) != 0:
+                raise RuntimeError("kernel status word reports an error in the feature backward")
+            del fdq, fdk, fdv, ws_fb
         del xq_, xk_, fo
 
     # ---- positive random features (the D = 256 workload's feature map) from

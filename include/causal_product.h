@@ -296,11 +296,15 @@ CP_API cp_status_t causal_product_fwd_feature(const void* q, const void* k, cons
 
 /* Backward of causal_product_fwd_feature: grad_q = phi'(q) * dL/dphi(q),
  * grad_k = phi'(k) * dL/dphi(k) (elementwise), grad_v as causal_product_bwd,
- * with phi'(x) = 1 for x > 0 and e^x otherwise.  Runs phi(q) and phi(k)
- * into the workspace, the product backward on them, then the elementwise
- * chain rule in place on grad_q and grad_k.  Workspace: at least
- * causal_product_feature_workspace_size(..., backward = 1) bytes (NULL:
- * allocated and freed on `stream`). */
+ * with phi'(x) = 1 for x > 0 and e^x otherwise.  bf16: three tensor-core
+ * products on the raw rows (dq from (g, v, phi(k)), dv from the reverse
+ * (phi(k), phi(q), g), dk from the reverse (v, g, phi(q))), phi applied to
+ * the tiles in shared memory and phi' to each gradient element before its
+ * store, so neither phi(q), phi(k) nor an unscaled gradient is written.
+ * fp32 and fp16: phi(q) and phi(k) into the workspace, the product backward
+ * on them, then the elementwise chain rule in place on grad_q and grad_k.
+ * Workspace: at least causal_product_feature_workspace_size(..., backward =
+ * 1) bytes (NULL: allocated and freed on `stream`). */
 CP_API cp_status_t causal_product_bwd_feature(const void* q, const void* k, const void* v,
                                               const void* grad_out, void* grad_q, void* grad_k,
                                               void* grad_v, cp_feature_t feature, int64_t B,
@@ -310,7 +314,8 @@ CP_API cp_status_t causal_product_bwd_feature(const void* q, const void* k, cons
 
 /* Workspace bytes of causal_product_fwd_feature (backward = 0, the same as
  * causal_product_fwd) or causal_product_bwd_feature (backward = 1: the
- * backward's workspace plus phi(q) and phi(k)); 0 for rejected arguments. */
+ * backward's workspace, plus phi(q) and phi(k) for fp32 and fp16); 0 for
+ * rejected arguments. */
 CP_API size_t causal_product_feature_workspace_size(int64_t B, int64_t H, int64_t N, int64_t D,
                                                     int64_t M, cp_dtype_t dtype, int backward);
 

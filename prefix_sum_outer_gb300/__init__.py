@@ -32,7 +32,8 @@ __all__ = [
     "causal_product_normalizer", "causal_product_normalizer_bwd", "normalizer",
     "causal_product_fwd_norm",
     "causal_product_fwd_feature", "causal_product_bwd_feature", "FEATURES",
-    "causal_product_workspace_size", "causal_product_launch_count", "causal_product_status",
+    "causal_product_workspace_size", "causal_product_feature_workspace_size",
+    "causal_product_launch_count", "causal_product_status",
     "causal_product_checkpoint_size", "causal_product_fwd_ckpt", "causal_product_bwd_ckpt",
     "causal_product_fwd_favor", "causal_product_bwd_favor", "causal_product_favor",
     "causal_product_error_string", "library_path", "load_library",
@@ -202,6 +203,14 @@ def causal_product_workspace_size(B: int, H: int, N: int, D: int, M: int,
                                   backward: bool = False) -> int:
     return int(load_library().causal_product_workspace_size(B, H, N, D, M, _DTYPES[dtype],
                                                             int(bool(backward))))
+
+
+def causal_product_feature_workspace_size(B: int, H: int, N: int, D: int, M: int,
+                                          dtype: torch.dtype = torch.bfloat16,
+                                          backward: bool = False) -> int:
+    """Workspace bytes of causal_product_fwd_feature / _bwd_feature."""
+    return int(load_library().causal_product_feature_workspace_size(
+        B, H, N, D, M, _DTYPES[dtype], int(bool(backward))))
 
 
 def causal_product_launch_count(B: int, H: int, N: int, D: int, M: int,

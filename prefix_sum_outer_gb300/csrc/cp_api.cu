@@ -290,7 +290,9 @@ size_t causal_product_feature_workspace_size(int64_t B, int64_t H, int64_t N, in
                                              int64_t M, cp_dtype_t dtype, int backward) {
   if (cp::check_dims(B, H, N, D, M, dtype) != CP_OK) return 0;
   size_t ws = cp::workspace_bytes(B * H, N, D, M, dtype, backward != 0);
-  if (backward) ws += 2 * cp::round_up(cp::feature_copy_bytes(B * H, N, D, dtype));
+  // bf16 maps inside the product kernels; the others keep phi(q), phi(k)
+  if (backward && dtype != CP_DTYPE_BF16)
+    ws += 2 * cp::round_up(cp::feature_copy_bytes(B * H, N, D, dtype));
   return ws;
 }
 
@@ -355,7 +357,8 @@ cp_status_t causal_product_bwd_feature(const void* q, const void* k, const void*
     }
   }
   const size_t bwd_ws = cp::workspace_bytes(BH, N, D, M, dtype, true);
-  const size_t copy = cp::round_up(cp::feature_copy_bytes(BH, N, D, dtype));
+  const size_t copy =
+      dtype == CP_DTYPE_BF16 ? 0 : cp::round_up(cp::feature_copy_bytes(BH, N, D, dtype));
   const size_t need = bwd_ws + 2 * copy;
   if (workspace != nullptr && workspace_bytes < need) return CP_ERR_WORKSPACE_TOO_SMALL;
   if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
@@ -365,6 +368,28 @@ cp_status_t causal_product_bwd_feature(const void* q, const void* k, const void*
   cp::Scratch s;
   st = cp::acquire(s, workspace, workspace_bytes, need, stream);
   if (st != CP_OK) return st;
+  if (dtype == CP_DTYPE_BF16) {
+    // Three products on the raw rows, phi applied to the tiles in shared
+    // memory and phi' to the outputs before their store, so that neither
+    // phi(q), phi(k) nor an unscaled gradient reaches memory:
+    //   dq_i = phi'(q_i) * sum_{j<=i} (g_i . v_j) phi(k_j)   product (g, v, phi(k))
+    //   dv_j = sum_{i>=j} (phi(k_j) . phi(q_i)) g_i         reverse (phi(k), phi(q), g)
+    //   dk_j = phi'(k_j) * sum_{i>=j} (v_j . g_i) phi(q_i)  reverse (v, g, phi(q))
+    int* status = static_cast<int*>(s.base);
+    float* agg = reinterpret_cast<float*>(static_cast<char*>(s.base) + cp::kStatusBytes);
+    cp::Product pq{grad_out, v, k, grad_q, BH, N, M, D, false};
+    pq.feature_v = 1;
+    pq.epi_x = q;
+    cp::Product pv{k, q, grad_out, grad_v, BH, N, D, M, true};
+    pv.feature = feature;
+    cp::Product pk{v, grad_out, q, grad_k, BH, N, M, D, true};
+    pk.feature_v = 1;
+    pk.epi_x = k;
+    st = cp::run_product(pq, dtype, agg, status, stream);
+    if (st == CP_OK) st = cp::run_product(pv, dtype, agg, status, stream);
+    if (st == CP_OK) st = cp::run_product(pk, dtype, agg, status, stream);
+    return st;
+  }
   char* fq = static_cast<char*>(s.base) + bwd_ws;
   char* fk = fq + copy;
   const int64_t n = BH * N * D;

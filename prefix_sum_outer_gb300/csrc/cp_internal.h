@@ -75,6 +75,12 @@ struct Product {
   // bf16 forward of an unsplit problem with D, M <= 64 (tc_norm_fused):
   // also write the normaliser z = q_i . sum_{j<=i} k_j, [BH][N] fp32
   float* z = nullptr;
+  // bf16 backward products on raw rows (feature map cp_feature_t): map v by
+  // phi as it is loaded (feature_v), and multiply each output element by
+  // phi'(x) of the raw rows epi_x ([BH][N][M], the output's shape); used
+  // together
+  int feature_v = 0;
+  const void* epi_x = nullptr;
 };
 
 // The dq product (g, v, k) of a backward seeded from a forward's checkpoints

@@ -17,28 +17,31 @@ template <bool EXT>
 using KArgs = std::conditional_t<EXT, ArgsX, Args>;
 
 template <int DP, int MB, bool AGG_ONLY, bool STATE_OUT, bool FEAT, bool CKPT, bool SEED,
-          bool NORM>
+          bool NORM, bool FEAT_V, bool EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_causal_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_o,
-                     const KArgs<CKPT || SEED || NORM> a) {
-  causal_body<DP, MB, AGG_ONLY, STATE_OUT, FEAT, CKPT, SEED, NORM, KArgs<CKPT || SEED || NORM>>(
-      tm_q, tm_k, tm_v, tm_o, a, Phase{(int)blockIdx.x, true, true});
+                     const __grid_constant__ CUtensorMap tm_x,
+                     const KArgs<CKPT || SEED || NORM || EPI> a) {
+  causal_body<DP, MB, AGG_ONLY, STATE_OUT, FEAT, CKPT, SEED, NORM, FEAT_V, EPI,
+              KArgs<CKPT || SEED || NORM || EPI>>(tm_q, tm_k, tm_v, tm_o, a,
+                                                  Phase{(int)blockIdx.x, true, true}, &tm_x);
 }
 
 // ------------------------------------------------------------------ host
 template <int DP, int MB, bool AGG, bool STATE_OUT = false, bool FEAT = false, bool CKPT = false,
-          bool SEED = false, bool NORM = false>
+          bool SEED = false, bool NORM = false, bool FEAT_V = false, bool EPI = false>
 cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                       const CUtensorMap& o, const ArgsX& ax, unsigned grid, cudaStream_t st) {
+                       const CUtensorMap& o, const ArgsX& ax, unsigned grid, cudaStream_t st,
+                       const CUtensorMap* x = nullptr) {
   // the plain kernels get the plain arguments (a copy of the base part)
-  const KArgs<CKPT || SEED || NORM> a = ax;
+  const KArgs<CKPT || SEED || NORM || EPI> a = ax;
   using L = Layout<DP, MB, AGG>;
   constexpr int kSmem = L::kSmemBytes + (NORM ? kNormBytes<DP> : 0);
   static_assert(kSmem <= kSmemLimit, "shared memory overflow");
-  auto kern = tc_causal_kernel<DP, MB, AGG, STATE_OUT, FEAT, CKPT, SEED, NORM>;
+  auto kern = tc_causal_kernel<DP, MB, AGG, STATE_OUT, FEAT, CKPT, SEED, NORM, FEAT_V, EPI>;
   // the shared-memory opt-in is set once per device for each instantiation
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
@@ -60,13 +63,15 @@ cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, q, k, v, o, a);
+  // the raw-row map of the derivative epilogue (unused elsewhere)
+  return cudaLaunchKernelEx(&cfg, kern, q, k, v, o, x != nullptr ? *x : o, a);
 }
 
 template <int DP, int MB>
 cudaError_t launch_pair(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                         const CUtensorMap& o, ArgsX a, const TcPlan& plan, int64_t problems,
-                        float* agg, bool agg_only, cudaStream_t st) {
+                        float* agg, bool agg_only, cudaStream_t st, bool feat_v,
+                        const CUtensorMap* x) {
   cudaError_t e = cudaSuccess;
   if (plan.G > 1) {
     ArgsX b = a;
@@ -76,6 +81,8 @@ cudaError_t launch_pair(const CUtensorMap& q, const CUtensorMap& k, const CUtens
     b.state_out = nullptr;
     const unsigned g1 = (unsigned)(problems * (plan.G - 1));
     e = a.feature ? launch_one<DP, MB, true, false, true>(q, k, v, o, b, g1, st)
+        : feat_v  ? launch_one<DP, MB, true, false, false, false, false, false, true>(q, k, v, o,
+                                                                                    b, g1, st)
                   : launch_one<DP, MB, true>(q, k, v, o, b, g1, st);
     // each segment's starting state: one slot per second-pass CTA
     if (e == cudaSuccess)
@@ -86,6 +93,15 @@ cudaError_t launch_pair(const CUtensorMap& q, const CUtensorMap& k, const CUtens
     return cudaSuccess;
   }
   const unsigned g2 = (unsigned)(problems * plan.G);
+  if (feat_v || a.epi_x != nullptr) {
+    // a backward product on raw rows: the value map and the derivative
+    // epilogue, together and alone
+    if (!feat_v || a.epi_x == nullptr || x == nullptr || a.feature || a.state_out != nullptr ||
+        a.ckpt != nullptr || a.z != nullptr)
+      return cudaErrorInvalidValue;
+    return launch_one<DP, MB, false, false, false, false, false, false, true, true>(q, k, v, o, a,
+                                                                                  g2, st, x);
+  }
   // (a feature map, a carried state, checkpoints and the normaliser are
   // never combined)
   if constexpr (DP == 64 && MB == 64) {
@@ -169,11 +185,12 @@ namespace {
 cp_status_t tc_run(const Product& p, const TcPlan& plan, float* agg, int* status,
                    cudaStream_t stream, bool agg_only) {
   if (!plan.ok) return CP_ERR_UNSUPPORTED_SHAPE;
-  CUtensorMap mq, mk, mv, mo;
+  CUtensorMap mq, mk, mv, mo, mx;
   if (!tc::make_map(&mq, p.q, p.BH, p.N, p.D, p.ld_qk) ||
       !tc::make_map(&mk, p.k, p.BH, p.N, p.D, p.ld_qk) ||
       !tc::make_map(&mv, p.v, p.BH, p.N, p.M, p.ld_v) ||
-      !tc::make_map(&mo, p.out, p.BH, p.N, p.M, p.ld_o))
+      !tc::make_map(&mo, p.out, p.BH, p.N, p.M, p.ld_o) ||
+      (p.epi_x != nullptr && !tc::make_map(&mx, p.epi_x, p.BH, p.N, p.M, p.ld_o)))
     return CP_ERR_UNSUPPORTED_SHAPE;
   tc::ArgsX a{};
   a.N = p.N;
@@ -195,12 +212,14 @@ cp_status_t tc_run(const Product& p, const TcPlan& plan, float* agg, int* status
   a.ck_tiles = p.ck.tiles;
   a.ck_G = p.ck.G;
   a.z = p.z;
+  a.epi_x = p.epi_x;
   const int64_t problems = p.BH * plan.n_mb;
   const bool seeded = p.seed != nullptr;
   if (seeded) {
     // segments each seeded from a precomputed state (read through the
     // carried-state strides; no carried state besides)
     if (agg_only || p.seed_G < 2 || p.seed_tiles < 1 || p.state_in != nullptr || p.feature ||
+        p.feature_v || p.epi_x != nullptr ||
         (int64_t)(p.seed_G - 1) * p.seed_tiles >= plan.n_tiles)
       return CP_ERR_INVALID_ARG;
     a.G = p.seed_G;
@@ -216,7 +235,8 @@ cp_status_t tc_run(const Product& p, const TcPlan& plan, float* agg, int* status
   if (plan.DP == DP_ && plan.MB == MB_)                                                       \
     e = seeded ? tc::launch_seeded<DP_, MB_>(mq, mk, mv, mo, a, problems, stream)             \
                : tc::launch_pair<DP_, MB_>(mq, mk, mv, mo, a, plan, problems, agg, agg_only,  \
-                                           stream);                                           \
+                                           stream, p.feature_v != 0,                          \
+                                           p.epi_x != nullptr ? &mx : nullptr);               \
   else
   CP_TC_CASE(64, 64)
   CP_TC_CASE(64, 128)

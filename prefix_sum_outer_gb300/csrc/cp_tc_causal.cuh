@@ -45,6 +45,11 @@
 // column sums of k, off the P chain; the P group sums each masked fp32 row
 // of P while packing it (the terms j of the tile) and writes z.
 //
+// FEAT_V maps the value tiles the same way (the value operand is a raw
+// input), and EPI multiplies every output element by phi'(x) = min(1,
+// phi(x)) of a raw row given apart (a.epi_x): the chain rule of the feature
+// map, for the products of a backward whose inputs are raw rows.
+//
 // Long sequences with few problems are split into G segments per problem;
 // a first launch of the same kernel in aggregate-only mode writes each
 // segment's sum of k v^T, and every segment of the second launch starts
@@ -116,6 +121,9 @@ struct ArgsX : Args {
   int seed_seg_off;
   // NORM instantiation: z [BH][N] fp32, z_i = q_i . sum_{j<=i} k_j
   float* z;
+  // EPI instantiation: raw rows x [BH][N][Mc] bf16; each output element is
+  // multiplied by phi'(x) of its position (phi = elu + 1)
+  const void* epi_x;
 };
 
 // Shared memory of the NORM instantiation beyond the layout: q_i . s_k for
@@ -141,6 +149,47 @@ __device__ __forceinline__ uint32_t elu1_bf16x2(uint32_t w) {
   asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(e) : "r"(y));
   asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(e), "r"(mx));
   return r;
+}
+
+// e^min(x, 0) on a bf16 pair: phi'(x) for phi = elu + 1 (1 for x > 0, e^x
+// otherwise), with the exponent formed as in elu1_bf16x2.
+__device__ __forceinline__ uint32_t exp_min0_bf16x2(uint32_t w) {
+  constexpr uint32_t kLog2eHi = 0x3fb93fb9u, kLog2eLo = 0xbb2cbb2cu;
+  uint32_t mn, t, y, e;
+  asm("min.NaN.bf16x2 %0, %1, %2;" : "=r"(mn) : "r"(w), "r"(0u));
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(t) : "r"(mn), "r"(kLog2eLo));
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(y) : "r"(mn), "r"(kLog2eHi), "r"(t));
+  asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(e) : "r"(y));
+  return e;
+}
+
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// The chain rule of phi = elu + 1 on 32 fp32 values of a row: each value,
+// rounded to bf16, times phi'(x) = e^min(x, 0) in bf16, x the bf16 element at
+// the same position of a staged tile (the raw row), and the product stored
+// over it (two bf16 roundings and the bf16 exponential: within the bf16
+// output's own error).
+__device__ __forceinline__ void scale_store_chunk32(uint8_t* tile, int row, int col0,
+                                                    int box_stride, const uint32_t (&r)[32]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint4* p = reinterpret_cast<uint4*>(tile + sw128_offset(row, col0 + 8 * c, box_stride));
+    const uint4 xw = *p;
+    const uint32_t u[4] = {xw.x, xw.y, xw.z, xw.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      o[e] = mul_bf16x2(pack_bf16x2(__uint_as_float(r[8 * c + 2 * e]),
+                                    __uint_as_float(r[8 * c + 2 * e + 1])),
+                        exp_min0_bf16x2(u[e]));
+    }
+    *p = make_uint4(o[0], o[1], o[2], o[3]);
+  }
 }
 
 // AGG: the aggregate-only pass.  It loads no Q and keeps neither state
@@ -218,14 +267,22 @@ struct Layout {
 // prefix of a segment-sum pass (separate instantiations: both cost the
 // plain scan registers and time when compiled in).
 // NORM: the forward scan of an unsplit problem also writes z (a.z).
+// FEAT_V: v is a raw input mapped by phi = elu + 1 in shared memory.
+// EPI: every output element times phi'(x) of the raw row a.epi_x (tm_x: its
+// tensor map, the output's shape).
 // Returns false when a wait gave up.
 template <int DP, int MB, bool AGG_ONLY, bool STATE_OUT, bool FEAT = false, bool CKPT = false,
-          bool SEED = false, bool NORM = false, typename A = Args>
+          bool SEED = false, bool NORM = false, bool FEAT_V = false, bool EPI = false,
+          typename A = Args>
 __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                             const CUtensorMap& tm_v, const CUtensorMap& tm_o,
-                                            const A& a, const Phase ph) {
-  static_assert(!(CKPT || SEED || NORM) || sizeof(A) == sizeof(ArgsX),
-                "CKPT, SEED and NORM take ArgsX");
+                                            const A& a, const Phase ph,
+                                            const CUtensorMap* tm_x = nullptr) {
+  static_assert(!(CKPT || SEED || NORM || EPI) || sizeof(A) == sizeof(ArgsX),
+                "CKPT, SEED, NORM and EPI take ArgsX");
+  static_assert(!(FEAT_V || EPI) || !(FEAT || STATE_OUT || CKPT || SEED || NORM),
+                "the value map and the derivative epilogue serve plain backward products");
+  static_assert(!EPI || !AGG_ONLY, "the aggregate pass writes no output");
   static_assert(!NORM || !(AGG_ONLY || STATE_OUT || FEAT || CKPT || SEED),
                 "the normaliser is written by the plain forward scan alone");
   static_assert(!NORM || DP == 64, "the normaliser uses the state group's two idle warps");
@@ -269,10 +326,26 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
   uint64_t* zq_free = zq_ready + 1;         // NORM: P group -> state group: z_q read
   // the barrier the MMA issuers wait on before reading a Q/K stage
   uint64_t* const qk_bar = FEAT ? qk_ready : full_qk;
+  // FEAT_V: V(t) mapped, by the same warps (after qk_ready; the normaliser's
+  // barriers, which never meet FEAT_V, sit there too)
+  uint64_t* v_ready = qk_ready + NQK;
+  uint64_t* const v_bar = FEAT_V ? v_ready : full_v;
+  // EPI: raw rows of tile t landed in output staging buffer t % kOBufs
+  uint64_t* x_full = v_ready + NV;
   // FEAT: warps that map a tile: the O group, whose read-out has slack (NO
   // accumulators), not the state group, which sits on the state chain; the
   // state group only in the aggregate-only mode, which has no read-out
   constexpr int kMapWarps = AGG_ONLY ? kSWarps : kOWarps;
+  // FEAT, FEAT_V: with a state of at most 64 rows (TMEM lane quarters 0
+  // and 1) the state group's warps of quarters 2 and 3 have no rows: they
+  // map every tile as soon as it lands, apart from the state chain, and the
+  // O group only reads out; wider states leave the map to the O group
+  constexpr bool kQKMapS = false;  // two warps map Q and K too slowly
+  constexpr bool kVMapS = FEAT_V && !AGG_ONLY && DP <= 64;
+  constexpr int kQKMapWarps = kQKMapS ? 2 : kMapWarps;
+  constexpr int kVMapWarps = kVMapS ? 2 : kMapWarps;
+  // the state group's warps that arrive on s_ready
+  constexpr int kSChainWarps = (kQKMapS || kVMapS) ? 2 : kSWarps;
   // a group maps tile it + kAhead during its iteration it: as far ahead as
   // the Q/K ring allows, off the MMA chain (mapping tile it + kAhead needs
   // only the stage tile it - 1 releases)
@@ -317,7 +390,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
       mbar_init(&full_qk[i], 1);
       // NORM: every state-group warp also reads Q (and two of them K)
       mbar_init(&empty_qk[i], kRel + (NORM ? kSWarps : 0));
-      if (FEAT) mbar_init(&qk_ready[i], kMapWarps);
+      if (FEAT) mbar_init(&qk_ready[i], kQKMapWarps);
     }
     if (NORM) {
       mbar_init(zq_ready, kSWarps);
@@ -326,7 +399,9 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
     for (int i = 0; i < NV; ++i) {
       mbar_init(&full_v[i], 1);
       mbar_init(&empty_v[i], kRel);
+      if (FEAT_V) mbar_init(&v_ready[i], kVMapWarps);
     }
+    for (int i = 0; EPI && i < L::kOBufs; ++i) mbar_init(&x_full[i], 1);
     for (int i = 0; i < NP; ++i) {
       mbar_init(&p_done[i], 1);
       mbar_init(&p_ready[i], kPWarps);
@@ -339,7 +414,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
       mbar_init(&o_free[i], kOWarps);
     }
     mbar_init(s_done, 1);
-    mbar_init(s_ready, kSWarps);
+    mbar_init(s_ready, kSChainWarps);
     mbar_init(&fin[0], 1);
     mbar_init(&fin[1], 1);
     mbar_init(&fin[2], 1);
@@ -353,6 +428,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
     if (!AGG_ONLY) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_o);
+      if (EPI) tma_prefetch_desc(tm_x);
     }
   }
   if (warp == 1) {
@@ -406,13 +482,13 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
     };
     if (a.Dr == DP) {
 #pragma unroll 2
-      for (int i = mtid; i < kChunks; i += 32 * kMapWarps) map_chunk(i);
+      for (int i = mtid; i < kChunks; i += 32 * kQKMapWarps) map_chunk(i);
     } else {
       // columns D..DP-1 of the boxes are zero padding, and phi(0) would be
       // 1: leave them.  A box row is 128 bytes (8 chunks of 8 columns)
       // stored with the 128-byte swizzle, so chunk c of row r holds
       // logical chunk c ^ (r % 8).
-      for (int i = mtid; i < kChunks; i += 32 * kMapWarps) {
+      for (int i = mtid; i < kChunks; i += 32 * kQKMapWarps) {
         const int local = i % kTileChunks, b = local / kBoxChunks, rc = local % kBoxChunks;
         const int col0 = b * kBoxCols + (((rc & 7) ^ ((rc >> 3) & 7)) << 3);
         if (col0 < a.Dr) map_chunk(i);
@@ -423,6 +499,40 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
     if (lane == 0) mbar_arrive(&qk_ready[it % NQK]);
     return true;
   };
+
+  // FEAT_V: phi applied in place to the landed V tile of tile it (columns
+  // mb * MB .. of the value), the same way; the issuers wait on v_ready
+  auto map_v = [&](int it, int mtid) -> bool {
+    if (!mbar_wait(&full_v[it % NV], (it / NV) & 1, abort_flag)) return false;
+    uint4* p = reinterpret_cast<uint4*>(v_ring + (it % NV) * L::kVBytes);
+    constexpr int kChunks = L::kVBytes / 16, kBoxChunks = kBoxBytes / 16;
+    auto map_chunk = [&](int i) {
+      uint4 w = p[i];
+      w.x = elu1_bf16x2(w.x);
+      w.y = elu1_bf16x2(w.y);
+      w.z = elu1_bf16x2(w.z);
+      w.w = elu1_bf16x2(w.w);
+      p[i] = w;
+    };
+    if ((mb + 1) * MB <= a.Mc) {
+#pragma unroll 2
+      for (int i = mtid; i < kChunks; i += 32 * kVMapWarps) map_chunk(i);
+    } else {
+      // zero padding beyond column Mc stays zero (phi(0) would be 1)
+      for (int i = mtid; i < kChunks; i += 32 * kVMapWarps) {
+        const int b = i / kBoxChunks, rc = i % kBoxChunks;
+        const int col0 = mb * MB + b * kBoxCols + (((rc & 7) ^ ((rc >> 3) & 7)) << 3);
+        if (col0 < a.Mc) map_chunk(i);
+      }
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&v_ready[it % NV]);
+    return true;
+  };
+  // a group maps V tile it + kAheadV during its iteration it (mapping it
+  // needs only the stage tile it - 1 releases)
+  constexpr int kAheadV = NV - 1;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -531,7 +641,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
       if (AGG_ONLY) {
         for (int it = 0; it < n_it; ++it) {
           if (!mbar_wait(&qk_bar[it % NQK], (it / NQK) & 1, abort_flag) ||
-              !mbar_wait(&full_v[it % NV], (it / NV) & 1, abort_flag)) {
+              !mbar_wait(&v_bar[it % NV], (it / NV) & 1, abort_flag)) {
             ok = false;
             break;
           }
@@ -549,7 +659,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
         while (nQ < n_it) {
           bool progressed = false;
           if (nS < n_it && mbar_test_wait(&qk_bar[nS % NQK], (nS / NQK) & 1) &&
-              mbar_test_wait(&full_v[nS % NV], (nS / NV) & 1) &&
+              mbar_test_wait(&v_bar[nS % NV], (nS / NV) & 1) &&
               mbar_test_wait(s_ready, nS & 1)) {
             tc_fence_after();
             issue_s(nS);
@@ -610,7 +720,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
         for (int it = 0; it < n_it; ++it) {
           const int b = it % NP;
           if (!mbar_wait(&p_ready[b], (it / NP) & 1, abort_flag) ||
-              !mbar_wait(&full_v[it % NV], (it / NV) & 1, abort_flag) ||
+              !mbar_wait(&v_bar[it % NV], (it / NV) & 1, abort_flag) ||
               !mbar_wait(&o_qs[it % NO], (it / NO) & 1, abort_flag)) {
             ok = false;
             break;
@@ -645,6 +755,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
     bool ok = true;
     if (AGG_ONLY) {
       for (int it = 0; FEAT && it < n_it && ok; ++it) ok = map_qk(it, threadIdx.x - 32 * kSWarp0);
+      for (int it = 0; FEAT_V && it < n_it && ok; ++it) ok = map_v(it, threadIdx.x - 32 * kSWarp0);
       if (!ok) {
         record_timeout(a.status, abort_flag);
       } else if (!mbar_wait(s_done, 0, abort_flag)) {
@@ -669,6 +780,10 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
           }
         }
       }
+    } else if ((kQKMapS || kVMapS) && wq >= 2) {
+      // the feature map (no state rows in these lane quarters)
+      for (int it = 0; it < n_it && ok; ++it) ok = kQKMapS ? map_qk(it, row - 64) : map_v(it, row - 64);
+      if (!ok) record_timeout(a.status, abort_flag);
     } else {
       // initial state: the carried state plus the sum of the preceding
       // segments' aggregates (slot seg of agg_in, prefixed between passes)
@@ -988,14 +1103,43 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
     // ------------------------------------------------------------ O group
     const int o_tid = threadIdx.x - 32 * kOWarp0;   // 0..kOThreads-1
     bool ok = true;
+    // EPI: the raw rows of tile j go by TMA into staging buffer j % kOBufs
+    // (the output's box layout) once the store of tile j - kOBufs has read
+    // it; the read-out multiplies each value by phi'(x) of the element at
+    // its own staging position and stores the product there
+    [[maybe_unused]] int x_next = 0;
+    [[maybe_unused]] auto epi_load = [&]() {
+      if constexpr (EPI) {
+        const int b = x_next % L::kOBufs;
+        uint8_t* xb = o_tile + b * L::kOBytes;
+        mbar_arrive_expect_tx(&x_full[b], L::kOBytes);
+#pragma unroll
+        for (int bx = 0; bx < L::kVBoxes; ++bx)
+          tma_load_3d(xb + bx * kBoxBytes, tm_x, &x_full[b], mb * MB + bx * kBoxCols,
+                      tile_of(x_next) * kTile, bh, policy_evict_first());
+        ++x_next;
+      }
+    };
+    if (EPI && o_tid == 0 && n_it > 0 && !AGG_ONLY) epi_load();
     // FEAT: the O group maps every tile, tile it + kAhead before the
     // read-out of tile it
-    for (int j = 0; FEAT && !AGG_ONLY && j < kAhead && j < n_it && ok; ++j)
+    for (int j = 0; FEAT && !kQKMapS && !AGG_ONLY && j < kAhead && j < n_it && ok; ++j)
       ok = map_qk(j, o_tid);
+    for (int j = 0; FEAT_V && !kVMapS && !AGG_ONLY && j < kAheadV && j < n_it && ok; ++j)
+      ok = map_v(j, o_tid);
     for (int it = 0; !AGG_ONLY && it < n_it && ok; ++it) {
-      if (FEAT && it + kAhead < n_it && !map_qk(it + kAhead, o_tid)) {
+      if (FEAT && !kQKMapS && it + kAhead < n_it && !map_qk(it + kAhead, o_tid)) {
         ok = false;
         break;
+      }
+      if (FEAT_V && !kVMapS && it + kAheadV < n_it && !map_v(it + kAheadV, o_tid)) {
+        ok = false;
+        break;
+      }
+      if (EPI && L::kOBufs == 2 && o_tid == 0 && it + 1 < n_it) {
+        // the other buffer's last store (tile it - 1) has been read
+        tma_store_wait_read_all();
+        epi_load();
       }
       uint8_t* ob = o_tile + (it % L::kOBufs) * L::kOBytes;
       if (!mbar_wait(&o_done[it % NO], (it / NO) & 1, abort_flag)) {
@@ -1024,17 +1168,36 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&o_free[it % NO]);
-        wait_staging();
+        if constexpr (EPI) {
+          if (!mbar_wait(&x_full[it % L::kOBufs], (it / L::kOBufs) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
 #pragma unroll
-        for (int c = 0; c < MB / 32; ++c) store_chunk32(ob, row, c * 32, kBoxBytes, r[c]);
+          for (int c = 0; c < MB / 32; ++c) scale_store_chunk32(ob, row, c * 32, kBoxBytes, r[c]);
+        } else {
+          wait_staging();
+#pragma unroll
+          for (int c = 0; c < MB / 32; ++c) store_chunk32(ob, row, c * 32, kBoxBytes, r[c]);
+        }
       } else {
-        wait_staging();
+        if constexpr (EPI) {
+          if (!mbar_wait(&x_full[it % L::kOBufs], (it / L::kOBufs) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+        } else {
+          wait_staging();
+        }
 #pragma unroll 1
         for (int c = 0; c < MB / 32; ++c) {
           uint32_t r[32];
           tmem_ld32(t_o + c * 32, r);
           tmem_ld_wait();
-          store_chunk32(ob, row, c * 32, kBoxBytes, r);
+          if constexpr (EPI)
+            scale_store_chunk32(ob, row, c * 32, kBoxBytes, r);
+          else
+            store_chunk32(ob, row, c * 32, kBoxBytes, r);
         }
         tc_fence_before();
         __syncwarp();
@@ -1048,9 +1211,19 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
         for (int bx = 0; bx < L::kVBoxes; ++bx)
           tma_store_3d(&tm_o, ob + bx * kBoxBytes, mb * MB + bx * kBoxCols, tile * kTile, bh);
         tma_store_commit();
+        if (EPI && L::kOBufs == 1 && it + 1 < n_it) {
+          tma_store_wait_read_all();
+          epi_load();
+        }
       }
     }
     if (!ok) record_timeout(a.status, abort_flag);
+    if (EPI && o_tid == 0) {
+      // raw-row loads still in flight land before the CTA's memory goes away
+      for (int j = x_next - L::kOBufs; j < x_next; ++j)
+        if (j >= 0) mbar_wait_timeout(&x_full[j % L::kOBufs], (j / L::kOBufs) & 1,
+                                      CP_WAIT_TIMEOUT_NS);
+    }
     if (o_tid == 0) tma_store_wait_all();
   }
 
@@ -1074,6 +1247,10 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
       for (uint64_t* b = bars; b < fin + 3; ++b) mbar_inval(b);
       if (FEAT)
         for (int i = 0; i < NQK; ++i) mbar_inval(&qk_ready[i]);
+      if (FEAT_V)
+        for (int i = 0; i < NV; ++i) mbar_inval(&v_ready[i]);
+      if (EPI)
+        for (int i = 0; i < L::kOBufs; ++i) mbar_inval(&x_full[i]);
 
     }
     __syncthreads();

@@ -363,8 +363,11 @@ def test_feature_argument_checks(lib):
     plain_f = lib.causal_product_workspace_size(8, 16, 4096, 64, 64, BF16, 0)
     plain_b = lib.causal_product_workspace_size(8, 16, 4096, 64, 64, BF16, 1)
     assert ws(8, 16, 4096, 64, 64, BF16, 0) == plain_f
-    # the backward keeps phi(q) and phi(k) next to its own workspace
-    assert ws(8, 16, 4096, 64, 64, BF16, 1) == plain_b + 2 * 8 * 16 * 4096 * 64 * 2
+    # bf16 maps inside the product kernels: the plain backward's workspace
+    assert ws(8, 16, 4096, 64, 64, BF16, 1) == plain_b
+    # fp32 and fp16 keep phi(q) and phi(k) next to the backward's workspace
+    plain_b32 = lib.causal_product_workspace_size(8, 16, 4096, 64, 64, F32, 1)
+    assert ws(8, 16, 4096, 64, 64, F32, 1) == plain_b32 + 2 * 8 * 16 * 4096 * 64 * 4
     assert ws(8, 16, 4096, 12, 64, BF16, 1) == 0
 
     def fwd(**kw):

@@ -30,13 +30,26 @@ FWD_SHAPES = [
     (2, 3, 200, 16, 16, "f32"),
     (1, 2, 513, 36, 20, "f32"),
 ]
+# bf16 runs three products on the raw rows (phi on the loaded tiles, phi' on
+# the stored gradients): every tile geometry of dq/dk (D' = M, M' = D) and dv
+# (D' = D, M' = M), value blocks (D = 256), segmented scans whose aggregate
+# pass maps the value tiles, padded widths on either side, ragged tails
 BWD_SHAPES = [
     (2, 4, 1000, 64, 64, "bf16"),
     (8, 16, 1024, 64, 64, "bf16"),
     (1, 2, 777, 128, 128, "bf16"),
     (2, 2, 400, 40, 64, "bf16"),
+    (2, 3, 300, 64, 24, "bf16"),
+    (1, 2, 700, 256, 64, "bf16"),
+    (2, 2, 300, 192, 64, "bf16"),
+    (3, 5, 129, 64, 128, "bf16"),
+    (1, 2, 5000, 64, 64, "bf16"),
+    (1, 2, 8229, 128, 128, "bf16"),
+    (1, 3, 1, 64, 64, "bf16"),
     (2, 3, 200, 16, 16, "f32"),
+    (1, 2, 300, 40, 24, "f16"),
 ]
+DT["f16"] = torch.float16
 
 
 def _raw(shape, seed, backward):
@@ -97,3 +110,43 @@ def test_feature_matches_mapped_inputs():
     mapped = cp.causal_product_fwd(phi(q.float()).to(DEV), phi(k.float()).to(DEV), v.to(DEV))
     torch.cuda.synchronize()
     assert row_rel_err(to_np(fused), to_np(mapped)) <= 1e-2
+
+
+def test_feature_backward_bf16_workspace_holds_no_features():
+    """bf16 maps inside the kernels: the feature backward needs no more
+    workspace than the plain backward, and runs in a caller's workspace of
+    exactly that size."""
+    B, H, N, D, M = 2, 4, 1000, 64, 64
+    plain = cp.causal_product_workspace_size(B, H, N, D, M, torch.bfloat16, backward=True)
+    feat = cp.causal_product_feature_workspace_size(B, H, N, D, M, torch.bfloat16, backward=True)
+    assert feat == plain
+    q, k, v, g = _raw((B, H, N, D, M, "bf16"), 9, True)
+    ws = torch.zeros(feat, dtype=torch.uint8, device=DEV)
+    dq, dk, dv = cp.causal_product_bwd_feature(q.to(DEV), k.to(DEV), v.to(DEV), g.to(DEV), "elu1",
+                                               workspace=ws)
+    dq2, dk2, dv2 = cp.causal_product_bwd_feature(q.to(DEV), k.to(DEV), v.to(DEV), g.to(DEV),
+                                                  "elu1")
+    torch.cuda.synchronize()
+    assert cp.causal_product_status(ws) == 0
+    for a, b in ((dq, dq2), (dk, dk2), (dv, dv2)):
+        assert torch.equal(a, b)
+
+
+def test_feature_backward_bf16_matches_mapped_inputs():
+    """The fused bf16 backward agrees with the plain backward on phi(q),
+    phi(k) (phi rounded to bf16 once, as the kernels do) followed by the
+    chain rule in fp32, within the bf16 tolerance: the two differ by the
+    fused path's bf16 phi' (e^min(x, 0) from a bf16 exponent) and product,
+    the composed path's bf16 rounding of the unscaled gradients, and the
+    plain backward's own order of summation (its one-launch dk/dv scan)."""
+    q, k, v, g = _raw((2, 4, 1000, 64, 64, "bf16"), 13, True)
+    qd, kd, vd, gd = (t.to(DEV) for t in (q, k, v, g))
+    phi = lambda x: torch.where(x > 0, x + 1, torch.exp(x)).to(torch.bfloat16)
+    dphi = lambda x: torch.where(x > 0, torch.ones_like(x), torch.exp(x))
+    dq, dk, dv = cp.causal_product_bwd_feature(qd, kd, vd, gd, "elu1")
+    fq, fk, fv = cp.causal_product_bwd(phi(qd.float()), phi(kd.float()), vd, gd)
+    torch.cuda.synchronize()
+    assert row_rel_err(to_np(dv), to_np(fv)) <= 1e-2
+    for got, mapped, x in ((dq, fq, q), (dk, fk, k)):
+        ref = (mapped.float() * dphi(x.to(DEV).float())).cpu().numpy()
+        assert row_rel_err(to_np(got), ref) <= TOL["bf16"]
