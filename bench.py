@@ -52,12 +52,12 @@ BWD_SOURCES = ("cp_tc_dkdv.cu", "cp_tc_dkdv.cuh", "cp_tc_causal.cuh", "cp_tc_com
 # --no-cpu-baseline` (the outputs a launch writes partly stay in the 126 MB
 # L2 when it ends, so its write bytes undercount them).
 PROFILED_TRAFFIC = {
-    "source_sha256": "98bc186908cfe4841eae7f6c6ceb3ca983e7483c772fd5d68f4faf8697e66771",
-    "bytes_per_launch": 209961088,  # 201.41 MB read + 8.55 MB written (forward launch)
+    "source_sha256": "e2d65f69ed9d85b866c7da889434a085b959b9b0a5f4bcb4c65808024b3243b8",
+    "bytes_per_launch": 209917312,  # 201.39 MB read + 8.52 MB written (forward launch)
 }
 PROFILED_TRAFFIC_BWD = {
-    "source_sha256": "63a4bb5949e45944f0e4937520636b26e7033e969b21d4008f94b86865010618",
-    "bytes_per_launch": 601913472,  # 463.05 MB read + 138.87 MB written (one backward launch)
+    "source_sha256": "b7a433b6007ca190be12401962352e300b4269ee29e2f6d057a0ec9d46bf1916",
+    "bytes_per_launch": 601920000,  # 463.18 MB read + 138.74 MB written (one backward launch)
 }
 
 
@@ -676,8 +676,10 @@ def run_ours(args, world, rank, local):
                          "bwd_achieved_gbs": bb / (fbw_ms / 1e3) / 1e9,
                          "bwd_frac": bb / (fbw_ms / 1e3) / 1e9 / load_peaks()[0],
                          "plain_bwd_us": bwd_ms / args.steps * 1e3,
-                         "bwd_kernels": "three tc_causal_kernel products (dq, dv, dk), "
-                                        "no phi workspace"
+                         "bwd_kernels": ("D, M <= 64: the dk/dv scan and the dq scan of "
+                                         "tc_bwd_kernel on raw rows (phi on the loaded tiles, "
+                                         "phi' on the stored gradients); wider: three "
+                                         "tc_causal_kernel products; no phi workspace")
                                         if w.dtype == "bf16" else "map, backward, chain rule"})
             if int(cp.causal_product_status(ws_fb, stream)) != 0:
                 raise RuntimeError("kernel status word reports an error in the feature backward")

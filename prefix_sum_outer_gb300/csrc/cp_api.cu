@@ -377,6 +377,14 @@ cp_status_t causal_product_bwd_feature(const void* q, const void* k, const void*
     //   dk_j = phi'(k_j) * sum_{i>=j} (v_j . g_i) phi(q_i)  reverse (v, g, phi(q))
     int* status = static_cast<int*>(s.base);
     float* agg = reinterpret_cast<float*>(static_cast<char*>(s.base) + cp::kStatusBytes);
+    // D, M <= 64: dk and dv from one reverse scan that maps q and k (dK
+    // times phi'(k) from the mapped K box), dq as below, in one launch on
+    // unsplit problems
+    const cp::TcPlan plan = cp::tc_plan(BH, N, D, M);
+    if (cp::tc_dkdv_supported(plan))
+      return cp::tc_bwd_launch(q, k, v, grad_out, grad_q, grad_k, grad_v, nullptr, nullptr,
+                               nullptr, BH, N, D, M, plan, agg, status, nullptr, cp::CkptPlan{},
+                               stream, true);
     cp::Product pq{grad_out, v, k, grad_q, BH, N, M, D, false};
     pq.feature_v = 1;
     pq.epi_x = q;

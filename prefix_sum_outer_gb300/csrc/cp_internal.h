@@ -148,13 +148,15 @@ cudaError_t seg_prefix_launch(float* agg, int64_t P, int G, int64_t E, bool reve
 // them (on split problems; the one-launch backward keeps whole dq scans).
 bool tc_dkdv_supported(const TcPlan& plan);
 // state_in (S_0), grad_state_out (dL/dS_N) and grad_state_in (dL/dS_0) are
-// [BH][D][M] fp32 or null.
+// [BH][D][M] fp32 or null.  feature: q and k are raw rows of phi = elu + 1
+// (mapped inside the scans; dq and dk are the gradients with respect to the
+// raw rows); no state, no checkpoints.
 cp_status_t tc_bwd_launch(const void* q, const void* k, const void* v, const void* g, void* dq,
                           void* dk, void* dv, const float* state_in,
                           const float* grad_state_out, float* grad_state_in, int64_t BH,
                           int64_t N, int64_t D, int64_t M, const TcPlan& plan, float* agg,
                           int* status, const float* ckpt, const CkptPlan& ck,
-                          cudaStream_t stream);
+                          cudaStream_t stream, bool feature = false);
 
 // ---- decoding step (SIMT): S += k v^T, out = S^T q for every problem;
 // M <= 256

@@ -13,9 +13,6 @@
 namespace cp {
 namespace tc {
 
-template <bool EXT>
-using KArgs = std::conditional_t<EXT, ArgsX, Args>;
-
 template <int DP, int MB, bool AGG_ONLY, bool STATE_OUT, bool FEAT, bool CKPT, bool SEED,
           bool NORM, bool FEAT_V, bool EPI>
 __global__ void __launch_bounds__(kThreads, 1)

@@ -56,6 +56,7 @@
 // from the fixed-order sum of its predecessors' aggregates (a two-pass scan
 // across segments, deterministic).
 #pragma once
+#include <type_traits>
 #include "cp_tc_common.cuh"
 
 namespace cp {
@@ -126,71 +127,16 @@ struct ArgsX : Args {
   const void* epi_x;
 };
 
+// Kernel arguments: the extended set only where an instantiation reads it
+// (the plain kernels keep the smaller parameter block).
+template <bool EXT>
+using KArgs = std::conditional_t<EXT, ArgsX, Args>;
+
 // Shared memory of the NORM instantiation beyond the layout: q_i . s_k for
 // the tile's 128 rows, s_k and one half of a tile's column sums of k (DP
 // fp32 each).
 template <int DP>
 constexpr int kNormBytes = 128 * 4 + 2 * DP * 4;
-
-// phi(x) = elu(x) + 1 on a pair of bf16 values, in packed bf16x2
-// arithmetic: phi(x) = e^min(x, 0) + max(x, 0), with min and max exact
-// (NaN-propagating) and e^n = 2^(n log2 e) by the change of base.  log2 e
-// is split into two bf16 parts (0x3fb9 = 1.4453125 and 0xbb2c =
-// -0.00262451171875, together within 5e-6 of it) so the product n log2 e
-// is rounded once, by the FMA; 2^y is the hardware base-2 exponential on
-// bf16 pairs, and the sum is rounded to bf16 once.
-__device__ __forceinline__ uint32_t elu1_bf16x2(uint32_t w) {
-  constexpr uint32_t kLog2eHi = 0x3fb93fb9u, kLog2eLo = 0xbb2cbb2cu;
-  uint32_t mn, mx, t, y, e, r;
-  asm("min.NaN.bf16x2 %0, %1, %2;" : "=r"(mn) : "r"(w), "r"(0u));
-  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(mx) : "r"(w), "r"(0u));
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(t) : "r"(mn), "r"(kLog2eLo));
-  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(y) : "r"(mn), "r"(kLog2eHi), "r"(t));
-  asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(e) : "r"(y));
-  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(e), "r"(mx));
-  return r;
-}
-
-// e^min(x, 0) on a bf16 pair: phi'(x) for phi = elu + 1 (1 for x > 0, e^x
-// otherwise), with the exponent formed as in elu1_bf16x2.
-__device__ __forceinline__ uint32_t exp_min0_bf16x2(uint32_t w) {
-  constexpr uint32_t kLog2eHi = 0x3fb93fb9u, kLog2eLo = 0xbb2cbb2cu;
-  uint32_t mn, t, y, e;
-  asm("min.NaN.bf16x2 %0, %1, %2;" : "=r"(mn) : "r"(w), "r"(0u));
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(t) : "r"(mn), "r"(kLog2eLo));
-  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(y) : "r"(mn), "r"(kLog2eHi), "r"(t));
-  asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(e) : "r"(y));
-  return e;
-}
-
-__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-
-// The chain rule of phi = elu + 1 on 32 fp32 values of a row: each value,
-// rounded to bf16, times phi'(x) = e^min(x, 0) in bf16, x the bf16 element at
-// the same position of a staged tile (the raw row), and the product stored
-// over it (two bf16 roundings and the bf16 exponential: within the bf16
-// output's own error).
-__device__ __forceinline__ void scale_store_chunk32(uint8_t* tile, int row, int col0,
-                                                    int box_stride, const uint32_t (&r)[32]) {
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    uint4* p = reinterpret_cast<uint4*>(tile + sw128_offset(row, col0 + 8 * c, box_stride));
-    const uint4 xw = *p;
-    const uint32_t u[4] = {xw.x, xw.y, xw.z, xw.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      o[e] = mul_bf16x2(pack_bf16x2(__uint_as_float(r[8 * c + 2 * e]),
-                                    __uint_as_float(r[8 * c + 2 * e + 1])),
-                        exp_min0_bf16x2(u[e]));
-    }
-    *p = make_uint4(o[0], o[1], o[2], o[3]);
-  }
-}
 
 // AGG: the aggregate-only pass.  It loads no Q and keeps neither state
 // copies nor output staging, so its Q/K stages hold K alone and the whole
@@ -336,16 +282,17 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
   // accumulators), not the state group, which sits on the state chain; the
   // state group only in the aggregate-only mode, which has no read-out
   constexpr int kMapWarps = AGG_ONLY ? kSWarps : kOWarps;
-  // FEAT, FEAT_V: with a state of at most 64 rows (TMEM lane quarters 0
-  // and 1) the state group's warps of quarters 2 and 3 have no rows: they
-  // map every tile as soon as it lands, apart from the state chain, and the
-  // O group only reads out; wider states leave the map to the O group
-  constexpr bool kQKMapS = false;  // two warps map Q and K too slowly
+  // FEAT_V: with a state of at most 64 rows (TMEM lane quarters 0 and 1)
+  // the state group's warps of quarters 2 and 3 have no rows: they map every
+  // V tile as soon as it lands, apart from the state chain, and the O group
+  // only reads out; wider states leave the map to the O group.  (Q and K
+  // tiles, twice the elements, took longer on those two warps than on the
+  // O group: measured 75 against 67 us for the feature forward at B=8 H=16
+  // N=4096 D=M=64.)
   constexpr bool kVMapS = FEAT_V && !AGG_ONLY && DP <= 64;
-  constexpr int kQKMapWarps = kQKMapS ? 2 : kMapWarps;
   constexpr int kVMapWarps = kVMapS ? 2 : kMapWarps;
   // the state group's warps that arrive on s_ready
-  constexpr int kSChainWarps = (kQKMapS || kVMapS) ? 2 : kSWarps;
+  constexpr int kSChainWarps = kVMapS ? 2 : kSWarps;
   // a group maps tile it + kAhead during its iteration it: as far ahead as
   // the Q/K ring allows, off the MMA chain (mapping tile it + kAhead needs
   // only the stage tile it - 1 releases)
@@ -390,7 +337,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
       mbar_init(&full_qk[i], 1);
       // NORM: every state-group warp also reads Q (and two of them K)
       mbar_init(&empty_qk[i], kRel + (NORM ? kSWarps : 0));
-      if (FEAT) mbar_init(&qk_ready[i], kQKMapWarps);
+      if (FEAT) mbar_init(&qk_ready[i], kMapWarps);
     }
     if (NORM) {
       mbar_init(zq_ready, kSWarps);
@@ -482,13 +429,13 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
     };
     if (a.Dr == DP) {
 #pragma unroll 2
-      for (int i = mtid; i < kChunks; i += 32 * kQKMapWarps) map_chunk(i);
+      for (int i = mtid; i < kChunks; i += 32 * kMapWarps) map_chunk(i);
     } else {
       // columns D..DP-1 of the boxes are zero padding, and phi(0) would be
       // 1: leave them.  A box row is 128 bytes (8 chunks of 8 columns)
       // stored with the 128-byte swizzle, so chunk c of row r holds
       // logical chunk c ^ (r % 8).
-      for (int i = mtid; i < kChunks; i += 32 * kQKMapWarps) {
+      for (int i = mtid; i < kChunks; i += 32 * kMapWarps) {
         const int local = i % kTileChunks, b = local / kBoxChunks, rc = local % kBoxChunks;
         const int col0 = b * kBoxCols + (((rc & 7) ^ ((rc >> 3) & 7)) << 3);
         if (col0 < a.Dr) map_chunk(i);
@@ -780,9 +727,9 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
           }
         }
       }
-    } else if ((kQKMapS || kVMapS) && wq >= 2) {
-      // the feature map (no state rows in these lane quarters)
-      for (int it = 0; it < n_it && ok; ++it) ok = kQKMapS ? map_qk(it, row - 64) : map_v(it, row - 64);
+    } else if (kVMapS && wq >= 2) {
+      // the value map (no state rows in these lane quarters)
+      for (int it = 0; it < n_it && ok; ++it) ok = map_v(it, row - 64);
       if (!ok) record_timeout(a.status, abort_flag);
     } else {
       // initial state: the carried state plus the sum of the preceding
@@ -1123,12 +1070,12 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
     if (EPI && o_tid == 0 && n_it > 0 && !AGG_ONLY) epi_load();
     // FEAT: the O group maps every tile, tile it + kAhead before the
     // read-out of tile it
-    for (int j = 0; FEAT && !kQKMapS && !AGG_ONLY && j < kAhead && j < n_it && ok; ++j)
+    for (int j = 0; FEAT && !AGG_ONLY && j < kAhead && j < n_it && ok; ++j)
       ok = map_qk(j, o_tid);
     for (int j = 0; FEAT_V && !kVMapS && !AGG_ONLY && j < kAheadV && j < n_it && ok; ++j)
       ok = map_v(j, o_tid);
     for (int it = 0; !AGG_ONLY && it < n_it && ok; ++it) {
-      if (FEAT && !kQKMapS && it + kAhead < n_it && !map_qk(it + kAhead, o_tid)) {
+      if (FEAT && it + kAhead < n_it && !map_qk(it + kAhead, o_tid)) {
         ok = false;
         break;
       }

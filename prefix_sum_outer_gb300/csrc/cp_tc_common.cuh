@@ -190,5 +190,90 @@ inline bool make_map(CUtensorMap* m, const void* ptr, int64_t BH, int64_t N, int
   return r == CUDA_SUCCESS;
 }
 
+// phi(x) = elu(x) + 1 on a pair of bf16 values, in packed bf16x2
+// arithmetic: phi(x) = e^min(x, 0) + max(x, 0), with min and max exact
+// (NaN-propagating) and e^n = 2^(n log2 e) by the change of base.  log2 e
+// is split into two bf16 parts (0x3fb9 = 1.4453125 and 0xbb2c =
+// -0.00262451171875, together within 5e-6 of it) so the product n log2 e
+// is rounded once, by the FMA; 2^y is the hardware base-2 exponential on
+// bf16 pairs, and the sum is rounded to bf16 once.
+__device__ __forceinline__ uint32_t elu1_bf16x2(uint32_t w) {
+  constexpr uint32_t kLog2eHi = 0x3fb93fb9u, kLog2eLo = 0xbb2cbb2cu;
+  uint32_t mn, mx, t, y, e, r;
+  asm("min.NaN.bf16x2 %0, %1, %2;" : "=r"(mn) : "r"(w), "r"(0u));
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(mx) : "r"(w), "r"(0u));
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(t) : "r"(mn), "r"(kLog2eLo));
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(y) : "r"(mn), "r"(kLog2eHi), "r"(t));
+  asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(e) : "r"(y));
+  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(e), "r"(mx));
+  return r;
+}
+
+// e^min(x, 0) on a bf16 pair: phi'(x) for phi = elu + 1 (1 for x > 0, e^x
+// otherwise), with the exponent formed as in elu1_bf16x2.
+__device__ __forceinline__ uint32_t exp_min0_bf16x2(uint32_t w) {
+  constexpr uint32_t kLog2eHi = 0x3fb93fb9u, kLog2eLo = 0xbb2cbb2cu;
+  uint32_t mn, t, y, e;
+  asm("min.NaN.bf16x2 %0, %1, %2;" : "=r"(mn) : "r"(w), "r"(0u));
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(t) : "r"(mn), "r"(kLog2eLo));
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(y) : "r"(mn), "r"(kLog2eHi), "r"(t));
+  asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(e) : "r"(y));
+  return e;
+}
+
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// The chain rule of phi = elu + 1 on 32 fp32 values of a row: each value,
+// rounded to bf16, times phi'(x) = e^min(x, 0) in bf16, x the bf16 element at
+// the same position of a staged tile (the raw row), and the product stored
+// over it (two bf16 roundings and the bf16 exponential: within the bf16
+// output's own error).
+__device__ __forceinline__ void scale_store_chunk32(uint8_t* tile, int row, int col0,
+                                                    int box_stride, const uint32_t (&r)[32]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint4* p = reinterpret_cast<uint4*>(tile + sw128_offset(row, col0 + 8 * c, box_stride));
+    const uint4 xw = *p;
+    const uint32_t u[4] = {xw.x, xw.y, xw.z, xw.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      o[e] = mul_bf16x2(pack_bf16x2(__uint_as_float(r[8 * c + 2 * e]),
+                                    __uint_as_float(r[8 * c + 2 * e + 1])),
+                        exp_min0_bf16x2(u[e]));
+    }
+    *p = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// The same chain rule with phi'(x) = min(1, phi(x)) read from a staged
+// tile of phi(x) (the mapped operand; 1 for x > 0, where phi(x) = x + 1 >=
+// 1, and e^x otherwise), the product stored at the same position of `dst`.
+__device__ __forceinline__ void scale_store_chunk32_phi(uint8_t* dst, const uint8_t* phi_tile,
+                                                        int row, int col0, int box_stride,
+                                                        const uint32_t (&r)[32]) {
+  constexpr uint32_t kOnes = 0x3f803f80u;  // bf16 pair (1, 1)
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint32_t off = sw128_offset(row, col0 + 8 * c, box_stride);
+    const uint4 fw = *reinterpret_cast<const uint4*>(phi_tile + off);
+    const uint32_t f[4] = {fw.x, fw.y, fw.z, fw.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      uint32_t d;
+      asm("min.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(f[e]), "r"(kOnes));
+      o[e] = mul_bf16x2(pack_bf16x2(__uint_as_float(r[8 * c + 2 * e]),
+                                    __uint_as_float(r[8 * c + 2 * e + 1])),
+                        d);
+    }
+    *reinterpret_cast<uint4*>(dst + off) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 }  // namespace tc
 }  // namespace cp

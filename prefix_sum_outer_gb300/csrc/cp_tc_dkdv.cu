@@ -25,44 +25,50 @@ namespace cp {
 namespace tc {
 namespace {
 
-template <bool STATE_OUT>
+template <bool STATE_OUT, bool FEAT>
 __global__ void __launch_bounds__(dkdv::kThreads, 1)
     tc_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                    const __grid_constant__ CUtensorMap tm_dk,
                    const __grid_constant__ CUtensorMap tm_dv, const dkdv::DkdvArgs a) {
-  dkdv::dkdv_body<STATE_OUT>(tm_q, tm_k, tm_v, tm_g, tm_dk, tm_dv, a,
-                             Phase{(int)blockIdx.x, true, true});
+  dkdv::dkdv_body<STATE_OUT, FEAT>(tm_q, tm_k, tm_v, tm_g, tm_dk, tm_dv, a,
+                                   Phase{(int)blockIdx.x, true, true});
 }
 
 constexpr int kDqPerSpare = 2;
 
 // CTA c < BH: the dk/dv scan of problem c, then dq of problem c when c <
 // n_main_dq.  CTA BH + e: dq of problems n_main_dq + kDqPerSpare * e + j.
-template <bool STATE_OUT>
+// FEAT: q and k are raw rows of phi = elu + 1: the dk/dv scan maps them (see
+// dkdv_body), and the dq scan maps its value operand k and multiplies dq by
+// phi'(q) read through tm_xq (the raw q; aq.epi_x).
+template <bool STATE_OUT, bool FEAT>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                   const __grid_constant__ CUtensorMap tm_dk,
                   const __grid_constant__ CUtensorMap tm_dv,
-                  const __grid_constant__ CUtensorMap tm_dq, const dkdv::DkdvArgs a, const Args aq,
-                  int n_main_dq) {
+                  const __grid_constant__ CUtensorMap tm_dq,
+                  const __grid_constant__ CUtensorMap tm_xq, const dkdv::DkdvArgs a,
+                  const KArgs<FEAT> aq, int n_main_dq) {
+  // dq_i = sum_{j<=i} (g_i . v_j) k_j: the forward product (g, v, k)
+  auto dq_scan = [&](int p, bool first, bool last) {
+    return causal_body<dkdv::kW, dkdv::kW, false, false, false, false, false, false, FEAT, FEAT,
+                       KArgs<FEAT>>(tm_g, tm_v, tm_k, tm_dq, aq, Phase{p, first, last}, &tm_xq);
+  };
   const int c = (int)blockIdx.x;
   if (c < a.BH) {
     const bool more = c < n_main_dq;
-    if (dkdv::dkdv_body<STATE_OUT>(tm_q, tm_k, tm_v, tm_g, tm_dk, tm_dv, a, Phase{c, true, !more}) &&
+    if (dkdv::dkdv_body<STATE_OUT, FEAT>(tm_q, tm_k, tm_v, tm_g, tm_dk, tm_dv, a,
+                                         Phase{c, true, !more}) &&
         more)
-      causal_body<dkdv::kW, dkdv::kW, false, false>(tm_g, tm_v, tm_k, tm_dq, aq,
-                                                    Phase{c, false, true});
+      dq_scan(c, false, true);
     return;
   }
-  // dq_i = sum_{j<=i} (g_i . v_j) k_j: the forward product (g, v, k)
   const int p0 = n_main_dq + kDqPerSpare * (c - a.BH);
   const int n = min(kDqPerSpare, a.BH - p0);
   for (int j = 0; j < n; ++j)
-    if (!causal_body<dkdv::kW, dkdv::kW, false, false>(tm_g, tm_v, tm_k, tm_dq, aq,
-                                                       Phase{p0 + j, j == 0, j == n - 1}))
-      return;
+    if (!dq_scan(p0 + j, j == 0, j == n - 1)) return;
 }
 
 static_assert(dkdv::kThreads == kThreads, "both scans run on the same CTA");
@@ -116,12 +122,16 @@ cp_status_t tc_bwd_launch(const void* q, const void* k, const void* v, const voi
                           const float* grad_state_out, float* grad_state_in, int64_t BH,
                           int64_t N, int64_t D, int64_t M, const TcPlan& plan, float* agg,
                           int* status, const float* ckpt, const CkptPlan& ck,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, bool feature) {
   using namespace tc;
   // checkpoints replace the carried S_0 (they already contain it) and need
   // the segment geometry of the dq product
   const bool seeded = ckpt != nullptr && ck.G > 1;
   if (seeded && state_in != nullptr) return CP_ERR_INVALID_ARG;
+  // the feature backward (raw q, k) carries no state and takes no checkpoints
+  if (feature && (state_in != nullptr || grad_state_out != nullptr || grad_state_in != nullptr ||
+                  ckpt != nullptr))
+    return CP_ERR_INVALID_ARG;
   if (!tc_dkdv_supported(plan)) return CP_ERR_UNSUPPORTED_SHAPE;
   CUtensorMap mq, mk, mv, mg, mdk, mdv;
   if (!make_map(&mq, q, BH, N, D) || !make_map(&mk, k, BH, N, D) || !make_map(&mv, v, BH, N, M) ||
@@ -148,7 +158,7 @@ cp_status_t tc_bwd_launch(const void* q, const void* k, const void* v, const voi
     // one launch: dk/dv scans on BH CTAs, dq scans on the spare SMs first
     CUtensorMap mdq;
     if (!make_map(&mdq, dq, BH, N, D)) return CP_ERR_UNSUPPORTED_SHAPE;
-    Args aq{};
+    ArgsX aq{};
     aq.N = N;
     aq.n_tiles = plan.n_tiles;
     aq.seg_tiles = plan.n_tiles;
@@ -163,23 +173,32 @@ cp_status_t tc_bwd_launch(const void* q, const void* k, const void* v, const voi
     aq.st_ld_c = M;
     aq.Dr = (int)M;
     aq.Mc = (int)D;
+    // the feature backward: dq times phi'(q), the raw q read with q's map
+    aq.epi_x = feature ? q : nullptr;
     const int64_t spare = n_sm - BH;
     const int64_t n_spare_dq = std::min<int64_t>(BH, spare * kDqPerSpare);
     const int n_main_dq = (int)(BH - n_spare_dq);
     const unsigned grid = (unsigned)(BH + (n_spare_dq + kDqPerSpare - 1) / kDqPerSpare);
     constexpr int kSmem = dkdv::kSmemBytes;
-    if (grad_state_in != nullptr) {
+    const Args aq_plain = aq;
+    if (feature) {
       static std::atomic<uint64_t> configured{0};
-      e = set_smem_once(tc_bwd_kernel<true>, kSmem, configured);
+      e = set_smem_once(tc_bwd_kernel<false, true>, kSmem, configured);
       if (e == cudaSuccess)
-        e = launch_bwd(tc_bwd_kernel<true>, grid, kSmem, stream, mq, mk, mv, mg, mdk, mdv, mdq, a,
-                       aq, n_main_dq);
+        e = launch_bwd(tc_bwd_kernel<false, true>, grid, kSmem, stream, mq, mk, mv, mg, mdk, mdv,
+                       mdq, mq, a, aq, n_main_dq);
+    } else if (grad_state_in != nullptr) {
+      static std::atomic<uint64_t> configured{0};
+      e = set_smem_once(tc_bwd_kernel<true, false>, kSmem, configured);
+      if (e == cudaSuccess)
+        e = launch_bwd(tc_bwd_kernel<true, false>, grid, kSmem, stream, mq, mk, mv, mg, mdk, mdv,
+                       mdq, mdq, a, aq_plain, n_main_dq);
     } else {
       static std::atomic<uint64_t> configured{0};
-      e = set_smem_once(tc_bwd_kernel<false>, kSmem, configured);
+      e = set_smem_once(tc_bwd_kernel<false, false>, kSmem, configured);
       if (e == cudaSuccess)
-        e = launch_bwd(tc_bwd_kernel<false>, grid, kSmem, stream, mq, mk, mv, mg, mdk, mdv, mdq,
-                       a, aq, n_main_dq);
+        e = launch_bwd(tc_bwd_kernel<false, false>, grid, kSmem, stream, mq, mk, mv, mg, mdk, mdv,
+                       mdq, mdq, a, aq_plain, n_main_dq);
     }
     return e == cudaSuccess ? CP_OK : CP_ERR_CUDA;
   }
@@ -192,26 +211,39 @@ cp_status_t tc_bwd_launch(const void* q, const void* k, const void* v, const voi
   pq.st_ld_r = 1;
   pq.st_ld_c = M;
   if (seeded) seed_from_ckpt(pq, ckpt, ck);
+  if (feature) {
+    // the value operand k mapped on load, dq times phi'(q)
+    pq.feature_v = 1;
+    pq.epi_x = q;
+  }
   cp_status_t st = tc_launch(pq, tc_plan(BH, N, M, D), agg, status, stream);
   if (st != CP_OK) return st;
   if (plan.G > 1) {
-    const Product pa{k, q, g, dv, BH, N, D, M, true};
+    Product pa{k, q, g, dv, BH, N, D, M, true};
+    // the segment sums of phi(q) g^T: the aggregate pass maps its K operand
+    if (feature) pa.feature = CP_FEATURE_ELU1;
     st = tc_aggregate(pa, plan, agg, status, stream);
     if (st != CP_OK) return st;
   }
   const unsigned grid = (unsigned)(BH * plan.G);
-  if (grad_state_in != nullptr) {
+  if (feature) {
     static std::atomic<uint64_t> configured{0};
-    e = set_smem_once(tc_dkdv_kernel<true>, dkdv::kSmemBytes, configured);
+    e = set_smem_once(tc_dkdv_kernel<false, true>, dkdv::kSmemBytes, configured);
     if (e == cudaSuccess)
-      e = launch_bwd(tc_dkdv_kernel<true>, grid, dkdv::kSmemBytes, stream, mq, mk, mv, mg, mdk,
-                     mdv, a);
+      e = launch_bwd(tc_dkdv_kernel<false, true>, grid, dkdv::kSmemBytes, stream, mq, mk, mv, mg,
+                     mdk, mdv, a);
+  } else if (grad_state_in != nullptr) {
+    static std::atomic<uint64_t> configured{0};
+    e = set_smem_once(tc_dkdv_kernel<true, false>, dkdv::kSmemBytes, configured);
+    if (e == cudaSuccess)
+      e = launch_bwd(tc_dkdv_kernel<true, false>, grid, dkdv::kSmemBytes, stream, mq, mk, mv, mg,
+                     mdk, mdv, a);
   } else {
     static std::atomic<uint64_t> configured{0};
-    e = set_smem_once(tc_dkdv_kernel<false>, dkdv::kSmemBytes, configured);
+    e = set_smem_once(tc_dkdv_kernel<false, false>, dkdv::kSmemBytes, configured);
     if (e == cudaSuccess)
-      e = launch_bwd(tc_dkdv_kernel<false>, grid, dkdv::kSmemBytes, stream, mq, mk, mv, mg, mdk,
-                     mdv, a);
+      e = launch_bwd(tc_dkdv_kernel<false, false>, grid, dkdv::kSmemBytes, stream, mq, mk, mv, mg,
+                     mdk, mdv, a);
   }
   return e == cudaSuccess ? CP_OK : CP_ERR_CUDA;
 }

@@ -94,8 +94,13 @@ __device__ __forceinline__ void pack_p_reverse(uint32_t pc, int wq, int lane) {
 // One CTA's work: the fused reverse scan of one (segment, problem).  The
 // tensor maps are the kernel's __grid_constant__ parameters.  STATE_OUT: the
 // launch writes dL/dS_0 (a separate instantiation, as for the product).
+// FEAT: q and k are raw rows of the feature map phi = elu + 1: the output
+// group maps the Q and K boxes of each stage in place one tile ahead (the
+// MMAs wait for the map), and dK, read out before dV overwrites the K box,
+// is multiplied by phi'(k) = min(1, phi(k)) from that box, so that dK and
+// dV are the gradients with respect to the raw k and v.
 // Returns false when a wait gave up.
-template <bool STATE_OUT>
+template <bool STATE_OUT, bool FEAT = false>
 __device__ __forceinline__ bool dkdv_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                           const CUtensorMap& tm_v, const CUtensorMap& tm_g,
                                           const CUtensorMap& tm_dk, const CUtensorMap& tm_dv,
@@ -118,6 +123,10 @@ __device__ __forceinline__ bool dkdv_body(const CUtensorMap& tm_q, const CUtenso
   uint64_t* fin = s_done + 1;               // [3]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(fin + 3);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(fin + 4);
+  uint64_t* qk_mapped = fin + 5;            // [kNS] FEAT: output group -> issuers: Q, K mapped
+  // what an MMA that reads Q or K waits for
+  uint64_t* const qk_bar = FEAT ? qk_mapped : full;
+  static_assert(!(FEAT && STATE_OUT), "the feature backward carries no state");
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -149,6 +158,7 @@ __device__ __forceinline__ bool dkdv_body(const CUtensorMap& tm_q, const CUtenso
     }
     mbar_init(s_done, 1);
     for (int i = 0; i < 3; ++i) mbar_init(&fin[i], 1);
+    for (int i = 0; FEAT && i < kNS; ++i) mbar_init(&qk_mapped[i], 4);
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -210,7 +220,7 @@ __device__ __forceinline__ bool dkdv_body(const CUtensorMap& tm_q, const CUtenso
       const uint32_t t_s = tmem + kColS;
       bool ok = true;
       for (int it = 0; it < n_it; ++it) {
-        if (!mbar_wait(&full[it % kNS], (it / kNS) & 1, abort_flag) ||
+        if (!mbar_wait(&qk_bar[it % kNS], (it / kNS) & 1, abort_flag) ||
             !mbar_wait(&copy_ready[it % kNSB], (it / kNSB) & 1, abort_flag)) {
           ok = false;
           break;
@@ -254,7 +264,8 @@ __device__ __forceinline__ bool dkdv_body(const CUtensorMap& tm_q, const CUtenso
       const uint32_t off_x = (x == 0 ? 3 : 0) * kBoxBytes;  // G or Q
       bool ok = true;
       for (int it = 0; it < n_it; ++it) {
-        if (!mbar_wait(&full[it % kNS], (it / kNS) & 1, abort_flag) ||
+        // P1 = K Q^T reads mapped boxes; P2 = V G^T does not
+        if (!mbar_wait(x == 0 ? &qk_bar[it % kNS] : &full[it % kNS], (it / kNS) & 1, abort_flag) ||
             (it > 0 && !mbar_wait(&o_done[x], (it - 1) & 1, abort_flag))) {
           ok = false;
           break;
@@ -295,7 +306,8 @@ __device__ __forceinline__ bool dkdv_body(const CUtensorMap& tm_q, const CUtenso
           }
         }
         mma_commit(&qs_done[it % kNSB]);
-        if (!mbar_wait(&p_ready[x], it & 1, abort_flag)) {
+        if (!mbar_wait(&p_ready[x], it & 1, abort_flag) ||
+            (FEAT && x == 1 && !mbar_wait(&qk_mapped[it % kNS], (it / kNS) & 1, abort_flag))) {
           ok = false;
           break;
         }
@@ -454,10 +466,48 @@ __device__ __forceinline__ bool dkdv_body(const CUtensorMap& tm_q, const CUtenso
     // The stage is released after both stores have read it.
     const int o_tid = threadIdx.x - 32 * kOWarp0;
     bool ok = true;
+    // FEAT: phi applied in place to the Q and K boxes of tile it (columns
+    // D.. of a box are zero padding and stay zero; a box row is 8 chunks of
+    // 16 bytes under the 128-byte swizzle: chunk c of row r holds logical
+    // chunk c ^ (r % 8)).  Tile it + 1 is mapped before the read-out of tile
+    // it: its stage was released at the end of iteration it - 2.
+    [[maybe_unused]] auto map_stage = [&](int it) -> bool {
+      if (!mbar_wait(&full[it % kNS], (it / kNS) & 1, abort_flag)) return false;
+      uint4* p = reinterpret_cast<uint4*>(ring + (it % kNS) * kStageBytes);  // Q box, K box
+      constexpr int kChunks = 2 * kBoxBytes / 16, kBoxChunks = kBoxBytes / 16;
+      auto map_chunk = [&](int i) {
+        uint4 w = p[i];
+        w.x = elu1_bf16x2(w.x);
+        w.y = elu1_bf16x2(w.y);
+        w.z = elu1_bf16x2(w.z);
+        w.w = elu1_bf16x2(w.w);
+        p[i] = w;
+      };
+      if (a.D == kW) {
+#pragma unroll 2
+        for (int i = o_tid; i < kChunks; i += 128) map_chunk(i);
+      } else {
+        for (int i = o_tid; i < kChunks; i += 128) {
+          const int rc = i % kBoxChunks;
+          if ((((rc & 7) ^ ((rc >> 3) & 7)) << 3) < a.D) map_chunk(i);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&qk_mapped[it % kNS]);
+      return true;
+    };
+    if (FEAT && n_it > 0) ok = map_stage(0);
     for (int it = 0; it < n_it && ok; ++it) {
       const int st = it % kNS;
       const int row0 = tile_of(it) * kTile;
-      for (int x = 0; x < 2; ++x) {
+      if (FEAT && it + 1 < n_it && !map_stage(it + 1)) {
+        ok = false;
+        break;
+      }
+      for (int xi = 0; xi < 2; ++xi) {
+        // FEAT: dK first, while the K box still holds phi(k)
+        const int x = FEAT ? 1 - xi : xi;
         if (!mbar_wait(&o_done[x], it & 1, abort_flag)) {
           ok = false;
           break;
@@ -483,8 +533,14 @@ __device__ __forceinline__ bool dkdv_body(const CUtensorMap& tm_q, const CUtenso
         __syncwarp();
         if (lane == 0) mbar_arrive(&o_free[x]);
         uint8_t* ob = ring + st * kStageBytes + (x == 0 ? 1 : 2) * kBoxBytes;
-        store_chunk32(ob, row, 0, kBoxBytes, r[0]);
-        store_chunk32(ob, row, 32, kBoxBytes, r[1]);
+        if (FEAT && x == 1) {
+          const uint8_t* kb = ring + st * kStageBytes + kBoxBytes;
+          scale_store_chunk32_phi(ob, kb, row, 0, kBoxBytes, r[0]);
+          scale_store_chunk32_phi(ob, kb, row, 32, kBoxBytes, r[1]);
+        } else {
+          store_chunk32(ob, row, 0, kBoxBytes, r[0]);
+          store_chunk32(ob, row, 32, kBoxBytes, r[1]);
+        }
         fence_proxy_async_smem();
         named_barrier_sync(1, 128);
         if (o_tid == 0) {
@@ -517,8 +573,10 @@ __device__ __forceinline__ bool dkdv_body(const CUtensorMap& tm_q, const CUtenso
   if (!ph.last) {
     // a later scan of this CTA reuses the barriers' memory
     __syncthreads();
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0) {
       for (uint64_t* b = bars; b < fin + 3; ++b) mbar_inval(b);
+      for (int i = 0; FEAT && i < kNS; ++i) mbar_inval(&qk_mapped[i]);
+    }
     __syncthreads();
   }
   return completed;

@@ -30,13 +30,17 @@ FWD_SHAPES = [
     (2, 3, 200, 16, 16, "f32"),
     (1, 2, 513, 36, 20, "f32"),
 ]
-# bf16 runs three products on the raw rows (phi on the loaded tiles, phi' on
-# the stored gradients): every tile geometry of dq/dk (D' = M, M' = D) and dv
-# (D' = D, M' = M), value blocks (D = 256), segmented scans whose aggregate
-# pass maps the value tiles, padded widths on either side, ragged tails
+# bf16 maps phi on the loaded tiles and applies phi' to the stored gradients.
+# D, M <= 64: the fused dk/dv scan and the dq scan, in one launch on unsplit
+# problems fewer than the SMs, else as a dq product and a dk/dv launch (more
+# problems than SMs; segmented scans, whose aggregate passes map their
+# tiles).  Wider: three products, every tile geometry of dq/dk (D' = M,
+# M' = D) and dv (D' = D, M' = M), value blocks (D = 256).  Padded widths on
+# either side, ragged tails.
 BWD_SHAPES = [
     (2, 4, 1000, 64, 64, "bf16"),
     (8, 16, 1024, 64, 64, "bf16"),
+    (16, 16, 300, 64, 64, "bf16"),
     (1, 2, 777, 128, 128, "bf16"),
     (2, 2, 400, 40, 64, "bf16"),
     (2, 3, 300, 64, 24, "bf16"),
