@@ -115,9 +115,13 @@ CP_API size_t causal_product_workspace_size(int64_t B, int64_t H, int64_t N, int
  * (the segment sums, their prefix, the scan), 1 for a scan seeded from
  * precomputed states (dq from checkpoints; bf16 dk from dv's segment
  * prefixes), and 1 for the whole backward when bf16 with D, M <= 64 runs
- * unsplit on fewer problems than SMs.  Pure host computation (the SM count
- * of the current device, else 152).  Returns -1 for arguments the entry
- * points would reject, 0 when N = 0. */
+ * unsplit on fewer problems than SMs.  With the environment variable
+ * CP_SPLIT_SCAN=lookback (read at each call) a bf16 forward scan split into
+ * segments runs as one launch instead of three when its grid fits the SMs
+ * (each segment sums itself, publishes the sum, adds the sums before it in
+ * scan order and scans; the same bits as the two passes), and is counted as
+ * 1.  Pure host computation (the SM count of the current device, else 152).
+ * Returns -1 for arguments the entry points would reject, 0 when N = 0. */
 CP_API int causal_product_launch_count(int64_t B, int64_t H, int64_t N, int64_t D, int64_t M,
                                        cp_dtype_t dtype, int backward);
 

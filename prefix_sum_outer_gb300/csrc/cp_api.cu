@@ -2,6 +2,8 @@
 // carving and the launches of the per-dtype kernels.  See
 // include/causal_product.h for the contract.
 #include <algorithm>
+#include <cstdlib>
+#include <cstring>
 #include <cstdint>
 #include <mutex>
 
@@ -10,6 +12,23 @@
 #include "cp_internal.h"
 
 namespace cp {
+
+bool lookback_enabled() {
+  const char* v = std::getenv("CP_SPLIT_SCAN");
+  return v != nullptr && std::strcmp(v, "lookback") == 0;
+}
+
+int device_sm_count() {
+  int dev = 0, n_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      n_sm <= 0) {
+    cudaGetLastError();  // no device here: plan for the 152-SM part
+    return kPlanSMs;
+  }
+  return n_sm;
+}
+
 namespace {
 
 constexpr size_t kAlign = 256;
@@ -152,45 +171,45 @@ int causal_product_launch_count(int64_t B, int64_t H, int64_t N, int64_t D, int6
   if (cp::check_dims(B, H, N, D, M, dtype) != CP_OK) return -1;
   if (N == 0) return 0;
   const int64_t BH = B * H;
-  // a split scan is three launches: segment sums, their prefix, the scan
-  auto product = [&](int64_t d, int64_t m) {
-    const int G = dtype == CP_DTYPE_BF16 ? cp::tc_plan(BH, N, d, m).G
-                                         : cp::simt_plan(BH, N, d, m).G;
-    return G > 1 ? 3 : 1;
+  // a split scan is three launches: segment sums, their prefix, the scan; a
+  // bf16 forward split scan whose grid fits the device is one
+  auto product = [&](int64_t d, int64_t m, bool reverse) {
+    if (dtype == CP_DTYPE_BF16) {
+      const cp::TcPlan p = cp::tc_plan(BH, N, d, m);
+      if (p.G <= 1) return 1;
+      return !reverse && cp::lookback_enabled() && BH * p.n_mb * p.G <= cp::device_sm_count()
+                 ? 1
+                 : 3;
+    }
+    return cp::simt_plan(BH, N, d, m).G > 1 ? 3 : 1;
   };
   if (backward < 0 || backward > 4) return -1;
   // mode 4: the forward with the normaliser (one launch when fused)
   if (backward == 4) {
     if (dtype == CP_DTYPE_BF16 && cp::tc_norm_fused(cp::tc_plan(BH, N, D, M))) return 1;
-    return product(D, M) + cp::norm_launch_count(BH, N, D, dtype);
+    return product(D, M, false) + cp::norm_launch_count(BH, N, D, dtype);
   }
   // modes 2 and 3 are the checkpoint calls (forward and backward); with
   // checkpoints the dq product is one launch, seeded from them
   const bool ckpt = backward >= 2 && cp::call_ckpt_plan(B, H, N, D, M, dtype).G > 1;
-  if (backward == 0 || backward == 2) return product(D, M);
-  const int dq_launches = ckpt ? 1 : product(M, D);
+  if (backward == 0 || backward == 2) return product(D, M, false);
+  const int dq_launches = ckpt ? 1 : product(M, D, false);
   if (dtype == CP_DTYPE_BF16) {
     const cp::TcPlan plan = cp::tc_plan(BH, N, D, M);
     if (cp::tc_dkdv_supported(plan)) {
-      int dev = 0, n_sm = 0;
-      if (cudaGetDevice(&dev) != cudaSuccess ||
-          cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-        cudaGetLastError();  // no device here: plan for the 152-SM part
-        n_sm = cp::kPlanSMs;
-      }
-      if (plan.G == 1 && BH < n_sm) return 1;
+      if (plan.G == 1 && BH < cp::device_sm_count()) return 1;
       // dq product, the reverse segment sums and their prefix, the dk/dv scan
       return dq_launches + (plan.G > 1 ? 2 : 0) + 1;
     }
   }
   // dq (g, v, k), dv (k, q, g), dk (v, g, q); bf16 dk starts from dv's
   // segment prefixes when dv's scan is split with one value block
-  int dk_launches = product(M, D);
+  int dk_launches = product(M, D, true);
   if (dtype == CP_DTYPE_BF16) {
     const cp::TcPlan pvp = cp::tc_plan(BH, N, D, M);
     if (pvp.ok && pvp.G > 1 && pvp.n_mb == 1) dk_launches = 1;
   }
-  return dq_launches + product(D, M) + dk_launches;
+  return dq_launches + product(D, M, true) + dk_launches;
 }
 
 }  // extern "C"

@@ -25,6 +25,16 @@ namespace cp {
 // Planning is a pure function of the problem so that the workspace size is
 // known on the host without a device; it assumes the 152 SMs of a GB300.
 constexpr int kPlanSMs = 152;
+// SMs of the current device (kPlanSMs when there is none)
+int device_sm_count();
+// Split forward scans in one launch (tc_lookback_kernel) instead of three:
+// environment variable CP_SPLIT_SCAN=lookback, read at each call.  Off by
+// default: measured slower on the 16-problem N = 32768 D = M = 128 forward.
+bool lookback_enabled();
+// flags of a forward split scan run as one launch, after the segments' sums
+inline size_t lb_flag_bytes(int64_t problems, int G) {
+  return ((size_t)problems * G * sizeof(unsigned int) + 15) / 16 * 16;
+}
 constexpr size_t kStatusBytes = 256;
 
 // Checkpoints a bf16 forward product leaves for the backward's dq product:

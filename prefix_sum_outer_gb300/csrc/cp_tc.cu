@@ -64,12 +64,34 @@ cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
   return cudaLaunchKernelEx(&cfg, kern, q, k, v, o, x != nullptr ? *x : o, a);
 }
 
+// A split scan that runs as one launch (tc_lookback_kernel): when enabled,
+// forward, plain or writing checkpoints, and every CTA resident at once (one
+// per SM).
+bool lookback_eligible(const ArgsX& a, bool feat_v, int64_t grid) {
+  if (!lookback_enabled() || a.reverse || a.state_out != nullptr || a.feature || feat_v ||
+      a.epi_x != nullptr || a.z != nullptr)
+    return false;
+  return grid <= device_sm_count();
+}
+
 template <int DP, int MB>
 cudaError_t launch_pair(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                         const CUtensorMap& o, ArgsX a, const TcPlan& plan, int64_t problems,
                         float* agg, bool agg_only, cudaStream_t st, bool feat_v,
                         const CUtensorMap* x) {
   cudaError_t e = cudaSuccess;
+  if (plan.G > 1 && !agg_only && lookback_eligible(a, feat_v, problems * plan.G)) {
+    // one launch: each segment's sum, its prefix, its scan (the prefixes and
+    // the flags follow the sums)
+    const size_t slots = (size_t)problems * plan.G * DP * MB;
+    ArgsX b = a;
+    b.agg_out = agg;
+    b.agg_in = agg + slots;
+    b.lb_flags = reinterpret_cast<unsigned int*>(agg + 2 * slots);
+    e = cudaMemsetAsync(b.lb_flags, 0, sizeof(unsigned int) * (size_t)problems * plan.G, st);
+    if (e != cudaSuccess) return e;
+    return lookback_launch(DP, MB, q, k, v, o, b, (unsigned)(problems * plan.G), st);
+  }
   if (plan.G > 1) {
     ArgsX b = a;
     b.agg_in = nullptr;
@@ -148,7 +170,11 @@ TcPlan tc_plan(int64_t BH, int64_t N, int64_t D, int64_t M) {
   p.seg_tiles = (int)((p.n_tiles + G - 1) / G);
   p.G = p.seg_tiles > 0 ? (p.n_tiles + p.seg_tiles - 1) / p.seg_tiles : 1;
   if (p.G < 1) p.G = 1;
-  p.agg_bytes = p.G > 1 ? sizeof(float) * (size_t)problems * p.G * p.DP * p.MB : 0;
+  // the segments' sums, then (forward scans in one launch) their prefixes
+  // and flags
+  p.agg_bytes = p.G > 1 ? 2 * sizeof(float) * (size_t)problems * p.G * p.DP * p.MB +
+                              lb_flag_bytes(problems, p.G)
+                        : 0;
   // the entry points allow M <= 256; internal products (the gradients of the
   // positive random features, with hi | lo value halves) go to 512
   p.ok = p.DP <= 256 && Mpad <= 512;

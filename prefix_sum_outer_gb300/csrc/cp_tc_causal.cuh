@@ -125,6 +125,10 @@ struct ArgsX : Args {
   // EPI instantiation: raw rows x [BH][N][Mc] bf16; each output element is
   // multiplied by phi'(x) of its position (phi = elu + 1)
   const void* epi_x;
+  // the one-launch split scan (tc_lookback_kernel): agg_out holds each
+  // segment's own sum, slot s written once lb_flags[pidx * G + s] is nonzero;
+  // agg_in (the prefix slots) is filled by the launch itself
+  unsigned int* lb_flags;
 };
 
 // Kernel arguments: the extended set only where an instantiation reads it
@@ -182,9 +186,15 @@ struct Layout {
       (NP >= 2 && rings(kAvail - 4 * kSOneBytes - 2 * kOBytes) / 8 >= 2) ? 2 : 1;
   static constexpr bool kSplit = rings(kAvail - NSB * 2 * kSOneBytes - kOBytes) / 8 >= 1;
   static constexpr int kSBufBytes = (kSplit ? 2 : 1) * kSOneBytes;
-  // output staging: two buffers (one store in flight) when they fit
+  // output staging: two buffers (one store in flight) when they fit next to
+  // the state copies and rings of at least one Q/K and two V stages (a
+  // single V stage would serialise each tile's V load behind the previous
+  // tile's P V)
   static constexpr int kOBufs =
-      rings(kAvail - NSB * kSBufBytes - 2 * kOBytes) / 8 >= (NSB == 2 ? 2 : 1) ? 2 : 1;
+      (rings(kAvail - NSB * kSBufBytes - 2 * kOBytes) / 8 >= (NSB == 2 ? 2 : 1) &&
+       rings(kAvail - NSB * kSBufBytes - 2 * kOBytes) >= 8 + 2)
+          ? 2
+          : 1;
   static constexpr int kSRegion = AGG ? 0 : NSB * kSBufBytes;
   static constexpr int kORegion = AGG ? 0 : kOBufs * kOBytes;
   static constexpr int kFixed = kSRegion + kORegion;
@@ -760,7 +770,9 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
                   a.agg_in + (((size_t)pidx * a.G + s2) * DP + d) * MB + c * 32);
 #pragma unroll
               for (int x = 0; x < 8; ++x) {
-                const float4 f = __ldg(src + x);
+                // (coherent loads: the one-launch split scan writes the
+                // slot within the same launch)
+                const float4 f = __ldcg(src + x);
                 acc[4 * x] += f.x;
                 acc[4 * x + 1] += f.y;
                 acc[4 * x + 2] += f.z;
@@ -1204,6 +1216,14 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
   }
   return completed;
 }
+
+// The split forward scan in one launch (csrc/cp_tc_lookback.cu): a.agg_out
+// the segments' sums and a.agg_in their prefixes, each [P][G][DP][MB];
+// a.lb_flags [P][G] cleared; grid P * G CTAs, all resident at once.  Plain
+// and checkpoint scans.
+cudaError_t lookback_launch(int DP, int MB, const CUtensorMap& q, const CUtensorMap& k,
+                            const CUtensorMap& v, const CUtensorMap& o, const ArgsX& a,
+                            unsigned grid, cudaStream_t st);
 
 }  // namespace tc
 }  // namespace cp

@@ -97,7 +97,7 @@ def test_launch_count(lib):
     assert lc(8, 16, 4096, 64, 64, BF16, 1) == 1
     # 16 problems of 32768 rows: every scan split (sums, prefix, scan),
     # three products in the backward, dk seeded from dv's segment prefixes
-    # (one launch); with checkpoints dq is one seeded launch too
+    # (one launch); with checkpoints dq is one seeded launch
     assert lc(2, 8, 32768, 128, 128, BF16, 0) == 3
     assert lc(2, 8, 32768, 128, 128, BF16, 1) == 7
     assert lc(2, 8, 32768, 128, 128, BF16, 2) == 3
@@ -428,3 +428,24 @@ def test_normalizer_feature_argument_checks(lib):
     b = lib.causal_product_normalizer_bwd_feature
     assert b(A, 2 * A, 3 * A, 4 * A, 5 * A, 5, 1, 2, 64, 16, F32, None, 0, None) == INVALID_ARG
     assert b(A, 2 * A, 3 * A, 4 * A, 5 * A, 1, 1, 2, 64, 12, BF16, None, 0, None) == UNSUPPORTED_SHAPE
+
+
+def test_launch_count_one_launch_split_scan(lib, monkeypatch):
+    """CP_SPLIT_SCAN=lookback: a bf16 forward split scan whose grid fits the
+    SMs is one launch (each segment's sum, its prefix, its scan); reverse
+    scans keep three."""
+    import torch
+    if torch.cuda.is_available() and torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("counts below are for a 152-SM device")
+    lc = lib.causal_product_launch_count
+    monkeypatch.setenv("CP_SPLIT_SCAN", "lookback")
+    assert lc(2, 8, 32768, 128, 128, BF16, 0) == 1
+    assert lc(2, 8, 32768, 128, 128, BF16, 2) == 1
+    # backward: dq (forward, one launch), dv (reverse, three), dk seeded (one)
+    assert lc(2, 8, 32768, 128, 128, BF16, 1) == 5
+    assert lc(4, 8, 8229, 256, 64, BF16, 0) == 1
+    assert lc(1, 2, 8192, 64, 64, BF16, 1) == 4
+    # fp32 keeps its two passes
+    assert lc(4, 8, 1024, 64, 64, F32, 0) == 3
+    monkeypatch.setenv("CP_SPLIT_SCAN", "twopass")
+    assert lc(2, 8, 32768, 128, 128, BF16, 0) == 3
