@@ -45,19 +45,20 @@ UNIT = "Mtok·head/s"
 CAUSAL_SOURCES = ("cp_tc.cu", "cp_tc_causal.cuh", "cp_tc_common.cuh", "sm103_ptx.cuh")
 BWD_SOURCES = ("cp_tc_dkdv.cu", "cp_tc_dkdv.cuh", "cp_tc_causal.cuh", "cp_tc_common.cuh",
                "sm103_ptx.cuh")
-# Both figures are means over 2 launches of each kernel, from
+# Each figure is one launch of its kernel (the fourth of the run, after the
+# three warm-up steps), from
 # `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
-# --clock-control none -k regex:"tc_bwd_kernel|tc_causal_kernel" -s 6 -c 4` of
-# `bench.py --steps 2 --warmup 3 --no-e2e --no-extras --no-others
-# --no-cpu-baseline` (the outputs a launch writes partly stay in the 126 MB
-# L2 when it ends, so its write bytes undercount them).
+# --clock-control none -k regex:<kernel> -s 3 -c 1` of `bench.py --steps 2
+# --warmup 3 --no-e2e --no-extras --no-others --no-cpu-baseline`, one capture
+# per kernel (the outputs a launch writes partly stay in the 126 MB L2 when
+# it ends, so its write bytes undercount them).
 PROFILED_TRAFFIC = {
-    "source_sha256": "e2d65f69ed9d85b866c7da889434a085b959b9b0a5f4bcb4c65808024b3243b8",
-    "bytes_per_launch": 209917312,  # 201.39 MB read + 8.52 MB written (forward launch)
+    "source_sha256": "97bfa1ca46cdab442d5f340e3f7dd6720ae1fd3fa72c3c3e6edeb1171be07480",
+    "bytes_per_launch": 211139584,  # 201.40 MB read + 9.74 MB written (forward launch)
 }
 PROFILED_TRAFFIC_BWD = {
-    "source_sha256": "b7a433b6007ca190be12401962352e300b4269ee29e2f6d057a0ec9d46bf1916",
-    "bytes_per_launch": 601920000,  # 463.18 MB read + 138.74 MB written (one backward launch)
+    "source_sha256": "c41509d35a4df239fccdd0ef556673ee606cee9599eb77dbf339b7d3ebd654b8",
+    "bytes_per_launch": 604890112,  # 463.04 MB read + 141.85 MB written (one backward launch)
 }
 
 
