@@ -46,6 +46,9 @@ def check(q, k, v, g, tol):
 SHAPES = [
     (8, 15, 1000, 64, 64),   # one-launch backward (no checkpoints), ragged tail
     (1, 120, 300, 64, 64),   # one-launch backward, 3 tiles
+    (1, 151, 1100, 64, 64),  # one-launch backward, one spare SM
+    (2, 57, 777, 48, 40),    # one-launch backward, padded widths
+    (1, 130, 100, 64, 64),   # one-launch backward, one tile
     (1, 4, 3000, 64, 64),    # split fused backward: dq seeded, dk/dv two-pass
     (2, 3, 2000, 32, 48),    # padded widths, split
     (1, 2, 4100, 128, 64),   # general backward (D > 64), dq seeded
