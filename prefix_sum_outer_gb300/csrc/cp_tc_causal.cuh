@@ -438,7 +438,9 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
       p[i] = w;
     };
     if (a.Dr == DP) {
-#pragma unroll 2
+      // four chunks in flight per thread (two: the feature forward at B=8
+      // H=16 N=4096 D=M=64 took 67 us, four 59 us, eight 60 us)
+#pragma unroll 4
       for (int i = mtid; i < kChunks; i += 32 * kMapWarps) map_chunk(i);
     } else {
       // columns D..DP-1 of the boxes are zero padding, and phi(0) would be
