@@ -1119,9 +1119,12 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
         }
         named_barrier_sync(1, kOThreads);
       };
-      if constexpr (MB <= 64) {
+      if constexpr (MB <= 64 && !EPI) {
         // the whole row fits in registers: release the buffer before
-        // converting and storing
+        // converting and storing.  (EPI takes the chunk loop below: one copy
+        // of its arithmetic instead of one per chunk; on the feature
+        // backward at B=8 H=16 N=4096 D=M=64, 183 against 192 us, the
+        // instruction stream being the first stall reason there.)
         uint32_t r[MB / 32][32];
 #pragma unroll
         for (int c = 0; c < MB / 32; ++c) tmem_ld32(t_o + c * 32, r[c]);
@@ -1129,18 +1132,9 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&o_free[it % NO]);
-        if constexpr (EPI) {
-          if (!mbar_wait(&x_full[it % L::kOBufs], (it / L::kOBufs) & 1, abort_flag)) {
-            ok = false;
-            break;
-          }
+        wait_staging();
 #pragma unroll
-          for (int c = 0; c < MB / 32; ++c) scale_store_chunk32(ob, row, c * 32, kBoxBytes, r[c]);
-        } else {
-          wait_staging();
-#pragma unroll
-          for (int c = 0; c < MB / 32; ++c) store_chunk32(ob, row, c * 32, kBoxBytes, r[c]);
-        }
+        for (int c = 0; c < MB / 32; ++c) store_chunk32(ob, row, c * 32, kBoxBytes, r[c]);
       } else {
         if constexpr (EPI) {
           if (!mbar_wait(&x_full[it % L::kOBufs], (it / L::kOBufs) & 1, abort_flag)) {
