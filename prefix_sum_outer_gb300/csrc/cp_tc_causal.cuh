@@ -1119,45 +1119,32 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
         }
         named_barrier_sync(1, kOThreads);
       };
-      if constexpr (MB <= 64 && !EPI) {
-        // the whole row fits in registers: release the buffer before
-        // converting and storing.  (EPI takes the chunk loop below: one copy
-        // of its arithmetic instead of one per chunk; on the feature
-        // backward at B=8 H=16 N=4096 D=M=64, 183 against 192 us, the
-        // instruction stream being the first stall reason there.)
-        uint32_t r[MB / 32][32];
-#pragma unroll
-        for (int c = 0; c < MB / 32; ++c) tmem_ld32(t_o + c * 32, r[c]);
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&o_free[it % NO]);
-        wait_staging();
-#pragma unroll
-        for (int c = 0; c < MB / 32; ++c) store_chunk32(ob, row, c * 32, kBoxBytes, r[c]);
+      // a chunk of 32 columns at a time, one copy of the conversion in the
+      // instruction stream (reading the whole row first, then releasing the
+      // buffer, measured slower in the one-launch backward, whose two scan
+      // bodies share the instruction cache: 127.1 against 124.6 us; the
+      // feature backward 192 against 181 us)
+      if constexpr (EPI) {
+        if (!mbar_wait(&x_full[it % L::kOBufs], (it / L::kOBufs) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
       } else {
-        if constexpr (EPI) {
-          if (!mbar_wait(&x_full[it % L::kOBufs], (it / L::kOBufs) & 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-        } else {
-          wait_staging();
-        }
-#pragma unroll 1
-        for (int c = 0; c < MB / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(t_o + c * 32, r);
-          tmem_ld_wait();
-          if constexpr (EPI)
-            scale_store_chunk32(ob, row, c * 32, kBoxBytes, r);
-          else
-            store_chunk32(ob, row, c * 32, kBoxBytes, r);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&o_free[it % NO]);
+        wait_staging();
       }
+#pragma unroll 1
+      for (int c = 0; c < MB / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(t_o + c * 32, r);
+        tmem_ld_wait();
+        if constexpr (EPI)
+          scale_store_chunk32(ob, row, c * 32, kBoxBytes, r);
+        else
+          store_chunk32(ob, row, c * 32, kBoxBytes, r);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&o_free[it % NO]);
       fence_proxy_async_smem();
       named_barrier_sync(1, kOThreads);
       if (o_tid == 0) {
