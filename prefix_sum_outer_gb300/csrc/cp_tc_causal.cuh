@@ -242,6 +242,11 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
   static_assert(!NORM || !(AGG_ONLY || STATE_OUT || FEAT || CKPT || SEED),
                 "the normaliser is written by the plain forward scan alone");
   static_assert(!NORM || DP == 64, "the normaliser uses the state group's two idle warps");
+  // the feature-map instantiations wait with the polling loop out of line
+  // (their instruction stream is their first stall reason: the one-launch
+  // feature backward measured 172 against 183 us; the plain kernels are
+  // faster with it inline)
+  constexpr bool kOutlineWaits = FEAT || FEAT_V || EPI;
   using L = Layout<DP, MB, AGG_ONLY>;
   constexpr int NQK = L::NQK;
   constexpr int NV = L::NV;
@@ -424,7 +429,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
   // warps, each thread taking every (32 kMapWarps)-th 16-byte chunk from
   // mtid on; the issuers wait on qk_ready for all of them
   auto map_qk = [&](int it, int mtid) -> bool {
-    if (!mbar_wait(&full_qk[it % NQK], (it / NQK) & 1, abort_flag)) return false;
+    if (!mbar_wait_t<kOutlineWaits>(&full_qk[it % NQK], (it / NQK) & 1, abort_flag)) return false;
     uint8_t* q_s = qk_ring + (it % NQK) * L::kQKStage;
     uint4* p = reinterpret_cast<uint4*>(AGG_ONLY ? q_s + L::kKOff : q_s);
     constexpr int kChunks = (AGG_ONLY ? 1 : 2) * L::kQBytes / 16;
@@ -462,7 +467,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
   // FEAT_V: phi applied in place to the landed V tile of tile it (columns
   // mb * MB .. of the value), the same way; the issuers wait on v_ready
   auto map_v = [&](int it, int mtid) -> bool {
-    if (!mbar_wait(&full_v[it % NV], (it / NV) & 1, abort_flag)) return false;
+    if (!mbar_wait_t<kOutlineWaits>(&full_v[it % NV], (it / NV) & 1, abort_flag)) return false;
     uint4* p = reinterpret_cast<uint4*>(v_ring + (it % NV) * L::kVBytes);
     constexpr int kChunks = L::kVBytes / 16, kBoxChunks = kBoxBytes / 16;
     auto map_chunk = [&](int i) {
@@ -599,8 +604,8 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
       };
       if (AGG_ONLY) {
         for (int it = 0; it < n_it; ++it) {
-          if (!mbar_wait(&qk_bar[it % NQK], (it / NQK) & 1, abort_flag) ||
-              !mbar_wait(&v_bar[it % NV], (it / NV) & 1, abort_flag)) {
+          if (!mbar_wait_t<kOutlineWaits>(&qk_bar[it % NQK], (it / NQK) & 1, abort_flag) ||
+              !mbar_wait_t<kOutlineWaits>(&v_bar[it % NV], (it / NV) & 1, abort_flag)) {
             ok = false;
             break;
           }
@@ -656,8 +661,8 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
         // issuer B: P(t) needs Q/K(t) landed and P buffer t%NP free (P V of
         // tile t - NP completed)
         for (int it = 0; it < n_it; ++it) {
-          if (!mbar_wait(&qk_bar[it % NQK], (it / NQK) & 1, abort_flag) ||
-              (it >= NP && !mbar_wait(&pv_done[it % NP], ((it - NP) / NP) & 1, abort_flag))) {
+          if (!mbar_wait_t<kOutlineWaits>(&qk_bar[it % NQK], (it / NQK) & 1, abort_flag) ||
+              (it >= NP && !mbar_wait_t<kOutlineWaits>(&pv_done[it % NP], ((it - NP) / NP) & 1, abort_flag))) {
             ok = false;
             break;
           }
@@ -678,9 +683,9 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
         // completed in the output buffer it accumulates onto
         for (int it = 0; it < n_it; ++it) {
           const int b = it % NP;
-          if (!mbar_wait(&p_ready[b], (it / NP) & 1, abort_flag) ||
-              !mbar_wait(&v_bar[it % NV], (it / NV) & 1, abort_flag) ||
-              !mbar_wait(&o_qs[it % NO], (it / NO) & 1, abort_flag)) {
+          if (!mbar_wait_t<kOutlineWaits>(&p_ready[b], (it / NP) & 1, abort_flag) ||
+              !mbar_wait_t<kOutlineWaits>(&v_bar[it % NV], (it / NV) & 1, abort_flag) ||
+              !mbar_wait_t<kOutlineWaits>(&o_qs[it % NO], (it / NO) & 1, abort_flag)) {
             ok = false;
             break;
           }
@@ -717,7 +722,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
       for (int it = 0; FEAT_V && it < n_it && ok; ++it) ok = map_v(it, threadIdx.x - 32 * kSWarp0);
       if (!ok) {
         record_timeout(a.status, abort_flag);
-      } else if (!mbar_wait(s_done, 0, abort_flag)) {
+      } else if (!mbar_wait_t<kOutlineWaits>(s_done, 0, abort_flag)) {
         record_timeout(a.status, abort_flag);
       } else if (n_it > 0) {
         tc_fence_after();
@@ -797,7 +802,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
         const int b = it % NSB;
         uint8_t* sbuf = s_tile + b * L::kSBufBytes;
         // the Q S that last read this copy (tile it - NSB) has completed
-        if (it >= NSB && !mbar_wait(&qs_done[b], ((it - NSB) / NSB) & 1, abort_flag)) {
+        if (it >= NSB && !mbar_wait_t<kOutlineWaits>(&qs_done[b], ((it - NSB) / NSB) & 1, abort_flag)) {
           ok = false;
           break;
         }
@@ -813,7 +818,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
           }
         } else {
           if (it > 0) {
-            if (!mbar_wait(s_done, (it - 1) & 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait_t<kOutlineWaits>(s_done, (it - 1) & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
           }
 #pragma unroll
@@ -842,8 +847,8 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
           // quarters 2 and 3 (no state rows at D <= 64), lane l owning
           // columns 2l, 2l + 1, four interleaved partial sums; fixed order
           const int st = it % NQK;
-          if (!mbar_wait(&full_qk[st], (it / NQK) & 1, abort_flag) ||
-              (it > 0 && !mbar_wait(zq_free, (it - 1) & 1, abort_flag))) {
+          if (!mbar_wait_t<kOutlineWaits>(&full_qk[st], (it / NQK) & 1, abort_flag) ||
+              (it > 0 && !mbar_wait_t<kOutlineWaits>(zq_free, (it - 1) & 1, abort_flag))) {
             ok = false;
             break;
           }
@@ -941,7 +946,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
       // CKPT: a checkpoint boundary right after this segment's last tile
       // (the state is exact here: no copy follows it)
       if (CKPT && ok && n_it > 0 && ckpt_slot(tile_of(n_it - 1) + 1) > 0) {
-        if (!mbar_wait(s_done, (n_it - 1) & 1, abort_flag)) {
+        if (!mbar_wait_t<kOutlineWaits>(s_done, (n_it - 1) & 1, abort_flag)) {
           ok = false;
         } else {
           tc_fence_after();
@@ -972,7 +977,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
       }
       // the last segment in scan order hands on the state after its last tile
       if (STATE_OUT && ok && last_seg && n_it > 0) {
-        if (!mbar_wait(s_done, (n_it - 1) & 1, abort_flag)) {
+        if (!mbar_wait_t<kOutlineWaits>(s_done, (n_it - 1) & 1, abort_flag)) {
           ok = false;
         } else {
           tc_fence_after();
@@ -1007,7 +1012,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
     bool ok = true;
     for (int it = 0; !AGG_ONLY && it < n_it && ok; ++it) {
       const int b = it % NP;
-      if (!mbar_wait(&p_done[b], (it / NP) & 1, abort_flag)) { ok = false; break; }
+      if (!mbar_wait_t<kOutlineWaits>(&p_done[b], (it / NP) & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
       const uint32_t pc = lane_base + L::kColP + b * 128;
       float zrow = 0.f;  // NORM: sum over the row's unmasked fp32 entries, in column order
@@ -1048,7 +1053,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
       if (lane == 0) mbar_arrive(&p_ready[b]);
       if constexpr (NORM) {
         // z_i = (row sum of P: the terms j of this tile) + q_i . s_k
-        if (!mbar_wait(zq_ready, it & 1, abort_flag)) {
+        if (!mbar_wait_t<kOutlineWaits>(zq_ready, it & 1, abort_flag)) {
           ok = false;
           break;
         }
@@ -1103,7 +1108,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
         epi_load();
       }
       uint8_t* ob = o_tile + (it % L::kOBufs) * L::kOBytes;
-      if (!mbar_wait(&o_done[it % NO], (it / NO) & 1, abort_flag)) {
+      if (!mbar_wait_t<kOutlineWaits>(&o_done[it % NO], (it / NO) & 1, abort_flag)) {
         ok = false;
         break;
       }
@@ -1125,7 +1130,7 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
       // bodies share the instruction cache: 127.1 against 124.6 us; the
       // feature backward 192 against 181 us)
       if constexpr (EPI) {
-        if (!mbar_wait(&x_full[it % L::kOBufs], (it / L::kOBufs) & 1, abort_flag)) {
+        if (!mbar_wait_t<kOutlineWaits>(&x_full[it % L::kOBufs], (it / L::kOBufs) & 1, abort_flag)) {
           ok = false;
           break;
         }

@@ -194,7 +194,7 @@ __device__ __forceinline__ bool dkdv_body(const CUtensorMap& tm_q, const CUtenso
       int n = 0;
       for (; n < n_it; ++n) {
         const int st = n % kNS;
-        if (n >= kNS && !mbar_wait(&empty[st], ((n / kNS) - 1) & 1, abort_flag)) {
+        if (n >= kNS && !mbar_wait_t<FEAT>(&empty[st], ((n / kNS) - 1) & 1, abort_flag)) {
           record_timeout(a.status, abort_flag);
           break;
         }
@@ -220,8 +220,8 @@ __device__ __forceinline__ bool dkdv_body(const CUtensorMap& tm_q, const CUtenso
       const uint32_t t_s = tmem + kColS;
       bool ok = true;
       for (int it = 0; it < n_it; ++it) {
-        if (!mbar_wait(&qk_bar[it % kNS], (it / kNS) & 1, abort_flag) ||
-            !mbar_wait(&copy_ready[it % kNSB], (it / kNSB) & 1, abort_flag)) {
+        if (!mbar_wait_t<FEAT>(&qk_bar[it % kNS], (it / kNS) & 1, abort_flag) ||
+            !mbar_wait_t<FEAT>(&copy_ready[it % kNSB], (it / kNSB) & 1, abort_flag)) {
           ok = false;
           break;
         }
@@ -265,8 +265,8 @@ __device__ __forceinline__ bool dkdv_body(const CUtensorMap& tm_q, const CUtenso
       bool ok = true;
       for (int it = 0; it < n_it; ++it) {
         // P1 = K Q^T reads mapped boxes; P2 = V G^T does not
-        if (!mbar_wait(x == 0 ? &qk_bar[it % kNS] : &full[it % kNS], (it / kNS) & 1, abort_flag) ||
-            (it > 0 && !mbar_wait(&o_done[x], (it - 1) & 1, abort_flag))) {
+        if (!mbar_wait_t<FEAT>(x == 0 ? &qk_bar[it % kNS] : &full[it % kNS], (it / kNS) & 1, abort_flag) ||
+            (it > 0 && !mbar_wait_t<FEAT>(&o_done[x], (it - 1) & 1, abort_flag))) {
           ok = false;
           break;
         }
@@ -278,8 +278,8 @@ __device__ __forceinline__ bool dkdv_body(const CUtensorMap& tm_q, const CUtenso
         for (int kk = 0; kk < kW / 16; ++kk)
           mma_ss_lo<kHi, kHi>(t_p, a_lo + kk * 2, b_lo + kk * 2, idesc_p, kk > 0 ? 1u : 0u);
         mma_commit(&p_done[x]);
-        if (!mbar_wait(&copy_ready[it % kNSB], (it / kNSB) & 1, abort_flag) ||
-            (it > 0 && !mbar_wait(&o_free[x], (it - 1) & 1, abort_flag))) {
+        if (!mbar_wait_t<FEAT>(&copy_ready[it % kNSB], (it / kNSB) & 1, abort_flag) ||
+            (it > 0 && !mbar_wait_t<FEAT>(&o_free[x], (it - 1) & 1, abort_flag))) {
           ok = false;
           break;
         }
@@ -306,8 +306,8 @@ __device__ __forceinline__ bool dkdv_body(const CUtensorMap& tm_q, const CUtenso
           }
         }
         mma_commit(&qs_done[it % kNSB]);
-        if (!mbar_wait(&p_ready[x], it & 1, abort_flag) ||
-            (FEAT && x == 1 && !mbar_wait(&qk_mapped[it % kNS], (it / kNS) & 1, abort_flag))) {
+        if (!mbar_wait_t<FEAT>(&p_ready[x], it & 1, abort_flag) ||
+            (FEAT && x == 1 && !mbar_wait_t<FEAT>(&qk_mapped[it % kNS], (it / kNS) & 1, abort_flag))) {
           ok = false;
           break;
         }
@@ -425,7 +425,7 @@ __device__ __forceinline__ bool dkdv_body(const CUtensorMap& tm_q, const CUtenso
     }
     // the first segment (last in scan order) hands on R after row 0: dL/dS_0
     if (STATE_OUT && ok && seg == 0 && n_it > 0) {
-      if (!mbar_wait(s_done, (n_it - 1) & 1, abort_flag)) {
+      if (!mbar_wait_t<FEAT>(s_done, (n_it - 1) & 1, abort_flag)) {
         ok = false;
       } else if (wq < 2) {
         tc_fence_after();
@@ -448,7 +448,7 @@ __device__ __forceinline__ bool dkdv_body(const CUtensorMap& tm_q, const CUtenso
     // ------------------------------------------------------------ P1 group
     bool ok = true;
     for (int it = 0; it < n_it && ok; ++it) {
-      if (!mbar_wait(&p_done[0], it & 1, abort_flag)) {
+      if (!mbar_wait_t<FEAT>(&p_done[0], it & 1, abort_flag)) {
         ok = false;
         break;
       }
@@ -472,7 +472,7 @@ __device__ __forceinline__ bool dkdv_body(const CUtensorMap& tm_q, const CUtenso
     // chunk c ^ (r % 8)).  Tile it + 1 is mapped before the read-out of tile
     // it: its stage was released at the end of iteration it - 2.
     [[maybe_unused]] auto map_stage = [&](int it) -> bool {
-      if (!mbar_wait(&full[it % kNS], (it / kNS) & 1, abort_flag)) return false;
+      if (!mbar_wait_t<FEAT>(&full[it % kNS], (it / kNS) & 1, abort_flag)) return false;
       uint4* p = reinterpret_cast<uint4*>(ring + (it % kNS) * kStageBytes);  // Q box, K box
       constexpr int kChunks = 2 * kBoxBytes / 16, kBoxChunks = kBoxBytes / 16;
       auto map_chunk = [&](int i) {
@@ -508,7 +508,7 @@ __device__ __forceinline__ bool dkdv_body(const CUtensorMap& tm_q, const CUtenso
       for (int xi = 0; xi < 2; ++xi) {
         // FEAT: dK first, while the K box still holds phi(k)
         const int x = FEAT ? 1 - xi : xi;
-        if (!mbar_wait(&o_done[x], it & 1, abort_flag)) {
+        if (!mbar_wait_t<FEAT>(&o_done[x], it & 1, abort_flag)) {
           ok = false;
           break;
         }

@@ -94,6 +94,35 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// The waiting part of mbar_wait out of line, one copy per translation unit:
+// for the kernels whose instruction stream is the first stall reason (the
+// feature-map instantiations), where the polling loop inlined at every wait
+// site made the code larger than the instruction cache holds.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity,
+                                                   volatile int* abort_flag) {
+  const uint64_t t0 = globaltimer();
+  uint32_t spins = 0;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((++spins & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > CP_WAIT_TIMEOUT_NS) return false;
+    }
+  }
+}
+
+// mbar_wait, with the polling loop out of line when OUTLINE.
+template <bool OUTLINE>
+__device__ __forceinline__ bool mbar_wait_t(uint64_t* bar, uint32_t parity,
+                                            volatile int* abort_flag) {
+  if constexpr (OUTLINE) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, abort_flag);
+  } else {
+    return mbar_wait(bar, parity, abort_flag);
+  }
+}
+
 // Wait with a wall-time limit only (used while draining after an abort).
 __device__ __forceinline__ bool mbar_wait_timeout(uint64_t* bar, uint32_t parity,
                                                   uint64_t limit_ns) {
