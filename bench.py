@@ -53,12 +53,12 @@ BWD_SOURCES = ("cp_tc_dkdv.cu", "cp_tc_dkdv.cuh", "cp_tc_causal.cuh", "cp_tc_com
 # per kernel (the outputs a launch writes partly stay in the 126 MB L2 when
 # it ends, so its write bytes undercount them).
 PROFILED_TRAFFIC = {
-    "source_sha256": "97bfa1ca46cdab442d5f340e3f7dd6720ae1fd3fa72c3c3e6edeb1171be07480",
-    "bytes_per_launch": 211139584,  # 201.40 MB read + 9.74 MB written (forward launch)
+    "source_sha256": "7765005973abf5ffefe5ca98dea85e13c94ccbc78bc54d9f3c8c77258a50aaf5",
+    "bytes_per_launch": 211141120,  # 201.42 MB read + 9.72 MB written (forward launch)
 }
 PROFILED_TRAFFIC_BWD = {
-    "source_sha256": "c41509d35a4df239fccdd0ef556673ee606cee9599eb77dbf339b7d3ebd654b8",
-    "bytes_per_launch": 604890112,  # 463.04 MB read + 141.85 MB written (one backward launch)
+    "source_sha256": "72511931b178067545aadf3a6dca89a14808d7a440c5dc47430c0bc2ad9e0262",
+    "bytes_per_launch": 605895936,  # 463.82 MB read + 142.07 MB written (one backward launch)
 }
 
 
