@@ -242,11 +242,12 @@ __device__ __forceinline__ bool causal_body(const CUtensorMap& tm_q, const CUten
   static_assert(!NORM || !(AGG_ONLY || STATE_OUT || FEAT || CKPT || SEED),
                 "the normaliser is written by the plain forward scan alone");
   static_assert(!NORM || DP == 64, "the normaliser uses the state group's two idle warps");
-  // the feature-map instantiations wait with the polling loop out of line
-  // (their instruction stream is their first stall reason: the one-launch
-  // feature backward measured 172 against 183 us; the plain kernels are
+  // the feature-map and normaliser instantiations wait with the polling
+  // loop out of line (their instruction stream is a leading stall reason:
+  // the one-launch feature backward measured 172 against 183 us, the
+  // forward with the normaliser 79 against 82.5 us; the plain kernels are
   // faster with it inline)
-  constexpr bool kOutlineWaits = FEAT || FEAT_V || EPI;
+  constexpr bool kOutlineWaits = FEAT || FEAT_V || EPI || NORM;
   using L = Layout<DP, MB, AGG_ONLY>;
   constexpr int NQK = L::NQK;
   constexpr int NV = L::NV;
