@@ -53,12 +53,12 @@ BWD_SOURCES = ("cp_tc_dkdv.cu", "cp_tc_dkdv.cuh", "cp_tc_causal.cuh", "cp_tc_com
 # per kernel (the outputs a launch writes partly stay in the 126 MB L2 when
 # it ends, so its write bytes undercount them).
 PROFILED_TRAFFIC = {
-    "source_sha256": "7765005973abf5ffefe5ca98dea85e13c94ccbc78bc54d9f3c8c77258a50aaf5",
-    "bytes_per_launch": 211141120,  # 201.42 MB read + 9.72 MB written (forward launch)
+    "source_sha256": "c55654417449854cafe01a3592c067a6cdc92527f23a3aed6e8214924ee78505",
+    "bytes_per_launch": 211120896,  # 201.43 MB read + 9.69 MB written (forward launch)
 }
 PROFILED_TRAFFIC_BWD = {
-    "source_sha256": "72511931b178067545aadf3a6dca89a14808d7a440c5dc47430c0bc2ad9e0262",
-    "bytes_per_launch": 605895936,  # 463.82 MB read + 142.07 MB written (one backward launch)
+    "source_sha256": "3d5f0084ac9e327b22b66036cc1d6f2f0bdbf42cd435297a677a8a2d36f1719d",
+    "bytes_per_launch": 605626624,  # 463.83 MB read + 141.80 MB written (one backward launch)
 }
 
 
