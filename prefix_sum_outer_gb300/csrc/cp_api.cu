@@ -29,6 +29,16 @@ int device_sm_count() {
   return n_sm;
 }
 
+size_t device_l2_bytes() {
+  int dev = 0, l2 = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess || l2 <= 0) {
+    cudaGetLastError();
+    return kPlanL2Bytes;
+  }
+  return (size_t)l2;
+}
+
 namespace {
 
 constexpr size_t kAlign = 256;

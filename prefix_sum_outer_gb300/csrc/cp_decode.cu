@@ -79,7 +79,23 @@ __global__ void __launch_bounds__(kDecThreads)
 // The same step with 16-byte state accesses (M % 4 == 0): a thread owns four
 // consecutive columns of a row group and issues the loads of four rows
 // before using them, so a CTA keeps its whole state tile in flight.
-template <typename T>
+// STREAM: a state larger than the L2 cannot stay there until the next step,
+// so it is read and written with the evict-first (streaming) hints (B=512
+// H=16 D=M=64, 128 MiB of state: 48.1 against 43.6 us per step).
+template <bool STREAM>
+__device__ __forceinline__ float4 ld_state(const float4* p) {
+  if constexpr (STREAM) return __ldcs(p);
+  return *p;
+}
+template <bool STREAM>
+__device__ __forceinline__ void st_state(float4* p, float4 v) {
+  if constexpr (STREAM)
+    __stcs(p, v);
+  else
+    *p = v;
+}
+
+template <typename T, bool STREAM>
 __global__ void __launch_bounds__(kDecThreads)
     decode_kernel_v4(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                      T* __restrict__ out, float* __restrict__ state, int D, int M) {
@@ -89,25 +105,34 @@ __global__ void __launch_bounds__(kDecThreads)
   float* vs = ks + D;      // [M]
   float* part = vs + M;    // [groups][M]
   const int64_t p = blockIdx.x;
+  const int c4 = M / 4;                  // float4 columns
+  const int groups = kDecThreads / c4;   // row groups (>= 4)
+  const int cq = threadIdx.x % c4, g = threadIdx.x / c4;
+  float4* S4 = reinterpret_cast<float4*>(state + p * D * M);
+  // the first four rows' state loads do not depend on q, k, v: they go out
+  // before the staging below, so the two latencies overlap
+  float4 st[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int d = g + u * groups;
+    if (g < groups && d < D) st[u] = ld_state<STREAM>(&S4[(int64_t)d * c4 + cq]);
+  }
   for (int i = threadIdx.x; i < D; i += kDecThreads) {
     qs[i] = to_f32(q[p * D + i]);
     ks[i] = to_f32(k[p * D + i]);
   }
   for (int i = threadIdx.x; i < M; i += kDecThreads) vs[i] = to_f32(v[p * M + i]);
   __syncthreads();
-  const int c4 = M / 4;                  // float4 columns
-  const int groups = kDecThreads / c4;   // row groups (>= 4)
-  const int cq = threadIdx.x % c4, g = threadIdx.x / c4;
-  float4* S4 = reinterpret_cast<float4*>(state + p * D * M);
   if (g < groups) {
     const float4 vm = make_float4(vs[4 * cq], vs[4 * cq + 1], vs[4 * cq + 2], vs[4 * cq + 3]);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int d0 = g; d0 < D; d0 += 4 * groups) {
-      float4 st[4];
+      if (d0 != g) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int d = d0 + u * groups;
-        if (d < D) st[u] = S4[(int64_t)d * c4 + cq];
+        for (int u = 0; u < 4; ++u) {
+          const int d = d0 + u * groups;
+          if (d < D) st[u] = ld_state<STREAM>(&S4[(int64_t)d * c4 + cq]);
+        }
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -118,7 +143,7 @@ __global__ void __launch_bounds__(kDecThreads)
           st[u].y = fmaf(kd, vm.y, st[u].y);
           st[u].z = fmaf(kd, vm.z, st[u].z);
           st[u].w = fmaf(kd, vm.w, st[u].w);
-          S4[(int64_t)d * c4 + cq] = st[u];
+          st_state<STREAM>(&S4[(int64_t)d * c4 + cq], st[u]);
           acc.x = fmaf(qd, st[u].x, acc.x);
           acc.y = fmaf(qd, st[u].y, acc.y);
           acc.z = fmaf(qd, st[u].z, acc.z);
@@ -141,6 +166,26 @@ __global__ void __launch_bounds__(kDecThreads)
   }
 }
 
+template <bool STREAM>
+cudaError_t decode_v4(const void* q, const void* k, const void* v, void* out, float* state,
+                      int64_t BH, int64_t D, int64_t M, cp_dtype_t dtype, size_t smem,
+                      cudaStream_t stream) {
+  if (dtype == CP_DTYPE_BF16)
+    decode_kernel_v4<__nv_bfloat16, STREAM><<<(unsigned)BH, kDecThreads, smem, stream>>>(
+        static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+        static_cast<const __nv_bfloat16*>(v), static_cast<__nv_bfloat16*>(out), state, (int)D,
+        (int)M);
+  else if (dtype == CP_DTYPE_F16)
+    decode_kernel_v4<__half, STREAM><<<(unsigned)BH, kDecThreads, smem, stream>>>(
+        static_cast<const __half*>(q), static_cast<const __half*>(k),
+        static_cast<const __half*>(v), static_cast<__half*>(out), state, (int)D, (int)M);
+  else
+    decode_kernel_v4<float, STREAM><<<(unsigned)BH, kDecThreads, smem, stream>>>(
+        static_cast<const float*>(q), static_cast<const float*>(k),
+        static_cast<const float*>(v), static_cast<float*>(out), state, (int)D, (int)M);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 size_t decode_smem_bytes(int64_t D, int64_t M) {
@@ -152,20 +197,9 @@ cudaError_t decode_launch(const void* q, const void* k, const void* v, void* out
                           cudaStream_t stream) {
   if (M % 4 == 0) {
     const size_t smem = sizeof(float) * (size_t)(2 * D + M + (kDecThreads / (M / 4)) * M);
-    if (dtype == CP_DTYPE_BF16)
-      decode_kernel_v4<__nv_bfloat16><<<(unsigned)BH, kDecThreads, smem, stream>>>(
-          static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
-          static_cast<const __nv_bfloat16*>(v), static_cast<__nv_bfloat16*>(out), state, (int)D,
-          (int)M);
-    else if (dtype == CP_DTYPE_F16)
-      decode_kernel_v4<__half><<<(unsigned)BH, kDecThreads, smem, stream>>>(
-          static_cast<const __half*>(q), static_cast<const __half*>(k),
-          static_cast<const __half*>(v), static_cast<__half*>(out), state, (int)D, (int)M);
-    else
-      decode_kernel_v4<float><<<(unsigned)BH, kDecThreads, smem, stream>>>(
-          static_cast<const float*>(q), static_cast<const float*>(k),
-          static_cast<const float*>(v), static_cast<float*>(out), state, (int)D, (int)M);
-    return cudaGetLastError();
+    const bool stream_state = (size_t)BH * D * M * sizeof(float) > device_l2_bytes() / 2;
+    return stream_state ? decode_v4<true>(q, k, v, out, state, BH, D, M, dtype, smem, stream)
+                        : decode_v4<false>(q, k, v, out, state, BH, D, M, dtype, smem, stream);
   }
   const size_t smem = decode_smem_bytes(D, M);
   if (dtype == CP_DTYPE_BF16)

@@ -27,6 +27,9 @@ namespace cp {
 constexpr int kPlanSMs = 152;
 // SMs of the current device (kPlanSMs when there is none)
 int device_sm_count();
+// L2 bytes of the current device (kPlanL2Bytes, a GB300's, when there is none)
+constexpr size_t kPlanL2Bytes = 126u << 20;
+size_t device_l2_bytes();
 // Split forward scans in one launch (tc_lookback_kernel) instead of three:
 // environment variable CP_SPLIT_SCAN=lookback, read at each call.  Off by
 // default: measured slower on the 16-problem N = 32768 D = M = 128 forward.

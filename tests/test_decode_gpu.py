@@ -20,7 +20,10 @@ STATE_TOL = {"f32": 1e-5, "bf16": 1e-4}
 @pytest.mark.parametrize("shape", [(8, 16, 64, 64, "bf16"), (3, 5, 128, 32, "bf16"),
                                    (2, 2, 16, 256, "bf16"), (1, 4, 256, 64, "bf16"),
                                    (2, 3, 8, 8, "bf16"), (2, 3, 64, 64, "f32"),
-                                   (1, 2, 80, 24, "f32"), (1, 1, 5, 3, "f32")],
+                                   (1, 2, 80, 24, "f32"), (1, 1, 5, 3, "f32"),
+                                   # a 128 MiB state, larger than the L2: the
+                                   # streaming variant
+                                   (512, 16, 64, 64, "bf16")],
                          ids=lambda s: "x".join(map(str, s)))
 def test_decode_step_against_oracle(shape):
     B, H, D, M, dt = shape
