@@ -592,15 +592,16 @@ def run_ours(args, world, rank, local):
         nf_bytes = (2 * s_ * w.D + 4) * w.token_heads
         nb_bytes = (4 * s_ * w.D + 8) * w.token_heads
         peak = load_peaks()[0]
-        norm = {"kernel": "norm_lb_kernel (single pass, look-back)", "bound": "hbm",
+        norm = {"kernel": "z: norm_pp_kernel (one CTA per problem); dq, dk: norm_lb_kernel "
+                          "(single pass, look-back)", "bound": "hbm",
                 "fwd": {"us": nf_ms * 1e3, "bytes": nf_bytes,
                         "achieved_gbs": nf_bytes / (nf_ms / 1e3) / 1e9,
                         "frac": nf_bytes / (nf_ms / 1e3) / 1e9 / peak},
                 "bwd": {"us": nb_ms * 1e3, "bytes": nb_bytes,
                         "achieved_gbs": nb_bytes / (nb_ms / 1e3) / 1e9,
                         "frac": nb_bytes / (nb_ms / 1e3) / 1e9 / peak},
-                "timing": "CUDA events over 20 calls each; a call is a workspace fill and "
-                          "one launch per output (z; dq then dk)"}
+                "timing": "CUDA events over 20 calls each; one launch per output (z; dq "
+                          "then dk), after a workspace fill on the look-back kernel"}
         # the same with phi = elu + 1 applied to raw x ~ N(0, 1) in the kernel;
         # its backward streams q and k in both launches
         rq, rk, _, _ = make_inputs(w.B, w.H, w.N, w.D, 1, w.torch_dtype, seed=80,
@@ -612,6 +613,7 @@ def run_ours(args, world, rank, local):
                                                                stream=stream, feature="elu1"))
         fb_bytes = (6 * s_ * w.D + 8) * w.token_heads
         norm["feature_elu1"] = {
+            "kernel": "z: norm_lb_kernel; dq, dk: norm_pp_kernel",
             "fwd": {"us": ff_ms * 1e3, "bytes": nf_bytes,
                     "frac": nf_bytes / (ff_ms / 1e3) / 1e9 / peak},
             "bwd": {"us": fb_ms * 1e3, "bytes": fb_bytes,

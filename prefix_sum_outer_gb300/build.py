@@ -22,7 +22,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libcausal_product.so")
 SOURCES = ["cp_api.cu", "cp_simt.cu", "cp_tc.cu", "cp_tc_dkdv.cu", "cp_decode.cu",
            "cp_selftest.cu", "cp_norm.cu", "cp_feature.cu", "cp_segscan.cu", "cp_favor.cu", "cp_favor_fwd.cu",
-           "cp_tc_lookback.cu"]
+           "cp_tc_lookback.cu", "cp_norm_pp.cu"]
 HEADERS = ["cp_internal.h", "cp_tc_common.cuh", "cp_tc_causal.cuh", "cp_tc_dkdv.cuh",
            "sm103_ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -191,6 +191,15 @@ cudaError_t norm_launch(int mode, const void* q, const void* k, const float* gra
                         void* out, int64_t BH, int64_t N, int64_t D, cp_dtype_t dtype,
                         void* scratch, int* status, cudaStream_t stream, int feature = 0);
 
+// The normaliser with one CTA per problem (no look-back, no scratch): rows
+// of D = 64, at least half as many problems as SMs, and the calls it is
+// faster for (z of plain rows; dq and dk of mapped rows).  Modes as for
+// norm_launch.
+bool norm_pp_eligible(int mode, int feature, int64_t BH, int64_t N, int64_t D);
+cudaError_t norm_pp_launch(int mode, const void* q, const void* k, const float* grad_z, float* z,
+                           void* out, int64_t BH, int64_t N, cp_dtype_t dtype, int* status,
+                           cudaStream_t stream, int feature);
+
 // ---- feature map, elementwise over n elements of `dtype`:
 // feature_map: y = phi(x); feature_grad: g *= phi'(x) in place
 cudaError_t feature_map_launch(int feature, const void* x, void* y, int64_t n, cp_dtype_t dtype,

@@ -916,6 +916,8 @@ cudaError_t norm_launch(int mode, const void* q, const void* k, const float* gra
                         void* out, int64_t BH, int64_t N, int64_t D, cp_dtype_t dtype,
                         void* scratch, int* status, cudaStream_t stream, int feature) {
   const bool feat = feature != 0;
+  if (norm_pp_eligible(mode, feature, BH, N, D) && (!feat || single_pass(D, dtype)))
+    return norm_pp_launch(mode, q, k, grad_z, z, out, BH, N, dtype, status, stream, feature);
   if (single_pass(D, dtype)) {
     const LbPlan pl = lb_plan(BH, N, D, dtype);
     LbArgs a{};

@@ -40,6 +40,10 @@ SHAPES = [
     (1, 2, 900, 256, "f32", "elu"),
     (1, 1, 333, 7, "f32", "elu"),
     (1, 1, 1, 1, "f32", "elu"),
+    # D = 64 with at least half as many problems as SMs: one CTA per problem
+    (8, 16, 1000, 64, "f32", "elu"),
+    (4, 20, 129, 64, "bf16", "normal"),
+    (4, 19, 77, 64, "bf16", "elu"),
 ]
 
 
@@ -75,8 +79,11 @@ def test_normalizer_backward_against_oracle(shape):
     assert row_rel_err(to_np(dk), r_dk) <= TOL[dt]
 
 
-def test_normalizer_is_bitwise_reproducible():
-    q, k, gz = (t.to(DEV) for t in _inputs((2, 2, 20000, 64, "bf16", "elu"), seed=5))
+@pytest.mark.parametrize("shape", [(2, 2, 20000, 64, "bf16", "elu"),
+                                   (8, 16, 2000, 64, "bf16", "elu")],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_normalizer_is_bitwise_reproducible(shape):
+    q, k, gz = (t.to(DEV) for t in _inputs(shape, seed=5))
     z1 = cp.causal_product_normalizer(q, k)
     z2 = cp.causal_product_normalizer(q, k)
     a = cp.causal_product_normalizer_bwd(q, k, gz)
@@ -125,6 +132,8 @@ def test_normalised_attention_composes():
 # kernel); phi > 0, so z itself is the scale of its summation error
 FEAT_SHAPES = [
     (2, 3, 1000, 64, "bf16"),
+    (8, 16, 1000, 64, "bf16"),
+    (4, 19, 77, 64, "f32"),
     (1, 1, 20000, 128, "bf16"),
     (2, 2, 300, 256, "f32"),
     (2, 3, 500, 36, "f32"),
