@@ -13,8 +13,8 @@ from prefix_sum_outer_gb300.workloads import make_inputs
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda:0"
-DT = {"f32": torch.float32, "bf16": torch.bfloat16}
-STATE_TOL = {"f32": 1e-5, "bf16": 1e-4}
+DT = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+STATE_TOL = {"f32": 1e-5, "bf16": 1e-4, "f16": 1e-4}
 
 
 @pytest.mark.parametrize("shape", [(8, 16, 64, 64, "bf16"), (3, 5, 128, 32, "bf16"),
@@ -23,7 +23,9 @@ STATE_TOL = {"f32": 1e-5, "bf16": 1e-4}
                                    (1, 2, 80, 24, "f32"), (1, 1, 5, 3, "f32"),
                                    # a 128 MiB state, larger than the L2: the
                                    # streaming variant
-                                   (512, 16, 64, 64, "bf16")],
+                                   (512, 16, 64, 64, "bf16"),
+                                   # fp16 rows, plain and streaming
+                                   (2, 3, 64, 64, "f16"), (512, 16, 64, 64, "f16")],
                          ids=lambda s: "x".join(map(str, s)))
 def test_decode_step_against_oracle(shape):
     B, H, D, M, dt = shape

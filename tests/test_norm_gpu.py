@@ -19,7 +19,7 @@ from prefix_sum_outer_gb300.workloads import make_norm_inputs
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda:0"
-DT = {"f32": torch.float32, "bf16": torch.bfloat16}
+DT = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
 Z_TOL = 1e-4
 
 # (B, H, N, D, dtype, feature): segmented and unsplit problems, every lane
@@ -44,6 +44,7 @@ SHAPES = [
     (8, 16, 1000, 64, "f32", "elu"),
     (4, 20, 129, 64, "bf16", "normal"),
     (4, 19, 77, 64, "bf16", "elu"),
+    (4, 20, 300, 64, "f16", "elu"),
 ]
 
 
@@ -134,6 +135,7 @@ FEAT_SHAPES = [
     (2, 3, 1000, 64, "bf16"),
     (8, 16, 1000, 64, "bf16"),
     (4, 19, 77, 64, "f32"),
+    (4, 20, 300, 64, "f16"),
     (1, 1, 20000, 128, "bf16"),
     (2, 2, 300, 256, "f32"),
     (2, 3, 500, 36, "f32"),
