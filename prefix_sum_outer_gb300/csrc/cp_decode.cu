@@ -79,9 +79,9 @@ __global__ void __launch_bounds__(kDecThreads)
 // The same step with 16-byte state accesses (M % 4 == 0): a thread owns four
 // consecutive columns of a row group and issues the loads of four rows
 // before using them, so a CTA keeps its whole state tile in flight.
-// STREAM: a state larger than the L2 cannot stay there until the next step,
-// so it is read and written with the evict-first (streaming) hints (B=512
-// H=16 D=M=64, 128 MiB of state: 48.1 against 43.6 us per step).
+// STREAM: a state larger than half the L2 cannot stay there until the next
+// step, so it is read and written with the evict-first (streaming) hints
+// (B=512 H=16 D=M=64, 128 MiB of state: 48.1 against 43.6 us per step).
 template <bool STREAM>
 __device__ __forceinline__ float4 ld_state(const float4* p) {
   if constexpr (STREAM) return __ldcs(p);
